@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark of the int8 quantized projection hot path on GB300.
+
+Default workload (the headline): the batch-1 decode GEMV sweep -- q8_0
+quantization of the activation, then Q8_0 GEMVs (n, k) = (12288, 7168),
+(96, 7168), (512, 128) -- reported as algorithmic HBM GB/s.  The same JSON
+line carries a ``prefill`` object: the qwen2-7B-shaped prefill chain
+(3325 tokens, d = 3584, nf = 18944: rmsnorm_quant -> gate and up GEMMs ->
+swiglu_quant -> down GEMM) with the GEMMs' int8-op throughput.
+
+Inputs are seeded synthetic tensors (no dataset); weights rotate through
+copies totalling more than 4x the 129 MB L2 (decode), and the prefill step's
+own working set is about 1.2 GB, so no step reads the previous step's data
+from L2.
+
+``--impl reference`` times the plain CPU oracle on the host cores on a
+bounded sample of the same workload and prints the same line with
+``"impl": "reference"``.  Under torchrun every rank runs an independent
+replica (the path has no exchange step) and rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from int8_quantized_projection_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "Q8_0 GEMV HBM GB/s (b=1) and prefill int8 GEMM TOPS, as % of GB300 roofline"
+L2_BYTES = 129 * 1000 * 1000
+DECODE_SHAPES = [(12288, 7168), (96, 7168), (512, 128)]
+PREFILL = dict(tokens=3325, d=3584, nf=18944, eps=1e-6)
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
+# kernel from the ncu capture summarised under profiles/ (None until taken,
+# and reset to None whenever that kernel changes).
+NCU_TRAFFIC_BYTES = {"gemv_staged_kernel 12288x7168": None, "gemm 18944x3584 t=3325": None}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes / ops per call (counted with the true token count)
+# ---------------------------------------------------------------------------
+def bytes_quantize(rows, k):
+    return 4 * rows * k + rows * k + 4 * rows * (k // 32)
+
+
+def bytes_gemv(n, k):
+    return n * (k // 32) * 34 + k + 4 * (k // 32) + 4 * n
+
+
+def bytes_rmsnorm_quant(rows, d):
+    return 8 * rows * d + 4 * d + rows * d + 4 * rows * (d // 32)
+
+
+def bytes_swiglu_quant(rows, nf):
+    return 12 * rows * nf + rows * nf + 4 * rows * (nf // 32)
+
+
+def ops_gemm(t, n, k):
+    return 2 * t * n * k
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_smi_id(torch, dev):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return str(dev)
+
+
+# ---------------------------------------------------------------------------
+# decode workload (headline)
+# ---------------------------------------------------------------------------
+def decode_inputs():
+    g = syn.rng(1, 0)
+    xs = {k: syn.activations(g, 1, k, sigma=1.5, outlier_frac=0.01) for k in (7168, 128)}
+    ws = [syn.q8_0_weights(syn.rng(1, 1 + i), n, k)[0] for i, (n, k) in enumerate(DECODE_SHAPES)]
+    return xs, ws
+
+
+def decode_bytes():
+    return (bytes_quantize(1, 7168) + bytes_quantize(1, 128) + sum(bytes_gemv(n, k) for n, k in DECODE_SHAPES))
+
+
+def run_decode(torch, q8p, steps, warmup, dev, sampler):
+    xs_h, ws_h = decode_inputs()
+    per_copy = sum(w.nbytes for w in ws_h)
+    copies = max(2, -(-4 * L2_BYTES // per_copy))
+    ws = [[torch.from_numpy(w).to(dev) for w in ws_h] for _ in range(copies)]
+    xs = {k: torch.from_numpy(v).to(dev) for k, v in xs_h.items()}
+    planes = {k: q8p.empty_plane(1, k, dev) for k in xs}
+    ys = [torch.empty(n, dtype=torch.float32, device=dev) for n, _ in DECODE_SHAPES]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        wset = ws[i % copies]
+        for k in (7168, 128):
+            q8p.quantize_q8_0(xs[k], *planes[k])
+        for j, (n, k) in enumerate(DECODE_SHAPES):
+            if j == 0 and ev is not None:
+                ev[0].record(stream)
+            q8p.q8_0_gemv(wset[j], n, k, *planes[k], ys[j])
+            if j == 0 and ev is not None:
+                ev[1].record(stream)
+
+    for i in range(warmup):
+        step(i)
+    q8p.q8_check()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    t0.record(stream)
+    for i in range(steps):
+        step(warmup + i, evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    q8p.q8_check()
+    ms = t0.elapsed_time(t1)
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # end to end through the public API with host buffers (weights resident)
+    xh = {k: torch.from_numpy(v).pin_memory() for k, v in xs_h.items()}
+    yh = [torch.empty(n, dtype=torch.float32).pin_memory() for n, _ in DECODE_SHAPES]
+
+    def e2e_step(i):
+        wset = ws[i % copies]
+        for k in (7168, 128):
+            xs[k].copy_(xh[k], non_blocking=True)
+            q8p.quantize_q8_0(xs[k], *planes[k])
+        for j, (n, k) in enumerate(DECODE_SHAPES):
+            q8p.q8_0_gemv(wset[j], n, k, *planes[k], ys[j])
+            yh[j].copy_(ys[j], non_blocking=True)
+        stream.synchronize()
+
+    for i in range(warmup):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    e0 = time.perf_counter()
+    for i in range(steps):
+        e2e_step(warmup + i)
+    e_s = time.perf_counter() - e0
+    q8p.q8_check()
+    return dict(ms=ms, kern_ms=kern_ms, clocks=clocks, e2e_s=e2e_s, copies=copies,
+                h2d=sum(v.nbytes for v in xs_h.values()), d2h=4 * sum(n for n, _ in DECODE_SHAPES))
+
+
+# ---------------------------------------------------------------------------
+# prefill chain
+# ---------------------------------------------------------------------------
+def prefill_inputs():
+    T, d, nf = PREFILL["tokens"], PREFILL["d"], PREFILL["nf"]
+    g = syn.rng(3, 0)
+    x = syn.activations(g, T, d)
+    w = syn.uniform(g, d, 0.5, 1.5)
+    wg = syn.q8_0_weights(syn.rng(3, 1), nf, d)[0]
+    wu = syn.q8_0_weights(syn.rng(3, 2), nf, d)[0]
+    wd = syn.q8_0_weights(syn.rng(3, 3), d, nf)[0]
+    return x, w, wg, wu, wd
+
+
+def run_prefill(torch, q8p, steps, warmup, dev):
+    T, d, nf, eps = PREFILL["tokens"], PREFILL["d"], PREFILL["nf"], PREFILL["eps"]
+    x_h, w_h, wg_h, wu_h, wd_h = prefill_inputs()
+    x, w, wg, wu, wd = (torch.from_numpy(a).to(dev) for a in (x_h, w_h, wg_h, wu_h, wd_h))
+    tp = q8p.q8_plane_rows(T)
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    pa = q8p.empty_plane(tp, d, dev)
+    G = torch.empty((T, nf), dtype=torch.float32, device=dev)
+    U = torch.empty((T, nf), dtype=torch.float32, device=dev)
+    Y = torch.empty((T, nf), dtype=torch.float32, device=dev)
+    pb = q8p.empty_plane(tp, nf, dev)
+    O = torch.empty((T, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    names = ["rmsnorm_quant", "gemm_gate", "gemm_up", "swiglu_quant", "gemm_down"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+
+        mark(0)
+        q8p.rmsnorm_quant(x, w, eps, y, *pa)
+        mark(1)
+        q8p.q8_0_gemm(wg, nf, d, *pa, T, G)
+        mark(2)
+        q8p.q8_0_gemm(wu, nf, d, *pa, T, U)
+        mark(3)
+        q8p.swiglu_quant(G, U, Y, *pb)
+        mark(4)
+        q8p.q8_0_gemm(wd, d, nf, *pb, T, O)
+        mark(5)
+
+    for _ in range(warmup):
+        step()
+    q8p.q8_check()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    q8p.q8_check()
+    per = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, nm in enumerate(names)}
+    return per
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reported baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_decode_sample(budget_s):
+    import oracle
+
+    xs, ws = decode_inputs()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        planes = {k: oracle.quantize(v) for k, v in xs.items()}
+        for (n, k), wb in zip(DECODE_SHAPES, ws):
+            oracle.gemv(wb, n, k, *planes[k])
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return dict(value=decode_bytes() * reps / el / 1e9, unit="GB/s", cores=oracle.num_threads(), kind="oracle",
+                sample=f"{reps} full decode steps (quantize + 3 GEMVs of the sweep) in {el:.1f} s")
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+
+    xs, ws = decode_inputs()
+    per = []
+    for _ in range(args.warmup):
+        planes = {k: oracle.quantize(v) for k, v in xs.items()}
+        oracle.gemv(ws[0], *DECODE_SHAPES[0], *planes[7168])
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        planes = {k: oracle.quantize(v) for k, v in xs.items()}
+        for (n, k), wb in zip(DECODE_SHAPES, ws):
+            oracle.gemv(wb, n, k, *planes[k])
+        per.append(time.perf_counter() - t0)
+    tot = sum(per)
+    value = decode_bytes() * args.steps / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": decode_config(None),
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{args.steps} full decode steps of the sweep, each timed"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def decode_config(copies):
+    return {"workload": "decode GEMV sweep b=1: q8_0 quantize + Q8_0 GEMV (n,k) in {(12288,7168),(96,7168),(512,128)}",
+            "activation": "f32 ~N(0,1.5), 1% outliers x20, seed 1", "weights": "Q8_0, d~U(0.002,0.02), q~U{-127..127}",
+            "l2": (f"weights rotate through {copies} copies ({copies} x 94.4 MB > 4 x L2)" if copies else "n/a (CPU)"),
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+
+    import int8_quantized_projection_gb300 as q8p
+    from int8_quantized_projection_gb300 import build as b
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    if rank == 0:
+        b.build()
+    if world > 1:
+        torch.distributed.barrier()
+    q8p.lib()
+
+    cpu = None
+    if rank == 0:  # oracle baseline before any GPU work is timed (host cores only)
+        cpu = oracle_decode_sample(args.cpu_budget)
+
+    sampler = ClockSampler(gpu_smi_id(torch, dev))
+    if world > 1:
+        torch.distributed.barrier()
+    dec = run_decode(torch, q8p, args.steps, args.warmup, dev, sampler)
+    ms, e2e_s = dec["ms"], dec["e2e_s"]
+    if world > 1:
+        t = torch.tensor([ms, e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_s = float(t[0]), float(t[1])
+
+    pre = None
+    if not args.no_prefill:
+        pre = run_prefill(torch, q8p, max(3, args.steps // 6), args.warmup, dev)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peaks = measured_peaks()
+    step_bytes = decode_bytes()
+    value = world * step_bytes * args.steps / (ms / 1e3) / 1e9
+    big = bytes_gemv(*DECODE_SHAPES[0])
+    achieved = big / (dec["kern_ms"] / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": decode_config(dec["copies"]),
+        "roofline": {"kernel": "q8_0_gemv 12288x7168 (gemv_staged_kernel)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+                     "traffic": NCU_TRAFFIC_BYTES["gemv_staged_kernel 12288x7168"],
+                     "algorithmic_bytes": big, "avg_launch_us": round(dec["kern_ms"] * 1e3, 3)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * step_bytes * args.steps / dec["e2e_s"] / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"]},
+        "clocks": dec["clocks"],
+        "gpu_launches": 5 * args.steps,
+    }
+    if pre is not None:
+        T, d, nf = PREFILL["tokens"], PREFILL["d"], PREFILL["nf"]
+        gemm_ms = pre["gemm_gate"] + pre["gemm_up"] + pre["gemm_down"]
+        tops = 3 * ops_gemm(T, nf, d) / (gemm_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        line["prefill"] = {
+            "workload": f"prefill chain T={T} d={d} nf={nf}: rmsnorm_quant, gate/up GEMM, swiglu_quant, down GEMM",
+            "ms_per_chain": round(sum(pre.values()), 4), "ms": {k: round(v, 4) for k, v in pre.items()},
+            "gemm_tops": round(tops, 2), "unit": "int8 TOPS (2*T*N*K per GEMM)",
+            "roofline_gemm": {"bound": "tensor", "achieved": round(tops, 2), "peak": peak, "unit": "TFLOP/s",
+                              "frac": round(tops / peak, 4),
+                              "peak_note": f"sustained dense bf16/f16 tensor peak ({peaks['source']}); sm_103a has "
+                                           "no int8 tcgen05 kind"},
+            "quantize_gbs": {"rmsnorm_quant": round(bytes_rmsnorm_quant(T, d) / pre["rmsnorm_quant"] / 1e6, 1),
+                             "swiglu_quant": round(bytes_swiglu_quant(T, nf) / pre["swiglu_quant"] / 1e6, 1)},
+            "l2": "step working set ~1.2 GB > L2",
+        }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,153 @@
+/*
+ * q8proj.h -- C ABI of the GB300 (sm_103a) int8 quantized projection library
+ * (libq8proj.so).
+ *
+ * The path: an f32 activation is encoded once into a q8_0 "plane", either by a
+ * standalone quantizer or by the producer kernel that computes it (RMSNorm or
+ * SwiGLU), and that plane is contracted with Q8_0 weights by a batch-1 GEMV
+ * (decode) or a GEMM (prefill).
+ *
+ * Formats
+ *   Q8_0 weight block: 34 bytes -- little-endian f16 scale d at +0, then 32
+ *     int8 values at +2.  A weight matrix of n rows and k columns is n rows of
+ *     k/32 consecutive blocks (row pitch 34*k/32 bytes), with no padding.
+ *     ("Part 4 - Lecture 05 - Fusion and the Activation-Quantization
+ *     Discipline", sec. 2.1.)
+ *   q8_0 activation plane: per token row t and 32-element block b,
+ *       qs[t*k + 32*b + j]  int8, j = 0..31
+ *       ds[t*(k/32) + b]    uint32: f16 bits of d in bits 0..15, the int16
+ *                           block sum ssum = sum_j q_j in bits 16..31
+ *     with d = amax/127 (computed in f32), q = rint(x * (1/d)) clamped to
+ *     [-127, 127], d stored rounded to f16.  The plane has rows_pad >= rows
+ *     rows; rows rows..rows_pad-1 are written as zeros.
+ *     ("54 - r51 - producer-fused A-quantize mode 1", sec. 2.1 and 3.1.)
+ *
+ * Conventions for every entry point
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or caches device memory between calls.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; the call returns before the
+ *     GPU finishes.  Errors that only the GPU can detect (a bounded wait that
+ *     ran out) are reported by q8_check().
+ *   - Outputs are overwritten, never accumulated into, and must not alias
+ *     any input.
+ *   - Sizes are int64_t element counts; k must be a positive multiple of 32.
+ *   - Pointers must be 16-byte aligned (Q8_ERR_ALIGN otherwise).
+ *   - The return value is a status code (Q8_OK = 0).  On a non-zero return
+ *     nothing was enqueued.  There is no fallback path: a rejected shape is
+ *     an error, not a slow path.
+ */
+#ifndef Q8PROJ_H
+#define Q8PROJ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define Q8_API __attribute__((visibility("default")))
+#else
+#define Q8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q8_OK                 0
+#define Q8_ERR_ARG            1  /* NULL pointer, non-positive or inconsistent size, k % 32 != 0 */
+#define Q8_ERR_ALIGN          2  /* a pointer is not 16-byte aligned */
+#define Q8_ERR_DEVICE         3  /* current device is not sm_103 (GB300) or cannot be queried */
+#define Q8_ERR_LAUNCH         4  /* the kernel launch failed (cudaGetLastError) */
+#define Q8_ERR_DEVICE_TIMEOUT 5  /* a bounded on-device wait ran out (reported by q8_check) */
+#define Q8_ERR_CUDA           6  /* another CUDA runtime error (stream sync, symbol copy) */
+
+/* Recommended number of plane rows for `rows` tokens: rows rounded up to a
+ * multiple of 128 (the GEMM's token tile).  Any rows_pad >= rows is accepted
+ * by every entry point; this is a convenience only. */
+Q8_API int64_t q8_plane_rows(int64_t rows);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+Q8_API const char *q8_strerror(int status);
+
+/*
+ * quantize_q8_0 -- standalone q8_0 quantizer (the "prepass").
+ *   x   : f32 [rows][k] row-major (input)
+ *   qs  : int8 [rows_pad][k] (output plane values)
+ *   ds  : uint32 [rows_pad][k/32] (output packed d | ssum)
+ * rows >= 0 (rows = 0 only zero-fills), rows_pad >= max(rows, 1), k % 32 == 0.
+ * Defined by the quantize body of "54 - r51 - producer-fused A-quantize
+ * mode 1", sec. 3.2, and the zero tail of sec. 3.1.
+ */
+Q8_API int quantize_q8_0(const float *x, int64_t rows, int64_t k,
+                  int8_t *qs, uint32_t *ds, int64_t rows_pad, void *stream);
+
+/*
+ * rmsnorm_quant -- RMSNorm fused with q8_0 quantization of its output.
+ *   x   : f32 [rows][d] (input)       w : f32 [d] (input weight)
+ *   y   : f32 [rows][d] (output, y = (x * rsqrt(mean(x^2) + eps)) * w)
+ *   qs, ds : plane of y with rows_pad rows (output); the plane is exactly the
+ *            q8_0 encoding of the f32 values written to y.
+ * d % 32 == 0, d <= 32768 (the row is held in registers), rows >= 0,
+ * rows_pad >= max(rows, 1).
+ * "54 - r51 - producer-fused A-quantize mode 1", sec. 2.3 and 3.2
+ * (rms_norm_quant_f32_t: one pass writes y and the plane).
+ */
+Q8_API int rmsnorm_quant(const float *x, const float *w, float eps, float *y,
+                  int64_t rows, int64_t d,
+                  int8_t *qs, uint32_t *ds, int64_t rows_pad, void *stream);
+
+/*
+ * swiglu_quant -- SwiGLU fused with q8_0 quantization of its output.
+ *   gate, up : f32 [rows][nf] (inputs)
+ *   y        : f32 [rows][nf] (output, y = gate / (1 + exp(-gate)) * up)
+ *   qs, ds   : plane of y (output), exactly the q8_0 encoding of y.
+ * nf % 32 == 0, rows >= 0, rows_pad >= max(rows, 1).
+ * "54 - r51 - producer-fused A-quantize mode 1", sec. 3.2
+ * (swiglu_quant_f32_t).
+ */
+Q8_API int swiglu_quant(const float *gate, const float *up, float *y,
+                 int64_t rows, int64_t nf,
+                 int8_t *qs, uint32_t *ds, int64_t rows_pad, void *stream);
+
+/*
+ * q8_0_gemv -- batch-1 projection y[i] = sum_b d_w(i,b) * d_a(b) * sum_j qw*qa.
+ *   w      : n rows of k/32 Q8_0 blocks (input, 16-byte aligned base)
+ *   qs, ds : plane row 0 (input; only row 0 is read)
+ *   y      : f32 [n] (output)
+ * n >= 1, k % 32 == 0.  Row grouping and the split of k across warps are
+ * chosen from (n, k) alone, deterministically; results are run-to-run
+ * identical.  "Part 4 - Lecture 05", sec. 2.1-2.4.
+ */
+Q8_API int q8_0_gemv(const void *w, int64_t n, int64_t k,
+              const int8_t *qs, const uint32_t *ds, float *y, void *stream);
+
+/*
+ * q8_0_gemm -- prefill projection Y[t][i] = sum_b d_w(i,b) * d_a(t,b) * isum.
+ *   w      : n rows of k/32 Q8_0 blocks (input)
+ *   qs, ds : plane with rows_pad >= t rows (input; rows >= t are not read)
+ *   y      : f32 [t][n] row-major (output)
+ * n >= 1, t >= 1, k % 32 == 0.  Every 32-wide k block is one q8_0 block on
+ * both sides, so its integer dot product is scaled by d_w * d_a once.
+ * "12 - r5-r6 re-ranking + structural rewrite spec", sec. 2 and 3.1;
+ * "54 - r51 - producer-fused A-quantize mode 1", sec. 2.1.
+ */
+Q8_API int q8_0_gemm(const void *w, int64_t n, int64_t k,
+              const int8_t *qs, const uint32_t *ds, int64_t t, int64_t rows_pad,
+              float *y, void *stream);
+
+/*
+ * q8_check -- synchronise `stream`, then read and clear the library's device
+ * error word.  Returns Q8_OK, Q8_ERR_DEVICE_TIMEOUT if a bounded on-device
+ * wait ran out since the last check (the affected outputs are undefined), or
+ * Q8_ERR_CUDA if the synchronisation itself failed.
+ */
+Q8_API int q8_check(void *stream);
+
+/* Number of SMs of the current device (0 on error); used by the host-side
+ * dispatch and exported for tests. */
+Q8_API int q8_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q8PROJ_H */

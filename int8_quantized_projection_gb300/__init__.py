@@ -1,1 +1,23 @@
-"""GB300-native int8 quantized projection (q8_0 activation quantize -> Q8_0 GEMV / GEMM)."""
+"""GB300-native int8 quantized projection: q8_0 activation quantization (standalone or
+fused into RMSNorm / SwiGLU) feeding a batch-1 Q8_0 GEMV and a prefill Q8_0 GEMM.
+
+The compute is in ``libq8proj.so`` (hand-written CUDA for sm_103a, C ABI in
+``include/q8proj.h``); this package only builds it and binds it.  Importing
+the package does not load the library; the first call does, and fails loudly
+if it was not built.
+"""
+from ._binding import (  # noqa: F401
+    Q8Error,
+    empty_plane,
+    lib,
+    library_path,
+    load,
+    q8_0_gemm,
+    q8_0_gemv,
+    q8_check,
+    q8_num_sms,
+    q8_plane_rows,
+    quantize_q8_0,
+    rmsnorm_quant,
+    swiglu_quant,
+)

@@ -1,0 +1,174 @@
+"""ctypes binding of libq8proj.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of its own: it checks tensor dtypes/shapes/devices, passes raw
+device pointers, sizes and the current CUDA stream, and turns a non-zero
+status into :class:`Q8Error`.  If the library is missing the call fails
+loudly; there is no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS_NAMES = {0: "Q8_OK", 1: "Q8_ERR_ARG", 2: "Q8_ERR_ALIGN", 3: "Q8_ERR_DEVICE", 4: "Q8_ERR_LAUNCH",
+                5: "Q8_ERR_DEVICE_TIMEOUT", 6: "Q8_ERR_CUDA"}
+
+# (name, restype, argtypes) of every symbol include/q8proj.h declares.
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+SIGNATURES = {
+    "q8_plane_rows": (_I64, [_I64]),
+    "q8_strerror": (ctypes.c_char_p, [_INT]),
+    "quantize_q8_0": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P]),
+    "rmsnorm_quant": (_INT, [_P, _P, ctypes.c_float, _P, _I64, _I64, _P, _P, _I64, _P]),
+    "swiglu_quant": (_INT, [_P, _P, _P, _I64, _I64, _P, _P, _I64, _P]),
+    "q8_0_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "q8_0_gemm": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
+    "q8_check": (_INT, [_P]),
+    "q8_num_sms": (_INT, []),
+}
+
+
+class Q8Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = lib().q8_strerror(status).decode() if _lib is not None else ""
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}: {msg}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libq8proj.so (built in-tree by ``build.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libq8proj.so is not built ({path}); run int8_quantized_projection_gb300.build")
+            h = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(h, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = h
+        return _lib
+
+
+def load():
+    return lib()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn, st):
+    if st != 0:
+        raise Q8Error(fn, st)
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA tensor of {dtype}, got {t.dtype} on {t.device}")
+
+
+def q8_plane_rows(rows: int) -> int:
+    return int(lib().q8_plane_rows(rows))
+
+
+def q8_num_sms() -> int:
+    return int(lib().q8_num_sms())
+
+
+def q8_check(stream=None) -> None:
+    _check("q8_check", lib().q8_check(_stream(stream)))
+
+
+def quantize_q8_0(x, qs, ds, stream=None):
+    """x f32 [rows][k] -> plane (qs int8 [rows_pad][k], ds int32 [rows_pad][k/32])."""
+    import torch
+
+    _need(x, torch.float32, "x"), _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds")
+    rows, k = x.shape
+    rows_pad = qs.shape[0]
+    if qs.shape != (rows_pad, k) or ds.shape != (rows_pad, k // 32):
+        raise ValueError("plane shape mismatch")
+    _check("quantize_q8_0", lib().quantize_q8_0(_ptr(x), rows, k, _ptr(qs), _ptr(ds), rows_pad, _stream(stream)))
+
+
+def rmsnorm_quant(x, w, eps: float, y, qs, ds, stream=None):
+    import torch
+
+    for t, n in ((x, "x"), (w, "w"), (y, "y")):
+        _need(t, torch.float32, n)
+    _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds")
+    rows, d = x.shape
+    rows_pad = qs.shape[0]
+    if y.shape != x.shape or w.shape != (d,) or qs.shape != (rows_pad, d) or ds.shape != (rows_pad, d // 32):
+        raise ValueError("shape mismatch")
+    _check("rmsnorm_quant", lib().rmsnorm_quant(_ptr(x), _ptr(w), ctypes.c_float(eps), _ptr(y), rows, d, _ptr(qs),
+                                                _ptr(ds), rows_pad, _stream(stream)))
+
+
+def swiglu_quant(gate, up, y, qs, ds, stream=None):
+    import torch
+
+    for t, n in ((gate, "gate"), (up, "up"), (y, "y")):
+        _need(t, torch.float32, n)
+    _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds")
+    rows, nf = gate.shape
+    rows_pad = qs.shape[0]
+    if up.shape != gate.shape or y.shape != gate.shape or qs.shape != (rows_pad, nf) or ds.shape != (rows_pad, nf // 32):
+        raise ValueError("shape mismatch")
+    _check("swiglu_quant", lib().swiglu_quant(_ptr(gate), _ptr(up), _ptr(y), rows, nf, _ptr(qs), _ptr(ds), rows_pad,
+                                              _stream(stream)))
+
+
+def q8_0_gemv(w, n: int, k: int, qs, ds, y, stream=None):
+    """w uint8 [n*k/32*34] Q8_0 blocks; plane row 0 of (qs, ds); y f32 [n]."""
+    import torch
+
+    _need(w, torch.uint8, "w"), _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds"), _need(y, torch.float32, "y")
+    if w.numel() != n * (k // 32) * 34 or y.numel() < n or qs.shape[-1] != k:
+        raise ValueError("shape mismatch")
+    _check("q8_0_gemv", lib().q8_0_gemv(_ptr(w), n, k, _ptr(qs), _ptr(ds), _ptr(y), _stream(stream)))
+
+
+def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, stream=None):
+    """Y[t][n] f32 = plane rows [0, t) x Q8_0 weights."""
+    import torch
+
+    _need(w, torch.uint8, "w"), _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds"), _need(y, torch.float32, "y")
+    rows_pad = qs.shape[0]
+    if w.numel() != n * (k // 32) * 34 or y.numel() < t * n or qs.shape[-1] != k or ds.shape[0] != rows_pad:
+        raise ValueError("shape mismatch")
+    _check("q8_0_gemm", lib().q8_0_gemm(_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y), _stream(stream)))
+
+
+def empty_plane(rows_pad: int, k: int, device="cuda"):
+    """Allocate (with PyTorch) an uninitialised plane: (qs int8, ds int32)."""
+    import torch
+
+    return (torch.empty((rows_pad, k), dtype=torch.int8, device=device),
+            torch.empty((rows_pad, k // 32), dtype=torch.int32, device=device))

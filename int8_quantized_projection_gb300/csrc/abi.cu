@@ -1,0 +1,127 @@
+// abi.cu -- C ABI plumbing of libq8proj: device checks, status codes,
+// q8_check, and the GEMM dispatch by shape.
+#include <mutex>
+
+#include "q8_common.cuh"
+
+namespace q8 {
+
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSlots = 8;
+int g_sms[kMaxDevices];        // 0 = not queried yet
+int g_is103[kMaxDevices];      // 0 = unknown, 1 = yes, 2 = no
+int g_smem_set[kMaxDevices][kMaxSlots];
+std::mutex g_mu;
+
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+void query(int dev)
+{
+    cudaDeviceProp p;
+    if (cudaGetDeviceProperties(&p, dev) != cudaSuccess) {
+        g_sms[dev] = 0;
+        g_is103[dev] = 2;
+        return;
+    }
+    g_sms[dev] = p.multiProcessorCount;
+    g_is103[dev] = (p.major == 10 && p.minor == 3) ? 1 : 2;
+}
+} // namespace
+
+int device_sm_count()
+{
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_is103[dev] == 0) query(dev);
+    return g_sms[dev];
+}
+
+bool device_is_sm103()
+{
+    const int dev = current_device();
+    if (dev < 0) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_is103[dev] == 0) query(dev);
+    return g_is103[dev] == 1;
+}
+
+bool set_max_dynamic_smem(const void *func, int bytes, int slot)
+{
+    const int dev = current_device();
+    if (dev < 0 || slot < 0 || slot >= kMaxSlots) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_smem_set[dev][slot] >= bytes) return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    g_smem_set[dev][slot] = bytes;
+    return true;
+}
+
+int launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_LAUNCH;
+}
+
+int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                        int64_t tokens, cudaStream_t s);
+int gemm_mma_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t, float *y,
+                    cudaStream_t s);
+
+// No GEMM kernel has a bounded wait yet; its error word is always clear.
+int gemm_take_error(cudaStream_t) { return Q8_OK; }
+
+} // namespace q8
+
+extern "C" int64_t q8_plane_rows(int64_t rows)
+{
+    if (rows <= 0) return 128;
+    return (rows + 127) / 128 * 128;
+}
+
+extern "C" const char *q8_strerror(int status)
+{
+    switch (status) {
+    case Q8_OK: return "ok";
+    case Q8_ERR_ARG: return "invalid argument (null pointer, size, or k % 32 != 0)";
+    case Q8_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case Q8_ERR_DEVICE: return "current device is not sm_103 (GB300)";
+    case Q8_ERR_LAUNCH: return "kernel launch failed";
+    case Q8_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait ran out";
+    case Q8_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int q8_num_sms(void) { return q8::device_sm_count(); }
+
+extern "C" int q8_check(void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return Q8_ERR_CUDA;
+    const int a = q8::gemv_take_error(s);
+    const int b = q8::gemm_take_error(s);
+    if (a == Q8_ERR_CUDA || b == Q8_ERR_CUDA) return Q8_ERR_CUDA;
+    if (a != Q8_OK) return a;
+    return b;
+}
+
+extern "C" int q8_0_gemm(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t,
+                         int64_t rows_pad, float *y, void *stream)
+{
+    if (!w || !qs || !ds || !y || n < 1 || t < 1 || k <= 0 || (k % 32) != 0 || rows_pad < t) return Q8_ERR_ARG;
+    if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((k / 32) % 8 != 0) {
+        if (t > 65535) return Q8_ERR_ARG;  // generic kernel: one grid row per token
+        return q8::gemv_generic_launch(w, n, k, qs, ds, y, t, s);
+    }
+    if (t > int64_t(65535) * 64) return Q8_ERR_ARG;
+    return q8::gemm_mma_launch(w, n, k, qs, ds, t, y, s);
+}

@@ -1,0 +1,303 @@
+// gemv.cu -- batch-1 Q8_0 x q8_0 projection (decode).
+//
+// y[i] = sum_b d_w(i,b) * d_a(b) * sum_j qw(i,b,j) * qa(b,j)
+//
+// The defects listed in "Part 4 - Lecture 05 - Fusion and the
+// Activation-Quantization Discipline" (sec. 2.1-2.4) and how this kernel
+// avoids them on GB300:
+//   2.1  A 34-byte block is only 2-byte aligned.  Eight consecutive blocks
+//        are 272 = 17 x 16 bytes, so when k/32 is a multiple of 8 every row,
+//        and every group of 8 blocks in it, starts 16-byte aligned.  The
+//        weight stream is moved by cp.async.bulk (the TMA unit) in pieces of
+//        up to 32 such units straight into shared memory; lanes then read
+//        their unit with conflict-free 16-byte shared loads and rebuild the
+//        unaligned qs words with one byte-permute each.
+//   2.2  The inner product is __dp4a on packed int8 words.
+//   2.3  The activation (k bytes of qs + k/8 bytes of d|ssum) is staged once
+//        per CTA in shared memory, padded so that lanes reading different
+//        units hit different banks; no activation traffic reaches HBM/L2
+//        after the prologue.
+//   2.4  Lanes per row is the next power of two of the row's unit count
+//        (capped at 32), so short rows share a warp instead of idling lanes;
+//        the grid is a persistent set of at most one CTA per SM whose warp
+//        count shrinks for small n, so small projections still spread over
+//        many SMs.
+// Shapes whose k/32 is not a multiple of 8 (or whose activation would not
+// fit in shared memory) use gemv_generic_kernel: plain 2-byte loads, the same
+// lanes-per-row fitting, no staging.
+#include "q8_common.cuh"
+
+namespace {
+
+__device__ unsigned int g_gemv_err;
+
+constexpr int kUnitBytes = 272;                 // 8 Q8_0 blocks
+constexpr int kActUnitBytes = 304;              // 256 B qs + 32 B ds, padded to 76 words
+constexpr int kPieceUnits = 32;
+constexpr int kPieceBytes = kPieceUnits * kUnitBytes;  // 8704
+constexpr int kStages = 3;
+constexpr int kMaxWarps = 4;
+constexpr int kMaxActUnits = 256;               // k <= 65536 on the staged path
+
+struct GvGeom {
+    int64_t n;       // weight rows
+    int nu;          // 8-block units per row
+    int lpr_log2;    // lanes per row = 1 << lpr_log2
+    int rpw;         // rows per piece
+    int ppr;         // pieces per row group
+    int64_t groups;  // row groups = ceil(n / rpw)
+};
+
+__host__ __device__ inline int smem_header_bytes() { return kMaxWarps * kStages * 8 + 128; }
+
+// One 8-block unit: 17 x 16 B of weights (in shared memory) against the
+// matching 256 B of qs and 8 ds words of the activation (in shared memory).
+__device__ __forceinline__ float unit_dot(const uint8_t *wu, const uint8_t *au)
+{
+    uint32_t wv[68];
+#pragma unroll
+    for (int c = 0; c < 17; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(wu + 16 * c);
+        wv[4 * c + 0] = v.x;
+        wv[4 * c + 1] = v.y;
+        wv[4 * c + 2] = v.z;
+        wv[4 * c + 3] = v.w;
+    }
+    const uint4 ad0 = *reinterpret_cast<const uint4 *>(au + 256);
+    const uint4 ad1 = *reinterpret_cast<const uint4 *>(au + 272);
+    const uint32_t ad[8] = {ad0.x, ad0.y, ad0.z, ad0.w, ad1.x, ad1.y, ad1.z, ad1.w};
+    float acc = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const uint4 a0 = *reinterpret_cast<const uint4 *>(au + 32 * b);
+        const uint4 a1 = *reinterpret_cast<const uint4 *>(au + 32 * b + 16);
+        const uint32_t aq[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        // block b: f16 d at byte 34b, qs at 34b + 2 (word-aligned for odd b only)
+        const uint32_t dbits = (b & 1) ? (wv[(17 * b - 1) / 2] >> 16) : (wv[17 * b / 2] & 0xffffu);
+        int isum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int o = 34 * b + 2 + 4 * i;
+            const uint32_t qw = (o & 3) ? __byte_perm(wv[o >> 2], wv[(o >> 2) + 1], 0x5432) : wv[o >> 2];
+            isum = q8::dp4a(qw, aq[i], isum);
+        }
+        const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+        const float da = __half2float(__ushort_as_half(static_cast<unsigned short>(ad[b] & 0xffffu)));
+        acc = fmaf(dw * da, static_cast<float>(isum), acc);  // dw*da is exact in f32
+    }
+    return acc;
+}
+
+__global__ void __launch_bounds__(kMaxWarps * 32)
+gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_row,
+                   const uint4 *__restrict__ ds_row, float *__restrict__ y, GvGeom g)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nwarp = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *act = smem + smem_header_bytes();
+    uint8_t *ring = act + ((g.nu * kActUnitBytes + 127) & ~127);
+    uint64_t *mybar = bars + warp * kStages;
+    uint8_t *myring = ring + warp * kStages * kPieceBytes;
+
+    const int64_t pitch = static_cast<int64_t>(g.nu) * kUnitBytes;
+    const int64_t W = static_cast<int64_t>(gridDim.x) * nwarp;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarp + warp;
+    const int64_t g0 = g.groups * gw / W, g1 = g.groups * (gw + 1) / W;
+    const int64_t npieces = (g1 - g0) * g.ppr;
+
+    // piece i of this warp -> (global source, bytes)
+    auto piece = [&](int64_t i, uint32_t &bytes) -> const uint8_t * {
+        const int64_t grp = g0 + i / g.ppr;
+        if (g.rpw == 1) {  // one row per piece, up to 32 units of it
+            const int p = static_cast<int>(i % g.ppr);
+            const int units = min(kPieceUnits, g.nu - kPieceUnits * p);
+            bytes = static_cast<uint32_t>(units * kUnitBytes);
+            return w + grp * pitch + static_cast<int64_t>(kPieceUnits) * p * kUnitBytes;
+        }
+        const int64_t r0 = grp * g.rpw;
+        const int64_t rows = min(static_cast<int64_t>(g.rpw), g.n - r0);
+        bytes = static_cast<uint32_t>(rows * pitch);
+        return w + r0 * pitch;
+    };
+
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) q8::mbar_init(&mybar[s], 1);
+        q8::fence_mbar_init();
+        for (int s = 0; s < kStages && s < npieces; ++s) {
+            uint32_t bytes;
+            const uint8_t *src = piece(s, bytes);
+            q8::mbar_arrive_expect_tx(&mybar[s], bytes);
+            q8::bulk_g2s(myring + s * kPieceBytes, src, bytes, &mybar[s]);
+        }
+    }
+    // stage the activation: unit u = 16 x 16 B of qs then 2 x 16 B of ds
+    for (int idx = threadIdx.x; idx < g.nu * 18; idx += blockDim.x) {
+        const int u = idx / 18, c = idx - u * 18;
+        const uint4 v = (c < 16) ? __ldg(qs_row + u * 16 + c) : __ldg(ds_row + u * 2 + (c - 16));
+        *reinterpret_cast<uint4 *>(act + u * kActUnitBytes + 16 * c) = v;
+    }
+    __syncthreads();
+
+    const int lpr = 1 << g.lpr_log2;
+    const int ri = lane >> g.lpr_log2;         // row within a piece
+    const int uj = lane & (lpr - 1);           // unit within a piece
+    float acc = 0.0f;
+    for (int64_t i = 0; i < npieces; ++i) {
+        const int s = static_cast<int>(i % kStages);
+        const uint32_t par = static_cast<uint32_t>((i / kStages) & 1);
+        const bool ok = q8::mbar_wait_bounded(&mybar[s], par);
+        if (!__all_sync(Q8_FULL_MASK, ok)) {
+            if (lane == 0) atomicOr(&g_gemv_err, 1u);
+            return;
+        }
+        const uint8_t *buf = myring + s * kPieceBytes;
+        const int64_t grp = g0 + i / g.ppr;
+        const int p = static_cast<int>(i % g.ppr);
+        int64_t row;
+        int unit, soff;
+        bool valid;
+        if (g.rpw == 1) {
+            row = grp;
+            unit = kPieceUnits * p + lane;
+            soff = lane * kUnitBytes;
+            valid = unit < g.nu;
+        } else {
+            row = grp * g.rpw + ri;
+            unit = uj;
+            soff = (ri * g.nu + uj) * kUnitBytes;
+            valid = uj < g.nu && row < g.n;
+        }
+        if (valid) acc += unit_dot(buf + soff, act + unit * kActUnitBytes);
+        __syncwarp();
+        if (lane == 0 && i + kStages < npieces) {
+            uint32_t bytes;
+            const uint8_t *src = piece(i + kStages, bytes);
+            q8::mbar_arrive_expect_tx(&mybar[s], bytes);
+            q8::bulk_g2s(myring + s * kPieceBytes, src, bytes, &mybar[s]);
+        }
+        if (p == g.ppr - 1) {  // row group complete: reduce over the lanes of each row
+            for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(Q8_FULL_MASK, acc, o);
+            if (uj == 0 && row < g.n) y[row] = acc;
+            acc = 0.0f;
+        }
+    }
+}
+
+// Generic path: any k % 32 == 0.  Warp = 32 / lpr rows; lane (i, j) handles
+// blocks j, j + lpr, ... of row r0 + i.  blockIdx.y selects the token (the
+// same kernel serves the GEMM's odd shapes).
+__global__ void __launch_bounds__(128)
+gemv_generic_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, const int8_t *__restrict__ qs,
+                    const uint32_t *__restrict__ ds, float *__restrict__ y, int lpr_log2)
+{
+    const int lane = threadIdx.x & 31;
+    const int lpr = 1 << lpr_log2;
+    const int rpw = 32 >> lpr_log2;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t tok = blockIdx.y;
+    const int64_t row = warp * rpw + (lane >> lpr_log2);
+    const int j = lane & (lpr - 1);
+    const int64_t pitch = static_cast<int64_t>(nb) * 34;
+    const int8_t *qa = qs + tok * static_cast<int64_t>(nb) * 32;
+    const uint32_t *da = ds + tok * nb;
+    float acc = 0.0f;
+    if (row < n) {
+        const uint16_t *wr = reinterpret_cast<const uint16_t *>(w + row * pitch);
+        for (int b = j; b < nb; b += lpr) {
+            const uint16_t *blk = wr + 17 * b;
+            const uint4 a0 = __ldg(reinterpret_cast<const uint4 *>(qa + 32 * b));
+            const uint4 a1 = __ldg(reinterpret_cast<const uint4 *>(qa + 32 * b + 16));
+            const uint32_t aq[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            int isum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t qw = static_cast<uint32_t>(__ldg(blk + 1 + 2 * i)) |
+                                    (static_cast<uint32_t>(__ldg(blk + 2 + 2 * i)) << 16);
+                isum = q8::dp4a(qw, aq[i], isum);
+            }
+            const float dw = __half2float(__ushort_as_half(__ldg(blk)));
+            const float dav = __half2float(__ushort_as_half(static_cast<unsigned short>(__ldg(da + b) & 0xffffu)));
+            acc = fmaf(dw * dav, static_cast<float>(isum), acc);
+        }
+    }
+    for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(Q8_FULL_MASK, acc, o);
+    if (j == 0 && row < n) y[tok * n + row] = acc;
+}
+
+int ceil_log2(int v)
+{
+    int l = 0;
+    while ((1 << l) < v) ++l;
+    return l;
+}
+
+} // namespace
+
+namespace q8 {
+
+int gemv_take_error(cudaStream_t s)
+{
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_gemv_err, sizeof(v), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_gemv_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return Q8_ERR_CUDA;
+    return v ? Q8_ERR_DEVICE_TIMEOUT : Q8_OK;
+}
+
+// Launch the generic kernel for `tokens` plane rows (used by the GEMM too).
+int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                        int64_t tokens, cudaStream_t s)
+{
+    const int nb = static_cast<int>(k / 32);
+    const int lpr_log2 = min(5, ceil_log2(nb));
+    const int rpw = 32 >> lpr_log2;
+    const int64_t warps = (n + rpw - 1) / rpw;
+    const dim3 grid(static_cast<unsigned>((warps + 3) / 4), static_cast<unsigned>(tokens));
+    gemv_generic_kernel<<<grid, 128, 0, s>>>(static_cast<const uint8_t *>(w), n, nb, qs, ds, y, lpr_log2);
+    return launch_status();
+}
+
+} // namespace q8
+
+extern "C" int q8_0_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                         void *stream)
+{
+    if (!w || !qs || !ds || !y || n < 1 || k <= 0 || (k % 32) != 0) return Q8_ERR_ARG;
+    if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t nb = k / 32;
+    if (nb % 8 != 0 || nb / 8 > kMaxActUnits || n > (int64_t(1) << 40))
+        return q8::gemv_generic_launch(w, n, k, qs, ds, y, 1, s);
+
+    GvGeom g;
+    g.n = n;
+    g.nu = static_cast<int>(nb / 8);
+    if (g.nu > kPieceUnits) {
+        g.lpr_log2 = 5;
+        g.rpw = 1;
+        g.ppr = (g.nu + kPieceUnits - 1) / kPieceUnits;
+    } else {
+        g.lpr_log2 = ceil_log2(g.nu);
+        g.rpw = 32 >> g.lpr_log2;
+        g.ppr = 1;
+    }
+    g.groups = (n + g.rpw - 1) / g.rpw;
+    const int sms = q8::device_sm_count();
+    if (sms <= 0) return Q8_ERR_DEVICE;
+    int64_t nw = (g.groups + sms - 1) / sms;
+    nw = nw < 1 ? 1 : (nw > kMaxWarps ? kMaxWarps : nw);
+    int64_t grid = (g.groups + nw - 1) / nw;
+    grid = grid > sms ? sms : grid;
+    const int smem = smem_header_bytes() + ((g.nu * kActUnitBytes + 127) & ~127) +
+                     static_cast<int>(nw) * kStages * kPieceBytes;
+    const int maxs = smem_header_bytes() + kMaxActUnits * kActUnitBytes + kMaxWarps * kStages * kPieceBytes;
+    if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(gemv_staged_kernel), maxs, 0)) return Q8_ERR_LAUNCH;
+    gemv_staged_kernel<<<static_cast<unsigned>(grid), static_cast<unsigned>(nw * 32), smem, s>>>(
+        static_cast<const uint8_t *>(w), reinterpret_cast<const uint4 *>(qs), reinterpret_cast<const uint4 *>(ds), y,
+        g);
+    return q8::launch_status();
+}

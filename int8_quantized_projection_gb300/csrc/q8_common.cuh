@@ -1,0 +1,168 @@
+// q8_common.cuh -- internal helpers of libq8proj (not part of the C ABI).
+//
+// PTX wrappers for sm_103a (mbarrier, bulk/TMA copies, globaltimer), the
+// status plumbing shared by every translation unit, and the register-level
+// q8_0 block encoder used by all three quantizing kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/q8proj.h"
+
+#define Q8_FULL_MASK 0xffffffffu
+
+// A bounded on-device wait gives up after this many nanoseconds, records
+// Q8_ERR_DEVICE_TIMEOUT in the translation unit's error word and lets the
+// kernel return instead of hanging the GPU.
+#ifndef Q8_WAIT_LIMIT_NS
+#define Q8_WAIT_LIMIT_NS 1000000000ull
+#endif
+
+namespace q8 {
+
+// ---------------------------------------------------------------------------
+// host-side helpers (defined in abi.cu)
+// ---------------------------------------------------------------------------
+int device_sm_count();                 // cached per device; 0 on error
+bool device_is_sm103();                // current device is compute capability 10.3
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int launch_status();                   // Q8_OK or Q8_ERR_LAUNCH from cudaGetLastError
+// Raise a kernel's dynamic shared-memory limit once per (device, slot);
+// slots are small integers owned by the calling translation unit.
+bool set_max_dynamic_smem(const void *func, int bytes, int slot);
+
+// Per-translation-unit device error words are read and cleared through these
+// (each .cu file that has bounded waits defines one).
+int gemv_take_error(cudaStream_t s);
+int gemm_take_error(cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// device-side PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false if the wait
+// ran past `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns = Q8_WAIT_LIMIT_NS)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Bulk (non-tensor) copy global -> shared, completion counted in bytes on
+// `bar`.  src, dst 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c)
+{
+    return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
+}
+
+// ---------------------------------------------------------------------------
+// q8_0 encoder: one 32-element block held by 8 consecutive lanes, 4 values
+// per lane (lane & 7 == 0 holds elements 0..3).  Every lane of the warp must
+// call it (full-mask shuffles); lanes whose group is out of range simply
+// discard the result.  Steps as in the quantize body of "54 - r51 -
+// producer-fused A-quantize mode 1", sec. 3.2: block amax, d = amax/127 in
+// f32, di = 1/d (0 when d = 0), q = rint(x*di) clamped to +-127, ssum = sum q,
+// d stored as f16 (round to nearest even).  Division, reciprocal and product
+// are the IEEE round-to-nearest forms, so the codes are a pure function of
+// the f32 inputs.
+// ---------------------------------------------------------------------------
+struct Q8Enc {
+    uint32_t qword;  // 4 int8 codes of this lane, little-endian
+    uint32_t dsword; // f16(d) | ssum << 16 (same value on all 8 lanes)
+};
+
+__device__ __forceinline__ int clamp127(int v) { return max(-127, min(127, v)); }
+
+__device__ __forceinline__ Q8Enc q8_encode8(float4 v)
+{
+    float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    a = fmaxf(a, __shfl_xor_sync(Q8_FULL_MASK, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(Q8_FULL_MASK, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(Q8_FULL_MASK, a, 4));
+    const float d = __fdiv_rn(a, 127.0f);
+    const float di = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+    const int q0 = clamp127(__float2int_rn(__fmul_rn(v.x, di)));
+    const int q1 = clamp127(__float2int_rn(__fmul_rn(v.y, di)));
+    const int q2 = clamp127(__float2int_rn(__fmul_rn(v.z, di)));
+    const int q3 = clamp127(__float2int_rn(__fmul_rn(v.w, di)));
+    int s = q0 + q1 + q2 + q3;
+    s += __shfl_xor_sync(Q8_FULL_MASK, s, 1);
+    s += __shfl_xor_sync(Q8_FULL_MASK, s, 2);
+    s += __shfl_xor_sync(Q8_FULL_MASK, s, 4);
+    Q8Enc e;
+    e.qword = (static_cast<uint32_t>(q0) & 0xffu) | ((static_cast<uint32_t>(q1) & 0xffu) << 8) |
+              ((static_cast<uint32_t>(q2) & 0xffu) << 16) | (static_cast<uint32_t>(q3) << 24);
+    e.dsword = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(d))) |
+               (static_cast<uint32_t>(static_cast<uint16_t>(static_cast<int16_t>(s))) << 16);
+    return e;
+}
+
+} // namespace q8

@@ -1,0 +1,88 @@
+"""Host-side checks of the C ABI: the library builds, loads without a GPU, exports
+every symbol include/q8proj.h declares, and rejects bad arguments before it
+touches the device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int8_quantized_projection_gb300 as q8p
+from int8_quantized_projection_gb300 import _binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q8proj.h")
+
+FAKE = 0x10000      # 16-byte aligned, never dereferenced: every call below fails validation first
+MISALIGNED = 0x10004
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return q8p.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^Q8_API\s+[\w\s\*]+?\**\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    assert declared_symbols() == sorted(_binding.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    # and nothing else of ours leaks (kernels and helpers are hidden)
+    out = os.popen(f"nm -D --defined-only {build.LIB}").read().split("\n")
+    ours = {ln.split()[-1] for ln in out if ln.strip() and ln.split()[-1].startswith(("q8", "quantize", "rmsnorm",
+                                                                                       "swiglu"))}
+    assert ours == set(declared_symbols())
+
+
+def test_plane_rows_and_strerror(lib):
+    assert lib.q8_plane_rows(1) == 128
+    assert lib.q8_plane_rows(128) == 128
+    assert lib.q8_plane_rows(3325) == 3328
+    assert lib.q8_plane_rows(0) == 128
+    for st in range(0, 7):
+        assert lib.q8_strerror(st)
+    assert lib.q8_strerror(99) == b"unknown status"
+
+
+P = ctypes.c_void_p
+
+
+def test_argument_errors_are_reported_before_any_device_work(lib):
+    s = P(0)
+    ERR_ARG, ERR_ALIGN = 1, 2
+    # quantize_q8_0: k % 32, rows_pad < rows, null plane
+    assert lib.quantize_q8_0(P(FAKE), 4, 48, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert lib.quantize_q8_0(P(FAKE), 4, 64, P(FAKE), P(FAKE), 3, s) == ERR_ARG
+    assert lib.quantize_q8_0(P(FAKE), 4, 64, P(0), P(FAKE), 4, s) == ERR_ARG
+    assert lib.quantize_q8_0(P(0), 4, 64, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert lib.quantize_q8_0(P(FAKE), 4, 64, P(MISALIGNED), P(FAKE), 4, s) == ERR_ALIGN
+    assert lib.quantize_q8_0(P(MISALIGNED), 4, 64, P(FAKE), P(FAKE), 4, s) == ERR_ALIGN
+    # rmsnorm_quant: d limit and alignment
+    assert lib.rmsnorm_quant(P(FAKE), P(FAKE), 1e-6, P(FAKE), 2, 32768 + 32, P(FAKE), P(FAKE), 2, s) == ERR_ARG
+    assert lib.rmsnorm_quant(P(FAKE), P(MISALIGNED), 1e-6, P(FAKE), 2, 64, P(FAKE), P(FAKE), 2, s) == ERR_ALIGN
+    # swiglu_quant
+    assert lib.swiglu_quant(P(FAKE), P(FAKE), P(FAKE), 2, 40, P(FAKE), P(FAKE), 2, s) == ERR_ARG
+    assert lib.swiglu_quant(P(FAKE), P(FAKE), P(MISALIGNED), 2, 64, P(FAKE), P(FAKE), 2, s) == ERR_ALIGN
+    # q8_0_gemv
+    assert lib.q8_0_gemv(P(FAKE), 0, 64, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
+    assert lib.q8_0_gemv(P(FAKE), 8, 100, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
+    assert lib.q8_0_gemv(P(FAKE + 2), 8, 64, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ALIGN
+    # q8_0_gemm: rows_pad < t, t < 1
+    assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(FAKE), 5, 4, P(FAKE), s) == ERR_ARG
+    assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(FAKE), 0, 4, P(FAKE), s) == ERR_ARG
+    assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(MISALIGNED), 4, 4, P(FAKE), s) == ERR_ALIGN
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _binding.lib()

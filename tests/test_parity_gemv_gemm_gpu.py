@@ -1,0 +1,202 @@
+"""GPU parity of q8_0_gemv and q8_0_gemm against the oracle.
+
+Outputs are compared element by element with the oracle's fp64 value
+(|dy| <= 1e-5 * sum_b |term_b|), outputs are NaN-poisoned first so a cell the
+kernel never writes fails ("12 - r5-r6 re-ranking + structural rewrite
+spec", sec. 3.3: "zero cells"), and the exact-epilogue configuration
+(power-of-two scales, small values: every f32 operation exact) requires
+bit-equality, which checks the int32 block dot products themselves.  Shapes
+cover the dispatch boundaries of "Part 4 - Lecture 05" sec. 8 (32/64/65
+blocks per row), ragged row counts, k/32 not a multiple of 8 (generic
+kernel), rows longer than one 32-unit piece, tiny n, and every configuration
+of the workloads (full size where the oracle finishes in seconds, sampled
+outputs otherwise).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from int8_quantized_projection_gb300 import synthetic as syn
+
+from ._parity import assert_gemm_close, dev, host, nan_f32
+
+pytestmark = pytest.mark.gpu
+
+
+def _weights(seed, n, k, exact=False):
+    g = syn.rng(60, seed, n, k)
+    blob, d16, q = syn.q8_0_weights(g, n, k)
+    if exact:  # power-of-two scales, |q| <= 3: every f32 product and sum is exact
+        e = g.integers(-12, -2, size=d16.shape)
+        d16 = (2.0 ** e).astype(np.float16).view(np.uint16)
+        q = g.integers(-3, 4, size=q.shape).astype(np.int8)
+        blob = syn.pack_q8_0(d16, q)
+    return blob
+
+
+def _plane(seed, t, k, rows_pad=None, exact=False, sigma=1.5, outlier_frac=0.01):
+    g = syn.rng(61, seed, t, k)
+    if exact:
+        qa = g.integers(-3, 4, size=(t, k)).astype(np.int8)
+        e = g.integers(-12, -2, size=(t, k // 32))
+        d16 = (2.0 ** e).astype(np.float16).view(np.uint16)
+        ssum = qa.reshape(t, k // 32, 32).astype(np.int64).sum(-1)
+        ds = d16.astype(np.uint32) | (ssum.astype(np.int16).view(np.uint16).astype(np.uint32) << 16)
+        rp = rows_pad or t
+        qs_p = np.zeros((rp, k), np.int8)
+        ds_p = np.zeros((rp, k // 32), np.uint32)
+        qs_p[:t], ds_p[:t] = qa, ds
+        return qs_p, ds_p
+    x = syn.activations(g, t, k, sigma=sigma, outlier_frac=outlier_frac)
+    return oracle.quantize(x, rows_pad or t)
+
+
+def _run_gemv(q8, blob, n, k, qs, ds):
+    y = nan_f32(n)
+    q8.q8_0_gemv(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), y)
+    q8.q8_check()
+    return host(y)
+
+
+def _run_gemm(q8, blob, n, k, qs, ds, t):
+    y = nan_f32(t, n)
+    q8.q8_0_gemm(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), t, y)
+    q8.q8_check()
+    return host(y)
+
+
+GEMV_SHAPES = [
+    (256, 512),      # tiny decode (16 blocks/row)
+    (96, 7168),      # small-n grid
+    (512, 128),      # 4 blocks/row: generic kernel, 8 rows per warp
+    (1000, 1024),    # 32 blocks/row (dispatch boundary)
+    (1001, 2048),    # 64 blocks/row, ragged n
+    (333, 2080),     # 65 blocks/row (generic)
+    (77, 18944),     # 592 blocks/row: rows span several 32-unit pieces
+    (1, 256), (3, 96), (5, 32),
+    (4099, 3584),    # ragged n, 112 blocks/row
+]
+
+
+@pytest.mark.parametrize("n,k", GEMV_SHAPES)
+def test_gemv_matches_oracle(q8, n, k):
+    blob = _weights(1, n, k)
+    qs, ds = _plane(1, 1, k)
+    y = _run_gemv(q8, blob, n, k, qs, ds)
+    yr, ar = oracle.gemv(blob, n, k, qs, ds)
+    assert_gemm_close(y, yr, ar, f"gemv {n}x{k}")
+
+
+@pytest.mark.parametrize("n,k", [(12288, 7168), (3072, 7168), (512, 7168), (18944, 3584), (3584, 18944)])
+def test_gemv_full_size_configs(q8, n, k):
+    blob = _weights(2, n, k)
+    qs, ds = _plane(2, 1, k)
+    y = _run_gemv(q8, blob, n, k, qs, ds)
+    yr, ar = oracle.gemv(blob, n, k, qs, ds)
+    assert_gemm_close(y, yr, ar, f"gemv {n}x{k}")
+
+
+@pytest.mark.parametrize("n,k", [(300, 2048), (77, 18944), (512, 128), (129, 7168)])
+def test_gemv_exact_epilogue_bit_equal(q8, n, k):
+    blob = _weights(3, n, k, exact=True)
+    qs, ds = _plane(3, 1, k, exact=True)
+    y = _run_gemv(q8, blob, n, k, qs, ds)
+    yr, _ = oracle.gemv(blob, n, k, qs, ds)
+    assert np.array_equal(y.astype(np.float64), yr)
+
+
+def test_gemv_deterministic(q8):
+    import torch
+
+    n, k = 12288, 7168
+    blob = dev(_weights(4, n, k))
+    qs, ds = _plane(4, 1, k)
+    qs, ds = dev(qs), dev(ds.view(np.int32))
+    outs = []
+    for _ in range(3):
+        y = nan_f32(n)
+        q8.q8_0_gemv(blob, n, k, qs, ds, y)
+        q8.q8_check()
+        outs.append(y.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+GEMM_SHAPES = [
+    (128, 256, 64), (100, 512, 1), (1000, 3584, 63), (1000, 3584, 64), (1000, 3584, 65),
+    (257, 2048, 129), (64, 18944, 200), (300, 1024, 300), (33, 96, 17), (600, 128, 40),
+]
+
+
+@pytest.mark.parametrize("n,k,t", GEMM_SHAPES)
+def test_gemm_matches_oracle(q8, n, k, t):
+    blob = _weights(5, n, k)
+    qs, ds = _plane(5, t, k, rows_pad=((t + 127) // 128) * 128)
+    y = _run_gemm(q8, blob, n, k, qs, ds, t)
+    yr, ar = oracle.gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+    assert_gemm_close(y, yr, ar, f"gemm {n}x{k} t={t}")
+
+
+@pytest.mark.parametrize("n,k,t", [(256, 2048, 130), (640, 18944, 33), (200, 96, 5)])
+def test_gemm_exact_epilogue_bit_equal(q8, n, k, t):
+    blob = _weights(6, n, k, exact=True)
+    qs, ds = _plane(6, t, k, exact=True)
+    y = _run_gemm(q8, blob, n, k, qs, ds, t)
+    yr, _ = oracle.gemm(blob, n, k, qs, ds)
+    assert np.array_equal(y.astype(np.float64), yr)
+
+
+@pytest.mark.parametrize("n,k,t", [(18944, 3584, 3325), (3584, 18944, 3325), (152064, 3584, 16), (3584, 3584, 2048)])
+def test_gemm_full_size_sampled(q8, n, k, t):
+    """Full-size prefill shapes; every output checked for NaN, a sample against the oracle."""
+    import torch
+
+    blob = _weights(7, n, k)
+    qs, ds = _plane(7, t, k, rows_pad=((t + 127) // 128) * 128)
+    y = nan_f32(t, n)
+    q8.q8_0_gemm(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), t, y)
+    q8.q8_check()
+    assert not torch.isnan(y).any().item(), "unwritten outputs"
+    g = syn.rng(62, n, k, t)
+    ti = np.unique(np.concatenate([[0, t - 1], g.integers(0, t, 24)]))
+    ni = np.unique(np.concatenate([[0, n - 1, (n // 128) * 128 - 1], g.integers(0, n, 96)]))
+    yr, ar = oracle.gemm(blob, n, k, qs, ds, t_idx=ti, n_idx=ni)
+    assert_gemm_close(host(y)[np.ix_(ti, ni)], yr, ar, f"gemm {n}x{k} t={t} (sampled)")
+
+
+def test_gemm_deterministic(q8):
+    import torch
+
+    n, k, t = 2048, 3584, 300
+    blob = dev(_weights(8, n, k))
+    qs, ds = _plane(8, t, k, rows_pad=384)
+    qs, ds = dev(qs), dev(ds.view(np.int32))
+    outs = []
+    for _ in range(2):
+        y = nan_f32(t, n)
+        q8.q8_0_gemm(blob, n, k, qs, ds, t, y)
+        q8.q8_check()
+        outs.append(y.clone())
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_shared_activation_decode_chain(q8):
+    """Decode chain of the shared-activation workload: one rmsnorm_quant feeds four GEMVs."""
+    g = syn.rng(2, 0)
+    d = 7168
+    x = syn.activations(g, 1, d)
+    w = syn.uniform(g, d, 0.5, 1.5)
+    y = nan_f32(1, d)
+    import torch
+
+    qs = torch.empty((1, d), dtype=torch.int8, device="cuda")
+    ds = torch.empty((1, d // 32), dtype=torch.int32, device="cuda")
+    q8.rmsnorm_quant(dev(x), dev(w), 1e-6, y, qs, ds)
+    q8.q8_check()
+    qsh, dsh = host(qs), host(ds).view(np.uint32)
+    for i, n in enumerate([3072, 512, 512, 3072]):
+        blob = syn.q8_0_weights(syn.rng(2, 1 + i), n, d)[0]
+        out = nan_f32(n)
+        q8.q8_0_gemv(dev(blob), n, d, qs, ds, out)
+        q8.q8_check()
+        yr, ar = oracle.gemv(blob, n, d, qsh, dsh)
+        assert_gemm_close(host(out), yr, ar, f"decode chain proj {i}")

@@ -1,0 +1,135 @@
+"""GPU parity of the three quantizing kernels against the oracle.
+
+The plane must equal the oracle's encoding bit for bit: of the given x for
+quantize_q8_0, and of the f32 output the kernel itself wrote for the fused
+producers (quantization is a pure function of the f32 bits, "54 - r51 -
+producer-fused A-quantize mode 1", sec. 2.3).  Planes are pre-poisoned so
+an unwritten byte (notably in the zero tail) shows up (sec. 4 of the same
+page).  Shapes include the page's verifier set: nt = 1/63/64/129/3354 at
+d = 3584, d = 896 nt = 300, d = 640 nt = 100, and nf = 18944.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from int8_quantized_projection_gb300 import synthetic as syn
+
+from ._parity import assert_plane_equal, assert_y_close, dev, host, nan_f32, poisoned_plane
+
+pytestmark = pytest.mark.gpu
+
+
+def _edge_rows(k):
+    """Rows of special blocks: zeros, single non-zero, +-amax ties, tiny amax, huge outliers."""
+    rows = np.zeros((6, k), np.float32)
+    rows[1, 5] = -3.25
+    rows[2, 0::2] = 2.0
+    rows[2, 1::2] = -2.0
+    g = syn.rng(50, k)
+    rows[3] = syn.activations(g, 1, k)[0] * np.float32(2.0 ** -100)
+    rows[4] = syn.activations(g, 1, k, sigma=1.5, outlier_frac=0.05, outlier_mult=1000.0)[0]
+    rows[5] = -0.0
+    return rows
+
+
+@pytest.mark.parametrize("rows,k,rows_pad", [(1, 32, 1), (1, 7168, 1), (5, 96, 128), (63, 3584, 128),
+                                             (64, 3584, 64), (129, 640, 256), (300, 896, 300), (3354, 3584, 3456)])
+def test_quantize_q8_0_bit_exact(q8, rows, k, rows_pad):
+    g = syn.rng(51, rows, k)
+    x = syn.activations(g, rows, k, sigma=1.5, outlier_frac=0.01)
+    if rows >= 6:
+        x[:6] = _edge_rows(k)
+    qs, ds = poisoned_plane(rows_pad, k)
+    q8.quantize_q8_0(dev(x), qs, ds)
+    q8.q8_check()
+    qr, dr = oracle.quantize(x, rows_pad)
+    assert_plane_equal(qs, ds, qr, dr, f"quantize {rows}x{k}")
+
+
+def test_quantize_q8_0_zero_rows_only_fills_tail(q8):
+    import torch
+
+    qs, ds = poisoned_plane(128, 64)
+    q8.quantize_q8_0(torch.empty((0, 64), dtype=torch.float32, device="cuda"), qs, ds)
+    q8.q8_check()
+    assert (host(qs) == 0).all() and (host(ds) == 0).all()
+
+
+@pytest.mark.parametrize("rows,d,rows_pad", [(1, 3584, 1), (63, 3584, 64), (64, 3584, 64), (129, 3584, 192),
+                                             (300, 896, 384), (100, 640, 128), (1, 7168, 1), (7, 18944, 8),
+                                             (3354, 3584, 3456), (2, 32768, 2)])
+def test_rmsnorm_quant(q8, rows, d, rows_pad):
+    import torch
+
+    g = syn.rng(52, rows, d)
+    x = syn.activations(g, rows, d)
+    if rows >= 6:
+        x[:6] = _edge_rows(d)
+        x[0, 0] = 1.0  # avoid an all-zero row (ss = 0 -> finite scale, but a degenerate case covered below)
+    w = syn.uniform(g, d, 0.5, 1.5)
+    eps = 1e-6
+    y = nan_f32(rows, d)
+    qs, ds = poisoned_plane(rows_pad, d)
+    q8.rmsnorm_quant(dev(x), dev(w), eps, y, qs, ds)
+    q8.q8_check()
+    assert_y_close(y, oracle.rmsnorm(x, w, eps), f"rmsnorm y {rows}x{d}")
+    qr, dr = oracle.quantize(host(y), rows_pad)
+    assert_plane_equal(qs, ds, qr, dr, f"rmsnorm plane {rows}x{d}")
+    # fused == the standalone quantizer applied to the kernel's own output
+    qs2, ds2 = poisoned_plane(rows_pad, d)
+    q8.quantize_q8_0(y, qs2, ds2)
+    q8.q8_check()
+    assert torch.equal(qs, qs2) and torch.equal(ds, ds2)
+
+
+def test_rmsnorm_quant_zero_row(q8):
+    x = np.zeros((2, 256), np.float32)
+    x[1] = 1.0
+    w = np.ones(256, np.float32)
+    y = nan_f32(2, 256)
+    qs, ds = poisoned_plane(2, 256)
+    q8.rmsnorm_quant(dev(x), dev(w), 1e-6, y, qs, ds)
+    q8.q8_check()
+    assert_y_close(y, oracle.rmsnorm(x, w, 1e-6), "zero row")
+    assert (host(qs)[0] == 0).all() and (host(ds)[0] == 0).all()
+
+
+@pytest.mark.parametrize("rows,nf,rows_pad", [(1, 18944, 1), (63, 18944, 64), (65, 4096, 128),
+                                              (100, 640, 128), (3325, 18944, 3328)])
+def test_swiglu_quant(q8, rows, nf, rows_pad):
+    import torch
+
+    g = syn.rng(53, rows, nf)
+    gate = syn.activations(g, rows, nf)
+    up = syn.activations(g, rows, nf)
+    if rows >= 2:
+        gate[0, :64] = np.array([-100.0, -88.0, -80.0, 0.0, 30.0, 90.0] * 10 + [1, 2, 3, 4], np.float32)
+        up[1] = 0.0
+    y = nan_f32(rows, nf)
+    qs, ds = poisoned_plane(rows_pad, nf)
+    q8.swiglu_quant(dev(gate), dev(up), y, qs, ds)
+    q8.q8_check()
+    assert_y_close(y, oracle.swiglu(gate, up), f"swiglu y {rows}x{nf}")
+    qr, dr = oracle.quantize(host(y), rows_pad)
+    assert_plane_equal(qs, ds, qr, dr, f"swiglu plane {rows}x{nf}")
+    qs2, ds2 = poisoned_plane(rows_pad, nf)
+    q8.quantize_q8_0(y, qs2, ds2)
+    q8.q8_check()
+    assert torch.equal(qs, qs2) and torch.equal(ds, ds2)
+
+
+def test_quantizers_are_deterministic(q8):
+    import torch
+
+    g = syn.rng(54, 0)
+    x = dev(syn.activations(g, 257, 3584))
+    w = dev(syn.uniform(g, 3584, 0.5, 1.5))
+    outs = []
+    for _ in range(2):
+        y = nan_f32(257, 3584)
+        qs, ds = poisoned_plane(384, 3584)
+        q8.rmsnorm_quant(x, w, 1e-6, y, qs, ds)
+        q8.q8_check()
+        outs.append((y.view(torch.int32).clone(), qs.clone(), ds.clone()))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
