@@ -218,7 +218,7 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     e0 = time.perf_counter()
     for i in range(steps):
         e2e_step(warmup + i)
-    e_s = time.perf_counter() - e0
+    e2e_s = time.perf_counter() - e0
     q8p.q8_check()
     return dict(ms=ms, kern_ms=kern_ms, clocks=clocks, e2e_s=e2e_s, copies=copies,
                 h2d=sum(v.nbytes for v in xs_h.values()), d2h=4 * sum(n for n, _ in DECODE_SHAPES))

@@ -136,6 +136,16 @@ Q8_API int q8_0_gemm(const void *w, int64_t n, int64_t k,
               float *y, void *stream);
 
 /*
+ * q8_0_gemm_mma -- the same contraction as q8_0_gemm on the warp-level int8
+ * tensor instruction (mma.sync.m16n8k32.s8) instead of tcgen05: the legacy
+ * tensor path, kept as an exact A/B baseline for q8_0_gemm.  Requires
+ * (k/32) % 8 == 0 (Q8_ERR_ARG otherwise); arguments as q8_0_gemm.
+ */
+Q8_API int q8_0_gemm_mma(const void *w, int64_t n, int64_t k,
+                         const int8_t *qs, const uint32_t *ds, int64_t t, int64_t rows_pad,
+                         float *y, void *stream);
+
+/*
  * q8_check -- synchronise `stream`, then read and clear the library's device
  * error word.  Returns Q8_OK, Q8_ERR_DEVICE_TIMEOUT if a bounded on-device
  * wait ran out since the last check (the affected outputs are undefined), or

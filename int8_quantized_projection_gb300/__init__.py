@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     library_path,
     load,
     q8_0_gemm,
+    q8_0_gemm_mma,
     q8_0_gemv,
     q8_check,
     q8_num_sms,

@@ -32,6 +32,7 @@ SIGNATURES = {
     "swiglu_quant": (_INT, [_P, _P, _P, _I64, _I64, _P, _P, _I64, _P]),
     "q8_0_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q8_0_gemm": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
+    "q8_0_gemm_mma": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
     "q8_check": (_INT, [_P]),
     "q8_num_sms": (_INT, []),
 }
@@ -164,6 +165,18 @@ def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, stream=None):
     if w.numel() != n * (k // 32) * 34 or y.numel() < t * n or qs.shape[-1] != k or ds.shape[0] != rows_pad:
         raise ValueError("shape mismatch")
     _check("q8_0_gemm", lib().q8_0_gemm(_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y), _stream(stream)))
+
+
+def q8_0_gemm_mma(w, n: int, k: int, qs, ds, t: int, y, stream=None):
+    """Legacy-tensor-path A/B twin of :func:`q8_0_gemm` (mma.sync.m16n8k32.s8)."""
+    import torch
+
+    _need(w, torch.uint8, "w"), _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds"), _need(y, torch.float32, "y")
+    rows_pad = qs.shape[0]
+    if w.numel() != n * (k // 32) * 34 or y.numel() < t * n or qs.shape[-1] != k or ds.shape[0] != rows_pad:
+        raise ValueError("shape mismatch")
+    _check("q8_0_gemm_mma", lib().q8_0_gemm_mma(_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y),
+                                                _stream(stream)))
 
 
 def empty_plane(rows_pad: int, k: int, device="cuda"):

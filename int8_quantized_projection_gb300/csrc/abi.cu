@@ -73,8 +73,8 @@ int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, c
 int gemm_mma_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t, float *y,
                     cudaStream_t s);
 
-// No GEMM kernel has a bounded wait yet; its error word is always clear.
-int gemm_take_error(cudaStream_t) { return Q8_OK; }
+int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t, float *y,
+                   cudaStream_t s);
 
 } // namespace q8
 
@@ -122,6 +122,16 @@ extern "C" int q8_0_gemm(const void *w, int64_t n, int64_t k, const int8_t *qs, 
         if (t > 65535) return Q8_ERR_ARG;  // generic kernel: one grid row per token
         return q8::gemv_generic_launch(w, n, k, qs, ds, y, t, s);
     }
-    if (t > int64_t(65535) * 64) return Q8_ERR_ARG;
-    return q8::gemm_mma_launch(w, n, k, qs, ds, t, y, s);
+    if (t > int64_t(65535) * 128 || n > (int64_t(1) << 31) - 128) return Q8_ERR_ARG;
+    return q8::gemm_tc_launch(w, n, k, qs, ds, t, y, s);
+}
+
+extern "C" int q8_0_gemm_mma(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t,
+                             int64_t rows_pad, float *y, void *stream)
+{
+    if (!w || !qs || !ds || !y || n < 1 || t < 1 || k <= 0 || (k % 32) != 0 || rows_pad < t) return Q8_ERR_ARG;
+    if ((k / 32) % 8 != 0 || t > int64_t(65535) * 64) return Q8_ERR_ARG;
+    if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    return q8::gemm_mma_launch(w, n, k, qs, ds, t, y, static_cast<cudaStream_t>(stream));
 }

@@ -6,18 +6,21 @@
 // Activation-Quantization Discipline" (sec. 2.1-2.4) and how this kernel
 // avoids them on GB300:
 //   2.1  A 34-byte block is only 2-byte aligned.  Eight consecutive blocks
-//        are 272 = 17 x 16 bytes, so when k/32 is a multiple of 8 every row,
-//        and every group of 8 blocks in it, starts 16-byte aligned.  The
-//        weight stream is moved by cp.async.bulk (the TMA unit) in pieces of
-//        up to 32 such units straight into shared memory; lanes then read
-//        their unit with conflict-free 16-byte shared loads and rebuild the
-//        unaligned qs words with one byte-permute each.
+//        are 272 = 17 x 16 bytes, so when k/32 is a multiple of 8 every row
+//        starts 16-byte aligned.  The weight stream is moved by cp.async.bulk
+//        (the TMA unit) in pieces of up to 32 four-block chunks (136 bytes,
+//        8-byte aligned) straight into shared memory; each lane reads its
+//        chunk with conflict-free 8-byte shared loads (lanes 34 words apart)
+//        and rebuilds the unaligned qs words with one byte-permute each.
+//        Every warp owns a two-deep ring, and a CTA has up to 16 warps, so
+//        an SM keeps ~139 KB of weights in flight and several warps per
+//        scheduler to hide shared-memory latency.
 //   2.2  The inner product is __dp4a on packed int8 words.
 //   2.3  The activation (k bytes of qs + k/8 bytes of d|ssum) is staged once
-//        per CTA in shared memory, padded so that lanes reading different
-//        units hit different banks; no activation traffic reaches HBM/L2
-//        after the prologue.
-//   2.4  Lanes per row is the next power of two of the row's unit count
+//        per CTA in shared memory, 144 bytes per chunk so that lanes reading
+//        different chunks hit different banks; no activation traffic reaches
+//        HBM/L2 after the prologue.
+//   2.4  Lanes per row is the next power of two of the row's chunk count
 //        (capped at 32), so short rows share a warp instead of idling lanes;
 //        the grid is a persistent set of at most one CTA per SM whose warp
 //        count shrinks for small n, so small projections still spread over
@@ -31,17 +34,17 @@ namespace {
 
 __device__ unsigned int g_gemv_err;
 
-constexpr int kUnitBytes = 272;                 // 8 Q8_0 blocks
-constexpr int kActUnitBytes = 304;              // 256 B qs + 32 B ds, padded to 76 words
-constexpr int kPieceUnits = 32;
-constexpr int kPieceBytes = kPieceUnits * kUnitBytes;  // 8704
-constexpr int kStages = 3;
-constexpr int kMaxWarps = 4;
-constexpr int kMaxActUnits = 256;               // k <= 65536 on the staged path
+constexpr int kChunkBytes = 136;                // 4 Q8_0 blocks (8-byte aligned when the row is 16-byte aligned)
+constexpr int kActChunkBytes = 144;             // 128 B qs + 16 B ds: 36 words, so lanes hit distinct banks
+constexpr int kPieceChunks = 32;                // one chunk per lane
+constexpr int kPieceBytes = kPieceChunks * kChunkBytes;  // 4352 = 272 x 16
+constexpr int kStages = 2;
+constexpr int kMaxWarps = 16;
+constexpr int kMaxActChunks = 512;              // k <= 65536 on the staged path
 
 struct GvGeom {
     int64_t n;       // weight rows
-    int nu;          // 8-block units per row
+    int nc;          // 4-block chunks per row (even: k/32 % 8 == 0)
     int lpr_log2;    // lanes per row = 1 << lpr_log2
     int rpw;         // rows per piece
     int ppr;         // pieces per row group
@@ -50,27 +53,24 @@ struct GvGeom {
 
 __host__ __device__ inline int smem_header_bytes() { return kMaxWarps * kStages * 8 + 128; }
 
-// One 8-block unit: 17 x 16 B of weights (in shared memory) against the
-// matching 256 B of qs and 8 ds words of the activation (in shared memory).
-__device__ __forceinline__ float unit_dot(const uint8_t *wu, const uint8_t *au)
+// One 4-block chunk: 34 words of raw weights (shared memory, 8-byte aligned)
+// against 128 B of qs and 4 ds words of the activation (shared memory).
+__device__ __forceinline__ float chunk_dot(const uint8_t *wc, const uint8_t *ac)
 {
-    uint32_t wv[68];
+    uint32_t wv[34];
 #pragma unroll
     for (int c = 0; c < 17; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(wu + 16 * c);
-        wv[4 * c + 0] = v.x;
-        wv[4 * c + 1] = v.y;
-        wv[4 * c + 2] = v.z;
-        wv[4 * c + 3] = v.w;
+        const uint2 v = *reinterpret_cast<const uint2 *>(wc + 8 * c);
+        wv[2 * c + 0] = v.x;
+        wv[2 * c + 1] = v.y;
     }
-    const uint4 ad0 = *reinterpret_cast<const uint4 *>(au + 256);
-    const uint4 ad1 = *reinterpret_cast<const uint4 *>(au + 272);
-    const uint32_t ad[8] = {ad0.x, ad0.y, ad0.z, ad0.w, ad1.x, ad1.y, ad1.z, ad1.w};
+    const uint4 ad = *reinterpret_cast<const uint4 *>(ac + 128);
+    const uint32_t adw[4] = {ad.x, ad.y, ad.z, ad.w};
     float acc = 0.0f;
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-        const uint4 a0 = *reinterpret_cast<const uint4 *>(au + 32 * b);
-        const uint4 a1 = *reinterpret_cast<const uint4 *>(au + 32 * b + 16);
+    for (int b = 0; b < 4; ++b) {
+        const uint4 a0 = *reinterpret_cast<const uint4 *>(ac + 32 * b);
+        const uint4 a1 = *reinterpret_cast<const uint4 *>(ac + 32 * b + 16);
         const uint32_t aq[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         // block b: f16 d at byte 34b, qs at 34b + 2 (word-aligned for odd b only)
         const uint32_t dbits = (b & 1) ? (wv[(17 * b - 1) / 2] >> 16) : (wv[17 * b / 2] & 0xffffu);
@@ -82,7 +82,7 @@ __device__ __forceinline__ float unit_dot(const uint8_t *wu, const uint8_t *au)
             isum = q8::dp4a(qw, aq[i], isum);
         }
         const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
-        const float da = __half2float(__ushort_as_half(static_cast<unsigned short>(ad[b] & 0xffffu)));
+        const float da = __half2float(__ushort_as_half(static_cast<unsigned short>(adw[b] & 0xffffu)));
         acc = fmaf(dw * da, static_cast<float>(isum), acc);  // dw*da is exact in f32
     }
     return acc;
@@ -90,31 +90,32 @@ __device__ __forceinline__ float unit_dot(const uint8_t *wu, const uint8_t *au)
 
 __global__ void __launch_bounds__(kMaxWarps * 32)
 gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_row,
-                   const uint4 *__restrict__ ds_row, float *__restrict__ y, GvGeom g)
+                   const uint32_t *__restrict__ ds_row, float *__restrict__ y, GvGeom g)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int nwarp = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     uint8_t *act = smem + smem_header_bytes();
-    uint8_t *ring = act + ((g.nu * kActUnitBytes + 127) & ~127);
+    uint8_t *ring = act + ((g.nc * kActChunkBytes + 127) & ~127);
     uint64_t *mybar = bars + warp * kStages;
     uint8_t *myring = ring + warp * kStages * kPieceBytes;
 
-    const int64_t pitch = static_cast<int64_t>(g.nu) * kUnitBytes;
+    const int64_t pitch = static_cast<int64_t>(g.nc) * kChunkBytes;
     const int64_t W = static_cast<int64_t>(gridDim.x) * nwarp;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarp + warp;
     const int64_t g0 = g.groups * gw / W, g1 = g.groups * (gw + 1) / W;
     const int64_t npieces = (g1 - g0) * g.ppr;
 
-    // piece i of this warp -> (global source, bytes)
+    // piece i of this warp -> (global source, bytes); every piece is a whole
+    // number of 16-byte granules because chunks come in pairs (272 B).
     auto piece = [&](int64_t i, uint32_t &bytes) -> const uint8_t * {
         const int64_t grp = g0 + i / g.ppr;
-        if (g.rpw == 1) {  // one row per piece, up to 32 units of it
+        if (g.rpw == 1) {  // one row per piece, up to 32 chunks of it
             const int p = static_cast<int>(i % g.ppr);
-            const int units = min(kPieceUnits, g.nu - kPieceUnits * p);
-            bytes = static_cast<uint32_t>(units * kUnitBytes);
-            return w + grp * pitch + static_cast<int64_t>(kPieceUnits) * p * kUnitBytes;
+            const int chunks = min(kPieceChunks, g.nc - kPieceChunks * p);
+            bytes = static_cast<uint32_t>(chunks * kChunkBytes);
+            return w + grp * pitch + static_cast<int64_t>(kPieceChunks) * p * kChunkBytes;
         }
         const int64_t r0 = grp * g.rpw;
         const int64_t rows = min(static_cast<int64_t>(g.rpw), g.n - r0);
@@ -132,17 +133,17 @@ gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_r
             q8::bulk_g2s(myring + s * kPieceBytes, src, bytes, &mybar[s]);
         }
     }
-    // stage the activation: unit u = 16 x 16 B of qs then 2 x 16 B of ds
-    for (int idx = threadIdx.x; idx < g.nu * 18; idx += blockDim.x) {
-        const int u = idx / 18, c = idx - u * 18;
-        const uint4 v = (c < 16) ? __ldg(qs_row + u * 16 + c) : __ldg(ds_row + u * 2 + (c - 16));
-        *reinterpret_cast<uint4 *>(act + u * kActUnitBytes + 16 * c) = v;
+    // stage the activation: chunk c = 8 x 16 B of qs then its 4 ds words
+    for (int idx = threadIdx.x; idx < g.nc * 9; idx += blockDim.x) {
+        const int c = idx / 9, j = idx - c * 9;
+        const uint4 v = (j < 8) ? __ldg(qs_row + c * 8 + j) : __ldg(reinterpret_cast<const uint4 *>(ds_row) + c);
+        *reinterpret_cast<uint4 *>(act + c * kActChunkBytes + 16 * j) = v;
     }
     __syncthreads();
 
     const int lpr = 1 << g.lpr_log2;
     const int ri = lane >> g.lpr_log2;         // row within a piece
-    const int uj = lane & (lpr - 1);           // unit within a piece
+    const int cj = lane & (lpr - 1);           // chunk within a piece
     float acc = 0.0f;
     for (int64_t i = 0; i < npieces; ++i) {
         const int s = static_cast<int>(i % kStages);
@@ -156,20 +157,20 @@ gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_r
         const int64_t grp = g0 + i / g.ppr;
         const int p = static_cast<int>(i % g.ppr);
         int64_t row;
-        int unit, soff;
+        int chunk, soff;
         bool valid;
         if (g.rpw == 1) {
             row = grp;
-            unit = kPieceUnits * p + lane;
-            soff = lane * kUnitBytes;
-            valid = unit < g.nu;
+            chunk = kPieceChunks * p + lane;
+            soff = lane * kChunkBytes;
+            valid = chunk < g.nc;
         } else {
             row = grp * g.rpw + ri;
-            unit = uj;
-            soff = (ri * g.nu + uj) * kUnitBytes;
-            valid = uj < g.nu && row < g.n;
+            chunk = cj;
+            soff = (ri * g.nc + cj) * kChunkBytes;
+            valid = cj < g.nc && row < g.n;
         }
-        if (valid) acc += unit_dot(buf + soff, act + unit * kActUnitBytes);
+        if (valid) acc += chunk_dot(buf + soff, act + chunk * kActChunkBytes);
         __syncwarp();
         if (lane == 0 && i + kStages < npieces) {
             uint32_t bytes;
@@ -179,7 +180,7 @@ gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_r
         }
         if (p == g.ppr - 1) {  // row group complete: reduce over the lanes of each row
             for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(Q8_FULL_MASK, acc, o);
-            if (uj == 0 && row < g.n) y[row] = acc;
+            if (cj == 0 && row < g.n) y[row] = acc;
             acc = 0.0f;
         }
     }
@@ -270,18 +271,18 @@ extern "C" int q8_0_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, 
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t nb = k / 32;
-    if (nb % 8 != 0 || nb / 8 > kMaxActUnits || n > (int64_t(1) << 40))
+    if (nb % 8 != 0 || nb / 4 > kMaxActChunks || n > (int64_t(1) << 40))
         return q8::gemv_generic_launch(w, n, k, qs, ds, y, 1, s);
 
     GvGeom g;
     g.n = n;
-    g.nu = static_cast<int>(nb / 8);
-    if (g.nu > kPieceUnits) {
+    g.nc = static_cast<int>(nb / 4);
+    if (g.nc > kPieceChunks) {
         g.lpr_log2 = 5;
         g.rpw = 1;
-        g.ppr = (g.nu + kPieceUnits - 1) / kPieceUnits;
+        g.ppr = (g.nc + kPieceChunks - 1) / kPieceChunks;
     } else {
-        g.lpr_log2 = ceil_log2(g.nu);
+        g.lpr_log2 = ceil_log2(g.nc);
         g.rpw = 32 >> g.lpr_log2;
         g.ppr = 1;
     }
@@ -292,12 +293,11 @@ extern "C" int q8_0_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, 
     nw = nw < 1 ? 1 : (nw > kMaxWarps ? kMaxWarps : nw);
     int64_t grid = (g.groups + nw - 1) / nw;
     grid = grid > sms ? sms : grid;
-    const int smem = smem_header_bytes() + ((g.nu * kActUnitBytes + 127) & ~127) +
+    const int smem = smem_header_bytes() + ((g.nc * kActChunkBytes + 127) & ~127) +
                      static_cast<int>(nw) * kStages * kPieceBytes;
-    const int maxs = smem_header_bytes() + kMaxActUnits * kActUnitBytes + kMaxWarps * kStages * kPieceBytes;
+    const int maxs = smem_header_bytes() + kMaxActChunks * kActChunkBytes + kMaxWarps * kStages * kPieceBytes;
     if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(gemv_staged_kernel), maxs, 0)) return Q8_ERR_LAUNCH;
     gemv_staged_kernel<<<static_cast<unsigned>(grid), static_cast<unsigned>(nw * 32), smem, s>>>(
-        static_cast<const uint8_t *>(w), reinterpret_cast<const uint4 *>(qs), reinterpret_cast<const uint4 *>(ds), y,
-        g);
+        static_cast<const uint8_t *>(w), reinterpret_cast<const uint4 *>(qs), ds, y, g);
     return q8::launch_status();
 }
