@@ -86,7 +86,7 @@ def measured_peaks():
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -94,6 +94,14 @@ class ClockSampler:
         self.gpu_id = gpu_id
         self.proc = None
         self.path = None
+        self.window = None
+
+    def mark(self, begin):
+        """Record the host time at which the timed region begins / ends."""
+        if begin:
+            self.window = [time.time(), None]
+        elif self.window is not None:
+            self.window[1] = time.time()
 
     def start(self):
         try:
@@ -101,8 +109,9 @@ class ClockSampler:
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.out,
                                          stderr=subprocess.DEVNULL)
+            time.sleep(0.5)  # let the sampler reach its steady cadence before the timed region
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -122,6 +131,20 @@ class ClockSampler:
                 if len(p) >= 9:
                     rows.append(p)
         os.unlink(self.path)
+        # keep the samples taken during the timed region, widened by one
+        # sampling interval on each side so that short regions still get some
+        if self.window and self.window[1]:
+            lo, hi = self.window[0] - 0.06, self.window[1] + 0.06
+            kept = []
+            for r in rows:
+                try:
+                    ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S")) + float(
+                        "0." + r[0].split(".")[1]) if "." in r[0] else 0.0
+                except (ValueError, IndexError):
+                    ts = None
+                if ts is None or lo <= ts <= hi:
+                    kept.append(r)
+            rows = kept or rows[-2:]
         if not rows:
             return None
 
@@ -188,11 +211,13 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     sampler.start()
+    sampler.mark(True)
     t0.record(stream)
     for i in range(steps):
         step(warmup + i, evs[i])
     t1.record(stream)
     torch.cuda.synchronize(dev)
+    sampler.mark(False)
     clocks = sampler.stop()
     q8p.q8_check()
     ms = t0.elapsed_time(t1)
@@ -350,6 +375,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill"],
+                    help="decode and/or prefill legs (profiling runs select one)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -382,16 +409,17 @@ def main():
     sampler = ClockSampler(gpu_smi_id(torch, dev))
     if world > 1:
         torch.distributed.barrier()
-    dec = run_decode(torch, q8p, args.steps, args.warmup, dev, sampler)
-    ms, e2e_s = dec["ms"], dec["e2e_s"]
-    if world > 1:
-        t = torch.tensor([ms, e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_s = float(t[0]), float(t[1])
+    dec = None
+    if args.workload in ("all", "decode"):
+        dec = run_decode(torch, q8p, args.steps, args.warmup, dev, sampler)
+        if world > 1:
+            t = torch.tensor([dec["ms"], dec["e2e_s"]], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            dec["ms"], dec["e2e_s"] = float(t[0]), float(t[1])
 
     pre = None
-    if not args.no_prefill:
-        pre = run_prefill(torch, q8p, max(3, args.steps // 6), args.warmup, dev)
+    if args.workload == "prefill" or (args.workload == "all" and not args.no_prefill):
+        pre = run_prefill(torch, q8p, args.steps if dec is None else max(3, args.steps // 6), args.warmup, dev)
 
     if rank != 0:
         if world > 1:
@@ -399,43 +427,51 @@ def main():
         return 0
 
     peaks = measured_peaks()
-    step_bytes = decode_bytes()
-    value = world * step_bytes * args.steps / (ms / 1e3) / 1e9
-    big = bytes_gemv(*DECODE_SHAPES[0])
-    achieved = big / (dec["kern_ms"] / 1e3) / 1e9
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": decode_config(dec["copies"]),
-        "roofline": {"kernel": "q8_0_gemv 12288x7168 (gemv_staged_kernel)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-                     "traffic": NCU_TRAFFIC_BYTES["gemv_staged_kernel 12288x7168"],
-                     "algorithmic_bytes": big, "avg_launch_us": round(dec["kern_ms"] * 1e3, 3)},
-        "cpu_baseline": cpu,
-        "e2e": {"value": round(world * step_bytes * args.steps / dec["e2e_s"] / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"]},
-        "clocks": dec["clocks"],
-        "gpu_launches": 5 * args.steps,
-    }
+    line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic"}
+    if dec is not None:
+        ms = dec["ms"]
+        step_bytes = decode_bytes()
+        value = world * step_bytes * args.steps / (ms / 1e3) / 1e9
+        big = bytes_gemv(*DECODE_SHAPES[0])
+        achieved = big / (dec["kern_ms"] / 1e3) / 1e9
+        line.update({
+            "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms / args.steps, 5),
+            "config": decode_config(dec["copies"]),
+            "roofline": {"kernel": "q8_0_gemv 12288x7168 (gemv_staged_kernel)", "bound": "hbm",
+                         "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+                         "traffic": NCU_TRAFFIC_BYTES["gemv_staged_kernel 12288x7168"],
+                         "algorithmic_bytes": big, "avg_launch_us": round(dec["kern_ms"] * 1e3, 3)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(world * step_bytes * args.steps / dec["e2e_s"] / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"]},
+            "clocks": dec["clocks"],
+            "gpu_launches": 5 * args.steps,
+        })
     if pre is not None:
         T, d, nf = PREFILL["tokens"], PREFILL["d"], PREFILL["nf"]
         gemm_ms = pre["gemm_gate"] + pre["gemm_up"] + pre["gemm_down"]
         tops = 3 * ops_gemm(T, nf, d) / (gemm_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
-        line["prefill"] = {
+        pobj = {
             "workload": f"prefill chain T={T} d={d} nf={nf}: rmsnorm_quant, gate/up GEMM, swiglu_quant, down GEMM",
             "ms_per_chain": round(sum(pre.values()), 4), "ms": {k: round(v, 4) for k, v in pre.items()},
             "gemm_tops": round(tops, 2), "unit": "int8 TOPS (2*T*N*K per GEMM)",
-            "roofline_gemm": {"bound": "tensor", "achieved": round(tops, 2), "peak": peak, "unit": "TFLOP/s",
-                              "frac": round(tops / peak, 4),
+            "roofline_gemm": {"kernel": "q8_0_gemm (gemm_tc_kernel)", "bound": "tensor", "achieved": round(tops, 2),
+                              "peak": peak, "unit": "TFLOP/s", "frac": round(tops / peak, 4),
+                              "traffic": NCU_TRAFFIC_BYTES["gemm 18944x3584 t=3325"],
                               "peak_note": f"sustained dense bf16/f16 tensor peak ({peaks['source']}); sm_103a has "
                                            "no int8 tcgen05 kind"},
             "quantize_gbs": {"rmsnorm_quant": round(bytes_rmsnorm_quant(T, d) / pre["rmsnorm_quant"] / 1e6, 1),
                              "swiglu_quant": round(bytes_swiglu_quant(T, nf) / pre["swiglu_quant"] / 1e6, 1)},
             "l2": "step working set ~1.2 GB > L2",
         }
+        if dec is None:  # prefill-only run: the GEMM throughput is the headline
+            line.update({"value": pobj["gemm_tops"], "unit": "TOPS", "ms_per_step": pobj["ms_per_chain"],
+                         "config": {"workload": pobj["workload"], "l2": pobj["l2"], "parallelism": "replicas"},
+                         "roofline": pobj["roofline_gemm"], "gpu_launches": 5 * args.steps})
+        line["prefill"] = pobj
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
