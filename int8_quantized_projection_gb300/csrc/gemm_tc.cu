@@ -15,15 +15,18 @@
 // A-quantize mode 1" (sec. 2.1).
 //
 // One CTA computes a 128 (weight rows) x 128 (tokens) tile over all of k.
-// Warp roles (320 threads):
-//   warp 0     TMA producer: raw Q8_0 rows (2D u16 map, 8 blocks per stage),
-//              plane qs (2D u8 map, 128B swizzle) and ds words (2D u32 map)
-//   warp 1     TMEM allocator and single-thread MMA issuer
-//   warps 2-5  converters: raw int8 -> f16 operand tiles in the canonical
-//              K-major no-swizzle layout, one 32-wide block at a time, plus
-//              the block's scales as f32
-//   warps 6-9  epilogue: per block, tcgen05.ld of the 128x128 partial,
-//              acc += (d_w * d_a) * partial, then one coalesced store of Y
+// Warp roles (512 threads):
+//   warp 0      TMA producer: raw Q8_0 rows (2D u16 map, 8 blocks per stage),
+//               plane qs (2D u8 map, 128B swizzle) and ds words (2D u32 map)
+//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warps 2-7   converters: raw int8 -> f16 operand tiles in the canonical
+//               K-major no-swizzle layout, one 32-wide block at a time, plus
+//               the block's scales as f32 (weight rows read with three
+//               16-byte loads, bank-conflict free)
+//   warps 8-15  epilogue: two warps per TMEM lane quarter, 64 tokens each;
+//               per block, tcgen05.ld of the partial, acc += (d_w * d_a) *
+//               partial with packed f32x2 multiply / fma, then one coalesced
+//               store of Y
 // Every mbarrier wait is bounded; a wait that runs out sets the CTA abort
 // flag and the library error word, and all roles drain and exit.
 #include <cuda.h>
@@ -40,7 +43,9 @@ constexpr int kRawStages = 2;
 constexpr int kF16Slots = 4;
 constexpr int kAcc = 4;                            // TMEM block buffers of BN columns
 constexpr int kTmemCols = kAcc * BN;               // 512
-constexpr int kThreads = 320;
+constexpr int kConvThreads = 192;                  // warps 2-7
+constexpr int kEpiThreads = 256;                   // warps 8-15
+constexpr int kThreads = 64 + kConvThreads + kEpiThreads;  // 512
 
 constexpr int kARawBytes = BM * 272;               // 34816
 constexpr int kBRawHalf = BN * 128;                // 16384 (128B-swizzled rows)
@@ -92,6 +97,7 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per thread.
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32])
 {
     uint32_t r[32];
@@ -139,29 +145,25 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t q, uint32_t &lo, uint32_t
     hi = *reinterpret_cast<const uint32_t *>(&hv);
 }
 
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)  // suspend up to 20 us per try instead of spinning
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait shared by all roles: gives up on the CTA abort flag or after
 // the time limit (then raises the flag and the error word).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag)
 {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
+    if (try_wait(bar, parity)) return true;
     const uint64_t t0 = q8::globaltimer_ns();
     for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i) {
-            asm volatile(
-                "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, "
-                "p;\n\t}"
-                : "=r"(ok)
-                : "r"(bar), "r"(parity)
-                : "memory");
-            if (ok) return true;
-        }
+        if (try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (q8::globaltimer_ns() - t0 > Q8_WAIT_LIMIT_NS) {
             *abort_flag = 1;
@@ -176,14 +178,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity)
 {
     const uint64_t t0 = q8::globaltimer_ns();
-    for (;;) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (ok) return;
+    while (!try_wait(bar, parity)) {
         if (q8::globaltimer_ns() - t0 > Q8_WAIT_LIMIT_NS) {
             atomicOr(&g_gemm_err, 1u);
             return;
@@ -196,6 +191,112 @@ __device__ __forceinline__ void arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Converter step for weight row r, raw block BETA of the stage: read the 48
+// bytes (three 16-byte aligned, bank-conflict-free loads) that contain the
+// row's 34-byte block, write the 32 codes as f16 into the A tile and d as f32.
+template <int BETA>
+__device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16, float *sw, int r)
+{
+    constexpr int off = 34 * BETA;
+    constexpr int c0 = off >> 4;        // first 16-byte chunk
+    constexpr int o = off & 15;         // block start within it (even)
+    uint32_t w[12];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(arow + 16 * (c0 + c));
+        w[4 * c + 0] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+    }
+    const uint32_t dbits = (o & 2) ? (w[o >> 2] >> 16) : (w[o >> 2] & 0xffffu);
+    sw[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+    uint32_t qw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int ob = o + 2 + 4 * i;   // compile-time after unrolling
+        qw[i] = (ob & 3) ? __byte_perm(w[ob >> 2], w[(ob >> 2) + 1], 0x5432) : w[ob >> 2];
+    }
+#pragma unroll
+    for (int kc = 0; kc < 4; ++kc) {
+        uint4 v;
+        i8x4_to_f16x4(qw[2 * kc], v.x, v.y);
+        i8x4_to_f16x4(qw[2 * kc + 1], v.z, v.w);
+        *reinterpret_cast<uint4 *>(a16 + (r >> 3) * 512 + kc * 128 + (r & 7) * 16) = v;
+    }
+}
+
+// Converter step for one (token, 16-byte half-block) task of raw block BETA.
+template <int BETA>
+__device__ __forceinline__ void convert_b_task(const uint8_t *braw_stage, const uint8_t *draw_stage, uint8_t *b16,
+                                               float *sa, int id)
+{
+    const int l = id & 31;
+    const int tok = 16 * (id >> 5) + (l & 7) + 8 * (l >> 4);
+    const int h = (l >> 3) & 1;
+    constexpr int hh = BETA >> 2, bq = BETA & 3;
+    const int c16 = 2 * bq + h;
+    const uint8_t *braw = braw_stage + hh * kBRawHalf;
+    const uint4 v = *reinterpret_cast<const uint4 *>(braw + tok * 128 + ((c16 ^ (tok & 7)) << 4));
+    uint4 o0, o1;
+    i8x4_to_f16x4(v.x, o0.x, o0.y);
+    i8x4_to_f16x4(v.y, o0.z, o0.w);
+    i8x4_to_f16x4(v.z, o1.x, o1.y);
+    i8x4_to_f16x4(v.w, o1.z, o1.w);
+    uint8_t *dst = b16 + (tok >> 3) * 512 + (tok & 7) * 16 + (2 * h) * 128;
+    *reinterpret_cast<uint4 *>(dst) = o0;
+    *reinterpret_cast<uint4 *>(dst + 128) = o1;
+    if (h == 0) {
+        const uint32_t dw = *reinterpret_cast<const uint32_t *>(draw_stage + tok * 32 + 4 * BETA);
+        sa[tok] = __half2float(__ushort_as_half(static_cast<unsigned short>(dw & 0xffffu)));
+    }
+}
+
+struct Bars {
+    uint32_t b0;
+    __device__ uint32_t raw_full(int s) const { return b0 + 8u * s; }
+    __device__ uint32_t raw_empty(int s) const { return b0 + 8u * (kRawStages + s); }
+    __device__ uint32_t f16_full(int s) const { return b0 + 8u * (2 * kRawStages + s); }
+    __device__ uint32_t f16_empty(int s) const { return b0 + 8u * (2 * kRawStages + kF16Slots + s); }
+    __device__ uint32_t acc_full(int s) const { return b0 + 8u * (2 * kRawStages + 2 * kF16Slots + s); }
+    __device__ uint32_t acc_empty(int s) const { return b0 + 8u * (2 * kRawStages + 2 * kF16Slots + kAcc + s); }
+    __device__ uint32_t sc_full(int s) const { return b0 + 8u * (2 * kRawStages + 2 * kF16Slots + 2 * kAcc + s); }
+    __device__ uint32_t sc_empty(int s) const { return b0 + 8u * (2 * kRawStages + 2 * kF16Slots + 3 * kAcc + s); }
+    __device__ uint32_t drain() const { return b0 + 8u * (kNumBars - 1); }
+};
+
+// One 32-wide block of the stage for the converter role.
+template <int BETA>
+__device__ __forceinline__ bool convert_block(const Bars &B, uint8_t *sm, float *scales, int s, int c,
+                                              volatile int *abort_flag)
+{
+    const int slot = s % kRawStages;
+    const int j = s * kBlocksPerStage + BETA;
+    constexpr int fs = BETA % kF16Slots, sc = BETA % kAcc;
+    if (BETA == 0 && !wait_bar(B.raw_full(slot), static_cast<uint32_t>(s / kRawStages) & 1u, abort_flag))
+        return false;
+    if (!wait_bar(B.f16_empty(fs), (static_cast<uint32_t>(j / kF16Slots) & 1u) ^ 1u, abort_flag)) return false;
+    if (!wait_bar(B.sc_empty(sc), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) return false;
+    uint8_t *a16 = sm + OFF_F16 + fs * kF16SlotBytes;
+    uint8_t *b16 = a16 + kF16Tile;
+    float *sw = scales + sc * 256;
+    float *sa = sw + 128;
+    const uint8_t *braw = sm + OFF_BRAW + slot * kBRawBytes;
+    const uint8_t *draw = sm + OFF_DRAW + slot * kDRawBytes;
+    if (c < 128) {
+        convert_a_row<BETA>(sm + OFF_ARAW + slot * kARawBytes + c * 272, a16, sw, c);
+        convert_b_task<BETA>(braw, draw, b16, sa, c);
+    } else {
+        convert_b_task<BETA>(braw, draw, b16, sa, 128 + (c - 128));
+        convert_b_task<BETA>(braw, draw, b16, sa, 192 + (c - 128));
+    }
+    q8::fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+    arrive(B.f16_full(fs));
+    arrive(B.sc_full(sc));
+    if (BETA == kBlocksPerStage - 1) arrive(B.raw_empty(slot));
+    return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmD, int64_t n, int64_t t, int nb, float *__restrict__ y)
@@ -205,17 +306,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t *sm = smem_raw + (base - raw_base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const uint32_t bar0 = base + OFF_BAR;
-    auto raw_full = [&](int s) { return bar0 + 8u * s; };
-    auto raw_empty = [&](int s) { return bar0 + 8u * (kRawStages + s); };
-    auto f16_full = [&](int s) { return bar0 + 8u * (2 * kRawStages + s); };
-    auto f16_empty = [&](int s) { return bar0 + 8u * (2 * kRawStages + kF16Slots + s); };
-    auto acc_full = [&](int s) { return bar0 + 8u * (2 * kRawStages + 2 * kF16Slots + s); };
-    auto acc_empty = [&](int s) { return bar0 + 8u * (2 * kRawStages + 2 * kF16Slots + kAcc + s); };
-    auto sc_full = [&](int s) { return bar0 + 8u * (2 * kRawStages + 2 * kF16Slots + 2 * kAcc + s); };
-    auto sc_empty = [&](int s) { return bar0 + 8u * (2 * kRawStages + 2 * kF16Slots + 3 * kAcc + s); };
-    const uint32_t drain = bar0 + 8u * (kNumBars - 1);
+    const Bars B{base + OFF_BAR};
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 4);
     float *scales = reinterpret_cast<float *>(sm + OFF_SCALE);  // [kAcc][2][128]: d_w rows, d_a tokens
@@ -226,22 +317,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_gemm_err) != 0u) ? 1 : 0;
+        uint64_t *b = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
         for (int s = 0; s < kRawStages; ++s) {
-            q8::mbar_init(reinterpret_cast<uint64_t *>(sm + OFF_BAR) + s, 1);
-            q8::mbar_init(reinterpret_cast<uint64_t *>(sm + OFF_BAR) + kRawStages + s, 128);
+            q8::mbar_init(b + s, 1);                               // raw_full: TMA bytes
+            q8::mbar_init(b + kRawStages + s, kConvThreads);       // raw_empty
         }
         for (int s = 0; s < kF16Slots; ++s) {
-            q8::mbar_init(reinterpret_cast<uint64_t *>(sm + OFF_BAR) + 2 * kRawStages + s, 128);
-            q8::mbar_init(reinterpret_cast<uint64_t *>(sm + OFF_BAR) + 2 * kRawStages + kF16Slots + s, 1);
+            q8::mbar_init(b + 2 * kRawStages + s, kConvThreads);   // f16_full
+            q8::mbar_init(b + 2 * kRawStages + kF16Slots + s, 1);  // f16_empty: tcgen05.commit
         }
+        uint64_t *a = b + 2 * kRawStages + 2 * kF16Slots;
         for (int s = 0; s < kAcc; ++s) {
-            uint64_t *b = reinterpret_cast<uint64_t *>(sm + OFF_BAR) + 2 * kRawStages + 2 * kF16Slots;
-            q8::mbar_init(b + s, 1);              // acc_full: tcgen05.commit
-            q8::mbar_init(b + kAcc + s, 128);     // acc_empty: epilogue threads
-            q8::mbar_init(b + 2 * kAcc + s, 128); // sc_full: converter threads
-            q8::mbar_init(b + 3 * kAcc + s, 128); // sc_empty: epilogue threads
+            q8::mbar_init(a + s, 1);                     // acc_full: tcgen05.commit
+            q8::mbar_init(a + kAcc + s, kEpiThreads);    // acc_empty
+            q8::mbar_init(a + 2 * kAcc + s, kConvThreads); // sc_full
+            q8::mbar_init(a + 3 * kAcc + s, kEpiThreads);  // sc_empty
         }
-        q8::mbar_init(reinterpret_cast<uint64_t *>(sm + OFF_BAR) + kNumBars - 1, 1);  // MMA drain
+        q8::mbar_init(b + kNumBars - 1, 1);              // MMA drain
         q8::fence_mbar_init();
     }
     if (warp == 1) {
@@ -263,28 +355,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int s = 0; s < nstages && !*abort_flag; ++s) {
                 const int slot = s % kRawStages;
                 const uint32_t use = static_cast<uint32_t>(s / kRawStages);
-                if (!wait_bar(raw_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(raw_full(slot)),
+                if (!wait_bar(B.raw_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.raw_full(slot)),
                              "r"(kStageTx)
                              : "memory");
-                tma_load_2d(base + OFF_ARAW + slot * kARawBytes, &tmA, s * 136, static_cast<int>(n0), raw_full(slot));
-                tma_load_2d(base + OFF_BRAW + slot * kBRawBytes, &tmB, s * 256, static_cast<int>(t0), raw_full(slot));
+                tma_load_2d(base + OFF_ARAW + slot * kARawBytes, &tmA, s * 136, static_cast<int>(n0), B.raw_full(slot));
+                tma_load_2d(base + OFF_BRAW + slot * kBRawBytes, &tmB, s * 256, static_cast<int>(t0), B.raw_full(slot));
                 tma_load_2d(base + OFF_BRAW + slot * kBRawBytes + kBRawHalf, &tmB, s * 256 + 128,
-                            static_cast<int>(t0), raw_full(slot));
-                tma_load_2d(base + OFF_DRAW + slot * kDRawBytes, &tmD, s * 8, static_cast<int>(t0), raw_full(slot));
+                            static_cast<int>(t0), B.raw_full(slot));
+                tma_load_2d(base + OFF_DRAW + slot * kDRawBytes, &tmD, s * 8, static_cast<int>(t0), B.raw_full(slot));
                 issued = s + 1;
             }
             // drain: the last stages issued must have landed before the CTA exits
             for (int s = issued - kRawStages < 0 ? 0 : issued - kRawStages; s < issued; ++s)
-                drain_bar(raw_full(s % kRawStages), static_cast<uint32_t>(s / kRawStages) & 1u);
+                drain_bar(B.raw_full(s % kRawStages), static_cast<uint32_t>(s / kRawStages) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             for (int j = 0; j < nb; ++j) {
                 const int fs = j % kF16Slots, ab = j % kAcc;
-                if (!wait_bar(f16_full(fs), static_cast<uint32_t>(j / kF16Slots) & 1u, abort_flag)) break;
-                if (!wait_bar(acc_empty(ab), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) break;
+                if (!wait_bar(B.f16_full(fs), static_cast<uint32_t>(j / kF16Slots) & 1u, abort_flag)) break;
+                if (!wait_bar(B.acc_empty(ab), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t a_addr = base + OFF_F16 + fs * kF16SlotBytes;
                 const uint32_t b_addr = a_addr + kF16Tile;
@@ -293,128 +385,73 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int kk = 0; kk < 2; ++kk)  // two K=16 steps = one 32-wide block
                     tc_mma_f16(d, smem_desc(a_addr + 256 * kk, 128, 512), smem_desc(b_addr + 256 * kk, 128, 512),
                                kIdesc, kk);
-                tc_commit(f16_empty(fs));
-                tc_commit(acc_full(ab));
+                tc_commit(B.f16_empty(fs));
+                tc_commit(B.acc_full(ab));
             }
             // drain: every MMA issued must have completed before TMEM is freed
-            tc_commit(drain);
-            drain_bar(drain, 0);
+            tc_commit(B.drain());
+            drain_bar(B.drain(), 0);
         }
-    } else if (warp < 6) {
+    } else if (warp < 8) {
         // ------------------------------------------------------------ converters
-        const int c = threadIdx.x - 64;  // 0..127
-        const int cw = c >> 5;           // converter warp 0..3
-        for (int j = 0; j < nb && !*abort_flag; ++j) {
-            const int s = j / kBlocksPerStage, beta = j % kBlocksPerStage;
-            const int slot = s % kRawStages, fs = j % kF16Slots, sc = j % kAcc;
-            if (beta == 0 && !wait_bar(raw_full(slot), static_cast<uint32_t>(s / kRawStages) & 1u, abort_flag)) break;
-            if (!wait_bar(f16_empty(fs), (static_cast<uint32_t>(j / kF16Slots) & 1u) ^ 1u, abort_flag)) break;
-            if (!wait_bar(sc_empty(sc), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) break;
-            uint8_t *a16 = sm + OFF_F16 + fs * kF16SlotBytes;
-            uint8_t *b16 = a16 + kF16Tile;
-            float *sw = scales + sc * 256;
-            float *sa = sw + 128;
-            {   // A: weight row r = c, raw block beta (34 bytes at 34*beta in a 272-byte row)
-                const int r = c;
-                const uint8_t *rowp = sm + OFF_ARAW + slot * kARawBytes + r * 272;
-                const int off = 34 * beta;
-                const uint32_t *wp = reinterpret_cast<const uint32_t *>(rowp + (off & ~3));
-                uint32_t wv[9];
-#pragma unroll
-                for (int i = 0; i < 9; ++i) wv[i] = wp[i];
-                uint32_t qw[8];
-                uint32_t dbits;
-                if ((off & 3) == 0) {  // even beta: d in word 0 (low), qs from byte 2
-                    dbits = wv[0] & 0xffffu;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) qw[i] = __byte_perm(wv[i], wv[i + 1], 0x5432);
-                } else {               // odd beta: d in word 0 (high), qs word-aligned from word 1
-                    dbits = wv[0] >> 16;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) qw[i] = wv[i + 1];
-                }
-                sw[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
-#pragma unroll
-                for (int kc = 0; kc < 4; ++kc) {
-                    uint4 o;
-                    i8x4_to_f16x4(qw[2 * kc], o.x, o.y);
-                    i8x4_to_f16x4(qw[2 * kc + 1], o.z, o.w);
-                    *reinterpret_cast<uint4 *>(a16 + (r >> 3) * 512 + kc * 128 + (r & 7) * 16) = o;
-                }
-            }
-            {   // B: two (token, 16-byte half-block) tasks per thread
-                const int hh = beta >> 2, bq = beta & 3;
-                const uint8_t *braw = sm + OFF_BRAW + slot * kBRawBytes + hh * kBRawHalf;
-#pragma unroll
-                for (int it = 0; it < 2; ++it) {
-                    const int tok = 16 * (cw + 4 * it) + (lane & 7) + 8 * (lane >> 4);
-                    const int h = (lane >> 3) & 1;
-                    const int c16 = 2 * bq + h;
-                    const uint4 v =
-                        *reinterpret_cast<const uint4 *>(braw + tok * 128 + ((c16 ^ (tok & 7)) << 4));
-                    uint4 o0, o1;
-                    i8x4_to_f16x4(v.x, o0.x, o0.y);
-                    i8x4_to_f16x4(v.y, o0.z, o0.w);
-                    i8x4_to_f16x4(v.z, o1.x, o1.y);
-                    i8x4_to_f16x4(v.w, o1.z, o1.w);
-                    uint8_t *dst = b16 + (tok >> 3) * 512 + (tok & 7) * 16 + (2 * h) * 128;
-                    *reinterpret_cast<uint4 *>(dst) = o0;
-                    *reinterpret_cast<uint4 *>(dst + 128) = o1;
-                    if (h == 0) {
-                        const uint32_t dw = *reinterpret_cast<const uint32_t *>(
-                            sm + OFF_DRAW + slot * kDRawBytes + tok * 32 + 4 * beta);
-                        sa[tok] = __half2float(__ushort_as_half(static_cast<unsigned short>(dw & 0xffffu)));
-                    }
-                }
-            }
-            q8::fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
-            arrive(f16_full(fs));
-            arrive(sc_full(sc));
-            if (beta == kBlocksPerStage - 1) arrive(raw_empty(slot));
+        const int c = threadIdx.x - 64;  // 0..191
+        for (int s = 0; s < nstages && !*abort_flag; ++s) {
+            if (!convert_block<0>(B, sm, scales, s, c, abort_flag)) break;
+            if (!convert_block<1>(B, sm, scales, s, c, abort_flag)) break;
+            if (!convert_block<2>(B, sm, scales, s, c, abort_flag)) break;
+            if (!convert_block<3>(B, sm, scales, s, c, abort_flag)) break;
+            if (!convert_block<4>(B, sm, scales, s, c, abort_flag)) break;
+            if (!convert_block<5>(B, sm, scales, s, c, abort_flag)) break;
+            if (!convert_block<6>(B, sm, scales, s, c, abort_flag)) break;
+            if (!convert_block<7>(B, sm, scales, s, c, abort_flag)) break;
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;            // TMEM lane quarter of this warp
+        const int hcol = (warp - 8) >> 2;  // column half: tokens [64*hcol, 64*hcol + 64)
         const int r = 32 * q + lane;       // tile row = TMEM lane
-        float acc[BN];
+        float2 acc[32];
 #pragma unroll
-        for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.0f, 0.0f);
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
             const int ab = j % kAcc;
-            if (!wait_bar(acc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
-            if (!wait_bar(sc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
+            if (!wait_bar(B.acc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
+            if (!wait_bar(B.sc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const float *sw = scales + ab * 256;
-            const float *sa = sw + 128;
+            const float *sa = sw + 128 + 64 * hcol;
             const float dw = sw[r];
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BN);
+            const float2 dw2 = make_float2(dw, dw);
+            const uint32_t taddr =
+                tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BN + 64 * hcol);
 #pragma unroll
-            for (int cc = 0; cc < BN / 32; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 float p[32];
                 tc_ld32(taddr + 32 * cc, p);
-                if (cc == BN / 32 - 1) {
+                if (cc == 1) {
                     tc_fence_before();
-                    arrive(acc_empty(ab));  // TMEM buffer free for the next MMA
+                    arrive(B.acc_empty(ab));  // TMEM buffer free for the next MMA
                 }
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     const float4 a4 = *reinterpret_cast<const float4 *>(sa + 32 * cc + i);
-                    acc[32 * cc + i + 0] = fmaf(dw * a4.x, p[i + 0], acc[32 * cc + i + 0]);
-                    acc[32 * cc + i + 1] = fmaf(dw * a4.y, p[i + 1], acc[32 * cc + i + 1]);
-                    acc[32 * cc + i + 2] = fmaf(dw * a4.z, p[i + 2], acc[32 * cc + i + 2]);
-                    acc[32 * cc + i + 3] = fmaf(dw * a4.w, p[i + 3], acc[32 * cc + i + 3]);
+                    const float2 s01 = __fmul2_rn(dw2, make_float2(a4.x, a4.y));
+                    const float2 s23 = __fmul2_rn(dw2, make_float2(a4.z, a4.w));
+                    acc[16 * cc + i / 2] = __ffma2_rn(s01, make_float2(p[i], p[i + 1]), acc[16 * cc + i / 2]);
+                    acc[16 * cc + i / 2 + 1] = __ffma2_rn(s23, make_float2(p[i + 2], p[i + 3]), acc[16 * cc + i / 2 + 1]);
                 }
             }
-            arrive(sc_empty(ab));
+            arrive(B.sc_empty(ab));
         }
         if (ok && !*abort_flag) {
             const int64_t row = n0 + r;
             if (row < n) {
 #pragma unroll
-                for (int i = 0; i < BN; ++i) {
-                    const int64_t tok = t0 + i;
-                    if (tok < t) y[tok * n + row] = acc[i];
+                for (int i = 0; i < 32; ++i) {
+                    const int64_t tok = t0 + 64 * hcol + 2 * i;
+                    if (tok < t) y[tok * n + row] = acc[i].x;
+                    if (tok + 1 < t) y[(tok + 1) * n + row] = acc[i].y;
                 }
             }
         }
