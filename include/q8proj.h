@@ -117,6 +117,11 @@ Q8_API int swiglu_quant(const float *gate, const float *up, float *y,
  * n >= 1, k % 32 == 0.  Row grouping and the split of k across warps are
  * chosen from (n, k) alone, deterministically; results are run-to-run
  * identical.  "Part 4 - Lecture 05", sec. 2.1-2.4.
+ * The kernel is launched with programmatic dependent launch: it may start
+ * streaming `w` while the kernel enqueued just before it on `stream` is
+ * still running, and reads the plane only after that kernel has finished.
+ * `w` (the model weights) must therefore not be written by the kernel
+ * immediately preceding the call on the same stream.
  */
 Q8_API int q8_0_gemv(const void *w, int64_t n, int64_t k,
               const int8_t *qs, const uint32_t *ds, float *y, void *stream);

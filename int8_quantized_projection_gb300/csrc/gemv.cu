@@ -51,7 +51,8 @@ struct GvGeom {
     int64_t groups;  // row groups = ceil(n / rpw)
 };
 
-__host__ __device__ inline int smem_header_bytes() { return kMaxWarps * kStages * 8 + 128; }
+// header: per-warp mbarriers, per-warp stage metadata, the CTA's row-group counter
+__host__ __device__ inline int smem_header_bytes() { return kMaxWarps * kStages * 8 * 2 + 128; }
 
 // One 4-block chunk: 34 words of raw weights (shared memory, 8-byte aligned)
 // against 128 B of qs and 4 ds words of the activation (shared memory).
@@ -96,43 +97,76 @@ gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_r
     const int nwarp = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    int2 *meta = reinterpret_cast<int2 *>(smem + kMaxWarps * kStages * 8);  // (row group, piece) per stage
+    unsigned int *counter = reinterpret_cast<unsigned int *>(smem + kMaxWarps * kStages * 16);
     uint8_t *act = smem + smem_header_bytes();
     uint8_t *ring = act + ((g.nc * kActChunkBytes + 127) & ~127);
     uint64_t *mybar = bars + warp * kStages;
+    int2 *mymeta = meta + warp * kStages;
     uint8_t *myring = ring + warp * kStages * kPieceBytes;
 
+    // This CTA owns a contiguous range of row groups; its warps take groups
+    // from it one at a time (a warp always computes whole rows, so the result
+    // does not depend on which warp takes which group).
     const int64_t pitch = static_cast<int64_t>(g.nc) * kChunkBytes;
-    const int64_t W = static_cast<int64_t>(gridDim.x) * nwarp;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * nwarp + warp;
-    const int64_t g0 = g.groups * gw / W, g1 = g.groups * (gw + 1) / W;
-    const int64_t npieces = (g1 - g0) * g.ppr;
+    const int64_t cg0 = g.groups * blockIdx.x / gridDim.x;
+    const int64_t cg1 = g.groups * (blockIdx.x + 1) / gridDim.x;
+    const unsigned int ngroups = static_cast<unsigned int>(cg1 - cg0);
 
-    // piece i of this warp -> (global source, bytes); every piece is a whole
-    // number of 16-byte granules because chunks come in pairs (272 B).
-    auto piece = [&](int64_t i, uint32_t &bytes) -> const uint8_t * {
-        const int64_t grp = g0 + i / g.ppr;
+    // lane 0's fetch cursor
+    int fetch_grp = -1, fetch_p = 0;
+    bool fetch_done = false;
+    auto issue = [&](int s) {
+        int grp = -1, p = 0;
+        if (!fetch_done) {
+            if (fetch_grp >= 0 && fetch_p < g.ppr) {
+                grp = fetch_grp;
+                p = fetch_p++;
+            } else {
+                const unsigned int gn = atomicAdd(counter, 1u);
+                if (gn < ngroups) {
+                    fetch_grp = grp = static_cast<int>(gn);
+                    fetch_p = 1;
+                    p = 0;
+                } else {
+                    fetch_done = true;
+                }
+            }
+        }
+        mymeta[s] = make_int2(grp, p);
+        if (grp < 0) {  // nothing left: complete the phase so the warp sees the end marker
+            q8::mbar_arrive(&mybar[s]);
+            return;
+        }
+        const int64_t G = cg0 + grp;
+        const uint8_t *src;
+        uint32_t bytes;
         if (g.rpw == 1) {  // one row per piece, up to 32 chunks of it
-            const int p = static_cast<int>(i % g.ppr);
             const int chunks = min(kPieceChunks, g.nc - kPieceChunks * p);
             bytes = static_cast<uint32_t>(chunks * kChunkBytes);
-            return w + grp * pitch + static_cast<int64_t>(kPieceChunks) * p * kChunkBytes;
+            src = w + G * pitch + static_cast<int64_t>(kPieceChunks) * p * kChunkBytes;
+        } else {
+            const int64_t r0 = G * g.rpw;
+            const int64_t rows = min(static_cast<int64_t>(g.rpw), g.n - r0);
+            bytes = static_cast<uint32_t>(rows * pitch);
+            src = w + r0 * pitch;
         }
-        const int64_t r0 = grp * g.rpw;
-        const int64_t rows = min(static_cast<int64_t>(g.rpw), g.n - r0);
-        bytes = static_cast<uint32_t>(rows * pitch);
-        return w + r0 * pitch;
+        q8::mbar_arrive_expect_tx(&mybar[s], bytes);
+        q8::bulk_g2s(myring + s * kPieceBytes, src, bytes, &mybar[s]);
     };
 
+    if (threadIdx.x == 0) *counter = 0u;
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) q8::mbar_init(&mybar[s], 1);
         q8::fence_mbar_init();
-        for (int s = 0; s < kStages && s < npieces; ++s) {
-            uint32_t bytes;
-            const uint8_t *src = piece(s, bytes);
-            q8::mbar_arrive_expect_tx(&mybar[s], bytes);
-            q8::bulk_g2s(myring + s * kPieceBytes, src, bytes, &mybar[s]);
-        }
     }
+    __syncthreads();
+    // The weights do not depend on the previous kernel in the stream: start
+    // streaming them before waiting for it (programmatic dependent launch).
+    if (lane == 0)
+        for (int s = 0; s < kStages; ++s) issue(s);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // stage the activation: chunk c = 8 x 16 B of qs then its 4 ds words
     for (int idx = threadIdx.x; idx < g.nc * 9; idx += blockDim.x) {
         const int c = idx / 9, j = idx - c * 9;
@@ -145,40 +179,37 @@ gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_r
     const int ri = lane >> g.lpr_log2;         // row within a piece
     const int cj = lane & (lpr - 1);           // chunk within a piece
     float acc = 0.0f;
-    for (int64_t i = 0; i < npieces; ++i) {
+    for (uint32_t i = 0;; ++i) {
         const int s = static_cast<int>(i % kStages);
-        const uint32_t par = static_cast<uint32_t>((i / kStages) & 1);
+        const uint32_t par = (i / kStages) & 1u;
         const bool ok = q8::mbar_wait_bounded(&mybar[s], par);
         if (!__all_sync(Q8_FULL_MASK, ok)) {
             if (lane == 0) atomicOr(&g_gemv_err, 1u);
             return;
         }
+        const int2 m = mymeta[s];
+        if (m.x < 0) break;
         const uint8_t *buf = myring + s * kPieceBytes;
-        const int64_t grp = g0 + i / g.ppr;
-        const int p = static_cast<int>(i % g.ppr);
+        const int64_t G = cg0 + m.x;
+        const int p = m.y;
         int64_t row;
         int chunk, soff;
         bool valid;
         if (g.rpw == 1) {
-            row = grp;
+            row = G;
             chunk = kPieceChunks * p + lane;
             soff = lane * kChunkBytes;
             valid = chunk < g.nc;
         } else {
-            row = grp * g.rpw + ri;
+            row = G * g.rpw + ri;
             chunk = cj;
             soff = (ri * g.nc + cj) * kChunkBytes;
             valid = cj < g.nc && row < g.n;
         }
         if (valid) acc += chunk_dot(buf + soff, act + chunk * kActChunkBytes);
         __syncwarp();
-        if (lane == 0 && i + kStages < npieces) {
-            uint32_t bytes;
-            const uint8_t *src = piece(i + kStages, bytes);
-            q8::mbar_arrive_expect_tx(&mybar[s], bytes);
-            q8::bulk_g2s(myring + s * kPieceBytes, src, bytes, &mybar[s]);
-        }
-        if (p == g.ppr - 1) {  // row group complete: reduce over the lanes of each row
+        if (lane == 0) issue(s);  // refill the slot just consumed
+        if (p == g.ppr - 1) {     // row group complete: reduce over the lanes of each row
             for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(Q8_FULL_MASK, acc, o);
             if (cj == 0 && row < g.n) y[row] = acc;
             acc = 0.0f;
@@ -297,7 +328,18 @@ extern "C" int q8_0_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, 
                      static_cast<int>(nw) * kStages * kPieceBytes;
     const int maxs = smem_header_bytes() + kMaxActChunks * kActChunkBytes + kMaxWarps * kStages * kPieceBytes;
     if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(gemv_staged_kernel), maxs, 0)) return Q8_ERR_LAUNCH;
-    gemv_staged_kernel<<<static_cast<unsigned>(grid), static_cast<unsigned>(nw * 32), smem, s>>>(
-        static_cast<const uint8_t *>(w), reinterpret_cast<const uint4 *>(qs), ds, y, g);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(nw * 32));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the producer ends
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemv_staged_kernel, static_cast<const uint8_t *>(w), reinterpret_cast<const uint4 *>(qs),
+                           ds, y, g) != cudaSuccess)
+        return Q8_ERR_LAUNCH;
     return q8::launch_status();
 }

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 quantize_q8_0_kernel(const float4 *__restrict__ x, int64_t n4_valid, int64_t n4_total,
                      uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // consumers may start their prologue
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -74,6 +75,7 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
                      uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
     __shared__ float red[32];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // consumers may start their prologue
     const int64_t t = blockIdx.x;
     const int F = d >> 2;
     const int P = blockDim.x;
@@ -148,6 +150,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 swiglu_quant_kernel(const float4 *__restrict__ g, const float4 *__restrict__ u, float4 *__restrict__ y,
                     int64_t n4_valid, int64_t n4_total, uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // consumers may start their prologue
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
