@@ -7,6 +7,7 @@ the package does not load the library; the first call does, and fails loudly
 if it was not built.
 """
 from ._binding import (  # noqa: F401
+    Bound,
     Q8Error,
     empty_plane,
     lib,

@@ -89,6 +89,34 @@ def _check(fn, st):
         raise Q8Error(fn, st)
 
 
+class Bound:
+    """A C entry point with its arguments already marshalled.
+
+    Calling it re-issues the same launch (same pointers, sizes and stream)
+    with one ctypes call, which keeps the host cost of a decode step far below
+    the GPU time of its kernels.  Returned by the ``bind=True`` form of every
+    launching function."""
+
+    __slots__ = ("name", "fn", "args")
+
+    def __init__(self, name, args):
+        self.name = name
+        self.fn = getattr(lib(), name)
+        self.args = args
+
+    def __call__(self):
+        st = self.fn(*self.args)
+        if st != 0:
+            raise Q8Error(self.name, st)
+
+
+def _launch(name, args, bind):
+    if bind:
+        return Bound(name, args)
+    _check(name, getattr(lib(), name)(*args))
+    return None
+
+
 def _need(t, dtype, name):
     if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name}: expected a contiguous CUDA tensor of {dtype}, got {t.dtype} on {t.device}")
@@ -106,7 +134,7 @@ def q8_check(stream=None) -> None:
     _check("q8_check", lib().q8_check(_stream(stream)))
 
 
-def quantize_q8_0(x, qs, ds, stream=None):
+def quantize_q8_0(x, qs, ds, stream=None, bind=False):
     """x f32 [rows][k] -> plane (qs int8 [rows_pad][k], ds int32 [rows_pad][k/32])."""
     import torch
 
@@ -115,10 +143,10 @@ def quantize_q8_0(x, qs, ds, stream=None):
     rows_pad = qs.shape[0]
     if qs.shape != (rows_pad, k) or ds.shape != (rows_pad, k // 32):
         raise ValueError("plane shape mismatch")
-    _check("quantize_q8_0", lib().quantize_q8_0(_ptr(x), rows, k, _ptr(qs), _ptr(ds), rows_pad, _stream(stream)))
+    return _launch("quantize_q8_0", (_ptr(x), rows, k, _ptr(qs), _ptr(ds), rows_pad, _stream(stream)), bind)
 
 
-def rmsnorm_quant(x, w, eps: float, y, qs, ds, stream=None):
+def rmsnorm_quant(x, w, eps: float, y, qs, ds, stream=None, bind=False):
     import torch
 
     for t, n in ((x, "x"), (w, "w"), (y, "y")):
@@ -128,11 +156,11 @@ def rmsnorm_quant(x, w, eps: float, y, qs, ds, stream=None):
     rows_pad = qs.shape[0]
     if y.shape != x.shape or w.shape != (d,) or qs.shape != (rows_pad, d) or ds.shape != (rows_pad, d // 32):
         raise ValueError("shape mismatch")
-    _check("rmsnorm_quant", lib().rmsnorm_quant(_ptr(x), _ptr(w), ctypes.c_float(eps), _ptr(y), rows, d, _ptr(qs),
-                                                _ptr(ds), rows_pad, _stream(stream)))
+    return _launch("rmsnorm_quant", (_ptr(x), _ptr(w), ctypes.c_float(eps), _ptr(y), rows, d, _ptr(qs), _ptr(ds),
+                                     rows_pad, _stream(stream)), bind)
 
 
-def swiglu_quant(gate, up, y, qs, ds, stream=None):
+def swiglu_quant(gate, up, y, qs, ds, stream=None, bind=False):
     import torch
 
     for t, n in ((gate, "gate"), (up, "up"), (y, "y")):
@@ -142,21 +170,21 @@ def swiglu_quant(gate, up, y, qs, ds, stream=None):
     rows_pad = qs.shape[0]
     if up.shape != gate.shape or y.shape != gate.shape or qs.shape != (rows_pad, nf) or ds.shape != (rows_pad, nf // 32):
         raise ValueError("shape mismatch")
-    _check("swiglu_quant", lib().swiglu_quant(_ptr(gate), _ptr(up), _ptr(y), rows, nf, _ptr(qs), _ptr(ds), rows_pad,
-                                              _stream(stream)))
+    return _launch("swiglu_quant", (_ptr(gate), _ptr(up), _ptr(y), rows, nf, _ptr(qs), _ptr(ds), rows_pad,
+                                    _stream(stream)), bind)
 
 
-def q8_0_gemv(w, n: int, k: int, qs, ds, y, stream=None):
+def q8_0_gemv(w, n: int, k: int, qs, ds, y, stream=None, bind=False):
     """w uint8 [n*k/32*34] Q8_0 blocks; plane row 0 of (qs, ds); y f32 [n]."""
     import torch
 
     _need(w, torch.uint8, "w"), _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds"), _need(y, torch.float32, "y")
     if w.numel() != n * (k // 32) * 34 or y.numel() < n or qs.shape[-1] != k:
         raise ValueError("shape mismatch")
-    _check("q8_0_gemv", lib().q8_0_gemv(_ptr(w), n, k, _ptr(qs), _ptr(ds), _ptr(y), _stream(stream)))
+    return _launch("q8_0_gemv", (_ptr(w), n, k, _ptr(qs), _ptr(ds), _ptr(y), _stream(stream)), bind)
 
 
-def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, stream=None):
+def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=False):
     """Y[t][n] f32 = plane rows [0, t) x Q8_0 weights."""
     import torch
 
@@ -164,10 +192,10 @@ def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, stream=None):
     rows_pad = qs.shape[0]
     if w.numel() != n * (k // 32) * 34 or y.numel() < t * n or qs.shape[-1] != k or ds.shape[0] != rows_pad:
         raise ValueError("shape mismatch")
-    _check("q8_0_gemm", lib().q8_0_gemm(_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y), _stream(stream)))
+    return _launch("q8_0_gemm", (_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y), _stream(stream)), bind)
 
 
-def q8_0_gemm_mma(w, n: int, k: int, qs, ds, t: int, y, stream=None):
+def q8_0_gemm_mma(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=False):
     """Legacy-tensor-path A/B twin of :func:`q8_0_gemm` (mma.sync.m16n8k32.s8)."""
     import torch
 
@@ -175,8 +203,7 @@ def q8_0_gemm_mma(w, n: int, k: int, qs, ds, t: int, y, stream=None):
     rows_pad = qs.shape[0]
     if w.numel() != n * (k // 32) * 34 or y.numel() < t * n or qs.shape[-1] != k or ds.shape[0] != rows_pad:
         raise ValueError("shape mismatch")
-    _check("q8_0_gemm_mma", lib().q8_0_gemm_mma(_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y),
-                                                _stream(stream)))
+    return _launch("q8_0_gemm_mma", (_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y), _stream(stream)), bind)
 
 
 def empty_plane(rows_pad: int, k: int, device="cuda"):

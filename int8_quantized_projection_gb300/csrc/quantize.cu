@@ -62,77 +62,90 @@ quantize_q8_0_kernel(const float4 *__restrict__ x, int64_t n4_valid, int64_t n4_
 }
 
 // --------------------------------------------------------------------------
-// rmsnorm_quant: one CTA per token row; each thread keeps J float4 of the
-// row in registers (float4 index f = tid + j*blockDim), so x is read once,
-// y written once and the plane encoded from the same registers.
-// "54 - r51 - producer-fused A-quantize mode 1", sec. 3.2: ss = sum x^2,
-// scale = rsqrt(ss/d + eps), y = (x * scale) * w.
+// rmsnorm_quant: persistent CTAs, one token row at a time; each thread keeps
+// J float4 of the row in registers (float4 index f = tid + j*blockDim) and
+// prefetches its share of the CTA's next row before reducing the current one,
+// so x is read once, y written once and the plane encoded from the same
+// registers.  "54 - r51 - producer-fused A-quantize mode 1", sec. 3.2:
+// ss = sum x^2, scale = rsqrt(ss/d + eps), y = (x * scale) * w.
 // --------------------------------------------------------------------------
 template <int J>
 __global__ void __launch_bounds__(512)
 rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, float eps,
-                     float *__restrict__ y, int64_t rows, int d,
+                     float *__restrict__ y, int64_t rows, int64_t rows_pad, int d,
                      uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
-    __shared__ float red[32];
+    __shared__ float red[2][32];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // consumers may start their prologue
-    const int64_t t = blockIdx.x;
     const int F = d >> 2;
     const int P = blockDim.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
-    uint32_t *qrow = qs + t * F;
-    uint32_t *drow = ds + t * (F >> 3);
-
-    if (t >= rows) {  // padded token row: zero plane row
-        for (int f = tid; f < F; f += P) {
-            qrow[f] = 0u;
-            if ((f & 7) == 0) drow[f >> 3] = 0u;
-        }
-        return;
-    }
-
-    const float4 *xr = reinterpret_cast<const float4 *>(x + t * static_cast<int64_t>(d));
-    float4 v[J];
-    float ss = 0.0f;
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int f = tid + j * P;
-        v[j] = (f < F) ? ld_stream(xr + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-        ss = fmaf(v[j].x, v[j].x, ss);
-        ss = fmaf(v[j].y, v[j].y, ss);
-        ss = fmaf(v[j].z, v[j].z, ss);
-        ss = fmaf(v[j].w, v[j].w, ss);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(Q8_FULL_MASK, ss, o);
-    if (lane == 0) red[tid >> 5] = ss;
-    __syncthreads();
-    float tot = 0.0f;
     const int nw = P >> 5;
-    for (int i = 0; i < nw; ++i) tot += red[i];  // same fixed order in every thread
-    const float scale = rsqrtf(tot / static_cast<float>(d) + eps);
-
     const float4 *w4 = reinterpret_cast<const float4 *>(w);
-    float4 *yr = reinterpret_cast<float4 *>(y + t * static_cast<int64_t>(d));
+
+    auto load_row = [&](int64_t t, float4 (&v)[J]) {
+        const float4 *xr = reinterpret_cast<const float4 *>(x + t * static_cast<int64_t>(d));
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int f = tid + j * P;
-        const bool ok = f < F;  // uniform over each 8-lane block group
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ok) {
-            const float4 wv = __ldg(w4 + f);
-            o.x = __fmul_rn(__fmul_rn(v[j].x, scale), wv.x);
-            o.y = __fmul_rn(__fmul_rn(v[j].y, scale), wv.y);
-            o.z = __fmul_rn(__fmul_rn(v[j].z, scale), wv.z);
-            o.w = __fmul_rn(__fmul_rn(v[j].w, scale), wv.w);
-            yr[f] = o;
+        for (int j = 0; j < J; ++j) {
+            const int f = tid + j * P;
+            v[j] = (t < rows && f < F) ? ld_stream(xr + f) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const q8::Q8Enc e = q8::q8_encode8(o);
-        if (ok) {
-            qrow[f] = e.qword;
-            if ((lane & 7) == 0) drow[f >> 3] = e.dsword;
+    };
+
+    float4 v[J], vn[J];
+    int64_t t = blockIdx.x;
+    load_row(t, v);
+    for (int it = 0; t < rows_pad; ++it, t += gridDim.x) {
+        const int64_t tn = t + gridDim.x;
+        load_row(tn, vn);  // next row in flight while this one is reduced and written
+        uint32_t *qrow = qs + t * F;
+        uint32_t *drow = ds + t * (F >> 3);
+        if (t >= rows) {  // padded token row: zero plane row
+            for (int f = tid; f < F; f += P) {
+                qrow[f] = 0u;
+                if ((f & 7) == 0) drow[f >> 3] = 0u;
+            }
+        } else {
+            float ss = 0.0f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                ss = fmaf(v[j].x, v[j].x, ss);
+                ss = fmaf(v[j].y, v[j].y, ss);
+                ss = fmaf(v[j].z, v[j].z, ss);
+                ss = fmaf(v[j].w, v[j].w, ss);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(Q8_FULL_MASK, ss, o);
+            float *rb = red[it & 1];  // alternate buffers: one barrier per row suffices
+            if (lane == 0) rb[tid >> 5] = ss;
+            __syncthreads();
+            float tot = 0.0f;
+            for (int i = 0; i < nw; ++i) tot += rb[i];  // same fixed order in every thread
+            const float scale = rsqrtf(tot / static_cast<float>(d) + eps);
+            float4 *yr = reinterpret_cast<float4 *>(y + t * static_cast<int64_t>(d));
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int f = tid + j * P;
+                const bool ok = f < F;  // uniform over each 8-lane block group
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (ok) {
+                    const float4 wv = __ldg(w4 + f);
+                    o.x = __fmul_rn(__fmul_rn(v[j].x, scale), wv.x);
+                    o.y = __fmul_rn(__fmul_rn(v[j].y, scale), wv.y);
+                    o.z = __fmul_rn(__fmul_rn(v[j].z, scale), wv.z);
+                    o.w = __fmul_rn(__fmul_rn(v[j].w, scale), wv.w);
+                    yr[f] = o;
+                }
+                const q8::Q8Enc e = q8::q8_encode8(o);
+                if (ok) {
+                    qrow[f] = e.qword;
+                    if ((lane & 7) == 0) drow[f >> 3] = e.dsword;
+                }
+            }
         }
+#pragma unroll
+        for (int j = 0; j < J; ++j) v[j] = vn[j];
     }
 }
 
@@ -141,9 +154,13 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
 // ("54 - r51 - producer-fused A-quantize mode 1", sec. 3.2), encoded from
 // registers into the plane in the same pass.
 // --------------------------------------------------------------------------
+// silu(g) * u with the hardware exp2 and reciprocal (a few ulp; the f32
+// result is what gets encoded, so the plane stays its exact q8_0 encoding).
+// For g < -87.3 the denominator exceeds 2^126 and the quotient is 0, where
+// the true value is below 1e-36.
 __device__ __forceinline__ float silu_mul(float g, float u)
 {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
 }
 
 __global__ void __launch_bounds__(kQuantThreads)
@@ -229,17 +246,22 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     const int F = static_cast<int>(d / 4);
     int J = 1;
     while (J < 16 && (F + J - 1) / J > 256) J *= 2;
-    int P = ((F + J - 1) / J + 31) / 32 * 32;
+    const int P = ((F + J - 1) / J + 31) / 32 * 32;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const dim3 grid(static_cast<unsigned>(rows_pad));
+    const int sms = q8::device_sm_count();
+    // persistent grid: enough CTAs to fill the SMs (registers allow ~4 per SM
+    // at these block sizes), each walking rows with a stride of the grid
+    const int64_t per_sm = P <= 256 ? 4 : 2;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * per_sm;
+    const dim3 grid(static_cast<unsigned>(rows_pad < cap ? rows_pad : cap));
     uint32_t *q32 = reinterpret_cast<uint32_t *>(qs);
     const int di = static_cast<int>(d);
     switch (J) {
-    case 1: rmsnorm_quant_kernel<1><<<grid, P, 0, s>>>(x, w, eps, y, rows, di, q32, ds); break;
-    case 2: rmsnorm_quant_kernel<2><<<grid, P, 0, s>>>(x, w, eps, y, rows, di, q32, ds); break;
-    case 4: rmsnorm_quant_kernel<4><<<grid, P, 0, s>>>(x, w, eps, y, rows, di, q32, ds); break;
-    case 8: rmsnorm_quant_kernel<8><<<grid, P, 0, s>>>(x, w, eps, y, rows, di, q32, ds); break;
-    default: rmsnorm_quant_kernel<16><<<grid, P, 0, s>>>(x, w, eps, y, rows, di, q32, ds); break;
+    case 1: rmsnorm_quant_kernel<1><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
+    case 2: rmsnorm_quant_kernel<2><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
+    case 4: rmsnorm_quant_kernel<4><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
+    case 8: rmsnorm_quant_kernel<8><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
+    default: rmsnorm_quant_kernel<16><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
     }
     return q8::launch_status();
 }
