@@ -127,6 +127,31 @@ Q8_API int q8_0_gemv(const void *w, int64_t n, int64_t k,
               const int8_t *qs, const uint32_t *ds, float *y, void *stream);
 
 /*
+ * q8_0_gemv_grouped -- several batch-1 projections of ONE activation in one
+ * launch: for each i < count, projs[i].y[r] = sum_b d_w * d_a * isum over the
+ * rows of projs[i].w, all against plane row 0 of (qs, ds) with the same k.
+ *   projs : host array of `count` descriptors (read during the call only);
+ *           each w and y is a device pointer as for q8_0_gemv, n >= 1.
+ *   count : 1..Q8_MAX_GROUP.
+ * Rows of all projections are spread over the whole GPU together, so small
+ * projections ride along with large ones instead of each paying a launch and
+ * a partly idle grid.  Same numerics as q8_0_gemv (one row is always computed
+ * the same way), and the same programmatic-dependent-launch precondition on w.
+ * "Part 4 - Lecture 05", sec. 2.5 (one launch for the consumers of one
+ * activation) and sec. 6 (generalised to projections of different widths).
+ * When (k/32) % 8 != 0 the projections are launched one by one.
+ */
+#define Q8_MAX_GROUP 8
+typedef struct q8_gemv_proj {
+    const void *w;   /* n rows of k/32 Q8_0 blocks */
+    int64_t n;       /* rows (outputs) */
+    float *y;        /* f32 [n] output */
+} q8_gemv_proj;
+
+Q8_API int q8_0_gemv_grouped(const q8_gemv_proj *projs, int count, int64_t k,
+                             const int8_t *qs, const uint32_t *ds, void *stream);
+
+/*
  * q8_0_gemm -- prefill projection Y[t][i] = sum_b d_w(i,b) * d_a(t,b) * isum.
  *   w      : n rows of k/32 Q8_0 blocks (input)
  *   qs, ds : plane with rows_pad >= t rows (input; rows >= t are not read)

@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     q8_0_gemm,
     q8_0_gemm_mma,
     q8_0_gemv,
+    q8_0_gemv_grouped,
     q8_check,
     q8_num_sms,
     q8_plane_rows,

@@ -33,9 +33,19 @@ SIGNATURES = {
     "q8_0_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q8_0_gemm": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
     "q8_0_gemm_mma": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
+    "q8_0_gemv_grouped": (_INT, [_P, _INT, _I64, _P, _P, _P]),
     "q8_check": (_INT, [_P]),
     "q8_num_sms": (_INT, []),
 }
+
+
+MAX_GROUP = 8
+
+
+class GemvProj(ctypes.Structure):
+    """C struct q8_gemv_proj: one projection of a grouped GEMV."""
+
+    _fields_ = [("w", ctypes.c_void_p), ("n", ctypes.c_int64), ("y", ctypes.c_void_p)]
 
 
 class Q8Error(RuntimeError):
@@ -97,12 +107,13 @@ class Bound:
     the GPU time of its kernels.  Returned by the ``bind=True`` form of every
     launching function."""
 
-    __slots__ = ("name", "fn", "args")
+    __slots__ = ("name", "fn", "args", "_keep")
 
     def __init__(self, name, args):
         self.name = name
         self.fn = getattr(lib(), name)
         self.args = args
+        self._keep = None
 
     def __call__(self):
         st = self.fn(*self.args)
@@ -182,6 +193,33 @@ def q8_0_gemv(w, n: int, k: int, qs, ds, y, stream=None, bind=False):
     if w.numel() != n * (k // 32) * 34 or y.numel() < n or qs.shape[-1] != k:
         raise ValueError("shape mismatch")
     return _launch("q8_0_gemv", (_ptr(w), n, k, _ptr(qs), _ptr(ds), _ptr(y), _stream(stream)), bind)
+
+
+def q8_0_gemv_grouped(projs, k: int, qs, ds, stream=None, bind=False):
+    """Several projections of one activation in one launch.
+
+    ``projs`` is a sequence of (w uint8 Q8_0 blocks, n, y f32 [n]) sharing k and
+    plane row 0 of (qs, ds)."""
+    import torch
+
+    _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds")
+    if not 1 <= len(projs) <= MAX_GROUP or qs.shape[-1] != k:
+        raise ValueError("1..8 projections sharing k")
+    arr = (GemvProj * len(projs))()
+    keep = []
+    for i, (w, n, y) in enumerate(projs):
+        _need(w, torch.uint8, "w"), _need(y, torch.float32, "y")
+        if w.numel() != n * (k // 32) * 34 or y.numel() < n:
+            raise ValueError("shape mismatch")
+        arr[i] = GemvProj(w.data_ptr(), n, y.data_ptr())
+        keep.append((w, y))
+    args = (ctypes.cast(arr, ctypes.c_void_p), len(projs), k, _ptr(qs), _ptr(ds), _stream(stream))
+    if bind:
+        b = Bound("q8_0_gemv_grouped", args)
+        b._keep = (arr, keep)  # the descriptor array must outlive the bound launch
+        return b
+    _check("q8_0_gemv_grouped", lib().q8_0_gemv_grouped(*args))
+    return None
 
 
 def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=False):

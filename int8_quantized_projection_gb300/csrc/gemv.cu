@@ -42,14 +42,35 @@ constexpr int kStages = 2;
 constexpr int kMaxWarps = 16;
 constexpr int kMaxActChunks = 512;              // k <= 65536 on the staged path
 
+constexpr int kMaxProj = Q8_MAX_GROUP;        // projections of one activation per launch
+
+struct GvProj {
+    const uint8_t *w;  // n rows of Q8_0 blocks
+    float *y;          // n outputs
+    int64_t n;
+    int64_t g_begin;   // first row group of this projection in the launch's group list
+};
+
+// Geometry shared by all projections of a launch (they share k).
 struct GvGeom {
-    int64_t n;       // weight rows
+    GvProj p[kMaxProj];
+    int count;
     int nc;          // 4-block chunks per row (even: k/32 % 8 == 0)
     int lpr_log2;    // lanes per row = 1 << lpr_log2
     int rpw;         // rows per piece
     int ppr;         // pieces per row group
-    int64_t groups;  // row groups = ceil(n / rpw)
+    int64_t groups;  // total row groups over all projections
 };
+
+// global row group -> projection index
+__device__ __forceinline__ int proj_of(const GvGeom &g, int64_t G)
+{
+    int j = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxProj; ++i)
+        if (i < g.count && G >= g.p[i].g_begin) j = i;
+    return j;
+}
 
 // header: per-warp mbarriers, per-warp stage metadata, the CTA's row-group counter
 __host__ __device__ inline int smem_header_bytes() { return kMaxWarps * kStages * 8 * 2 + 128; }
@@ -90,11 +111,10 @@ __device__ __forceinline__ float chunk_dot(const uint8_t *wc, const uint8_t *ac)
 }
 
 __global__ void __launch_bounds__(kMaxWarps * 32)
-gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_row,
-                   const uint32_t *__restrict__ ds_row, float *__restrict__ y, GvGeom g)
+gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict__ ds_row,
+                   const __grid_constant__ GvGeom g)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int nwarp = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     int2 *meta = reinterpret_cast<int2 *>(smem + kMaxWarps * kStages * 8);  // (row group, piece) per stage
@@ -139,17 +159,19 @@ gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_r
             return;
         }
         const int64_t G = cg0 + grp;
+        const GvProj &pj = g.p[proj_of(g, G)];
+        const int64_t Gl = G - pj.g_begin;  // row group within the projection
         const uint8_t *src;
         uint32_t bytes;
         if (g.rpw == 1) {  // one row per piece, up to 32 chunks of it
             const int chunks = min(kPieceChunks, g.nc - kPieceChunks * p);
             bytes = static_cast<uint32_t>(chunks * kChunkBytes);
-            src = w + G * pitch + static_cast<int64_t>(kPieceChunks) * p * kChunkBytes;
+            src = pj.w + Gl * pitch + static_cast<int64_t>(kPieceChunks) * p * kChunkBytes;
         } else {
-            const int64_t r0 = G * g.rpw;
-            const int64_t rows = min(static_cast<int64_t>(g.rpw), g.n - r0);
+            const int64_t r0 = Gl * g.rpw;
+            const int64_t rows = min(static_cast<int64_t>(g.rpw), pj.n - r0);
             bytes = static_cast<uint32_t>(rows * pitch);
-            src = w + r0 * pitch;
+            src = pj.w + r0 * pitch;
         }
         q8::mbar_arrive_expect_tx(&mybar[s], bytes);
         q8::bulk_g2s(myring + s * kPieceBytes, src, bytes, &mybar[s]);
@@ -191,27 +213,29 @@ gemv_staged_kernel(const uint8_t *__restrict__ w, const uint4 *__restrict__ qs_r
         if (m.x < 0) break;
         const uint8_t *buf = myring + s * kPieceBytes;
         const int64_t G = cg0 + m.x;
+        const GvProj &pj = g.p[proj_of(g, G)];
+        const int64_t Gl = G - pj.g_begin;
         const int p = m.y;
         int64_t row;
         int chunk, soff;
         bool valid;
         if (g.rpw == 1) {
-            row = G;
+            row = Gl;
             chunk = kPieceChunks * p + lane;
             soff = lane * kChunkBytes;
             valid = chunk < g.nc;
         } else {
-            row = G * g.rpw + ri;
+            row = Gl * g.rpw + ri;
             chunk = cj;
             soff = (ri * g.nc + cj) * kChunkBytes;
-            valid = cj < g.nc && row < g.n;
+            valid = cj < g.nc && row < pj.n;
         }
         if (valid) acc += chunk_dot(buf + soff, act + chunk * kActChunkBytes);
         __syncwarp();
         if (lane == 0) issue(s);  // refill the slot just consumed
         if (p == g.ppr - 1) {     // row group complete: reduce over the lanes of each row
             for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(Q8_FULL_MASK, acc, o);
-            if (cj == 0 && row < g.n) y[row] = acc;
+            if (cj == 0 && row < pj.n) pj.y[row] = acc;
             acc = 0.0f;
         }
     }
@@ -294,19 +318,15 @@ int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, c
 
 } // namespace q8
 
-extern "C" int q8_0_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
-                         void *stream)
-{
-    if (!w || !qs || !ds || !y || n < 1 || k <= 0 || (k % 32) != 0) return Q8_ERR_ARG;
-    if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
-    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t nb = k / 32;
-    if (nb % 8 != 0 || nb / 4 > kMaxActChunks || n > (int64_t(1) << 40))
-        return q8::gemv_generic_launch(w, n, k, qs, ds, y, 1, s);
+namespace {
 
+// Launch the staged kernel for `count` projections of one activation.
+int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds,
+                       cudaStream_t s)
+{
+    const int64_t nb = k / 32;
     GvGeom g;
-    g.n = n;
+    g.count = count;
     g.nc = static_cast<int>(nb / 4);
     if (g.nc > kPieceChunks) {
         g.lpr_log2 = 5;
@@ -317,7 +337,22 @@ extern "C" int q8_0_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, 
         g.rpw = 32 >> g.lpr_log2;
         g.ppr = 1;
     }
-    g.groups = (n + g.rpw - 1) / g.rpw;
+    int64_t groups = 0;
+    for (int i = 0; i < kMaxProj; ++i) {
+        if (i < count) {
+            g.p[i].w = static_cast<const uint8_t *>(projs[i].w);
+            g.p[i].y = projs[i].y;
+            g.p[i].n = projs[i].n;
+            g.p[i].g_begin = groups;
+            groups += (projs[i].n + g.rpw - 1) / g.rpw;
+        } else {
+            g.p[i].w = nullptr;
+            g.p[i].y = nullptr;
+            g.p[i].n = 0;
+            g.p[i].g_begin = groups;
+        }
+    }
+    g.groups = groups;
     const int sms = q8::device_sm_count();
     if (sms <= 0) return Q8_ERR_DEVICE;
     int64_t nw = (g.groups + sms - 1) / sms;
@@ -338,8 +373,50 @@ extern "C" int q8_0_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemv_staged_kernel, static_cast<const uint8_t *>(w), reinterpret_cast<const uint4 *>(qs),
-                           ds, y, g) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, gemv_staged_kernel, reinterpret_cast<const uint4 *>(qs), ds, g) != cudaSuccess)
         return Q8_ERR_LAUNCH;
     return q8::launch_status();
+}
+
+int check_gemv_args(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds)
+{
+    if (!projs || count < 1 || count > Q8_MAX_GROUP || !qs || !ds || k <= 0 || (k % 32) != 0) return Q8_ERR_ARG;
+    for (int i = 0; i < count; ++i) {
+        if (!projs[i].w || !projs[i].y || projs[i].n < 1 || projs[i].n > (int64_t(1) << 40)) return Q8_ERR_ARG;
+        if (!q8::aligned16(projs[i].w) || !q8::aligned16(projs[i].y)) return Q8_ERR_ALIGN;
+    }
+    if (!q8::aligned16(qs) || !q8::aligned16(ds)) return Q8_ERR_ALIGN;
+    return Q8_OK;
+}
+
+int gemv_dispatch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds, void *stream)
+{
+    int st = check_gemv_args(projs, count, k, qs, ds);
+    if (st != Q8_OK) return st;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t nb = k / 32;
+    if (nb % 8 != 0 || nb / 4 > kMaxActChunks) {  // generic kernel, one launch per projection
+        for (int i = 0; i < count; ++i) {
+            st = q8::gemv_generic_launch(projs[i].w, projs[i].n, k, qs, ds, projs[i].y, 1, s);
+            if (st != Q8_OK) return st;
+        }
+        return Q8_OK;
+    }
+    return gemv_staged_launch(projs, count, k, qs, ds, s);
+}
+
+} // namespace
+
+extern "C" int q8_0_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                         void *stream)
+{
+    const q8_gemv_proj p = {w, n, y};
+    return gemv_dispatch(&p, 1, k, qs, ds, stream);
+}
+
+extern "C" int q8_0_gemv_grouped(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs,
+                                 const uint32_t *ds, void *stream)
+{
+    return gemv_dispatch(projs, count, k, qs, ds, stream);
 }

@@ -61,6 +61,46 @@ def _run_gemv(q8, blob, n, k, qs, ds):
     return host(y)
 
 
+@pytest.mark.parametrize("k,ns", [(7168, [3072, 512, 512, 3072]), (7168, [12288, 96]),
+                                  (3584, [1, 7, 64, 129, 1000, 33, 5, 2048]), (18944, [77, 3584]), (128, [512, 3])])
+def test_gemv_grouped_equals_single_and_oracle(q8, k, ns):
+    """One launch for several projections of one activation: bit-identical to
+    the per-projection calls (a row is computed the same way) and within the
+    oracle tolerance."""
+    import torch
+
+    qs, ds = _plane(9, 1, k)
+    qd, dd = dev(qs), dev(ds.view(np.int32))
+    blobs = [_weights(10 + i, n, k) for i, n in enumerate(ns)]
+    wd = [dev(b) for b in blobs]
+    ys = [nan_f32(n) for n in ns]
+    q8.q8_0_gemv_grouped([(w, n, y) for w, n, y in zip(wd, ns, ys)], k, qd, dd)
+    q8.q8_check()
+    for w, blob, n, y in zip(wd, blobs, ns, ys):
+        y1 = nan_f32(n)
+        q8.q8_0_gemv(w, n, k, qd, dd, y1)
+        q8.q8_check()
+        assert torch.equal(y, y1)
+        yr, ar = oracle.gemv(blob, n, k, qs, ds)
+        assert_gemm_close(host(y), yr, ar, f"grouped gemv {n}x{k}")
+
+
+def test_gemv_grouped_rejects_bad_counts(q8):
+    import torch
+
+    qs = torch.zeros((1, 64), dtype=torch.int8, device="cuda")
+    ds = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    lib = q8.lib()
+    assert lib.q8_0_gemv_grouped(None, 1, 64, qs.data_ptr(), ds.data_ptr(), None) == 1
+    w = torch.zeros(34 * 2, dtype=torch.uint8, device="cuda")
+    y = torch.zeros(1, dtype=torch.float32, device="cuda")
+    arr = (q8._binding.GemvProj * 9)(*[q8._binding.GemvProj(w.data_ptr(), 1, y.data_ptr())] * 9)
+    import ctypes
+
+    assert lib.q8_0_gemv_grouped(ctypes.cast(arr, ctypes.c_void_p), 9, 64, qs.data_ptr(), ds.data_ptr(), None) == 1
+    assert lib.q8_0_gemv_grouped(ctypes.cast(arr, ctypes.c_void_p), 0, 64, qs.data_ptr(), ds.data_ptr(), None) == 1
+
+
 GEMM_ENTRY = ["q8_0_gemm", "q8_0_gemm_mma"]
 
 
@@ -206,10 +246,12 @@ def test_shared_activation_decode_chain(q8):
     q8.rmsnorm_quant(dev(x), dev(w), 1e-6, y, qs, ds)
     q8.q8_check()
     qsh, dsh = host(qs), host(ds).view(np.uint32)
-    for i, n in enumerate([3072, 512, 512, 3072]):
-        blob = syn.q8_0_weights(syn.rng(2, 1 + i), n, d)[0]
-        out = nan_f32(n)
-        q8.q8_0_gemv(dev(blob), n, d, qs, ds, out)
-        q8.q8_check()
+    ns = [3072, 512, 512, 3072]
+    blobs = [syn.q8_0_weights(syn.rng(2, 1 + i), n, d)[0] for i, n in enumerate(ns)]
+    outs = [nan_f32(n) for n in ns]
+    # the whole shared-activation chain is two launches: rmsnorm_quant + one grouped GEMV
+    q8.q8_0_gemv_grouped([(dev(b), n, o) for b, n, o in zip(blobs, ns, outs)], d, qs, ds)
+    q8.q8_check()
+    for i, (blob, n, out) in enumerate(zip(blobs, ns, outs)):
         yr, ar = oracle.gemv(blob, n, d, qsh, dsh)
         assert_gemm_close(host(out), yr, ar, f"decode chain proj {i}")
