@@ -44,7 +44,8 @@ PREFILL = dict(tokens=3325, d=3584, nf=18944, eps=1e-6)
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
 # kernel from the ncu capture summarised under profiles/ (None until taken,
 # and reset to None whenever that kernel changes).
-NCU_TRAFFIC_BYTES = {"gemv_staged_kernel 12288x7168": None, "gemm 18944x3584 t=3325": None}
+NCU_TRAFFIC_BYTES = {"gemv_staged 12288x7168+96x7168": 97_942_016,     # profiles/gemv_staged_12288x7168_plus_96x7168.md
+                     "gemm_tc 18944x3584 t=3325": 619_668_000}         # profiles/gemm_tc_18944x3584_t3325.md
 
 
 # ---------------------------------------------------------------------------
@@ -450,7 +451,7 @@ def main():
             "roofline": {"kernel": "q8_0_gemv_grouped 12288x7168 + 96x7168 (gemv_staged_kernel)", "bound": "hbm",
                          "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-                         "traffic": NCU_TRAFFIC_BYTES["gemv_staged_kernel 12288x7168"],
+                         "traffic": NCU_TRAFFIC_BYTES["gemv_staged 12288x7168+96x7168"],
                          "algorithmic_bytes": big, "avg_launch_us": round(dec["kern_ms"] * 1e3, 3)},
             "cpu_baseline": cpu,
             "e2e": {"value": round(world * step_bytes * args.steps / dec["e2e_s"] / 1e9, 2), "unit": "GB/s",
@@ -469,7 +470,7 @@ def main():
             "gemm_tops": round(tops, 2), "unit": "int8 TOPS (2*T*N*K per GEMM)",
             "roofline_gemm": {"kernel": "q8_0_gemm (gemm_tc_kernel)", "bound": "tensor", "achieved": round(tops, 2),
                               "peak": peak, "unit": "TFLOP/s", "frac": round(tops / peak, 4),
-                              "traffic": NCU_TRAFFIC_BYTES["gemm 18944x3584 t=3325"],
+                              "traffic": NCU_TRAFFIC_BYTES["gemm_tc 18944x3584 t=3325"],
                               "peak_note": f"sustained dense bf16/f16 tensor peak ({peaks['source']}); sm_103a has "
                                            "no int8 tcgen05 kind"},
             "quantize_gbs": {"rmsnorm_quant": round(bytes_rmsnorm_quant(T, d) / pre["rmsnorm_quant"] / 1e6, 1),

@@ -348,9 +348,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    q8::griddep_launch_dependents();
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            // Inputs may come from the previous kernel on the stream; every other
+            // role only touches data this thread brings in, and Y is written
+            // after the last MMA, so this is the only wait needed.
+            q8::griddep_wait();
             int issued = 0;
             for (int s = 0; s < nstages && !*abort_flag; ++s) {
                 const int slot = s % kRawStages;
@@ -532,8 +537,7 @@ int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const 
         return Q8_ERR_LAUNCH;
     if (!set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel), kSmemBytes, 2)) return Q8_ERR_LAUNCH;
     const dim3 grid(static_cast<unsigned>((n + BM - 1) / BM), static_cast<unsigned>((t + BN - 1) / BN));
-    gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(ma, mb, md, n, t, static_cast<int>(nb), y);
-    return launch_status();
+    return launch_pdl(gemm_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, ma, mb, md, n, t, static_cast<int>(nb), y);
 }
 
 } // namespace q8

@@ -248,6 +248,8 @@ __global__ void __launch_bounds__(128)
 gemv_generic_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, const int8_t *__restrict__ qs,
                     const uint32_t *__restrict__ ds, float *__restrict__ y, int lpr_log2)
 {
+    q8::griddep_launch_dependents();
+    q8::griddep_wait();  // the plane may come from the previous kernel
     const int lane = threadIdx.x & 31;
     const int lpr = 1 << lpr_log2;
     const int rpw = 32 >> lpr_log2;
@@ -312,8 +314,8 @@ int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, c
     const int rpw = 32 >> lpr_log2;
     const int64_t warps = (n + rpw - 1) / rpw;
     const dim3 grid(static_cast<unsigned>((warps + 3) / 4), static_cast<unsigned>(tokens));
-    gemv_generic_kernel<<<grid, 128, 0, s>>>(static_cast<const uint8_t *>(w), n, nb, qs, ds, y, lpr_log2);
-    return launch_status();
+    return launch_pdl(gemv_generic_kernel, grid, dim3(128), 0, s, static_cast<const uint8_t *>(w), n, nb, qs, ds, y,
+                      lpr_log2);
 }
 
 } // namespace q8

@@ -33,6 +33,26 @@ int launch_status();                   // Q8_OK or Q8_ERR_LAUNCH from cudaGetLas
 // slots are small integers owned by the calling translation unit.
 bool set_max_dynamic_smem(const void *func, int bytes, int slot);
 
+// Launch `kernel` with programmatic dependent launch allowed: it may start
+// while the previous kernel on the stream is still running, so it must call
+// griddep_wait() before touching memory that kernel may write.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) return Q8_ERR_LAUNCH;
+    return launch_status();
+}
+
 // Per-translation-unit device error words are read and cleared through these
 // (each .cu file that has bounded waits defines one).
 int gemv_take_error(cudaStream_t s);
@@ -116,6 +136,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Wait until the previous kernel on the stream has finished and its writes
+// are visible (no-op when launched without programmatic dependent launch).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel on the stream to begin launching.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c)

@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 quantize_q8_0_kernel(const float4 *__restrict__ x, int64_t n4_valid, int64_t n4_total,
                      uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // consumers may start their prologue
+    q8::griddep_launch_dependents();  // consumers may start their prologue
+    q8::griddep_wait();               // inputs may come from the previous kernel
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -76,7 +77,8 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
                      uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
     __shared__ float red[2][32];
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // consumers may start their prologue
+    q8::griddep_launch_dependents();  // consumers may start their prologue
+    q8::griddep_wait();               // inputs may come from the previous kernel
     const int F = d >> 2;
     const int P = blockDim.x;
     const int tid = threadIdx.x;
@@ -167,7 +169,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 swiglu_quant_kernel(const float4 *__restrict__ g, const float4 *__restrict__ u, float4 *__restrict__ y,
                     int64_t n4_valid, int64_t n4_total, uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // consumers may start their prologue
+    q8::griddep_launch_dependents();  // consumers may start their prologue
+    q8::griddep_wait();               // inputs may come from the previous kernel
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -229,9 +232,9 @@ extern "C" int quantize_q8_0(const float *x, int64_t rows, int64_t k, int8_t *qs
     if (rows > 0 && !q8::aligned16(x)) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     const int64_t n4_valid = rows * k / 4, n4_total = rows_pad * k / 4;
-    quantize_q8_0_kernel<<<flat_grid(n4_total, kQuantUnroll), kQuantThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const float4 *>(x), n4_valid, n4_total, reinterpret_cast<uint32_t *>(qs), ds);
-    return q8::launch_status();
+    return q8::launch_pdl(quantize_q8_0_kernel, dim3(flat_grid(n4_total, kQuantUnroll)), dim3(kQuantThreads), 0,
+                          static_cast<cudaStream_t>(stream), reinterpret_cast<const float4 *>(x), n4_valid, n4_total,
+                          reinterpret_cast<uint32_t *>(qs), ds);
 }
 
 extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y, int64_t rows, int64_t d,
@@ -257,13 +260,12 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     uint32_t *q32 = reinterpret_cast<uint32_t *>(qs);
     const int di = static_cast<int>(d);
     switch (J) {
-    case 1: rmsnorm_quant_kernel<1><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
-    case 2: rmsnorm_quant_kernel<2><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
-    case 4: rmsnorm_quant_kernel<4><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
-    case 8: rmsnorm_quant_kernel<8><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
-    default: rmsnorm_quant_kernel<16><<<grid, P, 0, s>>>(x, w, eps, y, rows, rows_pad, di, q32, ds); break;
+    case 1: return q8::launch_pdl(rmsnorm_quant_kernel<1>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    case 2: return q8::launch_pdl(rmsnorm_quant_kernel<2>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    case 4: return q8::launch_pdl(rmsnorm_quant_kernel<4>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    case 8: return q8::launch_pdl(rmsnorm_quant_kernel<8>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    default: return q8::launch_pdl(rmsnorm_quant_kernel<16>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
     }
-    return q8::launch_status();
 }
 
 extern "C" int swiglu_quant(const float *gate, const float *up, float *y, int64_t rows, int64_t nf, int8_t *qs,
@@ -275,8 +277,8 @@ extern "C" int swiglu_quant(const float *gate, const float *up, float *y, int64_
     if (rows > 0 && (!q8::aligned16(gate) || !q8::aligned16(up) || !q8::aligned16(y))) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     const int64_t n4_valid = rows * nf / 4, n4_total = rows_pad * nf / 4;
-    swiglu_quant_kernel<<<flat_grid(n4_total, 2), kQuantThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const float4 *>(gate), reinterpret_cast<const float4 *>(up), reinterpret_cast<float4 *>(y),
-        n4_valid, n4_total, reinterpret_cast<uint32_t *>(qs), ds);
-    return q8::launch_status();
+    return q8::launch_pdl(swiglu_quant_kernel, dim3(flat_grid(n4_total, 2)), dim3(kQuantThreads), 0,
+                          static_cast<cudaStream_t>(stream), reinterpret_cast<const float4 *>(gate),
+                          reinterpret_cast<const float4 *>(up), reinterpret_cast<float4 *>(y), n4_valid, n4_total,
+                          reinterpret_cast<uint32_t *>(qs), ds);
 }
