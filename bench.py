@@ -287,23 +287,21 @@ def run_prefill(torch, q8p, steps, warmup, dev):
     O = torch.empty((T, d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     names = ["rmsnorm_quant", "gemm_gate", "gemm_up", "swiglu_quant", "gemm_down"]
+    ws_d = q8p.gemm_workspace(T, d, dev)    # gate and up: same plane, ordered on one stream
+    ws_f = q8p.gemm_workspace(T, nf, dev)   # down
+    calls = [q8p.rmsnorm_quant(x, w, eps, y, *pa, bind=True),
+             q8p.q8_0_gemm(wg, nf, d, *pa, T, G, workspace=ws_d, bind=True),
+             q8p.q8_0_gemm(wu, nf, d, *pa, T, U, workspace=ws_d, bind=True),
+             q8p.swiglu_quant(G, U, Y, *pb, bind=True),
+             q8p.q8_0_gemm(wd, d, nf, *pb, T, O, workspace=ws_f, bind=True)]
 
     def step(ev=None):
-        def mark(i):
+        for i, call in enumerate(calls):
             if ev is not None:
                 ev[i].record(stream)
-
-        mark(0)
-        q8p.rmsnorm_quant(x, w, eps, y, *pa)
-        mark(1)
-        q8p.q8_0_gemm(wg, nf, d, *pa, T, G)
-        mark(2)
-        q8p.q8_0_gemm(wu, nf, d, *pa, T, U)
-        mark(3)
-        q8p.swiglu_quant(G, U, Y, *pb)
-        mark(4)
-        q8p.q8_0_gemm(wd, d, nf, *pb, T, O)
-        mark(5)
+            call()
+        if ev is not None:
+            ev[5].record(stream)
 
     for _ in range(warmup):
         step()

@@ -152,18 +152,33 @@ Q8_API int q8_0_gemv_grouped(const q8_gemv_proj *projs, int count, int64_t k,
                              const int8_t *qs, const uint32_t *ds, void *stream);
 
 /*
+ * q8_0_gemm_workspace_bytes -- device workspace q8_0_gemm needs for t tokens
+ * of width k: t*k*2 bytes (rounded up to 256) + t*(k/32)*16 bytes; 0 when
+ * (k/32) % 8 != 0 (that shape needs none).
+ */
+Q8_API size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k);
+
+/*
  * q8_0_gemm -- prefill projection Y[t][i] = sum_b d_w(i,b) * d_a(t,b) * isum.
  *   w      : n rows of k/32 Q8_0 blocks (input)
  *   qs, ds : plane with rows_pad >= t rows (input; rows >= t are not read)
  *   y      : f32 [t][n] row-major (output)
+ *   workspace, workspace_bytes : caller-owned device scratch of at least
+ *            q8_0_gemm_workspace_bytes(t, k) bytes, 16-byte aligned; its
+ *            contents on entry are ignored and on return are unspecified.
+ *            Two calls may share a workspace only if they are ordered on one
+ *            stream.  May be NULL when that size is 0.
  * n >= 1, t >= 1, k % 32 == 0.  Every 32-wide k block is one q8_0 block on
- * both sides, so its integer dot product is scaled by d_w * d_a once.
+ * both sides, so its integer dot product is scaled by d_w * d_a once.  The
+ * call enqueues a pre-pass that writes the plane's codes as f16 (exact) and
+ * its scales into the workspace, then the tcgen05 GEMM (both with
+ * programmatic dependent launch; the same precondition on w as q8_0_gemv).
  * "12 - r5-r6 re-ranking + structural rewrite spec", sec. 2 and 3.1;
  * "54 - r51 - producer-fused A-quantize mode 1", sec. 2.1.
  */
 Q8_API int q8_0_gemm(const void *w, int64_t n, int64_t k,
-              const int8_t *qs, const uint32_t *ds, int64_t t, int64_t rows_pad,
-              float *y, void *stream);
+                     const int8_t *qs, const uint32_t *ds, int64_t t, int64_t rows_pad,
+                     float *y, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * q8_0_gemm_mma -- the same contraction as q8_0_gemm on the warp-level int8

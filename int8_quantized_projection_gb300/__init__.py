@@ -10,11 +10,13 @@ from ._binding import (  # noqa: F401
     Bound,
     Q8Error,
     empty_plane,
+    gemm_workspace,
     lib,
     library_path,
     load,
     q8_0_gemm,
     q8_0_gemm_mma,
+    q8_0_gemm_workspace_bytes,
     q8_0_gemv,
     q8_0_gemv_grouped,
     q8_check,

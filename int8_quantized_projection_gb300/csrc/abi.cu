@@ -74,7 +74,8 @@ int gemm_mma_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const
                     cudaStream_t s);
 
 int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t, float *y,
-                   cudaStream_t s);
+                   void *workspace, cudaStream_t s);
+size_t gemm_workspace_bytes(int64_t t, int64_t k);
 
 } // namespace q8
 
@@ -111,19 +112,28 @@ extern "C" int q8_check(void *stream)
     return b;
 }
 
+extern "C" size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k)
+{
+    if (t < 1 || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0) return 0;
+    return q8::gemm_workspace_bytes(t, k);
+}
+
 extern "C" int q8_0_gemm(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t,
-                         int64_t rows_pad, float *y, void *stream)
+                         int64_t rows_pad, float *y, void *workspace, size_t workspace_bytes, void *stream)
 {
     if (!w || !qs || !ds || !y || n < 1 || t < 1 || k <= 0 || (k % 32) != 0 || rows_pad < t) return Q8_ERR_ARG;
+    const size_t need = q8_0_gemm_workspace_bytes(t, k);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return Q8_ERR_ARG;
     if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
+    if (need > 0 && !q8::aligned16(workspace)) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((k / 32) % 8 != 0) {
         if (t > 65535) return Q8_ERR_ARG;  // generic kernel: one grid row per token
         return q8::gemv_generic_launch(w, n, k, qs, ds, y, t, s);
     }
-    if (t > int64_t(65535) * 128 || n > (int64_t(1) << 31) - 128) return Q8_ERR_ARG;
-    return q8::gemm_tc_launch(w, n, k, qs, ds, t, y, s);
+    if (t > int64_t(65535) * 128 || n > (int64_t(1) << 31) - 128 || k > (int64_t(1) << 31) / 2) return Q8_ERR_ARG;
+    return q8::gemm_tc_launch(w, n, k, qs, ds, t, y, workspace, s);
 }
 
 extern "C" int q8_0_gemm_mma(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t,

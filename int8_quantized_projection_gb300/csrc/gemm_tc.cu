@@ -14,19 +14,26 @@
 // unpacked at MMA time) and the q8_0 plane of "54 - r51 - producer-fused
 // A-quantize mode 1" (sec. 2.1).
 //
+// Before the GEMM proper, a small pre-pass (gemm_prep_kernel) writes the
+// plane once per call into the caller's workspace as f16 tokens x k plus one
+// f16 d_a column per block ("prepared operand"), so the GEMM loads it with
+// TMA directly in the layout the tensor core reads -- every weight tile reuses
+// it, instead of converting the same activation in every CTA.
+//
 // One CTA computes a 128 (weight rows) x 128 (tokens) tile over all of k.
+// Per 32-wide block, three MMAs: two K=16 steps for the exact integer partial
+// P, and one K=16 MMA whose operands hold only d_w (weights side, column 0)
+// and d_a (token side, column 0) -- the other core matrices point at a zero
+// tile -- producing S = d_w (x) d_a exactly in TMEM.  The epilogue is then a
+// single acc += S * P per output (packed f32x2 fma), with no shared-memory
+// traffic.
 // Warp roles (512 threads):
-//   warp 0      TMA producer: raw Q8_0 rows (2D u16 map, 8 blocks per stage),
-//               plane qs (2D u8 map, 128B swizzle) and ds words (2D u32 map)
+//   warp 0      TMA producer for raw Q8_0 weight rows (8 blocks per stage)
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2-7   converters: raw int8 -> f16 operand tiles in the canonical
-//               K-major no-swizzle layout, one 32-wide block at a time, plus
-//               the block's scales as f32 (weight rows read with three
-//               16-byte loads, bank-conflict free)
-//   warps 8-15  epilogue: two warps per TMEM lane quarter, 64 tokens each;
-//               per block, tcgen05.ld of the partial, acc += (d_w * d_a) *
-//               partial with packed f32x2 multiply / fma, then one coalesced
-//               store of Y
+//   warp 2      TMA producer for the prepared activation (4 blocks per stage)
+//   warps 4-7   converters: one weight row each, raw int8 -> f16 canonical
+//               K-major tile and the row's d_w as an f16 operand column
+//   warps 8-15  epilogue: two warps per TMEM lane quarter, 64 tokens each
 // Every mbarrier wait is bounded; a wait that runs out sets the CTA abort
 // flag and the library error word, and all roles drain and exit.
 #include <cuda.h>
@@ -38,33 +45,35 @@ namespace {
 __device__ unsigned int g_gemm_err;
 
 constexpr int BM = 128, BN = 128;
-constexpr int kBlocksPerStage = 8;                 // k = 256 per raw stage
-constexpr int kRawStages = 2;
-constexpr int kF16Slots = 4;
-constexpr int kAcc = 4;                            // TMEM block buffers of BN columns
-constexpr int kTmemCols = kAcc * BN;               // 512
-constexpr int kConvThreads = 192;                  // warps 2-7
+constexpr int kABlocksPerStage = 8;                // raw weight stage: 8 blocks = 272 bytes per row
+constexpr int kBBlocksPerStage = 4;                // prepared activation stage: 4 blocks = 128 f16 per token
+constexpr int kAStages = 2, kBStages = 2, kF16Slots = 4, kAcc = 2;
+constexpr int kTmemCols = 512;                     // kAcc x (partial BN + scale BN)
+constexpr int kConvThreads = 128;                  // warps 4-7
 constexpr int kEpiThreads = 256;                   // warps 8-15
-constexpr int kThreads = 64 + kConvThreads + kEpiThreads;  // 512
+constexpr int kThreads = 512;
 
 constexpr int kARawBytes = BM * 272;               // 34816
-constexpr int kBRawHalf = BN * 128;                // 16384 (128B-swizzled rows)
-constexpr int kBRawBytes = 2 * kBRawHalf;          // 32768
-constexpr int kDRawBytes = BN * 32;                // 4096
-constexpr int kStageTx = kARawBytes + kBRawBytes + kDRawBytes;  // 71680
-constexpr int kF16Tile = 128 * 64;                 // 8192: 128 rows x 32 f16
-constexpr int kF16SlotBytes = 2 * kF16Tile;        // A and B
+constexpr int kB16Box = BN * 128;                  // 16384: 128 tokens x 64 f16 (one 128B-swizzle atom column)
+constexpr int kB16Bytes = 2 * kB16Box;             // 32768 per stage
+constexpr int kBsBlock = BN * 16;                  // 2048: 128 tokens x (d_a, 7 zeros) f16
+constexpr int kBsBytes = kBBlocksPerStage * kBsBlock;  // 8192 per stage
+constexpr int kBStageTx = kB16Bytes + kBsBytes;    // 40960
+constexpr int kA16Tile = BM * 64;                  // 8192: 128 rows x 32 f16, no swizzle
+constexpr int kAsTile = BM * 16;                   // 2048: 128 rows x (d_w, 7 zeros) f16
+constexpr int kZeroBytes = 2048;                   // the zero core matrices of both scale operands
 
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int OFF_BRAW = 0;                                        // 2 x 32768 (1024-aligned)
-constexpr int OFF_ARAW = OFF_BRAW + kRawStages * kBRawBytes;       // 65536
-constexpr int OFF_DRAW = OFF_ARAW + kRawStages * kARawBytes;       // 135168
-constexpr int OFF_F16 = OFF_DRAW + kRawStages * kDRawBytes;        // 143360
-constexpr int OFF_SCALE = OFF_F16 + kF16Slots * kF16SlotBytes;     // 208896
-constexpr int OFF_BAR = OFF_SCALE + kAcc * 2 * 128 * 4;            // 212992
-constexpr int kNumBars = 2 * kRawStages + 2 * kF16Slots + 4 * kAcc + 1; // 29 (last: MMA drain)
-constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
-constexpr int kSmemBytes = OFF_MISC + 16 + 1024;                   // + alignment slack
+constexpr int OFF_B16 = 0;                                      // 2 x 32768 (1024-aligned boxes)
+constexpr int OFF_BS = OFF_B16 + kBStages * kB16Bytes;          // 65536
+constexpr int OFF_ARAW = OFF_BS + kBStages * kBsBytes;          // 81920
+constexpr int OFF_A16 = OFF_ARAW + kAStages * kARawBytes;       // 151552
+constexpr int OFF_AS = OFF_A16 + kF16Slots * kA16Tile;          // 184320
+constexpr int OFF_ZERO = OFF_AS + kF16Slots * kAsTile;          // 192512
+constexpr int OFF_BAR = OFF_ZERO + kZeroBytes;                  // 194560
+constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kF16Slots + 2 * kAcc + 1;  // 21 (last: MMA drain)
+constexpr int OFF_MISC = OFF_BAR + kNumBars * 8 + 8;
+constexpr int kSmemBytes = OFF_MISC + 16 + 1024;                // + alignment slack
 
 // ---------------------------------------------------------------------------
 // PTX wrappers specific to this kernel
@@ -97,35 +106,34 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per thread.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32])
+// 16 consecutive TMEM columns of this warp's 32 lanes -> 16 registers per
+// thread, without waiting (pair with tc_wait_ld).
+__device__ __forceinline__ void tc_ld16_nowait(uint32_t taddr, uint32_t (&r)[16])
 {
-    uint32_t r[32];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of
-// 8 rows x 16 bytes; LBO = byte step between core matrices along k, SBO =
-// byte step between 8-row groups.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major.  No swizzle: core matrices of
+// 8 rows x 16 bytes, LBO = byte step between core matrices along k, SBO =
+// byte step between 8-row groups.  128-byte swizzle: rows of 128 bytes in
+// 1024-byte atoms of 8 rows, SBO = 1024, LBO unused; a k offset inside the
+// atom is added to the start address.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, bool sw128 = false)
 {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((addr >> 4) & 0x3fffu);
     d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
     d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
-    return d;                             // base offset 0, swizzle none
+    if (sw128) d |= static_cast<uint64_t>(2) << 61;
+    return d;                             // base offset 0
 }
 
 // Instruction descriptor: D f32, A and B f16, both K-major, M = 128, N = BN.
@@ -193,9 +201,10 @@ __device__ __forceinline__ void arrive(uint32_t bar)
 
 // Converter step for weight row r, raw block BETA of the stage: read the 48
 // bytes (three 16-byte aligned, bank-conflict-free loads) that contain the
-// row's 34-byte block, write the 32 codes as f16 into the A tile and d as f32.
+// row's 34-byte block, write the 32 codes as f16 into the A tile and d_w into
+// the row's slot of the scale-operand column.
 template <int BETA>
-__device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16, float *sw, int r)
+__device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16, uint8_t *as, int r)
 {
     constexpr int off = 34 * BETA;
     constexpr int c0 = off >> 4;        // first 16-byte chunk
@@ -210,7 +219,8 @@ __device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16,
         w[4 * c + 3] = v.w;
     }
     const uint32_t dbits = (o & 2) ? (w[o >> 2] >> 16) : (w[o >> 2] & 0xffffu);
-    sw[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+    // d_w operand column: row r of an 8-wide core-matrix column, k = 0 holds d_w
+    *reinterpret_cast<uint4 *>(as + (r >> 3) * 128 + (r & 7) * 16) = make_uint4(dbits, 0u, 0u, 0u);
     uint32_t qw[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -226,80 +236,42 @@ __device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16,
     }
 }
 
-// Converter step for one (token, 16-byte half-block) task of raw block BETA.
-template <int BETA>
-__device__ __forceinline__ void convert_b_task(const uint8_t *braw_stage, const uint8_t *draw_stage, uint8_t *b16,
-                                               float *sa, int id)
-{
-    const int l = id & 31;
-    const int tok = 16 * (id >> 5) + (l & 7) + 8 * (l >> 4);
-    const int h = (l >> 3) & 1;
-    constexpr int hh = BETA >> 2, bq = BETA & 3;
-    const int c16 = 2 * bq + h;
-    const uint8_t *braw = braw_stage + hh * kBRawHalf;
-    const uint4 v = *reinterpret_cast<const uint4 *>(braw + tok * 128 + ((c16 ^ (tok & 7)) << 4));
-    uint4 o0, o1;
-    i8x4_to_f16x4(v.x, o0.x, o0.y);
-    i8x4_to_f16x4(v.y, o0.z, o0.w);
-    i8x4_to_f16x4(v.z, o1.x, o1.y);
-    i8x4_to_f16x4(v.w, o1.z, o1.w);
-    uint8_t *dst = b16 + (tok >> 3) * 512 + (tok & 7) * 16 + (2 * h) * 128;
-    *reinterpret_cast<uint4 *>(dst) = o0;
-    *reinterpret_cast<uint4 *>(dst + 128) = o1;
-    if (h == 0) {
-        const uint32_t dw = *reinterpret_cast<const uint32_t *>(draw_stage + tok * 32 + 4 * BETA);
-        sa[tok] = __half2float(__ushort_as_half(static_cast<unsigned short>(dw & 0xffffu)));
-    }
-}
-
 struct Bars {
     uint32_t b0;
-    __device__ uint32_t raw_full(int s) const { return b0 + 8u * s; }
-    __device__ uint32_t raw_empty(int s) const { return b0 + 8u * (kRawStages + s); }
-    __device__ uint32_t f16_full(int s) const { return b0 + 8u * (2 * kRawStages + s); }
-    __device__ uint32_t f16_empty(int s) const { return b0 + 8u * (2 * kRawStages + kF16Slots + s); }
-    __device__ uint32_t acc_full(int s) const { return b0 + 8u * (2 * kRawStages + 2 * kF16Slots + s); }
-    __device__ uint32_t acc_empty(int s) const { return b0 + 8u * (2 * kRawStages + 2 * kF16Slots + kAcc + s); }
-    __device__ uint32_t sc_full(int s) const { return b0 + 8u * (2 * kRawStages + 2 * kF16Slots + 2 * kAcc + s); }
-    __device__ uint32_t sc_empty(int s) const { return b0 + 8u * (2 * kRawStages + 2 * kF16Slots + 3 * kAcc + s); }
+    __device__ uint32_t a_full(int s) const { return b0 + 8u * s; }
+    __device__ uint32_t a_empty(int s) const { return b0 + 8u * (kAStages + s); }
+    __device__ uint32_t b_full(int s) const { return b0 + 8u * (2 * kAStages + s); }
+    __device__ uint32_t b_empty(int s) const { return b0 + 8u * (2 * kAStages + kBStages + s); }
+    __device__ uint32_t f_full(int s) const { return b0 + 8u * (2 * kAStages + 2 * kBStages + s); }
+    __device__ uint32_t f_empty(int s) const { return b0 + 8u * (2 * kAStages + 2 * kBStages + kF16Slots + s); }
+    __device__ uint32_t acc_full(int s) const { return b0 + 8u * (2 * kAStages + 2 * kBStages + 2 * kF16Slots + s); }
+    __device__ uint32_t acc_empty(int s) const
+    {
+        return b0 + 8u * (2 * kAStages + 2 * kBStages + 2 * kF16Slots + kAcc + s);
+    }
     __device__ uint32_t drain() const { return b0 + 8u * (kNumBars - 1); }
 };
 
-// One 32-wide block of the stage for the converter role.
+// One 32-wide block of a raw weight stage for the converter role.
 template <int BETA>
-__device__ __forceinline__ bool convert_block(const Bars &B, uint8_t *sm, float *scales, int s, int c,
-                                              volatile int *abort_flag)
+__device__ __forceinline__ bool convert_block(const Bars &B, uint8_t *sm, int s, int r, volatile int *abort_flag)
 {
-    const int slot = s % kRawStages;
-    const int j = s * kBlocksPerStage + BETA;
-    constexpr int fs = BETA % kF16Slots, sc = BETA % kAcc;
-    if (BETA == 0 && !wait_bar(B.raw_full(slot), static_cast<uint32_t>(s / kRawStages) & 1u, abort_flag))
-        return false;
-    if (!wait_bar(B.f16_empty(fs), (static_cast<uint32_t>(j / kF16Slots) & 1u) ^ 1u, abort_flag)) return false;
-    if (!wait_bar(B.sc_empty(sc), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) return false;
-    uint8_t *a16 = sm + OFF_F16 + fs * kF16SlotBytes;
-    uint8_t *b16 = a16 + kF16Tile;
-    float *sw = scales + sc * 256;
-    float *sa = sw + 128;
-    const uint8_t *braw = sm + OFF_BRAW + slot * kBRawBytes;
-    const uint8_t *draw = sm + OFF_DRAW + slot * kDRawBytes;
-    if (c < 128) {
-        convert_a_row<BETA>(sm + OFF_ARAW + slot * kARawBytes + c * 272, a16, sw, c);
-        convert_b_task<BETA>(braw, draw, b16, sa, c);
-    } else {
-        convert_b_task<BETA>(braw, draw, b16, sa, 128 + (c - 128));
-        convert_b_task<BETA>(braw, draw, b16, sa, 192 + (c - 128));
-    }
+    const int slot = s % kAStages;
+    const int j = s * kABlocksPerStage + BETA;
+    constexpr int fs = BETA % kF16Slots;
+    if (BETA == 0 && !wait_bar(B.a_full(slot), static_cast<uint32_t>(s / kAStages) & 1u, abort_flag)) return false;
+    if (!wait_bar(B.f_empty(fs), (static_cast<uint32_t>(j / kF16Slots) & 1u) ^ 1u, abort_flag)) return false;
+    convert_a_row<BETA>(sm + OFF_ARAW + slot * kARawBytes + r * 272, sm + OFF_A16 + fs * kA16Tile,
+                        sm + OFF_AS + fs * kAsTile, r);
     q8::fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
-    arrive(B.f16_full(fs));
-    arrive(B.sc_full(sc));
-    if (BETA == kBlocksPerStage - 1) arrive(B.raw_empty(slot));
+    arrive(B.f_full(fs));
+    if (BETA == kABlocksPerStage - 1) arrive(B.a_empty(slot));
     return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmD, int64_t n, int64_t t, int nb, float *__restrict__ y)
+               const __grid_constant__ CUtensorMap tmS, int64_t n, int64_t t, int nb, float *__restrict__ y)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = q8::smem_u32(smem_raw);
@@ -309,33 +281,38 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const Bars B{base + OFF_BAR};
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + 4);
-    float *scales = reinterpret_cast<float *>(sm + OFF_SCALE);  // [kAcc][2][128]: d_w rows, d_a tokens
 
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * BM;
     const int64_t t0 = static_cast<int64_t>(blockIdx.y) * BN;
-    const int nstages = nb / kBlocksPerStage;
 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_gemm_err) != 0u) ? 1 : 0;
         uint64_t *b = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-        for (int s = 0; s < kRawStages; ++s) {
-            q8::mbar_init(b + s, 1);                               // raw_full: TMA bytes
-            q8::mbar_init(b + kRawStages + s, kConvThreads);       // raw_empty
+        for (int i = 0; i < kAStages; ++i) {
+            q8::mbar_init(b + i, 1);                                   // a_full: TMA bytes
+            q8::mbar_init(b + kAStages + i, kConvThreads);             // a_empty
         }
-        for (int s = 0; s < kF16Slots; ++s) {
-            q8::mbar_init(b + 2 * kRawStages + s, kConvThreads);   // f16_full
-            q8::mbar_init(b + 2 * kRawStages + kF16Slots + s, 1);  // f16_empty: tcgen05.commit
+        for (int i = 0; i < kBStages; ++i) {
+            q8::mbar_init(b + 2 * kAStages + i, 1);                    // b_full: TMA bytes
+            q8::mbar_init(b + 2 * kAStages + kBStages + i, 1);         // b_empty: tcgen05.commit
         }
-        uint64_t *a = b + 2 * kRawStages + 2 * kF16Slots;
-        for (int s = 0; s < kAcc; ++s) {
-            q8::mbar_init(a + s, 1);                     // acc_full: tcgen05.commit
-            q8::mbar_init(a + kAcc + s, kEpiThreads);    // acc_empty
-            q8::mbar_init(a + 2 * kAcc + s, kConvThreads); // sc_full
-            q8::mbar_init(a + 3 * kAcc + s, kEpiThreads);  // sc_empty
+        uint64_t *f = b + 2 * kAStages + 2 * kBStages;
+        for (int i = 0; i < kF16Slots; ++i) {
+            q8::mbar_init(f + i, kConvThreads);                        // f_full
+            q8::mbar_init(f + kF16Slots + i, 1);                       // f_empty: tcgen05.commit
         }
-        q8::mbar_init(b + kNumBars - 1, 1);              // MMA drain
+        uint64_t *a = f + 2 * kF16Slots;
+        for (int i = 0; i < kAcc; ++i) {
+            q8::mbar_init(a + i, 1);                                   // acc_full: tcgen05.commit
+            q8::mbar_init(a + kAcc + i, kEpiThreads);                  // acc_empty
+        }
+        q8::mbar_init(b + kNumBars - 1, 1);                            // MMA drain
         q8::fence_mbar_init();
     }
+    // the zero core matrices of the two scale operands
+    for (int i = threadIdx.x; i < kZeroBytes / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(sm + OFF_ZERO)[i] = make_uint4(0u, 0u, 0u, 0u);
+    q8::fence_proxy_async_smem();
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          q8::smem_u32(tmem_slot)),
@@ -349,68 +326,93 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
 
     q8::griddep_launch_dependents();
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ TMA producers
         if (lane == 0) {
             // Inputs may come from the previous kernel on the stream; every other
-            // role only touches data this thread brings in, and Y is written
-            // after the last MMA, so this is the only wait needed.
+            // role only touches data these threads bring in, and Y is written
+            // after the last MMA, so these are the only waits needed.
             q8::griddep_wait();
+            const bool is_a = warp == 0;
+            const int nstages = is_a ? nb / kABlocksPerStage : nb / kBBlocksPerStage;
+            const int nbuf = is_a ? kAStages : kBStages;
             int issued = 0;
             for (int s = 0; s < nstages && !*abort_flag; ++s) {
-                const int slot = s % kRawStages;
-                const uint32_t use = static_cast<uint32_t>(s / kRawStages);
-                if (!wait_bar(B.raw_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.raw_full(slot)),
-                             "r"(kStageTx)
-                             : "memory");
-                tma_load_2d(base + OFF_ARAW + slot * kARawBytes, &tmA, s * 136, static_cast<int>(n0), B.raw_full(slot));
-                tma_load_2d(base + OFF_BRAW + slot * kBRawBytes, &tmB, s * 256, static_cast<int>(t0), B.raw_full(slot));
-                tma_load_2d(base + OFF_BRAW + slot * kBRawBytes + kBRawHalf, &tmB, s * 256 + 128,
-                            static_cast<int>(t0), B.raw_full(slot));
-                tma_load_2d(base + OFF_DRAW + slot * kDRawBytes, &tmD, s * 8, static_cast<int>(t0), B.raw_full(slot));
+                const int slot = s % nbuf;
+                const uint32_t use = static_cast<uint32_t>(s / nbuf);
+                if (is_a) {
+                    if (!wait_bar(B.a_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.a_full(slot)),
+                                 "r"(kARawBytes)
+                                 : "memory");
+                    tma_load_2d(base + OFF_ARAW + slot * kARawBytes, &tmA, s * 136, static_cast<int>(n0),
+                                B.a_full(slot));
+                } else {
+                    if (!wait_bar(B.b_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.b_full(slot)),
+                                 "r"(kBStageTx)
+                                 : "memory");
+                    const uint32_t dst = base + OFF_B16 + slot * kB16Bytes;
+                    tma_load_2d(dst, &tmB, s * 128, static_cast<int>(t0), B.b_full(slot));
+                    tma_load_2d(dst + kB16Box, &tmB, s * 128 + 64, static_cast<int>(t0), B.b_full(slot));
+#pragma unroll
+                    for (int j = 0; j < kBBlocksPerStage; ++j)
+                        tma_load_2d(base + OFF_BS + slot * kBsBytes + j * kBsBlock, &tmS,
+                                    (s * kBBlocksPerStage + j) * 8, static_cast<int>(t0), B.b_full(slot));
+                }
                 issued = s + 1;
             }
             // drain: the last stages issued must have landed before the CTA exits
-            for (int s = issued - kRawStages < 0 ? 0 : issued - kRawStages; s < issued; ++s)
-                drain_bar(B.raw_full(s % kRawStages), static_cast<uint32_t>(s / kRawStages) & 1u);
+            for (int s = issued - nbuf < 0 ? 0 : issued - nbuf; s < issued; ++s)
+                drain_bar(is_a ? B.a_full(s % nbuf) : B.b_full(s % nbuf), static_cast<uint32_t>(s / nbuf) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             for (int j = 0; j < nb; ++j) {
                 const int fs = j % kF16Slots, ab = j % kAcc;
-                if (!wait_bar(B.f16_full(fs), static_cast<uint32_t>(j / kF16Slots) & 1u, abort_flag)) break;
+                const int sb = (j / kBBlocksPerStage) % kBStages, bq = j % kBBlocksPerStage;
+                if (!wait_bar(B.f_full(fs), static_cast<uint32_t>(j / kF16Slots) & 1u, abort_flag)) break;
+                if (bq == 0 &&
+                    !wait_bar(B.b_full(sb), static_cast<uint32_t>(j / (kBBlocksPerStage * kBStages)) & 1u, abort_flag))
+                    break;
                 if (!wait_bar(B.acc_empty(ab), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t a_addr = base + OFF_F16 + fs * kF16SlotBytes;
-                const uint32_t b_addr = a_addr + kF16Tile;
-                const uint32_t d = tmem + static_cast<uint32_t>(ab * BN);
+                const uint32_t dP = tmem + static_cast<uint32_t>(ab * 2 * BN);
+                const uint32_t dS = dP + BN;
+                const uint32_t a_addr = base + OFF_A16 + fs * kA16Tile;
+                const uint32_t b_addr = base + OFF_B16 + sb * kB16Bytes + (bq >> 1) * kB16Box + 64 * (bq & 1);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)  // two K=16 steps = one 32-wide block
-                    tc_mma_f16(d, smem_desc(a_addr + 256 * kk, 128, 512), smem_desc(b_addr + 256 * kk, 128, 512),
+                    tc_mma_f16(dP, smem_desc(a_addr + 256 * kk, 128, 512), smem_desc(b_addr + 32 * kk, 16, 1024, true),
                                kIdesc, kk);
-                tc_commit(B.f16_empty(fs));
+                const uint32_t as_addr = base + OFF_AS + fs * kAsTile;
+                const uint32_t bs_addr = base + OFF_BS + sb * kBsBytes + bq * kBsBlock;
+                tc_mma_f16(dS, smem_desc(as_addr, base + OFF_ZERO - as_addr, 128),
+                           smem_desc(bs_addr, base + OFF_ZERO - bs_addr, 128), kIdesc, 0);
+                tc_commit(B.f_empty(fs));
                 tc_commit(B.acc_full(ab));
+                if (bq == kBBlocksPerStage - 1) tc_commit(B.b_empty(sb));
             }
             // drain: every MMA issued must have completed before TMEM is freed
             tc_commit(B.drain());
             drain_bar(B.drain(), 0);
         }
-    } else if (warp < 8) {
+    } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ converters
-        const int c = threadIdx.x - 64;  // 0..191
+        const int r = threadIdx.x - 128;  // weight row of the tile, 0..127
+        const int nstages = nb / kABlocksPerStage;
         for (int s = 0; s < nstages && !*abort_flag; ++s) {
-            if (!convert_block<0>(B, sm, scales, s, c, abort_flag)) break;
-            if (!convert_block<1>(B, sm, scales, s, c, abort_flag)) break;
-            if (!convert_block<2>(B, sm, scales, s, c, abort_flag)) break;
-            if (!convert_block<3>(B, sm, scales, s, c, abort_flag)) break;
-            if (!convert_block<4>(B, sm, scales, s, c, abort_flag)) break;
-            if (!convert_block<5>(B, sm, scales, s, c, abort_flag)) break;
-            if (!convert_block<6>(B, sm, scales, s, c, abort_flag)) break;
-            if (!convert_block<7>(B, sm, scales, s, c, abort_flag)) break;
+            if (!convert_block<0>(B, sm, s, r, abort_flag)) break;
+            if (!convert_block<1>(B, sm, s, r, abort_flag)) break;
+            if (!convert_block<2>(B, sm, s, r, abort_flag)) break;
+            if (!convert_block<3>(B, sm, s, r, abort_flag)) break;
+            if (!convert_block<4>(B, sm, s, r, abort_flag)) break;
+            if (!convert_block<5>(B, sm, s, r, abort_flag)) break;
+            if (!convert_block<6>(B, sm, s, r, abort_flag)) break;
+            if (!convert_block<7>(B, sm, s, r, abort_flag)) break;
         }
-    } else {
+    } else if (warp >= 8) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;            // TMEM lane quarter of this warp
         const int hcol = (warp - 8) >> 2;  // column half: tokens [64*hcol, 64*hcol + 64)
@@ -422,32 +424,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int j = 0; j < nb; ++j) {
             const int ab = j % kAcc;
             if (!wait_bar(B.acc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
-            if (!wait_bar(B.sc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const float *sw = scales + ab * 256;
-            const float *sa = sw + 128 + 64 * hcol;
-            const float dw = sw[r];
-            const float2 dw2 = make_float2(dw, dw);
             const uint32_t taddr =
-                tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BN + 64 * hcol);
+                tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * 2 * BN + 64 * hcol);
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                float p[32];
-                tc_ld32(taddr + 32 * cc, p);
-                if (cc == 1) {
+            for (int c = 0; c < 4; ++c) {
+                uint32_t p[16], sv[16];
+                tc_ld16_nowait(taddr + 16 * c, p);
+                tc_ld16_nowait(taddr + BN + 16 * c, sv);
+                tc_wait_ld();
+                if (c == 3) {
                     tc_fence_before();
-                    arrive(B.acc_empty(ab));  // TMEM buffer free for the next MMA
+                    arrive(B.acc_empty(ab));  // TMEM buffer free for the next block's MMAs
                 }
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(sa + 32 * cc + i);
-                    const float2 s01 = __fmul2_rn(dw2, make_float2(a4.x, a4.y));
-                    const float2 s23 = __fmul2_rn(dw2, make_float2(a4.z, a4.w));
-                    acc[16 * cc + i / 2] = __ffma2_rn(s01, make_float2(p[i], p[i + 1]), acc[16 * cc + i / 2]);
-                    acc[16 * cc + i / 2 + 1] = __ffma2_rn(s23, make_float2(p[i + 2], p[i + 3]), acc[16 * cc + i / 2 + 1]);
-                }
+                for (int i = 0; i < 8; ++i)
+                    acc[8 * c + i] = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
+                                                make_float2(__uint_as_float(p[2 * i]), __uint_as_float(p[2 * i + 1])),
+                                                acc[8 * c + i]);
             }
-            arrive(B.sc_empty(ab));
         }
         if (ok && !*abort_flag) {
             const int64_t row = n0 + r;
@@ -467,6 +462,33 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// Pre-pass: plane (qs, ds) rows [0, t) -> prepared operand in the workspace:
+// b16[t][k] = f16(q) (exact) and bs[t][k/32][8] = (f16 d_a, 0 x 7).
+__global__ void __launch_bounds__(256)
+gemm_prep_kernel(const uint4 *__restrict__ qs, const uint32_t *__restrict__ ds, int64_t t, int64_t k,
+                 uint4 *__restrict__ b16, uint4 *__restrict__ bs)
+{
+    q8::griddep_launch_dependents();
+    q8::griddep_wait();  // the plane may come from the previous kernel
+    const int64_t c16 = k / 16;  // 16-code chunks per token
+    const int64_t total = t * c16;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint4 v = __ldg(qs + i);  // qs row stride k == c16 chunks: flat index
+        uint4 o0, o1;
+        i8x4_to_f16x4(v.x, o0.x, o0.y);
+        i8x4_to_f16x4(v.y, o0.z, o0.w);
+        i8x4_to_f16x4(v.z, o1.x, o1.y);
+        i8x4_to_f16x4(v.w, o1.z, o1.w);
+        b16[2 * i] = o0;
+        b16[2 * i + 1] = o1;
+        if ((i & 1) == 0) {  // first chunk of a 32-wide block: its d_a column entry
+            const int64_t blk = i >> 1;  // == tok * (k/32) + block
+            bs[blk] = make_uint4(__ldg(ds + blk) & 0xffffu, 0u, 0u, 0u);
+        }
     }
 }
 
@@ -521,23 +543,41 @@ int gemm_take_error(cudaStream_t s)
     return v ? Q8_ERR_DEVICE_TIMEOUT : Q8_OK;
 }
 
-// Requires k/32 % 8 == 0, 16-byte aligned pointers (checked by the caller).
+size_t gemm_workspace_bytes(int64_t t, int64_t k)
+{
+    const size_t b16 = static_cast<size_t>(t) * static_cast<size_t>(k) * 2;
+    return (b16 + 255) / 256 * 256 + static_cast<size_t>(t) * static_cast<size_t>(k / 32) * 16;
+}
+
+// Requires k/32 % 8 == 0, 16-byte aligned pointers and a workspace of at least
+// gemm_workspace_bytes(t, k) bytes (checked by the caller).
 int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t, float *y,
-                   cudaStream_t s)
+                   void *workspace, cudaStream_t s)
 {
     const int64_t nb = k / 32;
     const int64_t pitch = nb * 34;
-    CUtensorMap ma, mb, md;
+    uint8_t *b16 = static_cast<uint8_t *>(workspace);
+    uint8_t *bs = b16 + (static_cast<size_t>(t) * static_cast<size_t>(k) * 2 + 255) / 256 * 256;
+    CUtensorMap ma, mb, ms;
     if (!make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w, static_cast<uint64_t>(pitch / 2),
                      static_cast<uint64_t>(n), static_cast<uint64_t>(pitch), 136, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qs, static_cast<uint64_t>(k), static_cast<uint64_t>(t),
-                     static_cast<uint64_t>(k), 128, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ds, static_cast<uint64_t>(nb), static_cast<uint64_t>(t),
-                     static_cast<uint64_t>(nb * 4), 8, BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, b16, static_cast<uint64_t>(k), static_cast<uint64_t>(t),
+                     static_cast<uint64_t>(k * 2), 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, bs, static_cast<uint64_t>(nb * 8), static_cast<uint64_t>(t),
+                     static_cast<uint64_t>(nb * 16), 8, BN, CU_TENSOR_MAP_SWIZZLE_NONE))
         return Q8_ERR_LAUNCH;
+    const int sms = device_sm_count();
+    const int64_t chunks = t * (k / 16);
+    int64_t pgrid = (chunks + 255) / 256;
+    const int64_t pcap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
+    pgrid = pgrid < pcap ? pgrid : pcap;
+    int st = launch_pdl(gemm_prep_kernel, dim3(static_cast<unsigned>(pgrid)), dim3(256), 0, s,
+                        reinterpret_cast<const uint4 *>(qs), ds, t, k, reinterpret_cast<uint4 *>(b16),
+                        reinterpret_cast<uint4 *>(bs));
+    if (st != Q8_OK) return st;
     if (!set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel), kSmemBytes, 2)) return Q8_ERR_LAUNCH;
     const dim3 grid(static_cast<unsigned>((n + BM - 1) / BM), static_cast<unsigned>((t + BN - 1) / BN));
-    return launch_pdl(gemm_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, ma, mb, md, n, t, static_cast<int>(nb), y);
+    return launch_pdl(gemm_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, ma, mb, ms, n, t, static_cast<int>(nb), y);
 }
 
 } // namespace q8
