@@ -60,6 +60,7 @@ extern "C" {
 #define Q8_ERR_LAUNCH         4  /* the kernel launch failed (cudaGetLastError) */
 #define Q8_ERR_DEVICE_TIMEOUT 5  /* a bounded on-device wait ran out (reported by q8_check) */
 #define Q8_ERR_CUDA           6  /* another CUDA runtime error (stream sync, symbol copy) */
+#define Q8_ERR_TOO_BIG        7  /* the request needs more than the fixed scratch of q8_0_gemm_noalloc */
 
 /* Recommended number of plane rows for `rows` tokens: rows rounded up to a
  * multiple of 128 (the GEMM's token tile).  Any rows_pad >= rows is accepted
@@ -179,6 +180,37 @@ Q8_API size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k);
 Q8_API int q8_0_gemm(const void *w, int64_t n, int64_t k,
                      const int8_t *qs, const uint32_t *ds, int64_t t, int64_t rows_pad,
                      float *y, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * q8_0_gemm_noalloc -- q8_0_gemm without a workspace argument, for callers
+ * that cannot allocate device memory at this point: a serving engine that
+ * handed all of the GPU's memory to its own pool at start-up, a plugin whose
+ * host application forbids allocation after initialisation, or a
+ * latency-critical path that cannot pay for cudaMalloc's implicit device
+ * synchronisation.  The pages have no counterpart of this entry point; it
+ * exists for those callers only.
+ *   Arguments, results and numerics are those of q8_0_gemm (same kernels).
+ *   The scratch q8_0_gemm takes from `workspace` comes instead from a 32 MiB
+ *   array that is part of this library's device code
+ *   (q8_0_gemm_noalloc_max_bytes()).  Every GPU that loads the library's GEMM
+ *   code holds those 32 MiB until the process exits.  A request whose
+ *   q8_0_gemm_workspace_bytes(t, k) exceeds it returns Q8_ERR_TOO_BIG (for
+ *   example t = 3325 fits k = 3584 but not k = 18944).
+ *   The entry point itself calls no cudaMalloc/cudaFree or allocating
+ *   routine.  Its first call on a device looks up that device's address of
+ *   the array (cudaGetSymbolAddress, with the device current); make that
+ *   first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents;
+ *   nothing in it needs to start at zero (each call rewrites every byte it
+ *   reads), but calls that overlap on the GPU -- different streams, or
+ *   different host threads -- race on it and give undefined results.
+ */
+Q8_API int q8_0_gemm_noalloc(const void *w, int64_t n, int64_t k,
+                             const int8_t *qs, const uint32_t *ds, int64_t t, int64_t rows_pad,
+                             float *y, void *stream);
+
+/* Size in bytes of the fixed scratch behind q8_0_gemm_noalloc. */
+Q8_API size_t q8_0_gemm_noalloc_max_bytes(void);
 
 /*
  * q8_0_gemm_mma -- the same contraction as q8_0_gemm on the warp-level int8

@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     load,
     q8_0_gemm,
     q8_0_gemm_mma,
+    q8_0_gemm_noalloc,
     q8_0_gemm_workspace_bytes,
     q8_0_gemv,
     q8_0_gemv_grouped,

@@ -18,7 +18,7 @@ _lock = threading.Lock()
 _lib = None
 
 STATUS_NAMES = {0: "Q8_OK", 1: "Q8_ERR_ARG", 2: "Q8_ERR_ALIGN", 3: "Q8_ERR_DEVICE", 4: "Q8_ERR_LAUNCH",
-                5: "Q8_ERR_DEVICE_TIMEOUT", 6: "Q8_ERR_CUDA"}
+                5: "Q8_ERR_DEVICE_TIMEOUT", 6: "Q8_ERR_CUDA", 7: "Q8_ERR_TOO_BIG"}
 
 # (name, restype, argtypes) of every symbol include/q8proj.h declares.
 _P = ctypes.c_void_p
@@ -34,6 +34,8 @@ SIGNATURES = {
     "q8_0_gemm_workspace_bytes": (ctypes.c_size_t, [_I64, _I64]),
     "q8_0_gemm": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, ctypes.c_size_t, _P]),
     "q8_0_gemm_mma": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
+    "q8_0_gemm_noalloc": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
+    "q8_0_gemm_noalloc_max_bytes": (ctypes.c_size_t, []),
     "q8_0_gemv_grouped": (_INT, [_P, _INT, _I64, _P, _P, _P]),
     "q8_check": (_INT, [_P]),
     "q8_num_sms": (_INT, []),
@@ -259,6 +261,22 @@ def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, workspace=None, stream=None,
         return b
     _check("q8_0_gemm", lib().q8_0_gemm(*args))
     return None
+
+
+def q8_0_gemm_noalloc(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=False):
+    """q8_0_gemm whose scratch is the library's fixed device array (no allocation anywhere).
+
+    For callers that cannot allocate device memory here; requests larger than
+    q8_0_gemm_noalloc_max_bytes() raise Q8Error(Q8_ERR_TOO_BIG).  Calls that overlap
+    on the GPU share that array and race."""
+    import torch
+
+    _need(w, torch.uint8, "w"), _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds"), _need(y, torch.float32, "y")
+    rows_pad = qs.shape[0]
+    if w.numel() != n * (k // 32) * 34 or y.numel() < t * n or qs.shape[-1] != k or ds.shape[0] != rows_pad:
+        raise ValueError("shape mismatch")
+    return _launch("q8_0_gemm_noalloc", (_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y), _stream(stream)),
+                   bind)
 
 
 def q8_0_gemm_mma(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=False):

@@ -68,8 +68,6 @@ int launch_status()
     return cudaGetLastError() == cudaSuccess ? Q8_OK : Q8_ERR_LAUNCH;
 }
 
-int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
-                        int64_t tokens, cudaStream_t s);
 int gemm_mma_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t, float *y,
                     cudaStream_t s);
 
@@ -95,6 +93,7 @@ extern "C" const char *q8_strerror(int status)
     case Q8_ERR_LAUNCH: return "kernel launch failed";
     case Q8_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait ran out";
     case Q8_ERR_CUDA: return "CUDA runtime error";
+    case Q8_ERR_TOO_BIG: return "request exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
     }
 }

@@ -38,6 +38,8 @@
 // flag and the library error word, and all roles drain and exit.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "q8_common.cuh"
 
 namespace {
@@ -581,3 +583,64 @@ int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const 
 }
 
 } // namespace q8
+
+// ---------------------------------------------------------------------------
+// q8_0_gemm_noalloc: the same GEMM with its scratch in a fixed device array.
+//
+// Some callers cannot allocate device memory on the way to this call: a
+// serving engine that reserved all of the GPU's memory for its own pool at
+// start-up, a plugin whose host forbids allocation once it is initialised,
+// or a latency-critical path that cannot afford cudaMalloc's implicit
+// synchronisation.  For them the prepared activation lives in the array
+// below.  It is part of the library's device image, so every GPU on which
+// this library's GEMM module is loaded keeps these bytes until the process
+// exits, whether or not this entry point is ever called.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;  // 32 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64];  // device address of g_noalloc_scratch, per device ordinal
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the array's name in host code is only a stand-in for it).
+int noalloc_scratch(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q8_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return Q8_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return Q8_OK;
+}
+
+} // namespace
+
+extern "C" int q8_0_gemm_noalloc(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds,
+                                 int64_t t, int64_t rows_pad, float *y, void *stream)
+{
+    if (!w || !qs || !ds || !y || n < 1 || t < 1 || k <= 0 || (k % 32) != 0 || rows_pad < t) return Q8_ERR_ARG;
+    const size_t need = q8_0_gemm_workspace_bytes(t, k);
+    if (need > kNoAllocScratchBytes) return Q8_ERR_TOO_BIG;
+    if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((k / 32) % 8 != 0) {  // this shape needs no scratch
+        if (t > 65535) return Q8_ERR_ARG;
+        return q8::gemv_generic_launch(w, n, k, qs, ds, y, t, s);
+    }
+    if (t > int64_t(65535) * 128 || n > (int64_t(1) << 31) - 128) return Q8_ERR_ARG;
+    void *scratch = nullptr;
+    const int st = noalloc_scratch(&scratch);
+    if (st != Q8_OK) return st;
+    return q8::gemm_tc_launch(w, n, k, qs, ds, t, y, scratch, s);
+}
+
+extern "C" size_t q8_0_gemm_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
+

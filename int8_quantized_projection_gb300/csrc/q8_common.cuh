@@ -56,6 +56,8 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
 // Per-translation-unit device error words are read and cleared through these
 // (each .cu file that has bounded waits defines one).
 int gemv_take_error(cudaStream_t s);
+int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                        int64_t tokens, cudaStream_t s);
 int gemm_take_error(cudaStream_t s);
 
 // ---------------------------------------------------------------------------
