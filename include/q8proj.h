@@ -154,7 +154,7 @@ Q8_API int q8_0_gemv_grouped(const q8_gemv_proj *projs, int count, int64_t k,
 
 /*
  * q8_0_gemm_workspace_bytes -- device workspace q8_0_gemm needs for t tokens
- * of width k: t*k*2 bytes (rounded up to 256) + t*(k/32)*16 bytes; 0 when
+ * of width k: t*k*2 bytes (the activation's codes as f16); 0 when
  * (k/32) % 8 != 0 (that shape needs none).
  */
 Q8_API size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k);
@@ -171,8 +171,8 @@ Q8_API size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k);
  *            stream.  May be NULL when that size is 0.
  * n >= 1, t >= 1, k % 32 == 0.  Every 32-wide k block is one q8_0 block on
  * both sides, so its integer dot product is scaled by d_w * d_a once.  The
- * call enqueues a pre-pass that writes the plane's codes as f16 (exact) and
- * its scales into the workspace, then the tcgen05 GEMM (both with
+ * call enqueues a pre-pass that writes the plane's codes as f16 (exact) into
+ * the workspace, then the tcgen05 GEMM (both with
  * programmatic dependent launch; the same precondition on w as q8_0_gemv).
  * "12 - r5-r6 re-ranking + structural rewrite spec", sec. 2 and 3.1;
  * "54 - r51 - producer-fused A-quantize mode 1", sec. 2.1.

@@ -15,25 +15,26 @@
 // A-quantize mode 1" (sec. 2.1).
 //
 // Before the GEMM proper, a small pre-pass (gemm_prep_kernel) writes the
-// plane once per call into the caller's workspace as f16 tokens x k plus one
-// f16 d_a column per block ("prepared operand"), so the GEMM loads it with
-// TMA directly in the layout the tensor core reads -- every weight tile reuses
-// it, instead of converting the same activation in every CTA.
+// plane's codes once per call into the caller's workspace as f16 tokens x k
+// ("prepared operand"), so the GEMM loads them with TMA directly in the layout
+// the tensor core reads -- every weight tile reuses it, instead of converting
+// the same activation in every CTA.
 //
-// One CTA computes a 128 (weight rows) x 128 (tokens) tile over all of k.
-// Per 32-wide block, three MMAs: two K=16 steps for the exact integer partial
-// P, and one K=16 MMA whose operands hold only d_w (weights side, column 0)
-// and d_a (token side, column 0) -- the other core matrices point at a zero
-// tile -- producing S = d_w (x) d_a exactly in TMEM.  The epilogue is then a
-// single acc += S * P per output (packed f32x2 fma), with no shared-memory
-// traffic.
-// Warp roles (512 threads):
+// One CTA computes a 128 (weight rows) x 256 (tokens) tile over all of k.
+// Per 32-wide block two K=16 MMAs produce the exact integer partial P in one
+// of two 256-column TMEM buffers; the epilogue adds (d_w * d_a) * P to f32
+// register accumulators.  Every block needs a round trip between the tensor
+// core and the epilogue (MMA completion -> epilogue -> buffer free); 256-token
+// tiles make each round trip cover twice the tensor work of 128-token tiles.
+// Warp roles (512 threads; setmaxnreg moves registers to the epilogue):
 //   warp 0      TMA producer for raw Q8_0 weight rows (8 blocks per stage)
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warp 2      TMA producer for the prepared activation (4 blocks per stage)
+//   warp 2      TMA producer for the prepared activation (2 blocks per stage)
 //   warps 4-7   converters: one weight row each, raw int8 -> f16 canonical
-//               K-major tile and the row's d_w as an f16 operand column
-//   warps 8-15  epilogue: two warps per TMEM lane quarter, 64 tokens each
+//               K-major tile; the block's d_w (row) and d_a (256 tokens, read
+//               from the plane) as f32 into a scale ring
+//   warps 8-15  epilogue: two warps per TMEM lane quarter, 128 tokens each,
+//               packed f32x2 multiply/fma, 128 accumulators per thread
 // Every mbarrier wait is bounded; a wait that runs out sets the CTA abort
 // flag and the library error word, and all roles drain and exit.
 #include <cuda.h>
@@ -46,34 +47,30 @@ namespace {
 
 __device__ unsigned int g_gemm_err;
 
-constexpr int BM = 128, BN = 128;
+constexpr int BM = 128, BN = 256;
 constexpr int kABlocksPerStage = 8;                // raw weight stage: 8 blocks = 272 bytes per row
-constexpr int kBBlocksPerStage = 4;                // prepared activation stage: 4 blocks = 128 f16 per token
-constexpr int kAStages = 2, kBStages = 2, kF16Slots = 4, kAcc = 2;
-constexpr int kTmemCols = 512;                     // kAcc x (partial BN + scale BN)
+constexpr int kBBlocksPerStage = 2;                // prepared activation stage: 2 blocks = 64 f16 per token
+constexpr int kAStages = 2, kBStages = 3, kF16Slots = 4, kScSlots = 4, kAcc = 2;
+constexpr int kTmemCols = kAcc * BN;               // 512
 constexpr int kConvThreads = 128;                  // warps 4-7
 constexpr int kEpiThreads = 256;                   // warps 8-15
 constexpr int kThreads = 512;
+// registers per thread after setmaxnreg (launch: 128 x 512 threads):
+// 128*48 + 128*96 + 256*184 = 65536
+constexpr int kRegsCtl = 48, kRegsConv = 96, kRegsEpi = 184;
 
 constexpr int kARawBytes = BM * 272;               // 34816
-constexpr int kB16Box = BN * 128;                  // 16384: 128 tokens x 64 f16 (one 128B-swizzle atom column)
-constexpr int kB16Bytes = 2 * kB16Box;             // 32768 per stage
-constexpr int kBsBlock = BN * 16;                  // 2048: 128 tokens x (d_a, 7 zeros) f16
-constexpr int kBsBytes = kBBlocksPerStage * kBsBlock;  // 8192 per stage
-constexpr int kBStageTx = kB16Bytes + kBsBytes;    // 40960
+constexpr int kBStageBytes = BN * 128;             // 32768: 256 tokens x 64 f16, 128B swizzle
 constexpr int kA16Tile = BM * 64;                  // 8192: 128 rows x 32 f16, no swizzle
-constexpr int kAsTile = BM * 16;                   // 2048: 128 rows x (d_w, 7 zeros) f16
-constexpr int kZeroBytes = 2048;                   // the zero core matrices of both scale operands
+constexpr int kScBytes = (BM + BN) * 4;            // 1536: d_w[128], d_a[256] as f32
 
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int OFF_B16 = 0;                                      // 2 x 32768 (1024-aligned boxes)
-constexpr int OFF_BS = OFF_B16 + kBStages * kB16Bytes;          // 65536
-constexpr int OFF_ARAW = OFF_BS + kBStages * kBsBytes;          // 81920
-constexpr int OFF_A16 = OFF_ARAW + kAStages * kARawBytes;       // 151552
-constexpr int OFF_AS = OFF_A16 + kF16Slots * kA16Tile;          // 184320
-constexpr int OFF_ZERO = OFF_AS + kF16Slots * kAsTile;          // 192512
-constexpr int OFF_BAR = OFF_ZERO + kZeroBytes;                  // 194560
-constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kF16Slots + 2 * kAcc + 1;  // 21 (last: MMA drain)
+constexpr int OFF_B = 0;                                        // 3 x 32768 (1024-aligned)
+constexpr int OFF_ARAW = OFF_B + kBStages * kBStageBytes;       // 98304
+constexpr int OFF_A16 = OFF_ARAW + kAStages * kARawBytes;       // 167936
+constexpr int OFF_SC = OFF_A16 + kF16Slots * kA16Tile;          // 200704
+constexpr int OFF_BAR = OFF_SC + kScSlots * kScBytes;           // 206848
+constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kF16Slots + 2 * kScSlots + 2 * kAcc + 1;  // 31
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8 + 8;
 constexpr int kSmemBytes = OFF_MISC + 16 + 1024;                // + alignment slack
 
@@ -108,19 +105,22 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 16 consecutive TMEM columns of this warp's 32 lanes -> 16 registers per
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per
 // thread, without waiting (pair with tc_wait_ld).
-__device__ __forceinline__ void tc_ld16_nowait(uint32_t taddr, uint32_t (&r)[16])
+__device__ __forceinline__ void tc_ld32_nowait(uint32_t taddr, uint32_t (&r)[32])
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
 }
-
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor, K-major.  No swizzle: core matrices of
 // 8 rows x 16 bytes, LBO = byte step between core matrices along k, SBO =
@@ -203,10 +203,10 @@ __device__ __forceinline__ void arrive(uint32_t bar)
 
 // Converter step for weight row r, raw block BETA of the stage: read the 48
 // bytes (three 16-byte aligned, bank-conflict-free loads) that contain the
-// row's 34-byte block, write the 32 codes as f16 into the A tile and d_w into
-// the row's slot of the scale-operand column.
+// row's 34-byte block, write the 32 codes as f16 into the A tile and d_w as
+// f32 into the scale ring.
 template <int BETA>
-__device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16, uint8_t *as, int r)
+__device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16, float *sw, int r)
 {
     constexpr int off = 34 * BETA;
     constexpr int c0 = off >> 4;        // first 16-byte chunk
@@ -221,8 +221,7 @@ __device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16,
         w[4 * c + 3] = v.w;
     }
     const uint32_t dbits = (o & 2) ? (w[o >> 2] >> 16) : (w[o >> 2] & 0xffffu);
-    // d_w operand column: row r of an 8-wide core-matrix column, k = 0 holds d_w
-    *reinterpret_cast<uint4 *>(as + (r >> 3) * 128 + (r & 7) * 16) = make_uint4(dbits, 0u, 0u, 0u);
+    sw[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
     uint32_t qw[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -240,40 +239,82 @@ __device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16,
 
 struct Bars {
     uint32_t b0;
-    __device__ uint32_t a_full(int s) const { return b0 + 8u * s; }
-    __device__ uint32_t a_empty(int s) const { return b0 + 8u * (kAStages + s); }
-    __device__ uint32_t b_full(int s) const { return b0 + 8u * (2 * kAStages + s); }
-    __device__ uint32_t b_empty(int s) const { return b0 + 8u * (2 * kAStages + kBStages + s); }
-    __device__ uint32_t f_full(int s) const { return b0 + 8u * (2 * kAStages + 2 * kBStages + s); }
-    __device__ uint32_t f_empty(int s) const { return b0 + 8u * (2 * kAStages + 2 * kBStages + kF16Slots + s); }
-    __device__ uint32_t acc_full(int s) const { return b0 + 8u * (2 * kAStages + 2 * kBStages + 2 * kF16Slots + s); }
+    __device__ uint32_t at(int i) const { return b0 + 8u * i; }
+    __device__ uint32_t a_full(int s) const { return at(s); }
+    __device__ uint32_t a_empty(int s) const { return at(kAStages + s); }
+    __device__ uint32_t b_full(int s) const { return at(2 * kAStages + s); }
+    __device__ uint32_t b_empty(int s) const { return at(2 * kAStages + kBStages + s); }
+    __device__ uint32_t f_full(int s) const { return at(2 * kAStages + 2 * kBStages + s); }
+    __device__ uint32_t f_empty(int s) const { return at(2 * kAStages + 2 * kBStages + kF16Slots + s); }
+    __device__ uint32_t sc_full(int s) const { return at(2 * kAStages + 2 * kBStages + 2 * kF16Slots + s); }
+    __device__ uint32_t sc_empty(int s) const
+    {
+        return at(2 * kAStages + 2 * kBStages + 2 * kF16Slots + kScSlots + s);
+    }
+    __device__ uint32_t acc_full(int s) const { return at(2 * kAStages + 2 * kBStages + 2 * kF16Slots + 2 * kScSlots + s); }
     __device__ uint32_t acc_empty(int s) const
     {
-        return b0 + 8u * (2 * kAStages + 2 * kBStages + 2 * kF16Slots + kAcc + s);
+        return at(2 * kAStages + 2 * kBStages + 2 * kF16Slots + 2 * kScSlots + kAcc + s);
     }
-    __device__ uint32_t drain() const { return b0 + 8u * (kNumBars - 1); }
+    __device__ uint32_t drain() const { return at(kNumBars - 1); }
 };
+
+// The d_a words of the 8 blocks of a raw weight stage for two tokens (32
+// contiguous bytes of the plane's ds row each); 0 for tokens past t.
+struct StageDa {
+    uint32_t w[2][8];
+};
+
+__device__ __forceinline__ StageDa load_stage_da(const uint32_t *__restrict__ ds, int64_t nb, int64_t t, int64_t tok0,
+                                                 int s)
+{
+    StageDa d;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int64_t tok = tok0 + 128 * h;
+        if (tok < t) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(ds + tok * nb + 8 * s);
+            const uint4 a = __ldg(p), b = __ldg(p + 1);
+            d.w[h][0] = a.x; d.w[h][1] = a.y; d.w[h][2] = a.z; d.w[h][3] = a.w;
+            d.w[h][4] = b.x; d.w[h][5] = b.y; d.w[h][6] = b.z; d.w[h][7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d.w[h][i] = 0u;
+        }
+    }
+    return d;
+}
 
 // One 32-wide block of a raw weight stage for the converter role.
 template <int BETA>
-__device__ __forceinline__ bool convert_block(const Bars &B, uint8_t *sm, int s, int r, volatile int *abort_flag)
+__device__ __forceinline__ bool convert_block(const Bars &B, uint8_t *sm, int s, int r, const StageDa &da,
+                                              volatile int *abort_flag)
 {
     const int slot = s % kAStages;
     const int j = s * kABlocksPerStage + BETA;
-    constexpr int fs = BETA % kF16Slots;
-    if (BETA == 0 && !wait_bar(B.a_full(slot), static_cast<uint32_t>(s / kAStages) & 1u, abort_flag)) return false;
+    constexpr int fs = BETA % kF16Slots, ss = BETA % kScSlots;
     if (!wait_bar(B.f_empty(fs), (static_cast<uint32_t>(j / kF16Slots) & 1u) ^ 1u, abort_flag)) return false;
-    convert_a_row<BETA>(sm + OFF_ARAW + slot * kARawBytes + r * 272, sm + OFF_A16 + fs * kA16Tile,
-                        sm + OFF_AS + fs * kAsTile, r);
+    if (!wait_bar(B.sc_empty(ss), (static_cast<uint32_t>(j / kScSlots) & 1u) ^ 1u, abort_flag)) return false;
+    float *sw = reinterpret_cast<float *>(sm + OFF_SC + ss * kScBytes);
+    float *sa = sw + BM;
+    convert_a_row<BETA>(sm + OFF_ARAW + slot * kARawBytes + r * 272, sm + OFF_A16 + fs * kA16Tile, sw, r);
+    sa[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(da.w[0][BETA] & 0xffffu)));
+    sa[r + 128] = __half2float(__ushort_as_half(static_cast<unsigned short>(da.w[1][BETA] & 0xffffu)));
     q8::fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
     arrive(B.f_full(fs));
+    arrive(B.sc_full(ss));
     if (BETA == kABlocksPerStage - 1) arrive(B.a_empty(slot));
     return true;
 }
 
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmS, int64_t n, int64_t t, int nb, float *__restrict__ y)
+               const uint32_t *__restrict__ ds, int64_t n, int64_t t, int nb, float *__restrict__ y)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = q8::smem_u32(smem_raw);
@@ -290,31 +331,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_gemm_err) != 0u) ? 1 : 0;
         uint64_t *b = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-        for (int i = 0; i < kAStages; ++i) {
-            q8::mbar_init(b + i, 1);                                   // a_full: TMA bytes
-            q8::mbar_init(b + kAStages + i, kConvThreads);             // a_empty
-        }
-        for (int i = 0; i < kBStages; ++i) {
-            q8::mbar_init(b + 2 * kAStages + i, 1);                    // b_full: TMA bytes
-            q8::mbar_init(b + 2 * kAStages + kBStages + i, 1);         // b_empty: tcgen05.commit
-        }
-        uint64_t *f = b + 2 * kAStages + 2 * kBStages;
-        for (int i = 0; i < kF16Slots; ++i) {
-            q8::mbar_init(f + i, kConvThreads);                        // f_full
-            q8::mbar_init(f + kF16Slots + i, 1);                       // f_empty: tcgen05.commit
-        }
-        uint64_t *a = f + 2 * kF16Slots;
-        for (int i = 0; i < kAcc; ++i) {
-            q8::mbar_init(a + i, 1);                                   // acc_full: tcgen05.commit
-            q8::mbar_init(a + kAcc + i, kEpiThreads);                  // acc_empty
-        }
-        q8::mbar_init(b + kNumBars - 1, 1);                            // MMA drain
+        int i = 0;
+        for (int k = 0; k < kAStages; ++k) q8::mbar_init(b + i++, 1);              // a_full: TMA bytes
+        for (int k = 0; k < kAStages; ++k) q8::mbar_init(b + i++, kConvThreads);   // a_empty
+        for (int k = 0; k < kBStages; ++k) q8::mbar_init(b + i++, 1);              // b_full: TMA bytes
+        for (int k = 0; k < kBStages; ++k) q8::mbar_init(b + i++, 1);              // b_empty: tcgen05.commit
+        for (int k = 0; k < kF16Slots; ++k) q8::mbar_init(b + i++, kConvThreads);  // f_full
+        for (int k = 0; k < kF16Slots; ++k) q8::mbar_init(b + i++, 1);             // f_empty: tcgen05.commit
+        for (int k = 0; k < kScSlots; ++k) q8::mbar_init(b + i++, kConvThreads);   // sc_full
+        for (int k = 0; k < kScSlots; ++k) q8::mbar_init(b + i++, kEpiThreads);    // sc_empty
+        for (int k = 0; k < kAcc; ++k) q8::mbar_init(b + i++, 1);                  // acc_full: tcgen05.commit
+        for (int k = 0; k < kAcc; ++k) q8::mbar_init(b + i++, kEpiThreads);        // acc_empty
+        q8::mbar_init(b + i++, 1);                                                 // MMA drain
         q8::fence_mbar_init();
     }
-    // the zero core matrices of the two scale operands
-    for (int i = threadIdx.x; i < kZeroBytes / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(sm + OFF_ZERO)[i] = make_uint4(0u, 0u, 0u, 0u);
-    q8::fence_proxy_async_smem();
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          q8::smem_u32(tmem_slot)),
@@ -328,130 +358,138 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
 
     q8::griddep_launch_dependents();
-    if (warp == 0 || warp == 2) {
-        // ------------------------------------------------------------ TMA producers
-        if (lane == 0) {
-            // Inputs may come from the previous kernel on the stream; every other
-            // role only touches data these threads bring in, and Y is written
-            // after the last MMA, so these are the only waits needed.
-            q8::griddep_wait();
-            const bool is_a = warp == 0;
-            const int nstages = is_a ? nb / kABlocksPerStage : nb / kBBlocksPerStage;
-            const int nbuf = is_a ? kAStages : kBStages;
-            int issued = 0;
-            for (int s = 0; s < nstages && !*abort_flag; ++s) {
-                const int slot = s % nbuf;
-                const uint32_t use = static_cast<uint32_t>(s / nbuf);
-                if (is_a) {
-                    if (!wait_bar(B.a_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
-                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.a_full(slot)),
-                                 "r"(kARawBytes)
-                                 : "memory");
-                    tma_load_2d(base + OFF_ARAW + slot * kARawBytes, &tmA, s * 136, static_cast<int>(n0),
-                                B.a_full(slot));
-                } else {
-                    if (!wait_bar(B.b_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
-                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.b_full(slot)),
-                                 "r"(kBStageTx)
-                                 : "memory");
-                    const uint32_t dst = base + OFF_B16 + slot * kB16Bytes;
-                    tma_load_2d(dst, &tmB, s * 128, static_cast<int>(t0), B.b_full(slot));
-                    tma_load_2d(dst + kB16Box, &tmB, s * 128 + 64, static_cast<int>(t0), B.b_full(slot));
-#pragma unroll
-                    for (int j = 0; j < kBBlocksPerStage; ++j)
-                        tma_load_2d(base + OFF_BS + slot * kBsBytes + j * kBsBlock, &tmS,
-                                    (s * kBBlocksPerStage + j) * 8, static_cast<int>(t0), B.b_full(slot));
+    if (warp < 4) {
+        setmaxnreg_dec<kRegsCtl>();
+        if (warp == 0 || warp == 2) {
+            // -------------------------------------------------------- TMA producers
+            if (lane == 0) {
+                // Inputs may come from the previous kernel on the stream; the
+                // converters also wait before reading the plane's scales, and Y
+                // is written after the last MMA.
+                q8::griddep_wait();
+                const bool is_a = warp == 0;
+                const int nstages = is_a ? nb / kABlocksPerStage : nb / kBBlocksPerStage;
+                const int nbuf = is_a ? kAStages : kBStages;
+                int issued = 0;
+                for (int s = 0; s < nstages && !*abort_flag; ++s) {
+                    const int slot = s % nbuf;
+                    const uint32_t use = static_cast<uint32_t>(s / nbuf);
+                    if (is_a) {
+                        if (!wait_bar(B.a_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.a_full(slot)),
+                                     "r"(kARawBytes)
+                                     : "memory");
+                        tma_load_2d(base + OFF_ARAW + slot * kARawBytes, &tmA, s * 136, static_cast<int>(n0),
+                                    B.a_full(slot));
+                    } else {
+                        if (!wait_bar(B.b_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.b_full(slot)),
+                                     "r"(kBStageBytes)
+                                     : "memory");
+                        tma_load_2d(base + OFF_B + slot * kBStageBytes, &tmB, s * 32 * kBBlocksPerStage,
+                                    static_cast<int>(t0), B.b_full(slot));
+                    }
+                    issued = s + 1;
                 }
-                issued = s + 1;
+                // drain: the last stages issued must have landed before the CTA exits
+                for (int s = issued - nbuf < 0 ? 0 : issued - nbuf; s < issued; ++s)
+                    drain_bar(is_a ? B.a_full(s % nbuf) : B.b_full(s % nbuf), static_cast<uint32_t>(s / nbuf) & 1u);
             }
-            // drain: the last stages issued must have landed before the CTA exits
-            for (int s = issued - nbuf < 0 ? 0 : issued - nbuf; s < issued; ++s)
-                drain_bar(is_a ? B.a_full(s % nbuf) : B.b_full(s % nbuf), static_cast<uint32_t>(s / nbuf) & 1u);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            for (int j = 0; j < nb; ++j) {
-                const int fs = j % kF16Slots, ab = j % kAcc;
-                const int sb = (j / kBBlocksPerStage) % kBStages, bq = j % kBBlocksPerStage;
-                if (!wait_bar(B.f_full(fs), static_cast<uint32_t>(j / kF16Slots) & 1u, abort_flag)) break;
-                if (bq == 0 &&
-                    !wait_bar(B.b_full(sb), static_cast<uint32_t>(j / (kBBlocksPerStage * kBStages)) & 1u, abort_flag))
-                    break;
-                if (!wait_bar(B.acc_empty(ab), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t dP = tmem + static_cast<uint32_t>(ab * 2 * BN);
-                const uint32_t dS = dP + BN;
-                const uint32_t a_addr = base + OFF_A16 + fs * kA16Tile;
-                const uint32_t b_addr = base + OFF_B16 + sb * kB16Bytes + (bq >> 1) * kB16Box + 64 * (bq & 1);
+        } else if (warp == 1) {
+            // -------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                for (int j = 0; j < nb; ++j) {
+                    const int fs = j % kF16Slots, ab = j % kAcc;
+                    const int sb = (j / kBBlocksPerStage) % kBStages, bq = j % kBBlocksPerStage;
+                    if (!wait_bar(B.f_full(fs), static_cast<uint32_t>(j / kF16Slots) & 1u, abort_flag)) break;
+                    if (bq == 0 && !wait_bar(B.b_full(sb),
+                                             static_cast<uint32_t>(j / (kBBlocksPerStage * kBStages)) & 1u, abort_flag))
+                        break;
+                    if (!wait_bar(B.acc_empty(ab), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem + static_cast<uint32_t>(ab * BN);
+                    const uint32_t a_addr = base + OFF_A16 + fs * kA16Tile;
+                    const uint32_t b_addr = base + OFF_B + sb * kBStageBytes + 64 * bq;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk)  // two K=16 steps = one 32-wide block
-                    tc_mma_f16(dP, smem_desc(a_addr + 256 * kk, 128, 512), smem_desc(b_addr + 32 * kk, 16, 1024, true),
-                               kIdesc, kk);
-                const uint32_t as_addr = base + OFF_AS + fs * kAsTile;
-                const uint32_t bs_addr = base + OFF_BS + sb * kBsBytes + bq * kBsBlock;
-                tc_mma_f16(dS, smem_desc(as_addr, base + OFF_ZERO - as_addr, 128),
-                           smem_desc(bs_addr, base + OFF_ZERO - bs_addr, 128), kIdesc, 0);
-                tc_commit(B.f_empty(fs));
-                tc_commit(B.acc_full(ab));
-                if (bq == kBBlocksPerStage - 1) tc_commit(B.b_empty(sb));
+                    for (int kk = 0; kk < 2; ++kk)  // two K=16 steps = one 32-wide block
+                        tc_mma_f16(d, smem_desc(a_addr + 256 * kk, 128, 512),
+                                   smem_desc(b_addr + 32 * kk, 16, 1024, true), kIdesc, kk);
+                    tc_commit(B.f_empty(fs));
+                    tc_commit(B.acc_full(ab));
+                    if (bq == kBBlocksPerStage - 1) tc_commit(B.b_empty(sb));
+                }
+                // drain: every MMA issued must have completed before TMEM is freed
+                tc_commit(B.drain());
+                drain_bar(B.drain(), 0);
             }
-            // drain: every MMA issued must have completed before TMEM is freed
-            tc_commit(B.drain());
-            drain_bar(B.drain(), 0);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp < 8) {
+        setmaxnreg_dec<kRegsConv>();
         // ------------------------------------------------------------ converters
-        const int r = threadIdx.x - 128;  // weight row of the tile, 0..127
+        const int r = threadIdx.x - 128;  // weight row of the tile and token pair (r, r + 128), 0..127
         const int nstages = nb / kABlocksPerStage;
+        q8::griddep_wait();               // the plane's scales may come from the previous kernel
         for (int s = 0; s < nstages && !*abort_flag; ++s) {
-            if (!convert_block<0>(B, sm, s, r, abort_flag)) break;
-            if (!convert_block<1>(B, sm, s, r, abort_flag)) break;
-            if (!convert_block<2>(B, sm, s, r, abort_flag)) break;
-            if (!convert_block<3>(B, sm, s, r, abort_flag)) break;
-            if (!convert_block<4>(B, sm, s, r, abort_flag)) break;
-            if (!convert_block<5>(B, sm, s, r, abort_flag)) break;
-            if (!convert_block<6>(B, sm, s, r, abort_flag)) break;
-            if (!convert_block<7>(B, sm, s, r, abort_flag)) break;
+            const StageDa da = load_stage_da(ds, nb, t, t0 + r, s);
+            if (!wait_bar(B.a_full(s % kAStages), static_cast<uint32_t>(s / kAStages) & 1u, abort_flag)) break;
+            if (!convert_block<0>(B, sm, s, r, da, abort_flag)) break;
+            if (!convert_block<1>(B, sm, s, r, da, abort_flag)) break;
+            if (!convert_block<2>(B, sm, s, r, da, abort_flag)) break;
+            if (!convert_block<3>(B, sm, s, r, da, abort_flag)) break;
+            if (!convert_block<4>(B, sm, s, r, da, abort_flag)) break;
+            if (!convert_block<5>(B, sm, s, r, da, abort_flag)) break;
+            if (!convert_block<6>(B, sm, s, r, da, abort_flag)) break;
+            if (!convert_block<7>(B, sm, s, r, da, abort_flag)) break;
         }
-    } else if (warp >= 8) {
+    } else {
+        setmaxnreg_inc<kRegsEpi>();
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;            // TMEM lane quarter of this warp
-        const int hcol = (warp - 8) >> 2;  // column half: tokens [64*hcol, 64*hcol + 64)
+        const int hcol = (warp - 8) >> 2;  // token half: [128*hcol, 128*hcol + 128)
         const int r = 32 * q + lane;       // tile row = TMEM lane
-        float2 acc[32];
+        float2 acc[64];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
-            const int ab = j % kAcc;
+            const int ab = j % kAcc, ss = j % kScSlots;
             if (!wait_bar(B.acc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
+            if (!wait_bar(B.sc_full(ss), static_cast<uint32_t>(j / kScSlots) & 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
+            const float *sw = reinterpret_cast<const float *>(sm + OFF_SC + ss * kScBytes);
+            const float *sa = sw + BM + 128 * hcol;
+            const float dw = sw[r];
+            const float2 dw2 = make_float2(dw, dw);
             const uint32_t taddr =
-                tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * 2 * BN + 64 * hcol);
+                tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BN + 128 * hcol);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t p[16], sv[16];
-                tc_ld16_nowait(taddr + 16 * c, p);
-                tc_ld16_nowait(taddr + BN + 16 * c, sv);
+                uint32_t p[32];
+                tc_ld32_nowait(taddr + 32 * c, p);
                 tc_wait_ld();
                 if (c == 3) {
                     tc_fence_before();
                     arrive(B.acc_empty(ab));  // TMEM buffer free for the next block's MMAs
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc[8 * c + i] = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
-                                                make_float2(__uint_as_float(p[2 * i]), __uint_as_float(p[2 * i + 1])),
-                                                acc[8 * c + i]);
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(sa + 32 * c + i);
+                    const float2 s01 = __fmul2_rn(dw2, make_float2(a4.x, a4.y));
+                    const float2 s23 = __fmul2_rn(dw2, make_float2(a4.z, a4.w));
+                    acc[16 * c + i / 2] = __ffma2_rn(s01, make_float2(__uint_as_float(p[i]), __uint_as_float(p[i + 1])),
+                                                     acc[16 * c + i / 2]);
+                    acc[16 * c + i / 2 + 1] = __ffma2_rn(
+                        s23, make_float2(__uint_as_float(p[i + 2]), __uint_as_float(p[i + 3])), acc[16 * c + i / 2 + 1]);
+                }
             }
+            arrive(B.sc_empty(ss));
         }
         if (ok && !*abort_flag) {
             const int64_t row = n0 + r;
             if (row < n) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int64_t tok = t0 + 64 * hcol + 2 * i;
+                for (int i = 0; i < 64; ++i) {
+                    const int64_t tok = t0 + 128 * hcol + 2 * i;
                     if (tok < t) y[tok * n + row] = acc[i].x;
                     if (tok + 1 < t) y[(tok + 1) * n + row] = acc[i].y;
                 }
@@ -467,19 +505,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
 }
 
-// Pre-pass: plane (qs, ds) rows [0, t) -> prepared operand in the workspace:
-// b16[t][k] = f16(q) (exact) and bs[t][k/32][8] = (f16 d_a, 0 x 7).
+// Pre-pass: plane codes (qs) rows [0, t) -> prepared operand b16[t][k] = f16(q), exact.
 __global__ void __launch_bounds__(256)
-gemm_prep_kernel(const uint4 *__restrict__ qs, const uint32_t *__restrict__ ds, int64_t t, int64_t k,
-                 uint4 *__restrict__ b16, uint4 *__restrict__ bs)
+gemm_prep_kernel(const uint4 *__restrict__ qs, int64_t t, int64_t k, uint4 *__restrict__ b16)
 {
     q8::griddep_launch_dependents();
     q8::griddep_wait();  // the plane may come from the previous kernel
-    const int64_t c16 = k / 16;  // 16-code chunks per token
-    const int64_t total = t * c16;
+    const int64_t total = t * (k / 16);  // 16-code chunks; qs row stride k: flat index
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const uint4 v = __ldg(qs + i);  // qs row stride k == c16 chunks: flat index
+        const uint4 v = __ldg(qs + i);
         uint4 o0, o1;
         i8x4_to_f16x4(v.x, o0.x, o0.y);
         i8x4_to_f16x4(v.y, o0.z, o0.w);
@@ -487,10 +522,6 @@ gemm_prep_kernel(const uint4 *__restrict__ qs, const uint32_t *__restrict__ ds, 
         i8x4_to_f16x4(v.w, o1.z, o1.w);
         b16[2 * i] = o0;
         b16[2 * i + 1] = o1;
-        if ((i & 1) == 0) {  // first chunk of a 32-wide block: its d_a column entry
-            const int64_t blk = i >> 1;  // == tok * (k/32) + block
-            bs[blk] = make_uint4(__ldg(ds + blk) & 0xffffu, 0u, 0u, 0u);
-        }
     }
 }
 
@@ -547,8 +578,7 @@ int gemm_take_error(cudaStream_t s)
 
 size_t gemm_workspace_bytes(int64_t t, int64_t k)
 {
-    const size_t b16 = static_cast<size_t>(t) * static_cast<size_t>(k) * 2;
-    return (b16 + 255) / 256 * 256 + static_cast<size_t>(t) * static_cast<size_t>(k / 32) * 16;
+    return static_cast<size_t>(t) * static_cast<size_t>(k) * 2;  // the prepared f16 codes
 }
 
 // Requires k/32 % 8 == 0, 16-byte aligned pointers and a workspace of at least
@@ -559,14 +589,11 @@ int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const 
     const int64_t nb = k / 32;
     const int64_t pitch = nb * 34;
     uint8_t *b16 = static_cast<uint8_t *>(workspace);
-    uint8_t *bs = b16 + (static_cast<size_t>(t) * static_cast<size_t>(k) * 2 + 255) / 256 * 256;
-    CUtensorMap ma, mb, ms;
+    CUtensorMap ma, mb;
     if (!make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w, static_cast<uint64_t>(pitch / 2),
                      static_cast<uint64_t>(n), static_cast<uint64_t>(pitch), 136, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, b16, static_cast<uint64_t>(k), static_cast<uint64_t>(t),
-                     static_cast<uint64_t>(k * 2), 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, bs, static_cast<uint64_t>(nb * 8), static_cast<uint64_t>(t),
-                     static_cast<uint64_t>(nb * 16), 8, BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+                     static_cast<uint64_t>(k * 2), 64, BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return Q8_ERR_LAUNCH;
     const int sms = device_sm_count();
     const int64_t chunks = t * (k / 16);
@@ -574,12 +601,11 @@ int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const 
     const int64_t pcap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
     pgrid = pgrid < pcap ? pgrid : pcap;
     int st = launch_pdl(gemm_prep_kernel, dim3(static_cast<unsigned>(pgrid)), dim3(256), 0, s,
-                        reinterpret_cast<const uint4 *>(qs), ds, t, k, reinterpret_cast<uint4 *>(b16),
-                        reinterpret_cast<uint4 *>(bs));
+                        reinterpret_cast<const uint4 *>(qs), t, k, reinterpret_cast<uint4 *>(b16));
     if (st != Q8_OK) return st;
     if (!set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel), kSmemBytes, 2)) return Q8_ERR_LAUNCH;
     const dim3 grid(static_cast<unsigned>((n + BM - 1) / BM), static_cast<unsigned>((t + BN - 1) / BN));
-    return launch_pdl(gemm_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, ma, mb, ms, n, t, static_cast<int>(nb), y);
+    return launch_pdl(gemm_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, ma, mb, ds, n, t, static_cast<int>(nb), y);
 }
 
 } // namespace q8
