@@ -44,8 +44,10 @@ PREFILL = dict(tokens=3325, d=3584, nf=18944, eps=1e-6)
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
 # kernel from the ncu capture summarised under profiles/ (None until taken,
 # and reset to None whenever that kernel changes).
+# DRAM bytes per launch from one ncu capture of the current kernel; None when
+# the kernel changed after the capture (the figure would describe old code).
 NCU_TRAFFIC_BYTES = {"gemv_staged 12288x7168+96x7168": 97_942_016,     # profiles/gemv_staged_12288x7168_plus_96x7168.md
-                     "gemm_tc 18944x3584 t=3325": 619_668_000}         # profiles/gemm_tc_18944x3584_t3325.md
+                     "gemm_tc 18944x3584 t=3325": None}                # recapture pending for the current gemm_tc
 
 
 # ---------------------------------------------------------------------------

@@ -26,15 +26,20 @@
 // register accumulators.  Every block needs a round trip between the tensor
 // core and the epilogue (MMA completion -> epilogue -> buffer free); 256-token
 // tiles make each round trip cover twice the tensor work of 128-token tiles.
+// The tensor core queues little ahead of the thread issuing to it, so each
+// TMEM buffer has its own issuing thread, and the epilogue is bound by its
+// f32 work (one scale product and one fma per output and block).
 // Warp roles (512 threads; setmaxnreg moves registers to the epilogue):
 //   warp 0      TMA producer for raw Q8_0 weight rows (8 blocks per stage)
-//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warp 1      TMEM allocator; MMA issuer (one thread) for the even blocks
 //   warp 2      TMA producer for the prepared activation (2 blocks per stage)
+//   warp 3      MMA issuer (one thread) for the odd blocks
 //   warps 4-7   converters: one weight row each, raw int8 -> f16 canonical
 //               K-major tile; the block's d_w (row) and d_a (256 tokens, read
 //               from the plane) as f32 into a scale ring
 //   warps 8-15  epilogue: two warps per TMEM lane quarter, 128 tokens each,
-//               packed f32x2 multiply/fma, 128 accumulators per thread
+//               read in the 16x256b shape (4 rows x 32 tokens per thread and
+//               block), packed f32x2 multiply/fma, 128 accumulators per thread
 // Every mbarrier wait is bounded; a wait that runs out sets the CTA abort
 // flag and the library error word, and all roles drain and exit.
 #include <cuda.h>
@@ -52,6 +57,7 @@ constexpr int kABlocksPerStage = 8;                // raw weight stage: 8 blocks
 constexpr int kBBlocksPerStage = 2;                // prepared activation stage: 2 blocks = 64 f16 per token
 constexpr int kAStages = 2, kBStages = 3, kF16Slots = 4, kScSlots = 4, kAcc = 2;
 constexpr int kTmemCols = kAcc * BN;               // 512
+static_assert(kBBlocksPerStage == kAcc, "each activation stage feeds one block of each MMA issuer");
 constexpr int kConvThreads = 128;                  // warps 4-7
 constexpr int kEpiThreads = 256;                   // warps 8-15
 constexpr int kThreads = 512;
@@ -70,7 +76,7 @@ constexpr int OFF_ARAW = OFF_B + kBStages * kBStageBytes;       // 98304
 constexpr int OFF_A16 = OFF_ARAW + kAStages * kARawBytes;       // 167936
 constexpr int OFF_SC = OFF_A16 + kF16Slots * kA16Tile;          // 200704
 constexpr int OFF_BAR = OFF_SC + kScSlots * kScBytes;           // 206848
-constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kF16Slots + 2 * kScSlots + 2 * kAcc + 1;  // 31
+constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kF16Slots + 2 * kScSlots + 2 * kAcc + kAcc;  // 32
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8 + 8;
 constexpr int kSmemBytes = OFF_MISC + 16 + 1024;                // + alignment slack
 
@@ -105,21 +111,30 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per
-// thread, without waiting (pair with tc_wait_ld).
-__device__ __forceinline__ void tc_ld32_nowait(uint32_t taddr, uint32_t (&r)[32])
+// 16 lanes x 32 columns (16x256b shape, 4 repetitions along the columns) ->
+// 16 registers per thread.  Thread i of the warp receives, for repetition
+// rep, lanes (i/4) and (i/4 + 8) of the 16 at columns 8*rep + 2*(i%4) + {0,1}:
+// registers 4*rep + {0,1} (lane i/4), 4*rep + {2,3} (lane i/4 + 8).
+// Asynchronous: the registers are valid only after tc_wait_ld16.
+__device__ __forceinline__ void tc_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16])
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// Wait for this thread's outstanding TMEM loads.  The registers of the load
+// being waited for pass through the statement, so no use of them can be
+// scheduled before it; having no memory clobber, it leaves shared-memory
+// loads free to move across it.
+__device__ __forceinline__ void tc_wait_ld16(uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]));
 }
 
 // Shared-memory matrix descriptor, K-major.  No swizzle: core matrices of
@@ -159,9 +174,9 @@ __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(20000u)  // suspend up to 20 us per try instead of spinning
+        : "r"(bar), "r"(parity)  // no suspend-time hint: a suspended waiter wakes late
         : "memory");
     return ok != 0;
 }
@@ -201,10 +216,24 @@ __device__ __forceinline__ void arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Scale-ring order.  The epilogue reads TMEM in the 16x256b shape, so each
+// of its threads holds four weight rows (32q + 16*sub + g + 8*e) and, per
+// 32-column group cg, eight token columns (32cg + 8*rep + 2m + {0,1}); the
+// converters store d_w and d_a so that those sets are contiguous, which
+// makes the epilogue's scale reads 16-byte, bank-conflict-free loads.
+__device__ __forceinline__ int dw_slot(int r)  // weight row 0..127
+{
+    return (r >> 5) * 32 + (r & 7) * 4 + ((r >> 4) & 1) * 2 + ((r >> 3) & 1);
+}
+__device__ __forceinline__ int da_slot(int c)  // token column 0..255
+{
+    return (c >> 7) * 128 + ((c >> 5) & 3) * 32 + ((c >> 1) & 3) * 8 + ((c >> 3) & 3) * 2 + (c & 1);
+}
+
 // Converter step for weight row r, raw block BETA of the stage: read the 48
 // bytes (three 16-byte aligned, bank-conflict-free loads) that contain the
 // row's 34-byte block, write the 32 codes as f16 into the A tile and d_w as
-// f32 into the scale ring.
+// f32 into the scale ring (at dw_slot(r)).
 template <int BETA>
 __device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16, float *sw, int r)
 {
@@ -221,7 +250,7 @@ __device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16,
         w[4 * c + 3] = v.w;
     }
     const uint32_t dbits = (o & 2) ? (w[o >> 2] >> 16) : (w[o >> 2] & 0xffffu);
-    sw[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
+    sw[dw_slot(r)] = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits)));
     uint32_t qw[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -234,6 +263,25 @@ __device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16,
         i8x4_to_f16x4(qw[2 * kc], v.x, v.y);
         i8x4_to_f16x4(qw[2 * kc + 1], v.z, v.w);
         *reinterpret_cast<uint4 *>(a16 + (r >> 3) * 512 + kc * 128 + (r & 7) * 16) = v;
+    }
+}
+
+// Epilogue step for one 16x256b.x4 load (two rows x eight token columns of
+// this thread): acc += (d_w * d_a) * P in token pairs.  The scale d_w * d_a
+// is rounded once before the fma, the order every block follows.
+__device__ __forceinline__ void epi_math(float2 *acc, const uint32_t (&p)[16], const float (&da)[8], float dw_lo,
+                                         float dw_hi)
+{
+    const float2 w0 = make_float2(dw_lo, dw_lo), w1 = make_float2(dw_hi, dw_hi);
+#pragma unroll
+    for (int rep = 0; rep < 4; ++rep) {
+        const float2 d2 = make_float2(da[2 * rep], da[2 * rep + 1]);
+        const float2 s0 = __fmul2_rn(w0, d2);
+        const float2 s1 = __fmul2_rn(w1, d2);
+        acc[2 * rep] = __ffma2_rn(s0, make_float2(__uint_as_float(p[4 * rep]), __uint_as_float(p[4 * rep + 1])),
+                                  acc[2 * rep]);
+        acc[2 * rep + 1] = __ffma2_rn(
+            s1, make_float2(__uint_as_float(p[4 * rep + 2]), __uint_as_float(p[4 * rep + 3])), acc[2 * rep + 1]);
     }
 }
 
@@ -256,7 +304,7 @@ struct Bars {
     {
         return at(2 * kAStages + 2 * kBStages + 2 * kF16Slots + 2 * kScSlots + kAcc + s);
     }
-    __device__ uint32_t drain() const { return at(kNumBars - 1); }
+    __device__ uint32_t drain(int issuer) const { return at(kNumBars - kAcc + issuer); }
 };
 
 // The d_a words of the 8 blocks of a raw weight stage for two tokens (32
@@ -298,8 +346,8 @@ __device__ __forceinline__ bool convert_block(const Bars &B, uint8_t *sm, int s,
     float *sw = reinterpret_cast<float *>(sm + OFF_SC + ss * kScBytes);
     float *sa = sw + BM;
     convert_a_row<BETA>(sm + OFF_ARAW + slot * kARawBytes + r * 272, sm + OFF_A16 + fs * kA16Tile, sw, r);
-    sa[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(da.w[0][BETA] & 0xffffu)));
-    sa[r + 128] = __half2float(__ushort_as_half(static_cast<unsigned short>(da.w[1][BETA] & 0xffffu)));
+    sa[da_slot(r)] = __half2float(__ushort_as_half(static_cast<unsigned short>(da.w[0][BETA] & 0xffffu)));
+    sa[da_slot(r + 128)] = __half2float(__ushort_as_half(static_cast<unsigned short>(da.w[1][BETA] & 0xffffu)));
     q8::fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
     arrive(B.f_full(fs));
     arrive(B.sc_full(ss));
@@ -335,14 +383,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int k = 0; k < kAStages; ++k) q8::mbar_init(b + i++, 1);              // a_full: TMA bytes
         for (int k = 0; k < kAStages; ++k) q8::mbar_init(b + i++, kConvThreads);   // a_empty
         for (int k = 0; k < kBStages; ++k) q8::mbar_init(b + i++, 1);              // b_full: TMA bytes
-        for (int k = 0; k < kBStages; ++k) q8::mbar_init(b + i++, 1);              // b_empty: tcgen05.commit
+        for (int k = 0; k < kBStages; ++k) q8::mbar_init(b + i++, kAcc);           // b_empty: one commit per issuer
         for (int k = 0; k < kF16Slots; ++k) q8::mbar_init(b + i++, kConvThreads);  // f_full
         for (int k = 0; k < kF16Slots; ++k) q8::mbar_init(b + i++, 1);             // f_empty: tcgen05.commit
         for (int k = 0; k < kScSlots; ++k) q8::mbar_init(b + i++, kConvThreads);   // sc_full
         for (int k = 0; k < kScSlots; ++k) q8::mbar_init(b + i++, kEpiThreads);    // sc_empty
         for (int k = 0; k < kAcc; ++k) q8::mbar_init(b + i++, 1);                  // acc_full: tcgen05.commit
         for (int k = 0; k < kAcc; ++k) q8::mbar_init(b + i++, kEpiThreads);        // acc_empty
-        q8::mbar_init(b + i++, 1);                                                 // MMA drain
+        for (int k = 0; k < kAcc; ++k) q8::mbar_init(b + i++, 1);                  // MMA drain, per issuer
         q8::fence_mbar_init();
     }
     if (warp == 1) {
@@ -395,15 +443,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int s = issued - nbuf < 0 ? 0 : issued - nbuf; s < issued; ++s)
                     drain_bar(is_a ? B.a_full(s % nbuf) : B.b_full(s % nbuf), static_cast<uint32_t>(s / nbuf) & 1u);
             }
-        } else if (warp == 1) {
-            // -------------------------------------------------------- MMA issuer
+        } else {
+            // -------------------------------------------------------- MMA issuers
+            // Warp 1 issues the even blocks (TMEM buffer 0), warp 3 the odd
+            // ones (buffer 1).  The tensor core hardly queues ahead of the
+            // issuing thread, so one issuer's barrier waits and bookkeeping
+            // would stall the pipe between blocks; two issuers hide each
+            // other's.
+            const int who = warp == 1 ? 0 : 1;
             if (lane == 0) {
-                for (int j = 0; j < nb; ++j) {
-                    const int fs = j % kF16Slots, ab = j % kAcc;
+                for (int j = who; j < nb; j += kAcc) {
+                    const int fs = j % kF16Slots, ab = who;
                     const int sb = (j / kBBlocksPerStage) % kBStages, bq = j % kBBlocksPerStage;
                     if (!wait_bar(B.f_full(fs), static_cast<uint32_t>(j / kF16Slots) & 1u, abort_flag)) break;
-                    if (bq == 0 && !wait_bar(B.b_full(sb),
-                                             static_cast<uint32_t>(j / (kBBlocksPerStage * kBStages)) & 1u, abort_flag))
+                    if (!wait_bar(B.b_full(sb), static_cast<uint32_t>(j / (kBBlocksPerStage * kBStages)) & 1u,
+                                  abort_flag))
                         break;
                     if (!wait_bar(B.acc_empty(ab), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) break;
                     tc_fence_after();
@@ -416,11 +470,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                    smem_desc(b_addr + 32 * kk, 16, 1024, true), kIdesc, kk);
                     tc_commit(B.f_empty(fs));
                     tc_commit(B.acc_full(ab));
-                    if (bq == kBBlocksPerStage - 1) tc_commit(B.b_empty(sb));
+                    tc_commit(B.b_empty(sb));  // counts one commit from each issuer per stage
                 }
-                // drain: every MMA issued must have completed before TMEM is freed
-                tc_commit(B.drain());
-                drain_bar(B.drain(), 0);
+                // drain: every MMA this thread issued must have completed before TMEM is freed
+                tc_commit(B.drain(who));
+                drain_bar(B.drain(who), 0);
             }
         }
     } else if (warp < 8) {
@@ -446,7 +500,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;            // TMEM lane quarter of this warp
         const int hcol = (warp - 8) >> 2;  // token half: [128*hcol, 128*hcol + 128)
-        const int r = 32 * q + lane;       // tile row = TMEM lane
+        const int g = lane >> 2, m = lane & 3;
+        // this thread's outputs: rows 32q + 16*sub + g + 8*e, token columns
+        // 128*hcol + 32*cg + 8*rep + 2m + {0,1}; acc index 8*(2cg + sub) + 2*rep + e
         float2 acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
@@ -457,41 +513,56 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!wait_bar(B.sc_full(ss), static_cast<uint32_t>(j / kScSlots) & 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const float *sw = reinterpret_cast<const float *>(sm + OFF_SC + ss * kScBytes);
-            const float *sa = sw + BM + 128 * hcol;
-            const float dw = sw[r];
-            const float2 dw2 = make_float2(dw, dw);
-            const uint32_t taddr =
+            const float4 w4 = *reinterpret_cast<const float4 *>(sw + 32 * q + 4 * g);  // dw_slot order
+            const float *sa = sw + BM + 128 * hcol + 8 * m;                             // da_slot order, + 32*cg
+            const uint32_t tbase =
                 tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BN + 128 * hcol);
+            // chunk c = (cg = c / 2, sub = c % 2): 16 lanes x 32 columns.  Loads
+            // are double-buffered: chunk c + 1 is in flight while chunk c is
+            // scaled and accumulated.  The buffer is released once its last
+            // chunk is in registers.
+            uint32_t p0[16], p1[16];
+            float da[8];
+            tc_ld16x256b_x4(tbase, p0);
+            tc_wait_ld16(p0);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t p[32];
-                tc_ld32_nowait(taddr + 32 * c, p);
-                tc_wait_ld();
-                if (c == 3) {
+            for (int c = 0; c < 8; ++c) {
+                uint32_t(&cur)[16] = (c & 1) ? p1 : p0;
+                uint32_t(&nxt)[16] = (c & 1) ? p0 : p1;
+                if ((c & 1) == 0) {
+                    const float4 a0 = *reinterpret_cast<const float4 *>(sa + 32 * (c >> 1));
+                    const float4 a1 = *reinterpret_cast<const float4 *>(sa + 32 * (c >> 1) + 4);
+                    da[0] = a0.x; da[1] = a0.y; da[2] = a0.z; da[3] = a0.w;
+                    da[4] = a1.x; da[5] = a1.y; da[6] = a1.z; da[7] = a1.w;
+                }
+                if (c < 7) {
+                    const int cn = c + 1;
+                    tc_ld16x256b_x4(tbase + (static_cast<uint32_t>(16 * (cn & 1)) << 16) + 32 * (cn >> 1), nxt);
+                }
+                if (c & 1) epi_math(acc + 8 * c, cur, da, w4.z, w4.w);
+                else epi_math(acc + 8 * c, cur, da, w4.x, w4.y);
+                if (c < 7) tc_wait_ld16(nxt);
+                if (c == 6) {
                     tc_fence_before();
                     arrive(B.acc_empty(ab));  // TMEM buffer free for the next block's MMAs
-                }
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(sa + 32 * c + i);
-                    const float2 s01 = __fmul2_rn(dw2, make_float2(a4.x, a4.y));
-                    const float2 s23 = __fmul2_rn(dw2, make_float2(a4.z, a4.w));
-                    acc[16 * c + i / 2] = __ffma2_rn(s01, make_float2(__uint_as_float(p[i]), __uint_as_float(p[i + 1])),
-                                                     acc[16 * c + i / 2]);
-                    acc[16 * c + i / 2 + 1] = __ffma2_rn(
-                        s23, make_float2(__uint_as_float(p[i + 2]), __uint_as_float(p[i + 3])), acc[16 * c + i / 2 + 1]);
                 }
             }
             arrive(B.sc_empty(ss));
         }
         if (ok && !*abort_flag) {
-            const int64_t row = n0 + r;
-            if (row < n) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const int64_t tok = t0 + 128 * hcol + 2 * i;
-                    if (tok < t) y[tok * n + row] = acc[i].x;
-                    if (tok + 1 < t) y[(tok + 1) * n + row] = acc[i].y;
+            for (int c = 0; c < 8; ++c) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int64_t row = n0 + 32 * q + 16 * (c & 1) + g + 8 * e;
+                    if (row >= n) continue;
+#pragma unroll
+                    for (int rep = 0; rep < 4; ++rep) {
+                        const int64_t tok = t0 + 128 * hcol + 32 * (c >> 1) + 8 * rep + 2 * m;
+                        const float2 v = acc[8 * c + 2 * rep + e];
+                        if (tok < t) y[tok * n + row] = v.x;
+                        if (tok + 1 < t) y[(tok + 1) * n + row] = v.y;
+                    }
                 }
             }
         }
