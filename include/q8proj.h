@@ -153,9 +153,35 @@ Q8_API int q8_0_gemv_grouped(const q8_gemv_proj *projs, int count, int64_t k,
                              const int8_t *qs, const uint32_t *ds, void *stream);
 
 /*
+ * q8_0_gemv_batched -- the projection for a few tokens at once (decode over
+ * a small batch of sequences): Y[t][i] = sum_b d_w(i,b) * d_a(t,b) * isum for
+ * plane rows t < tokens, reading the weights from memory once for all of
+ * them.  The formula is the GEMM's ("12 - r5-r6 re-ranking + structural
+ * rewrite spec", sec. 2); the pages build only its two ends, the batch-1 GEMV
+ * and the prefill GEMM, and this entry point fills the range between them.
+ *   w      : n rows of k/32 Q8_0 blocks (input, 16-byte aligned)
+ *   qs, ds : plane with at least `tokens` rows (input; rows >= tokens are
+ *            not read)
+ *   y      : f32 [tokens][n] row-major (output, overwritten)
+ * 1 <= tokens <= Q8_GEMV_MAX_TOKENS, n >= 1, k % 32 == 0.  When
+ * (k/32) % 8 == 0 the block dot products run on the tensor cores (int8 codes
+ * widened exactly to f16, f32 accumulation of an exact integer) and each
+ * block adds (d_w * d_a) * isum to one of four partial sums over k, which are
+ * added in a fixed order: results are run-to-run identical.  Other k use the
+ * generic kernel (weights read once per token).  Programmatic dependent
+ * launch, with the same precondition on w as q8_0_gemv.
+ * q8_0_gemm hands calls with t <= Q8_GEMV_MAX_TOKENS to this path (t == 1 to
+ * q8_0_gemv).
+ */
+#define Q8_GEMV_MAX_TOKENS 16
+Q8_API int q8_0_gemv_batched(const void *w, int64_t n, int64_t k,
+                             const int8_t *qs, const uint32_t *ds, int64_t tokens,
+                             float *y, void *stream);
+
+/*
  * q8_0_gemm_workspace_bytes -- device workspace q8_0_gemm needs for t tokens
  * of width k: t*k*2 bytes (the activation's codes as f16); 0 when
- * (k/32) % 8 != 0 (that shape needs none).
+ * (k/32) % 8 != 0 or t <= Q8_GEMV_MAX_TOKENS (those calls need none).
  */
 Q8_API size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k);
 

@@ -20,6 +20,8 @@ from ._binding import (  # noqa: F401
     q8_0_gemm_workspace_bytes,
     q8_0_gemv,
     q8_0_gemv_grouped,
+    q8_0_gemv_batched,
+    GEMV_MAX_TOKENS,
     q8_check,
     q8_num_sms,
     q8_plane_rows,

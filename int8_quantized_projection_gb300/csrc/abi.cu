@@ -52,6 +52,53 @@ bool device_is_sm103()
     return g_is103[dev] == 1;
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the
+// library does not link libcuda); looked up once, thread-safely.
+EncodeTiledFn encode_fn()
+{
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return nullptr;
+    }();
+    return fn;
+}
+
+bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t d0, uint64_t d1,
+                 uint64_t stride_bytes, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {d0, d1};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {b0, b1};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                 CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool set_max_dynamic_smem(const void *func, int bytes, int slot)
 {
     const int dev = current_device();
@@ -113,7 +160,7 @@ extern "C" int q8_check(void *stream)
 
 extern "C" size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k)
 {
-    if (t < 1 || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0) return 0;
+    if (t <= Q8_GEMV_MAX_TOKENS || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0) return 0;
     return q8::gemm_workspace_bytes(t, k);
 }
 
@@ -127,10 +174,12 @@ extern "C" int q8_0_gemm(const void *w, int64_t n, int64_t k, const int8_t *qs, 
     if (need > 0 && !q8::aligned16(workspace)) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (t == 1) return q8_0_gemv(w, n, k, qs, ds, y, stream);
     if ((k / 32) % 8 != 0) {
         if (t > 65535) return Q8_ERR_ARG;  // generic kernel: one grid row per token
         return q8::gemv_generic_launch(w, n, k, qs, ds, y, t, s);
     }
+    if (t <= Q8_GEMV_MAX_TOKENS) return q8::gemv_small_launch(w, n, k, qs, ds, y, t, s);
     if (t > int64_t(65535) * 128 || n > (int64_t(1) << 31) - 128 || k > (int64_t(1) << 31) / 2) return Q8_ERR_ARG;
     return q8::gemm_tc_launch(w, n, k, qs, ds, t, y, workspace, s);
 }

@@ -83,15 +83,6 @@ constexpr int kSmemBytes = OFF_MISC + 16 + 1024;                // + alignment s
 // ---------------------------------------------------------------------------
 // PTX wrappers specific to this kernel
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -155,20 +146,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 // Instruction descriptor: D f32, A and B f16, both K-major, M = 128, N = BN.
 constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
-
-// int8 x4 (one 32-bit word) -> two f16x2 words, exactly: byte b becomes the
-// f16 1024 + (b ^ 0x80), minus 1152.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t q, uint32_t &lo, uint32_t &hi)
-{
-    const uint32_t x = q ^ 0x80808080u;
-    const uint32_t l = __byte_perm(x, 0x64646464u, 0x5140);
-    const uint32_t h = __byte_perm(x, 0x64646464u, 0x5342);
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-    const __half2 lv = __hsub2(*reinterpret_cast<const __half2 *>(&l), bias);
-    const __half2 hv = __hsub2(*reinterpret_cast<const __half2 *>(&h), bias);
-    lo = *reinterpret_cast<const uint32_t *>(&lv);
-    hi = *reinterpret_cast<const uint32_t *>(&hv);
-}
 
 __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
 {
@@ -260,8 +237,8 @@ __device__ __forceinline__ void convert_a_row(const uint8_t *arow, uint8_t *a16,
 #pragma unroll
     for (int kc = 0; kc < 4; ++kc) {
         uint4 v;
-        i8x4_to_f16x4(qw[2 * kc], v.x, v.y);
-        i8x4_to_f16x4(qw[2 * kc + 1], v.z, v.w);
+        q8::i8x4_to_f16x4(qw[2 * kc], v.x, v.y);
+        q8::i8x4_to_f16x4(qw[2 * kc + 1], v.z, v.w);
         *reinterpret_cast<uint4 *>(a16 + (r >> 3) * 512 + kc * 128 + (r & 7) * 16) = v;
     }
 }
@@ -427,14 +404,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.a_full(slot)),
                                      "r"(kARawBytes)
                                      : "memory");
-                        tma_load_2d(base + OFF_ARAW + slot * kARawBytes, &tmA, s * 136, static_cast<int>(n0),
+                        q8::tma_load_2d(base + OFF_ARAW + slot * kARawBytes, &tmA, s * 136, static_cast<int>(n0),
                                     B.a_full(slot));
                     } else {
                         if (!wait_bar(B.b_empty(slot), (use & 1u) ^ 1u, abort_flag)) break;
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(B.b_full(slot)),
                                      "r"(kBStageBytes)
                                      : "memory");
-                        tma_load_2d(base + OFF_B + slot * kBStageBytes, &tmB, s * 32 * kBBlocksPerStage,
+                        q8::tma_load_2d(base + OFF_B + slot * kBStageBytes, &tmB, s * 32 * kBBlocksPerStage,
                                     static_cast<int>(t0), B.b_full(slot));
                     }
                     issued = s + 1;
@@ -587,50 +564,13 @@ gemm_prep_kernel(const uint4 *__restrict__ qs, int64_t t, int64_t k, uint4 *__re
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint4 v = __ldg(qs + i);
         uint4 o0, o1;
-        i8x4_to_f16x4(v.x, o0.x, o0.y);
-        i8x4_to_f16x4(v.y, o0.z, o0.w);
-        i8x4_to_f16x4(v.z, o1.x, o1.y);
-        i8x4_to_f16x4(v.w, o1.z, o1.w);
+        q8::i8x4_to_f16x4(v.x, o0.x, o0.y);
+        q8::i8x4_to_f16x4(v.y, o0.z, o0.w);
+        q8::i8x4_to_f16x4(v.z, o1.x, o1.y);
+        q8::i8x4_to_f16x4(v.w, o1.z, o1.w);
         b16[2 * i] = o0;
         b16[2 * i + 1] = o1;
     }
-}
-
-// ---------------------------------------------------------------------------
-// host side: tensor maps through the driver entry point (no libcuda link)
-// ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *ptr, uint64_t d0, uint64_t d1,
-                 uint64_t stride_bytes, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw)
-{
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {d0, d1};
-    const cuuint64_t strides[1] = {stride_bytes};
-    const cuuint32_t box[2] = {b0, b1};
-    const cuuint32_t estr[2] = {1, 1};
-    (void)esize;
-    return fn(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 } // namespace
@@ -661,9 +601,9 @@ int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const 
     const int64_t pitch = nb * 34;
     uint8_t *b16 = static_cast<uint8_t *>(workspace);
     CUtensorMap ma, mb;
-    if (!make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, w, static_cast<uint64_t>(pitch / 2),
+    if (!make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, static_cast<uint64_t>(pitch / 2),
                      static_cast<uint64_t>(n), static_cast<uint64_t>(pitch), 136, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, b16, static_cast<uint64_t>(k), static_cast<uint64_t>(t),
+        !make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT16, b16, static_cast<uint64_t>(k), static_cast<uint64_t>(t),
                      static_cast<uint64_t>(k * 2), 64, BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return Q8_ERR_LAUNCH;
     const int sms = device_sm_count();
@@ -728,10 +668,12 @@ extern "C" int q8_0_gemm_noalloc(const void *w, int64_t n, int64_t k, const int8
     if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((k / 32) % 8 != 0) {  // this shape needs no scratch
+    if (t == 1) return q8_0_gemv(w, n, k, qs, ds, y, stream);  // these shapes need no scratch
+    if ((k / 32) % 8 != 0) {
         if (t > 65535) return Q8_ERR_ARG;
         return q8::gemv_generic_launch(w, n, k, qs, ds, y, t, s);
     }
+    if (t <= Q8_GEMV_MAX_TOKENS) return q8::gemv_small_launch(w, n, k, qs, ds, y, t, s);
     if (t > int64_t(65535) * 128 || n > (int64_t(1) << 31) - 128) return Q8_ERR_ARG;
     void *scratch = nullptr;
     const int st = noalloc_scratch(&scratch);

@@ -28,7 +28,11 @@
 // Shapes whose k/32 is not a multiple of 8 (or whose activation would not
 // fit in shared memory) use gemv_generic_kernel: plain 2-byte loads, the same
 // lanes-per-row fitting, no staging.
+#include <cooperative_groups.h>
+
 #include "q8_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -284,6 +288,287 @@ gemv_generic_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, const int8
     if (j == 0 && row < n) y[tok * n + row] = acc;
 }
 
+// ---------------------------------------------------------------------------
+// Small-batch path: t = 1..16 tokens against one weight matrix, the weights
+// streamed from HBM once for all tokens (a decode step batched over a few
+// sequences; the bridge between the batch-1 GEMV and the prefill GEMM).
+// dp4a would need 8*t integer instructions per 4-byte weight word, more than
+// an SM issues at HBM rate for t = 16, so the block dot products run on the
+// tensor cores: mma.sync m16n8k16 on the int8 codes widened exactly to f16,
+// two MMAs per 32-wide block and 8 tokens, whose f32 result is the exact
+// integer dot product (|isum| <= 32*127*127 < 2^24).  (The int8 mma.sync
+// needs no widening but its rate on this GPU falls short of HBM at t = 16.)
+// Within a block the k order is permuted so that each thread's eight codes
+// are contiguous bytes -- the integer sum does not depend on the order, and
+// A and B use the same one.  Per block the scale is applied as in the GEMM:
+// acc += (d_w * d_a) * isum.
+//
+// Work split: a CTA computes kSbRows weight rows for all tokens over a slice
+// of k, in stages of kSbPieces "pieces" of 8 blocks (272 bytes of each row,
+// contiguous in memory, so a stage reads kSbPieces*272 consecutive bytes per
+// row).  One thread of a ninth warp moves each stage with three TMA loads:
+// the weights (one 3-D box: rows x pieces x 272 bytes), the tokens' code
+// bytes (128-byte boxes, 128-byte swizzled so the consumer warps' fragment
+// reads spread over the banks) and their d|ssum words; rows past n and
+// tokens past t arrive as zeros.  Consumer warp w takes 16 rows (tile
+// w % (kSbRows/16)) and one piece (w / (kSbRows/16)) of every stage.  The
+// CTAs of a thread-block cluster (1..8) split k between them, so narrow
+// matrices still fill the GPU.  Partial sums are added in piece order inside
+// a CTA, then in cluster-rank order by rank 0, which reads its peers' shared
+// memory: results are run-to-run identical.
+// ---------------------------------------------------------------------------
+#ifndef Q8_SB_PIECES
+#define Q8_SB_PIECES 1
+#endif
+#ifndef Q8_SB_STAGES
+#define Q8_SB_STAGES 2
+#endif
+constexpr int kSbWarps = 8;                              // consumer warps
+constexpr int kSbThreads = (kSbWarps + 1) * 32;          // + the producer warp
+constexpr int kSbPieces = Q8_SB_PIECES;                  // 8-block pieces per row and stage (1, 2 or 4)
+constexpr int kSbRows = 16 * kSbWarps / kSbPieces;       // weight rows per CTA
+constexpr int kSbTiles = kSbRows / 16;                   // 16-row MMA tiles per CTA
+constexpr int kSbGroup = 8;                              // Q8_0 blocks per piece
+constexpr int kSbMaxTokens = 16;
+constexpr int kSbPieceBytes = kSbGroup * 34;             // 272
+constexpr int kSbRowBytes = kSbPieces * kSbPieceBytes;   // weight bytes per row and stage
+// stage layout (offsets from a 1024-byte aligned stage base)
+constexpr int kSbOffAct = 0;                             // 2*kSbPieces boxes x 16 tokens x 128 B, swizzled
+constexpr int kSbOffDs = kSbPieces * 4096;               // 16 tokens x 8*kSbPieces words
+constexpr int kSbOffW = kSbOffDs + kSbPieces * 512;      // kSbRows rows x kSbRowBytes
+constexpr int kSbStageTx = kSbOffW + kSbRows * kSbRowBytes;        // bytes the TMA writes per stage
+constexpr int kSbStageBytes = (kSbStageTx + 1023) / 1024 * 1024;  // stage stride
+constexpr int kSbStages = Q8_SB_STAGES;
+constexpr int kSbOffBar = kSbStages * kSbStageBytes;     // full[], empty[], error flag
+constexpr int kSbSmem = kSbOffBar + 128 + 1024;          // + alignment slack
+constexpr int kSbCtasPerSm = 232448 / (kSbSmem + 1024);  // resident CTAs per SM (shared memory bound)
+constexpr int kSbMaxCluster = 8;
+static_assert(kSbPieces == 1 || kSbPieces == 2 || kSbPieces == 4, "pieces per stage");
+static_assert(kSbStages * 16 + 8 <= 128, "barrier area");
+static_assert(kSbOffW % 128 == 0, "TMA destination alignment");
+static_assert(kSbMaxTokens * kSbRows * kSbPieces * 4 <= kSbStages * kSbStageBytes, "partial sums reuse the ring");
+
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Codes 8*t4 .. 8*t4+7 of block BB of a staged piece (piece start 16-byte
+// aligned, block BB at byte 34*BB, its codes from byte 34*BB + 2).
+template <int BB>
+__device__ __forceinline__ uint2 sb_codes(const uint8_t *piece, int t4)
+{
+    constexpr int off = 34 * BB + 2;
+    if constexpr ((off & 3) == 0) {
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(piece + off + 8 * t4);
+        return make_uint2(p[0], p[1]);
+    } else {
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(piece + off - 2 + 8 * t4);
+        const uint32_t x0 = p[0], x1 = p[1], x2 = p[2];
+        return make_uint2(__byte_perm(x0, x1, 0x5432), __byte_perm(x1, x2, 0x5432));
+    }
+}
+
+// One 32-wide block (block BB of piece `pc` of the stage) for this warp's 16
+// rows (row g's piece at wpiece) and NT groups of 8 tokens (tokens past t
+// are zeros).  Thread (g = lane/4, t4 = lane%4) holds the MMA fragments of
+// rows g, g+8 and token g (+8 per token tile); its results are rows g, g+8
+// at tokens 2*t4, 2*t4+1 (+8 per token tile), kept as token pairs.
+template <int BB, int NT>
+__device__ __forceinline__ void sb_block(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
+                                         float2 (&acc)[NT][2])
+{
+    uint32_t bf[NT][4];  // token 8j+g: step 0 {codes 0,1 | 2,3}, step 1 {codes 4,5 | 6,7} of its eight
+    float2 da[NT];       // d_a of tokens 8j + 2*t4, 8j + 2*t4 + 1
+    // code byte 32*BB + 8*t4 of piece pc of token tok: box 2*pc + BB/4, 16-byte
+    // chunk 2*(BB%4) + t4/2 of the token's 128-byte line, XOR-swizzled by tok % 8
+    const int box = 2 * pc + (BB >> 2);
+    constexpr int c0 = 2 * (BB & 3);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int tok = 8 * j + g;
+        const int chunk = (c0 + (t4 >> 1)) ^ (tok & 7);
+        const uint2 v = *reinterpret_cast<const uint2 *>(stage + kSbOffAct + box * 2048 + tok * 128 + chunk * 16 +
+                                                         8 * (t4 & 1));
+        q8::i8x4_to_f16x4(v.x, bf[j][0], bf[j][1]);
+        q8::i8x4_to_f16x4(v.y, bf[j][2], bf[j][3]);
+        const int tk = 8 * j + 2 * t4;
+        const uint8_t *dsw = stage + kSbOffDs + 4 * (kSbGroup * pc + BB);
+        const uint32_t d0 = *reinterpret_cast<const uint32_t *>(dsw + tk * (32 * kSbPieces));
+        const uint32_t d1 = *reinterpret_cast<const uint32_t *>(dsw + (tk + 1) * (32 * kSbPieces));
+        da[j] = make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(d0 & 0xffffu))),
+                            __half2float(__ushort_as_half(static_cast<unsigned short>(d1 & 0xffffu))));
+    }
+    const uint8_t *rlo = wpiece + g * kSbRowBytes;  // row g of the tile
+    const uint8_t *rhi = rlo + 8 * kSbRowBytes;      // row g + 8
+    const uint2 clo = sb_codes<BB>(rlo, t4), chi = sb_codes<BB>(rhi, t4);
+    uint32_t a0[4], a1[4];  // per MMA step: {row g lo, row g+8 lo, row g hi, row g+8 hi}
+    q8::i8x4_to_f16x4(clo.x, a0[0], a0[2]);
+    q8::i8x4_to_f16x4(chi.x, a0[1], a0[3]);
+    q8::i8x4_to_f16x4(clo.y, a1[0], a1[2]);
+    q8::i8x4_to_f16x4(chi.y, a1[1], a1[3]);
+    const float dlo = __half2float(*reinterpret_cast<const __half *>(rlo + 34 * BB));
+    const float dhi = __half2float(*reinterpret_cast<const __half *>(rhi + 34 * BB));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_f16_16816(c, a0, bf[j][0], bf[j][1]);
+        mma_f16_16816(c, a1, bf[j][2], bf[j][3]);
+        // per output: the scale d_w * d_a rounded once, then one fma (packed in token pairs)
+        acc[j][0] = __ffma2_rn(__fmul2_rn(make_float2(dlo, dlo), da[j]), make_float2(c[0], c[1]), acc[j][0]);
+        acc[j][1] = __ffma2_rn(__fmul2_rn(make_float2(dhi, dhi), da[j]), make_float2(c[2], c[3]), acc[j][1]);
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kSbThreads)
+gemv_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmD, int64_t n, int nb, int t, float *__restrict__ y)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = q8::smem_u32(smem_raw);
+    uint8_t *ring = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);  // 1024-byte aligned (swizzle atoms)
+    cg::cluster_group cluster = cg::this_cluster();
+    const int ks = static_cast<int>(cluster.num_blocks());  // CTAs splitting k (the cluster spans x only)
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + kSbOffBar);  // [stage]: the stage's boxes landed
+    uint64_t *empty = full + kSbStages;                                 // [stage]: consumer warps done
+    volatile int *bad = reinterpret_cast<volatile int *>(ring + kSbOffBar + kSbStages * 16);
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x / ks) * kSbRows;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(kSbRows), n - row0));
+    // the last stage may hang past the end of the rows: those pieces, codes
+    // and scales arrive as zeros and add exactly nothing
+    const int stages_total = (nb + kSbGroup * kSbPieces - 1) / (kSbGroup * kSbPieces);
+    const int gc0 = static_cast<int>(static_cast<int64_t>(stages_total) * rank / ks);  // this CTA's share of k
+    const int ng = static_cast<int>(static_cast<int64_t>(stages_total) * (rank + 1) / ks) - gc0;
+
+    q8::griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        *bad = 0;
+        for (int s = 0; s < kSbStages; ++s) {
+            q8::mbar_init(&full[s], 1);
+            q8::mbar_init(&empty[s], kSbWarps);
+        }
+        q8::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kSbWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            // The weights do not depend on the previous kernel in the stream:
+            // the first stages' weight boxes go out before waiting for it
+            // (programmatic dependent launch), every activation box after.
+            const uint32_t rb = q8::smem_u32(ring);
+            auto issue_w = [&](int s, int gi) {
+                q8::mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(kSbStageTx));
+                q8::tma_load_3d(rb + s * kSbStageBytes + kSbOffW, &tmW, 0, gi * kSbPieces, static_cast<int>(row0),
+                                q8::smem_u32(&full[s]));
+            };
+            auto issue_a = [&](int s, int gi) {
+                const uint32_t st = rb + s * kSbStageBytes;
+#pragma unroll
+                for (int b = 0; b < 2 * kSbPieces; ++b)
+                    q8::tma_load_2d(st + kSbOffAct + 2048 * b, &tmQ, gi * (256 * kSbPieces) + 128 * b, 0,
+                                    q8::smem_u32(&full[s]));
+                q8::tma_load_2d(st + kSbOffDs, &tmD, gi * (kSbGroup * kSbPieces), 0, q8::smem_u32(&full[s]));
+            };
+            int i = 0;
+            for (; i < kSbStages && i < ng; ++i) issue_w(i, gc0 + i);
+            q8::griddep_wait();
+            for (int s = 0; s < i; ++s) issue_a(s, gc0 + s);
+            for (; i < ng; ++i) {
+                const int s = i % kSbStages;
+                if (!q8::mbar_wait_bounded(&empty[s], static_cast<uint32_t>(i / kSbStages - 1) & 1u)) {
+                    atomicOr(&g_gemv_err, 1u);
+                    *bad = 1;
+                    break;
+                }
+                issue_w(s, gc0 + i);
+                issue_a(s, gc0 + i);
+            }
+            // let every issued stage land (bounded) before the CTA can exit
+            for (int j = (i > kSbStages ? i - kSbStages : 0); j < i; ++j)
+                if (!q8::mbar_wait_bounded(&full[j % kSbStages], static_cast<uint32_t>(j / kSbStages) & 1u)) {
+                    atomicOr(&g_gemv_err, 1u);
+                    *bad = 1;
+                }
+        }
+    }
+    float2 acc[NT][2];  // [token tile][row g, row g+8]: tokens 2*t4, 2*t4+1
+#pragma unroll
+    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = make_float2(0.0f, 0.0f);
+    const int tile = warp % kSbTiles, pc = warp / kSbTiles;  // this warp's 16 rows and piece
+    if (warp < kSbWarps) {
+        // ------------------------------------------------------------ consumers
+        const int g = lane >> 2, t4 = lane & 3;
+        for (int i = 0; i < ng; ++i) {
+            const int s = i % kSbStages;
+            const bool got = q8::mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / kSbStages) & 1u);
+            if (!__all_sync(Q8_FULL_MASK, got)) {
+                if (lane == 0) {
+                    atomicOr(&g_gemv_err, 1u);
+                    *bad = 1;
+                }
+                break;
+            }
+            const uint8_t *st = ring + s * kSbStageBytes;
+            const uint8_t *wp = st + kSbOffW + tile * 16 * kSbRowBytes + pc * kSbPieceBytes;
+            sb_block<0, NT>(wp, st, pc, g, t4, acc);
+            sb_block<1, NT>(wp, st, pc, g, t4, acc);
+            sb_block<2, NT>(wp, st, pc, g, t4, acc);
+            sb_block<3, NT>(wp, st, pc, g, t4, acc);
+            sb_block<4, NT>(wp, st, pc, g, t4, acc);
+            sb_block<5, NT>(wp, st, pc, g, t4, acc);
+            sb_block<6, NT>(wp, st, pc, g, t4, acc);
+            sb_block<7, NT>(wp, st, pc, g, t4, acc);
+            __syncwarp();
+            if (lane == 0) q8::mbar_arrive(&empty[s]);
+        }
+    }
+    __syncthreads();  // the ring is consumed and every box has landed: reuse it for the partial sums
+    float *part = reinterpret_cast<float *>(ring);  // [piece][token 16][row]
+    if (warp < kSbWarps) {
+        const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = tile * 16 + g + 8 * e;
+                part[(pc * kSbMaxTokens + 8 * j + 2 * t4) * kSbRows + r] = acc[j][e].x;
+                part[(pc * kSbMaxTokens + 8 * j + 2 * t4 + 1) * kSbRows + r] = acc[j][e].y;
+            }
+    }
+    __syncthreads();
+    // this CTA's sum over its pieces, in piece order, into piece 0's slot
+    for (int o = threadIdx.x; o < 8 * NT * kSbRows; o += kSbThreads) {
+        float v = part[o];
+#pragma unroll
+        for (int p = 1; p < kSbPieces; ++p) v += part[p * kSbMaxTokens * kSbRows + o];
+        part[o] = v;
+    }
+    cluster.sync();  // every CTA's partial sums are in its shared memory
+    if (rank == 0) {
+        bool any_bad = *bad != 0;
+        for (int r = 1; r < ks; ++r) any_bad |= *cluster.map_shared_rank(const_cast<int *>(bad), r) != 0;
+        if (!any_bad) {
+            for (int o = threadIdx.x; o < 8 * NT * kSbRows; o += kSbThreads) {
+                const int tok = o / kSbRows, r = o % kSbRows;
+                if (tok < t && r < rows) {
+                    float v = part[o];
+                    for (int pr = 1; pr < ks; ++pr) v += *cluster.map_shared_rank(part + o, pr);
+                    y[tok * n + row0 + r] = v;
+                }
+            }
+        }
+    }
+    cluster.sync();  // peers keep their shared memory until rank 0 has read it
+}
+
 int ceil_log2(int v)
 {
     int l = 0;
@@ -316,6 +601,45 @@ int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, c
     const dim3 grid(static_cast<unsigned>((warps + 3) / 4), static_cast<unsigned>(tokens));
     return launch_pdl(gemv_generic_kernel, grid, dim3(128), 0, s, static_cast<const uint8_t *>(w), n, nb, qs, ds, y,
                       lpr_log2);
+}
+
+// Launch the small-batch kernel: 1 <= tokens <= 16, (k/32) % 8 == 0.  The
+// cluster size (CTAs splitting k, 1..8) makes the grid about one wave of the
+// CTAs that fit on the GPU at once.
+int gemv_small_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                      int64_t tokens, cudaStream_t s)
+{
+    const int64_t nb = k / 32;
+    if (tokens < 1 || tokens > kSbMaxTokens || nb % kSbGroup != 0 || nb > (int64_t(1) << 30)) return Q8_ERR_ARG;
+    const int64_t stages = (nb + kSbGroup * kSbPieces - 1) / (kSbGroup * kSbPieces);
+    const int sms = q8::device_sm_count();
+    if (sms <= 0) return Q8_ERR_DEVICE;
+    const int64_t tiles = (n + kSbRows - 1) / kSbRows;
+    // about one wave of resident CTAs, at least one stage per CTA
+    int64_t ks = (static_cast<int64_t>(kSbCtasPerSm) * sms) / tiles;
+    ks = ks < 1 ? 1 : (ks > kSbMaxCluster ? kSbMaxCluster : ks);
+    if (ks > stages) ks = stages;
+    if (tiles * ks > 0x7fffffff) return Q8_ERR_ARG;
+    const dim3 grid(static_cast<unsigned>(tiles * ks));
+    CUtensorMap mw, mq, md;
+    // weights as [n rows][nb/8 pieces][136 u16]; box = kSbRows rows x kSbPieces pieces
+    if (!make_map_3d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, kSbPieceBytes / 2, static_cast<uint64_t>(nb / kSbGroup),
+                     static_cast<uint64_t>(n), kSbPieceBytes, static_cast<uint64_t>(nb * 34), kSbPieceBytes / 2,
+                     kSbPieces, kSbRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qs, static_cast<uint64_t>(k), static_cast<uint64_t>(tokens),
+                     static_cast<uint64_t>(k), 128, kSbMaxTokens, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT32, ds, static_cast<uint64_t>(nb), static_cast<uint64_t>(tokens),
+                     static_cast<uint64_t>(nb * 4), kSbGroup * kSbPieces, kSbMaxTokens, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return Q8_ERR_LAUNCH;
+    const bool wide = tokens > 8;
+    const void *fn = wide ? reinterpret_cast<const void *>(gemv_small_kernel<2>)
+                          : reinterpret_cast<const void *>(gemv_small_kernel<1>);
+    if (!q8::set_max_dynamic_smem(fn, kSbSmem, wide ? 4 : 3)) return Q8_ERR_LAUNCH;
+    if (wide)
+        return launch_pdl_cluster(gemv_small_kernel<2>, grid, dim3(kSbThreads), kSbSmem, s, static_cast<int>(ks), mw, mq,
+                                  md, n, static_cast<int>(nb), static_cast<int>(tokens), y);
+    return launch_pdl_cluster(gemv_small_kernel<1>, grid, dim3(kSbThreads), kSbSmem, s, static_cast<int>(ks), mw, mq, md,
+                              n, static_cast<int>(nb), static_cast<int>(tokens), y);
 }
 
 } // namespace q8
@@ -421,4 +745,17 @@ extern "C" int q8_0_gemv_grouped(const q8_gemv_proj *projs, int count, int64_t k
                                  const uint32_t *ds, void *stream)
 {
     return gemv_dispatch(projs, count, k, qs, ds, stream);
+}
+
+extern "C" int q8_0_gemv_batched(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds,
+                                 int64_t tokens, float *y, void *stream)
+{
+    if (!w || !qs || !ds || !y || n < 1 || n > (int64_t(1) << 40) || k <= 0 || (k % 32) != 0 || tokens < 1 ||
+        tokens > Q8_GEMV_MAX_TOKENS)
+        return Q8_ERR_ARG;
+    if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((k / 32) % 8 != 0) return q8::gemv_generic_launch(w, n, k, qs, ds, y, tokens, s);
+    return q8::gemv_small_launch(w, n, k, qs, ds, y, tokens, s);
 }

@@ -5,6 +5,7 @@
 // q8_0 block encoder used by all three quantizing kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -53,11 +54,49 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
     return launch_status();
 }
 
+// The same with thread-block clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+int launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_x,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) return Q8_ERR_LAUNCH;
+    return launch_status();
+}
+
+// Host: a 2-D tiled TMA tensor map (element type dt, dims {d0 (inner), d1},
+// row stride in bytes, box {b0, b1}, out-of-bounds elements read as zero),
+// encoded through the driver entry point (abi.cu).  False on failure.
+bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t d0, uint64_t d1,
+                 uint64_t stride_bytes, uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw);
+
+// The same in three dimensions: dims {d0, d1, d2}, byte strides of
+// dimensions 1 and 2, box {b0, b1, b2}.
+bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                 CUtensorMapSwizzle sw);
+
 // Per-translation-unit device error words are read and cleared through these
 // (each .cu file that has bounded waits defines one).
 int gemv_take_error(cudaStream_t s);
 int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
                         int64_t tokens, cudaStream_t s);
+// small-batch kernel (gemv.cu): 1 <= tokens <= Q8_GEMV_MAX_TOKENS, (k/32) % 8 == 0
+int gemv_small_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                      int64_t tokens, cudaStream_t s);
 int gemm_take_error(cudaStream_t s);
 
 // ---------------------------------------------------------------------------
@@ -152,6 +191,41 @@ __device__ __forceinline__ void griddep_launch_dependents()
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c)
 {
     return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
+}
+
+// 2-D tiled TMA load of one box into shared memory at dst, completing on the
+// mbarrier at bar (shared addresses); x is the inner coordinate in elements.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// Four int8 codes (one 32-bit word) -> two f16x2 words, exactly: byte b
+// becomes the f16 1024 + (b ^ 0x80), minus 1152.  lo holds bytes 0 and 1
+// (byte 0 in the low half), hi bytes 2 and 3.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t q, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t x = q ^ 0x80808080u;
+    const uint32_t l = __byte_perm(x, 0x64646464u, 0x5140);
+    const uint32_t h = __byte_perm(x, 0x64646464u, 0x5342);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    const __half2 lv = __hsub2(*reinterpret_cast<const __half2 *>(&l), bias);
+    const __half2 hv = __hsub2(*reinterpret_cast<const __half2 *>(&h), bias);
+    lo = *reinterpret_cast<const uint32_t *>(&lv);
+    hi = *reinterpret_cast<const uint32_t *>(&hv);
 }
 
 // ---------------------------------------------------------------------------

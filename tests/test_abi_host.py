@@ -76,15 +76,21 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert lib.q8_0_gemv(P(FAKE), 8, 100, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
     assert lib.q8_0_gemv(P(FAKE + 2), 8, 64, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ALIGN
     # q8_0_gemm: rows_pad < t, t < 1, workspace missing or too small
-    ws = lib.q8_0_gemm_workspace_bytes(4, 256)
-    assert ws == 4 * 256 * 2                                  # the activation's codes as f16
-    assert lib.q8_0_gemm_workspace_bytes(4, 64) == 0          # k/32 % 8 != 0: generic kernel, no workspace
+    ws = lib.q8_0_gemm_workspace_bytes(20, 256)
+    assert ws == 20 * 256 * 2                                 # the activation's codes as f16
+    assert lib.q8_0_gemm_workspace_bytes(20, 64) == 0         # k/32 % 8 != 0: generic kernel, no workspace
+    assert lib.q8_0_gemm_workspace_bytes(16, 256) == 0        # t <= 16: small-batch kernel, no workspace
     assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(FAKE), 5, 4, P(FAKE), P(0), 0, s) == ERR_ARG
     assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(FAKE), 0, 4, P(FAKE), P(0), 0, s) == ERR_ARG
-    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 4, 4, P(FAKE), P(0), ws, s) == ERR_ARG
-    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 4, 4, P(FAKE), P(FAKE), ws - 1, s) == ERR_ARG
-    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 4, 4, P(FAKE), P(MISALIGNED), ws, s) == ERR_ALIGN
+    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 20, 20, P(FAKE), P(0), ws, s) == ERR_ARG
+    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 20, 20, P(FAKE), P(FAKE), ws - 1, s) == ERR_ARG
+    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 20, 20, P(FAKE), P(MISALIGNED), ws, s) == ERR_ALIGN
     assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(MISALIGNED), 4, 4, P(FAKE), P(0), 0, s) == ERR_ALIGN
+    # q8_0_gemv_batched: tokens outside 1..16, k % 32, alignment
+    assert lib.q8_0_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 0, P(FAKE), s) == ERR_ARG
+    assert lib.q8_0_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 17, P(FAKE), s) == ERR_ARG
+    assert lib.q8_0_gemv_batched(P(FAKE), 8, 100, P(FAKE), P(FAKE), 4, P(FAKE), s) == ERR_ARG
+    assert lib.q8_0_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 4, P(MISALIGNED), s) == ERR_ALIGN
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
