@@ -47,7 +47,8 @@ PREFILL = dict(tokens=3325, d=3584, nf=18944, eps=1e-6)
 # DRAM bytes per launch from one ncu capture of the current kernel; None when
 # the kernel changed after the capture (the figure would describe old code).
 NCU_TRAFFIC_BYTES = {"gemv_staged 12288x7168+96x7168": 97_942_016,     # profiles/gemv_staged_12288x7168_plus_96x7168.md
-                     "gemm_tc 18944x3584 t=3325": None}                # recapture pending for the current gemm_tc
+                     "gemm_tc 18944x3584 t=3325": 734_083_584,         # profiles/gemm_tc_18944x3584_t3325.md
+                     "gemv_small 12288x7168 t=16": 98_196_736}         # profiles/gemv_small_12288x7168_t16.md
 
 
 # ---------------------------------------------------------------------------
@@ -319,6 +320,41 @@ def run_prefill(torch, q8p, steps, warmup, dev):
 
 
 # ---------------------------------------------------------------------------
+# small-batch decode: one projection for a few tokens, weights read once
+# ---------------------------------------------------------------------------
+SMALL = {"n": 12288, "k": 7168, "tokens": 16}
+
+
+def bytes_small(n, k, t):
+    return n * (k // 32) * 34 + t * (k + 4 * (k // 32)) + 4 * t * n
+
+
+def run_small(torch, q8p, steps, warmup, dev):
+    n, k, t = SMALL["n"], SMALL["k"], SMALL["tokens"]
+    w_h = syn.q8_0_weights(syn.rng(4, 1), n, k)[0]
+    copies = max(2, -(-4 * L2_BYTES // w_h.nbytes))
+    ws = [torch.from_numpy(w_h).to(dev) for _ in range(copies)]
+    x = torch.from_numpy(syn.activations(syn.rng(4, 0), t, k, sigma=1.5, outlier_frac=0.01)).to(dev)
+    plane = q8p.empty_plane(q8p.q8_plane_rows(t), k, dev)
+    q8p.quantize_q8_0(x, *plane)
+    y = torch.empty((t, n), dtype=torch.float32, device=dev)
+    calls = [q8p.q8_0_gemv_batched(w, n, k, *plane, t, y, bind=True) for w in ws]
+    for i in range(warmup):
+        calls[i % copies]()
+    q8p.q8_check()
+    stream = torch.cuda.current_stream(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        calls[(warmup + i) % copies]()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    q8p.q8_check()
+    return dict(us=1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs), copies=copies)
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle (reported baseline and the reference arm)
 # ---------------------------------------------------------------------------
 def oracle_decode_sample(budget_s):
@@ -345,25 +381,39 @@ def reference_arm(args):
     import oracle
 
     xs, ws = decode_inputs()
-    per = []
+    t_full = []
     for _ in range(args.warmup):
-        planes = {k: oracle.quantize(v) for k, v in xs.items()}
-        oracle.gemv(ws[0], *DECODE_SHAPES[0], *planes[7168])
-    for _ in range(args.steps):
         t0 = time.perf_counter()
         planes = {k: oracle.quantize(v) for k, v in xs.items()}
         for (n, k), wb in zip(DECODE_SHAPES, ws):
             oracle.gemv(wb, n, k, *planes[k])
+        t_full.append(time.perf_counter() - t0)
+    # Each timed step is the decode step on a prefix of every weight matrix's
+    # rows, sized so that K steps take about a minute (all rows when K is small).
+    frac = min(1.0, 60.0 / (args.steps * statistics.median(t_full)))
+    rows = [max(1, int(frac * n)) for n, _ in DECODE_SHAPES]
+    subs = [wb[: r * (k // 32) * 34] for wb, r, (_, k) in zip(ws, rows, DECODE_SHAPES)]
+    step_bytes = (bytes_quantize(1, 7168) + bytes_quantize(1, 128) +
+                  sum(bytes_gemv(r, k) for r, (_, k) in zip(rows, DECODE_SHAPES)))
+    per = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        planes = {k: oracle.quantize(v) for k, v in xs.items()}
+        for r, (_, k), wb in zip(rows, DECODE_SHAPES, subs):
+            oracle.gemv(wb, r, k, *planes[k])
         per.append(time.perf_counter() - t0)
     tot = sum(per)
-    value = decode_bytes() * args.steps / tot / 1e9
+    value = step_bytes * args.steps / tot / 1e9
+    sample = (f"{args.steps} decode steps of the sweep, each timed" if frac >= 1.0 else
+              f"{args.steps} decode steps of the sweep on the first {rows} rows of each weight matrix "
+              f"({100 * frac:.1f}% of the rows, bounded to ~60 s), each timed")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": decode_config(None),
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": f"{args.steps} full decode steps of the sweep, each timed"},
+                         "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -381,11 +431,13 @@ def decode_config(copies):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    # 6000 decode steps keep the timed region ~0.2 s long, so the clock sampler
+    # (50 ms) sees it; the prefill chain runs steps // 6 times (~3.4 s)
+    ap.add_argument("--steps", type=int, default=6000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill"],
+    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "small"],
                     help="decode and/or prefill legs (profiling runs select one)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()
@@ -430,6 +482,11 @@ def main():
     pre = None
     if args.workload == "prefill" or (args.workload == "all" and not args.no_prefill):
         pre = run_prefill(torch, q8p, args.steps if dec is None else max(3, args.steps // 6), args.warmup, dev)
+
+    small = None
+    if args.workload in ("all", "small"):
+        small = run_small(torch, q8p, args.steps if dec is None and pre is None else max(20, args.steps // 30),
+                          args.warmup, dev)
 
     if rank != 0:
         if world > 1:
@@ -482,6 +539,22 @@ def main():
                          "config": {"workload": pobj["workload"], "l2": pobj["l2"], "parallelism": "replicas"},
                          "roofline": pobj["roofline_gemm"], "gpu_launches": 5 * args.steps})
         line["prefill"] = pobj
+    if small is not None:
+        n, k, t = SMALL["n"], SMALL["k"], SMALL["tokens"]
+        gbs = bytes_small(n, k, t) / (small["us"] / 1e6) / 1e9
+        sobj = {"workload": f"small-batch decode: q8_0_gemv_batched {n}x{k}, t={t} tokens, weights read once",
+                "us_per_call": round(small["us"], 2), "gbs": round(gbs, 1),
+                "roofline": {"kernel": "q8_0_gemv_batched (gemv_small_kernel)", "bound": "hbm",
+                             "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(gbs / peaks["hbm_gbs"], 4),
+                             "traffic": NCU_TRAFFIC_BYTES["gemv_small 12288x7168 t=16"],
+                             "algorithmic_bytes": bytes_small(n, k, t)},
+                "l2": f"weights rotate through {small['copies']} copies (> 4 x L2)"}
+        if dec is None and pre is None:
+            line.update({"value": sobj["gbs"], "unit": "GB/s", "ms_per_step": round(small["us"] / 1e3, 5),
+                         "config": {"workload": sobj["workload"], "l2": sobj["l2"], "parallelism": "replicas"},
+                         "roofline": sobj["roofline"], "gpu_launches": args.steps})
+        line["small_batch"] = sobj
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
