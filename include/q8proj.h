@@ -85,9 +85,14 @@ Q8_API int quantize_q8_0(const float *x, int64_t rows, int64_t k,
 /*
  * rmsnorm_quant -- RMSNorm fused with q8_0 quantization of its output.
  *   x   : f32 [rows][d] (input)       w : f32 [d] (input weight)
- *   y   : f32 [rows][d] (output, y = (x * rsqrt(mean(x^2) + eps)) * w)
+ *   y   : f32 [rows][d] (output, y = (x * rsqrt(mean(x^2) + eps)) * w), or
+ *         NULL when y is dead -- every consumer reads the plane -- and only
+ *         the plane is written ("mode 2", the sequel that "54 - r51 -
+ *         producer-fused A-quantize mode 1" sec. 5 points to: the f32 write
+ *         and its re-read are what is left to remove).
  *   qs, ds : plane of y with rows_pad rows (output); the plane is exactly the
- *            q8_0 encoding of the f32 values written to y.
+ *            q8_0 encoding of the f32 values y holds (or would hold), the
+ *            same bytes whether y is written or not.
  * d % 32 == 0, d <= 32768 (the row is held in registers), rows >= 0,
  * rows_pad >= max(rows, 1).
  * "54 - r51 - producer-fused A-quantize mode 1", sec. 2.3 and 3.2
@@ -100,8 +105,11 @@ Q8_API int rmsnorm_quant(const float *x, const float *w, float eps, float *y,
 /*
  * swiglu_quant -- SwiGLU fused with q8_0 quantization of its output.
  *   gate, up : f32 [rows][nf] (inputs)
- *   y        : f32 [rows][nf] (output, y = gate / (1 + exp(-gate)) * up)
- *   qs, ds   : plane of y (output), exactly the q8_0 encoding of y.
+ *   y        : f32 [rows][nf] (output, y = gate / (1 + exp(-gate)) * up), or
+ *              NULL when y is dead (mode 2, as for rmsnorm_quant): 4 of the
+ *              13.125 bytes per element this call moves are that write.
+ *   qs, ds   : plane of y (output), exactly the q8_0 encoding of y, the same
+ *              bytes whether y is written or not.
  * nf % 32 == 0, rows >= 0, rows_pad >= max(rows, 1).
  * "54 - r51 - producer-fused A-quantize mode 1", sec. 3.2
  * (swiglu_quant_f32_t).

@@ -163,30 +163,36 @@ def quantize_q8_0(x, qs, ds, stream=None, bind=False):
 
 
 def rmsnorm_quant(x, w, eps: float, y, qs, ds, stream=None, bind=False):
+    """``y=None``: mode 2, only the plane is written (the f32 output is dead)."""
     import torch
 
-    for t, n in ((x, "x"), (w, "w"), (y, "y")):
+    for t, n in ((x, "x"), (w, "w")) + (((y, "y"),) if y is not None else ()):
         _need(t, torch.float32, n)
     _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds")
     rows, d = x.shape
     rows_pad = qs.shape[0]
-    if y.shape != x.shape or w.shape != (d,) or qs.shape != (rows_pad, d) or ds.shape != (rows_pad, d // 32):
+    if ((y is not None and y.shape != x.shape) or w.shape != (d,) or qs.shape != (rows_pad, d)
+            or ds.shape != (rows_pad, d // 32)):
         raise ValueError("shape mismatch")
-    return _launch("rmsnorm_quant", (_ptr(x), _ptr(w), ctypes.c_float(eps), _ptr(y), rows, d, _ptr(qs), _ptr(ds),
+    yp = _ptr(y) if y is not None else ctypes.c_void_p(0)
+    return _launch("rmsnorm_quant", (_ptr(x), _ptr(w), ctypes.c_float(eps), yp, rows, d, _ptr(qs), _ptr(ds),
                                      rows_pad, _stream(stream)), bind)
 
 
 def swiglu_quant(gate, up, y, qs, ds, stream=None, bind=False):
+    """``y=None``: mode 2, only the plane is written (the f32 output is dead)."""
     import torch
 
-    for t, n in ((gate, "gate"), (up, "up"), (y, "y")):
+    for t, n in ((gate, "gate"), (up, "up")) + (((y, "y"),) if y is not None else ()):
         _need(t, torch.float32, n)
     _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds")
     rows, nf = gate.shape
     rows_pad = qs.shape[0]
-    if up.shape != gate.shape or y.shape != gate.shape or qs.shape != (rows_pad, nf) or ds.shape != (rows_pad, nf // 32):
+    if (up.shape != gate.shape or (y is not None and y.shape != gate.shape) or qs.shape != (rows_pad, nf)
+            or ds.shape != (rows_pad, nf // 32)):
         raise ValueError("shape mismatch")
-    return _launch("swiglu_quant", (_ptr(gate), _ptr(up), _ptr(y), rows, nf, _ptr(qs), _ptr(ds), rows_pad,
+    yp = _ptr(y) if y is not None else ctypes.c_void_p(0)
+    return _launch("swiglu_quant", (_ptr(gate), _ptr(up), yp, rows, nf, _ptr(qs), _ptr(ds), rows_pad,
                                     _stream(stream)), bind)
 
 

@@ -137,7 +137,7 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
                     o.y = __fmul_rn(__fmul_rn(v[j].y, scale), wv.y);
                     o.z = __fmul_rn(__fmul_rn(v[j].z, scale), wv.z);
                     o.w = __fmul_rn(__fmul_rn(v[j].w, scale), wv.w);
-                    yr[f] = o;
+                    if (y) yr[f] = o;  // mode 2 (y == NULL): the f32 output is dead, only the plane is written
                 }
                 const q8::Q8Enc e = q8::q8_encode8(o);
                 if (ok) {
@@ -193,7 +193,7 @@ swiglu_quant_kernel(const float4 *__restrict__ g, const float4 *__restrict__ u, 
                 o.y = silu_mul(gv[k].y, uv[k].y);
                 o.z = silu_mul(gv[k].z, uv[k].z);
                 o.w = silu_mul(gv[k].w, uv[k].w);
-                y[f] = o;
+                if (y) y[f] = o;  // mode 2 (y == NULL): the f32 output is dead, only the plane is written
             }
             const q8::Q8Enc e = q8::q8_encode8(o);
             if (f < n4_total) {
@@ -240,11 +240,11 @@ extern "C" int quantize_q8_0(const float *x, int64_t rows, int64_t k, int8_t *qs
 extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y, int64_t rows, int64_t d,
                              int8_t *qs, uint32_t *ds, int64_t rows_pad, void *stream)
 {
-    if (rows > 0 && (!x || !w || !y)) return Q8_ERR_ARG;
+    if (rows > 0 && (!x || !w)) return Q8_ERR_ARG;  // y may be NULL (mode 2)
     int st = check_plane_args(rows, d, qs, ds, rows_pad);
     if (st != Q8_OK) return st;
     if (d > 32768) return Q8_ERR_ARG;  // row held in registers: at most 16 float4 x 512 threads
-    if (rows > 0 && (!q8::aligned16(x) || !q8::aligned16(w) || !q8::aligned16(y))) return Q8_ERR_ALIGN;
+    if (rows > 0 && (!q8::aligned16(x) || !q8::aligned16(w) || (y && !q8::aligned16(y)))) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     const int F = static_cast<int>(d / 4);
     int J = 1;
@@ -271,10 +271,10 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
 extern "C" int swiglu_quant(const float *gate, const float *up, float *y, int64_t rows, int64_t nf, int8_t *qs,
                             uint32_t *ds, int64_t rows_pad, void *stream)
 {
-    if (rows > 0 && (!gate || !up || !y)) return Q8_ERR_ARG;
+    if (rows > 0 && (!gate || !up)) return Q8_ERR_ARG;  // y may be NULL (mode 2)
     int st = check_plane_args(rows, nf, qs, ds, rows_pad);
     if (st != Q8_OK) return st;
-    if (rows > 0 && (!q8::aligned16(gate) || !q8::aligned16(up) || !q8::aligned16(y))) return Q8_ERR_ALIGN;
+    if (rows > 0 && (!q8::aligned16(gate) || !q8::aligned16(up) || (y && !q8::aligned16(y)))) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     const int64_t n4_valid = rows * nf / 4, n4_total = rows_pad * nf / 4;
     return q8::launch_pdl(swiglu_quant_kernel, dim3(flat_grid(n4_total, 2)), dim3(kQuantThreads), 0,

@@ -6,7 +6,9 @@ producers (quantization is a pure function of the f32 bits, "54 - r51 -
 producer-fused A-quantize mode 1", sec. 2.3).  Planes are pre-poisoned so
 an unwritten byte (notably in the zero tail) shows up (sec. 4 of the same
 page).  Shapes include the page's verifier set: nt = 1/63/64/129/3354 at
-d = 3584, d = 896 nt = 300, d = 640 nt = 100, and nf = 18944.
+d = 3584, d = 896 nt = 300, d = 640 nt = 100, and nf = 18944.  Every fused
+shape also runs in mode 2 (no f32 output), whose plane must be the mode-1
+plane byte for byte.
 """
 import numpy as np
 import pytest
@@ -80,6 +82,11 @@ def test_rmsnorm_quant(q8, rows, d, rows_pad):
     q8.quantize_q8_0(y, qs2, ds2)
     q8.q8_check()
     assert torch.equal(qs, qs2) and torch.equal(ds, ds2)
+    # mode 2 (no f32 output): the same plane, byte for byte
+    qs3, ds3 = poisoned_plane(rows_pad, d)
+    q8.rmsnorm_quant(dev(x), dev(w), eps, None, qs3, ds3)
+    q8.q8_check()
+    assert torch.equal(qs, qs3) and torch.equal(ds, ds3)
 
 
 def test_rmsnorm_quant_zero_row(q8):
@@ -116,6 +123,11 @@ def test_swiglu_quant(q8, rows, nf, rows_pad):
     q8.quantize_q8_0(y, qs2, ds2)
     q8.q8_check()
     assert torch.equal(qs, qs2) and torch.equal(ds, ds2)
+    # mode 2 (no f32 output): the same plane, byte for byte
+    qs3, ds3 = poisoned_plane(rows_pad, nf)
+    q8.swiglu_quant(dev(gate), dev(up), None, qs3, ds3)
+    q8.q8_check()
+    assert torch.equal(qs, qs3) and torch.equal(ds, ds3)
 
 
 def test_quantizers_are_deterministic(q8):
