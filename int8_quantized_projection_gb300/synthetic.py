@@ -56,6 +56,40 @@ def q8_0_weights(g: np.random.Generator, n: int, k: int, scale_lo: float = 0.002
     return pack_q8_0(d16, q), d16, q
 
 
+Q4A_BLK_BYTES = 20  # asymmetric 4-bit block: f16 d, f16 m, 16 bytes of nibbles
+
+
+def pack_q4a(d16_bits: np.ndarray, m16_bits: np.ndarray, nib: np.ndarray) -> np.ndarray:
+    """Lay out (f16 d bits [n][nb], f16 m bits [n][nb], nibbles 0..15 [n][nb*32]) as n rows
+    of nb 20-byte asymmetric blocks: d at +0, m at +2, then byte j (j < 16) holds element
+    j in its low nibble and element j + 16 in its high nibble."""
+    n, nb = d16_bits.shape
+    assert m16_bits.shape == (n, nb) and nib.shape == (n, nb * QK)
+    v = np.asarray(nib, dtype=np.uint8).reshape(n, nb, QK)
+    assert int(v.max(initial=0)) <= 15
+    out = np.empty((n, nb, Q4A_BLK_BYTES), dtype=np.uint8)
+    out[:, :, 0:2] = np.ascontiguousarray(d16_bits.astype("<u2")).view(np.uint8).reshape(n, nb, 2)
+    out[:, :, 2:4] = np.ascontiguousarray(m16_bits.astype("<u2")).view(np.uint8).reshape(n, nb, 2)
+    out[:, :, 4:] = v[:, :, :16] | (v[:, :, 16:] << 4)
+    return out.reshape(-1)
+
+
+def q4a_weights(g: np.random.Generator, n: int, k: int, scale_lo: float = 0.001, scale_hi: float = 0.01):
+    """Random asymmetric 4-bit weight matrix: (blob, f16 d bits, f16 m bits, nibbles [n][k]).
+
+    d ~ U(scale_lo, scale_hi); m = d * U(0, 15) so that a block's values d*nib - m span
+    an interval around zero (as an asymmetric min/max fit of roughly centred weights
+    does); nibbles uniform in 0..15."""
+    assert k % QK == 0
+    nb = k // QK
+    d = g.uniform(scale_lo, scale_hi, size=(n, nb)).astype(np.float32)
+    m = (d * g.uniform(0.0, 15.0, size=(n, nb))).astype(np.float32)
+    d16 = d.astype(np.float16).view(np.uint16)
+    m16 = m.astype(np.float16).view(np.uint16)
+    nib = g.integers(0, 16, size=(n, k), dtype=np.int64).astype(np.uint8)
+    return pack_q4a(d16, m16, nib), d16, m16, nib
+
+
 def activations(g: np.random.Generator, rows: int, k: int, sigma: float = 1.0,
                 outlier_frac: float = 0.0, outlier_mult: float = 20.0) -> np.ndarray:
     """f32 ~N(0, sigma) [rows][k]; ``outlier_frac`` of the elements multiplied by ``outlier_mult``."""

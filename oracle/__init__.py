@@ -63,6 +63,7 @@ def _load():
         lib.oracle_swiglu.argtypes = [P, P, I64, P]
         lib.oracle_gemm.argtypes = [P, I64, I64, P, P, P, I64, P, I64, P, P]
         lib.oracle_block_dots.argtypes = [P, I64, I64, P, I64, P]
+        lib.oracle_q4a_gemm.argtypes = [P, I64, I64, P, P, P, I64, P, I64, P, P]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -164,6 +165,37 @@ def gemm(w_blob, n: int, k: int, qs, ds, t_idx=None, n_idx=None):
     _load().oracle_gemm(_ptr(w_blob), n, k, _ptr(qs), _ptr(ds), _ptr(t_idx), t_idx.size,
                         _ptr(n_idx), n_idx.size, _ptr(y), _ptr(a))
     return y, a
+
+
+Q4A_BLK_BYTES = 20  # f16 d, f16 m, 16 bytes of nibbles
+
+
+def q4a_gemm(w_blob, n: int, k: int, qs, ds, t_idx=None, n_idx=None):
+    """fp64 y[t][n] for asymmetric 4-bit weight blocks (value d*nib - m) and
+    absum = sum_b (|d*d_a*isum_b| + |m*d_a*ssum_b|).
+
+    ``w_blob`` holds n rows of k/32 20-byte blocks; the rest as in :func:`gemm`.
+    """
+    w_blob = _c(w_blob, np.uint8)
+    qs = _c(qs, np.int8)
+    ds = _c(ds, np.uint32)
+    assert k % QK == 0 and w_blob.size == n * (k // QK) * Q4A_BLK_BYTES
+    assert qs.shape[1] == k and ds.shape[1] == k // QK
+    t_idx = np.arange(qs.shape[0], dtype=np.int64) if t_idx is None else _c(t_idx, np.int64)
+    n_idx = np.arange(n, dtype=np.int64) if n_idx is None else _c(n_idx, np.int64)
+    assert t_idx.size == 0 or (t_idx.min() >= 0 and t_idx.max() < qs.shape[0])
+    assert n_idx.size == 0 or (n_idx.min() >= 0 and n_idx.max() < n)
+    y = np.empty((t_idx.size, n_idx.size), dtype=np.float64)
+    a = np.empty((t_idx.size, n_idx.size), dtype=np.float64)
+    _load().oracle_q4a_gemm(_ptr(w_blob), n, k, _ptr(qs), _ptr(ds), _ptr(t_idx), t_idx.size,
+                            _ptr(n_idx), n_idx.size, _ptr(y), _ptr(a))
+    return y, a
+
+
+def q4a_gemv(w_blob, n: int, k: int, qs, ds, n_idx=None):
+    """Batch-1 form of :func:`q4a_gemm` (plane row 0): returns (y[n], absum[n])."""
+    y, a = q4a_gemm(w_blob, n, k, qs, ds, t_idx=np.zeros(1, np.int64), n_idx=n_idx)
+    return y[0], a[0]
 
 
 def gemv(w_blob, n: int, k: int, qs, ds, n_idx=None):

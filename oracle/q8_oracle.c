@@ -23,7 +23,8 @@
  *          am/127, q = rint(e*di), clamp; swiglu: g/(1+exp(-g))*u).
  *   [R56]  "12 - r5-r6 re-ranking + structural rewrite spec"
  *          (yusiwen.cn/minfer): sec. 2 / 3.1 (q8_0 activation x Q8_0-style
- *          weight blocks contracted with per-block scales).
+ *          weight blocks contracted with per-block scales; the q4_K weight
+ *          value d*s*nib - dmin*m, whose min term the plane's ssum serves).
  *
  * Readings where the pages are silent or disagree (each is listed in
  * the design doc):
@@ -35,6 +36,9 @@
  *   - ds word = f16 bits of d in bits 0..15, int16 ssum in bits 16..31.
  *   - RMSNorm, SwiGLU and the contraction are evaluated in fp64 ("truth"),
  *     not as models of any GPU instruction.
+ *   - asymmetric 4-bit blocks: one f16 scale and one f16 min per 32 elements
+ *     (the q4_K super-block packing is left out), nibble j < 16 in the low
+ *     half of byte j, nibble j >= 16 in the high half of byte j - 16.
  *
  * Parity pins (tests/test_oracle_pins.py): exhaustive f32->f16 against numpy,
  * half-even ties, the round-trip bound |x - q*d| <= d/2 (+ f32 slack), the
@@ -294,6 +298,72 @@ void oracle_block_dots(const uint8_t *w, int64_t n, int64_t k,
             for (int64_t b = 0; b < nb; b++)
                 isum[(i * n + j) * nb + b] =
                     block_dot(w + j * pitch + b * WBLK_BYTES, qs + i * k + b * QK);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Asymmetric 4-bit weight blocks x q8_0 activations: the consumer of ssum    */
+/*                                          [R51 2.1; R56 sec. 2, q4_K value] */
+/* ------------------------------------------------------------------------ */
+
+/* A 32-element asymmetric weight block, 20 bytes: little-endian f16 d at +0,
+ * f16 m at +2, 16 bytes of unsigned nibbles at +4.  Element j (0..31) is
+ * nib_j = low nibble of byte j for j < 16, high nibble of byte j - 16 for
+ * j >= 16, and its value is d * nib_j - m: the pages' q4_K value form
+ * d*s*nib - dmin*m with the two-level (super-block, sub-block) scales folded
+ * into one f16 scale and one f16 min per 32-element block.                 */
+#define A4BLK_BYTES 20
+
+static inline int a4_nib(const uint8_t *blk, int j)
+{
+    const uint8_t b = blk[4 + (j & 15)];
+    return j < 16 ? (b & 15) : (b >> 4);
+}
+
+static inline float a4_half(const uint8_t *p)
+{
+    return oracle_f16_to_f32((uint16_t)(p[0] | ((uint16_t)p[1] << 8)));
+}
+
+/* y[i][j] = sum_b sum_e (d*nib_e - m) * (d_a*q_e) for weight row n_idx[j] and
+ * token t_idx[i].  Per block, as the pages' min-term correction does:
+ *     d * d_a * sum_e nib_e*q_e  -  m * d_a * ssum,
+ * with ssum = sum_e q_e taken from the plane (its int16 field) instead of a
+ * second dot product.  Both terms are exact in fp64 (11+11+16 and 11+11+13
+ * significant bits); absum gets the sum of their magnitudes.              */
+void oracle_q4a_gemm(const uint8_t *w, int64_t n, int64_t k,
+                     const int8_t *qs, const uint32_t *ds,
+                     const int64_t *t_idx, int64_t nt,
+                     const int64_t *n_idx, int64_t nn,
+                     double *y, double *absum)
+{
+    int64_t nb = k / QK;
+    int64_t pitch = nb * A4BLK_BYTES;
+    (void)n;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nt; i++) {
+        int64_t t = t_idx[i];
+        for (int64_t j = 0; j < nn; j++) {
+            const uint8_t *wr = w + n_idx[j] * pitch;
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t b = 0; b < nb; b++) {
+                const uint8_t *blk = wr + b * A4BLK_BYTES;
+                const int8_t *qa = qs + t * k + b * QK;
+                int32_t isum = 0;
+                for (int e = 0; e < QK; e++)
+                    isum += (int32_t)a4_nib(blk, e) * (int32_t)qa[e];
+                uint32_t dsw = ds[t * nb + b];
+                int16_t ssum = (int16_t)(uint16_t)(dsw >> 16);
+                double da = (double)plane_d(dsw);
+                double t1 = (double)a4_half(blk) * da * (double)isum;
+                double t2 = (double)a4_half(blk + 2) * da * (double)ssum;
+                acc += t1;
+                acc -= t2;
+                aacc += fabs(t1) + fabs(t2);
+            }
+            y[i * nn + j] = acc;
+            absum[i * nn + j] = aacc;
+        }
+    }
 }
 
 int oracle_num_threads(void)

@@ -306,6 +306,91 @@ def test_weight_layout_round_trip():
 
 
 # --------------------------------------------------------------------------
+# Asymmetric 4-bit weight blocks (value d*nib - m) and the ssum min term
+# --------------------------------------------------------------------------
+
+def test_q4a_block_layout_literal():
+    # d = 1.0 (f16 0x3C00), m = 2.0 (0x4000), element j = j % 16: byte j (j < 16)
+    # holds element j in its low nibble and element j + 16 in its high nibble
+    d16 = np.array([[0x3C00]], np.uint16)
+    m16 = np.array([[0x4000]], np.uint16)
+    nib = (np.arange(32) % 16).astype(np.uint8).reshape(1, 32)
+    blob = syn.pack_q4a(d16, m16, nib)
+    expect = bytes([0x00, 0x3C, 0x00, 0x40] + [0x11 * j for j in range(16)])
+    assert blob.tobytes() == expect
+
+
+def _q4a_exact(d16, m16, nib, qa, da16, i, j, k):
+    """Exact rational sum over the elements of (d*nib - m) * (d_a*q), from the
+    dequantized values themselves (no block sums, no ssum identity)."""
+    h = lambda bits: Fraction(float(np.array([bits], np.uint16).view(np.float16)[0]))
+    tot = Fraction(0)
+    for e in range(k):
+        b = e // 32
+        wv = h(d16[j, b]) * int(nib[j, e]) - h(m16[j, b])
+        tot += wv * h(da16[i, b]) * int(qa[i, e])
+    return tot
+
+
+def test_q4a_exact_rational_small():
+    g = syn.rng(96, 1)
+    n, k, t = 5, 160, 3
+    blob, d16, m16, nib = syn.q4a_weights(g, n, k)
+    qa = g.integers(-127, 128, size=(t, k)).astype(np.int8)
+    qa[0, :32] = 0           # a zero activation block (ssum = 0)
+    qa[1, 32:64] = -127      # a saturated one (ssum = -4064)
+    da16 = g.uniform(1e-3, 5e-2, size=(t, k // 32)).astype(np.float16).view(np.uint16)
+    qs, ds = _plane_from(qa, da16)
+    y, a = oracle.q4a_gemm(blob, n, k, qs, ds)
+    for i in range(t):
+        for j in range(n):
+            exact = _q4a_exact(d16, m16, nib, qa, da16, i, j, k)
+            assert abs(Fraction(y[i, j]) - exact) <= Fraction(a[i, j]) * Fraction(1, 2 ** 48)
+
+
+def test_q4a_zero_min_is_the_q8_0_contraction():
+    # m = 0: the block is d*nib, i.e. a Q8_0 block with codes nib and the same d
+    g = syn.rng(96, 2)
+    n, k = 7, 256
+    _, d16, _, nib = syn.q4a_weights(g, n, k)
+    blob4 = syn.pack_q4a(d16, np.zeros_like(d16), nib)
+    blob8 = syn.pack_q8_0(d16, nib.astype(np.int8))
+    qs, ds = oracle.quantize(syn.activations(g, 4, k))
+    y4, a4 = oracle.q4a_gemm(blob4, n, k, qs, ds)
+    y8, a8 = oracle.gemm(blob8, n, k, qs, ds)
+    assert np.array_equal(y4, y8) and np.array_equal(a4, a8)
+
+
+def test_q4a_constant_weights_reduce_to_the_activation_sum():
+    # nib = 0 everywhere: every weight is -m, so y = -m * sum_e xhat_e, a plain
+    # sum of the dequantized activation (numpy fp64 over exact products)
+    g = syn.rng(96, 3)
+    n, k, t = 3, 128, 2
+    d16 = np.full((n, k // 32), 0x2000, np.uint16)           # 2^-7
+    m16 = np.array([[0x3800], [0x3C00], [0x4000]], np.uint16).repeat(k // 32, 1)  # 0.5, 1, 2
+    blob = syn.pack_q4a(d16, m16, np.zeros((n, k), np.uint8))
+    qs, ds = oracle.quantize(syn.activations(g, t, k))
+    y, _ = oracle.q4a_gemm(blob, n, k, qs, ds)
+    da = (ds & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64)
+    xhat = qs.astype(np.float64) * np.repeat(da, 32, axis=1)
+    for j, mv in enumerate((0.5, 1.0, 2.0)):
+        np.testing.assert_allclose(y[:, j], -mv * xhat.sum(axis=1), rtol=1e-13, atol=1e-13)
+
+
+def test_q4a_sampling_and_gemv_match_full():
+    g = syn.rng(96, 4)
+    n, k = 30, 256
+    blob, _, _, _ = syn.q4a_weights(g, n, k)
+    qs, ds = oracle.quantize(syn.activations(g, 5, k))
+    y, a = oracle.q4a_gemm(blob, n, k, qs, ds)
+    ti, ni = np.array([4, 0]), np.array([29, 3, 11])
+    ys, as_ = oracle.q4a_gemm(blob, n, k, qs, ds, t_idx=ti, n_idx=ni)
+    assert np.array_equal(ys, y[np.ix_(ti, ni)]) and np.array_equal(as_, a[np.ix_(ti, ni)])
+    yv, av = oracle.q4a_gemv(blob, n, k, qs, ds)
+    assert np.array_equal(yv, y[0]) and np.array_equal(av, a[0])
+
+
+# --------------------------------------------------------------------------
 # Byte accounts printed on the pages (tests/golden/page_byte_accounts.json)
 # --------------------------------------------------------------------------
 
