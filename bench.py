@@ -355,6 +355,41 @@ def run_small(torch, q8p, steps, warmup, dev):
 
 
 # ---------------------------------------------------------------------------
+# asymmetric 4-bit weights (value d*nib - m), batch 1: the ssum consumer
+# ---------------------------------------------------------------------------
+ASYM = {"n": 12288, "k": 7168}
+
+
+def bytes_q4a_gemv(n, k):
+    return n * (k // 32) * 20 + k + 4 * (k // 32) + 4 * n
+
+
+def run_asym(torch, q8p, steps, warmup, dev):
+    n, k = ASYM["n"], ASYM["k"]
+    w_h = syn.q4a_weights(syn.rng(5, 1), n, k)[0]
+    copies = max(2, -(-4 * L2_BYTES // w_h.nbytes))
+    ws = [torch.from_numpy(w_h).to(dev) for _ in range(copies)]
+    x = torch.from_numpy(syn.activations(syn.rng(5, 0), 1, k, sigma=1.5, outlier_frac=0.01)).to(dev)
+    plane = q8p.empty_plane(1, k, dev)
+    q8p.quantize_q8_0(x, *plane)
+    y = torch.empty(n, dtype=torch.float32, device=dev)
+    calls = [q8p.q4a_gemv(w, n, k, *plane, y, bind=True) for w in ws]
+    for i in range(warmup):
+        calls[i % copies]()
+    q8p.q8_check()
+    stream = torch.cuda.current_stream(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        evs[i][0].record(stream)
+        calls[(warmup + i) % copies]()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    q8p.q8_check()
+    return dict(us=1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs), copies=copies)
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle (reported baseline and the reference arm)
 # ---------------------------------------------------------------------------
 def oracle_decode_sample(budget_s):
@@ -437,7 +472,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "small"],
+    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "small", "asym"],
                     help="decode and/or prefill legs (profiling runs select one)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()
@@ -487,6 +522,11 @@ def main():
     if args.workload in ("all", "small"):
         small = run_small(torch, q8p, args.steps if dec is None and pre is None else max(20, args.steps // 30),
                           args.warmup, dev)
+
+    asym = None
+    if args.workload in ("all", "asym"):
+        asym = run_asym(torch, q8p, args.steps if args.workload == "asym" else max(20, args.steps // 30),
+                        args.warmup, dev)
 
     if rank != 0:
         if world > 1:
@@ -557,6 +597,21 @@ def main():
                          "config": {"workload": sobj["workload"], "l2": sobj["l2"], "parallelism": "replicas"},
                          "roofline": sobj["roofline"], "gpu_launches": args.steps})
         line["small_batch"] = sobj
+    if asym is not None:
+        n, k = ASYM["n"], ASYM["k"]
+        gbs = bytes_q4a_gemv(n, k) / (asym["us"] / 1e6) / 1e9
+        aobj = {"workload": f"asymmetric 4-bit weights (d*nib - m, min term from the plane's ssum): q4a_gemv "
+                            f"{n}x{k}, batch 1",
+                "us_per_call": round(asym["us"], 2), "gbs": round(gbs, 1),
+                "roofline": {"kernel": "q4a_gemv (q4a_gemv_kernel)", "bound": "hbm", "achieved": round(gbs, 1),
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                             "traffic": None, "algorithmic_bytes": bytes_q4a_gemv(n, k)},
+                "l2": f"weights rotate through {asym['copies']} copies (> 4 x L2)"}
+        if args.workload == "asym":
+            line.update({"value": aobj["gbs"], "unit": "GB/s", "ms_per_step": round(asym["us"] / 1e3, 5),
+                         "config": {"workload": aobj["workload"], "l2": aobj["l2"], "parallelism": "replicas"},
+                         "roofline": aobj["roofline"], "gpu_launches": args.steps})
+        line["asym_gemv"] = aobj
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

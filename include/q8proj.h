@@ -187,6 +187,30 @@ Q8_API int q8_0_gemv_batched(const void *w, int64_t n, int64_t k,
                              float *y, void *stream);
 
 /*
+ * q4a_gemv -- batch-1 projection with asymmetric 4-bit weight blocks, the
+ * consumer of the plane's int16 block sums:
+ *     y[i] = sum_b ( d*d_a * sum_e nib_e*q_e  -  m*d_a * ssum_b ).
+ * The weight value d*nib - m is the q4_K form d*s*nib - dmin*m of "12 - r5-r6
+ * re-ranking + structural rewrite spec" (sec. 3) with one f16 scale and one
+ * f16 min per 32 elements, and its min term takes the plane's ssum instead
+ * of a second dot product, the use "54 - r51 - producer-fused A-quantize
+ * mode 1" (sec. 2.1) gives the int16 field.
+ *   w      : n rows of k/32 20-byte blocks (input, 16-byte aligned): f16 d at
+ *            +0, f16 m at +2, then byte j (j < 16) holds element j in its low
+ *            nibble and element j + 16 in its high nibble (unsigned 0..15).
+ *   qs, ds : plane row 0 (input; only row 0 is read)
+ *   y      : f32 [n] (output)
+ * n >= 1, k % 128 == 0 (16-byte aligned rows of whole 4-block chunks),
+ * k <= 206592 (the activation is staged in shared memory).  Per block two
+ * fmas, d*d_a*isum then -m*d_a*ssum (both scale products exact in f32); the
+ * split of a row over lanes depends on k only: results are run-to-run
+ * identical.  Programmatic dependent launch: the plane is read only after the
+ * kernel enqueued before it on `stream` has finished.
+ */
+Q8_API int q4a_gemv(const void *w, int64_t n, int64_t k,
+                    const int8_t *qs, const uint32_t *ds, float *y, void *stream);
+
+/*
  * q8_0_gemm_workspace_bytes -- device workspace q8_0_gemm needs for t tokens
  * of width k: t*k*2 bytes (the activation's codes as f16); 0 when
  * (k/32) % 8 != 0 or t <= Q8_GEMV_MAX_TOKENS (those calls need none).

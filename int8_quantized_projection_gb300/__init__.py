@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     q8_0_gemv,
     q8_0_gemv_grouped,
     q8_0_gemv_batched,
+    q4a_gemv,
     GEMV_MAX_TOKENS,
     q8_check,
     q8_num_sms,

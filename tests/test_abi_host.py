@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
     # and nothing else of ours leaks (kernels and helpers are hidden)
     out = os.popen(f"nm -D --defined-only {build.LIB}").read().split("\n")
-    ours = {ln.split()[-1] for ln in out if ln.strip() and ln.split()[-1].startswith(("q8", "quantize", "rmsnorm",
+    ours = {ln.split()[-1] for ln in out if ln.strip() and ln.split()[-1].startswith(("q8", "q4a", "quantize", "rmsnorm",
                                                                                        "swiglu"))}
     assert ours == set(declared_symbols())
 
@@ -91,6 +91,10 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert lib.q8_0_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 17, P(FAKE), s) == ERR_ARG
     assert lib.q8_0_gemv_batched(P(FAKE), 8, 100, P(FAKE), P(FAKE), 4, P(FAKE), s) == ERR_ARG
     assert lib.q8_0_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 4, P(MISALIGNED), s) == ERR_ALIGN
+    # q4a_gemv: k % 128, n < 1, alignment
+    assert lib.q4a_gemv(P(FAKE), 8, 96, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
+    assert lib.q4a_gemv(P(FAKE), 0, 256, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
+    assert lib.q4a_gemv(P(FAKE + 4), 8, 256, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ALIGN
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):

@@ -1,0 +1,116 @@
+"""GPU parity of q4a_gemv (asymmetric 4-bit weight blocks, value d*nib - m)
+against the oracle.
+
+Per block the kernel adds d*d_a*isum and -m*d_a*ssum, the min term taken from
+the plane's int16 block sum ("54 - r51 - producer-fused A-quantize mode 1",
+sec. 2.1).  Outputs are NaN-poisoned first and compared with the oracle's
+fp64 value within 1e-5 * sum_b (|d*d_a*isum| + |m*d_a*ssum|); the
+exact-epilogue configuration (power-of-two scales and mins, small codes:
+every f32 operation exact in any order) requires bit equality, which checks
+the nibble unpacking, the dp4a pairing of nibble halves with activation words
+and the sign and source of the min term.  Shapes cover one chunk per row
+(k = 128, 32 rows per warp), ragged row counts, rows spanning several lanes'
+chunk pairs and an odd trailing chunk, and the full-size decode projection.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from int8_quantized_projection_gb300 import synthetic as syn
+
+from ._parity import assert_gemm_close, dev, host, nan_f32
+
+pytestmark = pytest.mark.gpu
+
+
+def _weights(seed, n, k, exact=False):
+    g = syn.rng(80, seed, n, k)
+    blob, d16, m16, nib = syn.q4a_weights(g, n, k)
+    if exact:
+        e = g.integers(-4, -1, size=d16.shape)
+        d16 = (2.0 ** e).astype(np.float16).view(np.uint16)
+        em = g.integers(-3, 0, size=m16.shape)
+        m16 = (2.0 ** em).astype(np.float16).view(np.uint16)
+        blob = syn.pack_q4a(d16, m16, nib)
+    return blob
+
+
+def _plane(seed, k, exact=False):
+    g = syn.rng(81, seed, k)
+    if exact:
+        qa = g.integers(-3, 4, size=(1, k)).astype(np.int8)
+        e = g.integers(-4, -1, size=(1, k // 32))
+        d16 = (2.0 ** e).astype(np.float16).view(np.uint16)
+        ssum = qa.reshape(1, k // 32, 32).astype(np.int64).sum(-1)
+        ds = d16.astype(np.uint32) | (ssum.astype(np.int16).view(np.uint16).astype(np.uint32) << 16)
+        return qa, ds
+    return oracle.quantize(syn.activations(g, 1, k, sigma=1.5, outlier_frac=0.01))
+
+
+def _run(q8, blob, n, k, qs, ds):
+    y = nan_f32(n)
+    q8.q4a_gemv(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), y)
+    q8.q8_check()
+    return y
+
+
+SHAPES = [
+    (256, 128),      # one chunk per row: 32 rows per warp
+    (1000, 512),     # 4 chunks per row
+    (333, 1152),     # 9 chunks: lane pairs plus an odd trailing chunk
+    (1001, 2048),    # 16 chunks, ragged n
+    (77, 18944),     # 148 chunks: rows spanning many chunk pairs
+    (3, 256), (1, 128),
+    (4099, 7168),    # ragged n, 56 chunks
+    (12288, 7168),   # full-size decode projection
+]
+
+
+@pytest.mark.parametrize("n,k", SHAPES)
+def test_q4a_gemv_matches_oracle(q8, n, k):
+    blob = _weights(1, n, k)
+    qs, ds = _plane(1, k)
+    y = _run(q8, blob, n, k, qs, ds)
+    yr, ar = oracle.q4a_gemv(blob, n, k, qs, ds)
+    assert_gemm_close(host(y), yr, ar, f"q4a_gemv {n}x{k}")
+
+
+@pytest.mark.parametrize("n,k", [(300, 2048), (77, 18944), (512, 128), (129, 7168)])
+def test_q4a_gemv_exact_epilogue_bit_equal(q8, n, k):
+    blob = _weights(2, n, k, exact=True)
+    qs, ds = _plane(2, k, exact=True)
+    y = _run(q8, blob, n, k, qs, ds)
+    yr, _ = oracle.q4a_gemv(blob, n, k, qs, ds)
+    assert np.array_equal(host(y).astype(np.float64), yr)
+
+
+def test_q4a_gemv_deterministic(q8):
+    import torch
+
+    n, k = 12288, 7168
+    blob = dev(_weights(3, n, k))
+    qs, ds = _plane(3, k)
+    qs, ds = dev(qs), dev(ds.view(np.int32))
+    outs = []
+    for _ in range(3):
+        y = nan_f32(n)
+        q8.q4a_gemv(blob, n, k, qs, ds, y)
+        q8.q8_check()
+        outs.append(y.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+def test_q4a_decode_chain_from_the_gpu_plane(q8):
+    """quantize_q8_0 on the GPU, then q4a_gemv on that plane: the oracle applied to the
+    GPU's own plane (itself checked bit-exact elsewhere) agrees."""
+    n, k = 3584, 18944
+    g = syn.rng(82, 0)
+    x = syn.activations(g, 1, k)
+    qs, ds = q8.empty_plane(1, k)
+    q8.quantize_q8_0(dev(x), qs, ds)
+    blob = _weights(4, n, k)
+    y = nan_f32(n)
+    q8.q4a_gemv(dev(blob), n, k, qs, ds, y)
+    q8.q8_check()
+    yr, ar = oracle.q4a_gemv(blob, n, k, host(qs), host(ds).view(np.uint32))
+    assert_gemm_close(host(y), yr, ar, "q4a decode chain")
