@@ -65,11 +65,46 @@ __device__ __forceinline__ float a4_chunk(const uint32_t (&wv)[kA4ChunkWords], c
     return acc;
 }
 
+// Load chunks c and c + lpr of a row (zeros where invalid).
+__device__ __forceinline__ void a4_load_pair(const uint4 *__restrict__ wr, int c, int lpr, bool v0, bool v1,
+                                             uint32_t (&p0)[kA4ChunkWords], uint32_t (&p1)[kA4ChunkWords])
+{
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        const uint4 a = v0 ? ld_stream4(wr + c * 5 + i) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 b = v1 ? ld_stream4(wr + (c + lpr) * 5 + i) : make_uint4(0u, 0u, 0u, 0u);
+        p0[4 * i] = a.x; p0[4 * i + 1] = a.y; p0[4 * i + 2] = a.z; p0[4 * i + 3] = a.w;
+        p1[4 * i] = b.x; p1[4 * i + 1] = b.y; p1[4 * i + 2] = b.z; p1[4 * i + 3] = b.w;
+    }
+}
+
 __global__ void __launch_bounds__(kA4Threads)
 q4a_gemv_kernel(const uint4 *__restrict__ w, int64_t n, int nc, const uint4 *__restrict__ qs,
                 const uint4 *__restrict__ ds4, float *__restrict__ y, int lpr_log2)
 {
     extern __shared__ __align__(16) uint8_t act[];
+    const int lane = threadIdx.x & 31;
+    const int lpr = 1 << lpr_log2, rpw = 32 >> lpr_log2;
+    const int ri = lane >> lpr_log2, cj = lane & (lpr - 1);
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t groups = (n + rpw - 1) / rpw;
+    const int64_t pitch4 = static_cast<int64_t>(nc) * 5;  // row pitch in 16-byte units
+    const int nsteps = (nc + 2 * lpr - 1) / (2 * lpr);    // chunk pairs per row, the same for every lane
+
+    // A warp walks (row group, step) items; each step is one pair of chunks
+    // per lane, held in p0/p1 and loaded one item ahead.  The weights do not
+    // depend on the previous kernel in the stream, so the first item is loaded
+    // before waiting for it and before the activation is staged
+    // (programmatic dependent launch).
+    uint32_t p0[kA4ChunkWords], p1[kA4ChunkWords];
+    auto load_item = [&](int64_t G, int step) {
+        const int64_t row = G * rpw + ri;
+        const int c = cj + 2 * lpr * step;
+        const bool v0 = G < groups && row < n && c < nc;
+        a4_load_pair(w + (v0 ? row : 0) * pitch4, c, lpr, v0, v0 && c + lpr < nc, p0, p1);
+    };
+    load_item(warp, 0);
     q8::griddep_launch_dependents();
     q8::griddep_wait();  // the plane may come from the previous kernel
     for (int idx = threadIdx.x; idx < nc * 9; idx += blockDim.x) {
@@ -79,44 +114,28 @@ q4a_gemv_kernel(const uint4 *__restrict__ w, int64_t n, int nc, const uint4 *__r
     }
     __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int lpr = 1 << lpr_log2, rpw = 32 >> lpr_log2;
-    const int ri = lane >> lpr_log2, cj = lane & (lpr - 1);
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t groups = (n + rpw - 1) / rpw;
-    const int64_t pitch4 = static_cast<int64_t>(nc) * 5;  // row pitch in 16-byte units
-    for (int64_t G = warp; G < groups; G += nwarps) {
+    float acc = 0.0f;
+    int64_t G = warp;
+    int step = 0;
+    while (G < groups) {
         const int64_t row = G * rpw + ri;
-        float acc = 0.0f;
-        if (row < n) {
-            const uint4 *wr = w + row * pitch4;
-            int c = cj;
-            // two chunks per step: ten 16-byte loads in flight per lane
-            for (; c + lpr < nc; c += 2 * lpr) {
-                uint32_t w0[kA4ChunkWords], w1[kA4ChunkWords];
-#pragma unroll
-                for (int i = 0; i < 5; ++i) {
-                    const uint4 a = ld_stream4(wr + c * 5 + i);
-                    const uint4 b = ld_stream4(wr + (c + lpr) * 5 + i);
-                    w0[4 * i] = a.x; w0[4 * i + 1] = a.y; w0[4 * i + 2] = a.z; w0[4 * i + 3] = a.w;
-                    w1[4 * i] = b.x; w1[4 * i + 1] = b.y; w1[4 * i + 2] = b.z; w1[4 * i + 3] = b.w;
-                }
-                acc = a4_chunk(w0, act + c * kA4ActChunk, acc);
-                acc = a4_chunk(w1, act + (c + lpr) * kA4ActChunk, acc);
-            }
-            if (c < nc) {
-                uint32_t w0[kA4ChunkWords];
-#pragma unroll
-                for (int i = 0; i < 5; ++i) {
-                    const uint4 a = ld_stream4(wr + c * 5 + i);
-                    w0[4 * i] = a.x; w0[4 * i + 1] = a.y; w0[4 * i + 2] = a.z; w0[4 * i + 3] = a.w;
-                }
-                acc = a4_chunk(w0, act + c * kA4ActChunk, acc);
-            }
+        const int c = cj + 2 * lpr * step;
+        if (row < n && c < nc) acc = a4_chunk(p0, act + c * kA4ActChunk, acc);
+        if (row < n && c + lpr < nc) acc = a4_chunk(p1, act + (c + lpr) * kA4ActChunk, acc);
+        int64_t Gn = G;
+        int sn = step + 1;
+        if (sn == nsteps) {
+            sn = 0;
+            Gn = G + nwarps;
         }
-        for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(Q8_FULL_MASK, acc, o);
-        if (cj == 0 && row < n) y[row] = acc;
+        load_item(Gn, sn);
+        if (sn == 0) {  // row group complete: reduce over the lanes of each row
+            for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(Q8_FULL_MASK, acc, o);
+            if (cj == 0 && row < n) y[row] = acc;
+            acc = 0.0f;
+        }
+        G = Gn;
+        step = sn;
     }
 }
 
@@ -145,10 +164,16 @@ extern "C" int q4a_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, c
     if (sms <= 0) return Q8_ERR_DEVICE;
     const int64_t warps_per_cta = kA4Threads / 32;
     int64_t grid = (groups + warps_per_cta - 1) / warps_per_cta;
-    const int64_t cap = static_cast<int64_t>(sms) * 4;  // ~32 warps per SM; each CTA stages the activation once
-    grid = grid < cap ? grid : cap;
     if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(q4a_gemv_kernel), 227 * 1024, 5))
         return Q8_ERR_LAUNCH;
+    // one wave of resident CTAs (each stages the activation once), warps walking rows in a grid stride
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q4a_gemv_kernel, kA4Threads, static_cast<size_t>(smem)) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return Q8_ERR_LAUNCH;
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    grid = grid < cap ? grid : cap;
     return q8::launch_pdl(q4a_gemv_kernel, dim3(static_cast<unsigned>(grid)), dim3(kA4Threads),
                           static_cast<size_t>(smem), static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(w), n,
                           static_cast<int>(nc), reinterpret_cast<const uint4 *>(qs),
