@@ -41,11 +41,9 @@ L2_BYTES = 129 * 1000 * 1000
 DECODE_SHAPES = [(12288, 7168), (96, 7168), (512, 128)]
 PREFILL = dict(tokens=3325, d=3584, nf=18944, eps=1e-6)
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
-# kernel from the ncu capture summarised under profiles/ (None until taken,
-# and reset to None whenever that kernel changes).
-# DRAM bytes per launch from one ncu capture of the current kernel; None when
-# the kernel changed after the capture (the figure would describe old code).
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of a kernel, from
+# the ncu capture summarised under profiles/; None until taken, and reset to
+# None whenever that kernel changes (the figure would describe old code).
 NCU_TRAFFIC_BYTES = {"gemv_staged 12288x7168+96x7168": 97_942_016,     # profiles/gemv_staged_12288x7168_plus_96x7168.md
                      "gemm_tc 18944x3584 t=3325": 734_083_584,         # profiles/gemm_tc_18944x3584_t3325.md
                      "gemv_small 12288x7168 t=16": 98_196_736}         # profiles/gemv_small_12288x7168_t16.md
@@ -165,6 +163,15 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": reasons, "samples": len(rows)}
+
+
+def max_over_ranks(torch, values, device):
+    """Element-wise maximum of a list of floats over all ranks (one all-reduce).
+
+    Each replica times its own steps; a job is as slow as its slowest rank."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
 
 
 def gpu_smi_id(torch, dev):
@@ -545,10 +552,6 @@ def main():
     dec = None
     if args.workload in ("all", "decode"):
         dec = run_decode(torch, q8p, args.steps, args.warmup, dev, sampler)
-        if world > 1:
-            t = torch.tensor([dec["ms"], dec["e2e_s"]], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            dec["ms"], dec["e2e_s"] = float(t[0]), float(t[1])
 
     pre = None
     if args.workload == "prefill" or (args.workload == "all" and not args.no_prefill):
@@ -563,6 +566,21 @@ def main():
     if args.workload in ("all", "asym"):
         asym = run_asym(torch, q8p, args.steps if args.workload == "asym" else max(20, args.steps // 30),
                         args.warmup, dev)
+
+    if world > 1:  # every duration becomes the slowest rank's (same legs on every rank)
+        vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"]] if dec else []) + (list(pre.values()) if pre else [])
+                + ([small["us"]] if small else []) + ([asym["us"]] if asym else []))
+        red = max_over_ranks(torch, vals, dev)
+        if dec:
+            dec["ms"], dec["e2e_s"], dec["kern_ms"] = red[:3]
+            red = red[3:]
+        if pre:
+            pre = dict(zip(pre.keys(), red[:len(pre)]))
+            red = red[len(pre):]
+        if small:
+            small["us"] = red.pop(0)
+        if asym:
+            asym["us"] = red.pop(0)
 
     if rank != 0:
         if world > 1:
@@ -612,8 +630,9 @@ def main():
                                                          1)},
             "l2": "step working set ~1.2 GB > L2",
         }
-        if dec is None:  # prefill-only run: the GEMM throughput is the headline
-            line.update({"value": pobj["gemm_tops"], "unit": "TOPS", "ms_per_step": pobj["ms_per_chain"],
+        if dec is None:  # prefill-only run: the GEMM throughput (all replicas) is the headline
+            line.update({"value": round(world * pobj["gemm_tops"], 2), "unit": "TOPS",
+                         "ms_per_step": pobj["ms_per_chain"],
                          "config": {"workload": pobj["workload"], "l2": pobj["l2"], "parallelism": "replicas"},
                          "roofline": pobj["roofline_gemm"], "gpu_launches": 5 * args.steps})
         line["prefill"] = pobj
@@ -629,7 +648,8 @@ def main():
                              "algorithmic_bytes": bytes_small(n, k, t)},
                 "l2": f"weights rotate through {small['copies']} copies (> 4 x L2)"}
         if dec is None and pre is None:
-            line.update({"value": sobj["gbs"], "unit": "GB/s", "ms_per_step": round(small["us"] / 1e3, 5),
+            line.update({"value": round(world * sobj["gbs"], 1), "unit": "GB/s",
+                         "ms_per_step": round(small["us"] / 1e3, 5),
                          "config": {"workload": sobj["workload"], "l2": sobj["l2"], "parallelism": "replicas"},
                          "roofline": sobj["roofline"], "gpu_launches": args.steps})
         line["small_batch"] = sobj
@@ -644,7 +664,8 @@ def main():
                              "traffic": None, "algorithmic_bytes": bytes_q4a_gemv(n, k)},
                 "l2": f"weights rotate through {asym['copies']} copies (> 4 x L2)"}
         if args.workload == "asym":
-            line.update({"value": aobj["gbs"], "unit": "GB/s", "ms_per_step": round(asym["us"] / 1e3, 5),
+            line.update({"value": round(world * aobj["gbs"], 1), "unit": "GB/s",
+                         "ms_per_step": round(asym["us"] / 1e3, 5),
                          "config": {"workload": aobj["workload"], "l2": aobj["l2"], "parallelism": "replicas"},
                          "roofline": aobj["roofline"], "gpu_launches": args.steps})
         line["asym_gemv"] = aobj
