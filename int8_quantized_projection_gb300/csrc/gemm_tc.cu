@@ -20,16 +20,19 @@
 // the tensor core reads -- every weight tile reuses it, instead of converting
 // the same activation in every CTA.
 //
-// One CTA computes a 128 (weight rows) x 256 (tokens) tile over all of k.
+// One CTA computes a 128 (weight rows) x 192 (tokens) tile over all of k.
 // Per 32-wide block two K=16 MMAs produce the exact integer partial P in one
-// of two 256-column TMEM buffers; the epilogue adds (d_w * d_a) * P to f32
-// register accumulators.  Every block needs a round trip between the tensor
-// core and the epilogue (MMA completion -> epilogue -> buffer free); 256-token
-// tiles make each round trip cover twice the tensor work of 128-token tiles.
+// of two TMEM buffers; the epilogue adds (d_w * d_a) * P to f32 register
+// accumulators.  Every block needs a round trip between the tensor core and
+// the epilogue (MMA completion -> epilogue -> buffer free), so tiles are wide
+// (192 tokens); and a TMEM load takes ~130 cycles to land while
+// tcgen05.wait::ld waits for all of a thread's loads, so the epilogue runs
+// three warps per TMEM lane quarter (64 tokens and 64 accumulators each) to
+// hide that latency.
 // The tensor core queues little ahead of the thread issuing to it, so each
 // TMEM buffer has its own issuing thread, and the epilogue is bound by its
 // f32 work (one scale product and one fma per output and block).
-// Warp roles (512 threads; setmaxnreg moves registers to the epilogue):
+// Warp roles (640 threads; setmaxnreg moves registers to the epilogue):
 //   warp 0      TMA producer for raw Q8_0 weight rows (8 blocks per stage)
 //   warp 1      TMEM allocator; MMA issuer (one thread) for the even blocks
 //   warp 2      TMA producer for the prepared activation (2 blocks per stage)
@@ -37,9 +40,9 @@
 //   warps 4-7   converters: one weight row each, raw int8 -> f16 canonical
 //               K-major tile; the block's d_w (row) and d_a (256 tokens, read
 //               from the plane) as f32 into a scale ring
-//   warps 8-15  epilogue: two warps per TMEM lane quarter, 128 tokens each,
-//               read in the 16x256b shape (4 rows x 32 tokens per thread and
-//               block), packed f32x2 multiply/fma, 128 accumulators per thread
+//   warps 8-19  epilogue: three warps per TMEM lane quarter, 64 tokens each,
+//               read in the 16x256b shape (4 rows x 16 tokens per thread and
+//               load), packed f32x2 multiply/fma, 64 accumulators per thread
 // Every mbarrier wait is bounded; a wait that runs out sets the CTA abort
 // flag and the library error word, and all roles drain and exit.
 #include <cuda.h>
@@ -52,30 +55,35 @@ namespace {
 
 __device__ unsigned int g_gemm_err;
 
-constexpr int BM = 128, BN = 256;
+constexpr int BM = 128, BN = 192;
 constexpr int kABlocksPerStage = 8;                // raw weight stage: 8 blocks = 272 bytes per row
 constexpr int kBBlocksPerStage = 2;                // prepared activation stage: 2 blocks = 64 f16 per token
 constexpr int kAStages = 2, kBStages = 3, kF16Slots = 4, kScSlots = 4, kAcc = 2;
-constexpr int kTmemCols = kAcc * BN;               // 512
+constexpr int kEpiCols = 64;                       // token columns per epilogue warp
+constexpr int kEpiWarps = 4 * (BN / kEpiCols);     // 12: three per TMEM lane quarter
+constexpr int kTmemBuf = 256;                      // column stride of the accumulator buffers
+constexpr int kTmemCols = kAcc * kTmemBuf;         // 512 (allocations are powers of two)
 static_assert(kBBlocksPerStage == kAcc, "each activation stage feeds one block of each MMA issuer");
 constexpr int kConvThreads = 128;                  // warps 4-7
-constexpr int kEpiThreads = 256;                   // warps 8-15
-constexpr int kThreads = 512;
-// registers per thread after setmaxnreg (launch: 128 x 512 threads):
-// 128*48 + 128*96 + 256*184 = 65536
-constexpr int kRegsCtl = 48, kRegsConv = 96, kRegsEpi = 184;
+constexpr int kEpiThreads = 32 * kEpiWarps;        // 384: warps 8-19
+constexpr int kThreads = 256 + kEpiThreads;        // 640
+// registers per thread after setmaxnreg (launch: 96 x 640 = 61440 in the pool):
+// 128*32 + 128*72 + 384*120 = 59392
+constexpr int kRegsCtl = 32, kRegsConv = 72, kRegsEpi = 120;
+static_assert(128 * kRegsCtl + 128 * kRegsConv + kEpiThreads * kRegsEpi <= 96 * kThreads, "register split");
 
 constexpr int kARawBytes = BM * 272;               // 34816
-constexpr int kBStageBytes = BN * 128;             // 32768: 256 tokens x 64 f16, 128B swizzle
+constexpr int kBStageBytes = BN * 128;             // 24576: 192 tokens x 64 f16, 128B swizzle
 constexpr int kA16Tile = BM * 64;                  // 8192: 128 rows x 32 f16, no swizzle
-constexpr int kScBytes = (BM + BN) * 4;            // 1536: d_w[128], d_a[256] as f32
+constexpr int kScBytes = (BM + BN) * 4;            // 1280: d_w[128], d_a[192] as f32
 
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int OFF_B = 0;                                        // 3 x 32768 (1024-aligned)
-constexpr int OFF_ARAW = OFF_B + kBStages * kBStageBytes;       // 98304
-constexpr int OFF_A16 = OFF_ARAW + kAStages * kARawBytes;       // 167936
-constexpr int OFF_SC = OFF_A16 + kF16Slots * kA16Tile;          // 200704
-constexpr int OFF_BAR = OFF_SC + kScSlots * kScBytes;           // 206848
+constexpr int OFF_B = 0;                                        // 3 x 24576 (1024-aligned)
+constexpr int OFF_ARAW = OFF_B + kBStages * kBStageBytes;       // 73728
+constexpr int OFF_A16 = OFF_ARAW + kAStages * kARawBytes;       // 143360
+constexpr int OFF_SC = OFF_A16 + kF16Slots * kA16Tile;          // 176128
+constexpr int OFF_BAR = OFF_SC + kScSlots * kScBytes;           // 181248
+static_assert(kBStageBytes % 1024 == 0 && OFF_A16 % 1024 == 0, "swizzle atoms and tiles stay aligned");
 constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kF16Slots + 2 * kScSlots + 2 * kAcc + kAcc;  // 32
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8 + 8;
 constexpr int kSmemBytes = OFF_MISC + 16 + 1024;                // + alignment slack
@@ -195,16 +203,17 @@ __device__ __forceinline__ void arrive(uint32_t bar)
 
 // Scale-ring order.  The epilogue reads TMEM in the 16x256b shape, so each
 // of its threads holds four weight rows (32q + 16*sub + g + 8*e) and, per
-// 32-column group cg, eight token columns (32cg + 8*rep + 2m + {0,1}); the
-// converters store d_w and d_a so that those sets are contiguous, which
-// makes the epilogue's scale reads 16-byte, bank-conflict-free loads.
+// 32-column group cg of its 64 tokens, eight token columns
+// (64h + 32cg + 8*rep + 2m + {0,1}); the converters store d_w and d_a so that
+// those sets are contiguous, which makes the epilogue's scale reads 16-byte,
+// bank-conflict-free loads.
 __device__ __forceinline__ int dw_slot(int r)  // weight row 0..127
 {
     return (r >> 5) * 32 + (r & 7) * 4 + ((r >> 4) & 1) * 2 + ((r >> 3) & 1);
 }
-__device__ __forceinline__ int da_slot(int c)  // token column 0..255
+__device__ __forceinline__ int da_slot(int c)  // token column 0..BN-1
 {
-    return (c >> 7) * 128 + ((c >> 5) & 3) * 32 + ((c >> 1) & 3) * 8 + ((c >> 3) & 3) * 2 + (c & 1);
+    return (c >> 6) * 64 + ((c >> 5) & 1) * 32 + ((c >> 1) & 3) * 8 + ((c >> 3) & 3) * 2 + (c & 1);
 }
 
 // Converter step for weight row r, raw block BETA of the stage: read the 48
@@ -284,20 +293,21 @@ struct Bars {
     __device__ uint32_t drain(int issuer) const { return at(kNumBars - kAcc + issuer); }
 };
 
-// The d_a words of the 8 blocks of a raw weight stage for two tokens (32
-// contiguous bytes of the plane's ds row each); 0 for tokens past t.
+// The d_a words of the 8 blocks of a raw weight stage for the tile's tokens
+// r and r + 128 (32 contiguous bytes of the plane's ds row each); 0 for
+// tokens past t, and the second one only exists for r + 128 < BN.
 struct StageDa {
     uint32_t w[2][8];
 };
 
 __device__ __forceinline__ StageDa load_stage_da(const uint32_t *__restrict__ ds, int64_t nb, int64_t t, int64_t tok0,
-                                                 int s)
+                                                 int r, int s)
 {
     StageDa d;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int64_t tok = tok0 + 128 * h;
-        if (tok < t) {
+        if (tok < t && (h == 0 || r + 128 < BN)) {
             const uint4 *p = reinterpret_cast<const uint4 *>(ds + tok * nb + 8 * s);
             const uint4 a = __ldg(p), b = __ldg(p + 1);
             d.w[h][0] = a.x; d.w[h][1] = a.y; d.w[h][2] = a.z; d.w[h][3] = a.w;
@@ -324,7 +334,8 @@ __device__ __forceinline__ bool convert_block(const Bars &B, uint8_t *sm, int s,
     float *sa = sw + BM;
     convert_a_row<BETA>(sm + OFF_ARAW + slot * kARawBytes + r * 272, sm + OFF_A16 + fs * kA16Tile, sw, r);
     sa[da_slot(r)] = __half2float(__ushort_as_half(static_cast<unsigned short>(da.w[0][BETA] & 0xffffu)));
-    sa[da_slot(r + 128)] = __half2float(__ushort_as_half(static_cast<unsigned short>(da.w[1][BETA] & 0xffffu)));
+    if (r + 128 < BN)
+        sa[da_slot(r + 128)] = __half2float(__ushort_as_half(static_cast<unsigned short>(da.w[1][BETA] & 0xffffu)));
     q8::fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
     arrive(B.f_full(fs));
     arrive(B.sc_full(ss));
@@ -438,7 +449,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         break;
                     if (!wait_bar(B.acc_empty(ab), (static_cast<uint32_t>(j / kAcc) & 1u) ^ 1u, abort_flag)) break;
                     tc_fence_after();
-                    const uint32_t d = tmem + static_cast<uint32_t>(ab * BN);
+                    const uint32_t d = tmem + static_cast<uint32_t>(ab * kTmemBuf);
                     const uint32_t a_addr = base + OFF_A16 + fs * kA16Tile;
                     const uint32_t b_addr = base + OFF_B + sb * kBStageBytes + 64 * bq;
 #pragma unroll
@@ -457,11 +468,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     } else if (warp < 8) {
         setmaxnreg_dec<kRegsConv>();
         // ------------------------------------------------------------ converters
-        const int r = threadIdx.x - 128;  // weight row of the tile and token pair (r, r + 128), 0..127
+        const int r = threadIdx.x - 128;  // weight row of the tile and tokens r, r + 128 (if < BN), 0..127
         const int nstages = nb / kABlocksPerStage;
         q8::griddep_wait();               // the plane's scales may come from the previous kernel
         for (int s = 0; s < nstages && !*abort_flag; ++s) {
-            const StageDa da = load_stage_da(ds, nb, t, t0 + r, s);
+            const StageDa da = load_stage_da(ds, nb, t, t0 + r, r, s);
             if (!wait_bar(B.a_full(s % kAStages), static_cast<uint32_t>(s / kAStages) & 1u, abort_flag)) break;
             if (!convert_block<0>(B, sm, s, r, da, abort_flag)) break;
             if (!convert_block<1>(B, sm, s, r, da, abort_flag)) break;
@@ -476,13 +487,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         setmaxnreg_inc<kRegsEpi>();
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;            // TMEM lane quarter of this warp
-        const int hcol = (warp - 8) >> 2;  // token half: [128*hcol, 128*hcol + 128)
+        const int hcol = (warp - 8) >> 2;  // token group: [64*hcol, 64*hcol + 64)
         const int g = lane >> 2, m = lane & 3;
         // this thread's outputs: rows 32q + 16*sub + g + 8*e, token columns
-        // 128*hcol + 32*cg + 8*rep + 2m + {0,1}; acc index 8*(2cg + sub) + 2*rep + e
-        float2 acc[64];
+        // 64*hcol + 32*cg + 8*rep + 2m + {0,1}; acc index 8*(2cg + sub) + 2*rep + e
+        float2 acc[32];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.0f, 0.0f);
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
             const int ab = j % kAcc, ss = j % kScSlots;
@@ -491,9 +502,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_after();
             const float *sw = reinterpret_cast<const float *>(sm + OFF_SC + ss * kScBytes);
             const float4 w4 = *reinterpret_cast<const float4 *>(sw + 32 * q + 4 * g);  // dw_slot order
-            const float *sa = sw + BM + 128 * hcol + 8 * m;                             // da_slot order, + 32*cg
-            const uint32_t tbase =
-                tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BN + 128 * hcol);
+            const float *sa = sw + BM + kEpiCols * hcol + 8 * m;                        // da_slot order, + 32*cg
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                                   static_cast<uint32_t>(ab * kTmemBuf + kEpiCols * hcol);
             // chunk c = (cg = c / 2, sub = c % 2): 16 lanes x 32 columns.  Loads
             // are double-buffered: chunk c + 1 is in flight while chunk c is
             // scaled and accumulated.  The buffer is released once its last
@@ -503,7 +514,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_ld16x256b_x4(tbase, p0);
             tc_wait_ld16(p0);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t(&cur)[16] = (c & 1) ? p1 : p0;
                 uint32_t(&nxt)[16] = (c & 1) ? p0 : p1;
                 if ((c & 1) == 0) {
@@ -512,14 +523,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     da[0] = a0.x; da[1] = a0.y; da[2] = a0.z; da[3] = a0.w;
                     da[4] = a1.x; da[5] = a1.y; da[6] = a1.z; da[7] = a1.w;
                 }
-                if (c < 7) {
+                if (c < 3) {
                     const int cn = c + 1;
                     tc_ld16x256b_x4(tbase + (static_cast<uint32_t>(16 * (cn & 1)) << 16) + 32 * (cn >> 1), nxt);
                 }
                 if (c & 1) epi_math(acc + 8 * c, cur, da, w4.z, w4.w);
                 else epi_math(acc + 8 * c, cur, da, w4.x, w4.y);
-                if (c < 7) tc_wait_ld16(nxt);
-                if (c == 6) {
+                if (c < 3) tc_wait_ld16(nxt);
+                if (c == 2) {
                     tc_fence_before();
                     arrive(B.acc_empty(ab));  // TMEM buffer free for the next block's MMAs
                 }
@@ -528,14 +539,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         if (ok && !*abort_flag) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int64_t row = n0 + 32 * q + 16 * (c & 1) + g + 8 * e;
                     if (row >= n) continue;
 #pragma unroll
                     for (int rep = 0; rep < 4; ++rep) {
-                        const int64_t tok = t0 + 128 * hcol + 32 * (c >> 1) + 8 * rep + 2 * m;
+                        const int64_t tok = t0 + kEpiCols * hcol + 32 * (c >> 1) + 8 * rep + 2 * m;
                         const float2 v = acc[8 * c + 2 * rep + e];
                         if (tok < t) y[tok * n + row] = v.x;
                         if (tok + 1 < t) y[(tok + 1) * n + row] = v.y;
