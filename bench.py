@@ -45,7 +45,7 @@ PREFILL = dict(tokens=3325, d=3584, nf=18944, eps=1e-6)
 # the ncu capture summarised under profiles/; None until taken, and reset to
 # None whenever that kernel changes (the figure would describe old code).
 NCU_TRAFFIC_BYTES = {"gemv_staged 12288x7168+96x7168": 97_942_016,     # profiles/gemv_staged_12288x7168_plus_96x7168.md
-                     "gemm_tc 18944x3584 t=3325": 734_083_584,         # profiles/gemm_tc_18944x3584_t3325.md
+                     "gemm_tc 18944x3584 t=3325": None,                # recapture pending for the current gemm_tc
                      "gemv_small 12288x7168 t=16": 98_196_736}         # profiles/gemv_small_12288x7168_t16.md
 
 
@@ -331,8 +331,8 @@ def run_prefill(torch, q8p, steps, warmup, dev):
     O = torch.empty((T, d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     names = ["rmsnorm_quant", "gemm_gate", "gemm_up", "swiglu_quant", "gemm_down"]
-    ws_d = q8p.gemm_workspace(T, d, dev)    # gate and up: same plane, ordered on one stream
-    ws_f = q8p.gemm_workspace(T, nf, dev)   # down
+    ws_d = q8p.gemm_workspace(nf, T, d, dev)    # gate and up: same shapes, ordered on one stream
+    ws_f = q8p.gemm_workspace(d, T, nf, dev)    # down
     calls = [q8p.rmsnorm_quant(x, w, eps, y, *pa, bind=True),
              q8p.q8_0_gemm(wg, nf, d, *pa, T, G, workspace=ws_d, bind=True),
              q8p.q8_0_gemm(wu, nf, d, *pa, T, U, workspace=ws_d, bind=True),

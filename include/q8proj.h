@@ -211,11 +211,14 @@ Q8_API int q4a_gemv(const void *w, int64_t n, int64_t k,
                     const int8_t *qs, const uint32_t *ds, float *y, void *stream);
 
 /*
- * q8_0_gemm_workspace_bytes -- device workspace q8_0_gemm needs for t tokens
- * of width k: t*k*2 bytes (the activation's codes as f16); 0 when
+ * q8_0_gemm_workspace_bytes -- device workspace q8_0_gemm needs for n weight
+ * rows, t tokens and width k: the weight codes as f16 (n*k*2 bytes), the
+ * activation codes as f16 (t*k*2), and both sides' block scales as f32
+ * (k/32 * 4 bytes per weight row and per token, rows and tokens rounded up to
+ * the GEMM's 128 x 192 tiles), each part starting on a 1 KiB boundary; 0 when
  * (k/32) % 8 != 0 or t <= Q8_GEMV_MAX_TOKENS (those calls need none).
  */
-Q8_API size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k);
+Q8_API size_t q8_0_gemm_workspace_bytes(int64_t n, int64_t t, int64_t k);
 
 /*
  * q8_0_gemm -- prefill projection Y[t][i] = sum_b d_w(i,b) * d_a(t,b) * isum.
@@ -223,15 +226,16 @@ Q8_API size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k);
  *   qs, ds : plane with rows_pad >= t rows (input; rows >= t are not read)
  *   y      : f32 [t][n] row-major (output)
  *   workspace, workspace_bytes : caller-owned device scratch of at least
- *            q8_0_gemm_workspace_bytes(t, k) bytes, 16-byte aligned; its
+ *            q8_0_gemm_workspace_bytes(n, t, k) bytes, 16-byte aligned; its
  *            contents on entry are ignored and on return are unspecified.
  *            Two calls may share a workspace only if they are ordered on one
  *            stream.  May be NULL when that size is 0.
  * n >= 1, t >= 1, k % 32 == 0.  Every 32-wide k block is one q8_0 block on
  * both sides, so its integer dot product is scaled by d_w * d_a once.  The
- * call enqueues a pre-pass that writes the plane's codes as f16 (exact) into
- * the workspace, then the tcgen05 GEMM (both with
- * programmatic dependent launch; the same precondition on w as q8_0_gemv).
+ * call enqueues two pre-passes that write the weight codes and the plane's
+ * codes as f16 (exact) and both sides' block scales as f32 into the
+ * workspace, then the tcgen05 GEMM (all with programmatic dependent launch;
+ * the same precondition on w as q8_0_gemv).
  * "12 - r5-r6 re-ranking + structural rewrite spec", sec. 2 and 3.1;
  * "54 - r51 - producer-fused A-quantize mode 1", sec. 2.1.
  */

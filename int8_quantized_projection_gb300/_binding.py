@@ -31,7 +31,7 @@ SIGNATURES = {
     "rmsnorm_quant": (_INT, [_P, _P, ctypes.c_float, _P, _I64, _I64, _P, _P, _I64, _P]),
     "swiglu_quant": (_INT, [_P, _P, _P, _I64, _I64, _P, _P, _I64, _P]),
     "q8_0_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
-    "q8_0_gemm_workspace_bytes": (ctypes.c_size_t, [_I64, _I64]),
+    "q8_0_gemm_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "q8_0_gemm": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, ctypes.c_size_t, _P]),
     "q8_0_gemm_mma": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
     "q8_0_gemm_noalloc": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
@@ -254,22 +254,22 @@ def q8_0_gemv_grouped(projs, k: int, qs, ds, stream=None, bind=False):
     return None
 
 
-def q8_0_gemm_workspace_bytes(t: int, k: int) -> int:
-    return int(lib().q8_0_gemm_workspace_bytes(t, k))
+def q8_0_gemm_workspace_bytes(n: int, t: int, k: int) -> int:
+    return int(lib().q8_0_gemm_workspace_bytes(n, t, k))
 
 
-def gemm_workspace(t: int, k: int, device="cuda"):
+def gemm_workspace(n: int, t: int, k: int, device="cuda"):
     """Allocate (with PyTorch) the scratch q8_0_gemm needs for (t, k); None if it needs none."""
     import torch
 
-    nbytes = q8_0_gemm_workspace_bytes(t, k)
+    nbytes = q8_0_gemm_workspace_bytes(n, t, k)
     return torch.empty(nbytes, dtype=torch.uint8, device=device) if nbytes else None
 
 
 def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, workspace=None, stream=None, bind=False):
     """Y[t][n] f32 = plane rows [0, t) x Q8_0 weights.
 
-    ``workspace`` is a uint8 CUDA tensor of at least q8_0_gemm_workspace_bytes(t, k)
+    ``workspace`` is a uint8 CUDA tensor of at least q8_0_gemm_workspace_bytes(n, t, k)
     bytes; when None one is allocated here with PyTorch (the library never allocates)."""
     import torch
 
@@ -278,7 +278,7 @@ def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, workspace=None, stream=None,
     if w.numel() != n * (k // 32) * 34 or y.numel() < t * n or qs.shape[-1] != k or ds.shape[0] != rows_pad:
         raise ValueError("shape mismatch")
     if workspace is None:
-        workspace = gemm_workspace(t, k, y.device)
+        workspace = gemm_workspace(n, t, k, y.device)
     if workspace is not None:
         _need(workspace, torch.uint8, "workspace")
     wsp = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)

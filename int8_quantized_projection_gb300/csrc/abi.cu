@@ -120,7 +120,7 @@ int gemm_mma_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const
 
 int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t, float *y,
                    void *workspace, cudaStream_t s);
-size_t gemm_workspace_bytes(int64_t t, int64_t k);
+size_t gemm_workspace_bytes(int64_t n, int64_t t, int64_t k);
 
 } // namespace q8
 
@@ -158,17 +158,17 @@ extern "C" int q8_check(void *stream)
     return b;
 }
 
-extern "C" size_t q8_0_gemm_workspace_bytes(int64_t t, int64_t k)
+extern "C" size_t q8_0_gemm_workspace_bytes(int64_t n, int64_t t, int64_t k)
 {
-    if (t <= Q8_GEMV_MAX_TOKENS || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0) return 0;
-    return q8::gemm_workspace_bytes(t, k);
+    if (n < 1 || t <= Q8_GEMV_MAX_TOKENS || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0) return 0;
+    return q8::gemm_workspace_bytes(n, t, k);
 }
 
 extern "C" int q8_0_gemm(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t,
                          int64_t rows_pad, float *y, void *workspace, size_t workspace_bytes, void *stream)
 {
     if (!w || !qs || !ds || !y || n < 1 || t < 1 || k <= 0 || (k % 32) != 0 || rows_pad < t) return Q8_ERR_ARG;
-    const size_t need = q8_0_gemm_workspace_bytes(t, k);
+    const size_t need = q8_0_gemm_workspace_bytes(n, t, k);
     if (need > 0 && (!workspace || workspace_bytes < need)) return Q8_ERR_ARG;
     if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
     if (need > 0 && !q8::aligned16(workspace)) return Q8_ERR_ALIGN;
@@ -180,7 +180,8 @@ extern "C" int q8_0_gemm(const void *w, int64_t n, int64_t k, const int8_t *qs, 
         return q8::gemv_generic_launch(w, n, k, qs, ds, y, t, s);
     }
     if (t <= Q8_GEMV_MAX_TOKENS) return q8::gemv_small_launch(w, n, k, qs, ds, y, t, s);
-    if (t > int64_t(65535) * 128 || n > (int64_t(1) << 31) - 128 || k > (int64_t(1) << 31) / 2) return Q8_ERR_ARG;
+    // grid: token tiles of 192 along x, weight-row tiles of 128 along y (at most 65535)
+    if (n > int64_t(65535) * 128 || t > (int64_t(1) << 31) - 256 || k > (int64_t(1) << 31) / 2) return Q8_ERR_ARG;
     return q8::gemm_tc_launch(w, n, k, qs, ds, t, y, workspace, s);
 }
 

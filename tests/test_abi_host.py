@@ -76,10 +76,12 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert lib.q8_0_gemv(P(FAKE), 8, 100, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
     assert lib.q8_0_gemv(P(FAKE + 2), 8, 64, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ALIGN
     # q8_0_gemm: rows_pad < t, t < 1, workspace missing or too small
-    ws = lib.q8_0_gemm_workspace_bytes(20, 256)
-    assert ws == 20 * 256 * 2                                 # the activation's codes as f16
-    assert lib.q8_0_gemm_workspace_bytes(20, 64) == 0         # k/32 % 8 != 0: generic kernel, no workspace
-    assert lib.q8_0_gemm_workspace_bytes(16, 256) == 0        # t <= 16: small-batch kernel, no workspace
+    ws = lib.q8_0_gemm_workspace_bytes(8, 20, 256)
+    up = lambda v: -(-v // 1024) * 1024
+    # f16 weights | f16 activation | d_w per 128-row tile | d_a per 192-token tile, each from a 1 KiB boundary
+    assert ws == up(up(up(8 * 256 * 2) + 20 * 256 * 2) + 1 * 8 * 128 * 4) + up(1 * 8 * 192 * 4)
+    assert lib.q8_0_gemm_workspace_bytes(8, 20, 64) == 0      # k/32 % 8 != 0: generic kernel, no workspace
+    assert lib.q8_0_gemm_workspace_bytes(8, 16, 256) == 0     # t <= 16: small-batch kernel, no workspace
     assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(FAKE), 5, 4, P(FAKE), P(0), 0, s) == ERR_ARG
     assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(FAKE), 0, 4, P(FAKE), P(0), 0, s) == ERR_ARG
     assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 20, 20, P(FAKE), P(0), ws, s) == ERR_ARG

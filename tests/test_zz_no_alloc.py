@@ -40,7 +40,7 @@ def _call_c_abi(q8, fn, blob_d, n, k, qs_d, ds_d, t, y):
     args = [ctypes.c_void_p(blob_d.data_ptr()), n, k, ctypes.c_void_p(qs_d.data_ptr()),
             ctypes.c_void_p(ds_d.data_ptr()), t, qs_d.shape[0], ctypes.c_void_p(y.data_ptr())]
     if fn == "q8_0_gemm":
-        ws = q8.gemm_workspace(t, k)
+        ws = q8.gemm_workspace(n, t, k)
         args += [ctypes.c_void_p(ws.data_ptr()) if ws is not None else ctypes.c_void_p(0),
                  ws.numel() if ws is not None else 0]
         keep = ws
@@ -76,7 +76,7 @@ def test_noalloc_gemm_refuses_requests_beyond_its_scratch(q8):
     cap = lib.q8_0_gemm_noalloc_max_bytes()
     assert cap == 32 << 20
     t, k = 3325, 18944  # needs ~157 MB of scratch
-    assert lib.q8_0_gemm_workspace_bytes(t, k) > cap
+    assert lib.q8_0_gemm_workspace_bytes(8, t, k) > cap
     dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
     p = ctypes.c_void_p(dummy.data_ptr())
     st = lib.q8_0_gemm_noalloc(p, 8, k, p, p, t, t, p, ctypes.c_void_p(0))
