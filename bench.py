@@ -370,16 +370,14 @@ def bytes_small(n, k, t):
     return n * (k // 32) * 34 + t * (k + 4 * (k // 32)) + 4 * t * n
 
 
-def run_small(torch, q8p, steps, warmup, dev):
-    n, k, t = SMALL["n"], SMALL["k"], SMALL["tokens"]
-    w_h = syn.q8_0_weights(syn.rng(4, 1), n, k)[0]
-    copies = max(2, -(-4 * L2_BYTES // w_h.nbytes))
-    ws = [torch.from_numpy(w_h).to(dev) for _ in range(copies)]
-    x = torch.from_numpy(syn.activations(syn.rng(4, 0), t, k, sigma=1.5, outlier_frac=0.01)).to(dev)
-    plane = q8p.empty_plane(q8p.q8_plane_rows(t), k, dev)
-    q8p.quantize_q8_0(x, *plane)
-    y = torch.empty((t, n), dtype=torch.float32, device=dev)
-    calls = [q8p.q8_0_gemv_batched(w, n, k, *plane, t, y, bind=True) for w in ws]
+def time_calls(torch, q8p, calls, steps, warmup, dev):
+    """Mean device time of one launch, two ways: each launch bracketed by its
+    own pair of events (`us`, no overlap with its neighbours), and all `steps`
+    launches back to back under one pair (`us_b2b`, the prologue of each
+    overlapping the tail of the previous one as in a decode stream).  Launch i
+    uses weight copy i mod copies, so consecutive launches read different
+    memory (together > 4 x L2)."""
+    copies = len(calls)
     for i in range(warmup):
         calls[i % copies]()
     q8p.q8_check()
@@ -391,8 +389,28 @@ def run_small(torch, q8p, steps, warmup, dev):
         calls[(warmup + i) % copies]()
         evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        calls[(warmup + i) % copies]()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
     q8p.q8_check()
-    return dict(us=1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs), copies=copies)
+    return dict(us=1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs), us_b2b=1e3 * e0.elapsed_time(e1) / steps,
+                copies=copies)
+
+
+def run_small(torch, q8p, steps, warmup, dev):
+    n, k, t = SMALL["n"], SMALL["k"], SMALL["tokens"]
+    w_h = syn.q8_0_weights(syn.rng(4, 1), n, k)[0]
+    copies = max(2, -(-4 * L2_BYTES // w_h.nbytes))
+    ws = [torch.from_numpy(w_h).to(dev) for _ in range(copies)]
+    x = torch.from_numpy(syn.activations(syn.rng(4, 0), t, k, sigma=1.5, outlier_frac=0.01)).to(dev)
+    plane = q8p.empty_plane(q8p.q8_plane_rows(t), k, dev)
+    q8p.quantize_q8_0(x, *plane)
+    y = torch.empty((t, n), dtype=torch.float32, device=dev)
+    calls = [q8p.q8_0_gemv_batched(w, n, k, *plane, t, y, bind=True) for w in ws]
+    return time_calls(torch, q8p, calls, steps, warmup, dev)
 
 
 # ---------------------------------------------------------------------------
@@ -415,19 +433,7 @@ def run_asym(torch, q8p, steps, warmup, dev):
     q8p.quantize_q8_0(x, *plane)
     y = torch.empty(n, dtype=torch.float32, device=dev)
     calls = [q8p.q4a_gemv(w, n, k, *plane, y, bind=True) for w in ws]
-    for i in range(warmup):
-        calls[i % copies]()
-    q8p.q8_check()
-    stream = torch.cuda.current_stream(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    torch.cuda.synchronize(dev)
-    for i in range(steps):
-        evs[i][0].record(stream)
-        calls[(warmup + i) % copies]()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize(dev)
-    q8p.q8_check()
-    return dict(us=1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs), copies=copies)
+    return time_calls(torch, q8p, calls, steps, warmup, dev)
 
 
 # ---------------------------------------------------------------------------
@@ -569,7 +575,7 @@ def main():
 
     if world > 1:  # every duration becomes the slowest rank's (same legs on every rank)
         vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"]] if dec else []) + (list(pre.values()) if pre else [])
-                + ([small["us"]] if small else []) + ([asym["us"]] if asym else []))
+                + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else []))
         red = max_over_ranks(torch, vals, dev)
         if dec:
             dec["ms"], dec["e2e_s"], dec["kern_ms"] = red[:3]
@@ -578,9 +584,9 @@ def main():
             pre = dict(zip(pre.keys(), red[:len(pre)]))
             red = red[len(pre):]
         if small:
-            small["us"] = red.pop(0)
+            small["us"], small["us_b2b"] = red.pop(0), red.pop(0)
         if asym:
-            asym["us"] = red.pop(0)
+            asym["us"], asym["us_b2b"] = red.pop(0), red.pop(0)
 
     if rank != 0:
         if world > 1:
@@ -641,6 +647,8 @@ def main():
         gbs = bytes_small(n, k, t) / (small["us"] / 1e6) / 1e9
         sobj = {"workload": f"small-batch decode: q8_0_gemv_batched {n}x{k}, t={t} tokens, weights read once",
                 "us_per_call": round(small["us"], 2), "gbs": round(gbs, 1),
+                "us_back_to_back": round(small["us_b2b"], 2),
+                "gbs_back_to_back": round(bytes_small(n, k, t) / (small["us_b2b"] / 1e6) / 1e9, 1),
                 "roofline": {"kernel": "q8_0_gemv_batched (gemv_small_kernel)", "bound": "hbm",
                              "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": round(gbs / peaks["hbm_gbs"], 4),
@@ -651,7 +659,7 @@ def main():
             line.update({"value": round(world * sobj["gbs"], 1), "unit": "GB/s",
                          "ms_per_step": round(small["us"] / 1e3, 5),
                          "config": {"workload": sobj["workload"], "l2": sobj["l2"], "parallelism": "replicas"},
-                         "roofline": sobj["roofline"], "gpu_launches": args.steps})
+                         "roofline": sobj["roofline"], "gpu_launches": 2 * args.steps})
         line["small_batch"] = sobj
     if asym is not None:
         n, k = ASYM["n"], ASYM["k"]
@@ -659,7 +667,9 @@ def main():
         aobj = {"workload": f"asymmetric 4-bit weights (d*nib - m, min term from the plane's ssum): q4a_gemv "
                             f"{n}x{k}, batch 1",
                 "us_per_call": round(asym["us"], 2), "gbs": round(gbs, 1),
-                "roofline": {"kernel": "q4a_gemv (q4a_gemv_kernel)", "bound": "hbm", "achieved": round(gbs, 1),
+                "us_back_to_back": round(asym["us_b2b"], 2),
+                "gbs_back_to_back": round(bytes_q4a_gemv(n, k) / (asym["us_b2b"] / 1e6) / 1e9, 1),
+                "roofline": {"kernel": "q4a_gemv (gemv_staged_kernel<FmtQ4A>)", "bound": "hbm", "achieved": round(gbs, 1),
                              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                              "traffic": None, "algorithmic_bytes": bytes_q4a_gemv(n, k)},
                 "l2": f"weights rotate through {asym['copies']} copies (> 4 x L2)"}
@@ -667,7 +677,7 @@ def main():
             line.update({"value": round(world * aobj["gbs"], 1), "unit": "GB/s",
                          "ms_per_step": round(asym["us"] / 1e3, 5),
                          "config": {"workload": aobj["workload"], "l2": aobj["l2"], "parallelism": "replicas"},
-                         "roofline": aobj["roofline"], "gpu_launches": args.steps})
+                         "roofline": aobj["roofline"], "gpu_launches": 2 * args.steps})
         line["asym_gemv"] = aobj
     print(json.dumps(line))
     if world > 1:

@@ -30,6 +30,7 @@
 // lanes-per-row fitting, no staging.
 #include <cooperative_groups.h>
 
+#include "q4a_block.cuh"
 #include "q8_common.cuh"
 
 namespace cg = cooperative_groups;
@@ -38,13 +39,8 @@ namespace {
 
 __device__ unsigned int g_gemv_err;
 
-constexpr int kChunkBytes = 136;                // 4 Q8_0 blocks (8-byte aligned when the row is 16-byte aligned)
 constexpr int kActChunkBytes = 144;             // 128 B qs + 16 B ds: 36 words, so lanes hit distinct banks
-constexpr int kPieceChunks = 32;                // one chunk per lane
-constexpr int kPieceBytes = kPieceChunks * kChunkBytes;  // 4352 = 272 x 16
-constexpr int kStages = 2;
-constexpr int kMaxWarps = 16;
-constexpr int kMaxActChunks = 512;              // k <= 65536 on the staged path
+constexpr int kMaxActChunks = q8::kGemvStagedMaxChunks;  // k <= 65536 on the staged path
 
 constexpr int kMaxProj = Q8_MAX_GROUP;        // projections of one activation per launch
 
@@ -61,7 +57,7 @@ struct GvGeom {
     int count;
     int nc;          // 4-block chunks per row (even: k/32 % 8 == 0)
     int lpr_log2;    // lanes per row = 1 << lpr_log2
-    int rpw;         // rows per piece
+    int rpw;         // rows per piece (1: a piece is up to 32*J chunks of one row)
     int ppr;         // pieces per row group
     int64_t groups;  // total row groups over all projections
 };
@@ -76,12 +72,75 @@ __device__ __forceinline__ int proj_of(const GvGeom &g, int64_t G)
     return j;
 }
 
-// header: per-warp mbarriers, per-warp stage metadata, the CTA's row-group counter
-__host__ __device__ inline int smem_header_bytes() { return kMaxWarps * kStages * 8 * 2 + 128; }
+// A weight format of the staged kernel: the bytes of four consecutive blocks
+// of a row (a "chunk", k = 128), how many chunks a lane takes per ring slot
+// (J), the ring depth per warp, the warps per CTA, and the chunk's dot product
+// with a staged activation chunk (128 B of codes + 4 d|ssum words).  A ring
+// slot ("piece") holds 32*J chunks: up to 32*J chunks of one row, or whole
+// rows when a row has at most 32 chunks.
+//
+// Q8_0: a chunk is 136 bytes, 8-byte aligned in shared memory when rows start
+// 16-byte aligned (k/32 % 8 == 0); lanes read 8 bytes at a time, 34 words
+// apart, so a half-warp touches 32 distinct banks.
+#ifndef Q8_Q80_STAGES
+#define Q8_Q80_STAGES 2
+#endif
+#ifndef Q8_Q80_J
+#define Q8_Q80_J 1
+#endif
+#ifndef Q8_Q80_WARPS
+#define Q8_Q80_WARPS 16
+#endif
+struct FmtQ8_0 {
+    static constexpr int kChunkBytes = 136;
+    static constexpr int kLaneChunks = Q8_Q80_J;
+    static constexpr int kStages = Q8_Q80_STAGES;
+    static constexpr int kWarps = Q8_Q80_WARPS;
+    __device__ static float dot(const uint8_t *wc, const uint8_t *ac);
+};
 
-// One 4-block chunk: 34 words of raw weights (shared memory, 8-byte aligned)
-// against 128 B of qs and 4 ds words of the activation (shared memory).
-__device__ __forceinline__ float chunk_dot(const uint8_t *wc, const uint8_t *ac)
+// Asymmetric 4-bit blocks (q4a_block.cuh): a chunk is 80 bytes, 16-byte
+// aligned; lanes read it as five 16-byte words, 20 words apart, so each
+// quarter-warp touches 32 distinct banks.  At 80 bytes per 128 elements the
+// same HBM rate needs 1.7x the chunk rate of Q8_0, and the kernel is bound by
+// the latency of each warp's chunk arithmetic, so this format runs more
+// independent chunks at once (more warps, or more chunks per lane).
+#ifndef Q8_Q4A_STAGES
+#define Q8_Q4A_STAGES 2
+#endif
+#ifndef Q8_Q4A_J
+#define Q8_Q4A_J 2
+#endif
+#ifndef Q8_Q4A_WARPS
+#define Q8_Q4A_WARPS 16
+#endif
+struct FmtQ4A {
+    static constexpr int kChunkBytes = q8::kA4ChunkBytes;
+    static constexpr int kLaneChunks = Q8_Q4A_J;
+    static constexpr int kStages = Q8_Q4A_STAGES;
+    static constexpr int kWarps = Q8_Q4A_WARPS;
+    __device__ static float dot(const uint8_t *wc, const uint8_t *ac)
+    {
+        uint32_t wv[q8::kA4ChunkWords];
+#pragma unroll
+        for (int c = 0; c < 5; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(wc + 16 * c);
+            wv[4 * c + 0] = v.x;
+            wv[4 * c + 1] = v.y;
+            wv[4 * c + 2] = v.z;
+            wv[4 * c + 3] = v.w;
+        }
+        return q8::a4_chunk(wv, ac, 0.0f);
+    }
+};
+
+// header: per-warp mbarriers, per-warp stage metadata, the CTA's row-group counter
+template <class F>
+__host__ __device__ inline int smem_header_bytes() { return F::kWarps * F::kStages * 8 * 2 + 128; }
+
+// One 4-block Q8_0 chunk: 34 words of raw weights (shared memory, 8-byte
+// aligned) against 128 B of qs and 4 ds words of the activation.
+__device__ __forceinline__ float FmtQ8_0::dot(const uint8_t *wc, const uint8_t *ac)
 {
     uint32_t wv[34];
 #pragma unroll
@@ -114,16 +173,23 @@ __device__ __forceinline__ float chunk_dot(const uint8_t *wc, const uint8_t *ac)
     return acc;
 }
 
-__global__ void __launch_bounds__(kMaxWarps * 32)
+template <class F>
+__global__ void __launch_bounds__(F::kWarps * 32)
 gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict__ ds_row,
                    const __grid_constant__ GvGeom g)
 {
+    constexpr int kChunkBytes = F::kChunkBytes;
+    constexpr int J = F::kLaneChunks;
+    constexpr int kStages = F::kStages;
+    constexpr int kWarps = F::kWarps;
+    constexpr int kPieceChunks = 32 * J;
+    constexpr int kPieceBytes = kPieceChunks * kChunkBytes;  // a multiple of 16 bytes
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    int2 *meta = reinterpret_cast<int2 *>(smem + kMaxWarps * kStages * 8);  // (row group, piece) per stage
-    unsigned int *counter = reinterpret_cast<unsigned int *>(smem + kMaxWarps * kStages * 16);
-    uint8_t *act = smem + smem_header_bytes();
+    int2 *meta = reinterpret_cast<int2 *>(smem + kWarps * kStages * 8);  // (row group, piece) per stage
+    unsigned int *counter = reinterpret_cast<unsigned int *>(smem + kWarps * kStages * 16);
+    uint8_t *act = smem + smem_header_bytes<F>();
     uint8_t *ring = act + ((g.nc * kActChunkBytes + 127) & ~127);
     uint64_t *mybar = bars + warp * kStages;
     int2 *mymeta = meta + warp * kStages;
@@ -167,7 +233,7 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
         const int64_t Gl = G - pj.g_begin;  // row group within the projection
         const uint8_t *src;
         uint32_t bytes;
-        if (g.rpw == 1) {  // one row per piece, up to 32 chunks of it
+        if (g.rpw == 1) {  // one row per piece, up to 32*J chunks of it
             const int chunks = min(kPieceChunks, g.nc - kPieceChunks * p);
             bytes = static_cast<uint32_t>(chunks * kChunkBytes);
             src = pj.w + Gl * pitch + static_cast<int64_t>(kPieceChunks) * p * kChunkBytes;
@@ -201,10 +267,17 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
     }
     __syncthreads();
 
+    // Lane roles.  Long rows (rpw == 1): slot j of a piece is chunk
+    // 32*J*p + 32*j + lane of the row.  Short rows: lanes (ri, cj) with
+    // 1 << lpr_log2 lanes per row; slot j is row j*(32 >> lpr_log2) + ri of the
+    // piece, chunk cj.
     const int lpr = 1 << g.lpr_log2;
-    const int ri = lane >> g.lpr_log2;         // row within a piece
-    const int cj = lane & (lpr - 1);           // chunk within a piece
-    float acc = 0.0f;
+    const int rps = 32 >> g.lpr_log2;          // rows per slot
+    const int ri = lane >> g.lpr_log2;         // row within a slot
+    const int cj = lane & (lpr - 1);           // chunk within a row
+    float acc[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) acc[j] = 0.0f;
     for (uint32_t i = 0;; ++i) {
         const int s = static_cast<int>(i % kStages);
         const uint32_t par = (i / kStages) & 1u;
@@ -220,27 +293,42 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
         const GvProj &pj = g.p[proj_of(g, G)];
         const int64_t Gl = G - pj.g_begin;
         const int p = m.y;
-        int64_t row;
-        int chunk, soff;
-        bool valid;
-        if (g.rpw == 1) {
-            row = Gl;
-            chunk = kPieceChunks * p + lane;
-            soff = lane * kChunkBytes;
-            valid = chunk < g.nc;
-        } else {
-            row = Gl * g.rpw + ri;
-            chunk = cj;
-            soff = (ri * g.nc + cj) * kChunkBytes;
-            valid = cj < g.nc && row < pj.n;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            int chunk, soff;
+            bool valid;
+            if (g.rpw == 1) {
+                chunk = kPieceChunks * p + 32 * j + lane;
+                soff = (32 * j + lane) * kChunkBytes;
+                valid = chunk < g.nc;
+            } else {
+                const int rr = j * rps + ri;  // row within the piece
+                chunk = cj;
+                soff = (rr * g.nc + cj) * kChunkBytes;
+                valid = cj < g.nc && Gl * g.rpw + rr < pj.n;
+            }
+            if (valid) acc[j] += F::dot(buf + soff, act + chunk * kActChunkBytes);
         }
-        if (valid) acc += chunk_dot(buf + soff, act + chunk * kActChunkBytes);
         __syncwarp();
         if (lane == 0) issue(s);  // refill the slot just consumed
         if (p == g.ppr - 1) {     // row group complete: reduce over the lanes of each row
-            for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(Q8_FULL_MASK, acc, o);
-            if (cj == 0 && row < pj.n) pj.y[row] = acc;
-            acc = 0.0f;
+            if (g.rpw == 1) {
+                float a = acc[0];
+#pragma unroll
+                for (int j = 1; j < J; ++j) a += acc[j];
+                for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(Q8_FULL_MASK, a, o);
+                if (lane == 0) pj.y[Gl] = a;
+            } else {
+#pragma unroll
+                for (int j = 0; j < J; ++j) {
+                    float a = acc[j];
+                    for (int o = lpr >> 1; o > 0; o >>= 1) a += __shfl_xor_sync(Q8_FULL_MASK, a, o);
+                    const int64_t row = Gl * g.rpw + j * rps + ri;
+                    if (cj == 0 && row < pj.n) pj.y[row] = a;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < J; ++j) acc[j] = 0.0f;
         }
     }
 }
@@ -647,20 +735,25 @@ int gemv_small_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, con
 namespace {
 
 // Launch the staged kernel for `count` projections of one activation.
+template <class F>
 int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds,
-                       cudaStream_t s)
+                       cudaStream_t s, int smem_slot)
 {
+    constexpr int kStages = F::kStages;
+    constexpr int kMaxWarps = F::kWarps;
+    constexpr int kPieceBytes = 32 * F::kLaneChunks * F::kChunkBytes;
+    constexpr int kPieceChunks = 32 * F::kLaneChunks;
     const int64_t nb = k / 32;
     GvGeom g;
     g.count = count;
     g.nc = static_cast<int>(nb / 4);
-    if (g.nc > kPieceChunks) {
+    if (g.nc > 32) {  // long rows: one row per piece, 32*J chunks of it
         g.lpr_log2 = 5;
         g.rpw = 1;
         g.ppr = (g.nc + kPieceChunks - 1) / kPieceChunks;
-    } else {
+    } else {          // short rows: J slots of 32 >> lpr_log2 whole rows
         g.lpr_log2 = ceil_log2(g.nc);
-        g.rpw = 32 >> g.lpr_log2;
+        g.rpw = F::kLaneChunks * (32 >> g.lpr_log2);
         g.ppr = 1;
     }
     int64_t groups = 0;
@@ -681,14 +774,22 @@ int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const in
     g.groups = groups;
     const int sms = q8::device_sm_count();
     if (sms <= 0) return Q8_ERR_DEVICE;
+    // warps per CTA: enough to spread the row groups over every SM, at most
+    // kMaxWarps, and no more rings than fit beside the staged activation
+    constexpr int kSmemCap = 227 * 1024;
+    const int act_bytes = (g.nc * kActChunkBytes + 127) & ~127;
+    const int64_t fit = (kSmemCap - smem_header_bytes<F>() - act_bytes) / (kStages * kPieceBytes);
+    static_assert(kSmemCap - kMaxWarps * kStages * 16 - 128 - kMaxActChunks * kActChunkBytes >= 4 * kStages * kPieceBytes,
+                  "at least four warps' rings fit beside the longest staged activation");
+    static_assert(kMaxWarps * 32 <= 1024, "threads per CTA");
     int64_t nw = (g.groups + sms - 1) / sms;
     nw = nw < 1 ? 1 : (nw > kMaxWarps ? kMaxWarps : nw);
+    nw = nw > fit ? fit : nw;
     int64_t grid = (g.groups + nw - 1) / nw;
     grid = grid > sms ? sms : grid;
-    const int smem = smem_header_bytes() + ((g.nc * kActChunkBytes + 127) & ~127) +
-                     static_cast<int>(nw) * kStages * kPieceBytes;
-    const int maxs = smem_header_bytes() + kMaxActChunks * kActChunkBytes + kMaxWarps * kStages * kPieceBytes;
-    if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(gemv_staged_kernel), maxs, 0)) return Q8_ERR_LAUNCH;
+    const int smem = smem_header_bytes<F>() + act_bytes + static_cast<int>(nw) * kStages * kPieceBytes;
+    if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(gemv_staged_kernel<F>), kSmemCap, smem_slot))
+        return Q8_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(nw * 32));
@@ -699,7 +800,7 @@ int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemv_staged_kernel, reinterpret_cast<const uint4 *>(qs), ds, g) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, gemv_staged_kernel<F>, reinterpret_cast<const uint4 *>(qs), ds, g) != cudaSuccess)
         return Q8_ERR_LAUNCH;
     return q8::launch_status();
 }
@@ -729,10 +830,21 @@ int gemv_dispatch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t 
         }
         return Q8_OK;
     }
-    return gemv_staged_launch(projs, count, k, qs, ds, s);
+    return gemv_staged_launch<FmtQ8_0>(projs, count, k, qs, ds, s, 0);
 }
 
 } // namespace
+
+namespace q8 {
+
+int gemv_staged_q4a_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                           cudaStream_t s)
+{
+    const q8_gemv_proj p = {w, n, y};
+    return gemv_staged_launch<FmtQ4A>(&p, 1, k, qs, ds, s, 6);
+}
+
+} // namespace q8
 
 extern "C" int q8_0_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
                          void *stream)

@@ -2,28 +2,23 @@
 //
 // y[i] = sum_b ( d(i,b) * d_a(b) * sum_e nib(i,b,e) * q_a(b,e)  -  m(i,b) * d_a(b) * ssum_a(b) )
 //
-// A weight block holds 32 values d * nib - m (f16 d, f16 m, unsigned 4-bit
-// nib): the q4_K value form d*s*nib - dmin*m of "12 - r5-r6 re-ranking +
-// structural rewrite spec" (sec. 3) with its two-level scales folded into one
-// scale and one min per 32 elements.  Against a q8_0 activation block the min
-// term needs no second dot product: m * d_a * sum_e q_e, and sum_e q_e is the
-// int16 ssum that the plane carries for exactly this purpose ("54 - r51 -
-// producer-fused A-quantize mode 1", sec. 2.1).
-//
-// Layout: a block is 20 bytes -- d at +0, m at +2, then byte j (j < 16) holds
-// element j in its low nibble and element j + 16 in its high nibble -- so four
-// blocks are 80 bytes = five 16-byte loads, and every block is five whole
-// 32-bit words.  One nibble word gives two dp4a operands: w & 0x0f0f0f0f
-// (elements 4i..4i+3) and (w >> 4) & 0x0f0f0f0f (elements 16+4i..16+4i+3).
-// The activation (k bytes of codes + k/8 bytes of d|ssum) is staged once per
+// The block format and its dot product with a q8_0 activation chunk are in
+// q4a_block.cuh.  Shapes whose activation fits the staged kernel of gemv.cu
+// (k <= 65536) run there, instantiated for this format: per-warp rings fed by
+// bulk copies, as for Q8_0 weights.  This file holds the path for longer rows:
+// the activation (k bytes of codes + k/8 bytes of d|ssum) is staged once per
 // CTA in shared memory, 144 bytes per 4-block chunk so that lanes reading
-// different chunks hit different banks.  Lanes per row = the next power of two
-// of the row's chunk count (at most 32); warps take rows in a grid stride.
-#include "q8_common.cuh"
+// different chunks hit different banks, and each lane streams its weight
+// chunks from global memory with 16-byte loads.  Lanes per row = the next
+// power of two of the row's chunk count (at most 32); warps take rows in a
+// grid stride.
+#include "q4a_block.cuh"
 
 namespace {
 
-constexpr int kA4ChunkWords = 20;   // 4 blocks x 5 words (80 bytes)
+using q8::kA4ChunkWords;
+using q8::a4_chunk;
+
 constexpr int kA4ActChunk = 144;    // 128 B codes + 16 B ds words
 constexpr int kA4Threads = 256;
 
@@ -34,35 +29,6 @@ __device__ __forceinline__ uint4 ld_stream4(const uint4 *p)
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
-}
-
-// Four blocks of one row (20 words) against the staged activation chunk.
-__device__ __forceinline__ float a4_chunk(const uint32_t (&wv)[kA4ChunkWords], const uint8_t *ac, float acc)
-{
-    const uint4 dsv = *reinterpret_cast<const uint4 *>(ac + 128);
-    const uint32_t dsw[4] = {dsv.x, dsv.y, dsv.z, dsv.w};
-#pragma unroll
-    for (int bb = 0; bb < 4; ++bb) {
-        const uint4 a0 = *reinterpret_cast<const uint4 *>(ac + 32 * bb);
-        const uint4 a1 = *reinterpret_cast<const uint4 *>(ac + 32 * bb + 16);
-        const uint32_t aq[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        int isum = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t nw = wv[5 * bb + 1 + i];
-            isum = q8::dp4a(nw & 0x0f0f0f0fu, aq[i], isum);             // elements 4i .. 4i+3
-            isum = q8::dp4a((nw >> 4) & 0x0f0f0f0fu, aq[4 + i], isum);  // elements 16+4i .. 16+4i+3
-        }
-        const uint32_t dm = wv[5 * bb];
-        const float dw = __half2float(__ushort_as_half(static_cast<unsigned short>(dm & 0xffffu)));
-        const float mw = __half2float(__ushort_as_half(static_cast<unsigned short>(dm >> 16)));
-        const float da = __half2float(__ushort_as_half(static_cast<unsigned short>(dsw[bb] & 0xffffu)));
-        const int ssum = static_cast<int16_t>(static_cast<uint16_t>(dsw[bb] >> 16));
-        // d*d_a and m*d_a are exact in f32 (11 + 11 significant bits)
-        acc = __fmaf_rn(__fmul_rn(dw, da), static_cast<float>(isum), acc);
-        acc = __fmaf_rn(-__fmul_rn(mw, da), static_cast<float>(ssum), acc);
-    }
-    return acc;
 }
 
 // Load chunks c and c + lpr of a row (zeros where invalid).
@@ -157,6 +123,8 @@ extern "C" int q4a_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, c
     const int64_t smem = nc * kA4ActChunk;
     if (smem > 227 * 1024) return Q8_ERR_ARG;  // the staged activation must fit in shared memory (k <= 206592)
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    if (nc <= q8::kGemvStagedMaxChunks)
+        return q8::gemv_staged_q4a_launch(w, n, k, qs, ds, y, static_cast<cudaStream_t>(stream));
     const int lpr_log2 = ceil_log2_a4(static_cast<int>(nc < 32 ? nc : 32));
     const int rpw = 32 >> lpr_log2;
     const int64_t groups = (n + rpw - 1) / rpw;

@@ -11,6 +11,9 @@ the nibble unpacking, the dp4a pairing of nibble halves with activation words
 and the sign and source of the min term.  Shapes cover one chunk per row
 (k = 128, 32 rows per warp), ragged row counts, rows spanning several lanes'
 chunk pairs and an odd trailing chunk, and the full-size decode projection.
+Rows of at most 512 chunks (k <= 65536) run on the staged kernel (per-warp
+rings of bulk-copied pieces); longer rows on the wide kernel (weights loaded
+straight into registers): both sides of that boundary are covered.
 """
 import numpy as np
 import pytest
@@ -63,6 +66,9 @@ SHAPES = [
     (3, 256), (1, 128),
     (4099, 7168),    # ragged n, 56 chunks
     (12288, 7168),   # full-size decode projection
+    (40, 65536),     # 512 chunks: the longest row of the staged kernel
+    (50, 65664),     # 513 chunks: the wide kernel
+    (9, 131072),     # 1024 chunks, wide kernel
 ]
 
 
@@ -75,7 +81,7 @@ def test_q4a_gemv_matches_oracle(q8, n, k):
     assert_gemm_close(host(y), yr, ar, f"q4a_gemv {n}x{k}")
 
 
-@pytest.mark.parametrize("n,k", [(300, 2048), (77, 18944), (512, 128), (129, 7168)])
+@pytest.mark.parametrize("n,k", [(300, 2048), (77, 18944), (512, 128), (129, 7168), (33, 65536), (21, 65664)])
 def test_q4a_gemv_exact_epilogue_bit_equal(q8, n, k):
     blob = _weights(2, n, k, exact=True)
     qs, ds = _plane(2, k, exact=True)
