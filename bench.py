@@ -44,9 +44,10 @@ PREFILL = dict(tokens=3325, d=3584, nf=18944, eps=1e-6)
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of a kernel, from
 # the ncu capture summarised under profiles/; None until taken, and reset to
 # None whenever that kernel changes (the figure would describe old code).
-NCU_TRAFFIC_BYTES = {"gemv_staged 12288x7168+96x7168": None,           # profiles/gemv_staged_12288x7168_plus_96x7168.md
+NCU_TRAFFIC_BYTES = {"gemv_staged 12288x7168+96x7168": 97_547_008,     # profiles/gemv_staged_12288x7168_plus_96x7168.md
                      "gemm_tc 18944x3584 t=3325": 397_789_184,         # profiles/gemm_tc_18944x3584_t3325.md
-                     "gemv_small 12288x7168 t=16": 98_196_736}         # profiles/gemv_small_12288x7168_t16.md
+                     "gemv_small 12288x7168 t=16": 98_196_736,         # profiles/gemv_small_12288x7168_t16.md
+                     "gemv_staged_q4a 12288x7168": 55_083_776}         # profiles/gemv_staged_q4a_12288x7168.md
 
 
 # ---------------------------------------------------------------------------
@@ -677,7 +678,8 @@ def main():
                 "gbs_back_to_back": round(bytes_q4a_gemv(n, k) / (asym["us_b2b"] / 1e6) / 1e9, 1),
                 "roofline": {"kernel": "q4a_gemv (gemv_staged_kernel<FmtQ4A>)", "bound": "hbm", "achieved": round(gbs, 1),
                              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                             "traffic": None, "algorithmic_bytes": bytes_q4a_gemv(n, k)},
+                             "traffic": NCU_TRAFFIC_BYTES["gemv_staged_q4a 12288x7168"],
+                             "algorithmic_bytes": bytes_q4a_gemv(n, k)},
                 "l2": f"weights rotate through {asym['copies']} copies (> 4 x L2)"}
         if args.workload == "asym":
             line.update({"value": round(world * aobj["gbs"], 1), "unit": "GB/s",
