@@ -386,10 +386,11 @@ gemv_generic_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, const int8
 // two MMAs per 32-wide block and 8 tokens, whose f32 result is the exact
 // integer dot product (|isum| <= 32*127*127 < 2^24).  (The int8 mma.sync
 // needs no widening but its rate on this GPU falls short of HBM at t = 16.)
-// Within a block the k order is permuted so that each thread's eight codes
-// are contiguous bytes -- the integer sum does not depend on the order, and
-// A and B use the same one.  Per block the scale is applied as in the GEMM:
-// acc += (d_w * d_a) * isum.
+// Within a block the k order is permuted so that thread t4 of a quad holds
+// code words t4 and t4 + 4 of the block (the integer sum does not depend on
+// the order, and A and B use the same one); with rows 68 words apart in shared
+// memory the 32 lanes of a warp then read 32 distinct banks.  Per block the
+// scale is applied as in the GEMM: acc += (d_w * d_a) * isum.
 //
 // Work split: a CTA computes kSbRows weight rows for all tokens over a slice
 // of k, in stages of kSbPieces "pieces" of 8 blocks (272 bytes of each row,
@@ -411,7 +412,10 @@ gemv_generic_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, const int8
 #ifndef Q8_SB_STAGES
 #define Q8_SB_STAGES 2
 #endif
-constexpr int kSbWarps = 8;                              // consumer warps
+#ifndef Q8_SB_WARPS
+#define Q8_SB_WARPS 8
+#endif
+constexpr int kSbWarps = Q8_SB_WARPS;                    // consumer warps
 constexpr int kSbThreads = (kSbWarps + 1) * 32;          // + the producer warp
 constexpr int kSbPieces = Q8_SB_PIECES;                  // 8-block pieces per row and stage (1, 2 or 4)
 constexpr int kSbRows = 16 * kSbWarps / kSbPieces;       // weight rows per CTA
@@ -444,51 +448,49 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Codes 8*t4 .. 8*t4+7 of block BB of a staged piece (piece start 16-byte
-// aligned, block BB at byte 34*BB, its codes from byte 34*BB + 2).
+// Code words t4 and t4 + 4 of block BB of a staged row piece (piece start
+// 16-byte aligned, block BB at byte 34*BB, its codes from byte 34*BB + 2).
 template <int BB>
 __device__ __forceinline__ uint2 sb_codes(const uint8_t *piece, int t4)
 {
     constexpr int off = 34 * BB + 2;
     if constexpr ((off & 3) == 0) {
-        const uint32_t *p = reinterpret_cast<const uint32_t *>(piece + off + 8 * t4);
-        return make_uint2(p[0], p[1]);
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(piece + off);
+        return make_uint2(p[t4], p[t4 + 4]);
     } else {
-        const uint32_t *p = reinterpret_cast<const uint32_t *>(piece + off - 2 + 8 * t4);
-        const uint32_t x0 = p[0], x1 = p[1], x2 = p[2];
-        return make_uint2(__byte_perm(x0, x1, 0x5432), __byte_perm(x1, x2, 0x5432));
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(piece + off - 2);
+        return make_uint2(__byte_perm(p[t4], p[t4 + 1], 0x5432), __byte_perm(p[t4 + 4], p[t4 + 5], 0x5432));
     }
+}
+
+// Code words t4 and t4 + 4 of block BB of token tok in the stage's activation
+// boxes: box 2*pc + BB/4, 16-byte chunks 2*(BB%4) and 2*(BB%4) + 1 of the
+// token's 128-byte line, XOR-swizzled by tok % 8.
+template <int BB>
+__device__ __forceinline__ uint2 sb_act(const uint8_t *stage, int pc, int tok, int t4)
+{
+    constexpr int c0 = 2 * (BB & 3);
+    const uint8_t *line = stage + kSbOffAct + (2 * pc + (BB >> 2)) * 2048 + tok * 128;
+    return make_uint2(*reinterpret_cast<const uint32_t *>(line + ((c0 ^ (tok & 7)) << 4) + 4 * t4),
+                      *reinterpret_cast<const uint32_t *>(line + (((c0 + 1) ^ (tok & 7)) << 4) + 4 * t4));
 }
 
 // One 32-wide block (block BB of piece `pc` of the stage) for this warp's 16
 // rows (row g's piece at wpiece) and NT groups of 8 tokens (tokens past t
-// are zeros).  Thread (g = lane/4, t4 = lane%4) holds the MMA fragments of
-// rows g, g+8 and token g (+8 per token tile); its results are rows g, g+8
-// at tokens 2*t4, 2*t4+1 (+8 per token tile), kept as token pairs.
+// are zeros), on the f16 MMA with the codes widened exactly.  Thread
+// (g = lane/4, t4 = lane%4) holds the MMA fragments of rows g, g+8 and token
+// g (+8 per token tile); its results are rows g, g+8 at tokens 2*t4, 2*t4+1
+// (+8 per token tile), kept as token pairs.  da[j] is the d_a pair of tile j.
 template <int BB, int NT>
 __device__ __forceinline__ void sb_block(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
-                                         float2 (&acc)[NT][2])
+                                         const float2 (&da)[NT], float2 (&acc)[NT][2])
 {
-    uint32_t bf[NT][4];  // token 8j+g: step 0 {codes 0,1 | 2,3}, step 1 {codes 4,5 | 6,7} of its eight
-    float2 da[NT];       // d_a of tokens 8j + 2*t4, 8j + 2*t4 + 1
-    // code byte 32*BB + 8*t4 of piece pc of token tok: box 2*pc + BB/4, 16-byte
-    // chunk 2*(BB%4) + t4/2 of the token's 128-byte line, XOR-swizzled by tok % 8
-    const int box = 2 * pc + (BB >> 2);
-    constexpr int c0 = 2 * (BB & 3);
+    uint32_t bf[NT][4];  // token 8j+g: step 0 {codes 0,1 | 2,3} of word t4, step 1 the same of word t4 + 4
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-        const int tok = 8 * j + g;
-        const int chunk = (c0 + (t4 >> 1)) ^ (tok & 7);
-        const uint2 v = *reinterpret_cast<const uint2 *>(stage + kSbOffAct + box * 2048 + tok * 128 + chunk * 16 +
-                                                         8 * (t4 & 1));
+        const uint2 v = sb_act<BB>(stage, pc, 8 * j + g, t4);
         q8::i8x4_to_f16x4(v.x, bf[j][0], bf[j][1]);
         q8::i8x4_to_f16x4(v.y, bf[j][2], bf[j][3]);
-        const int tk = 8 * j + 2 * t4;
-        const uint8_t *dsw = stage + kSbOffDs + 4 * (kSbGroup * pc + BB);
-        const uint32_t d0 = *reinterpret_cast<const uint32_t *>(dsw + tk * (32 * kSbPieces));
-        const uint32_t d1 = *reinterpret_cast<const uint32_t *>(dsw + (tk + 1) * (32 * kSbPieces));
-        da[j] = make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(d0 & 0xffffu))),
-                            __half2float(__ushort_as_half(static_cast<unsigned short>(d1 & 0xffffu))));
     }
     const uint8_t *rlo = wpiece + g * kSbRowBytes;  // row g of the tile
     const uint8_t *rhi = rlo + 8 * kSbRowBytes;      // row g + 8
@@ -509,6 +511,63 @@ __device__ __forceinline__ void sb_block(const uint8_t *wpiece, const uint8_t *s
         acc[j][0] = __ffma2_rn(__fmul2_rn(make_float2(dlo, dlo), da[j]), make_float2(c[0], c[1]), acc[j][0]);
         acc[j][1] = __ffma2_rn(__fmul2_rn(make_float2(dhi, dhi), da[j]), make_float2(c[2], c[3]), acc[j][1]);
     }
+}
+
+__device__ __forceinline__ void mma_s8_16832(int (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same block for one token tile (t <= 8) on the int8 MMA: the codes enter
+// the tensor core as they are, with no widening, and the s32 result is the
+// same exact block dot.  One m16n8k32 covers the block: code words t4 and
+// t4 + 4 are its k ranges 4*t4.. and 16 + 4*t4.. for A and B alike.  One
+// tile needs about half of the int8 MMA rate at HBM speed; two tiles would
+// need more than all of it, so t > 8 keeps the f16 step.
+template <int BB>
+__device__ __forceinline__ void sb_block_s8(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
+                                            const float2 (&da)[1], float2 (&acc)[1][2])
+{
+    const uint2 v = sb_act<BB>(stage, pc, g, t4);
+    const uint8_t *rlo = wpiece + g * kSbRowBytes;  // row g of the tile
+    const uint8_t *rhi = rlo + 8 * kSbRowBytes;      // row g + 8
+    const uint2 clo = sb_codes<BB>(rlo, t4), chi = sb_codes<BB>(rhi, t4);
+    const float dlo = __half2float(*reinterpret_cast<const __half *>(rlo + 34 * BB));
+    const float dhi = __half2float(*reinterpret_cast<const __half *>(rhi + 34 * BB));
+    int c[4] = {0, 0, 0, 0};
+    mma_s8_16832(c, clo.x, chi.x, clo.y, chi.y, v.x, v.y);
+    acc[0][0] = __ffma2_rn(__fmul2_rn(make_float2(dlo, dlo), da[0]),
+                           make_float2(static_cast<float>(c[0]), static_cast<float>(c[1])), acc[0][0]);
+    acc[0][1] = __ffma2_rn(__fmul2_rn(make_float2(dhi, dhi), da[0]),
+                           make_float2(static_cast<float>(c[2]), static_cast<float>(c[3])), acc[0][1]);
+}
+
+// d_a of block BB from a token's eight d|ssum words of the stage
+__device__ __forceinline__ float sb_half_lo(uint32_t w)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+
+template <int BB, int NT>
+__device__ __forceinline__ void sb_step(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
+                                        const uint4 (&dsv)[NT][2][2], float2 (&acc)[NT][2])
+{
+    float2 da[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const uint4 &e = dsv[j][0][BB >> 2], &o = dsv[j][1][BB >> 2];  // tokens 8j + 2*t4, 8j + 2*t4 + 1
+        constexpr int q = BB & 3;
+        const uint32_t we = q == 0 ? e.x : q == 1 ? e.y : q == 2 ? e.z : e.w;
+        const uint32_t wo = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
+        da[j] = make_float2(sb_half_lo(we), sb_half_lo(wo));
+    }
+    if constexpr (NT == 1)
+        sb_block_s8<BB>(wpiece, stage, pc, g, t4, da, acc);
+    else
+        sb_block<BB, NT>(wpiece, stage, pc, g, t4, da, acc);
 }
 
 template <int NT>
@@ -606,14 +665,24 @@ gemv_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
             }
             const uint8_t *st = ring + s * kSbStageBytes;
             const uint8_t *wp = st + kSbOffW + tile * 16 * kSbRowBytes + pc * kSbPieceBytes;
-            sb_block<0, NT>(wp, st, pc, g, t4, acc);
-            sb_block<1, NT>(wp, st, pc, g, t4, acc);
-            sb_block<2, NT>(wp, st, pc, g, t4, acc);
-            sb_block<3, NT>(wp, st, pc, g, t4, acc);
-            sb_block<4, NT>(wp, st, pc, g, t4, acc);
-            sb_block<5, NT>(wp, st, pc, g, t4, acc);
-            sb_block<6, NT>(wp, st, pc, g, t4, acc);
-            sb_block<7, NT>(wp, st, pc, g, t4, acc);
+            uint4 dsv[NT][2][2];  // [tile][token 2*t4 + e][blocks 0-3, 4-7]: the stage's d|ssum words
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint4 *dw = reinterpret_cast<const uint4 *>(st + kSbOffDs + 4 * kSbGroup * pc +
+                                                                      (8 * j + 2 * t4 + e) * (32 * kSbPieces));
+                    dsv[j][e][0] = dw[0];
+                    dsv[j][e][1] = dw[1];
+                }
+            sb_step<0, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<1, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<2, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<3, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<4, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<5, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<6, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<7, NT>(wp, st, pc, g, t4, dsv, acc);
             __syncwarp();
             if (lane == 0) q8::mbar_arrive(&empty[s]);
         }
