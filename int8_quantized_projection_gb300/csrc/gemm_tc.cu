@@ -438,36 +438,60 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 // Pre-pass over the weights: codes -> f16 [n][k] (exact) and each block's d_w
 // as f32 into dwt[row tile][block][dw_slot(row % 128)] (0 for rows past n).
-__global__ void __launch_bounds__(256)
+// A warp takes 32 consecutive blocks of a row at a time (1088 bytes, 16-byte
+// aligned because k/32 % 8 == 0): coalesced 16-byte loads into shared memory,
+// then lane j widens block j from there and writes its 64 bytes of f16.
+constexpr int kPrepWarps = 8;
+constexpr int kPrepBlocks = 32;                     // blocks per warp item
+constexpr int kPrepBytes = kPrepBlocks * 34;         // 1088 = 68 x 16
+__global__ void __launch_bounds__(32 * kPrepWarps)
 gemm_prep_w_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, uint4 *__restrict__ a16, float *__restrict__ dwt)
 {
+    __shared__ __align__(16) uint8_t buf[kPrepWarps][kPrepBytes];
     q8::griddep_launch_dependents();
     q8::griddep_wait();  // the previous call may still read this workspace
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles = (n + BM - 1) / BM;
-    const int64_t total = tiles * BM * nb;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / nb;  // row (consecutive threads: consecutive blocks of a row)
-        const int b = static_cast<int>(i - r * nb);
+    const int chunks = (nb + kPrepBlocks - 1) / kPrepBlocks;  // per row
+    const int64_t items = tiles * BM * chunks;
+    uint8_t *mb = buf[warp];
+    for (int64_t it = (static_cast<int64_t>(blockIdx.x) * kPrepWarps + warp); it < items;
+         it += static_cast<int64_t>(gridDim.x) * kPrepWarps) {
+        const int64_t r = it / chunks;
+        const int c = static_cast<int>(it - r * chunks);
+        const int b0 = c * kPrepBlocks;
+        const int cb = min(kPrepBlocks, nb - b0);  // a multiple of 8
         const int64_t tile = r / BM;
+        const int j = lane, b = b0 + j;
         float dw = 0.0f;
         if (r < n) {
-            const uint16_t *blk = reinterpret_cast<const uint16_t *>(w + (r * nb + b) * 34);
-            dw = __half2float(__ushort_as_half(__ldg(blk)));
-            uint32_t qw[8];
+            const uint4 *src = reinterpret_cast<const uint4 *>(w + (r * nb + b0) * 34);
+            const int n16 = cb * 34 / 16;
+            for (int i = lane; i < n16; i += 32) reinterpret_cast<uint4 *>(mb)[i] = __ldg(src + i);
+            __syncwarp();
+            if (j < cb) {
+                // block j at byte 34j: its d at 34j, codes from 34j + 2; nine
+                // words from the word holding byte 34j cover both
+                const int base = (34 * j) >> 2, odd = j & 1;  // 34j % 4 == 2 for odd j
+                const uint32_t *wd = reinterpret_cast<const uint32_t *>(mb) + base;
+                uint32_t W[9];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                qw[u] = static_cast<uint32_t>(__ldg(blk + 1 + 2 * u)) | (static_cast<uint32_t>(__ldg(blk + 2 + 2 * u)) << 16);
-            uint4 *dst = a16 + (r * nb + b) * 4;  // 64 bytes of f16 per block
+                for (int u = 0; u < 9; ++u) W[u] = wd[u];
+                dw = __half2float(__ushort_as_half(static_cast<unsigned short>(odd ? (W[0] >> 16) : (W[0] & 0xffffu))));
+                uint4 *dst = a16 + (r * nb + b) * 4;  // 64 bytes of f16 per block
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                uint4 o;
-                q8::i8x4_to_f16x4(qw[2 * u], o.x, o.y);
-                q8::i8x4_to_f16x4(qw[2 * u + 1], o.z, o.w);
-                dst[u] = o;
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t q0 = odd ? W[2 * u + 1] : __byte_perm(W[2 * u], W[2 * u + 1], 0x5432);
+                    const uint32_t q1 = odd ? W[2 * u + 2] : __byte_perm(W[2 * u + 1], W[2 * u + 2], 0x5432);
+                    uint4 o;
+                    q8::i8x4_to_f16x4(q0, o.x, o.y);
+                    q8::i8x4_to_f16x4(q1, o.z, o.w);
+                    dst[u] = o;
+                }
             }
+            __syncwarp();  // the buffer is reused by the next item
         }
-        dwt[(tile * nb + b) * BM + dw_slot(static_cast<int>(r - tile * BM))] = dw;
+        if (j < cb) dwt[(tile * nb + b) * BM + dw_slot(static_cast<int>(r - tile * BM))] = dw;
     }
 }
 
@@ -563,10 +587,10 @@ int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const 
         return Q8_ERR_LAUNCH;
     const int sms = device_sm_count();
     const int64_t pcap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
-    const int64_t wwork = (n + BM - 1) / BM * BM * nb;
-    int64_t wgrid = (wwork + 255) / 256;
+    const int64_t witems = (n + BM - 1) / BM * BM * ((nb + kPrepBlocks - 1) / kPrepBlocks);
+    int64_t wgrid = (witems + kPrepWarps - 1) / kPrepWarps;
     wgrid = wgrid < pcap ? wgrid : pcap;
-    int st = launch_pdl(gemm_prep_w_kernel, dim3(static_cast<unsigned>(wgrid)), dim3(256), 0, s,
+    int st = launch_pdl(gemm_prep_w_kernel, dim3(static_cast<unsigned>(wgrid)), dim3(32 * kPrepWarps), 0, s,
                         static_cast<const uint8_t *>(w), n, static_cast<int>(nb), reinterpret_cast<uint4 *>(a16), dwt);
     if (st != Q8_OK) return st;
     const int64_t awork = t * (k / 16) + (t + BN - 1) / BN * nb * BN;
