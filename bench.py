@@ -483,6 +483,98 @@ def run_asym(torch, q8p, steps, warmup, dev):
 
 
 # ---------------------------------------------------------------------------
+# layer-stack decode: every projection of a 28-layer d = 3584 model and its
+# LM head for one token (batch 1), recorded as one CUDA graph
+# ---------------------------------------------------------------------------
+LAYERS = dict(layers=28, d=3584, nf=18944, q=3584, kv=512, vocab=152064, eps=1e-6)
+
+
+def layer_groups():
+    """One layer's launches of projections: (activation width k, [rows of each projection])."""
+    L = LAYERS
+    d, nf = L["d"], L["nf"]
+    return [(d, [L["q"], L["kv"], L["kv"]]), (d, [d]), (d, [nf, nf]), (nf, [d])]
+
+
+def bytes_gemv_group(k, ns):
+    # every projection's weights and outputs, the shared activation read once
+    return sum(n * (k // 32) * 34 + 4 * n for n in ns) + k + 4 * (k // 32)
+
+
+def bytes_layer_stack():
+    L = LAYERS
+    d, nf = L["d"], L["nf"]
+    producers = 2 * bytes_rmsnorm_quant(1, d, False) + bytes_quantize(1, d) + bytes_swiglu_quant(1, nf, False)
+    per_layer = producers + sum(bytes_gemv_group(k, ns) for k, ns in layer_groups())
+    return L["layers"] * per_layer + bytes_rmsnorm_quant(1, d, False) + bytes_gemv_group(d, [L["vocab"]])
+
+
+def run_layers(torch, q8p, steps, warmup, dev):
+    """Per layer: rmsnorm_quant -> q/k/v (one grouped launch); quantize of the
+    attention output -> o; rmsnorm_quant -> gate/up (one grouped launch);
+    swiglu_quant of their outputs -> down.  Then the final norm and the LM
+    head.  The producers run in mode 2 (their consumers read only the plane).
+    Layer 0's matrices are drawn from the synthetic recipe; layers 1..27 are
+    device copies of them (the same bytes, distinct memory, so every token
+    streams all 7.5 GB from HBM)."""
+    L = LAYERS
+    d, nf, eps = L["d"], L["nf"], L["eps"]
+    g = syn.rng(4, 0)
+    shapes = [(n, k) for k, ns in layer_groups() for n in ns]  # q k v o gate up down
+    host = [syn.q8_0_weights(syn.rng(4, 0, i), n, k)[0] for i, (n, k) in enumerate(shapes)]
+    head_h = syn.q8_0_weights(syn.rng(4, 0, len(shapes)), L["vocab"], d)[0]
+    layers = [[torch.from_numpy(w).to(dev) for w in host] for _ in range(L["layers"])]
+    head = torch.from_numpy(head_h).to(dev)
+    del host, head_h
+    x = torch.from_numpy(syn.activations(g, 1, d)).to(dev)        # hidden state entering each layer
+    attn = torch.from_numpy(syn.activations(g, 1, d)).to(dev)     # attention output
+    h = torch.from_numpy(syn.activations(g, 1, d)).to(dev)        # hidden state after attention
+    nw1, nw2, nwf = (torch.from_numpy(syn.uniform(g, d, 0.5, 1.5)).to(dev) for _ in range(3))
+    pd, pf = q8p.empty_plane(1, d, dev), q8p.empty_plane(1, nf, dev)
+    ys = [torch.empty((1, n), dtype=torch.float32, device=dev) for n, _ in shapes]
+    logits = torch.empty(L["vocab"], dtype=torch.float32, device=dev)
+    cap = torch.cuda.Stream(dev)
+    calls = []
+    for wl in layers:
+        wq, wk, wv, wo, wg, wu, wd = wl
+        calls += [q8p.rmsnorm_quant(x, nw1, eps, None, *pd, stream=cap, bind=True),
+                  q8p.q8_0_gemv_grouped([(wq, L["q"], ys[0]), (wk, L["kv"], ys[1]), (wv, L["kv"], ys[2])], d, *pd,
+                                        stream=cap, bind=True),
+                  q8p.quantize_q8_0(attn, *pd, stream=cap, bind=True),
+                  q8p.q8_0_gemv(wo, d, d, *pd, ys[3], stream=cap, bind=True),
+                  q8p.rmsnorm_quant(h, nw2, eps, None, *pd, stream=cap, bind=True),
+                  q8p.q8_0_gemv_grouped([(wg, nf, ys[4]), (wu, nf, ys[5])], d, *pd, stream=cap, bind=True),
+                  q8p.swiglu_quant(ys[4], ys[5], None, *pf, stream=cap, bind=True),
+                  q8p.q8_0_gemv(wd, d, nf, *pf, ys[6], stream=cap, bind=True)]
+    calls += [q8p.rmsnorm_quant(x, nwf, eps, None, *pd, stream=cap, bind=True),
+              q8p.q8_0_gemv(head, L["vocab"], d, *pd, logits, stream=cap, bind=True)]
+
+    stream = torch.cuda.current_stream(dev)
+    cap.wait_stream(stream)
+    for _ in range(max(1, warmup)):  # eager, outside the capture
+        for c in calls:
+            c()
+    q8p.q8_check()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for c in calls:
+            c()
+    stream.wait_stream(cap)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    q8p.q8_check()
+    return dict(ms=t0.elapsed_time(t1) / steps, launches=len(calls),
+                weight_bytes=sum(w.numel() for w in layers[0]) * L["layers"] + head.numel())
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle (reported baseline and the reference arm)
 # ---------------------------------------------------------------------------
 def oracle_decode_sample(budget_s):
@@ -567,7 +659,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "small", "asym"],
+    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "small", "asym", "layers"],
                     help="decode and/or prefill legs (profiling runs select one)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()
@@ -619,10 +711,16 @@ def main():
         asym = run_asym(torch, q8p, args.steps if args.workload == "asym" else max(20, args.steps // 30),
                         args.warmup, dev)
 
+    lay = None
+    if args.workload in ("all", "layers"):
+        lay = run_layers(torch, q8p, args.steps if args.workload == "layers" else max(10, args.steps // 200),
+                         args.warmup, dev)
+
     if world > 1:  # every duration becomes the slowest rank's (same legs on every rank)
         vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"]] if dec else [])
                 + (list(pre.values()) if pre else [])
-                + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else []))
+                + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else [])
+                + ([lay["ms"]] if lay else []))
         red = max_over_ranks(torch, vals, dev)
         if dec:
             dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"] = red[:4]
@@ -634,6 +732,8 @@ def main():
             small["us"], small["us_b2b"] = red.pop(0), red.pop(0)
         if asym:
             asym["us"], asym["us_b2b"] = red.pop(0), red.pop(0)
+        if lay:
+            lay["ms"] = red.pop(0)
 
     if rank != 0:
         if world > 1:
@@ -731,6 +831,27 @@ def main():
                          "config": {"workload": aobj["workload"], "l2": aobj["l2"], "parallelism": "replicas"},
                          "roofline": aobj["roofline"], "gpu_launches": 2 * args.steps})
         line["asym_gemv"] = aobj
+    if lay is not None:
+        L = LAYERS
+        byts = bytes_layer_stack()
+        gbs = byts / (lay["ms"] / 1e3) / 1e9
+        lobj = {"workload": f"layer-stack decode b=1: {L['layers']} layers (d={L['d']}, nf={L['nf']}; q {L['q']}, "
+                            f"k/v {L['kv']}, o, gate/up, down) + LM head {L['vocab']}x{L['d']}; per layer "
+                            "rmsnorm_quant, grouped q/k/v, quantize, o, rmsnorm_quant, grouped gate/up, swiglu_quant, "
+                            "down (producers in mode 2)",
+                "ms_per_token": round(lay["ms"], 4), "tokens_per_s": round(1e3 / lay["ms"], 1),
+                "gbs": round(gbs, 1), "algorithmic_bytes": byts, "weight_bytes": lay["weight_bytes"],
+                "launches_per_token": lay["launches"],
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(gbs / peaks["hbm_gbs"], 4)},
+                "launch": "one CUDA graph per token, replayed; layers 1..27 are device copies of layer 0's matrices "
+                          "(distinct memory: 7.5 GB streamed per token, > L2)"}
+        if args.workload == "layers":
+            line.update({"value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": lobj["ms_per_token"],
+                         "config": {"workload": lobj["workload"], "l2": "7.5 GB of weights per token > L2",
+                                    "parallelism": "replicas"},
+                         "roofline": lobj["roofline"], "gpu_launches": lay["launches"] * args.steps})
+        line["layer_stack"] = lobj
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
