@@ -70,6 +70,10 @@ quantize_q8_0_kernel(const float4 *__restrict__ x, int64_t n4_valid, int64_t n4_
 // registers.  "54 - r51 - producer-fused A-quantize mode 1", sec. 3.2:
 // ss = sum x^2, scale = rsqrt(ss/d + eps), y = (x * scale) * w.
 // --------------------------------------------------------------------------
+// widest row whose weight vector is staged in shared memory (32 KB: below the
+// 48 KB a kernel may use without opting in)
+constexpr int kNormSmemMax = 8192;
+
 template <int J>
 __global__ void __launch_bounds__(512)
 rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, float eps,
@@ -77,14 +81,22 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
                      uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
     __shared__ float red[2][32];
-    q8::griddep_launch_dependents();  // consumers may start their prologue
-    q8::griddep_wait();               // inputs may come from the previous kernel
+    extern __shared__ float4 wsm[];   // the weight vector, when it is staged (d <= kNormSmemMax)
     const int F = d >> 2;
     const int P = blockDim.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int nw = P >> 5;
+    const bool staged = d <= kNormSmemMax;
     const float4 *w4 = reinterpret_cast<const float4 *>(w);
+    q8::griddep_launch_dependents();  // consumers may start their prologue
+    // The weight vector is a constant input, the same for every row: stage it
+    // in shared memory before waiting for the previous kernel, so a row costs
+    // one memory round trip (its own) instead of two.  Ordered before its
+    // first use by the barrier in the first row's reduction.
+    if (staged)
+        for (int f = tid; f < F; f += P) wsm[f] = __ldg(w4 + f);
+    q8::griddep_wait();               // inputs may come from the previous kernel
 
     auto load_row = [&](int64_t t, float4 (&v)[J]) {
         const float4 *xr = reinterpret_cast<const float4 *>(x + t * static_cast<int64_t>(d));
@@ -132,7 +144,7 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
                 const bool ok = f < F;  // uniform over each 8-lane block group
                 float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (ok) {
-                    const float4 wv = __ldg(w4 + f);
+                    const float4 wv = staged ? wsm[f] : __ldg(w4 + f);
                     o.x = __fmul_rn(__fmul_rn(v[j].x, scale), wv.x);
                     o.y = __fmul_rn(__fmul_rn(v[j].y, scale), wv.y);
                     o.z = __fmul_rn(__fmul_rn(v[j].z, scale), wv.z);
@@ -259,12 +271,13 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     const dim3 grid(static_cast<unsigned>(rows_pad < cap ? rows_pad : cap));
     uint32_t *q32 = reinterpret_cast<uint32_t *>(qs);
     const int di = static_cast<int>(d);
+    const size_t wsmem = d <= kNormSmemMax ? static_cast<size_t>(d) * 4 : 0;
     switch (J) {
-    case 1: return q8::launch_pdl(rmsnorm_quant_kernel<1>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
-    case 2: return q8::launch_pdl(rmsnorm_quant_kernel<2>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
-    case 4: return q8::launch_pdl(rmsnorm_quant_kernel<4>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
-    case 8: return q8::launch_pdl(rmsnorm_quant_kernel<8>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
-    default: return q8::launch_pdl(rmsnorm_quant_kernel<16>, grid, dim3(P), 0, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    case 1: return q8::launch_pdl(rmsnorm_quant_kernel<1>, grid, dim3(P), wsmem, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    case 2: return q8::launch_pdl(rmsnorm_quant_kernel<2>, grid, dim3(P), wsmem, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    case 4: return q8::launch_pdl(rmsnorm_quant_kernel<4>, grid, dim3(P), wsmem, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    case 8: return q8::launch_pdl(rmsnorm_quant_kernel<8>, grid, dim3(P), wsmem, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    default: return q8::launch_pdl(rmsnorm_quant_kernel<16>, grid, dim3(P), wsmem, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
     }
 }
 
