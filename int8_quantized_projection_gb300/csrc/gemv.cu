@@ -409,6 +409,9 @@ gemv_generic_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, const int8
 #ifndef Q8_SB_PIECES
 #define Q8_SB_PIECES 1
 #endif
+#ifndef Q8_SB_S8_TILES
+#define Q8_SB_S8_TILES 1  // token tiles up to which the block step runs on the int8 MMA
+#endif
 #ifndef Q8_SB_STAGES
 #define Q8_SB_STAGES 2
 #endif
@@ -527,22 +530,25 @@ __device__ __forceinline__ void mma_s8_16832(int (&c)[4], uint32_t a0, uint32_t 
 // t4 + 4 are its k ranges 4*t4.. and 16 + 4*t4.. for A and B alike.  One
 // tile needs about half of the int8 MMA rate at HBM speed; two tiles would
 // need more than all of it, so t > 8 keeps the f16 step.
-template <int BB>
+template <int BB, int NT>
 __device__ __forceinline__ void sb_block_s8(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
-                                            const float2 (&da)[1], float2 (&acc)[1][2])
+                                            const float2 (&da)[NT], float2 (&acc)[NT][2])
 {
-    const uint2 v = sb_act<BB>(stage, pc, g, t4);
     const uint8_t *rlo = wpiece + g * kSbRowBytes;  // row g of the tile
     const uint8_t *rhi = rlo + 8 * kSbRowBytes;      // row g + 8
     const uint2 clo = sb_codes<BB>(rlo, t4), chi = sb_codes<BB>(rhi, t4);
     const float dlo = __half2float(*reinterpret_cast<const __half *>(rlo + 34 * BB));
     const float dhi = __half2float(*reinterpret_cast<const __half *>(rhi + 34 * BB));
-    int c[4] = {0, 0, 0, 0};
-    mma_s8_16832(c, clo.x, chi.x, clo.y, chi.y, v.x, v.y);
-    acc[0][0] = __ffma2_rn(__fmul2_rn(make_float2(dlo, dlo), da[0]),
-                           make_float2(static_cast<float>(c[0]), static_cast<float>(c[1])), acc[0][0]);
-    acc[0][1] = __ffma2_rn(__fmul2_rn(make_float2(dhi, dhi), da[0]),
-                           make_float2(static_cast<float>(c[2]), static_cast<float>(c[3])), acc[0][1]);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const uint2 v = sb_act<BB>(stage, pc, 8 * j + g, t4);
+        int c[4] = {0, 0, 0, 0};
+        mma_s8_16832(c, clo.x, chi.x, clo.y, chi.y, v.x, v.y);
+        acc[j][0] = __ffma2_rn(__fmul2_rn(make_float2(dlo, dlo), da[j]),
+                               make_float2(static_cast<float>(c[0]), static_cast<float>(c[1])), acc[j][0]);
+        acc[j][1] = __ffma2_rn(__fmul2_rn(make_float2(dhi, dhi), da[j]),
+                               make_float2(static_cast<float>(c[2]), static_cast<float>(c[3])), acc[j][1]);
+    }
 }
 
 // d_a of block BB from a token's eight d|ssum words of the stage
@@ -564,8 +570,8 @@ __device__ __forceinline__ void sb_step(const uint8_t *wpiece, const uint8_t *st
         const uint32_t wo = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
         da[j] = make_float2(sb_half_lo(we), sb_half_lo(wo));
     }
-    if constexpr (NT == 1)
-        sb_block_s8<BB>(wpiece, stage, pc, g, t4, da, acc);
+    if constexpr (NT <= Q8_SB_S8_TILES)
+        sb_block_s8<BB, NT>(wpiece, stage, pc, g, t4, da, acc);
     else
         sb_block<BB, NT>(wpiece, stage, pc, g, t4, da, acc);
 }
