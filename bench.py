@@ -293,59 +293,77 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
 
     # end to end through the public API with host buffers (weights resident).
-    # A serving loop records its step once -- the host-to-device copies of the
-    # inputs from pinned memory, the library calls, the device-to-host copies of
-    # the outputs -- as a CUDA graph, then replays it every step and
-    # synchronises to read the outputs (`e2e_s`); `e2e_eager_s` times the same
-    # step issued call by call from the host.
-    xh = x_all.cpu().pin_memory()
-    yh = torch.empty(y_all.shape, dtype=torch.float32).pin_memory()
+    # A serving loop records its step once -- the host-to-device copy of the
+    # inputs from pinned memory, the library calls, the device-to-host copy of
+    # the outputs -- as a CUDA graph and replays it every step.  It keeps one
+    # step in flight: it enqueues step i, then waits for step i-1 and reads its
+    # outputs, so the host's launch and wake-up overlap the GPU's work; host
+    # buffers alternate between steps, so a step never writes the buffer the
+    # host is reading (`e2e_s`).  `e2e_serial_s` waits for every step before
+    # enqueuing the next; `e2e_eager_s` also issues the step call by call.
+    xh = [x_all.cpu().pin_memory() for _ in range(2)]
+    yh = [torch.empty(y_all.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
 
-    def e2e_body(i):  # on the capture streams: the inputs in, one step, the outputs out
-        x_all.copy_(xh, non_blocking=True)
+    def e2e_body(i, par):  # on the capture streams: the inputs in, one step, the outputs out
+        x_all.copy_(xh[par], non_blocking=True)
         side.wait_stream(cap)
         quant_main()
         gemvs_c[i][0]()
         quant_side()
         gemvs_c[i][1]()
         cap.wait_stream(side)
-        yh.copy_(y_all, non_blocking=True)
+        yh[par].copy_(y_all, non_blocking=True)
 
     cap.wait_stream(stream)
     with torch.cuda.stream(cap):
         for i in range(copies):  # once outside the capture
-            e2e_body(i)
+            e2e_body(i, i % 2)
     stream.wait_stream(cap)
-    e2e_graphs = []
+    e2e_graphs = []  # [weight copy][host buffer]
     for i in range(copies):
-        gi = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gi, stream=cap):
-            e2e_body(i)
-        e2e_graphs.append(gi)
+        pair = []
+        for par in range(2):
+            gi = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gi, stream=cap):
+                e2e_body(i, par)
+            pair.append(gi)
+        e2e_graphs.append(pair)
     torch.cuda.synchronize(dev)
+    done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def e2e_step(i):
-        e2e_graphs[i % copies].replay()
-        stream.synchronize()
+    def e2e_run(n, start):  # one step in flight
+        for j in range(n):
+            i = start + j
+            e2e_graphs[i % copies][i % 2].replay()
+            done[i % 2].record(stream)
+            if j > 0:
+                done[(i - 1) % 2].synchronize()  # step i-1's outputs are in yh[(i-1) % 2]
+        done[(start + n - 1) % 2].synchronize()
 
-    def e2e_eager_step(i):
-        x_all.copy_(xh, non_blocking=True)
-        step(i)
-        yh.copy_(y_all, non_blocking=True)
-        stream.synchronize()
+    def e2e_serial_run(n, start):
+        for j in range(n):
+            i = start + j
+            e2e_graphs[i % copies][i % 2].replay()
+            stream.synchronize()
+
+    def e2e_eager_run(n, start):
+        for j in range(n):
+            x_all.copy_(xh[0], non_blocking=True)
+            step(start + j)
+            yh[0].copy_(y_all, non_blocking=True)
+            stream.synchronize()
 
     res = {}
-    for name, fn in (("e2e_s", e2e_step), ("e2e_eager_s", e2e_eager_step)):
-        for i in range(warmup):
-            fn(i)
+    for name, fn in (("e2e_s", e2e_run), ("e2e_serial_s", e2e_serial_run), ("e2e_eager_s", e2e_eager_run)):
+        fn(warmup, 0)
         torch.cuda.synchronize(dev)
         e0 = time.perf_counter()
-        for i in range(steps):
-            fn(warmup + i)
+        fn(steps, warmup)
         res[name] = time.perf_counter() - e0
         q8p.q8_check()
-    e2e_s, e2e_eager_s = res["e2e_s"], res["e2e_eager_s"]
-    return dict(ms=ms, kern_ms=kern_ms, clocks=clocks, e2e_s=e2e_s, e2e_eager_s=e2e_eager_s, copies=copies,
+    e2e_s, e2e_serial_s, e2e_eager_s = res["e2e_s"], res["e2e_serial_s"], res["e2e_eager_s"]
+    return dict(ms=ms, kern_ms=kern_ms, clocks=clocks, e2e_s=e2e_s, e2e_serial_s=e2e_serial_s, e2e_eager_s=e2e_eager_s,
+                copies=copies,
                 h2d=sum(v.nbytes for v in xs_h.values()), d2h=4 * sum(n for n, _ in DECODE_SHAPES))
 
 
@@ -717,14 +735,14 @@ def main():
                          args.warmup, dev)
 
     if world > 1:  # every duration becomes the slowest rank's (same legs on every rank)
-        vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"]] if dec else [])
+        vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"]] if dec else [])
                 + (list(pre.values()) if pre else [])
                 + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else [])
                 + ([lay["ms"]] if lay else []))
         red = max_over_ranks(torch, vals, dev)
         if dec:
-            dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"] = red[:4]
-            red = red[4:]
+            dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"] = red[:5]
+            red = red[5:]
         if pre:
             pre = dict(zip(pre.keys(), red[:len(pre)]))
             red = red[len(pre):]
@@ -760,8 +778,10 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": round(world * step_bytes * args.steps / dec["e2e_s"] / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"],
-                    "launch": "per step: one CUDA graph replay (pinned-memory copies in, the library calls, copies "
-                              "out; recorded once), then a host synchronise",
+                    "launch": "per step: one CUDA graph replay (pinned-memory copy in, the library calls, copy out; "
+                              "recorded once); one step in flight: the host reads step i-1's outputs after enqueuing "
+                              "step i (host buffers alternate)",
+                    "serial_value": round(world * step_bytes * args.steps / dec["e2e_serial_s"] / 1e9, 2),
                     "eager_value": round(world * step_bytes * args.steps / dec["e2e_eager_s"] / 1e9, 2)},
             "clocks": dec["clocks"],
             "gpu_launches": 4 * args.steps,
