@@ -501,6 +501,60 @@ def run_asym(torch, q8p, steps, warmup, dev):
 
 
 # ---------------------------------------------------------------------------
+# shared-activation decode: one RMSNorm-quantized activation feeding four
+# projections (q, k, v, gate) in one grouped launch
+# ---------------------------------------------------------------------------
+SHARED = dict(d=7168, ns=[3072, 512, 512, 3072], eps=1e-6)
+
+
+def bytes_shared():
+    d = SHARED["d"]
+    return bytes_rmsnorm_quant(1, d, False) + bytes_gemv_group(d, SHARED["ns"])
+
+
+def run_shared(torch, q8p, steps, warmup, dev):
+    """rmsnorm_quant (mode 2) -> q8_0_gemv_grouped over the four projections:
+    two launches per step, recorded as a CUDA graph of one step per weight
+    copy (copies together > 4 x L2)."""
+    d, ns, eps = SHARED["d"], SHARED["ns"], SHARED["eps"]
+    g = syn.rng(2, 0)
+    x = torch.from_numpy(syn.activations(g, 1, d)).to(dev)
+    nw = torch.from_numpy(syn.uniform(g, d, 0.5, 1.5)).to(dev)
+    host = [syn.q8_0_weights(syn.rng(2, 1 + i), n, d)[0] for i, n in enumerate(ns)]
+    per_copy = sum(w.nbytes for w in host)
+    copies = max(2, -(-4 * L2_BYTES // per_copy))
+    ws = [[torch.from_numpy(w).to(dev) for w in host] for _ in range(copies)]
+    plane = q8p.empty_plane(1, d, dev)
+    ys = [torch.empty(n, dtype=torch.float32, device=dev) for n in ns]
+    cap = torch.cuda.Stream(dev)
+    norm = q8p.rmsnorm_quant(x, nw, eps, None, *plane, stream=cap, bind=True)
+    gemvs = [q8p.q8_0_gemv_grouped(list(zip(wset, ns, ys)), d, *plane, stream=cap, bind=True) for wset in ws]
+    stream = torch.cuda.current_stream(dev)
+    cap.wait_stream(stream)
+    for i in range(max(copies, warmup)):
+        norm()
+        gemvs[i % copies]()
+    q8p.q8_check()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for i in range(copies):
+            norm()
+            gemvs[i]()
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(1, steps // copies)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    q8p.q8_check()
+    return dict(us=1e3 * t0.elapsed_time(t1) / (reps * copies), copies=copies, steps=reps * copies)
+
+
+# ---------------------------------------------------------------------------
 # layer-stack decode: every projection of a 28-layer d = 3584 model and its
 # LM head for one token (batch 1), recorded as one CUDA graph
 # ---------------------------------------------------------------------------
@@ -677,7 +731,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "small", "asym", "layers"],
+    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "small", "asym", "shared", "layers"],
                     help="decode and/or prefill legs (profiling runs select one)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args()
@@ -729,6 +783,11 @@ def main():
         asym = run_asym(torch, q8p, args.steps if args.workload == "asym" else max(20, args.steps // 30),
                         args.warmup, dev)
 
+    shr = None
+    if args.workload in ("all", "shared"):
+        shr = run_shared(torch, q8p, args.steps if args.workload == "shared" else max(60, args.steps // 10),
+                         args.warmup, dev)
+
     lay = None
     if args.workload in ("all", "layers"):
         lay = run_layers(torch, q8p, args.steps if args.workload == "layers" else max(10, args.steps // 200),
@@ -738,7 +797,7 @@ def main():
         vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"]] if dec else [])
                 + (list(pre.values()) if pre else [])
                 + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else [])
-                + ([lay["ms"]] if lay else []))
+                + ([lay["ms"]] if lay else []) + ([shr["us"]] if shr else []))
         red = max_over_ranks(torch, vals, dev)
         if dec:
             dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"] = red[:5]
@@ -752,6 +811,8 @@ def main():
             asym["us"], asym["us_b2b"] = red.pop(0), red.pop(0)
         if lay:
             lay["ms"] = red.pop(0)
+        if shr:
+            shr["us"] = red.pop(0)
 
     if rank != 0:
         if world > 1:
@@ -851,6 +912,22 @@ def main():
                          "config": {"workload": aobj["workload"], "l2": aobj["l2"], "parallelism": "replicas"},
                          "roofline": aobj["roofline"], "gpu_launches": 2 * args.steps})
         line["asym_gemv"] = aobj
+    if shr is not None:
+        byts = bytes_shared()
+        gbs = byts / (shr["us"] / 1e6) / 1e9
+        sobj2 = {"workload": f"shared-activation decode b=1: rmsnorm_quant (d={SHARED['d']}, mode 2) -> q/k/v/gate "
+                             f"{'/'.join(str(n) for n in SHARED['ns'])} in one grouped GEMV launch",
+                 "us_per_step": round(shr["us"], 2), "gbs": round(gbs, 1), "algorithmic_bytes": byts,
+                 "launches_per_step": 2,
+                 "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": round(gbs / peaks["hbm_gbs"], 4)},
+                 "launch": f"CUDA graph of one step per weight copy ({shr['copies']} copies > 4 x L2), replayed"}
+        if args.workload == "shared":
+            line.update({"value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": round(shr["us"] / 1e3, 5),
+                         "config": {"workload": sobj2["workload"], "l2": f"{shr['copies']} weight copies > 4 x L2",
+                                    "parallelism": "replicas"},
+                         "roofline": sobj2["roofline"], "gpu_launches": 2 * shr["steps"]})
+        line["shared_activation"] = sobj2
     if lay is not None:
         L = LAYERS
         byts = bytes_layer_stack()

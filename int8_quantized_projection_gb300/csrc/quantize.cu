@@ -259,11 +259,15 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     if (rows > 0 && (!q8::aligned16(x) || !q8::aligned16(w) || (y && !q8::aligned16(y)))) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     const int F = static_cast<int>(d / 4);
-    int J = 1;
-    while (J < 16 && (F + J - 1) / J > 256) J *= 2;
-    const int P = ((F + J - 1) / J + 31) / 32 * 32;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int sms = q8::device_sm_count();
+    // float4 per thread: up to 256 threads per row when CTAs take several rows
+    // (four CTAs per SM keep four rows in flight), up to 512 when every CTA
+    // has at most one row (a decode token: shorter chains per thread)
+    const int max_p = rows_pad <= (sms > 0 ? sms : 152) ? 512 : 256;
+    int J = 1;
+    while (J < 16 && (F + J - 1) / J > max_p) J *= 2;
+    const int P = ((F + J - 1) / J + 31) / 32 * 32;
     // persistent grid: enough CTAs to fill the SMs (registers allow ~4 per SM
     // at these block sizes), each walking rows with a stride of the grid
     const int64_t per_sm = P <= 256 ? 4 : 2;
