@@ -211,6 +211,26 @@ Q8_API int q4a_gemv(const void *w, int64_t n, int64_t k,
                     const int8_t *qs, const uint32_t *ds, float *y, void *stream);
 
 /*
+ * q4a_gemv_batched -- the asymmetric 4-bit projection for a few tokens at
+ * once, the weights streamed from HBM once for all of them:
+ *     Y[t][i] = sum_b ( d*d_a(t,b) * sum_e nib_e*q_e(t)  -  m*d_a(t,b) * ssum(t,b) )
+ * for tokens t < `tokens`.  Same weight blocks as q4a_gemv.
+ *   qs, ds : plane rows 0..tokens-1 (input; rows at and past `tokens` are not
+ *            read)
+ *   y      : f32 [tokens][n] (output)
+ * 1 <= tokens <= Q8_GEMV_MAX_TOKENS; k % 256 == 0 (8-block row pieces);
+ * tokens == 1 runs q4a_gemv.  Per block: the exact integer dot of the nibbles
+ * with the codes, then fma(d*d_a, isum) and fma(-(m*d_a), ssum) (scale
+ * products exact in f32).  Partial sums over k are added in a fixed order:
+ * results are run-to-run identical.  Errors: Q8_ERR_ARG (shape, tokens),
+ * Q8_ERR_ALIGN (a pointer not 16-byte aligned), Q8_ERR_DEVICE (not sm_103),
+ * Q8_ERR_LAUNCH.  Programmatic dependent launch as for q4a_gemv.
+ */
+Q8_API int q4a_gemv_batched(const void *w, int64_t n, int64_t k,
+                            const int8_t *qs, const uint32_t *ds, int64_t tokens,
+                            float *y, void *stream);
+
+/*
  * q8_0_gemm_workspace_bytes -- device workspace q8_0_gemm needs for n weight
  * rows, t tokens and width k: the weight codes as f16 (n*k*2 bytes), the
  * activation codes as f16 (t*k*2), and both sides' block scales as f32

@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     q8_0_gemv_grouped,
     q8_0_gemv_batched,
     q4a_gemv,
+    q4a_gemv_batched,
     GEMV_MAX_TOKENS,
     q8_check,
     q8_num_sms,

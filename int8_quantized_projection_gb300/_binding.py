@@ -39,6 +39,7 @@ SIGNATURES = {
     "q8_0_gemv_grouped": (_INT, [_P, _INT, _I64, _P, _P, _P]),
     "q8_0_gemv_batched": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P]),
     "q4a_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "q4a_gemv_batched": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P]),
     "q8_check": (_INT, [_P]),
     "q8_num_sms": (_INT, []),
 }
@@ -225,6 +226,16 @@ def q4a_gemv(w, n: int, k: int, qs, ds, y, stream=None, bind=False):
     if w.numel() != n * (k // 32) * 20 or y.numel() < n or qs.shape[-1] != k:
         raise ValueError("shape mismatch")
     return _launch("q4a_gemv", (_ptr(w), n, k, _ptr(qs), _ptr(ds), _ptr(y), _stream(stream)), bind)
+
+
+def q4a_gemv_batched(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=False):
+    """Asymmetric 4-bit weights, Y[t][n] f32 for plane rows [0, t), 1 <= t <= 16, weights read once for all t."""
+    import torch
+
+    _need(w, torch.uint8, "w"), _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds"), _need(y, torch.float32, "y")
+    if w.numel() != n * (k // 32) * 20 or y.numel() < t * n or qs.shape[-1] != k or qs.shape[0] < t:
+        raise ValueError("shape mismatch")
+    return _launch("q4a_gemv_batched", (_ptr(w), n, k, _ptr(qs), _ptr(ds), t, _ptr(y), _stream(stream)), bind)
 
 
 def q8_0_gemv_grouped(projs, k: int, qs, ds, stream=None, bind=False):

@@ -8,7 +8,7 @@ namespace q8 {
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSlots = 8;
+constexpr int kMaxSlots = 12;
 int g_sms[kMaxDevices];        // 0 = not queried yet
 int g_is103[kMaxDevices];      // 0 = unknown, 1 = yes, 2 = no
 int g_smem_set[kMaxDevices][kMaxSlots];

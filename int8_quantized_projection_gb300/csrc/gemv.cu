@@ -423,25 +423,86 @@ constexpr int kSbThreads = (kSbWarps + 1) * 32;          // + the producer warp
 constexpr int kSbPieces = Q8_SB_PIECES;                  // 8-block pieces per row and stage (1, 2 or 4)
 constexpr int kSbRows = 16 * kSbWarps / kSbPieces;       // weight rows per CTA
 constexpr int kSbTiles = kSbRows / 16;                   // 16-row MMA tiles per CTA
-constexpr int kSbGroup = 8;                              // Q8_0 blocks per piece
+constexpr int kSbGroup = 8;                              // weight blocks per piece
 constexpr int kSbMaxTokens = 16;
-constexpr int kSbPieceBytes = kSbGroup * 34;             // 272
-constexpr int kSbRowBytes = kSbPieces * kSbPieceBytes;   // weight bytes per row and stage
-// stage layout (offsets from a 1024-byte aligned stage base)
+// stage layout (offsets from a 1024-byte aligned stage base); the weight part
+// depends on the block format (SbLayout below)
 constexpr int kSbOffAct = 0;                             // 2*kSbPieces boxes x 16 tokens x 128 B, swizzled
 constexpr int kSbOffDs = kSbPieces * 4096;               // 16 tokens x 8*kSbPieces words
-constexpr int kSbOffW = kSbOffDs + kSbPieces * 512;      // kSbRows rows x kSbRowBytes
-constexpr int kSbStageTx = kSbOffW + kSbRows * kSbRowBytes;        // bytes the TMA writes per stage
-constexpr int kSbStageBytes = (kSbStageTx + 1023) / 1024 * 1024;  // stage stride
+constexpr int kSbOffW = kSbOffDs + kSbPieces * 512;      // kSbRows rows x the format's row bytes
 constexpr int kSbStages = Q8_SB_STAGES;
-constexpr int kSbOffBar = kSbStages * kSbStageBytes;     // full[], empty[], error flag
-constexpr int kSbSmem = kSbOffBar + 128 + 1024;          // + alignment slack
-constexpr int kSbCtasPerSm = 232448 / (kSbSmem + 1024);  // resident CTAs per SM (shared memory bound)
 constexpr int kSbMaxCluster = 8;
 static_assert(kSbPieces == 1 || kSbPieces == 2 || kSbPieces == 4, "pieces per stage");
 static_assert(kSbStages * 16 + 8 <= 128, "barrier area");
 static_assert(kSbOffW % 128 == 0, "TMA destination alignment");
-static_assert(kSbMaxTokens * kSbRows * kSbPieces * 4 <= kSbStages * kSbStageBytes, "partial sums reuse the ring");
+
+// Weight block formats of the small-batch kernel.  codes<BB>(row, t4) returns
+// the two 4-code words of block BB that thread t4 of a quad feeds the MMA (the
+// block's elements 4*t4.. and 16 + 4*t4.., matching the activation's words t4
+// and t4 + 4); d<BB> and m<BB> its scale and min.
+struct SbQ8_0 {  // 34-byte blocks: f16 d, 32 int8 codes
+    static constexpr int kBlockBytes = 34;
+    static constexpr bool kMin = false;
+    template <int BB>
+    __device__ static uint2 codes(const uint8_t *row, int t4)
+    {
+        constexpr int off = 34 * BB + 2;  // the codes of block BB (row pieces start 16-byte aligned)
+        if constexpr ((off & 3) == 0) {
+            const uint32_t *p = reinterpret_cast<const uint32_t *>(row + off);
+            return make_uint2(p[t4], p[t4 + 4]);
+        } else {
+            const uint32_t *p = reinterpret_cast<const uint32_t *>(row + off - 2);
+            return make_uint2(__byte_perm(p[t4], p[t4 + 1], 0x5432), __byte_perm(p[t4 + 4], p[t4 + 5], 0x5432));
+        }
+    }
+    template <int BB>
+    __device__ static float d(const uint8_t *row)
+    {
+        return __half2float(*reinterpret_cast<const __half *>(row + 34 * BB));
+    }
+    template <int BB>
+    __device__ static float m(const uint8_t *)
+    {
+        return 0.0f;
+    }
+};
+
+// Asymmetric 4-bit blocks (q4a_block.cuh): 20 bytes, f16 d, f16 m, then byte j
+// holding element j (low nibble) and element j + 16 (high nibble).  Nibble
+// word t4 is exactly the thread's pair: its low nibbles are elements
+// 4*t4.. and its high nibbles elements 16 + 4*t4.., as unsigned bytes 0..15.
+struct SbQ4A {
+    static constexpr int kBlockBytes = q8::kA4ChunkBytes / 4;
+    static constexpr bool kMin = true;
+    template <int BB>
+    __device__ static uint2 codes(const uint8_t *row, int t4)
+    {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(row + 20 * BB + 4 + 4 * t4);
+        return make_uint2(w & 0x0f0f0f0fu, (w >> 4) & 0x0f0f0f0fu);
+    }
+    template <int BB>
+    __device__ static float d(const uint8_t *row)
+    {
+        return __half2float(*reinterpret_cast<const __half *>(row + 20 * BB));
+    }
+    template <int BB>
+    __device__ static float m(const uint8_t *row)
+    {
+        return __half2float(*reinterpret_cast<const __half *>(row + 20 * BB + 2));
+    }
+};
+
+template <class W>
+struct SbLayout {
+    static constexpr int kPieceBytes = kSbGroup * W::kBlockBytes;   // 272 (Q8_0), 160 (Q4A): multiples of 16
+    static constexpr int kRowBytes = kSbPieces * kPieceBytes;       // weight bytes per row and stage
+    static constexpr int kStageTx = kSbOffW + kSbRows * kRowBytes;  // bytes the TMA writes per stage
+    static constexpr int kStageBytes = (kStageTx + 1023) / 1024 * 1024;
+    static constexpr int kOffBar = kSbStages * kStageBytes;         // full[], empty[], error flag
+    static constexpr int kSmem = kOffBar + 128 + 1024;              // + alignment slack
+    static_assert(kPieceBytes % 16 == 0, "TMA box rows");
+    static_assert(kSbMaxTokens * kSbRows * kSbPieces * 4 <= kSbStages * kStageBytes, "partial sums reuse the ring");
+};
 
 __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
@@ -449,21 +510,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Code words t4 and t4 + 4 of block BB of a staged row piece (piece start
-// 16-byte aligned, block BB at byte 34*BB, its codes from byte 34*BB + 2).
-template <int BB>
-__device__ __forceinline__ uint2 sb_codes(const uint8_t *piece, int t4)
-{
-    constexpr int off = 34 * BB + 2;
-    if constexpr ((off & 3) == 0) {
-        const uint32_t *p = reinterpret_cast<const uint32_t *>(piece + off);
-        return make_uint2(p[t4], p[t4 + 4]);
-    } else {
-        const uint32_t *p = reinterpret_cast<const uint32_t *>(piece + off - 2);
-        return make_uint2(__byte_perm(p[t4], p[t4 + 1], 0x5432), __byte_perm(p[t4 + 4], p[t4 + 5], 0x5432));
-    }
 }
 
 // Code words t4 and t4 + 4 of block BB of token tok in the stage's activation
@@ -478,16 +524,32 @@ __device__ __forceinline__ uint2 sb_act(const uint8_t *stage, int pc, int tok, i
                       *reinterpret_cast<const uint32_t *>(line + (((c0 + 1) ^ (tok & 7)) << 4) + 4 * t4));
 }
 
+// Per output and block: acc += (d_w * d_a) * P, the scale rounded once, then
+// for asymmetric weights acc += (-(m * d_a)) * ssum (both products exact in
+// f32), packed in token pairs.  P is the exact integer block dot.
+template <class W>
+__device__ __forceinline__ void sb_epilogue(float2 (&acc)[2], const float (&c)[4], float dlo, float dhi, float mlo,
+                                            float mhi, float2 da, float2 ss)
+{
+    acc[0] = __ffma2_rn(__fmul2_rn(make_float2(dlo, dlo), da), make_float2(c[0], c[1]), acc[0]);
+    acc[1] = __ffma2_rn(__fmul2_rn(make_float2(dhi, dhi), da), make_float2(c[2], c[3]), acc[1]);
+    if constexpr (W::kMin) {
+        acc[0] = __ffma2_rn(__fmul2_rn(make_float2(-mlo, -mlo), da), ss, acc[0]);
+        acc[1] = __ffma2_rn(__fmul2_rn(make_float2(-mhi, -mhi), da), ss, acc[1]);
+    }
+}
+
 // One 32-wide block (block BB of piece `pc` of the stage) for this warp's 16
 // rows (row g's piece at wpiece) and NT groups of 8 tokens (tokens past t
 // are zeros), on the f16 MMA with the codes widened exactly.  Thread
 // (g = lane/4, t4 = lane%4) holds the MMA fragments of rows g, g+8 and token
 // g (+8 per token tile); its results are rows g, g+8 at tokens 2*t4, 2*t4+1
 // (+8 per token tile), kept as token pairs.  da[j] is the d_a pair of tile j.
-template <int BB, int NT>
+template <class W, int BB, int NT>
 __device__ __forceinline__ void sb_block(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
-                                         const float2 (&da)[NT], float2 (&acc)[NT][2])
+                                         const float2 (&da)[NT], const float2 (&ss)[NT], float2 (&acc)[NT][2])
 {
+    constexpr int kRowBytes = SbLayout<W>::kRowBytes;
     uint32_t bf[NT][4];  // token 8j+g: step 0 {codes 0,1 | 2,3} of word t4, step 1 the same of word t4 + 4
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -495,24 +557,22 @@ __device__ __forceinline__ void sb_block(const uint8_t *wpiece, const uint8_t *s
         q8::i8x4_to_f16x4(v.x, bf[j][0], bf[j][1]);
         q8::i8x4_to_f16x4(v.y, bf[j][2], bf[j][3]);
     }
-    const uint8_t *rlo = wpiece + g * kSbRowBytes;  // row g of the tile
-    const uint8_t *rhi = rlo + 8 * kSbRowBytes;      // row g + 8
-    const uint2 clo = sb_codes<BB>(rlo, t4), chi = sb_codes<BB>(rhi, t4);
+    const uint8_t *rlo = wpiece + g * kRowBytes;  // row g of the tile
+    const uint8_t *rhi = rlo + 8 * kRowBytes;      // row g + 8
+    const uint2 clo = W::template codes<BB>(rlo, t4), chi = W::template codes<BB>(rhi, t4);
     uint32_t a0[4], a1[4];  // per MMA step: {row g lo, row g+8 lo, row g hi, row g+8 hi}
     q8::i8x4_to_f16x4(clo.x, a0[0], a0[2]);
     q8::i8x4_to_f16x4(chi.x, a0[1], a0[3]);
     q8::i8x4_to_f16x4(clo.y, a1[0], a1[2]);
     q8::i8x4_to_f16x4(chi.y, a1[1], a1[3]);
-    const float dlo = __half2float(*reinterpret_cast<const __half *>(rlo + 34 * BB));
-    const float dhi = __half2float(*reinterpret_cast<const __half *>(rhi + 34 * BB));
+    const float dlo = W::template d<BB>(rlo), dhi = W::template d<BB>(rhi);
+    const float mlo = W::template m<BB>(rlo), mhi = W::template m<BB>(rhi);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         mma_f16_16816(c, a0, bf[j][0], bf[j][1]);
         mma_f16_16816(c, a1, bf[j][2], bf[j][3]);
-        // per output: the scale d_w * d_a rounded once, then one fma (packed in token pairs)
-        acc[j][0] = __ffma2_rn(__fmul2_rn(make_float2(dlo, dlo), da[j]), make_float2(c[0], c[1]), acc[j][0]);
-        acc[j][1] = __ffma2_rn(__fmul2_rn(make_float2(dhi, dhi), da[j]), make_float2(c[2], c[3]), acc[j][1]);
+        sb_epilogue<W>(acc[j], c, dlo, dhi, mlo, mhi, da[j], ss[j]);
     }
 }
 
@@ -530,24 +590,24 @@ __device__ __forceinline__ void mma_s8_16832(int (&c)[4], uint32_t a0, uint32_t 
 // t4 + 4 are its k ranges 4*t4.. and 16 + 4*t4.. for A and B alike.  One
 // tile needs about half of the int8 MMA rate at HBM speed; two tiles would
 // need more than all of it, so t > 8 keeps the f16 step.
-template <int BB, int NT>
+template <class W, int BB, int NT>
 __device__ __forceinline__ void sb_block_s8(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
-                                            const float2 (&da)[NT], float2 (&acc)[NT][2])
+                                            const float2 (&da)[NT], const float2 (&ss)[NT], float2 (&acc)[NT][2])
 {
-    const uint8_t *rlo = wpiece + g * kSbRowBytes;  // row g of the tile
-    const uint8_t *rhi = rlo + 8 * kSbRowBytes;      // row g + 8
-    const uint2 clo = sb_codes<BB>(rlo, t4), chi = sb_codes<BB>(rhi, t4);
-    const float dlo = __half2float(*reinterpret_cast<const __half *>(rlo + 34 * BB));
-    const float dhi = __half2float(*reinterpret_cast<const __half *>(rhi + 34 * BB));
+    constexpr int kRowBytes = SbLayout<W>::kRowBytes;
+    const uint8_t *rlo = wpiece + g * kRowBytes;  // row g of the tile
+    const uint8_t *rhi = rlo + 8 * kRowBytes;      // row g + 8
+    const uint2 clo = W::template codes<BB>(rlo, t4), chi = W::template codes<BB>(rhi, t4);
+    const float dlo = W::template d<BB>(rlo), dhi = W::template d<BB>(rhi);
+    const float mlo = W::template m<BB>(rlo), mhi = W::template m<BB>(rhi);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         const uint2 v = sb_act<BB>(stage, pc, 8 * j + g, t4);
-        int c[4] = {0, 0, 0, 0};
-        mma_s8_16832(c, clo.x, chi.x, clo.y, chi.y, v.x, v.y);
-        acc[j][0] = __ffma2_rn(__fmul2_rn(make_float2(dlo, dlo), da[j]),
-                               make_float2(static_cast<float>(c[0]), static_cast<float>(c[1])), acc[j][0]);
-        acc[j][1] = __ffma2_rn(__fmul2_rn(make_float2(dhi, dhi), da[j]),
-                               make_float2(static_cast<float>(c[2]), static_cast<float>(c[3])), acc[j][1]);
+        int ci[4] = {0, 0, 0, 0};
+        mma_s8_16832(ci, clo.x, chi.x, clo.y, chi.y, v.x, v.y);
+        const float c[4] = {static_cast<float>(ci[0]), static_cast<float>(ci[1]), static_cast<float>(ci[2]),
+                            static_cast<float>(ci[3])};
+        sb_epilogue<W>(acc[j], c, dlo, dhi, mlo, mhi, da[j], ss[j]);
     }
 }
 
@@ -557,11 +617,11 @@ __device__ __forceinline__ float sb_half_lo(uint32_t w)
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
 }
 
-template <int BB, int NT>
+template <class W, int BB, int NT>
 __device__ __forceinline__ void sb_step(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
                                         const uint4 (&dsv)[NT][2][2], float2 (&acc)[NT][2])
 {
-    float2 da[NT];
+    float2 da[NT], ss[NT];  // d_a and (asymmetric weights) the plane's ssum of the token pair
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         const uint4 &e = dsv[j][0][BB >> 2], &o = dsv[j][1][BB >> 2];  // tokens 8j + 2*t4, 8j + 2*t4 + 1
@@ -569,18 +629,23 @@ __device__ __forceinline__ void sb_step(const uint8_t *wpiece, const uint8_t *st
         const uint32_t we = q == 0 ? e.x : q == 1 ? e.y : q == 2 ? e.z : e.w;
         const uint32_t wo = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
         da[j] = make_float2(sb_half_lo(we), sb_half_lo(wo));
+        ss[j] = make_float2(static_cast<float>(static_cast<int16_t>(we >> 16)),
+                            static_cast<float>(static_cast<int16_t>(wo >> 16)));
     }
     if constexpr (NT <= Q8_SB_S8_TILES)
-        sb_block_s8<BB, NT>(wpiece, stage, pc, g, t4, da, acc);
+        sb_block_s8<W, BB, NT>(wpiece, stage, pc, g, t4, da, ss, acc);
     else
-        sb_block<BB, NT>(wpiece, stage, pc, g, t4, da, acc);
+        sb_block<W, BB, NT>(wpiece, stage, pc, g, t4, da, ss, acc);
 }
 
-template <int NT>
+template <class W, int NT>
 __global__ void __launch_bounds__(kSbThreads)
 gemv_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmD, int64_t n, int nb, int t, float *__restrict__ y)
 {
+    using L = SbLayout<W>;
+    constexpr int kSbOffBar = L::kOffBar, kSbStageBytes = L::kStageBytes, kSbStageTx = L::kStageTx;
+    constexpr int kSbRowBytes = L::kRowBytes, kSbPieceBytes = L::kPieceBytes;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = q8::smem_u32(smem_raw);
     uint8_t *ring = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);  // 1024-byte aligned (swizzle atoms)
@@ -681,14 +746,14 @@ gemv_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
                     dsv[j][e][0] = dw[0];
                     dsv[j][e][1] = dw[1];
                 }
-            sb_step<0, NT>(wp, st, pc, g, t4, dsv, acc);
-            sb_step<1, NT>(wp, st, pc, g, t4, dsv, acc);
-            sb_step<2, NT>(wp, st, pc, g, t4, dsv, acc);
-            sb_step<3, NT>(wp, st, pc, g, t4, dsv, acc);
-            sb_step<4, NT>(wp, st, pc, g, t4, dsv, acc);
-            sb_step<5, NT>(wp, st, pc, g, t4, dsv, acc);
-            sb_step<6, NT>(wp, st, pc, g, t4, dsv, acc);
-            sb_step<7, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<W, 0, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<W, 1, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<W, 2, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<W, 3, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<W, 4, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<W, 5, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<W, 6, NT>(wp, st, pc, g, t4, dsv, acc);
+            sb_step<W, 7, NT>(wp, st, pc, g, t4, dsv, acc);
             __syncwarp();
             if (lane == 0) q8::mbar_arrive(&empty[s]);
         }
@@ -766,43 +831,71 @@ int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, c
                       lpr_log2);
 }
 
-// Launch the small-batch kernel: 1 <= tokens <= 16, (k/32) % 8 == 0.  The
-// cluster size (CTAs splitting k, 1..8) makes the grid about one wave of the
-// CTAs that fit on the GPU at once.
-int gemv_small_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
-                      int64_t tokens, cudaStream_t s)
+} // namespace q8
+
+namespace {
+
+// Launch the small-batch kernel for weight format W: 1 <= tokens <= 16,
+// (k/32) % 8 == 0.  The cluster size (CTAs splitting k, 1..8) makes the grid
+// about one wave of the CTAs that fit on the GPU at once (the occupancy the
+// runtime reports for this kernel, its shared memory and its registers).
+template <class W>
+int gemv_small_launch_t(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                        int64_t tokens, cudaStream_t s, int slot1, int slot2)
 {
+    using L = SbLayout<W>;
     const int64_t nb = k / 32;
     if (tokens < 1 || tokens > kSbMaxTokens || nb % kSbGroup != 0 || nb > (int64_t(1) << 30)) return Q8_ERR_ARG;
     const int64_t stages = (nb + kSbGroup * kSbPieces - 1) / (kSbGroup * kSbPieces);
     const int sms = q8::device_sm_count();
     if (sms <= 0) return Q8_ERR_DEVICE;
+    const bool wide = tokens > 8;
+    const void *fn = wide ? reinterpret_cast<const void *>(gemv_small_kernel<W, 2>)
+                          : reinterpret_cast<const void *>(gemv_small_kernel<W, 1>);
+    if (!q8::set_max_dynamic_smem(fn, L::kSmem, wide ? slot2 : slot1)) return Q8_ERR_LAUNCH;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kSbThreads, static_cast<size_t>(L::kSmem)) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return Q8_ERR_LAUNCH;
     const int64_t tiles = (n + kSbRows - 1) / kSbRows;
     // about one wave of resident CTAs, at least one stage per CTA
-    int64_t ks = (static_cast<int64_t>(kSbCtasPerSm) * sms) / tiles;
+    int64_t ks = (static_cast<int64_t>(per_sm) * sms) / tiles;
     ks = ks < 1 ? 1 : (ks > kSbMaxCluster ? kSbMaxCluster : ks);
     if (ks > stages) ks = stages;
     if (tiles * ks > 0x7fffffff) return Q8_ERR_ARG;
     const dim3 grid(static_cast<unsigned>(tiles * ks));
     CUtensorMap mw, mq, md;
-    // weights as [n rows][nb/8 pieces][136 u16]; box = kSbRows rows x kSbPieces pieces
-    if (!make_map_3d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, kSbPieceBytes / 2, static_cast<uint64_t>(nb / kSbGroup),
-                     static_cast<uint64_t>(n), kSbPieceBytes, static_cast<uint64_t>(nb * 34), kSbPieceBytes / 2,
-                     kSbPieces, kSbRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qs, static_cast<uint64_t>(k), static_cast<uint64_t>(tokens),
+    // weights as [n rows][nb/8 pieces][piece bytes / 2 u16]; box = kSbRows rows x kSbPieces pieces
+    if (!q8::make_map_3d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, L::kPieceBytes / 2, static_cast<uint64_t>(nb / kSbGroup),
+                     static_cast<uint64_t>(n), L::kPieceBytes, static_cast<uint64_t>(nb * W::kBlockBytes),
+                     L::kPieceBytes / 2, kSbPieces, kSbRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !q8::make_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qs, static_cast<uint64_t>(k), static_cast<uint64_t>(tokens),
                      static_cast<uint64_t>(k), 128, kSbMaxTokens, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT32, ds, static_cast<uint64_t>(nb), static_cast<uint64_t>(tokens),
+        !q8::make_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT32, ds, static_cast<uint64_t>(nb), static_cast<uint64_t>(tokens),
                      static_cast<uint64_t>(nb * 4), kSbGroup * kSbPieces, kSbMaxTokens, CU_TENSOR_MAP_SWIZZLE_NONE))
         return Q8_ERR_LAUNCH;
-    const bool wide = tokens > 8;
-    const void *fn = wide ? reinterpret_cast<const void *>(gemv_small_kernel<2>)
-                          : reinterpret_cast<const void *>(gemv_small_kernel<1>);
-    if (!q8::set_max_dynamic_smem(fn, kSbSmem, wide ? 4 : 3)) return Q8_ERR_LAUNCH;
     if (wide)
-        return launch_pdl_cluster(gemv_small_kernel<2>, grid, dim3(kSbThreads), kSbSmem, s, static_cast<int>(ks), mw, mq,
-                                  md, n, static_cast<int>(nb), static_cast<int>(tokens), y);
-    return launch_pdl_cluster(gemv_small_kernel<1>, grid, dim3(kSbThreads), kSbSmem, s, static_cast<int>(ks), mw, mq, md,
-                              n, static_cast<int>(nb), static_cast<int>(tokens), y);
+        return q8::launch_pdl_cluster(gemv_small_kernel<W, 2>, grid, dim3(kSbThreads), L::kSmem, s, static_cast<int>(ks),
+                                  mw, mq, md, n, static_cast<int>(nb), static_cast<int>(tokens), y);
+    return q8::launch_pdl_cluster(gemv_small_kernel<W, 1>, grid, dim3(kSbThreads), L::kSmem, s, static_cast<int>(ks), mw,
+                              mq, md, n, static_cast<int>(nb), static_cast<int>(tokens), y);
+}
+
+} // namespace
+
+namespace q8 {
+
+int gemv_small_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                      int64_t tokens, cudaStream_t s)
+{
+    return gemv_small_launch_t<SbQ8_0>(w, n, k, qs, ds, y, tokens, s, 3, 4);
+}
+
+int gemv_small_q4a_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                          int64_t tokens, cudaStream_t s)
+{
+    return gemv_small_launch_t<SbQ4A>(w, n, k, qs, ds, y, tokens, s, 7, 8);
 }
 
 } // namespace q8

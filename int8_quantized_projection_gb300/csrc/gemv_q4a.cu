@@ -147,3 +147,15 @@ extern "C" int q4a_gemv(const void *w, int64_t n, int64_t k, const int8_t *qs, c
                           static_cast<int>(nc), reinterpret_cast<const uint4 *>(qs),
                           reinterpret_cast<const uint4 *>(ds), y, lpr_log2);
 }
+
+extern "C" int q4a_gemv_batched(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds,
+                                int64_t tokens, float *y, void *stream)
+{
+    if (!w || !qs || !ds || !y || n < 1 || n > (int64_t(1) << 40) || k <= 0 || (k % 256) != 0 || tokens < 1 ||
+        tokens > Q8_GEMV_MAX_TOKENS)
+        return Q8_ERR_ARG;
+    if (tokens == 1) return q4a_gemv(w, n, k, qs, ds, y, stream);
+    if (!q8::aligned16(w) || !q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y)) return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    return q8::gemv_small_q4a_launch(w, n, k, qs, ds, y, tokens, static_cast<cudaStream_t>(stream));
+}

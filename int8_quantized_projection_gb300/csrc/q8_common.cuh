@@ -97,6 +97,9 @@ int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, c
 // small-batch kernel (gemv.cu): 1 <= tokens <= Q8_GEMV_MAX_TOKENS, (k/32) % 8 == 0
 int gemv_small_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
                       int64_t tokens, cudaStream_t s);
+// small-batch kernel (gemv.cu) for asymmetric 4-bit blocks: 1 <= tokens <= 16, (k/32) % 8 == 0
+int gemv_small_q4a_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                          int64_t tokens, cudaStream_t s);
 // staged batch-1 kernel (gemv.cu) for asymmetric 4-bit blocks: k % 128 == 0,
 // k / 128 <= kGemvStagedMaxChunks (the activation is staged in shared memory)
 constexpr int kGemvStagedMaxChunks = 512;

@@ -97,6 +97,12 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert lib.q4a_gemv(P(FAKE), 8, 96, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
     assert lib.q4a_gemv(P(FAKE), 0, 256, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
     assert lib.q4a_gemv(P(FAKE + 4), 8, 256, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ALIGN
+    # q4a_gemv_batched: k % 256 (whole 8-block pieces), tokens 1..16, alignment
+    assert lib.q4a_gemv_batched(P(FAKE), 8, 128, P(FAKE), P(FAKE), 4, P(FAKE), s) == ERR_ARG
+    assert lib.q4a_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 0, P(FAKE), s) == ERR_ARG
+    assert lib.q4a_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 17, P(FAKE), s) == ERR_ARG
+    assert lib.q4a_gemv_batched(P(0), 8, 256, P(FAKE), P(FAKE), 4, P(FAKE), s) == ERR_ARG
+    assert lib.q4a_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 4, P(MISALIGNED), s) == ERR_ALIGN
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):

@@ -120,3 +120,98 @@ def test_q4a_decode_chain_from_the_gpu_plane(q8):
     q8.q8_check()
     yr, ar = oracle.q4a_gemv(blob, n, k, host(qs), host(ds).view(np.uint32))
     assert_gemm_close(host(y), yr, ar, "q4a decode chain")
+
+
+# ---------------------------------------------------------------------------
+# q4a_gemv_batched: t = 2..16 tokens, the weights read once for all of them
+# (t <= 8: one token tile on the int8 MMA; t > 8: two tiles on the f16 MMA).
+# ---------------------------------------------------------------------------
+def _plane_t(seed, t, k, exact=False):
+    """Plane rows [0, t) of t tokens, padded to 128 rows (rows >= t zero)."""
+    g = syn.rng(83, seed, t, k)
+    if exact:
+        qa = np.zeros((128, k), np.int8)
+        qa[:t] = g.integers(-3, 4, size=(t, k)).astype(np.int8)
+        e = g.integers(-4, -1, size=(128, k // 32))
+        d16 = (2.0 ** e).astype(np.float16).view(np.uint16)
+        ssum = qa.reshape(128, k // 32, 32).astype(np.int64).sum(-1)
+        ds = d16.astype(np.uint32) | (ssum.astype(np.int16).view(np.uint16).astype(np.uint32) << 16)
+        ds[t:] = 0
+        return qa, ds
+    return oracle.quantize(syn.activations(g, t, k, sigma=1.5, outlier_frac=0.01), 128)
+
+
+def _run_batched(q8, blob, n, k, qs, ds, t):
+    y = nan_f32(t, n)
+    q8.q4a_gemv_batched(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), t, y)
+    q8.q8_check()
+    return y
+
+
+BATCHED = [
+    (256, 256, 2),     # one 8-block piece per row
+    (1000, 512, 5),    # ragged row tile, one token tile
+    (333, 2048, 8),
+    (77, 18944, 9),    # two token tiles (f16 MMA), long rows split over a cluster
+    (4099, 7168, 16),  # ragged n, full tile pair
+    (3, 256, 3),
+    (12288, 7168, 16), # full-size decode projection
+]
+
+
+@pytest.mark.parametrize("n,k,t", BATCHED)
+def test_q4a_gemv_batched_matches_oracle(q8, n, k, t):
+    blob = _weights(5, n, k)
+    qs, ds = _plane_t(5, t, k)
+    y = _run_batched(q8, blob, n, k, qs, ds, t)
+    yr, ar = oracle.q4a_gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+    assert_gemm_close(host(y), yr, ar, f"q4a_gemv_batched {n}x{k} t={t}")
+
+
+@pytest.mark.parametrize("n,k,t", [(300, 2048, 7), (129, 7168, 16), (77, 18944, 4)])
+def test_q4a_gemv_batched_exact_epilogue_bit_equal(q8, n, k, t):
+    blob = _weights(6, n, k, exact=True)
+    qs, ds = _plane_t(6, t, k, exact=True)
+    y = _run_batched(q8, blob, n, k, qs, ds, t)
+    yr, _ = oracle.q4a_gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+    assert np.array_equal(host(y).astype(np.float64), yr)
+
+
+def test_q4a_gemv_batched_one_token_is_q4a_gemv(q8):
+    n, k = 1001, 2048
+    blob = _weights(7, n, k)
+    qs, ds = _plane(7, k)
+    y1 = _run_batched(q8, blob, n, k, qs, ds, 1)
+    y = _run(q8, blob, n, k, qs, ds)
+    assert np.array_equal(host(y1).reshape(-1), host(y))
+
+
+def test_q4a_gemv_batched_ignores_plane_rows_past_t(q8):
+    """Rows at and past t hold garbage: the result is unchanged (they arrive
+    as zeros only through the tensor map's bounds, never from the plane)."""
+    n, k, t = 500, 2048, 6
+    blob = _weights(8, n, k)
+    qs, ds = _plane_t(8, t, k)
+    y = _run_batched(q8, blob, n, k, qs, ds, t)
+    g = syn.rng(84, 0)
+    qs2, ds2 = qs.copy(), ds.copy()
+    qs2[t:] = g.integers(-127, 128, size=qs2[t:].shape).astype(np.int8)
+    ds2[t:] = g.integers(0, 2**31, size=ds2[t:].shape).astype(np.uint32)
+    y2 = _run_batched(q8, blob, n, k, qs2, ds2, t)
+    assert np.array_equal(host(y), host(y2))
+
+
+def test_q4a_gemv_batched_deterministic(q8):
+    import torch
+
+    n, k, t = 12288, 7168, 12
+    blob = dev(_weights(9, n, k))
+    qs, ds = _plane_t(9, t, k)
+    qs, ds = dev(qs), dev(ds.view(np.int32))
+    outs = []
+    for _ in range(3):
+        y = nan_f32(t, n)
+        q8.q4a_gemv_batched(blob, n, k, qs, ds, t, y)
+        q8.q8_check()
+        outs.append(y.clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
