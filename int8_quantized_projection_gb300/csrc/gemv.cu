@@ -284,6 +284,11 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
         const bool ok = q8::mbar_wait_bounded(&mybar[s], par);
         if (!__all_sync(Q8_FULL_MASK, ok)) {
             if (lane == 0) atomicOr(&g_gemv_err, 1u);
+            // before leaving, let this warp's copies in flight land (each
+            // wait bounded): no copy may still write into shared memory once
+            // the CTA has exited
+            for (uint32_t j = 0; j < static_cast<uint32_t>(kStages); ++j)
+                (void)q8::mbar_wait_bounded(&mybar[(i + j) % kStages], ((i + j) / kStages) & 1u);
             return;
         }
         const int2 m = mymeta[s];
