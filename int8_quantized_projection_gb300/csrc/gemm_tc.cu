@@ -260,7 +260,7 @@ __device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const float *__restrict__ dwt, const float *__restrict__ dat, int64_t n, int64_t t, int nb,
-               float *__restrict__ y)
+               float *__restrict__ y, float *__restrict__ part)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = q8::smem_u32(smem_raw);
@@ -274,6 +274,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // token tiles vary fastest, so the CTAs running together share weight rows in L2
     const int64_t n0 = static_cast<int64_t>(blockIdx.y) * BM;
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * BN;
+    // split-K (gridDim.z > 1): this CTA takes stages [s0, s0 + nsl) of k and
+    // writes its partial tile to part[z]; j below counts this CTA's blocks
+    const int nst = nb / kStageBlocks;
+    const int s0 = static_cast<int>(static_cast<int64_t>(nst) * blockIdx.z / gridDim.z);
+    const int nsl = static_cast<int>(static_cast<int64_t>(nst) * (blockIdx.z + 1) / gridDim.z) - s0;
+    const int j0 = s0 * kStageBlocks, nbl = nsl * kStageBlocks;
+    float *out = gridDim.z > 1 ? part + static_cast<int64_t>(blockIdx.z) * t * n : y;
 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_gemm_err) != 0u) ? 1 : 0;
@@ -308,15 +315,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // Inputs come from the pre-passes just before on the stream; Y is
             // written only after the last MMA, which follows these loads.
             q8::griddep_wait();
-            const int nstages = nb / kStageBlocks;
             int issued = 0;
-            for (int s = 0; s < nstages && !*abort_flag; ++s) {
+            for (int s = 0; s < nsl && !*abort_flag; ++s) {
                 const int slot = s % kStages;
                 if (!wait_bar(B.empty(slot), (static_cast<uint32_t>(s / kStages) & 1u) ^ 1u, abort_flag)) break;
                 q8::mbar_arrive_expect_tx(reinterpret_cast<uint64_t *>(sm + OFF_BAR) + slot, kStageBytes);
                 const uint32_t dst = base + OFF_STAGE + slot * kStageBytes;
-                q8::tma_load_2d(dst, &tmA, s * 32 * kStageBlocks, static_cast<int>(n0), B.full(slot));
-                q8::tma_load_2d(dst + kATileBytes, &tmB, s * 32 * kStageBlocks, static_cast<int>(t0), B.full(slot));
+                const int kx = (s0 + s) * 32 * kStageBlocks;
+                q8::tma_load_2d(dst, &tmA, kx, static_cast<int>(n0), B.full(slot));
+                q8::tma_load_2d(dst + kATileBytes, &tmB, kx, static_cast<int>(t0), B.full(slot));
                 issued = s + 1;
             }
             // drain: the last stages issued must have landed before the CTA exits
@@ -325,10 +332,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         } else if (warp == 2 && lane == 0) {
             // ------------------------------------------------------------ scale producer
             q8::griddep_wait();
-            const float *dw_tile = dwt + static_cast<int64_t>(blockIdx.y) * nb * BM;
-            const float *da_tile = dat + static_cast<int64_t>(blockIdx.x) * nb * BN;
+            const float *dw_tile = dwt + (static_cast<int64_t>(blockIdx.y) * nb + j0) * BM;
+            const float *da_tile = dat + (static_cast<int64_t>(blockIdx.x) * nb + j0) * BN;
             int issued = 0;
-            for (int j = 0; j < nb && !*abort_flag; ++j) {
+            for (int j = 0; j < nbl && !*abort_flag; ++j) {
                 const int ss = j % kScSlots;
                 if (!wait_bar(B.sc_empty(ss), (static_cast<uint32_t>(j / kScSlots) & 1u) ^ 1u, abort_flag)) break;
                 uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR) + 2 * kStages + ss;
@@ -345,7 +352,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // Warp 1 issues the even blocks (TMEM buffer 0), warp 3 the odd
             // ones (buffer 1).
             const int who = warp == 1 ? 0 : 1;
-            for (int j = who; j < nb; j += kAcc) {
+            for (int j = who; j < nbl; j += kAcc) {
                 const int st = (j / kStageBlocks) % kStages, bq = j % kStageBlocks;
                 const uint32_t use = static_cast<uint32_t>(j / (kStageBlocks * kStages));
                 if (!wait_bar(B.full(st), use & 1u, abort_flag)) break;
@@ -377,7 +384,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.0f, 0.0f);
         bool ok = true;
-        for (int j = 0; j < nb; ++j) {
+        for (int j = 0; j < nbl; ++j) {
             const int ab = j % kAcc, ss = j % kScSlots;
             if (!wait_bar(B.acc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
@@ -420,8 +427,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     for (int rep = 0; rep < 4; ++rep) {
                         const int64_t tok = t0 + kEpiCols * hcol + 32 * (c >> 1) + 8 * rep + 2 * m;
                         const float2 v = acc[8 * c + 2 * rep + e];
-                        if (tok < t) y[tok * n + row] = v.x;
-                        if (tok + 1 < t) y[(tok + 1) * n + row] = v.y;
+                        if (tok < t) out[tok * n + row] = v.x;
+                        if (tok + 1 < t) out[(tok + 1) * n + row] = v.y;
                     }
                 }
             }
@@ -535,9 +542,42 @@ gemm_prep_a_kernel(const uint4 *__restrict__ qs, const uint32_t *__restrict__ ds
     }
 }
 
-// Workspace layout for (n, t, k): [f16 weights | f16 activation | d_w tiles | d_a tiles].
+// Split-K: y = sum over z of part[z], added in z order (deterministic).
+__global__ void __launch_bounds__(256)
+gemm_split_reduce_kernel(const float *__restrict__ part, int splits, int64_t count, float *__restrict__ y)
+{
+    q8::griddep_launch_dependents();
+    q8::griddep_wait();  // the partial tiles come from the GEMM just before
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float v = part[i];
+        for (int z = 1; z < splits; ++z) v += part[static_cast<int64_t>(z) * count + i];
+        y[i] = v;
+    }
+}
+
+// How many CTAs share k (1 = none).  When the tiles alone leave most SMs idle
+// (a few weight rows or tokens), k is split so that about one wave of CTAs
+// runs, each over at least 4 stages (8 blocks).  A fixed SM count is used so
+// that the workspace size is a function of the shape alone; splits * tiles
+// stays at most that count, which bounds the partial tiles by about 15 MB.
+constexpr int kSplitSms = 152, kMaxSplits = 8;
+int gemm_splits(int64_t n, int64_t t, int64_t k)
+{
+    const int64_t tiles = ((n + BM - 1) / BM) * ((t + BN - 1) / BN);
+    const int64_t nst = k / 32 / kStageBlocks;
+    if (2 * tiles > kSplitSms) return 1;
+    int64_t sp = kSplitSms / tiles;
+    sp = sp > kMaxSplits ? kMaxSplits : sp;
+    sp = sp > nst / 4 ? nst / 4 : sp;
+    return sp < 1 ? 1 : static_cast<int>(sp);
+}
+
+// Workspace layout for (n, t, k): [f16 weights | f16 activation | d_w tiles |
+// d_a tiles | partial tiles (split-K only: splits x t x n f32)].
 struct WsLayout {
-    size_t a16, b16, dwt, dat, total;
+    size_t a16, b16, dwt, dat, part, total;
+    int splits;
 };
 
 WsLayout ws_layout(int64_t n, int64_t t, int64_t k)
@@ -545,11 +585,13 @@ WsLayout ws_layout(int64_t n, int64_t t, int64_t k)
     auto up = [](size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); };
     const size_t nb = static_cast<size_t>(k / 32);
     WsLayout L;
+    L.splits = gemm_splits(n, t, k);
     L.a16 = 0;
     L.b16 = up(L.a16 + static_cast<size_t>(n) * k * 2);
     L.dwt = up(L.b16 + static_cast<size_t>(t) * k * 2);
     L.dat = up(L.dwt + static_cast<size_t>((n + BM - 1) / BM) * nb * BM * 4);
-    L.total = up(L.dat + static_cast<size_t>((t + BN - 1) / BN) * nb * BN * 4);
+    L.part = up(L.dat + static_cast<size_t>((t + BN - 1) / BN) * nb * BN * 4);
+    L.total = up(L.part + (L.splits > 1 ? static_cast<size_t>(L.splits) * t * n * 4 : 0));
     return L;
 }
 
@@ -600,9 +642,17 @@ int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const 
                     reinterpret_cast<const uint4 *>(qs), ds, t, k, reinterpret_cast<uint4 *>(b16), dat);
     if (st != Q8_OK) return st;
     if (!set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel), kSmemBytes, 2)) return Q8_ERR_LAUNCH;
-    const dim3 grid(static_cast<unsigned>((t + BN - 1) / BN), static_cast<unsigned>((n + BM - 1) / BM));
-    return launch_pdl(gemm_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, ma, mb, dwt, dat, n, t,
-                      static_cast<int>(nb), y);
+    float *part = reinterpret_cast<float *>(ws + L.part);
+    const dim3 grid(static_cast<unsigned>((t + BN - 1) / BN), static_cast<unsigned>((n + BM - 1) / BM),
+                    static_cast<unsigned>(L.splits));
+    st = launch_pdl(gemm_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, ma, mb, dwt, dat, n, t, static_cast<int>(nb),
+                    y, part);
+    if (st != Q8_OK || L.splits == 1) return st;
+    const int64_t count = t * n;
+    int64_t rgrid = (count + 255) / 256;
+    rgrid = rgrid < pcap ? rgrid : pcap;
+    return launch_pdl(gemm_split_reduce_kernel, dim3(static_cast<unsigned>(rgrid)), dim3(256), 0, s,
+                      static_cast<const float *>(part), L.splits, count, y);
 }
 
 } // namespace q8
