@@ -257,6 +257,7 @@ __device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const float *__restrict__ dwt, const float *__restrict__ dat, int64_t n, int64_t t, int nb,
@@ -276,11 +277,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * BN;
     // split-K (gridDim.z > 1): this CTA takes stages [s0, s0 + nsl) of k and
     // writes its partial tile to part[z]; j below counts this CTA's blocks
+    // (a separate instantiation, so the unsplit kernel carries none of it)
     const int nst = nb / kStageBlocks;
-    const int s0 = static_cast<int>(static_cast<int64_t>(nst) * blockIdx.z / gridDim.z);
-    const int nsl = static_cast<int>(static_cast<int64_t>(nst) * (blockIdx.z + 1) / gridDim.z) - s0;
-    const int j0 = s0 * kStageBlocks, nbl = nsl * kStageBlocks;
-    float *out = gridDim.z > 1 ? part + static_cast<int64_t>(blockIdx.z) * t * n : y;
+    const int s0 = kSplit ? static_cast<int>(static_cast<int64_t>(nst) * blockIdx.z / gridDim.z) : 0;
+    const int nsl = kSplit ? static_cast<int>(static_cast<int64_t>(nst) * (blockIdx.z + 1) / gridDim.z) - s0 : nst;
+    const int j0 = s0 * kStageBlocks, nbl = kSplit ? nsl * kStageBlocks : nb;
+    float *out = kSplit ? part + static_cast<int64_t>(blockIdx.z) * t * n : y;
 
     if (threadIdx.x == 0) {
         *abort_flag = (*reinterpret_cast<volatile unsigned int *>(&g_gemm_err) != 0u) ? 1 : 0;
@@ -641,13 +643,19 @@ int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const 
     st = launch_pdl(gemm_prep_a_kernel, dim3(static_cast<unsigned>(agrid)), dim3(256), 0, s,
                     reinterpret_cast<const uint4 *>(qs), ds, t, k, reinterpret_cast<uint4 *>(b16), dat);
     if (st != Q8_OK) return st;
-    if (!set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel), kSmemBytes, 2)) return Q8_ERR_LAUNCH;
     float *part = reinterpret_cast<float *>(ws + L.part);
     const dim3 grid(static_cast<unsigned>((t + BN - 1) / BN), static_cast<unsigned>((n + BM - 1) / BM),
                     static_cast<unsigned>(L.splits));
-    st = launch_pdl(gemm_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, ma, mb, dwt, dat, n, t, static_cast<int>(nb),
-                    y, part);
-    if (st != Q8_OK || L.splits == 1) return st;
+    if (L.splits == 1) {
+        if (!set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel<false>), kSmemBytes, 2))
+            return Q8_ERR_LAUNCH;
+        return launch_pdl(gemm_tc_kernel<false>, grid, dim3(kThreads), kSmemBytes, s, ma, mb, dwt, dat, n, t,
+                          static_cast<int>(nb), y, part);
+    }
+    if (!set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel<true>), kSmemBytes, 9)) return Q8_ERR_LAUNCH;
+    st = launch_pdl(gemm_tc_kernel<true>, grid, dim3(kThreads), kSmemBytes, s, ma, mb, dwt, dat, n, t,
+                    static_cast<int>(nb), y, part);
+    if (st != Q8_OK) return st;
     const int64_t count = t * n;
     int64_t rgrid = (count + 255) / 256;
     rgrid = rgrid < pcap ? rgrid : pcap;
