@@ -179,7 +179,9 @@ Q8_API int q8_0_gemv_grouped(const q8_gemv_proj *projs, int count, int64_t k,
  * generic kernel (weights read once per token).  Programmatic dependent
  * launch, with the same precondition on w as q8_0_gemv.
  * q8_0_gemm hands calls with t <= Q8_GEMV_MAX_TOKENS to this path (t == 1 to
- * q8_0_gemv).
+ * q8_0_gemv), and calls with Q8_GEMV_MAX_TOKENS < t <= 64 to this path over
+ * consecutive 16-token slices of the plane (each slice streams the weights
+ * again; up to four passes cost less than the GEMM's pre-pass).
  */
 #define Q8_GEMV_MAX_TOKENS 16
 Q8_API int q8_0_gemv_batched(const void *w, int64_t n, int64_t k,
@@ -240,8 +242,8 @@ Q8_API int q4a_gemv_batched(const void *w, int64_t n, int64_t k,
  * over up to 8 CTAs per tile and the workspace also holds their f32 partial
  * outputs (splits * t * n * 4 bytes, added in a fixed order by a reduction
  * kernel; splits * tiles <= 152, so at most about 15 MB).  The size depends
- * on (n, t, k) only.  0 when (k/32) % 8 != 0 or t <= Q8_GEMV_MAX_TOKENS (those
- * calls need none).
+ * on (n, t, k) only.  0 when (k/32) % 8 != 0 or t <= 64 (those calls run
+ * the generic or small-batch kernels and need none).
  */
 Q8_API size_t q8_0_gemm_workspace_bytes(int64_t n, int64_t t, int64_t k);
 
@@ -256,11 +258,15 @@ Q8_API size_t q8_0_gemm_workspace_bytes(int64_t n, int64_t t, int64_t k);
  *            Two calls may share a workspace only if they are ordered on one
  *            stream.  May be NULL when that size is 0.
  * n >= 1, t >= 1, k % 32 == 0.  Every 32-wide k block is one q8_0 block on
- * both sides, so its integer dot product is scaled by d_w * d_a once.  The
- * call enqueues two pre-passes that write the weight codes and the plane's
- * codes as f16 (exact) and both sides' block scales as f32 into the
- * workspace, then the tcgen05 GEMM (all with programmatic dependent launch;
- * the same precondition on w as q8_0_gemv).
+ * both sides, so its integer dot product is scaled by d_w * d_a once.
+ * Dispatch by shape: t == 1 -> q8_0_gemv; (k/32) % 8 != 0 -> the generic
+ * kernel; t <= 64 -> q8_0_gemv_batched's kernel (over 16-token slices above
+ * 16 tokens); otherwise the call enqueues two pre-passes that write the
+ * weight codes and the plane's codes as f16 (exact) and both sides' block
+ * scales as f32 into the workspace, then the tcgen05 GEMM (split over k when
+ * its tiles alone would leave most SMs idle, with a reduction kernel after
+ * it), all with programmatic dependent launch and the same precondition on w
+ * as q8_0_gemv.
  * "12 - r5-r6 re-ranking + structural rewrite spec", sec. 2 and 3.1;
  * "54 - r51 - producer-fused A-quantize mode 1", sec. 2.1.
  */
@@ -281,8 +287,9 @@ Q8_API int q8_0_gemm(const void *w, int64_t n, int64_t k,
  *   array that is part of this library's device code
  *   (q8_0_gemm_noalloc_max_bytes()).  Every GPU that loads the library's GEMM
  *   code holds those 32 MiB until the process exits.  A request whose
- *   q8_0_gemm_workspace_bytes(t, k) exceeds it returns Q8_ERR_TOO_BIG (for
- *   example t = 3325 fits k = 3584 but not k = 18944).
+ *   q8_0_gemm_workspace_bytes(n, t, k) exceeds it returns Q8_ERR_TOO_BIG
+ *   (the f16 copies of both operands must fit: small projections, or t <= 64
+ *   which needs no scratch at all).
  *   The entry point itself calls no cudaMalloc/cudaFree or allocating
  *   routine.  Its first call on a device looks up that device's address of
  *   the array (cudaGetSymbolAddress, with the device current); make that

@@ -158,9 +158,25 @@ extern "C" int q8_check(void *stream)
     return b;
 }
 
+namespace q8 {
+
+int gemv_sliced_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+                       int64_t tokens, cudaStream_t s)
+{
+    const int64_t nb = k / 32;
+    for (int64_t c = 0; c < tokens; c += Q8_GEMV_MAX_TOKENS) {  // slice starts stay 16-byte aligned
+        const int64_t tt = tokens - c < Q8_GEMV_MAX_TOKENS ? tokens - c : Q8_GEMV_MAX_TOKENS;
+        const int st = gemv_small_launch(w, n, k, qs + c * k, ds + c * nb, y + c * n, tt, s);
+        if (st != Q8_OK) return st;
+    }
+    return Q8_OK;
+}
+
+} // namespace q8
+
 extern "C" size_t q8_0_gemm_workspace_bytes(int64_t n, int64_t t, int64_t k)
 {
-    if (n < 1 || t <= Q8_GEMV_MAX_TOKENS || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0) return 0;
+    if (n < 1 || t <= q8::kSlicedMaxTokens || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0) return 0;
     return q8::gemm_workspace_bytes(n, t, k);
 }
 
@@ -180,6 +196,7 @@ extern "C" int q8_0_gemm(const void *w, int64_t n, int64_t k, const int8_t *qs, 
         return q8::gemv_generic_launch(w, n, k, qs, ds, y, t, s);
     }
     if (t <= Q8_GEMV_MAX_TOKENS) return q8::gemv_small_launch(w, n, k, qs, ds, y, t, s);
+    if (t <= q8::kSlicedMaxTokens) return q8::gemv_sliced_launch(w, n, k, qs, ds, y, t, s);
     // grid: token tiles of 192 along x, weight-row tiles of 128 along y (at most 65535)
     if (n > int64_t(65535) * 128 || t > (int64_t(1) << 31) - 256 || k > (int64_t(1) << 31) / 2) return Q8_ERR_ARG;
     return q8::gemm_tc_launch(w, n, k, qs, ds, t, y, workspace, s);

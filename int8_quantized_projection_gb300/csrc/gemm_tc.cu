@@ -718,6 +718,7 @@ extern "C" int q8_0_gemm_noalloc(const void *w, int64_t n, int64_t k, const int8
         return q8::gemv_generic_launch(w, n, k, qs, ds, y, t, s);
     }
     if (t <= Q8_GEMV_MAX_TOKENS) return q8::gemv_small_launch(w, n, k, qs, ds, y, t, s);
+    if (t <= q8::kSlicedMaxTokens) return q8::gemv_sliced_launch(w, n, k, qs, ds, y, t, s);
     if (n > int64_t(65535) * 128 || t > (int64_t(1) << 31) - 256 || k > (int64_t(1) << 31) / 2) return Q8_ERR_ARG;
     void *scratch = nullptr;
     const int st = noalloc_scratch(&scratch);

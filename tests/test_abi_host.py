@@ -76,10 +76,10 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert lib.q8_0_gemv(P(FAKE), 8, 100, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
     assert lib.q8_0_gemv(P(FAKE + 2), 8, 64, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ALIGN
     # q8_0_gemm: rows_pad < t, t < 1, workspace missing or too small
-    ws = lib.q8_0_gemm_workspace_bytes(8, 20, 256)
+    ws = lib.q8_0_gemm_workspace_bytes(8, 100, 256)
     up = lambda v: -(-v // 1024) * 1024
     # f16 weights | f16 activation | d_w per 128-row tile | d_a per 192-token tile, each from a 1 KiB boundary
-    assert ws == up(up(up(8 * 256 * 2) + 20 * 256 * 2) + 1 * 8 * 128 * 4) + up(1 * 8 * 192 * 4)
+    assert ws == up(up(up(8 * 256 * 2) + 100 * 256 * 2) + 1 * 8 * 128 * 4) + up(1 * 8 * 192 * 4)
     # a grid of 2 tiles splits k 8 ways (32 stages of 2 blocks, at least 4 per split): + 8 x t x n f32 partial tiles
     ws2 = lib.q8_0_gemm_workspace_bytes(256, 130, 2048)
     assert ws2 == up(up(up(up(256 * 2048 * 2) + 130 * 2048 * 2) + 2 * 64 * 128 * 4) + 1 * 64 * 192 * 4) \
@@ -88,11 +88,13 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
                                                                      + 148 * 112 * 128 * 4) + 18 * 112 * 192 * 4)
     assert lib.q8_0_gemm_workspace_bytes(8, 20, 64) == 0      # k/32 % 8 != 0: generic kernel, no workspace
     assert lib.q8_0_gemm_workspace_bytes(8, 16, 256) == 0     # t <= 16: small-batch kernel, no workspace
+    assert lib.q8_0_gemm_workspace_bytes(8, 64, 256) == 0     # t <= 64: 16-token slices, no workspace
+    assert lib.q8_0_gemm_workspace_bytes(8, 65, 256) > 0      # the GEMM from 65 tokens
     assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(FAKE), 5, 4, P(FAKE), P(0), 0, s) == ERR_ARG
     assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(FAKE), 0, 4, P(FAKE), P(0), 0, s) == ERR_ARG
-    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 20, 20, P(FAKE), P(0), ws, s) == ERR_ARG
-    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 20, 20, P(FAKE), P(FAKE), ws - 1, s) == ERR_ARG
-    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 20, 20, P(FAKE), P(MISALIGNED), ws, s) == ERR_ALIGN
+    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 100, 100, P(FAKE), P(0), ws, s) == ERR_ARG
+    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 100, 100, P(FAKE), P(FAKE), ws - 1, s) == ERR_ARG
+    assert lib.q8_0_gemm(P(FAKE), 8, 256, P(FAKE), P(FAKE), 100, 100, P(FAKE), P(MISALIGNED), ws, s) == ERR_ALIGN
     assert lib.q8_0_gemm(P(FAKE), 8, 64, P(FAKE), P(MISALIGNED), 4, 4, P(FAKE), P(0), 0, s) == ERR_ALIGN
     # q8_0_gemv_batched: tokens outside 1..16, k % 32, alignment
     assert lib.q8_0_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 0, P(FAKE), s) == ERR_ARG

@@ -170,6 +170,7 @@ def test_gemv_deterministic(q8):
 GEMM_SHAPES = [
     (128, 256, 64), (100, 512, 1), (1000, 3584, 63), (1000, 3584, 64), (1000, 3584, 65),
     (257, 2048, 129), (64, 18944, 200), (300, 1024, 300), (33, 96, 17), (600, 128, 40),
+    (1000, 3584, 17), (77, 18944, 33),  # 16-token slices with a short last slice
 ]
 
 
