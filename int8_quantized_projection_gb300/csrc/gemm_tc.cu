@@ -447,47 +447,75 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 // Pre-pass over the weights: codes -> f16 [n][k] (exact) and each block's d_w
 // as f32 into dwt[row tile][block][dw_slot(row % 128)] (0 for rows past n).
-// A warp takes 32 consecutive blocks of a row at a time (1088 bytes, 16-byte
-// aligned because k/32 % 8 == 0): coalesced 16-byte loads into shared memory,
-// then lane j widens block j from there and writes its 64 bytes of f16.
-constexpr int kPrepWarps = 8;
-constexpr int kPrepBlocks = 32;                     // blocks per warp item
-constexpr int kPrepBytes = kPrepBlocks * 34;         // 1088 = 68 x 16
-__global__ void __launch_bounds__(32 * kPrepWarps)
+// A CTA takes one 32-row group of a tile and B consecutive blocks (B * 34
+// bytes of each row, 16-byte aligned because k/32 % 8 == 0 and B % 8 == 0):
+// each warp loads four row pieces with coalesced 16-byte loads (all in
+// flight at once) to shared memory, then widens their (row, block) pairs,
+// one per lane at a time, each writing its 64 bytes of f16.  The group's d_w slots are
+// contiguous (32 per block), so the scales go through shared memory and out
+// as one 128-byte store per block.  B = 32 when the items fill the GPU
+// several times over; B = 8 spreads a small matrix over more SMs.
+template <int B, int NT>
+__global__ void __launch_bounds__(NT)
 gemm_prep_w_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, uint4 *__restrict__ a16, float *__restrict__ dwt)
 {
-    __shared__ __align__(16) uint8_t buf[kPrepWarps][kPrepBytes];
+    static_assert(B % 8 == 0 && B <= 32, "row pieces must be whole 16-byte words");
+    constexpr int kWarps = NT / 32;
+    constexpr int kRows = 32 / kWarps;                      // rows a warp loads and widens
+    constexpr int kRowWords = B * 34 / 16;                  // 16-byte words per row piece
+    constexpr int kWords = (kRowWords + 31) / 32;           // per lane and row
+    constexpr int kPairs = kRows * B / 32;                  // (row, block) pairs per lane
+    static_assert(kWarps * kRows == 32 && kPairs * 32 == kRows * B, "one 32-row group per CTA");
+    __shared__ __align__(16) uint4 buf[32][kRowWords];
+    __shared__ float sdw[B][33];  // [block][slot in the group], padded: conflict-free both ways
     q8::griddep_launch_dependents();
     q8::griddep_wait();  // the previous call may still read this workspace
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles = (n + BM - 1) / BM;
-    const int chunks = (nb + kPrepBlocks - 1) / kPrepBlocks;  // per row
-    const int64_t items = tiles * BM * chunks;
-    uint8_t *mb = buf[warp];
-    for (int64_t it = (static_cast<int64_t>(blockIdx.x) * kPrepWarps + warp); it < items;
-         it += static_cast<int64_t>(gridDim.x) * kPrepWarps) {
-        const int64_t r = it / chunks;
-        const int c = static_cast<int>(it - r * chunks);
-        const int b0 = c * kPrepBlocks;
-        const int cb = min(kPrepBlocks, nb - b0);  // a multiple of 8
-        const int64_t tile = r / BM;
-        const int j = lane, b = b0 + j;
-        float dw = 0.0f;
-        if (r < n) {
+    const int chunks = (nb + B - 1) / B;  // per row
+    const int64_t items = tiles * (BM / 32) * chunks;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t grp = it / chunks;
+        const int c = static_cast<int>(it - grp * chunks);
+        const int64_t r0 = grp * 32;  // first row of the group
+        const int b0 = c * B;
+        const int cb = min(B, nb - b0);  // a multiple of 8
+        const int n16 = cb * 34 / 16;
+        uint4 v[kRows][kWords];
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            const int64_t r = r0 + kRows * warp + q;
             const uint4 *src = reinterpret_cast<const uint4 *>(w + (r * nb + b0) * 34);
-            const int n16 = cb * 34 / 16;
-            for (int i = lane; i < n16; i += 32) reinterpret_cast<uint4 *>(mb)[i] = __ldg(src + i);
-            __syncwarp();
-            if (j < cb) {
+#pragma unroll
+            for (int u = 0; u < kWords; ++u) {
+                const int i = lane + 32 * u;
+                v[q][u] = (r < n && i < n16) ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kRows; ++q)
+#pragma unroll
+            for (int u = 0; u < kWords; ++u) {
+                const int i = lane + 32 * u;
+                if (i < n16) buf[kRows * warp + q][i] = v[q][u];
+            }
+        __syncwarp();
+#pragma unroll
+        for (int p = 0; p < kPairs; ++p) {
+            const int pi = lane + 32 * p, rr = kRows * warp + pi / B, j = pi % B;
+            const int64_t r = r0 + rr;
+            float dw = 0.0f;
+            if (r < n && j < cb) {
                 // block j at byte 34j: its d at 34j, codes from 34j + 2; nine
                 // words from the word holding byte 34j cover both
                 const int base = (34 * j) >> 2, odd = j & 1;  // 34j % 4 == 2 for odd j
-                const uint32_t *wd = reinterpret_cast<const uint32_t *>(mb) + base;
+                const uint32_t *wd = reinterpret_cast<const uint32_t *>(buf[rr]) + base;
                 uint32_t W[9];
 #pragma unroll
                 for (int u = 0; u < 9; ++u) W[u] = wd[u];
-                dw = __half2float(__ushort_as_half(static_cast<unsigned short>(odd ? (W[0] >> 16) : (W[0] & 0xffffu))));
-                uint4 *dst = a16 + (r * nb + b) * 4;  // 64 bytes of f16 per block
+                dw = __half2float(
+                    __ushort_as_half(static_cast<unsigned short>(odd ? (W[0] >> 16) : (W[0] & 0xffffu))));
+                uint4 *dst = a16 + (r * nb + b0 + j) * 4;  // 64 bytes of f16 per block
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const uint32_t q0 = odd ? W[2 * u + 1] : __byte_perm(W[2 * u], W[2 * u + 1], 0x5432);
@@ -498,9 +526,14 @@ gemm_prep_w_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, uint4 *__re
                     dst[u] = o;
                 }
             }
-            __syncwarp();  // the buffer is reused by the next item
+            sdw[j][dw_slot(rr)] = dw;  // rr < 32: its slot within the group
         }
-        if (j < cb) dwt[(tile * nb + b) * BM + dw_slot(static_cast<int>(r - tile * BM))] = dw;
+        __syncthreads();
+        const int64_t tile = r0 / BM;
+        const int gbase = static_cast<int>(r0 - tile * BM);  // 0, 32, 64, 96: the group's first slot
+        for (int i = threadIdx.x; i < cb * 32; i += NT)
+            dwt[(tile * nb + b0 + (i >> 5)) * BM + gbase + (i & 31)] = sdw[i >> 5][i & 31];
+        __syncthreads();  // sdw and buf are rewritten by the next item
     }
 }
 
@@ -631,11 +664,17 @@ int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const 
         return Q8_ERR_LAUNCH;
     const int sms = device_sm_count();
     const int64_t pcap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
-    const int64_t witems = (n + BM - 1) / BM * BM * ((nb + kPrepBlocks - 1) / kPrepBlocks);
-    int64_t wgrid = (witems + kPrepWarps - 1) / kPrepWarps;
-    wgrid = wgrid < pcap ? wgrid : pcap;
-    int st = launch_pdl(gemm_prep_w_kernel, dim3(static_cast<unsigned>(wgrid)), dim3(32 * kPrepWarps), 0, s,
-                        static_cast<const uint8_t *>(w), n, static_cast<int>(nb), reinterpret_cast<uint4 *>(a16), dwt);
+    const int64_t groups = (n + BM - 1) / BM * (BM / 32);
+    const int64_t wide = groups * ((nb + 31) / 32);  // items of 32 blocks
+    const bool many = wide >= static_cast<int64_t>(sms > 0 ? sms : 152) * 4;
+    const int64_t witems = many ? wide : groups * ((nb + 7) / 8);
+    const unsigned wgrid = static_cast<unsigned>(witems < pcap ? witems : pcap);
+    int st = many ? launch_pdl(gemm_prep_w_kernel<32, 256>, dim3(wgrid), dim3(256), 0, s,
+                               static_cast<const uint8_t *>(w), n, static_cast<int>(nb),
+                               reinterpret_cast<uint4 *>(a16), dwt)
+                  : launch_pdl(gemm_prep_w_kernel<8, 256>, dim3(wgrid), dim3(256), 0, s,
+                               static_cast<const uint8_t *>(w), n, static_cast<int>(nb),
+                               reinterpret_cast<uint4 *>(a16), dwt);
     if (st != Q8_OK) return st;
     const int64_t awork = t * (k / 16) + (t + BN - 1) / BN * nb * BN;
     int64_t agrid = (awork + 255) / 256;
