@@ -507,15 +507,19 @@ def run_asym(torch, q8p, steps, warmup, dev):
 SHARED = dict(d=7168, ns=[3072, 512, 512, 3072], eps=1e-6)
 
 
-def bytes_shared():
+def bytes_shared(fused=False):
     d = SHARED["d"]
+    if fused:
+        return bytes_gemv_fused(d, SHARED["ns"], "rmsnorm")
     return bytes_rmsnorm_quant(1, d, False) + bytes_gemv_group(d, SHARED["ns"])
 
 
 def run_shared(torch, q8p, steps, warmup, dev):
-    """rmsnorm_quant (mode 2) -> q8_0_gemv_grouped over the four projections:
-    two launches per step, recorded as a CUDA graph of one step per weight
-    copy (copies together > 4 x L2)."""
+    """RMSNorm + q8_0 quantize feeding the four projections, timed two ways:
+    one q8_0_gemv_fused launch per step (the norm computed inside the grouped
+    GEMV), and rmsnorm_quant (mode 2) -> q8_0_gemv_grouped (two launches).
+    Each is recorded as a CUDA graph of one step per weight copy (copies
+    together > 4 x L2)."""
     d, ns, eps = SHARED["d"], SHARED["ns"], SHARED["eps"]
     g = syn.rng(2, 0)
     x = torch.from_numpy(syn.activations(g, 1, d)).to(dev)
@@ -529,29 +533,37 @@ def run_shared(torch, q8p, steps, warmup, dev):
     cap = torch.cuda.Stream(dev)
     norm = q8p.rmsnorm_quant(x, nw, eps, None, *plane, stream=cap, bind=True)
     gemvs = [q8p.q8_0_gemv_grouped(list(zip(wset, ns, ys)), d, *plane, stream=cap, bind=True) for wset in ws]
+    fused = [q8p.q8_0_gemv_fused(list(zip(wset, ns, ys)), d, q8p.PRODUCER_RMSNORM, x[0], None, nw, eps,
+                                 stream=cap, bind=True) for wset in ws]
+    steps_two = [[norm, gm] for gm in gemvs]  # one step per weight copy
+    steps_fused = [[fu] for fu in fused]
     stream = torch.cuda.current_stream(dev)
-    cap.wait_stream(stream)
-    for i in range(max(copies, warmup)):
-        norm()
-        gemvs[i % copies]()
-    q8p.q8_check()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=cap):
-        for i in range(copies):
-            norm()
-            gemvs[i]()
-    stream.wait_stream(cap)
-    graph.replay()
-    torch.cuda.synchronize(dev)
     reps = max(1, steps // copies)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(reps):
+    res = {}
+    for name, per_copy_calls in (("fused", steps_fused), ("two", steps_two)):
+        cap.wait_stream(stream)
+        for i in range(max(copies, warmup)):
+            for c in per_copy_calls[i % copies]:
+                c()
+        q8p.q8_check()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for calls in per_copy_calls:
+                for c in calls:
+                    c()
+        stream.wait_stream(cap)
         graph.replay()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    q8p.q8_check()
-    return dict(us=1e3 * t0.elapsed_time(t1) / (reps * copies), copies=copies, steps=reps * copies)
+        torch.cuda.synchronize(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        q8p.q8_check()
+        res[name] = 1e3 * t0.elapsed_time(t1) / (reps * copies)
+        del graph
+    return dict(us=res["fused"], us_two=res["two"], copies=copies, steps=reps * copies)
 
 
 # ---------------------------------------------------------------------------
@@ -559,6 +571,12 @@ def run_shared(torch, q8p, steps, warmup, dev):
 # LM head for one token (batch 1), recorded as one CUDA graph
 # ---------------------------------------------------------------------------
 LAYERS = dict(layers=28, d=3584, nf=18944, q=3584, kv=512, vocab=152064, eps=1e-6)
+# Producers computed inside their consumer's launch (q8_0_gemv_fused) in the
+# layer stack's headline figure: where that measured faster than a separate
+# producer launch in the chain (RMSNorm -> q/k/v; the final RMSNorm -> LM head
+# is even).  Fusing quantize -> o is even, RMSNorm -> gate/up and SwiGLU ->
+# down measured slower: every CTA then recomputes a long row.
+LAYER_FUSED = ("qkv", "head")
 
 
 def layer_groups():
@@ -573,19 +591,40 @@ def bytes_gemv_group(k, ns):
     return sum(n * (k // 32) * 34 + 4 * n for n in ns) + k + 4 * (k // 32)
 
 
-def bytes_layer_stack():
+def bytes_gemv_fused(k, ns, producer):
+    # every projection's weights and outputs, and the producer's f32 inputs read
+    # once (x; x and the norm weight; gate and up): no plane is written or read
+    f32_in = {"quant": 4 * k, "rmsnorm": 8 * k, "swiglu": 8 * k}[producer]
+    return sum(n * (k // 32) * 34 + 4 * n for n in ns) + f32_in
+
+
+def bytes_layer_stack(fused=()):
+    """Algorithmic bytes of one token; `fused` = the producers computed inside
+    their consumer's launch (of "qkv", "o", "gu", "down", "head")."""
     L = LAYERS
     d, nf = L["d"], L["nf"]
-    producers = 2 * bytes_rmsnorm_quant(1, d, False) + bytes_quantize(1, d) + bytes_swiglu_quant(1, nf, False)
-    per_layer = producers + sum(bytes_gemv_group(k, ns) for k, ns in layer_groups())
-    return L["layers"] * per_layer + bytes_rmsnorm_quant(1, d, False) + bytes_gemv_group(d, [L["vocab"]])
+    (_, qkv), (_, o), (_, gu), (_, down) = layer_groups()
+    steps = [("qkv", d, qkv, "rmsnorm"), ("o", d, o, "quant"), ("gu", d, gu, "rmsnorm"), ("down", nf, down, "swiglu")]
+
+    def one(name, k, ns, producer):
+        if name in fused:
+            return bytes_gemv_fused(k, ns, producer)
+        prod = {"rmsnorm": bytes_rmsnorm_quant(1, k, False), "quant": bytes_quantize(1, k),
+                "swiglu": bytes_swiglu_quant(1, k, False)}[producer]
+        return prod + bytes_gemv_group(k, ns)
+    per_layer = sum(one(*st) for st in steps)
+    return L["layers"] * per_layer + one("head", d, [L["vocab"]], "rmsnorm")
 
 
 def run_layers(torch, q8p, steps, warmup, dev):
-    """Per layer: rmsnorm_quant -> q/k/v (one grouped launch); quantize of the
-    attention output -> o; rmsnorm_quant -> gate/up (one grouped launch);
-    swiglu_quant of their outputs -> down.  Then the final norm and the LM
-    head.  The producers run in mode 2 (their consumers read only the plane).
+    """Per layer: RMSNorm -> q/k/v (one grouped launch); quantize of the
+    attention output -> o; RMSNorm -> gate/up (one grouped launch); SwiGLU of
+    their outputs -> down.  Then the final norm and the LM head.  Timed three
+    ways, each as one CUDA graph per token: the producers of LAYER_FUSED
+    inside their consumer's launch (q8_0_gemv_fused) and the others as their
+    own launches in mode 2 (the headline); every producer as its own launch
+    (rmsnorm_quant / quantize_q8_0 / swiglu_quant, then the GEMV on the plane:
+    8 launches per layer); every producer fused (4 launches per layer).
     Layer 0's matrices are drawn from the synthetic recipe; layers 1..27 are
     device copies of them (the same bytes, distinct memory, so every token
     streams all 7.5 GB from HBM)."""
@@ -606,43 +645,63 @@ def run_layers(torch, q8p, steps, warmup, dev):
     ys = [torch.empty((1, n), dtype=torch.float32, device=dev) for n, _ in shapes]
     logits = torch.empty(L["vocab"], dtype=torch.float32, device=dev)
     cap = torch.cuda.Stream(dev)
-    calls = []
-    for wl in layers:
-        wq, wk, wv, wo, wg, wu, wd = wl
-        calls += [q8p.rmsnorm_quant(x, nw1, eps, None, *pd, stream=cap, bind=True),
-                  q8p.q8_0_gemv_grouped([(wq, L["q"], ys[0]), (wk, L["kv"], ys[1]), (wv, L["kv"], ys[2])], d, *pd,
-                                        stream=cap, bind=True),
-                  q8p.quantize_q8_0(attn, *pd, stream=cap, bind=True),
-                  q8p.q8_0_gemv(wo, d, d, *pd, ys[3], stream=cap, bind=True),
-                  q8p.rmsnorm_quant(h, nw2, eps, None, *pd, stream=cap, bind=True),
-                  q8p.q8_0_gemv_grouped([(wg, nf, ys[4]), (wu, nf, ys[5])], d, *pd, stream=cap, bind=True),
-                  q8p.swiglu_quant(ys[4], ys[5], None, *pf, stream=cap, bind=True),
-                  q8p.q8_0_gemv(wd, d, nf, *pf, ys[6], stream=cap, bind=True)]
-    calls += [q8p.rmsnorm_quant(x, nwf, eps, None, *pd, stream=cap, bind=True),
-              q8p.q8_0_gemv(head, L["vocab"], d, *pd, logits, stream=cap, bind=True)]
+    P_Q, P_R, P_S = q8p.PRODUCER_QUANT, q8p.PRODUCER_RMSNORM, q8p.PRODUCER_SWIGLU
 
+    def token(fuse):
+        """One token's launches; `fuse` = the producers computed inside their
+        consumer's launch, of {"qkv", "o", "gu", "down", "head"}."""
+        c = []
+        for wq, wk, wv, wo, wg, wu, wd in layers:
+            qkv = [(wq, L["q"], ys[0]), (wk, L["kv"], ys[1]), (wv, L["kv"], ys[2])]
+            gu = [(wg, nf, ys[4]), (wu, nf, ys[5])]
+            c += ([q8p.q8_0_gemv_fused(qkv, d, P_R, x[0], None, nw1, eps, stream=cap, bind=True)] if "qkv" in fuse
+                  else [q8p.rmsnorm_quant(x, nw1, eps, None, *pd, stream=cap, bind=True),
+                        q8p.q8_0_gemv_grouped(qkv, d, *pd, stream=cap, bind=True)])
+            c += ([q8p.q8_0_gemv_fused([(wo, d, ys[3])], d, P_Q, attn[0], stream=cap, bind=True)] if "o" in fuse
+                  else [q8p.quantize_q8_0(attn, *pd, stream=cap, bind=True),
+                        q8p.q8_0_gemv(wo, d, d, *pd, ys[3], stream=cap, bind=True)])
+            c += ([q8p.q8_0_gemv_fused(gu, d, P_R, h[0], None, nw2, eps, stream=cap, bind=True)] if "gu" in fuse
+                  else [q8p.rmsnorm_quant(h, nw2, eps, None, *pd, stream=cap, bind=True),
+                        q8p.q8_0_gemv_grouped(gu, d, *pd, stream=cap, bind=True)])
+            c += ([q8p.q8_0_gemv_fused([(wd, d, ys[6])], nf, P_S, ys[4][0], ys[5][0], stream=cap, bind=True)]
+                  if "down" in fuse else
+                  [q8p.swiglu_quant(ys[4], ys[5], None, *pf, stream=cap, bind=True),
+                   q8p.q8_0_gemv(wd, d, nf, *pf, ys[6], stream=cap, bind=True)])
+        c += ([q8p.q8_0_gemv_fused([(head, L["vocab"], logits)], d, P_R, x[0], None, nwf, eps, stream=cap,
+                                   bind=True)] if "head" in fuse
+              else [q8p.rmsnorm_quant(x, nwf, eps, None, *pd, stream=cap, bind=True),
+                    q8p.q8_0_gemv(head, L["vocab"], d, *pd, logits, stream=cap, bind=True)])
+        return c
+
+    variants = {"mixed": token(LAYER_FUSED), "two": token(()), "fused": token(("qkv", "o", "gu", "down", "head"))}
     stream = torch.cuda.current_stream(dev)
-    cap.wait_stream(stream)
-    for _ in range(max(1, warmup)):  # eager, outside the capture
-        for c in calls:
-            c()
-    q8p.q8_check()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=cap):
-        for c in calls:
-            c()
-    stream.wait_stream(cap)
-    for _ in range(warmup):
-        graph.replay()
-    torch.cuda.synchronize(dev)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        graph.replay()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    q8p.q8_check()
-    return dict(ms=t0.elapsed_time(t1) / steps, launches=len(calls),
+    res = {}
+    for name, calls in variants.items():
+        cap.wait_stream(stream)
+        for _ in range(max(1, warmup)):  # eager, outside the capture
+            for c in calls:
+                c()
+        q8p.q8_check()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for c in calls:
+                c()
+        stream.wait_stream(cap)
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        q8p.q8_check()
+        res[name] = t0.elapsed_time(t1) / steps
+        del graph
+    return dict(ms=res["mixed"], ms_two=res["two"], ms_fused=res["fused"],
+                launches=len(variants["mixed"]), launches_two=len(variants["two"]),
+                launches_fused=len(variants["fused"]),
                 weight_bytes=sum(w.numel() for w in layers[0]) * L["layers"] + head.numel())
 
 
@@ -797,7 +856,8 @@ def main():
         vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"]] if dec else [])
                 + (list(pre.values()) if pre else [])
                 + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else [])
-                + ([lay["ms"]] if lay else []) + ([shr["us"]] if shr else []))
+                + ([lay["ms"], lay["ms_two"], lay["ms_fused"]] if lay else [])
+                + ([shr["us"], shr["us_two"]] if shr else []))
         red = max_over_ranks(torch, vals, dev)
         if dec:
             dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"] = red[:5]
@@ -810,9 +870,9 @@ def main():
         if asym:
             asym["us"], asym["us_b2b"] = red.pop(0), red.pop(0)
         if lay:
-            lay["ms"] = red.pop(0)
+            lay["ms"], lay["ms_two"], lay["ms_fused"] = red.pop(0), red.pop(0), red.pop(0)
         if shr:
-            shr["us"] = red.pop(0)
+            shr["us"], shr["us_two"] = red.pop(0), red.pop(0)
 
     if rank != 0:
         if world > 1:
@@ -913,34 +973,50 @@ def main():
                          "roofline": aobj["roofline"], "gpu_launches": 2 * args.steps})
         line["asym_gemv"] = aobj
     if shr is not None:
-        byts = bytes_shared()
+        byts = bytes_shared(fused=True)
         gbs = byts / (shr["us"] / 1e6) / 1e9
-        sobj2 = {"workload": f"shared-activation decode b=1: rmsnorm_quant (d={SHARED['d']}, mode 2) -> q/k/v/gate "
-                             f"{'/'.join(str(n) for n in SHARED['ns'])} in one grouped GEMV launch",
+        byts2 = bytes_shared()
+        sobj2 = {"workload": f"shared-activation decode b=1: RMSNorm (d={SHARED['d']}) + q8_0 quantize feeding "
+                             f"q/k/v/gate {'/'.join(str(n) for n in SHARED['ns'])} in one q8_0_gemv_fused launch "
+                             "(the norm computed inside the grouped GEMV)",
                  "us_per_step": round(shr["us"], 2), "gbs": round(gbs, 1), "algorithmic_bytes": byts,
-                 "launches_per_step": 2,
+                 "launches_per_step": 1,
                  "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": round(gbs / peaks["hbm_gbs"], 4)},
+                 "two_launch": {"calls": "rmsnorm_quant (mode 2) -> q8_0_gemv_grouped",
+                                "us_per_step": round(shr["us_two"], 2),
+                                "gbs": round(byts2 / (shr["us_two"] / 1e6) / 1e9, 1), "algorithmic_bytes": byts2,
+                                "launches_per_step": 2},
                  "launch": f"CUDA graph of one step per weight copy ({shr['copies']} copies > 4 x L2), replayed"}
         if args.workload == "shared":
             line.update({"value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": round(shr["us"] / 1e3, 5),
                          "config": {"workload": sobj2["workload"], "l2": f"{shr['copies']} weight copies > 4 x L2",
                                     "parallelism": "replicas"},
-                         "roofline": sobj2["roofline"], "gpu_launches": 2 * shr["steps"]})
+                         "roofline": sobj2["roofline"], "gpu_launches": shr["steps"]})
         line["shared_activation"] = sobj2
     if lay is not None:
         L = LAYERS
-        byts = bytes_layer_stack()
+        byts = bytes_layer_stack(LAYER_FUSED)
         gbs = byts / (lay["ms"] / 1e3) / 1e9
+        byts2, byts3 = bytes_layer_stack(), bytes_layer_stack(("qkv", "o", "gu", "down", "head"))
         lobj = {"workload": f"layer-stack decode b=1: {L['layers']} layers (d={L['d']}, nf={L['nf']}; q {L['q']}, "
-                            f"k/v {L['kv']}, o, gate/up, down) + LM head {L['vocab']}x{L['d']}; per layer "
-                            "rmsnorm_quant, grouped q/k/v, quantize, o, rmsnorm_quant, grouped gate/up, swiglu_quant, "
-                            "down (producers in mode 2)",
+                            f"k/v {L['kv']}, o, gate/up, down) + LM head {L['vocab']}x{L['d']}; per layer RMSNorm "
+                            "-> grouped q/k/v, quantize -> o, RMSNorm -> grouped gate/up, SwiGLU -> down; producers "
+                            f"fused into their GEMV launch (q8_0_gemv_fused): {', '.join(LAYER_FUSED)}; the others "
+                            "as their own launches in mode 2",
                 "ms_per_token": round(lay["ms"], 4), "tokens_per_s": round(1e3 / lay["ms"], 1),
                 "gbs": round(gbs, 1), "algorithmic_bytes": byts, "weight_bytes": lay["weight_bytes"],
                 "launches_per_token": lay["launches"],
                 "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": round(gbs / peaks["hbm_gbs"], 4)},
+                "two_launch": {"calls": "every producer as its own launch (mode 2), then the GEMV on its plane",
+                               "ms_per_token": round(lay["ms_two"], 4),
+                               "gbs": round(byts2 / (lay["ms_two"] / 1e3) / 1e9, 1), "algorithmic_bytes": byts2,
+                               "launches_per_token": lay["launches_two"]},
+                "all_fused": {"calls": "every producer inside its GEMV launch (q8_0_gemv_fused)",
+                              "ms_per_token": round(lay["ms_fused"], 4),
+                              "gbs": round(byts3 / (lay["ms_fused"] / 1e3) / 1e9, 1), "algorithmic_bytes": byts3,
+                              "launches_per_token": lay["launches_fused"]},
                 "launch": "one CUDA graph per token, replayed; layers 1..27 are device copies of layer 0's matrices "
                           "(distinct memory: 7.5 GB streamed per token, > L2)"}
         if args.workload == "layers":

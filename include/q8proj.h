@@ -161,6 +161,41 @@ Q8_API int q8_0_gemv_grouped(const q8_gemv_proj *projs, int count, int64_t k,
                              const int8_t *qs, const uint32_t *ds, void *stream);
 
 /*
+ * q8_0_gemv_fused -- q8_0_gemv_grouped with its one-row producer in the same
+ * launch: every CTA computes the producer's f32 row and its q8_0 encoding
+ * straight into the shared memory it would otherwise fill from a plane, so
+ * the producer's launch, the plane's write and re-read, and the hand-off
+ * between two launches disappear.
+ *   producer : Q8_PRODUCER_QUANT    a = x f32 [k]            (as quantize_q8_0)
+ *              Q8_PRODUCER_RMSNORM  a = x f32 [k], norm_w = w f32 [k], eps
+ *                                   (as rmsnorm_quant)
+ *              Q8_PRODUCER_SWIGLU   a = gate f32 [k], b = up f32 [k]
+ *                                   (as swiglu_quant)
+ *              unused pointers may be NULL; all inputs are read only.
+ *   projs, count, k : as for q8_0_gemv_grouped; each projs[i].y is written.
+ * Result: bit for bit what the standalone producer (one row, rows_pad at most
+ * the SM count -- e.g. q8_plane_rows(1)) followed by q8_0_gemv_grouped on its
+ * plane returns: the producer arithmetic is one implementation shared by both
+ * paths, and for RMSNorm the row's sum of squares is formed in the standalone
+ * kernel's order.  No f32 row or plane is written.
+ * Requires (k/32) % 8 == 0 and k <= 65536 (the staged path), k <= 32768 for
+ * RMSNorm; otherwise Q8_ERR_ARG (run the producer and the GEMV as two calls).
+ * Pointers 16-byte aligned (Q8_ERR_ALIGN).  The producer's inputs are read
+ * only after the kernel enqueued before the call on `stream` has finished
+ * (the same programmatic-dependent-launch rule as q8_0_gemv: the weights may
+ * be streamed earlier); the outputs must not overlap the inputs.
+ * "Part 4 - Lecture 05", sec. 3 (a one-row quantize costs a launch, not
+ * bandwidth) and sec. 4 (its rule: make producer and consumer one launch, and
+ * keep one implementation for the fused and the unfused path).
+ */
+#define Q8_PRODUCER_QUANT   1
+#define Q8_PRODUCER_RMSNORM 2
+#define Q8_PRODUCER_SWIGLU  3
+Q8_API int q8_0_gemv_fused(const q8_gemv_proj *projs, int count, int64_t k, int producer,
+                           const float *a, const float *b, const float *norm_w, float eps,
+                           void *stream);
+
+/*
  * q8_0_gemv_batched -- the projection for a few tokens at once (decode over
  * a small batch of sequences): Y[t][i] = sum_b d_w(i,b) * d_a(t,b) * isum for
  * plane rows t < tokens, reading the weights from memory once for all of

@@ -20,7 +20,11 @@ from ._binding import (  # noqa: F401
     q8_0_gemm_workspace_bytes,
     q8_0_gemv,
     q8_0_gemv_grouped,
+    q8_0_gemv_fused,
     q8_0_gemv_batched,
+    PRODUCER_QUANT,
+    PRODUCER_RMSNORM,
+    PRODUCER_SWIGLU,
     q4a_gemv,
     q4a_gemv_batched,
     GEMV_MAX_TOKENS,

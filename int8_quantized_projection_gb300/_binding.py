@@ -37,6 +37,7 @@ SIGNATURES = {
     "q8_0_gemm_noalloc": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
     "q8_0_gemm_noalloc_max_bytes": (ctypes.c_size_t, []),
     "q8_0_gemv_grouped": (_INT, [_P, _INT, _I64, _P, _P, _P]),
+    "q8_0_gemv_fused": (_INT, [_P, _INT, _I64, _INT, _P, _P, _P, ctypes.c_float, _P]),
     "q8_0_gemv_batched": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P]),
     "q4a_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q4a_gemv_batched": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P]),
@@ -47,6 +48,7 @@ SIGNATURES = {
 
 MAX_GROUP = 8
 GEMV_MAX_TOKENS = 16
+PRODUCER_QUANT, PRODUCER_RMSNORM, PRODUCER_SWIGLU = 1, 2, 3
 
 
 class GemvProj(ctypes.Structure):
@@ -262,6 +264,49 @@ def q8_0_gemv_grouped(projs, k: int, qs, ds, stream=None, bind=False):
         b._keep = (arr, keep)  # the descriptor array must outlive the bound launch
         return b
     _check("q8_0_gemv_grouped", lib().q8_0_gemv_grouped(*args))
+    return None
+
+
+def _proj_array(projs, k):
+    import torch
+
+    if not 1 <= len(projs) <= MAX_GROUP:
+        raise ValueError("1..8 projections sharing k")
+    arr = (GemvProj * len(projs))()
+    keep = []
+    for i, (w, n, y) in enumerate(projs):
+        _need(w, torch.uint8, "w"), _need(y, torch.float32, "y")
+        if w.numel() != n * (k // 32) * 34 or y.numel() < n:
+            raise ValueError("shape mismatch")
+        arr[i] = GemvProj(w.data_ptr(), n, y.data_ptr())
+        keep.append((w, y))
+    return arr, keep
+
+
+def q8_0_gemv_fused(projs, k: int, producer: int, a, b=None, norm_w=None, eps: float = 0.0, stream=None,
+                    bind=False):
+    """Grouped batch-1 projections whose activation the same launch produces.
+
+    ``producer`` is PRODUCER_QUANT (a = x f32 [k]), PRODUCER_RMSNORM (a = x,
+    norm_w = w f32 [k], eps) or PRODUCER_SWIGLU (a = gate, b = up, f32 [k]);
+    ``projs`` as for :func:`q8_0_gemv_grouped`."""
+    import torch
+
+    for t, nm in ((a, "a"), (b, "b"), (norm_w, "norm_w")):
+        if t is not None:
+            _need(t, torch.float32, nm)
+            if t.numel() < k:
+                raise ValueError(f"{nm}: fewer than k elements")
+    arr, keep = _proj_array(projs, k)
+    nul = ctypes.c_void_p(0)
+    args = (ctypes.cast(arr, ctypes.c_void_p), len(projs), k, int(producer), _ptr(a),
+            _ptr(b) if b is not None else nul, _ptr(norm_w) if norm_w is not None else nul, float(eps),
+            _stream(stream))
+    if bind:
+        bd = Bound("q8_0_gemv_fused", args)
+        bd._keep = (arr, keep, a, b, norm_w)
+        return bd
+    _check("q8_0_gemv_fused", lib().q8_0_gemv_fused(*args))
     return None
 
 

@@ -51,8 +51,21 @@ struct GvProj {
     int64_t g_begin;   // first row group of this projection in the launch's group list
 };
 
+// Where the CTAs' staged activation comes from: a plane (row 0 of qs/ds),
+// or one f32 row that every CTA encodes itself with the producer's own
+// arithmetic (q8_0_gemv_fused).
+struct GvAct {
+    int producer;     // 0: plane; else Q8_PRODUCER_QUANT / _RMSNORM / _SWIGLU
+    const float4 *a;  // x, or gate
+    const float4 *b;  // up (SWIGLU)
+    const float4 *w;  // RMSNorm weight
+    float eps;
+    int rms_j, rms_p; // the standalone RMSNorm's thread mapping for this k
+};
+
 // Geometry shared by all projections of a launch (they share k).
 struct GvGeom {
+    GvAct act;
     GvProj p[kMaxProj];
     int count;
     int nc;          // 4-block chunks per row (even: k/32 % 8 == 0)
@@ -173,6 +186,54 @@ __device__ __forceinline__ float FmtQ8_0::dot(const uint8_t *wc, const uint8_t *
     return acc;
 }
 
+// Fused activation staging: the producer's f32 row and its q8_0 encoding,
+// computed by this CTA into the staged layout (chunk c: 32 qs words, then
+// the d|ssum words of its 4 blocks).  Warp w encodes chunks w, w + nwarps,
+// ...: lane l holds float4 32c + l, so 8 adjacent lanes hold one block, as
+// in the standalone producers.  For RMSNorm the row's sum of squares is
+// first formed exactly as the standalone kernel forms it with P threads:
+// this CTA's warps play its P/32 warps in turn (a CTA's thread count is a
+// multiple of 32, so lane l plays lane l), `red` collects the warp sums,
+// and every thread adds them in warp order.
+__device__ __forceinline__ void stage_produced(const GvGeom &g, uint8_t *act, float *red, int warp, int lane)
+{
+    const int nwarps = static_cast<int>(blockDim.x >> 5);
+    const int F = g.nc * 32;  // float4 per row
+    const GvAct &A = g.act;
+    float scale = 0.0f;
+    if (A.producer == Q8_PRODUCER_RMSNORM) {
+        const int vws = A.rms_p >> 5;
+        for (int vw = warp; vw < vws; vw += nwarps) {
+            const int vt = vw * 32 + lane;
+            float ss = 0.0f;
+            for (int j = 0; j < A.rms_j; ++j) {
+                const int f = vt + j * A.rms_p;
+                ss = q8::rms_sumsq4(ss, f < F ? __ldg(A.a + f) : make_float4(0.f, 0.f, 0.f, 0.f));
+            }
+            ss = q8::rms_warp_sum(ss);
+            if (lane == 0) red[vw] = ss;
+        }
+        __syncthreads();
+        float tot = 0.0f;
+        for (int i = 0; i < vws; ++i) tot += red[i];
+        scale = q8::rms_scale(tot, F * 4, A.eps);
+    }
+    for (int c = warp; c < g.nc; c += nwarps) {
+        const int f = c * 32 + lane;
+        float4 o;
+        if (A.producer == Q8_PRODUCER_RMSNORM)
+            o = q8::rms_apply4(__ldg(A.a + f), scale, __ldg(A.w + f));
+        else if (A.producer == Q8_PRODUCER_SWIGLU)
+            o = q8::silu_mul4(__ldg(A.a + f), __ldg(A.b + f));
+        else
+            o = __ldg(A.a + f);
+        const q8::Q8Enc e = q8::q8_encode8(o);
+        uint8_t *ch = act + c * kActChunkBytes;
+        reinterpret_cast<uint32_t *>(ch)[lane] = e.qword;
+        if ((lane & 7) == 0) reinterpret_cast<uint32_t *>(ch + 128)[lane >> 3] = e.dsword;
+    }
+}
+
 template <class F>
 __global__ void __launch_bounds__(F::kWarps * 32)
 gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict__ ds_row,
@@ -257,13 +318,21 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
     // streaming them before waiting for it (programmatic dependent launch).
     if (lane == 0)
         for (int s = 0; s < kStages; ++s) issue(s);
+    if (g.act.producer == Q8_PRODUCER_RMSNORM)  // the norm weight is a constant input too: to L1 now
+        for (int l = threadIdx.x; l < g.nc * 4; l += blockDim.x)  // 128-byte lines of k floats
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(g.act.w + 8 * l));
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // stage the activation: chunk c = 8 x 16 B of qs then its 4 ds words
-    for (int idx = threadIdx.x; idx < g.nc * 9; idx += blockDim.x) {
-        const int c = idx / 9, j = idx - c * 9;
-        const uint4 v = (j < 8) ? __ldg(qs_row + c * 8 + j) : __ldg(reinterpret_cast<const uint4 *>(ds_row) + c);
-        *reinterpret_cast<uint4 *>(act + c * kActChunkBytes + 16 * j) = v;
+    if (g.act.producer == 0) {
+        // stage the activation: chunk c = 8 x 16 B of qs then its 4 ds words
+        for (int idx = threadIdx.x; idx < g.nc * 9; idx += blockDim.x) {
+            const int c = idx / 9, j = idx - c * 9;
+            const uint4 v = (j < 8) ? __ldg(qs_row + c * 8 + j) : __ldg(reinterpret_cast<const uint4 *>(ds_row) + c);
+            *reinterpret_cast<uint4 *>(act + c * kActChunkBytes + 16 * j) = v;
+        }
+    } else {
+        // RMSNorm's warp sums: the free upper 64 bytes of the header's last 128
+        stage_produced(g, act, reinterpret_cast<float *>(counter + 16), warp, lane);
     }
     __syncthreads();
 
@@ -910,7 +979,7 @@ namespace {
 // Launch the staged kernel for `count` projections of one activation.
 template <class F>
 int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds,
-                       cudaStream_t s, int smem_slot)
+                       cudaStream_t s, int smem_slot, const GvAct *act = nullptr)
 {
     constexpr int kStages = F::kStages;
     constexpr int kMaxWarps = F::kWarps;
@@ -918,6 +987,11 @@ int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const in
     constexpr int kPieceChunks = 32 * F::kLaneChunks;
     const int64_t nb = k / 32;
     GvGeom g;
+    if (act) {
+        g.act = *act;
+    } else {
+        g.act = GvAct{};  // producer 0: stage plane row 0
+    }
     g.count = count;
     g.nc = static_cast<int>(nb / 4);
     if (g.nc > 32) {  // long rows: one row per piece, 32*J chunks of it
@@ -978,13 +1052,21 @@ int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const in
     return q8::launch_status();
 }
 
+int check_projs(const q8_gemv_proj *projs, int count, int64_t k)
+{
+    if (!projs || count < 1 || count > Q8_MAX_GROUP || k <= 0 || (k % 32) != 0) return Q8_ERR_ARG;
+    for (int i = 0; i < count; ++i)
+        if (!projs[i].w || !projs[i].y || projs[i].n < 1 || projs[i].n > (int64_t(1) << 40)) return Q8_ERR_ARG;
+    for (int i = 0; i < count; ++i)
+        if (!q8::aligned16(projs[i].w) || !q8::aligned16(projs[i].y)) return Q8_ERR_ALIGN;
+    return Q8_OK;
+}
+
 int check_gemv_args(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds)
 {
-    if (!projs || count < 1 || count > Q8_MAX_GROUP || !qs || !ds || k <= 0 || (k % 32) != 0) return Q8_ERR_ARG;
-    for (int i = 0; i < count; ++i) {
-        if (!projs[i].w || !projs[i].y || projs[i].n < 1 || projs[i].n > (int64_t(1) << 40)) return Q8_ERR_ARG;
-        if (!q8::aligned16(projs[i].w) || !q8::aligned16(projs[i].y)) return Q8_ERR_ALIGN;
-    }
+    if (!qs || !ds) return Q8_ERR_ARG;
+    const int st = check_projs(projs, count, k);
+    if (st != Q8_OK) return st;
     if (!q8::aligned16(qs) || !q8::aligned16(ds)) return Q8_ERR_ALIGN;
     return Q8_OK;
 }
@@ -1030,6 +1112,35 @@ extern "C" int q8_0_gemv_grouped(const q8_gemv_proj *projs, int count, int64_t k
                                  const uint32_t *ds, void *stream)
 {
     return gemv_dispatch(projs, count, k, qs, ds, stream);
+}
+
+extern "C" int q8_0_gemv_fused(const q8_gemv_proj *projs, int count, int64_t k, int producer, const float *a,
+                               const float *b, const float *norm_w, float eps, void *stream)
+{
+    if (producer != Q8_PRODUCER_QUANT && producer != Q8_PRODUCER_RMSNORM && producer != Q8_PRODUCER_SWIGLU)
+        return Q8_ERR_ARG;
+    int st = check_projs(projs, count, k);
+    if (st != Q8_OK) return st;
+    if (!a || (producer == Q8_PRODUCER_SWIGLU && !b) || (producer == Q8_PRODUCER_RMSNORM && !norm_w))
+        return Q8_ERR_ARG;
+    // the staged path only: whole 8-block row pieces, the row's encoding in
+    // shared memory, and (RMSNorm) the standalone kernel's row limit
+    if ((k / 32) % 8 != 0 || k / 128 > kMaxActChunks || (producer == Q8_PRODUCER_RMSNORM && k > 32768))
+        return Q8_ERR_ARG;
+    if (!q8::aligned16(a) || (producer == Q8_PRODUCER_SWIGLU && !q8::aligned16(b)) ||
+        (producer == Q8_PRODUCER_RMSNORM && !q8::aligned16(norm_w)))
+        return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    GvAct act{};
+    act.producer = producer;
+    act.a = reinterpret_cast<const float4 *>(a);
+    act.b = producer == Q8_PRODUCER_SWIGLU ? reinterpret_cast<const float4 *>(b) : nullptr;
+    act.w = producer == Q8_PRODUCER_RMSNORM ? reinterpret_cast<const float4 *>(norm_w) : nullptr;
+    act.eps = eps;
+    // one row: the standalone RMSNorm's mapping for rows_pad <= the SM count
+    q8::rms_row_mapping(static_cast<int>(k / 4), q8::kRmsMaxThreadsOneRow, act.rms_j, act.rms_p);
+    return gemv_staged_launch<FmtQ8_0>(projs, count, k, nullptr, nullptr, static_cast<cudaStream_t>(stream), 0,
+                                       &act);
 }
 
 extern "C" int q8_0_gemv_batched(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds,

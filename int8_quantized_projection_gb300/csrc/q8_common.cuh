@@ -284,4 +284,68 @@ __device__ __forceinline__ Q8Enc q8_encode8(float4 v)
     return e;
 }
 
+// Producer arithmetic, one implementation for the standalone producers
+// (quantize.cu) and the activation staging of the fused GEMV (gemv.cu), so
+// both compute the same f32 bits and therefore the same plane.
+//
+// SwiGLU element: silu(g) * u with the hardware exp2 and reciprocal (a few
+// ulp).  For g < -87.3 the denominator exceeds 2^126 and the quotient is 0,
+// where the true value is below 1e-36.
+__device__ __forceinline__ float silu_mul(float g, float u)
+{
+    return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
+}
+
+__device__ __forceinline__ float4 silu_mul4(float4 g, float4 u)
+{
+    return make_float4(silu_mul(g.x, u.x), silu_mul(g.y, u.y), silu_mul(g.z, u.z), silu_mul(g.w, u.w));
+}
+
+// RMSNorm.  A row's sum of squares is accumulated by P threads: thread p
+// adds the squares of float4 p, p + P, ..., p + (J-1)P in that order with
+// fused multiply-adds, each warp sums its 32 partials by xor shuffles
+// (16, 8, 4, 2, 1), and the P/32 warp sums are added in warp order.
+// (J, P) depend only on d and on max_p, the most threads a row may take.
+__device__ __forceinline__ float rms_sumsq4(float ss, float4 v)
+{
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    return fmaf(v.w, v.w, ss);
+}
+
+__device__ __forceinline__ float rms_warp_sum(float ss)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(Q8_FULL_MASK, ss, o);
+    return ss;
+}
+
+__device__ __forceinline__ float rms_scale(float total, int d, float eps)
+{
+    return rsqrtf(total / static_cast<float>(d) + eps);
+}
+
+// y = (x * scale) * w, two roundings per element
+__device__ __forceinline__ float4 rms_apply4(float4 v, float scale, float4 w)
+{
+    return make_float4(__fmul_rn(__fmul_rn(v.x, scale), w.x), __fmul_rn(__fmul_rn(v.y, scale), w.y),
+                       __fmul_rn(__fmul_rn(v.z, scale), w.z), __fmul_rn(__fmul_rn(v.w, scale), w.w));
+}
+
+// float4 per thread (J, a power of two up to 16) and threads per row (P, a
+// multiple of 32) for a row of F float4 with at most max_p threads.
+__host__ __device__ inline void rms_row_mapping(int F, int max_p, int &J, int &P)
+{
+    J = 1;
+    while (J < 16 && (F + J - 1) / J > max_p) J *= 2;
+    P = ((F + J - 1) / J + 31) / 32 * 32;
+}
+
+// The most threads a row of the standalone RMSNorm takes: 512 when every CTA
+// has at most one row (rows_pad <= the SM count, e.g. a decode token), else
+// 256 (several rows per CTA, four CTAs per SM).
+constexpr int kRmsMaxThreadsOneRow = 512;
+constexpr int kRmsMaxThreadsManyRows = 256;
+
 } // namespace q8

@@ -123,20 +123,14 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
         } else {
             float ss = 0.0f;
 #pragma unroll
-            for (int j = 0; j < J; ++j) {
-                ss = fmaf(v[j].x, v[j].x, ss);
-                ss = fmaf(v[j].y, v[j].y, ss);
-                ss = fmaf(v[j].z, v[j].z, ss);
-                ss = fmaf(v[j].w, v[j].w, ss);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(Q8_FULL_MASK, ss, o);
+            for (int j = 0; j < J; ++j) ss = q8::rms_sumsq4(ss, v[j]);
+            ss = q8::rms_warp_sum(ss);
             float *rb = red[it & 1];  // alternate buffers: one barrier per row suffices
             if (lane == 0) rb[tid >> 5] = ss;
             __syncthreads();
             float tot = 0.0f;
             for (int i = 0; i < nw; ++i) tot += rb[i];  // same fixed order in every thread
-            const float scale = rsqrtf(tot / static_cast<float>(d) + eps);
+            const float scale = q8::rms_scale(tot, d, eps);
             float4 *yr = reinterpret_cast<float4 *>(y + t * static_cast<int64_t>(d));
 #pragma unroll
             for (int j = 0; j < J; ++j) {
@@ -144,11 +138,7 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
                 const bool ok = f < F;  // uniform over each 8-lane block group
                 float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (ok) {
-                    const float4 wv = staged ? wsm[f] : __ldg(w4 + f);
-                    o.x = __fmul_rn(__fmul_rn(v[j].x, scale), wv.x);
-                    o.y = __fmul_rn(__fmul_rn(v[j].y, scale), wv.y);
-                    o.z = __fmul_rn(__fmul_rn(v[j].z, scale), wv.z);
-                    o.w = __fmul_rn(__fmul_rn(v[j].w, scale), wv.w);
+                    o = q8::rms_apply4(v[j], scale, staged ? wsm[f] : __ldg(w4 + f));
                     if (y) yr[f] = o;  // mode 2 (y == NULL): the f32 output is dead, only the plane is written
                 }
                 const q8::Q8Enc e = q8::q8_encode8(o);
@@ -168,15 +158,6 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
 // ("54 - r51 - producer-fused A-quantize mode 1", sec. 3.2), encoded from
 // registers into the plane in the same pass.
 // --------------------------------------------------------------------------
-// silu(g) * u with the hardware exp2 and reciprocal (a few ulp; the f32
-// result is what gets encoded, so the plane stays its exact q8_0 encoding).
-// For g < -87.3 the denominator exceeds 2^126 and the quotient is 0, where
-// the true value is below 1e-36.
-__device__ __forceinline__ float silu_mul(float g, float u)
-{
-    return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
-}
-
 __global__ void __launch_bounds__(kQuantThreads)
 swiglu_quant_kernel(const float4 *__restrict__ g, const float4 *__restrict__ u, float4 *__restrict__ y,
                     int64_t n4_valid, int64_t n4_total, uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
@@ -201,10 +182,7 @@ swiglu_quant_kernel(const float4 *__restrict__ g, const float4 *__restrict__ u, 
             const int64_t f = base + k * 32 + lane;
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
             if (f < n4_valid) {
-                o.x = silu_mul(gv[k].x, uv[k].x);
-                o.y = silu_mul(gv[k].y, uv[k].y);
-                o.z = silu_mul(gv[k].z, uv[k].z);
-                o.w = silu_mul(gv[k].w, uv[k].w);
+                o = q8::silu_mul4(gv[k], uv[k]);
                 if (y) y[f] = o;  // mode 2 (y == NULL): the f32 output is dead, only the plane is written
             }
             const q8::Q8Enc e = q8::q8_encode8(o);
@@ -264,10 +242,9 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     // float4 per thread: up to 256 threads per row when CTAs take several rows
     // (four CTAs per SM keep four rows in flight), up to 512 when every CTA
     // has at most one row (a decode token: shorter chains per thread)
-    const int max_p = rows_pad <= (sms > 0 ? sms : 152) ? 512 : 256;
-    int J = 1;
-    while (J < 16 && (F + J - 1) / J > max_p) J *= 2;
-    const int P = ((F + J - 1) / J + 31) / 32 * 32;
+    const int max_p = rows_pad <= (sms > 0 ? sms : 152) ? q8::kRmsMaxThreadsOneRow : q8::kRmsMaxThreadsManyRows;
+    int J, P;
+    q8::rms_row_mapping(F, max_p, J, P);
     // persistent grid: enough CTAs to fill the SMs (registers allow ~4 per SM
     // at these block sizes), each walking rows with a stride of the grid
     const int64_t per_sm = P <= 256 ? 4 : 2;

@@ -111,6 +111,24 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert lib.q4a_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 17, P(FAKE), s) == ERR_ARG
     assert lib.q4a_gemv_batched(P(0), 8, 256, P(FAKE), P(FAKE), 4, P(FAKE), s) == ERR_ARG
     assert lib.q4a_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 4, P(MISALIGNED), s) == ERR_ALIGN
+    # q8_0_gemv_fused: producer code, its inputs, the staged path's k, RMSNorm's row limit, alignment
+    one = (_binding.GemvProj * 1)(_binding.GemvProj(FAKE, 8, FAKE))
+    pr = ctypes.cast(one, ctypes.c_void_p)
+    fused = lib.q8_0_gemv_fused
+    assert fused(pr, 1, 256, 0, P(FAKE), P(0), P(0), 0.0, s) == ERR_ARG           # no producer 0
+    assert fused(pr, 1, 256, 4, P(FAKE), P(0), P(0), 0.0, s) == ERR_ARG           # nor 4
+    assert fused(pr, 0, 256, 1, P(FAKE), P(0), P(0), 0.0, s) == ERR_ARG           # count 0
+    assert fused(pr, 1, 256, 1, P(0), P(0), P(0), 0.0, s) == ERR_ARG              # x missing
+    assert fused(pr, 1, 256, 3, P(FAKE), P(0), P(0), 0.0, s) == ERR_ARG           # up missing
+    assert fused(pr, 1, 256, 2, P(FAKE), P(0), P(0), 1e-6, s) == ERR_ARG          # norm weight missing
+    assert fused(pr, 1, 2080, 1, P(FAKE), P(0), P(0), 0.0, s) == ERR_ARG          # 65 blocks per row
+    assert fused(pr, 1, 65536 + 256, 1, P(FAKE), P(0), P(0), 0.0, s) == ERR_ARG   # row longer than the staging
+    assert fused(pr, 1, 32768 + 256, 2, P(FAKE), P(0), P(FAKE), 1e-6, s) == ERR_ARG  # RMSNorm limit
+    assert fused(pr, 1, 256, 1, P(MISALIGNED), P(0), P(0), 0.0, s) == ERR_ALIGN
+    assert fused(pr, 1, 256, 3, P(FAKE), P(MISALIGNED), P(0), 0.0, s) == ERR_ALIGN
+    assert fused(pr, 1, 256, 2, P(FAKE), P(0), P(MISALIGNED), 1e-6, s) == ERR_ALIGN
+    bad = (_binding.GemvProj * 1)(_binding.GemvProj(FAKE + 8, 8, FAKE))
+    assert fused(ctypes.cast(bad, ctypes.c_void_p), 1, 256, 1, P(FAKE), P(0), P(0), 0.0, s) == ERR_ALIGN
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):

@@ -63,3 +63,26 @@ def test_grouped_and_layer_stack_accounts():
     head = L["vocab"] * _row_bytes(syn.q8_0_weights, L["d"])
     assert L["layers"] * w + head == 7_512_178_688  # every projection of the stack and the LM head
     assert 7_512_178_688 < bench.bytes_layer_stack() < 7_512_178_688 * 1.003  # + activations, planes, outputs
+
+
+def test_fused_accounts():
+    """A fused launch moves the weights, the outputs and the producer's f32
+    inputs once; no plane is written or read."""
+    f32 = np.dtype(np.float32).itemsize
+    k, ns = bench.SHARED["d"], bench.SHARED["ns"]
+    weights_out = sum(n * _row_bytes(syn.q8_0_weights, k) + 4 * n for n in ns)
+    assert bench.bytes_gemv_fused(k, ns, "rmsnorm") == weights_out + 2 * k * f32   # x and the norm weight
+    assert bench.bytes_gemv_fused(k, ns, "quant") == weights_out + k * f32
+    assert bench.bytes_gemv_fused(k, ns, "swiglu") == weights_out + 2 * k * f32    # gate and up
+    assert bench.bytes_shared(fused=True) == bench.bytes_shared() - bench.bytes_rmsnorm_quant(1, k, False) \
+        - _plane_row_bytes(k) + 2 * k * f32
+    L = bench.LAYERS
+    d, nf = L["d"], L["nf"]
+    # per layer: 2 RMSNorm inputs (x, w), the attention output, gate + up; the final norm's x and w
+    inputs = L["layers"] * (2 * 2 * d + d + 2 * nf) * f32 + 2 * d * f32
+    outputs = (L["layers"] * sum(n for _, group in bench.layer_groups() for n in group) + L["vocab"]) * f32
+    every = ("qkv", "o", "gu", "down", "head")
+    assert bench.bytes_layer_stack(every) == 7_512_178_688 + inputs + outputs
+    # fusing one producer removes its plane write and read and its mode-2 bytes, adds nothing else
+    one = bench.bytes_layer_stack() - bench.bytes_layer_stack(("qkv",))
+    assert one == L["layers"] * (bench.bytes_rmsnorm_quant(1, d, False) + _plane_row_bytes(d) - 2 * d * f32)

@@ -1,0 +1,121 @@
+"""GPU parity of q8_0_gemv_fused: the one-row producer computed inside the
+GEMV's activation staging ("Part 4 - Lecture 05", sec. 4: producer and
+consumer in one launch, one implementation for both paths).
+
+Every output must equal, bit for bit, the two-launch path it replaces: the
+standalone producer on one row (rows_pad = q8_plane_rows(1)) followed by
+q8_0_gemv_grouped on its plane.  That path is itself pinned to the oracle
+(the producers' planes bit-exact, the GEMV within its tolerance); here the
+fused outputs are also compared with the oracle's GEMV of the oracle's
+encoding of the producer's f32 row.  Shapes cover one and several
+projections, CTAs with few warps (small n: the RMSNorm sum of squares is
+then replayed by fewer warps than the standalone kernel has), rows of one
+and of several 32-chunk pieces, and the largest k of each producer.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from int8_quantized_projection_gb300 import synthetic as syn
+
+from ._parity import assert_gemm_close, dev, host, nan_f32
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # (k, ns)
+    (256, (64,)),
+    (3584, (3584, 512, 512)),
+    (3584, (37,)),
+    (7168, (3072, 512, 512, 3072)),
+    (7168, (96,)),
+    (18944, (3584,)),
+    (32768, (1000, 8)),
+]
+
+
+def _weights(seed, n, k):
+    return syn.q8_0_weights(syn.rng(70, seed, n, k), n, k)[0]
+
+
+def _inputs(producer, k, seed):
+    g = syn.rng(71, seed, producer, k)
+    a = syn.activations(g, 1, k, sigma=1.5, outlier_frac=0.01)[0]
+    b = syn.activations(g, 1, k)[0] if producer == 3 else None
+    w = syn.uniform(g, k, 0.5, 1.5) if producer == 2 else None
+    return a, b, w
+
+
+def _two_launch(q8, producer, k, a, b, w, eps, projs):
+    """The standalone producer (mode 1, one row) and the grouped GEMV on its plane."""
+    rp = q8.q8_plane_rows(1)
+    qs, ds = q8.empty_plane(rp, k)
+    yf = nan_f32(1, k)
+    if producer == q8.PRODUCER_QUANT:
+        q8.quantize_q8_0(a.view(1, k), qs, ds)
+        yf = a.view(1, k)
+    elif producer == q8.PRODUCER_RMSNORM:
+        q8.rmsnorm_quant(a.view(1, k), w, eps, yf, qs, ds)
+    else:
+        q8.swiglu_quant(a.view(1, k), b.view(1, k), yf, qs, ds)
+    q8.q8_0_gemv_grouped(projs, k, qs, ds)
+    q8.q8_check()
+    return yf
+
+
+@pytest.mark.parametrize("producer", [1, 2, 3])
+@pytest.mark.parametrize("k,ns", CASES)
+def test_fused_equals_two_launches_and_oracle(q8, producer, k, ns):
+    import torch
+
+    if producer == 2 and k > 32768:
+        pytest.skip("RMSNorm rows are limited to 32768")
+    a_h, b_h, w_h = _inputs(producer, k, len(ns))
+    a, b, w = dev(a_h), (dev(b_h) if b_h is not None else None), (dev(w_h) if w_h is not None else None)
+    eps = 1e-6
+    blobs = [_weights(i, n, k) for i, n in enumerate(ns)]
+    wd = [dev(bl) for bl in blobs]
+    yf_fused = [nan_f32(n) for n in ns]
+    q8.q8_0_gemv_fused([(x, n, y) for x, n, y in zip(wd, ns, yf_fused)], k, producer, a, b, w, eps)
+    q8.q8_check()
+    y_two = [nan_f32(n) for n in ns]
+    row = _two_launch(q8, producer, k, a, b, w, eps, [(x, n, y) for x, n, y in zip(wd, ns, y_two)])
+    qs_r, ds_r = oracle.quantize(host(row).reshape(1, k), 1)
+    for blob, n, yf, yt in zip(blobs, ns, yf_fused, y_two):
+        assert torch.equal(yf, yt), f"producer {producer} {n}x{k}: fused != two launches"
+        yr, ar = oracle.gemv(blob, n, k, qs_r, ds_r)
+        assert_gemm_close(host(yf), yr, ar, f"fused producer {producer} {n}x{k}")
+
+
+def test_fused_rmsnorm_zero_row(q8):
+    """An all-zero row: the scale is rsqrt(eps), every code and d is 0, every output exactly 0."""
+    k, n = 3584, 300
+    blob = _weights(5, n, k)
+    y = nan_f32(n)
+    import torch
+
+    x = torch.zeros(k, dtype=torch.float32, device="cuda")
+    w = torch.ones(k, dtype=torch.float32, device="cuda")
+    q8.q8_0_gemv_fused([(dev(blob), n, y)], k, q8.PRODUCER_RMSNORM, x, None, w, 1e-6)
+    q8.q8_check()
+    assert (host(y) == 0).all()
+
+
+def test_fused_rejects_unsupported(q8):
+    import torch
+
+    k = 2080  # 65 blocks: not a multiple of 8 blocks (the staged path only)
+    w = torch.zeros(34 * (k // 32), dtype=torch.uint8, device="cuda")
+    y = torch.zeros(1, dtype=torch.float32, device="cuda")
+    x = torch.zeros(k, dtype=torch.float32, device="cuda")
+    with pytest.raises(q8.Q8Error):
+        q8.q8_0_gemv_fused([(w, 1, y)], k, q8.PRODUCER_QUANT, x)
+    k = 256
+    w = torch.zeros(34 * (k // 32), dtype=torch.uint8, device="cuda")
+    x = torch.zeros(k, dtype=torch.float32, device="cuda")
+    with pytest.raises(q8.Q8Error):
+        q8.q8_0_gemv_fused([(w, 1, y)], k, 4, x)          # no such producer
+    with pytest.raises(q8.Q8Error):
+        q8.q8_0_gemv_fused([(w, 1, y)], k, q8.PRODUCER_SWIGLU, x)   # up missing
+    with pytest.raises(q8.Q8Error):
+        q8.q8_0_gemv_fused([(w, 1, y)], k, q8.PRODUCER_RMSNORM, x)  # weight missing
