@@ -44,10 +44,10 @@ PREFILL = dict(tokens=3325, d=3584, nf=18944, eps=1e-6)
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of a kernel, from
 # the ncu capture summarised under profiles/; None until taken, and reset to
 # None whenever that kernel changes (the figure would describe old code).
-NCU_TRAFFIC_BYTES = {"gemv_staged 12288x7168+96x7168": 97_571_840,     # profiles/gemv_staged_12288x7168_plus_96x7168.md
+NCU_TRAFFIC_BYTES = {"gemv_fused 12288x7168+96x7168": 97_617_920,      # profiles/gemv_fused_quant_12288x7168_plus_96x7168.md
                      "gemm_tc 18944x3584 t=3325": 397_260_544,         # profiles/gemm_tc_18944x3584_t3325.md
                      "gemv_small 12288x7168 t=16": 97_903_616,         # profiles/gemv_small_12288x7168_t16.md
-                     "gemv_staged_q4a 12288x7168": 55_086_848}         # profiles/gemv_staged_q4a_12288x7168.md
+                     "gemv_staged_q4a 12288x7168": 55_095_552}         # profiles/gemv_staged_q4a_12288x7168.md
 
 
 # ---------------------------------------------------------------------------
@@ -193,8 +193,14 @@ def decode_inputs():
     return xs, ws
 
 
-def decode_bytes():
-    return (bytes_quantize(1, 7168) + bytes_quantize(1, 128) + sum(bytes_gemv(n, k) for n, k in DECODE_SHAPES))
+def decode_bytes(fused=False):
+    """Algorithmic bytes of one decode step.  fused: the k = 7168 activation is
+    quantized inside the grouped GEMV (q8_0_gemv_fused), so it is read once as
+    f32 and no plane is written or read; the k = 128 chain is unchanged."""
+    side = bytes_quantize(1, 128) + bytes_gemv(*DECODE_SHAPES[2])
+    if fused:
+        return bytes_gemv_fused(7168, [DECODE_SHAPES[0][0], DECODE_SHAPES[1][0]], "quant") + side
+    return bytes_quantize(1, 7168) + sum(bytes_gemv(n, k) for n, k in DECODE_SHAPES[:2]) + side
 
 
 def run_decode(torch, q8p, steps, warmup, dev, sampler):
@@ -213,21 +219,25 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
 
     # every launch pre-marshalled once (one ctypes call per launch in the loop)
     # The two k = 7168 projections share one activation: one grouped launch
-    # ("Part 4 - Lecture 05", sec. 2.5); the k = 128 one uses its own plane.
-    quant = [q8p.quantize_q8_0(xs[k], *planes[k], bind=True) for k in (7168, 128)]
-    gemvs = [[q8p.q8_0_gemv_grouped([(wset[0], DECODE_SHAPES[0][0], ys[0]), (wset[1], DECODE_SHAPES[1][0], ys[1])],
-                                    7168, *planes[7168], bind=True),
-              q8p.q8_0_gemv(wset[2], *DECODE_SHAPES[2], *planes[128], ys[2], bind=True)] for wset in ws]
+    # ("Part 4 - Lecture 05", sec. 2.5) that also quantizes it (sec. 4: producer
+    # and consumer in one launch); the k = 128 one (4 blocks per row, not a
+    # staged shape) has its own quantize and plane.
+    def main_call(wset, stream_=None):
+        return q8p.q8_0_gemv_fused([(wset[0], DECODE_SHAPES[0][0], ys[0]), (wset[1], DECODE_SHAPES[1][0], ys[1])],
+                                   7168, q8p.PRODUCER_QUANT, xs[7168][0], stream=stream_, bind=True)
+
+    quant128 = q8p.quantize_q8_0(xs[128], *planes[128], bind=True)
+    gemvs = [[main_call(wset), q8p.q8_0_gemv(wset[2], *DECODE_SHAPES[2], *planes[128], ys[2], bind=True)]
+             for wset in ws]
 
     def step(i, ev=None):
-        for qz in quant:
-            qz()
         g = gemvs[i % copies]
         if ev is not None:
             ev[0].record(stream)
         g[0]()
         if ev is not None:
             ev[1].record(stream)
+        quant128()
         g[1]()
 
     for i in range(warmup):
@@ -244,26 +254,35 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     # CTAs sit beside the grouped GEMV's one CTA per SM instead of adding two
     # launch latencies to every step.
     cap, side = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    quant_main = q8p.quantize_q8_0(xs[7168], *planes[7168], stream=cap, bind=True)
     quant_side = q8p.quantize_q8_0(xs[128], *planes[128], stream=side, bind=True)
-    gemvs_c = [[q8p.q8_0_gemv_grouped([(wset[0], DECODE_SHAPES[0][0], ys[0]), (wset[1], DECODE_SHAPES[1][0], ys[1])],
-                                      7168, *planes[7168], stream=cap, bind=True),
+    gemvs_c = [[main_call(wset, cap),
                 q8p.q8_0_gemv(wset[2], *DECODE_SHAPES[2], *planes[128], ys[2], stream=side, bind=True)] for wset in ws]
+    # the same step with the k = 7168 quantize as its own launch (for comparison)
+    quant_main = q8p.quantize_q8_0(xs[7168], *planes[7168], stream=cap, bind=True)
+    grouped_c = [q8p.q8_0_gemv_grouped([(wset[0], DECODE_SHAPES[0][0], ys[0]), (wset[1], DECODE_SHAPES[1][0], ys[1])],
+                                       7168, *planes[7168], stream=cap, bind=True) for wset in ws]
 
-    def steps_c():
+    def steps_c(fused=True):
         side.wait_stream(cap)  # fork
         for i in range(copies):
-            quant_main()
-            gemvs_c[i][0]()
+            if fused:
+                gemvs_c[i][0]()
+            else:
+                quant_main()
+                grouped_c[i]()
             quant_side()
             gemvs_c[i][1]()
         cap.wait_stream(side)  # join
 
     cap.wait_stream(stream)
     steps_c()  # the same launches once outside the capture
+    steps_c(False)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=cap):
         steps_c()
+    graph_two = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_two, stream=cap):
+        steps_c(False)
     stream.wait_stream(cap)
     reps, rem = divmod(steps, copies)
 
@@ -282,6 +301,15 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     clocks = sampler.stop()
     q8p.q8_check()
     ms = t0.elapsed_time(t1)
+    for _ in range(3):
+        graph_two.replay()
+    t0.record(stream)
+    for _ in range(reps):
+        graph_two.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    q8p.q8_check()
+    ms_two = t0.elapsed_time(t1) / (reps * copies) if reps else float("nan")
     # The roofline's kernel duration: the same K steps again, with events
     # around every launch of the big GEMV (each launch then runs unoverlapped).
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
@@ -307,7 +335,6 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     def e2e_body(i, par):  # on the capture streams: the inputs in, one step, the outputs out
         x_all.copy_(xh[par], non_blocking=True)
         side.wait_stream(cap)
-        quant_main()
         gemvs_c[i][0]()
         quant_side()
         gemvs_c[i][1]()
@@ -363,7 +390,7 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
         q8p.q8_check()
     e2e_s, e2e_serial_s, e2e_eager_s = res["e2e_s"], res["e2e_serial_s"], res["e2e_eager_s"]
     return dict(ms=ms, kern_ms=kern_ms, clocks=clocks, e2e_s=e2e_s, e2e_serial_s=e2e_serial_s, e2e_eager_s=e2e_eager_s,
-                copies=copies,
+                copies=copies, ms_two=ms_two,
                 h2d=sum(v.nbytes for v in xs_h.values()), d2h=4 * sum(n for n, _ in DECODE_SHAPES))
 
 
@@ -772,7 +799,9 @@ def reference_arm(args):
 
 
 def decode_config(copies):
-    return {"workload": "decode GEMV sweep b=1: q8_0 quantize + Q8_0 GEMV (n,k) in {(12288,7168),(96,7168),(512,128)}",
+    return {"workload": "decode GEMV sweep b=1: q8_0 quantize + Q8_0 GEMV (n,k) in {(12288,7168),(96,7168),(512,128)}; "
+                        "the k = 7168 pair in one q8_0_gemv_fused launch (quantize inside), the k = 128 chain "
+                        "(quantize_q8_0 -> q8_0_gemv) on a parallel graph branch",
             "activation": "f32 ~N(0,1.5), 1% outliers x20, seed 1", "weights": "Q8_0, d~U(0.002,0.02), q~U{-127..127}",
             "l2": (f"weights rotate through {copies} copies ({copies} x 94.4 MB > 4 x L2)" if copies else "n/a (CPU)"),
             "launch": ("timed steps replayed from a CUDA graph of one step per weight copy" if copies
@@ -853,15 +882,16 @@ def main():
                          args.warmup, dev)
 
     if world > 1:  # every duration becomes the slowest rank's (same legs on every rank)
-        vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"]] if dec else [])
+        vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"]]
+                 if dec else [])
                 + (list(pre.values()) if pre else [])
                 + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else [])
                 + ([lay["ms"], lay["ms_two"], lay["ms_fused"]] if lay else [])
                 + ([shr["us"], shr["us_two"]] if shr else []))
         red = max_over_ranks(torch, vals, dev)
         if dec:
-            dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"] = red[:5]
-            red = red[5:]
+            dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"] = red[:6]
+            red = red[6:]
         if pre:
             pre = dict(zip(pre.keys(), red[:len(pre)]))
             red = red[len(pre):]
@@ -884,18 +914,21 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic"}
     if dec is not None:
         ms = dec["ms"]
-        step_bytes = decode_bytes()
+        step_bytes = decode_bytes(fused=True)
         value = world * step_bytes * args.steps / (ms / 1e3) / 1e9
-        big = bytes_gemv(*DECODE_SHAPES[0]) + bytes_gemv(*DECODE_SHAPES[1]) - 7168 - 4 * 224
+        big = bytes_gemv_fused(7168, [DECODE_SHAPES[0][0], DECODE_SHAPES[1][0]], "quant")
         achieved = big / (dec["kern_ms"] / 1e3) / 1e9
         line.update({
             "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms / args.steps, 5),
             "config": decode_config(dec["copies"]),
-            "roofline": {"kernel": "q8_0_gemv_grouped 12288x7168 + 96x7168 (gemv_staged_kernel)", "bound": "hbm",
-                         "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "roofline": {"kernel": "q8_0_gemv_fused 12288x7168 + 96x7168, quantize inside (gemv_staged_kernel)",
+                         "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-                         "traffic": NCU_TRAFFIC_BYTES["gemv_staged 12288x7168+96x7168"],
+                         "traffic": NCU_TRAFFIC_BYTES["gemv_fused 12288x7168+96x7168"],
                          "algorithmic_bytes": big, "avg_launch_us": round(dec["kern_ms"] * 1e3, 3)},
+            "two_launch": {"calls": "quantize_q8_0 (k = 7168) -> q8_0_gemv_grouped, the k = 128 chain unchanged",
+                           "ms_per_step": round(dec["ms_two"], 5),
+                           "gbs": round(world * decode_bytes() / (dec["ms_two"] / 1e3) / 1e9, 2)},
             "cpu_baseline": cpu,
             "e2e": {"value": round(world * step_bytes * args.steps / dec["e2e_s"] / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"],
@@ -905,7 +938,7 @@ def main():
                     "serial_value": round(world * step_bytes * args.steps / dec["e2e_serial_s"] / 1e9, 2),
                     "eager_value": round(world * step_bytes * args.steps / dec["e2e_eager_s"] / 1e9, 2)},
             "clocks": dec["clocks"],
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,
         })
     if pre is not None:
         T, d, nf = PREFILL["tokens"], PREFILL["d"], PREFILL["nf"]

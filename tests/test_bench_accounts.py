@@ -86,3 +86,9 @@ def test_fused_accounts():
     # fusing one producer removes its plane write and read and its mode-2 bytes, adds nothing else
     one = bench.bytes_layer_stack() - bench.bytes_layer_stack(("qkv",))
     assert one == L["layers"] * (bench.bytes_rmsnorm_quant(1, d, False) + _plane_row_bytes(d) - 2 * d * f32)
+
+
+def test_fused_decode_accounts():
+    """The decode step with its k = 7168 quantize inside the grouped GEMV: the plane's write and its reads by the two
+    projections (counted per projection in the unfused step) are gone, the f32 activation is read once."""
+    assert bench.decode_bytes() - bench.decode_bytes(fused=True) == 3 * _plane_row_bytes(7168)
