@@ -197,18 +197,26 @@ __device__ __forceinline__ float FmtQ8_0::dot(const uint8_t *wc, const uint8_t *
 // and every thread adds them in warp order.
 __device__ __forceinline__ void stage_produced(const GvGeom &g, uint8_t *act, float *red, int warp, int lane)
 {
+    constexpr int kBatch = 4;  // loads a thread keeps in flight before it uses them
     const int nwarps = static_cast<int>(blockDim.x >> 5);
     const int F = g.nc * 32;  // float4 per row
     const GvAct &A = g.act;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
     float scale = 0.0f;
     if (A.producer == Q8_PRODUCER_RMSNORM) {
         const int vws = A.rms_p >> 5;
         for (int vw = warp; vw < vws; vw += nwarps) {
             const int vt = vw * 32 + lane;
             float ss = 0.0f;
-            for (int j = 0; j < A.rms_j; ++j) {
-                const int f = vt + j * A.rms_p;
-                ss = q8::rms_sumsq4(ss, f < F ? __ldg(A.a + f) : make_float4(0.f, 0.f, 0.f, 0.f));
+            for (int j0 = 0; j0 < A.rms_j; j0 += kBatch) {
+                float4 v[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int f = vt + (j0 + u) * A.rms_p;
+                    v[u] = (j0 + u < A.rms_j && f < F) ? __ldg(A.a + f) : zero;
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) ss = q8::rms_sumsq4(ss, v[u]);  // zeros leave ss as it is
             }
             ss = q8::rms_warp_sum(ss);
             if (lane == 0) red[vw] = ss;
@@ -218,19 +226,33 @@ __device__ __forceinline__ void stage_produced(const GvGeom &g, uint8_t *act, fl
         for (int i = 0; i < vws; ++i) tot += red[i];
         scale = q8::rms_scale(tot, F * 4, A.eps);
     }
-    for (int c = warp; c < g.nc; c += nwarps) {
-        const int f = c * 32 + lane;
-        float4 o;
-        if (A.producer == Q8_PRODUCER_RMSNORM)
-            o = q8::rms_apply4(__ldg(A.a + f), scale, __ldg(A.w + f));
-        else if (A.producer == Q8_PRODUCER_SWIGLU)
-            o = q8::silu_mul4(__ldg(A.a + f), __ldg(A.b + f));
-        else
-            o = __ldg(A.a + f);
-        const q8::Q8Enc e = q8::q8_encode8(o);
-        uint8_t *ch = act + c * kActChunkBytes;
-        reinterpret_cast<uint32_t *>(ch)[lane] = e.qword;
-        if ((lane & 7) == 0) reinterpret_cast<uint32_t *>(ch + 128)[lane >> 3] = e.dsword;
+    for (int c0 = warp; c0 < g.nc; c0 += nwarps * kBatch) {
+        float4 p[kBatch], q[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int c = c0 + u * nwarps, f = c * 32 + lane;
+            const bool ok = c < g.nc;
+            p[u] = ok ? __ldg(A.a + f) : zero;
+            q[u] = (ok && A.producer != Q8_PRODUCER_QUANT)
+                       ? __ldg((A.producer == Q8_PRODUCER_RMSNORM ? A.w : A.b) + f)
+                       : zero;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int c = c0 + u * nwarps;
+            if (c >= g.nc) break;  // uniform over the warp
+            float4 o;
+            if (A.producer == Q8_PRODUCER_RMSNORM)
+                o = q8::rms_apply4(p[u], scale, q[u]);
+            else if (A.producer == Q8_PRODUCER_SWIGLU)
+                o = q8::silu_mul4(p[u], q[u]);
+            else
+                o = p[u];
+            const q8::Q8Enc e = q8::q8_encode8(o);
+            uint8_t *ch = act + c * kActChunkBytes;
+            reinterpret_cast<uint32_t *>(ch)[lane] = e.qword;
+            if ((lane & 7) == 0) reinterpret_cast<uint32_t *>(ch + 128)[lane >> 3] = e.dsword;
+        }
     }
 }
 
