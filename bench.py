@@ -598,12 +598,14 @@ def run_shared(torch, q8p, steps, warmup, dev):
 # LM head for one token (batch 1), recorded as one CUDA graph
 # ---------------------------------------------------------------------------
 LAYERS = dict(layers=28, d=3584, nf=18944, q=3584, kv=512, vocab=152064, eps=1e-6)
-# Producers computed inside their consumer's launch (q8_0_gemv_fused) in the
-# layer stack's headline figure: the set that measured fastest in the chain
-# (RMSNorm -> q/k/v, quantize -> o, the final RMSNorm -> LM head).  Fusing
-# SwiGLU -> down is slower (every CTA recomputes the 18944-wide row), and so,
-# in the chain, is RMSNorm -> gate/up.
-LAYER_FUSED = ("qkv", "o", "head")
+# The layer stack's headline launch plan, the set that measured fastest in
+# the chain: RMSNorm -> q/k/v, quantize -> o and the final RMSNorm -> LM head
+# inside their GEMV launch (q8_0_gemv_fused), and gate/up as one
+# q8_0_gemv_gate_up launch on rmsnorm_quant's plane whose epilogue writes the
+# SwiGLU output's plane for down ("gu_pair").  Fusing SwiGLU into down instead
+# is slower (every CTA recomputes the 18944-wide row), and so, in the chain,
+# is RMSNorm inside the gate/up launch.
+LAYER_FUSED = ("qkv", "o", "gu_pair", "head")
 
 
 def layer_groups():
@@ -639,7 +641,14 @@ def bytes_layer_stack(fused=()):
         prod = {"rmsnorm": bytes_rmsnorm_quant(1, k, False), "quant": bytes_quantize(1, k),
                 "swiglu": bytes_swiglu_quant(1, k, False)}[producer]
         return prod + bytes_gemv_group(k, ns)
-    per_layer = sum(one(*st) for st in steps)
+    if "gu_pair" in fused:  # gate/up on the norm's plane, writing the SwiGLU plane; down reads it
+        plane = lambda k: k + 4 * (k // 32)  # noqa: E731
+        pair = (bytes_rmsnorm_quant(1, d, False) + sum(n * (d // 32) * 34 for n in gu) + plane(d) + plane(nf)
+                + bytes_gemv(down[0], nf))
+        steps = steps[:2]
+    else:
+        pair = 0
+    per_layer = sum(one(*st) for st in steps) + pair
     return L["layers"] * per_layer + one("head", d, [L["vocab"]], "rmsnorm")
 
 
@@ -676,7 +685,8 @@ def run_layers(torch, q8p, steps, warmup, dev):
 
     def token(fuse):
         """One token's launches; `fuse` = the producers computed inside their
-        consumer's launch, of {"qkv", "o", "gu", "down", "head"}."""
+        consumer's launch, of {"qkv", "o", "gu", "down", "head"}, or "gu_pair"
+        (gate/up with the SwiGLU plane written by its epilogue)."""
         c = []
         for wq, wk, wv, wo, wg, wu, wd in layers:
             qkv = [(wq, L["q"], ys[0]), (wk, L["kv"], ys[1]), (wv, L["kv"], ys[2])]
@@ -687,6 +697,11 @@ def run_layers(torch, q8p, steps, warmup, dev):
             c += ([q8p.q8_0_gemv_fused([(wo, d, ys[3])], d, P_Q, attn[0], stream=cap, bind=True)] if "o" in fuse
                   else [q8p.quantize_q8_0(attn, *pd, stream=cap, bind=True),
                         q8p.q8_0_gemv(wo, d, d, *pd, ys[3], stream=cap, bind=True)])
+            if "gu_pair" in fuse:  # SwiGLU + quantize in the gate/up launch's epilogue, down on its plane
+                c += [q8p.rmsnorm_quant(h, nw2, eps, None, *pd, stream=cap, bind=True),
+                      q8p.q8_0_gemv_gate_up(wg, wu, nf, d, *pf, qs=pd[0], ds=pd[1], stream=cap, bind=True),
+                      q8p.q8_0_gemv(wd, d, nf, *pf, ys[6], stream=cap, bind=True)]
+                continue
             c += ([q8p.q8_0_gemv_fused(gu, d, P_R, h[0], None, nw2, eps, stream=cap, bind=True)] if "gu" in fuse
                   else [q8p.rmsnorm_quant(h, nw2, eps, None, *pd, stream=cap, bind=True),
                         q8p.q8_0_gemv_grouped(gu, d, *pd, stream=cap, bind=True)])
@@ -1034,9 +1049,9 @@ def main():
         byts2, byts3 = bytes_layer_stack(), bytes_layer_stack(("qkv", "o", "gu", "down", "head"))
         lobj = {"workload": f"layer-stack decode b=1: {L['layers']} layers (d={L['d']}, nf={L['nf']}; q {L['q']}, "
                             f"k/v {L['kv']}, o, gate/up, down) + LM head {L['vocab']}x{L['d']}; per layer RMSNorm "
-                            "-> grouped q/k/v, quantize -> o, RMSNorm -> grouped gate/up, SwiGLU -> down; producers "
-                            f"fused into their GEMV launch (q8_0_gemv_fused): {', '.join(LAYER_FUSED)}; the others "
-                            "as their own launches in mode 2",
+                            "-> grouped q/k/v and quantize -> o inside their GEMV launch (q8_0_gemv_fused), "
+                            "rmsnorm_quant -> gate/up with SwiGLU + quantize in its epilogue (q8_0_gemv_gate_up) -> "
+                            "down on that plane; the final RMSNorm inside the LM head's launch",
                 "ms_per_token": round(lay["ms"], 4), "tokens_per_s": round(1e3 / lay["ms"], 1),
                 "gbs": round(gbs, 1), "algorithmic_bytes": byts, "weight_bytes": lay["weight_bytes"],
                 "launches_per_token": lay["launches"],

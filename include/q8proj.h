@@ -196,6 +196,39 @@ Q8_API int q8_0_gemv_fused(const q8_gemv_proj *projs, int count, int64_t k, int 
                            void *stream);
 
 /*
+ * q8_0_gemv_gate_up -- the gate and up projections of one token with SwiGLU
+ * and its q8_0 encoding in the same launch: gate = Wg.x, up = Wu.x (x from
+ * plane row 0 of (qs, ds), or produced in the launch as for q8_0_gemv_fused),
+ * and the plane row of silu(gate) * up written straight to (qs_out, ds_out)
+ * -- the input of the down projection -- with no f32 SwiGLU output and no
+ * separate SwiGLU launch.  Row r of gate and row r of up are computed by the
+ * same CTA; the warp that completes the 32 rows of a block encodes it.
+ *   w_gate, w_up : nf rows of k/32 Q8_0 blocks each (inputs)
+ *   qs, ds       : activation plane row 0 when producer == 0, else unused
+ *   producer     : 0, Q8_PRODUCER_QUANT (a = x) or Q8_PRODUCER_RMSNORM
+ *                  (a = x, norm_w, eps), as for q8_0_gemv_fused
+ *   y_gate, y_up : f32 [nf] outputs, or NULL when not wanted
+ *   qs_out       : int8 [nf], ds_out : uint32 [nf/32] -- one plane row (row 0
+ *                  of a plane; other rows are not touched)
+ * Result: y_gate / y_up bit for bit as q8_0_gemv_grouped (or _fused) writes
+ * them, and the plane bit for bit as swiglu_quant writes it for those values
+ * (the same SwiGLU and encoding arithmetic).
+ * Requires nf % 32 == 0, (k/32) % 8 == 0, 2048 < k <= 65536 (whole rows per
+ * warp on the staged path), k <= 32768 for RMSNorm; otherwise Q8_ERR_ARG.
+ * Pointers 16-byte aligned (Q8_ERR_ALIGN).  The same programmatic-dependent-
+ * launch rule as q8_0_gemv; outputs must not overlap inputs.
+ * "54 - r51 - producer-fused A-quantize mode 1", sec. 3.2 (swiglu_quant_f32_t:
+ * SwiGLU and the quantize of its output in one pass) and sec. 6 (consume the
+ * data where it is hottest: here the registers of the gate/up GEMV); "Part 4 -
+ * Lecture 05", sec. 4 (one launch instead of a buffer passed between two).
+ */
+Q8_API int q8_0_gemv_gate_up(const void *w_gate, const void *w_up, int64_t nf, int64_t k,
+                             const int8_t *qs, const uint32_t *ds,
+                             int producer, const float *a, const float *norm_w, float eps,
+                             float *y_gate, float *y_up, int8_t *qs_out, uint32_t *ds_out,
+                             void *stream);
+
+/*
  * q8_0_gemv_batched -- the projection for a few tokens at once (decode over
  * a small batch of sequences): Y[t][i] = sum_b d_w(i,b) * d_a(t,b) * isum for
  * plane rows t < tokens, reading the weights from memory once for all of

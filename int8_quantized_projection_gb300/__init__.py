@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     q8_0_gemv,
     q8_0_gemv_grouped,
     q8_0_gemv_fused,
+    q8_0_gemv_gate_up,
     q8_0_gemv_batched,
     PRODUCER_QUANT,
     PRODUCER_RMSNORM,

@@ -38,6 +38,7 @@ SIGNATURES = {
     "q8_0_gemm_noalloc_max_bytes": (ctypes.c_size_t, []),
     "q8_0_gemv_grouped": (_INT, [_P, _INT, _I64, _P, _P, _P]),
     "q8_0_gemv_fused": (_INT, [_P, _INT, _I64, _INT, _P, _P, _P, ctypes.c_float, _P]),
+    "q8_0_gemv_gate_up": (_INT, [_P, _P, _I64, _I64, _P, _P, _INT, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P]),
     "q8_0_gemv_batched": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P]),
     "q4a_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q4a_gemv_batched": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P]),
@@ -308,6 +309,34 @@ def q8_0_gemv_fused(projs, k: int, producer: int, a, b=None, norm_w=None, eps: f
         return bd
     _check("q8_0_gemv_fused", lib().q8_0_gemv_fused(*args))
     return None
+
+
+def q8_0_gemv_gate_up(w_gate, w_up, nf: int, k: int, qs_out, ds_out, qs=None, ds=None, producer: int = 0, a=None,
+                      norm_w=None, eps: float = 0.0, y_gate=None, y_up=None, stream=None, bind=False):
+    """Gate and up projections of one token with SwiGLU + q8_0 quantize in the same launch.
+
+    The activation is plane row 0 of (qs, ds) when ``producer`` is 0, else
+    produced in the launch (PRODUCER_QUANT: a = x; PRODUCER_RMSNORM: a = x,
+    norm_w, eps).  Writes plane row 0 of silu(gate) * up into (qs_out,
+    ds_out); y_gate / y_up (f32 [nf]) are optional."""
+    import torch
+
+    _need(w_gate, torch.uint8, "w_gate"), _need(w_up, torch.uint8, "w_up")
+    _need(qs_out, torch.int8, "qs_out"), _need(ds_out, torch.int32, "ds_out")
+    if w_gate.numel() != nf * (k // 32) * 34 or w_up.numel() != w_gate.numel():
+        raise ValueError("weight shape mismatch")
+    if qs_out.shape[-1] != nf or ds_out.shape[-1] != nf // 32:
+        raise ValueError("output plane shape mismatch")
+    for t, nm, dt in ((qs, "qs", torch.int8), (ds, "ds", torch.int32), (a, "a", torch.float32),
+                      (norm_w, "norm_w", torch.float32), (y_gate, "y_gate", torch.float32),
+                      (y_up, "y_up", torch.float32)):
+        if t is not None:
+            _need(t, dt, nm)
+    nul = ctypes.c_void_p(0)
+    opt = lambda t: _ptr(t) if t is not None else nul  # noqa: E731
+    args = (_ptr(w_gate), _ptr(w_up), nf, k, opt(qs), opt(ds), int(producer), opt(a), opt(norm_w), float(eps),
+            opt(y_gate), opt(y_up), _ptr(qs_out), _ptr(ds_out), _stream(stream))
+    return _launch("q8_0_gemv_gate_up", args, bind)
 
 
 def q8_0_gemm_workspace_bytes(n: int, t: int, k: int) -> int:

@@ -73,7 +73,17 @@ struct GvGeom {
     int rpw;         // rows per piece (1: a piece is up to 32*J chunks of one row)
     int ppr;         // pieces per row group
     int64_t groups;  // total row groups over all projections
+    // SwiGLU pairing (q8_0_gemv_gate_up): projections 0 (gate) and 1 (up) of
+    // equal n, one row per group.  Groups are interleaved in units of 32 gate
+    // rows then the same 32 up rows, each CTA owns whole units, and the warp
+    // that completes a unit writes the q8_0 block of silu(gate) * up.
+    int pair_upc;       // 0: off; else the most units a CTA owns (sizes its buffer)
+    int8_t *pair_qs;    // the SwiGLU output's plane row 0: n codes
+    uint32_t *pair_ds;  // and its n/32 d|ssum words
 };
+
+// Shared bytes of the pairing buffer: per unit 64 f32 results and a counter.
+__host__ __device__ inline int pair_region_bytes(int upc) { return upc ? (upc * (64 * 4 + 4) + 127) & ~127 : 0; }
 
 // global row group -> projection index
 __device__ __forceinline__ int proj_of(const GvGeom &g, int64_t G)
@@ -83,6 +93,19 @@ __device__ __forceinline__ int proj_of(const GvGeom &g, int64_t G)
     for (int i = 1; i < kMaxProj; ++i)
         if (i < g.count && G >= g.p[i].g_begin) j = i;
     return j;
+}
+
+// global row group -> (projection, row group within it)
+__device__ __forceinline__ void locate(const GvGeom &g, int64_t G, int &pi, int64_t &Gl)
+{
+    if (g.pair_upc) {
+        const int w = static_cast<int>(G & 63);
+        pi = w >> 5;
+        Gl = (G >> 6) * 32 + (w & 31);
+        return;
+    }
+    pi = proj_of(g, G);
+    Gl = G - g.p[pi].g_begin;
 }
 
 // A weight format of the staged kernel: the bytes of four consecutive blocks
@@ -273,7 +296,10 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
     int2 *meta = reinterpret_cast<int2 *>(smem + kWarps * kStages * 8);  // (row group, piece) per stage
     unsigned int *counter = reinterpret_cast<unsigned int *>(smem + kWarps * kStages * 16);
     uint8_t *act = smem + smem_header_bytes<F>();
-    uint8_t *ring = act + ((g.nc * kActChunkBytes + 127) & ~127);
+    uint8_t *pairs = act + ((g.nc * kActChunkBytes + 127) & ~127);
+    float *pbuf = reinterpret_cast<float *>(pairs);                                 // [unit][64]
+    unsigned int *pcnt = reinterpret_cast<unsigned int *>(pbuf + 64 * g.pair_upc);  // [unit]
+    uint8_t *ring = pairs + pair_region_bytes(g.pair_upc);
     uint64_t *mybar = bars + warp * kStages;
     int2 *mymeta = meta + warp * kStages;
     uint8_t *myring = ring + warp * kStages * kPieceBytes;
@@ -282,8 +308,13 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
     // from it one at a time (a warp always computes whole rows, so the result
     // does not depend on which warp takes which group).
     const int64_t pitch = static_cast<int64_t>(g.nc) * kChunkBytes;
-    const int64_t cg0 = g.groups * blockIdx.x / gridDim.x;
-    const int64_t cg1 = g.groups * (blockIdx.x + 1) / gridDim.x;
+    int64_t cg0 = g.groups * blockIdx.x / gridDim.x;
+    int64_t cg1 = g.groups * (blockIdx.x + 1) / gridDim.x;
+    if (g.pair_upc) {  // whole units of 64 groups
+        const int64_t units = g.groups >> 6;
+        cg0 = (units * blockIdx.x / gridDim.x) << 6;
+        cg1 = (units * (blockIdx.x + 1) / gridDim.x) << 6;
+    }
     const unsigned int ngroups = static_cast<unsigned int>(cg1 - cg0);
 
     // lane 0's fetch cursor
@@ -312,8 +343,10 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
             return;
         }
         const int64_t G = cg0 + grp;
-        const GvProj &pj = g.p[proj_of(g, G)];
-        const int64_t Gl = G - pj.g_begin;  // row group within the projection
+        int pi;
+        int64_t Gl;  // row group within the projection
+        locate(g, G, pi, Gl);
+        const GvProj &pj = g.p[pi];
         const uint8_t *src;
         uint32_t bytes;
         if (g.rpw == 1) {  // one row per piece, up to 32*J chunks of it
@@ -331,6 +364,7 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
     };
 
     if (threadIdx.x == 0) *counter = 0u;
+    for (int i = threadIdx.x; i < g.pair_upc; i += blockDim.x) pcnt[i] = 0u;
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) q8::mbar_init(&mybar[s], 1);
         q8::fence_mbar_init();
@@ -386,8 +420,10 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
         if (m.x < 0) break;
         const uint8_t *buf = myring + s * kPieceBytes;
         const int64_t G = cg0 + m.x;
-        const GvProj &pj = g.p[proj_of(g, G)];
-        const int64_t Gl = G - pj.g_begin;
+        int pi;
+        int64_t Gl;
+        locate(g, G, pi, Gl);
+        const GvProj &pj = g.p[pi];
         const int p = m.y;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
@@ -413,7 +449,29 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
 #pragma unroll
                 for (int j = 1; j < J; ++j) a += acc[j];
                 for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(Q8_FULL_MASK, a, o);
-                if (lane == 0) pj.y[Gl] = a;
+                if (lane == 0 && pj.y) pj.y[Gl] = a;  // y may be absent only in pairing mode
+                if (g.pair_upc) {
+                    // this row's result into its unit; the warp that brings the
+                    // unit's count to 64 encodes silu(gate) * up for its 32 rows
+                    const int64_t ul = m.x >> 6;  // unit within this CTA (cg0 is unit-aligned)
+                    const int w = static_cast<int>(G & 63);
+                    unsigned int done = 0u;
+                    if (lane == 0) {
+                        pbuf[ul * 64 + w] = a;
+                        __threadfence_block();
+                        done = atomicAdd(&pcnt[ul], 1u);
+                    }
+                    done = __shfl_sync(Q8_FULL_MASK, done, 0);
+                    if (done == 63u) {
+                        __threadfence_block();
+                        const float gv = pbuf[ul * 64 + lane], uv = pbuf[ul * 64 + 32 + lane];
+                        uint32_t dsw;
+                        const int q = q8::q8_encode32(q8::silu_mul(gv, uv), dsw);
+                        const int64_t unit = G >> 6;
+                        g.pair_qs[unit * 32 + lane] = static_cast<int8_t>(q);
+                        if (lane == 0) g.pair_ds[unit] = dsw;
+                    }
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < J; ++j) {
@@ -999,9 +1057,15 @@ int gemv_small_q4a_launch(const void *w, int64_t n, int64_t k, const int8_t *qs,
 namespace {
 
 // Launch the staged kernel for `count` projections of one activation.
+// SwiGLU pairing output of a gate/up launch (plane row 0 of silu(gate) * up).
+struct GvPair {
+    int8_t *qs;
+    uint32_t *ds;
+};
+
 template <class F>
 int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds,
-                       cudaStream_t s, int smem_slot, const GvAct *act = nullptr)
+                       cudaStream_t s, int smem_slot, const GvAct *act = nullptr, const GvPair *pair = nullptr)
 {
     constexpr int kStages = F::kStages;
     constexpr int kMaxWarps = F::kWarps;
@@ -1041,6 +1105,10 @@ int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const in
         }
     }
     g.groups = groups;
+    g.pair_upc = 0;
+    g.pair_qs = pair ? pair->qs : nullptr;
+    g.pair_ds = pair ? pair->ds : nullptr;
+    if (pair && (count != 2 || g.rpw != 1 || projs[0].n != projs[1].n || projs[0].n % 32 != 0)) return Q8_ERR_ARG;
     const int sms = q8::device_sm_count();
     if (sms <= 0) return Q8_ERR_DEVICE;
     // warps per CTA: enough to spread the row groups over every SM, at most
@@ -1056,7 +1124,22 @@ int gemv_staged_launch(const q8_gemv_proj *projs, int count, int64_t k, const in
     nw = nw > fit ? fit : nw;
     int64_t grid = (g.groups + nw - 1) / nw;
     grid = grid > sms ? sms : grid;
-    const int smem = smem_header_bytes<F>() + act_bytes + static_cast<int>(nw) * kStages * kPieceBytes;
+    if (pair) {  // whole 64-row units per CTA, and their buffer beside the activation
+        const int64_t units = g.groups / 64;
+        int64_t upc = (units + grid - 1) / grid;
+        const int64_t fit2 = (kSmemCap - smem_header_bytes<F>() - act_bytes -
+                              pair_region_bytes(static_cast<int>(upc))) / (kStages * kPieceBytes);
+        if (upc > 4096 || fit2 < 1) return Q8_ERR_ARG;
+        if (nw > fit2) {  // fewer warps: more CTAs, so no more units per CTA than reserved
+            nw = fit2;
+            grid = (g.groups + nw - 1) / nw;
+            grid = grid > sms ? sms : grid;
+            upc = (units + grid - 1) / grid;
+        }
+        g.pair_upc = static_cast<int>(upc);
+    }
+    const int smem = smem_header_bytes<F>() + act_bytes + pair_region_bytes(g.pair_upc) +
+                     static_cast<int>(nw) * kStages * kPieceBytes;
     if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(gemv_staged_kernel<F>), kSmemCap, smem_slot))
         return Q8_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
@@ -1163,6 +1246,40 @@ extern "C" int q8_0_gemv_fused(const q8_gemv_proj *projs, int count, int64_t k, 
     q8::rms_row_mapping(static_cast<int>(k / 4), q8::kRmsMaxThreadsOneRow, act.rms_j, act.rms_p);
     return gemv_staged_launch<FmtQ8_0>(projs, count, k, nullptr, nullptr, static_cast<cudaStream_t>(stream), 0,
                                        &act);
+}
+
+extern "C" int q8_0_gemv_gate_up(const void *w_gate, const void *w_up, int64_t nf, int64_t k, const int8_t *qs,
+                                 const uint32_t *ds, int producer, const float *a, const float *norm_w, float eps,
+                                 float *y_gate, float *y_up, int8_t *qs_out, uint32_t *ds_out, void *stream)
+{
+    if (!w_gate || !w_up || !qs_out || !ds_out || nf < 32 || nf % 32 != 0 || nf > (int64_t(1) << 40) || k <= 0 ||
+        (k % 32) != 0)
+        return Q8_ERR_ARG;
+    if (producer == 0 ? (!qs || !ds)
+                      : ((producer != Q8_PRODUCER_QUANT && producer != Q8_PRODUCER_RMSNORM) || !a ||
+                         (producer == Q8_PRODUCER_RMSNORM && (!norm_w || k > 32768))))
+        return Q8_ERR_ARG;
+    // the staged path with whole rows per warp (more than 16 chunks of 4 blocks)
+    if ((k / 32) % 8 != 0 || k / 128 > kMaxActChunks || k / 128 <= 16) return Q8_ERR_ARG;
+    if (!q8::aligned16(w_gate) || !q8::aligned16(w_up) || !q8::aligned16(qs_out) || !q8::aligned16(ds_out) ||
+        (y_gate && !q8::aligned16(y_gate)) || (y_up && !q8::aligned16(y_up)))
+        return Q8_ERR_ALIGN;
+    if (producer == 0 ? (!q8::aligned16(qs) || !q8::aligned16(ds))
+                      : (!q8::aligned16(a) || (producer == Q8_PRODUCER_RMSNORM && !q8::aligned16(norm_w))))
+        return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    const q8_gemv_proj projs[2] = {{w_gate, nf, y_gate}, {w_up, nf, y_up}};
+    const GvPair pair{qs_out, ds_out};
+    GvAct act{};
+    if (producer != 0) {
+        act.producer = producer;
+        act.a = reinterpret_cast<const float4 *>(a);
+        act.w = producer == Q8_PRODUCER_RMSNORM ? reinterpret_cast<const float4 *>(norm_w) : nullptr;
+        act.eps = eps;
+        q8::rms_row_mapping(static_cast<int>(k / 4), q8::kRmsMaxThreadsOneRow, act.rms_j, act.rms_p);
+    }
+    return gemv_staged_launch<FmtQ8_0>(projs, 2, k, producer == 0 ? qs : nullptr, producer == 0 ? ds : nullptr,
+                                       static_cast<cudaStream_t>(stream), 0, &act, &pair);
 }
 
 extern "C" int q8_0_gemv_batched(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds,

@@ -260,18 +260,32 @@ struct Q8Enc {
 
 __device__ __forceinline__ int clamp127(int v) { return max(-127, min(127, v)); }
 
+// The scalar steps of the q8_0 encoding of one block: d = amax / 127 and its
+// reciprocal (both IEEE round-to-nearest), a code = rni(v * 1/d) clamped to
+// +-127, and the packed d | ssum word.  amax and ssum do not depend on the
+// order they are reduced in (a maximum; an integer sum).
+__device__ __forceinline__ float q8_block_d(float amax) { return __fdiv_rn(amax, 127.0f); }
+__device__ __forceinline__ float q8_block_di(float d) { return (d != 0.0f) ? __frcp_rn(d) : 0.0f; }
+__device__ __forceinline__ int q8_code(float v, float di) { return clamp127(__float2int_rn(__fmul_rn(v, di))); }
+__device__ __forceinline__ uint32_t q8_dsword(float d, int ssum)
+{
+    return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(d))) |
+           (static_cast<uint32_t>(static_cast<uint16_t>(static_cast<int16_t>(ssum))) << 16);
+}
+
+// 8 adjacent lanes hold one 32-element block, a float4 each.
 __device__ __forceinline__ Q8Enc q8_encode8(float4 v)
 {
     float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     a = fmaxf(a, __shfl_xor_sync(Q8_FULL_MASK, a, 1));
     a = fmaxf(a, __shfl_xor_sync(Q8_FULL_MASK, a, 2));
     a = fmaxf(a, __shfl_xor_sync(Q8_FULL_MASK, a, 4));
-    const float d = __fdiv_rn(a, 127.0f);
-    const float di = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
-    const int q0 = clamp127(__float2int_rn(__fmul_rn(v.x, di)));
-    const int q1 = clamp127(__float2int_rn(__fmul_rn(v.y, di)));
-    const int q2 = clamp127(__float2int_rn(__fmul_rn(v.z, di)));
-    const int q3 = clamp127(__float2int_rn(__fmul_rn(v.w, di)));
+    const float d = q8_block_d(a);
+    const float di = q8_block_di(d);
+    const int q0 = q8_code(v.x, di);
+    const int q1 = q8_code(v.y, di);
+    const int q2 = q8_code(v.z, di);
+    const int q3 = q8_code(v.w, di);
     int s = q0 + q1 + q2 + q3;
     s += __shfl_xor_sync(Q8_FULL_MASK, s, 1);
     s += __shfl_xor_sync(Q8_FULL_MASK, s, 2);
@@ -279,9 +293,24 @@ __device__ __forceinline__ Q8Enc q8_encode8(float4 v)
     Q8Enc e;
     e.qword = (static_cast<uint32_t>(q0) & 0xffu) | ((static_cast<uint32_t>(q1) & 0xffu) << 8) |
               ((static_cast<uint32_t>(q2) & 0xffu) << 16) | (static_cast<uint32_t>(q3) << 24);
-    e.dsword = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(d))) |
-               (static_cast<uint32_t>(static_cast<uint16_t>(static_cast<int16_t>(s))) << 16);
+    e.dsword = q8_dsword(d, s);
     return e;
+}
+
+// The 32 lanes of a warp hold one block, a value each: this lane's code,
+// and the block's d | ssum word (the same on every lane).
+__device__ __forceinline__ int q8_encode32(float v, uint32_t &dsword)
+{
+    float a = fabsf(v);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) a = fmaxf(a, __shfl_xor_sync(Q8_FULL_MASK, a, o));
+    const float d = q8_block_d(a);
+    const int q = q8_code(v, q8_block_di(d));
+    int s = q;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) s += __shfl_xor_sync(Q8_FULL_MASK, s, o);
+    dsword = q8_dsword(d, s);
+    return q;
 }
 
 // Producer arithmetic, one implementation for the standalone producers

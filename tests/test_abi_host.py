@@ -129,6 +129,22 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert fused(pr, 1, 256, 2, P(FAKE), P(0), P(MISALIGNED), 1e-6, s) == ERR_ALIGN
     bad = (_binding.GemvProj * 1)(_binding.GemvProj(FAKE + 8, 8, FAKE))
     assert fused(ctypes.cast(bad, ctypes.c_void_p), 1, 256, 1, P(FAKE), P(0), P(0), 0.0, s) == ERR_ALIGN
+    # q8_0_gemv_gate_up: nf % 32, k on the staged whole-row path (2048 < k <= 65536), producer and its inputs,
+    # the output plane, alignment
+    gu = lambda nf, k, qs, ds, prod, a, nw, yg, qo, do: lib.q8_0_gemv_gate_up(  # noqa: E731
+        P(FAKE), P(FAKE), nf, k, P(qs), P(ds), prod, P(a), P(nw), 1e-6, P(yg), P(0), P(qo), P(do), s)
+    assert gu(48, 3584, FAKE, FAKE, 0, 0, 0, 0, FAKE, FAKE) == ERR_ARG          # nf % 32
+    assert gu(64, 2048, FAKE, FAKE, 0, 0, 0, 0, FAKE, FAKE) == ERR_ARG          # rows share a warp at k <= 2048
+    assert gu(64, 2080, FAKE, FAKE, 0, 0, 0, 0, FAKE, FAKE) == ERR_ARG          # 65 blocks per row
+    assert gu(64, 65536 + 256, FAKE, FAKE, 0, 0, 0, 0, FAKE, FAKE) == ERR_ARG   # longer than the staging
+    assert gu(64, 3584, 0, FAKE, 0, 0, 0, 0, FAKE, FAKE) == ERR_ARG             # plane missing
+    assert gu(64, 3584, 0, 0, 3, FAKE, 0, 0, FAKE, FAKE) == ERR_ARG             # no SwiGLU producer here
+    assert gu(64, 3584, 0, 0, 2, FAKE, 0, 0, FAKE, FAKE) == ERR_ARG             # norm weight missing
+    assert gu(64, 32768 + 256, 0, 0, 2, FAKE, FAKE, 0, FAKE, FAKE) == ERR_ARG   # RMSNorm limit
+    assert gu(64, 3584, FAKE, FAKE, 0, 0, 0, 0, 0, FAKE) == ERR_ARG             # output plane missing
+    assert gu(64, 3584, FAKE, FAKE, 0, 0, 0, 0, MISALIGNED, FAKE) == ERR_ALIGN
+    assert gu(64, 3584, FAKE, FAKE, 0, 0, 0, MISALIGNED, FAKE, FAKE) == ERR_ALIGN
+    assert gu(64, 3584, 0, 0, 1, MISALIGNED, 0, 0, FAKE, FAKE) == ERR_ALIGN
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):

@@ -92,3 +92,12 @@ def test_fused_decode_accounts():
     """The decode step with its k = 7168 quantize inside the grouped GEMV: the plane's write and its reads by the two
     projections (counted per projection in the unfused step) are gone, the f32 activation is read once."""
     assert bench.decode_bytes() - bench.decode_bytes(fused=True) == 3 * _plane_row_bytes(7168)
+
+
+def test_gate_up_pair_accounts():
+    """Gate/up writing the SwiGLU plane in its epilogue: per layer the gate/up f32 outputs (written, then read by
+    swiglu_quant) disappear; every other byte stays."""
+    f32 = np.dtype(np.float32).itemsize
+    L = bench.LAYERS
+    nf = L["nf"]
+    assert bench.bytes_layer_stack() - bench.bytes_layer_stack(("gu_pair",)) == L["layers"] * 4 * nf * f32

@@ -119,3 +119,72 @@ def test_fused_rejects_unsupported(q8):
         q8.q8_0_gemv_fused([(w, 1, y)], k, q8.PRODUCER_SWIGLU, x)   # up missing
     with pytest.raises(q8.Q8Error):
         q8.q8_0_gemv_fused([(w, 1, y)], k, q8.PRODUCER_RMSNORM, x)  # weight missing
+
+
+GATE_UP = [
+    # (nf, k): the model's shape, a ragged number of 64-row units per CTA, long rows (several pieces), the k limits
+    (18944, 3584),
+    (96, 2304),
+    (4096, 18944),
+    (1024, 65536),
+    (32, 4096),
+]
+
+
+@pytest.mark.parametrize("producer", [0, 1, 2])
+@pytest.mark.parametrize("nf,k", GATE_UP)
+def test_gate_up_equals_grouped_then_swiglu_quant(q8, producer, nf, k):
+    """q8_0_gemv_gate_up: its gate/up outputs bit for bit those of the grouped GEMV (or the fused one) on the same
+    activation, its plane bit for bit swiglu_quant's encoding of those outputs, and that plane within the oracle's
+    pinned arithmetic (oracle.quantize of the f32 SwiGLU row the standalone kernel writes)."""
+    import torch
+
+    if producer == 2 and k > 32768:
+        pytest.skip("RMSNorm rows are limited to 32768")
+    wg_h, wu_h = _weights(20, nf, k), _weights(21, nf, k)
+    wg, wu = dev(wg_h), dev(wu_h)
+    a_h, _, w_h = _inputs(producer or 1, k, 7)
+    a, nw = dev(a_h), (dev(w_h) if w_h is not None else None)
+    eps = 1e-6
+    qs, ds = q8.empty_plane(1, k)
+    q8.quantize_q8_0(a.view(1, k), qs, ds)
+    q_out, d_out = q8.empty_plane(1, nf)
+    q_out.fill_(-91), d_out.fill_(0x5A5A5A5A)
+    yg, yu = nan_f32(nf), nan_f32(nf)
+    if producer == 0:
+        q8.q8_0_gemv_gate_up(wg, wu, nf, k, q_out, d_out, qs=qs, ds=ds, y_gate=yg, y_up=yu)
+    else:
+        q8.q8_0_gemv_gate_up(wg, wu, nf, k, q_out, d_out, producer=producer, a=a, norm_w=nw, eps=eps,
+                             y_gate=yg, y_up=yu)
+    q8.q8_check()
+    # the same projections the plain way
+    rg, ru = nan_f32(nf), nan_f32(nf)
+    if producer == 0:
+        q8.q8_0_gemv_grouped([(wg, nf, rg), (wu, nf, ru)], k, qs, ds)
+    else:
+        q8.q8_0_gemv_fused([(wg, nf, rg), (wu, nf, ru)], k, producer, a, None, nw, eps)
+    q8.q8_check()
+    assert torch.equal(yg, rg) and torch.equal(yu, ru), "gate/up outputs differ from the grouped GEMV"
+    ys = nan_f32(1, nf)
+    q_ref, d_ref = q8.empty_plane(1, nf)
+    q8.swiglu_quant(rg.view(1, nf), ru.view(1, nf), ys, q_ref, d_ref)
+    q8.q8_check()
+    assert torch.equal(q_out, q_ref) and torch.equal(d_out, d_ref), "plane differs from swiglu_quant's"
+    qo, do = oracle.quantize(host(ys), 1)
+    assert np.array_equal(host(q_out), qo) and np.array_equal(host(d_out).view(np.uint32), do)
+
+
+def test_gate_up_without_f32_outputs(q8):
+    """y_gate / y_up may be NULL: the plane is the same bytes."""
+    import torch
+
+    nf, k = 18944, 3584
+    wg, wu = dev(_weights(22, nf, k)), dev(_weights(23, nf, k))
+    a = dev(_inputs(1, k, 8)[0])
+    q1, d1 = q8.empty_plane(1, nf)
+    q2, d2 = q8.empty_plane(1, nf)
+    yg, yu = nan_f32(nf), nan_f32(nf)
+    q8.q8_0_gemv_gate_up(wg, wu, nf, k, q1, d1, producer=1, a=a, y_gate=yg, y_up=yu)
+    q8.q8_0_gemv_gate_up(wg, wu, nf, k, q2, d2, producer=1, a=a)
+    q8.q8_check()
+    assert torch.equal(q1, q2) and torch.equal(d1, d2)
