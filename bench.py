@@ -627,10 +627,10 @@ def bytes_gemv_fused(k, ns, producer):
     return sum(n * (k // 32) * 34 + 4 * n for n in ns) + f32_in
 
 
-def bytes_layer_stack(fused=()):
+def bytes_layer_stack(fused=(), layers=None):
     """Algorithmic bytes of one token; `fused` = the producers computed inside
     their consumer's launch (of "qkv", "o", "gu", "down", "head")."""
-    L = LAYERS
+    L = dict(LAYERS, layers=layers or LAYERS["layers"])
     d, nf = L["d"], L["nf"]
     (_, qkv), (_, o), (_, gu), (_, down) = layer_groups()
     steps = [("qkv", d, qkv, "rmsnorm"), ("o", d, o, "quant"), ("gu", d, gu, "rmsnorm"), ("down", nf, down, "swiglu")]
@@ -652,7 +652,7 @@ def bytes_layer_stack(fused=()):
     return L["layers"] * per_layer + one("head", d, [L["vocab"]], "rmsnorm")
 
 
-def run_layers(torch, q8p, steps, warmup, dev):
+def run_layers(torch, q8p, steps, warmup, dev, layer_count=LAYERS["layers"]):
     """Per layer: RMSNorm -> q/k/v (one grouped launch); quantize of the
     attention output -> o; RMSNorm -> gate/up (one grouped launch); SwiGLU of
     their outputs -> down.  Then the final norm and the LM head.  Timed three
@@ -664,7 +664,7 @@ def run_layers(torch, q8p, steps, warmup, dev):
     Layer 0's matrices are drawn from the synthetic recipe; layers 1..27 are
     device copies of them (the same bytes, distinct memory, so every token
     streams all 7.5 GB from HBM)."""
-    L = LAYERS
+    L = dict(LAYERS, layers=layer_count)
     d, nf, eps = L["d"], L["nf"], L["eps"]
     g = syn.rng(4, 0)
     shapes = [(n, k) for k, ns in layer_groups() for n in ns]  # q k v o gate up down
@@ -834,6 +834,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--layer-count", type=int, default=LAYERS["layers"],
+                    help="layers of the layer-stack leg (a shorter stack for profiling runs)")
     ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "small", "asym", "shared", "layers"],
                     help="decode and/or prefill legs (profiling runs select one)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
@@ -894,7 +896,8 @@ def main():
     lay = None
     if args.workload in ("all", "layers"):
         lay = run_layers(torch, q8p, args.steps if args.workload == "layers" else max(10, args.steps // 200),
-                         args.warmup, dev)
+                         args.warmup, dev,
+                         args.layer_count)
 
     if world > 1:  # every duration becomes the slowest rank's (same legs on every rank)
         vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"]]
@@ -1043,10 +1046,11 @@ def main():
                          "roofline": sobj2["roofline"], "gpu_launches": shr["steps"]})
         line["shared_activation"] = sobj2
     if lay is not None:
-        L = LAYERS
-        byts = bytes_layer_stack(LAYER_FUSED)
+        L = dict(LAYERS, layers=args.layer_count)
+        byts = bytes_layer_stack(LAYER_FUSED, args.layer_count)
         gbs = byts / (lay["ms"] / 1e3) / 1e9
-        byts2, byts3 = bytes_layer_stack(), bytes_layer_stack(("qkv", "o", "gu", "down", "head"))
+        byts2 = bytes_layer_stack((), args.layer_count)
+        byts3 = bytes_layer_stack(("qkv", "o", "gu", "down", "head"), args.layer_count)
         lobj = {"workload": f"layer-stack decode b=1: {L['layers']} layers (d={L['d']}, nf={L['nf']}; q {L['q']}, "
                             f"k/v {L['kv']}, o, gate/up, down) + LM head {L['vocab']}x{L['d']}; per layer RMSNorm "
                             "-> grouped q/k/v and quantize -> o inside their GEMV launch (q8_0_gemv_fused), "
@@ -1065,11 +1069,12 @@ def main():
                               "ms_per_token": round(lay["ms_fused"], 4),
                               "gbs": round(byts3 / (lay["ms_fused"] / 1e3) / 1e9, 1), "algorithmic_bytes": byts3,
                               "launches_per_token": lay["launches_fused"]},
-                "launch": "one CUDA graph per token, replayed; layers 1..27 are device copies of layer 0's matrices "
-                          "(distinct memory: 7.5 GB streamed per token, > L2)"}
+                "launch": f"one CUDA graph per token, replayed; layers 1..{L['layers'] - 1} are device copies of layer "
+                          f"0's matrices (distinct memory: {lay['weight_bytes'] / 1e9:.2f} GB streamed per token, > L2)"}
         if args.workload == "layers":
             line.update({"value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": lobj["ms_per_token"],
-                         "config": {"workload": lobj["workload"], "l2": "7.5 GB of weights per token > L2",
+                         "config": {"workload": lobj["workload"],
+                                    "l2": f"{lay['weight_bytes'] / 1e9:.2f} GB of weights per token > L2",
                                     "parallelism": "replicas"},
                          "roofline": lobj["roofline"], "gpu_launches": lay["launches"] * args.steps})
         line["layer_stack"] = lobj
