@@ -814,13 +814,12 @@ def reference_arm(args):
 
 
 def decode_config(copies):
-    return {"workload": "decode GEMV sweep b=1: q8_0 quantize + Q8_0 GEMV (n,k) in {(12288,7168),(96,7168),(512,128)}; "
-                        "the k = 7168 pair in one q8_0_gemv_fused launch (quantize inside), the k = 128 chain "
-                        "(quantize_q8_0 -> q8_0_gemv) on a parallel graph branch",
+    return {"workload": "decode GEMV sweep b=1: q8_0 quantize + Q8_0 GEMV (n,k) in {(12288,7168),(96,7168),(512,128)}",
             "activation": "f32 ~N(0,1.5), 1% outliers x20, seed 1", "weights": "Q8_0, d~U(0.002,0.02), q~U{-127..127}",
             "l2": (f"weights rotate through {copies} copies ({copies} x 94.4 MB > 4 x L2)" if copies else "n/a (CPU)"),
-            "launch": ("timed steps replayed from a CUDA graph of one step per weight copy" if copies
-                       else "n/a (CPU)"),
+            "launch": ("timed steps replayed from a CUDA graph of one step per weight copy; per step the k = 7168 "
+                       "pair is one q8_0_gemv_fused launch (quantize inside) and the k = 128 chain (quantize_q8_0 -> "
+                       "q8_0_gemv) a parallel graph branch" if copies else "n/a (CPU)"),
             "parallelism": "replicas"}
 
 
