@@ -26,8 +26,7 @@
  *          weight blocks contracted with per-block scales; the q4_K weight
  *          value d*s*nib - dmin*m, whose min term the plane's ssum serves).
  *
- * Readings where the pages are silent or disagree (each is listed in
- * the design doc):
+ * Readings where the pages are silent or disagree:
  *   - di = 1/d computed in f32 (the page multiplies by di); di = 0 when d = 0.
  *   - clamp to [-127, 127]: for finite inputs |x*di| < 127.5, so the page's
  *     [-128, 127] clamp and the +-127 clamp give identical codes.

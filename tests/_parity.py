@@ -1,7 +1,7 @@
 """Shared helpers of the GPU parity tests: moving seeded numpy inputs to the
 device, poisoning outputs, and the comparison rules.
 
-Comparison rules (written out here and in the design doc):
+Comparison rules:
   * planes (qs bytes, d bits, int16 ssum): bit-exact against the oracle;
   * f32 producer outputs (RMSNorm, SwiGLU): |y - y_ref| <= 1e-5 |y_ref| + 2^-100,
     y_ref the oracle's fp64 value;
