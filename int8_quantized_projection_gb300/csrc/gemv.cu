@@ -25,6 +25,17 @@
 //        the grid is a persistent set of at most one CTA per SM whose warp
 //        count shrinks for small n, so small projections still spread over
 //        many SMs.
+// Two more modes of the same kernel (same weight stream, same per-row
+// arithmetic, so the same output bits):
+//   - fused producer (q8_0_gemv_fused): instead of copying a plane row, every
+//     CTA computes the one-row producer (quantize, RMSNorm or SwiGLU) and its
+//     q8_0 encoding straight into the staged activation, with the producer
+//     arithmetic shared with the standalone kernels ("Part 4 - Lecture 05",
+//     sec. 4: producer and consumer in one launch, one implementation);
+//   - SwiGLU pairing (q8_0_gemv_gate_up): gate and up rows are interleaved in
+//     units of 32 + 32 owned by one CTA, and the warp that completes a unit
+//     writes the q8_0 block of silu(gate) * up, so the down projection's
+//     plane comes out of this launch.
 // Shapes whose k/32 is not a multiple of 8 (or whose activation would not
 // fit in shared memory) use gemv_generic_kernel: plain 2-byte loads, the same
 // lanes-per-row fitting, no staging.
