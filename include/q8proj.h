@@ -307,7 +307,7 @@ Q8_API int q4a_gemv_batched(const void *w, int64_t n, int64_t k,
  * (k/32 * 4 bytes per weight row and per token, rows and tokens rounded up to
  * the GEMM's 128 x 192 tiles), each part starting on a 1 KiB boundary; when
  * the tiles would leave most SMs idle (few weight rows or tokens) k is split
- * over up to 8 CTAs per tile and the workspace also holds their f32 partial
+ * over up to 12 CTAs per tile and the workspace also holds their f32 partial
  * outputs (splits * t * n * 4 bytes, added in a fixed order by a reduction
  * kernel; splits * tiles <= 152, so at most about 15 MB).  The size depends
  * on (n, t, k) only.  0 when (k/32) % 8 != 0 or t <= 64 (those calls run

@@ -596,7 +596,7 @@ gemm_split_reduce_kernel(const float *__restrict__ part, int splits, int64_t cou
 // runs, each over at least 4 stages (8 blocks).  A fixed SM count is used so
 // that the workspace size is a function of the shape alone; splits * tiles
 // stays at most that count, which bounds the partial tiles by about 15 MB.
-constexpr int kSplitSms = 152, kMaxSplits = 8;
+constexpr int kSplitSms = 152, kMaxSplits = 12;
 int gemm_splits(int64_t n, int64_t t, int64_t k)
 {
     const int64_t tiles = ((n + BM - 1) / BM) * ((t + BN - 1) / BN);
