@@ -86,6 +86,14 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
         + 8 * 130 * 256 * 4
     assert lib.q8_0_gemm_workspace_bytes(18944, 3325, 3584) == up(up(up(up(18944 * 3584 * 2) + 3325 * 3584 * 2)
                                                                      + 148 * 112 * 128 * 4) + 18 * 112 * 192 * 4)
+    # 4 x 3 = 12 tiles: k split 12 ways (152 // 12 = 12, the cap; 56 stages allow 14) -> 12 x t x n partials
+    assert lib.q8_0_gemm_workspace_bytes(512, 512, 3584) == up(up(up(up(512 * 3584 * 2) + 512 * 3584 * 2)
+                                                                 + 4 * 112 * 128 * 4) + 3 * 112 * 192 * 4) \
+        + 12 * 512 * 512 * 4
+    # 4 x 11 = 44 tiles: 152 // 44 = 3 splits
+    assert lib.q8_0_gemm_workspace_bytes(512, 2048, 3584) == up(up(up(up(512 * 3584 * 2) + 2048 * 3584 * 2)
+                                                                  + 4 * 112 * 128 * 4) + 11 * 112 * 192 * 4) \
+        + 3 * 2048 * 512 * 4
     assert lib.q8_0_gemm_workspace_bytes(8, 20, 64) == 0      # k/32 % 8 != 0: generic kernel, no workspace
     assert lib.q8_0_gemm_workspace_bytes(8, 16, 256) == 0     # t <= 16: small-batch kernel, no workspace
     assert lib.q8_0_gemm_workspace_bytes(8, 64, 256) == 0     # t <= 64: 16-token slices, no workspace
