@@ -188,3 +188,30 @@ def test_gate_up_without_f32_outputs(q8):
     q8.q8_0_gemv_gate_up(wg, wu, nf, k, q2, d2, producer=1, a=a)
     q8.q8_check()
     assert torch.equal(q1, q2) and torch.equal(d1, d2)
+
+
+def test_fused_decode_pair_full_size(q8):
+    """The decode step's launch at full size: quantize inside the grouped 12288 x 7168 + 96 x 7168 GEMV, on an
+    activation with the decode recipe (N(0, 1.5), 1 % outliers x20); every output against the two-launch path
+    (bit for bit) and the oracle."""
+    import torch
+
+    k, ns = 7168, (12288, 96)
+    g = syn.rng(72, k)
+    x_h = syn.activations(g, 1, k, sigma=1.5, outlier_frac=0.01, outlier_mult=20.0)[0]
+    x = dev(x_h)
+    blobs = [_weights(30 + i, n, k) for i, n in enumerate(ns)]
+    wd = [dev(b) for b in blobs]
+    yf = [nan_f32(n) for n in ns]
+    q8.q8_0_gemv_fused([(w, n, y) for w, n, y in zip(wd, ns, yf)], k, q8.PRODUCER_QUANT, x)
+    q8.q8_check()
+    yt = [nan_f32(n) for n in ns]
+    qs, ds = q8.empty_plane(q8.q8_plane_rows(1), k)
+    q8.quantize_q8_0(x.view(1, k), qs, ds)
+    q8.q8_0_gemv_grouped([(w, n, y) for w, n, y in zip(wd, ns, yt)], k, qs, ds)
+    q8.q8_check()
+    qr, dr = oracle.quantize(x_h.reshape(1, k), 1)
+    for blob, n, a, b in zip(blobs, ns, yf, yt):
+        assert torch.equal(a, b), f"{n}x{k}: fused != two launches"
+        yr, ar = oracle.gemv(blob, n, k, qr, dr)
+        assert_gemm_close(host(a), yr, ar, f"fused decode {n}x{k}")
