@@ -106,7 +106,8 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
 // 16 registers per thread.  Thread i of the warp receives, for repetition
 // rep, lanes (i/4) and (i/4 + 8) of the 16 at columns 8*rep + 2*(i%4) + {0,1}:
 // registers 4*rep + {0,1} (lane i/4), 4*rep + {2,3} (lane i/4 + 8).
-// Asynchronous: the registers are valid only after tc_wait_ld16.
+// Asynchronous: the registers are valid only after tc_wait_ld_all, and
+// tc_regs16 keeps their uses from being scheduled before that wait.
 __device__ __forceinline__ void tc_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16])
 {
     asm volatile(
@@ -114,18 +115,6 @@ __device__ __forceinline__ void tc_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-}
-
-// Wait for this thread's outstanding TMEM loads.  The registers of the load
-// being waited for pass through the statement, so no use of them can be
-// scheduled before it; having no memory clobber, it leaves shared-memory
-// loads free to move across it.
-__device__ __forceinline__ void tc_wait_ld16(uint32_t (&r)[16])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                   "+r"(r[15]));
 }
 
 // Shared-memory matrix descriptor, K-major.  No swizzle: core matrices of
@@ -216,7 +205,9 @@ __device__ __forceinline__ int dw_slot(int r)  // weight row 0..127
 {
     return (r >> 5) * 32 + (r & 7) * 4 + ((r >> 4) & 1) * 2 + ((r >> 3) & 1);
 }
-__device__ __forceinline__ int da_slot(int c)  // token column 0..BN-1
+// (da_slot is the definition of the order; the activation pre-pass writes
+// its inverse, and the epilogue reads slots in this order.)
+__device__ __forceinline__ __attribute__((unused)) int da_slot(int c)  // token column 0..BN-1
 {
     return (c >> 6) * 64 + ((c >> 5) & 1) * 32 + ((c >> 1) & 3) * 8 + ((c >> 3) & 3) * 2 + (c & 1);
 }
