@@ -5,7 +5,9 @@
  * The path: an f32 activation is encoded once into a q8_0 "plane", either by a
  * standalone quantizer or by the producer kernel that computes it (RMSNorm or
  * SwiGLU), and that plane is contracted with Q8_0 weights by a batch-1 GEMV
- * (decode) or a GEMM (prefill).
+ * (decode) or a GEMM (prefill).  For a decode token the encoding can also
+ * happen inside the GEMV launch that consumes it (q8_0_gemv_fused), and the
+ * gate/up GEMV can write the SwiGLU output's plane itself (q8_0_gemv_gate_up).
  *
  * Formats
  *   Q8_0 weight block: 34 bytes -- little-endian f16 scale d at +0, then 32
