@@ -1,0 +1,230 @@
+"""Bit-exact per-block integer sums at the full code range, on every
+contraction path.
+
+The target requires the int32 block dot products isum_b = sum_j qw_j * qa_j
+to be exact.  Here every scale is 1.0 (f16 0x3C00 in every weight block and
+every ds word, the plane's ssum consistent with its codes), so each output is
+the plain integer sum_b isum_b (or, for asymmetric blocks with a min of 0 or
+1, sum_b (isum_b - m * ssum_b)).  The codes span the whole [-127, 127] range
+and include saturated patterns (all +127, all -127, alternating signs, a ramp
+through every code), so a single block reaches |isum| = 32 * 127^2 = 516,128.
+Shapes keep sum_b |term_b| below 2^24 for every output -- asserted on the
+oracle's absolute sum before the comparison -- so every partial sum the GPU
+forms, in whatever order, is an integer that f32 holds exactly.  The GPU
+result must then equal the oracle bit for bit: an off-by-one in any block's
+integer sum (the f16 widening, a fragment permutation, a dp4a sign path, a
+split-K partial) shows as a mismatch.
+
+Sources: the Q8_0 block dot and its per-block scale ("12 - r5-r6 re-ranking +
+structural rewrite spec", sec. 2; "Part 4 - Lecture 05", sec. 2.2: dp4a on
+the int8 codes); the int16 block sum and its min-term use ("54 - r51 -
+producer-fused A-quantize mode 1", sec. 2.1).
+
+Paths: q8_0_gemv (staged kernel at k = 256/512/1024, generic at k = 96/128),
+q8_0_gemv_grouped, q8_0_gemv_gate_up (its f32 gate/up outputs),
+q8_0_gemv_batched (t = 1..8 on the int8 MMA, 9..16 on the f16 MMA), q8_0_gemm
+(16-token slices for 16 < t <= 64, the tcgen05 kernel unsplit and split over
+k, the generic kernel), q8_0_gemm_mma, q4a_gemv and q4a_gemv_batched.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from int8_quantized_projection_gb300 import synthetic as syn
+
+from ._parity import dev, host, nan_f32
+
+pytestmark = pytest.mark.gpu
+
+F16_ONE = 0x3C00
+EXACT_LIMIT = 2.0 ** 24
+PATTERNS = ("random", "random", "random", "pos", "neg", "alt", "ramp", "random")
+
+
+def _codes(g, rows, k, sat_cols):
+    """int8 codes [rows][k] over [-127, 127]: row r follows PATTERNS[r % 8] in
+    its first `sat_cols` columns and is uniform random after them."""
+    q = g.integers(-127, 128, size=(rows, k)).astype(np.int8)
+    j = np.arange(sat_cols)
+    for r in range(rows):
+        p = PATTERNS[r % len(PATTERNS)]
+        if p == "pos":
+            q[r, :sat_cols] = 127
+        elif p == "neg":
+            q[r, :sat_cols] = -127
+        elif p == "alt":
+            q[r, :sat_cols] = np.where(j % 2 == 0, 127, -127)
+        elif p == "ramp":
+            q[r, :sat_cols] = ((j * 37 + r) % 255) - 127
+    return q
+
+
+def _sat_cols(k):
+    # 32 saturated blocks reach 16,516,096 < 2^24; longer rows saturate their
+    # first 24 blocks and leave the random tail well inside the bound
+    return k if k <= 1024 else 768
+
+
+def _unit_weights(seed, n, k):
+    g = syn.rng(90, seed, n, k)
+    q = _codes(g, n, k, _sat_cols(k))
+    d16 = np.full((n, k // 32), F16_ONE, np.uint16)
+    return syn.pack_q8_0(d16, q)
+
+
+def _unit_plane(seed, t, k, rows_pad=None, shift=3):
+    """Plane with unit d and full-range codes; token t follows PATTERNS[(t + shift) % 8]."""
+    g = syn.rng(91, seed, t, k)
+    rp = rows_pad or t
+    qa = np.zeros((rp, k), np.int8)
+    q = _codes(g, t + shift, k, _sat_cols(k))[shift:]
+    qa[:t] = q
+    ssum = qa.reshape(rp, k // 32, 32).astype(np.int64).sum(-1)
+    ds = np.uint32(F16_ONE) | (ssum.astype(np.int16).view(np.uint16).astype(np.uint32) << 16)
+    ds[t:] = 0
+    return qa, ds.astype(np.uint32)
+
+
+def _assert_exact(y_gpu, y_ref, absum, what):
+    assert absum.max() < EXACT_LIMIT, f"{what}: test data leaves the exact range ({absum.max():.0f})"
+    assert np.all(y_ref == np.rint(y_ref)), f"{what}: unit-scale reference is not an integer"
+    yg = np.asarray(y_gpu, dtype=np.float64)
+    bad = np.argwhere(yg != y_ref)
+    assert bad.size == 0, (f"{what}: {len(bad)} outputs differ, first at {bad[:3].tolist()}: "
+                           f"gpu {yg[tuple(bad[0])]:.1f} vs {y_ref[tuple(bad[0])]:.1f}")
+
+
+# ---------------------------------------------------------------------------
+# batch 1
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("shift", [0, 3, 4, 5, 6])  # plane pattern: random, pos, neg, alt, ramp
+@pytest.mark.parametrize("n,k", [(300, 1024), (1000, 512), (33, 256), (1, 1024), (512, 128), (77, 96)])
+def test_gemv_full_range_bit_exact(q8, n, k, shift):
+    blob = _unit_weights(1, n, k)
+    qs, ds = _unit_plane(1, 1, k, shift=shift)
+    y = nan_f32(n)
+    q8.q8_0_gemv(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), y)
+    q8.q8_check()
+    yr, ar = oracle.gemv(blob, n, k, qs, ds)
+    _assert_exact(host(y), yr, ar, f"gemv {n}x{k} plane pattern {PATTERNS[shift]}")
+
+
+def test_gemv_grouped_full_range_bit_exact(q8):
+    k, ns = 1024, [300, 64, 7, 1000]
+    qs, ds = _unit_plane(2, 1, k, shift=5)
+    qd, dd = dev(qs), dev(ds.view(np.int32))
+    blobs = [_unit_weights(10 + i, n, k) for i, n in enumerate(ns)]
+    ys = [nan_f32(n) for n in ns]
+    q8.q8_0_gemv_grouped([(dev(b), n, y) for b, n, y in zip(blobs, ns, ys)], k, qd, dd)
+    q8.q8_check()
+    for blob, n, y in zip(blobs, ns, ys):
+        yr, ar = oracle.gemv(blob, n, k, qs, ds)
+        _assert_exact(host(y), yr, ar, f"grouped gemv {n}x{k}")
+
+
+@pytest.mark.parametrize("nf,k", [(256, 2304), (64, 3072)])
+def test_gate_up_full_range_bit_exact(q8, nf, k):
+    """q8_0_gemv_gate_up on a plane (producer 0): its f32 gate and up outputs
+    are the exact integer projections."""
+    import torch
+
+    wg, wu = _unit_weights(20, nf, k), _unit_weights(21, nf, k)
+    qs, ds = _unit_plane(22, 1, k, shift=4)
+    yg, yu = nan_f32(nf), nan_f32(nf)
+    qs_out = torch.empty((1, nf), dtype=torch.int8, device="cuda")
+    ds_out = torch.empty((1, nf // 32), dtype=torch.int32, device="cuda")
+    q8.q8_0_gemv_gate_up(dev(wg), dev(wu), nf, k, qs_out, ds_out, qs=dev(qs), ds=dev(ds.view(np.int32)),
+                         y_gate=yg, y_up=yu)
+    q8.q8_check()
+    for blob, y, nm in ((wg, yg, "gate"), (wu, yu, "up")):
+        yr, ar = oracle.gemv(blob, nf, k, qs, ds)
+        _assert_exact(host(y), yr, ar, f"gate_up {nm} {nf}x{k}")
+
+
+# ---------------------------------------------------------------------------
+# a few tokens: the small-batch kernel (int8 MMA up to 8 tokens, f16 beyond)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("t", [1, 2, 5, 8, 9, 12, 16])
+@pytest.mark.parametrize("n,k", [(300, 1024), (37, 256), (129, 512)])
+def test_gemv_batched_full_range_bit_exact(q8, n, k, t):
+    blob = _unit_weights(30, n, k)
+    qs, ds = _unit_plane(30, t, k, rows_pad=128)
+    y = nan_f32(t, n)
+    q8.q8_0_gemv_batched(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), t, y)
+    q8.q8_check()
+    yr, ar = oracle.gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+    _assert_exact(host(y), yr, ar, f"gemv_batched {n}x{k} t={t}")
+
+
+# ---------------------------------------------------------------------------
+# GEMM: every dispatch branch
+# ---------------------------------------------------------------------------
+GEMM_CASES = [
+    (300, 1024, 17),    # 16-token slices, a one-token last slice
+    (129, 1024, 40),    # slices
+    (300, 512, 64),     # slices, the last small-batch count
+    (512, 1024, 65),    # tcgen05, split over k (few tiles)
+    (256, 1024, 300),   # tcgen05, split over k
+    (2048, 1024, 1536), # tcgen05, unsplit (16 x 8 tiles)
+    (1000, 256, 400),   # tcgen05, short k
+    (300, 96, 40),      # generic kernel (k/32 = 3)
+    (77, 128, 100),     # generic kernel (k/32 = 4)
+]
+
+
+@pytest.mark.parametrize("entry", ["q8_0_gemm", "q8_0_gemm_mma"])
+@pytest.mark.parametrize("n,k,t", GEMM_CASES)
+def test_gemm_full_range_bit_exact(q8, n, k, t, entry):
+    if entry == "q8_0_gemm_mma" and (k // 32) % 8:
+        pytest.skip("the legacy kernel needs k/32 % 8 == 0")
+    blob = _unit_weights(40, n, k)
+    qs, ds = _unit_plane(40, t, k, rows_pad=((t + 127) // 128) * 128)
+    y = nan_f32(t, n)
+    getattr(q8, entry)(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), t, y)
+    q8.q8_check()
+    yr, ar = oracle.gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+    _assert_exact(host(y), yr, ar, f"{entry} {n}x{k} t={t}")
+
+
+# ---------------------------------------------------------------------------
+# asymmetric 4-bit weights: unit d, min 0 or 1, nibbles 0..15 (min term from ssum)
+# ---------------------------------------------------------------------------
+def _unit_q4a(seed, n, k):
+    g = syn.rng(92, seed, n, k)
+    nb = k // 32
+    nib = g.integers(0, 16, size=(n, k)).astype(np.uint8)
+    for r in range(n):
+        p = r % 4
+        if p == 1:
+            nib[r] = 15
+        elif p == 2:
+            nib[r] = np.where(np.arange(k) % 2 == 0, 15, 0)
+        elif p == 3:
+            nib[r] = 0
+    d16 = np.full((n, nb), F16_ONE, np.uint16)
+    m16 = np.where(g.integers(0, 2, size=(n, nb)) == 1, F16_ONE, 0).astype(np.uint16)
+    return syn.pack_q4a(d16, m16, nib)
+
+
+@pytest.mark.parametrize("shift", [0, 3, 4, 5])
+@pytest.mark.parametrize("n,k", [(300, 1024), (77, 4096), (4, 128)])
+def test_q4a_gemv_full_range_bit_exact(q8, n, k, shift):
+    blob = _unit_q4a(1, n, k)
+    qs, ds = _unit_plane(50, 1, k, shift=shift)
+    y = nan_f32(n)
+    q8.q4a_gemv(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), y)
+    q8.q8_check()
+    yr, ar = oracle.q4a_gemv(blob, n, k, qs, ds)
+    _assert_exact(host(y), yr, ar, f"q4a_gemv {n}x{k}")
+
+
+@pytest.mark.parametrize("t", [2, 7, 9, 16])
+@pytest.mark.parametrize("n,k", [(300, 1024), (33, 4096)])
+def test_q4a_gemv_batched_full_range_bit_exact(q8, n, k, t):
+    blob = _unit_q4a(2, n, k)
+    qs, ds = _unit_plane(51, t, k, rows_pad=128)
+    y = nan_f32(t, n)
+    q8.q4a_gemv_batched(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), t, y)
+    q8.q8_check()
+    yr, ar = oracle.q4a_gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+    _assert_exact(host(y), yr, ar, f"q4a_gemv_batched {n}x{k} t={t}")
