@@ -176,6 +176,16 @@ def max_over_ranks(torch, values, device):
     return [float(x) for x in t.tolist()]
 
 
+GRAPH_STEPS = 60  # steps per timed CUDA graph (rounded to a multiple of the weight copies)
+
+
+def hold_device(torch, launches):
+    """Keep the stream busy (a device-side sleep, before the start event) while
+    the host enqueues `launches` graph replays, so that the timed region
+    measures the device and not the host's launch latency."""
+    torch.cuda._sleep(int(2_000_000 + 40_000 * launches))  # cycles: ~1 ms + ~20 us per replay
+
+
 def gpu_smi_id(torch, dev):
     try:
         return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -243,8 +253,8 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     for i in range(warmup):
         step(i)
     q8p.q8_check()
-    # The headline region replays a CUDA graph holding one decode step per
-    # weight copy: a step's four launches are a few microseconds of GPU work
+    # The headline region replays CUDA graphs of decode steps (the weight
+    # copies in turn): a step's launches are a few microseconds of GPU work
     # each, so issuing them one by one from the host measures the host.  The
     # captured launches keep their programmatic-dependent-launch edges, and
     # nothing is recorded between them (an event between two launches would
@@ -262,75 +272,100 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     grouped_c = [q8p.q8_0_gemv_grouped([(wset[0], DECODE_SHAPES[0][0], ys[0]), (wset[1], DECODE_SHAPES[1][0], ys[1])],
                                        7168, *planes[7168], stream=cap, bind=True) for wset in ws]
 
-    def steps_c(fused=True):
+    def steps_main(n):  # the fused k = 7168 GEMV alone, n launches on weight copies 0, 1, ... in turn
+        for i in range(n):
+            gemvs_c[i % copies][0]()
+
+    def steps_part(n, fused=True):  # n decode steps on weight copies 0, 1, ... in turn
         side.wait_stream(cap)  # fork
-        for i in range(copies):
+        for i in range(n):
+            c = i % copies
             if fused:
-                gemvs_c[i][0]()
+                gemvs_c[c][0]()
             else:
                 quant_main()
-                grouped_c[i]()
+                grouped_c[c]()
             quant_side()
-            gemvs_c[i][1]()
+            gemvs_c[c][1]()
         cap.wait_stream(side)  # join
 
+    def capture(fn):
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_, stream=cap):
+            fn()
+        return g_
+
+    # K timed steps = reps replays of a graph of G steps (G a multiple of the
+    # copy count, so the weight copies keep rotating), then one replay of a
+    # graph of the remaining K mod G steps: every timed step is a graph
+    # replay, whatever K is.  The host enqueues the replays behind a device
+    # sleep (outside the events), so no host launch latency lands inside the
+    # timed region.
+    G = copies * max(1, GRAPH_STEPS // copies)
+    reps, rem = divmod(steps, G)
     cap.wait_stream(stream)
-    steps_c()  # the same launches once outside the capture
-    steps_c(False)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=cap):
-        steps_c()
-    graph_two = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_two, stream=cap):
-        steps_c(False)
+    steps_part(copies)  # the same launches once outside the capture
+    steps_part(copies, False)
+    graph = capture(lambda: steps_part(G))
+    graph_rem = capture(lambda: steps_part(rem)) if rem else None
+    graph_two = capture(lambda: steps_part(G, False))
+    graph_two_rem = capture(lambda: steps_part(rem, False)) if rem else None
+    graph_main = capture(lambda: steps_main(G))
+    graph_main_rem = capture(lambda: steps_main(rem)) if rem else None
     stream.wait_stream(cap)
-    reps, rem = divmod(steps, copies)
+
+    def timed(g_full, g_rem, sample=False):
+        g_full.replay()  # warm
+        torch.cuda.synchronize(dev)
+        if sample:
+            sampler.start()
+            sampler.mark(True)
+        hold_device(torch, reps + (g_rem is not None))
+        t0.record(stream)
+        for _ in range(reps):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        if sample:
+            sampler.mark(False)
+        q8p.q8_check()
+        return t0.elapsed_time(t1)
 
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    sampler.start()
-    sampler.mark(True)
-    t0.record(stream)
-    for _ in range(reps):
-        graph.replay()
-    for i in range(rem):
-        step(warmup + i)
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    sampler.mark(False)
+    ms = timed(graph, graph_rem, sample=True)
     clocks = sampler.stop()
-    q8p.q8_check()
-    ms = t0.elapsed_time(t1)
-    for _ in range(3):
-        graph_two.replay()
-    t0.record(stream)
-    for _ in range(reps):
-        graph_two.replay()
-    t1.record(stream)
+    ms_two = timed(graph_two, graph_two_rem) / steps
+    # The roofline's kernel duration: the fused k = 7168 GEMV alone, K launches
+    # back to back from graphs built like the step's (one launch per weight
+    # copy in turn, programmatic dependent launch between them, as in the
+    # step), CUDA events around the K launches, the mean per launch.
+    kern_ms = timed(graph_main, graph_main_rem) / steps
+    # The same launches each bracketed by its own events (no overlap with its
+    # neighbours): reported beside it as the isolated launch time.
+    nev = min(steps, 4 * copies)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nev)]
     torch.cuda.synchronize(dev)
-    q8p.q8_check()
-    ms_two = t0.elapsed_time(t1) / (reps * copies) if reps else float("nan")
-    # The roofline's kernel duration: the same K steps again, with events
-    # around every launch of the big GEMV (each launch then runs unoverlapped).
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    torch.cuda.synchronize(dev)
-    for i in range(steps):
+    for i in range(nev):
         step(warmup + i, evs[i])
     torch.cuda.synchronize(dev)
     q8p.q8_check()
-    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    iso_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
 
     # end to end through the public API with host buffers (weights resident).
     # A serving loop records its step once -- the host-to-device copy of the
     # inputs from pinned memory, the library calls, the device-to-host copy of
-    # the outputs -- as a CUDA graph and replays it every step.  It keeps one
-    # step in flight: it enqueues step i, then waits for step i-1 and reads its
-    # outputs, so the host's launch and wake-up overlap the GPU's work; host
-    # buffers alternate between steps, so a step never writes the buffer the
-    # host is reading (`e2e_s`).  `e2e_serial_s` waits for every step before
-    # enqueuing the next; `e2e_eager_s` also issues the step call by call.
-    xh = [x_all.cpu().pin_memory() for _ in range(2)]
-    yh = [torch.empty(y_all.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    # the outputs -- as a CUDA graph and replays it every step.  It keeps two
+    # steps in flight: it enqueues step i, then waits for step i-2 and reads
+    # its outputs, so the host's launch and wake-up overlap the GPU's work;
+    # the three host buffers rotate between steps, so a step never writes the
+    # buffer the host is reading (`e2e_s`).  `e2e_serial_s` waits for every
+    # step before enqueuing the next; `e2e_eager_s` also issues the step call
+    # by call.
+    nbuf = 3
+    xh = [x_all.cpu().pin_memory() for _ in range(nbuf)]
+    yh = [torch.empty(y_all.shape, dtype=torch.float32).pin_memory() for _ in range(nbuf)]
 
     def e2e_body(i, par):  # on the capture streams: the inputs in, one step, the outputs out
         x_all.copy_(xh[par], non_blocking=True)
@@ -344,28 +379,29 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     cap.wait_stream(stream)
     with torch.cuda.stream(cap):
         for i in range(copies):  # once outside the capture
-            e2e_body(i, i % 2)
+            e2e_body(i, i % nbuf)
     stream.wait_stream(cap)
     e2e_graphs = []  # [weight copy][host buffer]
     for i in range(copies):
-        pair = []
-        for par in range(2):
+        row = []
+        for par in range(nbuf):
             gi = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gi, stream=cap):
                 e2e_body(i, par)
-            pair.append(gi)
-        e2e_graphs.append(pair)
+            row.append(gi)
+        e2e_graphs.append(row)
     torch.cuda.synchronize(dev)
-    done = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def e2e_run(n, start):  # one step in flight
+    def e2e_run(n, start):  # up to nbuf - 1 steps in flight
         for j in range(n):
             i = start + j
-            e2e_graphs[i % copies][i % 2].replay()
-            done[i % 2].record(stream)
-            if j > 0:
-                done[(i - 1) % 2].synchronize()  # step i-1's outputs are in yh[(i-1) % 2]
-        done[(start + n - 1) % 2].synchronize()
+            e2e_graphs[i % copies][i % nbuf].replay()
+            done[i % nbuf].record(stream)
+            if j >= nbuf - 1:
+                done[(i - nbuf + 1) % nbuf].synchronize()  # that step's outputs are in yh[(i - nbuf + 1) % nbuf]
+        for j in range(max(0, n - nbuf + 1), n):
+            done[(start + j) % nbuf].synchronize()
 
     def e2e_serial_run(n, start):
         for j in range(n):
@@ -389,9 +425,89 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
         res[name] = time.perf_counter() - e0
         q8p.q8_check()
     e2e_s, e2e_serial_s, e2e_eager_s = res["e2e_s"], res["e2e_serial_s"], res["e2e_eager_s"]
-    return dict(ms=ms, kern_ms=kern_ms, clocks=clocks, e2e_s=e2e_s, e2e_serial_s=e2e_serial_s, e2e_eager_s=e2e_eager_s,
+    return dict(ms=ms, kern_ms=kern_ms, iso_ms=iso_ms, clocks=clocks, e2e_s=e2e_s, e2e_serial_s=e2e_serial_s, e2e_eager_s=e2e_eager_s,
                 copies=copies, ms_two=ms_two,
                 h2d=sum(v.nbytes for v in xs_h.values()), d2h=4 * sum(n for n, _ in DECODE_SHAPES))
+
+
+# ---------------------------------------------------------------------------
+# tiny GEMV (one 256 x 512 projection, batch 1): latency-bound
+# ---------------------------------------------------------------------------
+TINY = dict(n=256, k=512)
+
+
+def tiny_inputs():
+    n, k = TINY["n"], TINY["k"]
+    x = syn.activations(syn.rng(0, 0), 1, k)
+    w = syn.q8_0_weights(syn.rng(0, 1), n, k)[0]
+    return x, w
+
+
+def bytes_tiny():
+    n, k = TINY["n"], TINY["k"]
+    return bytes_quantize(1, k) + bytes_gemv(n, k)
+
+
+def graph_schedule(torch, cap, issue, steps, copies, per_graph=600):
+    """CUDA graphs that together issue steps 0..steps-1 (step i on weight copy
+    i mod copies) and the order to replay them in.  A graph holds at most
+    `per_graph` steps; graphs are shared between runs of steps that start on
+    the same copy."""
+    graphs, order, i = {}, [], 0
+    G = max(1, min(per_graph, steps))
+    while i < steps:
+        ln = min(G, steps - i)
+        key = (i % copies, ln)
+        if key not in graphs:
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_, stream=cap):
+                for j in range(ln):
+                    issue(i + j)
+            graphs[key] = g_
+        order.append(graphs[key])
+        i += ln
+    return order
+
+
+def run_tiny(torch, q8p, steps, warmup, dev):
+    """quantize_q8_0 (1 x 512) -> q8_0_gemv (256 x 512) per step, the weights
+    rotating through copies totalling > 4 x L2, every timed step a graph
+    replay."""
+    n, k = TINY["n"], TINY["k"]
+    x_h, w_h = tiny_inputs()
+    copies = -(-4 * L2_BYTES // w_h.nbytes)
+    wall = torch.from_numpy(w_h).to(dev).repeat(copies)
+    ws = [wall[i * w_h.nbytes:(i + 1) * w_h.nbytes] for i in range(copies)]
+    x = torch.from_numpy(x_h).to(dev)
+    plane = q8p.empty_plane(1, k, dev)
+    y = torch.empty(n, dtype=torch.float32, device=dev)
+    cap = torch.cuda.Stream(dev)
+    quant = q8p.quantize_q8_0(x, *plane, stream=cap, bind=True)
+    gemvs = [q8p.q8_0_gemv(w, n, k, *plane, y, stream=cap, bind=True) for w in ws]
+
+    def issue(i):
+        quant()
+        gemvs[i % copies]()
+
+    stream = torch.cuda.current_stream(dev)
+    cap.wait_stream(stream)
+    for i in range(max(warmup, 1)):
+        issue(i)
+    q8p.q8_check()
+    order = graph_schedule(torch, cap, issue, steps, copies)
+    stream.wait_stream(cap)
+    for g_ in order[:1]:
+        g_.replay()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_device(torch, len(order))
+    t0.record(stream)
+    for g_ in order:
+        g_.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    q8p.q8_check()
+    return dict(us=1e3 * t0.elapsed_time(t1) / steps, copies=copies, steps=steps)
 
 
 # ---------------------------------------------------------------------------
@@ -582,6 +698,7 @@ def run_shared(torch, q8p, steps, warmup, dev):
         graph.replay()
         torch.cuda.synchronize(dev)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_device(torch, reps)
         t0.record(stream)
         for _ in range(reps):
             graph.replay()
@@ -668,11 +785,9 @@ def run_layers(torch, q8p, steps, warmup, dev, layer_count=LAYERS["layers"]):
     d, nf, eps = L["d"], L["nf"], L["eps"]
     g = syn.rng(4, 0)
     shapes = [(n, k) for k, ns in layer_groups() for n in ns]  # q k v o gate up down
-    host = [syn.q8_0_weights(syn.rng(4, 0, i), n, k)[0] for i, (n, k) in enumerate(shapes)]
-    head_h = syn.q8_0_weights(syn.rng(4, 0, len(shapes)), L["vocab"], d)[0]
+    host, head_h = stack_weights_host()
     layers = [[torch.from_numpy(w).to(dev) for w in host] for _ in range(L["layers"])]
     head = torch.from_numpy(head_h).to(dev)
-    del host, head_h
     x = torch.from_numpy(syn.activations(g, 1, d)).to(dev)        # hidden state entering each layer
     attn = torch.from_numpy(syn.activations(g, 1, d)).to(dev)     # attention output
     h = torch.from_numpy(syn.activations(g, 1, d)).to(dev)        # hidden state after attention
@@ -733,6 +848,7 @@ def run_layers(torch, q8p, steps, warmup, dev, layer_count=LAYERS["layers"]):
             graph.replay()
         torch.cuda.synchronize(dev)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_device(torch, steps)
         t0.record(stream)
         for _ in range(steps):
             graph.replay()
@@ -745,6 +861,104 @@ def run_layers(torch, q8p, steps, warmup, dev, layer_count=LAYERS["layers"]):
                 launches=len(variants["mixed"]), launches_two=len(variants["two"]),
                 launches_fused=len(variants["fused"]),
                 weight_bytes=sum(w.numel() for w in layers[0]) * L["layers"] + head.numel())
+
+
+# ---------------------------------------------------------------------------
+# layer-stack prefill / small-batch sweep: every projection of the 28-layer
+# stack and the LM head through q8_0_gemm at T tokens
+# ---------------------------------------------------------------------------
+STACK_TOKENS = (16, 512, 2048, 3325)
+
+
+_STACK_HOST = {}
+
+
+def stack_weights_host():
+    """Layer 0's seven projection blobs and the LM head blob (host, generated once)."""
+    if not _STACK_HOST:
+        L = LAYERS
+        shapes = [(n, k) for k, ns in layer_groups() for n in ns]  # q k v o gate up down
+        _STACK_HOST["layer"] = [syn.q8_0_weights(syn.rng(4, 0, i), n, k)[0] for i, (n, k) in enumerate(shapes)]
+        _STACK_HOST["head"] = syn.q8_0_weights(syn.rng(4, 0, len(shapes)), L["vocab"], L["d"])[0]
+    return _STACK_HOST["layer"], _STACK_HOST["head"]
+
+
+def stack_shapes():
+    """(name, rows n, width k) of one layer's projections, in call order."""
+    L = LAYERS
+    d, nf = L["d"], L["nf"]
+    return [("q", L["q"], d), ("k", L["kv"], d), ("v", L["kv"], d), ("o", d, d), ("gate", nf, d), ("up", nf, d),
+            ("down", d, nf)]
+
+
+def bytes_stack_call(t, n, k):
+    # weights, the plane rows read, the f32 outputs
+    return n * (k // 32) * 34 + t * (k + 4 * (k // 32)) + 4 * t * n
+
+
+def run_stack_tokens(torch, q8p, reps, warmup, dev, tokens=STACK_TOKENS, layer_count=LAYERS["layers"]):
+    """Per token count T: one pass = every projection of every layer and the
+    LM head, each one q8_0_gemm call (28 x 7 + 1 = 197 calls) on a q8_0 plane
+    of T tokens per activation width (3584 and 18944), quantized on the GPU
+    from seeded f32 ~N(0,1).  Timed two ways: `reps` whole passes between one
+    pair of CUDA events (the stack time), and one pass with events around
+    every call (per-shape time, averaged over the layers).  Layers 1..27 are
+    device copies of layer 0's matrices (distinct memory; 7.5 GB of weights
+    per pass)."""
+    L = LAYERS
+    d, nf, V = L["d"], L["nf"], L["vocab"]
+    shapes = stack_shapes()
+    host, head_h = stack_weights_host()
+    layers = [[torch.from_numpy(w).to(dev) for w in host] for _ in range(layer_count)]
+    head = torch.from_numpy(head_h).to(dev)
+    tmax = max(tokens)
+    g = syn.rng(4, 1)
+    planes = {}
+    for k in (d, nf):
+        x = torch.from_numpy(syn.activations(g, tmax, k)).to(dev)
+        planes[k] = q8p.empty_plane(q8p.q8_plane_rows(tmax), k, dev)
+        q8p.quantize_q8_0(x, *planes[k])
+        del x
+    all_shapes = shapes + [("head", V, d)]
+    ws_bytes = max(q8p.q8_0_gemm_workspace_bytes(n, T, k) for T in tokens for (_, n, k) in all_shapes)
+    ws = torch.empty(max(ws_bytes, 1024), dtype=torch.uint8, device=dev)
+    Y = torch.empty(tmax * V, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for T in tokens:
+        calls = []
+        for lw in layers:
+            for (name, n, k), w in zip(shapes, lw):
+                calls.append((name, q8p.q8_0_gemm(w, n, k, *planes[k], T, Y, workspace=ws, bind=True)))
+        calls.append(("head", q8p.q8_0_gemm(head, V, d, *planes[d], T, Y, workspace=ws, bind=True)))
+        for _ in range(max(1, warmup // 3)):
+            for _, c in calls:
+                c()
+        q8p.q8_check()
+        torch.cuda.synchronize(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_device(torch, 8 * len(calls))
+        t0.record(stream)
+        for _ in range(reps):
+            for _, c in calls:
+                c()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        q8p.q8_check()
+        stack_ms = t0.elapsed_time(t1) / reps
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+        hold_device(torch, 8 * len(calls))
+        for (_, c), (a, b) in zip(calls, evs):
+            a.record(stream)
+            c()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        q8p.q8_check()
+        per = {}
+        for (name, _), (a, b) in zip(calls, evs):
+            per.setdefault(name, []).append(a.elapsed_time(b))
+        out[T] = dict(stack_ms=stack_ms, per_ms={nm: statistics.mean(v) for nm, v in per.items()}, reps=reps)
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -765,6 +979,133 @@ def oracle_decode_sample(budget_s):
             break
     return dict(value=decode_bytes() * reps / el / 1e9, unit="GB/s", cores=oracle.num_threads(), kind="oracle",
                 sample=f"{reps} full decode steps (quantize + 3 GEMVs of the sweep) in {el:.1f} s")
+
+
+def _oracle_time(fn, budget_s):
+    """Mean wall time of fn() over repeated calls filling about budget_s (at least one call)."""
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return el / reps, reps, el
+
+
+def oracle_leg_samples(budget_s, legs):
+    """cpu_baseline objects of the non-headline legs: the oracle as it stands,
+    timed on the host cores, each on the leg's own inputs or a stated slice
+    of them, the rate extrapolated linearly to the leg's whole workload."""
+    import oracle
+
+    cores = oracle.num_threads()
+    out = {}
+
+    def obj(value, unit, sample):
+        return dict(value=round(value, 4), unit=unit, cores=cores, kind="oracle", sample=sample)
+
+    if "tiny" in legs:
+        n, k = TINY["n"], TINY["k"]
+        x, w = tiny_inputs()
+        dt, reps, el = _oracle_time(lambda: oracle.gemv(w, n, k, *oracle.quantize(x)), budget_s)
+        out["tiny"] = obj(bytes_tiny() / dt / 1e9, "GB/s", f"{reps} full steps (quantize 1x{k} + GEMV {n}x{k}) in "
+                                                           f"{el:.1f} s")
+    if "shared" in legs:
+        d, ns, eps = SHARED["d"], SHARED["ns"], SHARED["eps"]
+        g = syn.rng(2, 0)
+        x, nw = syn.activations(g, 1, d), syn.uniform(g, d, 0.5, 1.5)
+        wb = [syn.q8_0_weights(syn.rng(2, 1 + i), n, d)[0] for i, n in enumerate(ns)]
+
+        def shared_step():
+            y = oracle.rmsnorm(x, nw, eps).astype(np.float32)
+            qs, ds = oracle.quantize(y)
+            for w, n in zip(wb, ns):
+                oracle.gemv(w, n, d, qs, ds)
+        dt, reps, el = _oracle_time(shared_step, budget_s)
+        out["shared"] = obj(bytes_shared(fused=True) / dt / 1e9, "GB/s",
+                            f"{reps} full steps (RMSNorm, quantize, 4 GEMVs) in {el:.1f} s")
+    if "prefill" in legs:
+        T, d, nf, eps = PREFILL["tokens"], PREFILL["d"], PREFILL["nf"], PREFILL["eps"]
+        x, w, wg, wu, wd = prefill_inputs()
+        ts = 4
+        ti = np.arange(ts)
+
+        def chain():
+            qa = oracle.quantize(oracle.rmsnorm(x[:ts], w, eps).astype(np.float32))
+            gt = oracle.gemm(wg, nf, d, *qa, t_idx=ti)[0].astype(np.float32)
+            ut = oracle.gemm(wu, nf, d, *qa, t_idx=ti)[0].astype(np.float32)
+            qb = oracle.quantize(oracle.swiglu(gt, ut).astype(np.float32))
+            oracle.gemm(wd, d, nf, *qb, t_idx=ti)
+        dt, reps, el = _oracle_time(chain, budget_s)
+        ops = 3 * ops_gemm(ts, nf, d)
+        out["prefill"] = obj(ops / dt / 1e12, "TOPS",
+                             f"{reps} chains on the first {ts} of {T} tokens (rmsnorm, gate/up, swiglu, down, all rows) "
+                             f"in {el:.1f} s; int8-op rate extrapolated linearly to {T} tokens "
+                             f"(chain ~{dt * T / ts:.0f} s)")
+    if "layers" in legs:
+        L = LAYERS
+        d, nf, eps = L["d"], L["nf"], L["eps"]
+        shapes = stack_shapes()
+        wb, head = stack_weights_host()
+        g = syn.rng(4, 0)
+        x, attn, h = (syn.activations(g, 1, d) for _ in range(3))
+        nw = syn.uniform(g, d, 0.5, 1.5)
+        hrows = L["vocab"] // 16
+        head_s = head[: hrows * (d // 32) * 34]
+
+        def layer():
+            qa = oracle.quantize(oracle.rmsnorm(x, nw, eps).astype(np.float32))
+            for (_, n, k), w in zip(shapes[:3], wb[:3]):
+                oracle.gemv(w, n, k, *qa)
+            oracle.gemv(wb[3], d, d, *oracle.quantize(attn))
+            qh = oracle.quantize(oracle.rmsnorm(h, nw, eps).astype(np.float32))
+            gt = oracle.gemv(wb[4], nf, d, *qh)[0].astype(np.float32)[None]
+            ut = oracle.gemv(wb[5], nf, d, *qh)[0].astype(np.float32)[None]
+            oracle.gemv(wb[6], d, nf, *oracle.quantize(oracle.swiglu(gt, ut).astype(np.float32)))
+        dl, rl, el1 = _oracle_time(layer, budget_s * 0.7)
+        dh, rh, el2 = _oracle_time(lambda: oracle.gemv(head_s, hrows, d, *oracle.quantize(x)), budget_s * 0.3)
+        tok = L["layers"] * dl + 16 * dh
+        out["layers"] = obj(bytes_layer_stack(LAYER_FUSED) / tok / 1e9, "GB/s",
+                            f"{rl} passes of one layer (producers + 7 GEMVs) in {el1:.1f} s and {rh} passes of the LM "
+                            f"head's first {hrows} rows in {el2:.1f} s; extrapolated to {L['layers']} layers + the "
+                            f"whole head (~{tok:.2f} s per token)")
+    for T in legs.get("stack", ()):
+        L = LAYERS
+        d, V = L["d"], L["vocab"]
+        shapes = stack_shapes() + [("head", V, d)]
+        wl_, hd_ = stack_weights_host()
+        wb = list(wl_) + [hd_]
+        ts, rows = min(T, 4), 256
+        g = syn.rng(4, 1)
+        pl = {k: oracle.quantize(syn.activations(g, ts, k)) for k in (d, L["nf"])}
+        ni = np.arange(rows)
+        times = []
+        for (_, n, k), w in zip(shapes, wb):
+            dt, _, _ = _oracle_time(lambda: oracle.gemm(w, n, k, *pl[k], t_idx=np.arange(ts), n_idx=ni),
+                                    budget_s / len(shapes))
+            times.append(dt * (T / ts) * (n / rows))
+        full = L["layers"] * sum(times[:-1]) + times[-1]
+        ops = L["layers"] * sum(ops_gemm(T, n, k) for _, n, k in shapes[:-1]) + ops_gemm(T, V, d)
+        byts = L["layers"] * sum(bytes_stack_call(T, n, k) for _, n, k in shapes[:-1]) + bytes_stack_call(T, V, d)
+        samp = (f"each projection shape timed on {ts} tokens x its first {rows} rows, extrapolated linearly to "
+                f"{T} tokens x all rows, 28 layers + LM head (~{full:.0f} s per pass)")
+        out[f"stack_{T}"] = (obj(byts / full / 1e9, "GB/s", samp) if T <= 16 else obj(ops / full / 1e12, "TOPS", samp))
+    if "small" in legs:
+        n, k, t = SMALL["n"], SMALL["k"], SMALL["tokens"]
+        w = syn.q8_0_weights(syn.rng(4, 1), n, k)[0]
+        qs, ds = oracle.quantize(syn.activations(syn.rng(4, 0), t, k, sigma=1.5, outlier_frac=0.01))
+        rows = 768
+        dt, reps, el = _oracle_time(lambda: oracle.gemm(w, n, k, qs, ds, n_idx=np.arange(rows)), budget_s)
+        out["small"] = obj(bytes_small(n, k, t) / (dt * n / rows) / 1e9, "GB/s",
+                           f"{reps} passes over the first {rows} of {n} rows, {t} tokens, in {el:.1f} s; "
+                           "extrapolated linearly to all rows")
+    if "asym" in legs:
+        n, k = ASYM["n"], ASYM["k"]
+        w = syn.q4a_weights(syn.rng(5, 1), n, k)[0]
+        qs, ds = oracle.quantize(syn.activations(syn.rng(5, 0), 1, k, sigma=1.5, outlier_frac=0.01))
+        dt, reps, el = _oracle_time(lambda: oracle.q4a_gemv(w, n, k, qs, ds), budget_s)
+        out["asym"] = obj(bytes_q4a_gemv(n, k) / dt / 1e9, "GB/s", f"{reps} full q4a_gemv calls in {el:.1f} s")
+    return out
 
 
 def reference_arm(args):
@@ -835,9 +1176,14 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--layer-count", type=int, default=LAYERS["layers"],
                     help="layers of the layer-stack leg (a shorter stack for profiling runs)")
-    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "small", "asym", "shared", "layers"],
+    ap.add_argument("--workload", default="all",
+                    choices=["all", "decode", "prefill", "small", "asym", "shared", "layers", "tiny", "stack"],
                     help="decode and/or prefill legs (profiling runs select one)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--cpu-leg-budget", type=float, default=1.5,
+                    help="seconds of oracle time for each other leg's cpu_baseline")
+    ap.add_argument("--stack-tokens", default=",".join(str(t) for t in STACK_TOKENS),
+                    help="token counts of the layer-stack sweep through q8_0_gemm")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -862,9 +1208,18 @@ def main():
         torch.distributed.barrier()
     q8p.lib()
 
-    cpu = None
-    if rank == 0:  # oracle baseline before any GPU work is timed (host cores only)
-        cpu = oracle_decode_sample(args.cpu_budget)
+    wl = args.workload
+    stack_tokens = tuple(int(v) for v in args.stack_tokens.split(",") if v)
+    cpu, cpu_legs = None, {}
+    if rank == 0:  # oracle baselines before any GPU work is timed (host cores only)
+        if wl in ("all", "decode"):
+            cpu = oracle_decode_sample(args.cpu_budget)
+        legs = {k: True for k in ("tiny", "shared", "small", "asym", "layers") if wl in ("all", k)}
+        if wl == "all" and not args.no_prefill or wl == "prefill":
+            legs["prefill"] = True
+        if wl in ("all", "stack"):
+            legs["stack"] = stack_tokens
+        cpu_legs = oracle_leg_samples(args.cpu_leg_budget, legs)
 
     sampler = ClockSampler(gpu_smi_id(torch, dev))
     if world > 1:
@@ -898,17 +1253,30 @@ def main():
                          args.warmup, dev,
                          args.layer_count)
 
+    tiny = None
+    if args.workload in ("all", "tiny"):
+        tiny = run_tiny(torch, q8p, args.steps, args.warmup, dev)
+
+    stk = None
+    if args.workload in ("all", "stack"):
+        stk = run_stack_tokens(torch, q8p, 3 if args.workload == "all" else max(1, min(args.steps, 20)), args.warmup,
+                               dev, stack_tokens, args.layer_count)
+
     if world > 1:  # every duration becomes the slowest rank's (same legs on every rank)
-        vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"]]
-                 if dec else [])
+        vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"],
+                  dec["iso_ms"]] if dec else [])
                 + (list(pre.values()) if pre else [])
                 + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else [])
                 + ([lay["ms"], lay["ms_two"], lay["ms_fused"]] if lay else [])
-                + ([shr["us"], shr["us_two"]] if shr else []))
+                + ([shr["us"], shr["us_two"]] if shr else [])
+                + ([tiny["us"]] if tiny else [])
+                + ([v for T in sorted(stk) for v in [stk[T]["stack_ms"]] + [stk[T]["per_ms"][nm] for nm in
+                                                                             sorted(stk[T]["per_ms"])]] if stk else []))
         red = max_over_ranks(torch, vals, dev)
         if dec:
-            dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"] = red[:6]
-            red = red[6:]
+            (dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"],
+             dec["iso_ms"]) = red[:7]
+            red = red[7:]
         if pre:
             pre = dict(zip(pre.keys(), red[:len(pre)]))
             red = red[len(pre):]
@@ -920,6 +1288,13 @@ def main():
             lay["ms"], lay["ms_two"], lay["ms_fused"] = red.pop(0), red.pop(0), red.pop(0)
         if shr:
             shr["us"], shr["us_two"] = red.pop(0), red.pop(0)
+        if tiny:
+            tiny["us"] = red.pop(0)
+        if stk:
+            for T in sorted(stk):
+                stk[T]["stack_ms"] = red.pop(0)
+                for nm in sorted(stk[T]["per_ms"]):
+                    stk[T]["per_ms"][nm] = red.pop(0)
 
     if rank != 0:
         if world > 1:
@@ -942,7 +1317,10 @@ def main():
                          "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
                          "traffic": NCU_TRAFFIC_BYTES["gemv_fused 12288x7168+96x7168"],
-                         "algorithmic_bytes": big, "avg_launch_us": round(dec["kern_ms"] * 1e3, 3)},
+                         "algorithmic_bytes": big, "avg_launch_us": round(dec["kern_ms"] * 1e3, 3),
+                         "timing": "the fused GEMV alone, K launches back to back from CUDA graphs (weight copies "
+                                   "in turn, programmatic dependent launch as in the step), CUDA events around them",
+                         "isolated_launch_us": round(dec["iso_ms"] * 1e3, 3)},
             "two_launch": {"calls": "quantize_q8_0 (k = 7168) -> q8_0_gemv_grouped, the k = 128 chain unchanged",
                            "ms_per_step": round(dec["ms_two"], 5),
                            "gbs": round(world * decode_bytes() / (dec["ms_two"] / 1e3) / 1e9, 2)},
@@ -950,8 +1328,8 @@ def main():
             "e2e": {"value": round(world * step_bytes * args.steps / dec["e2e_s"] / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"],
                     "launch": "per step: one CUDA graph replay (pinned-memory copy in, the library calls, copy out; "
-                              "recorded once); one step in flight: the host reads step i-1's outputs after enqueuing "
-                              "step i (host buffers alternate)",
+                              "recorded once); two steps in flight: the host reads step i-2's outputs after "
+                              "enqueuing step i (three host buffers rotate)",
                     "serial_value": round(world * step_bytes * args.steps / dec["e2e_serial_s"] / 1e9, 2),
                     "eager_value": round(world * step_bytes * args.steps / dec["e2e_eager_s"] / 1e9, 2)},
             "clocks": dec["clocks"],
@@ -983,6 +1361,7 @@ def main():
                          "ms_per_step": pobj["ms_per_chain"],
                          "config": {"workload": pobj["workload"], "l2": pobj["l2"], "parallelism": "replicas"},
                          "roofline": pobj["roofline_gemm"], "gpu_launches": 5 * args.steps})
+        pobj["cpu_baseline"] = cpu_legs.get("prefill")
         line["prefill"] = pobj
     if small is not None:
         n, k, t = SMALL["n"], SMALL["k"], SMALL["tokens"]
@@ -1002,6 +1381,7 @@ def main():
                          "ms_per_step": round(small["us"] / 1e3, 5),
                          "config": {"workload": sobj["workload"], "l2": sobj["l2"], "parallelism": "replicas"},
                          "roofline": sobj["roofline"], "gpu_launches": 2 * args.steps})
+        sobj["cpu_baseline"] = cpu_legs.get("small")
         line["small_batch"] = sobj
     if asym is not None:
         n, k = ASYM["n"], ASYM["k"]
@@ -1021,6 +1401,7 @@ def main():
                          "ms_per_step": round(asym["us"] / 1e3, 5),
                          "config": {"workload": aobj["workload"], "l2": aobj["l2"], "parallelism": "replicas"},
                          "roofline": aobj["roofline"], "gpu_launches": 2 * args.steps})
+        aobj["cpu_baseline"] = cpu_legs.get("asym")
         line["asym_gemv"] = aobj
     if shr is not None:
         byts = bytes_shared(fused=True)
@@ -1043,6 +1424,7 @@ def main():
                          "config": {"workload": sobj2["workload"], "l2": f"{shr['copies']} weight copies > 4 x L2",
                                     "parallelism": "replicas"},
                          "roofline": sobj2["roofline"], "gpu_launches": shr["steps"]})
+        sobj2["cpu_baseline"] = cpu_legs.get("shared")
         line["shared_activation"] = sobj2
     if lay is not None:
         L = dict(LAYERS, layers=args.layer_count)
@@ -1076,7 +1458,68 @@ def main():
                                     "l2": f"{lay['weight_bytes'] / 1e9:.2f} GB of weights per token > L2",
                                     "parallelism": "replicas"},
                          "roofline": lobj["roofline"], "gpu_launches": lay["launches"] * args.steps})
+        lobj["cpu_baseline"] = cpu_legs.get("layers")
         line["layer_stack"] = lobj
+    if tiny is not None:
+        n, k = TINY["n"], TINY["k"]
+        gbs = bytes_tiny() / (tiny["us"] / 1e6) / 1e9
+        tobj = {"workload": f"tiny GEMV b=1: quantize_q8_0 1x{k} -> q8_0_gemv {n}x{k} (weights d~U(0.002,0.02), "
+                            "activation f32 ~N(0,1), seed 0)",
+                "us_per_step": round(tiny["us"], 3), "gbs": round(gbs, 2), "algorithmic_bytes": bytes_tiny(),
+                "launches_per_step": 2,
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(gbs / peaks["hbm_gbs"], 5),
+                             "note": "139 KB per step: bound by two launches' latency, not by bandwidth"},
+                "launch": f"CUDA graphs of up to 600 steps replayed; weights rotate through {tiny['copies']} copies "
+                          "(> 4 x L2)",
+                "cpu_baseline": cpu_legs.get("tiny")}
+        if args.workload == "tiny":
+            line.update({"value": round(world * gbs, 2), "unit": "GB/s", "ms_per_step": round(tiny["us"] / 1e3, 6),
+                         "config": {"workload": tobj["workload"], "l2": tobj["launch"], "parallelism": "replicas"},
+                         "roofline": tobj["roofline"], "gpu_launches": 2 * args.steps,
+                         "cpu_baseline": tobj["cpu_baseline"]})
+        line["tiny"] = tobj
+    if stk is not None:
+        L = dict(LAYERS, layers=args.layer_count)
+        shapes = stack_shapes() + [("head", L["vocab"], L["d"])]
+        sw = {}
+        for T in sorted(stk):
+            r = stk[T]
+            ops = L["layers"] * sum(ops_gemm(T, n, k) for _, n, k in shapes[:-1]) + ops_gemm(T, *shapes[-1][1:])
+            byts = (L["layers"] * sum(bytes_stack_call(T, n, k) for _, n, k in shapes[:-1])
+                    + bytes_stack_call(T, *shapes[-1][1:]))
+            per = {}
+            for nm, n, k in shapes:
+                ms_ = r["per_ms"][nm]
+                per[f"{nm} {n}x{k}"] = {"ms": round(ms_, 4), "tops": round(ops_gemm(T, n, k) / ms_ / 1e9, 2),
+                                        "gbs": round(bytes_stack_call(T, n, k) / ms_ / 1e6, 1)}
+            tops = ops / (r["stack_ms"] / 1e3) / 1e12
+            gbs = byts / (r["stack_ms"] / 1e3) / 1e9
+            if T <= 16:
+                roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(gbs / peaks["hbm_gbs"], 4)}
+            else:
+                roof = {"bound": "tensor", "achieved": round(tops, 2), "peak": peaks["bf16_tflops_sustained"],
+                        "unit": "TFLOP/s", "frac": round(tops / peaks["bf16_tflops_sustained"], 4),
+                        "peak_note": "sustained dense bf16/f16 tensor peak; the int8 codes run on kind::f16 "
+                                     "(sm_103a has no int8 tcgen05 kind)"}
+            sw[str(T)] = {"tokens": T, "ms_per_pass": round(r["stack_ms"], 4), "tops": round(tops, 2),
+                          "gbs": round(gbs, 1), "int8_ops": ops, "algorithmic_bytes": byts, "roofline": roof,
+                          "per_shape": per, "cpu_baseline": cpu_legs.get(f"stack_{T}"), "passes_timed": r["reps"]}
+        sobj3 = {"workload": f"layer-stack sweep through q8_0_gemm: {L['layers']} layers x (q {L['q']}, k/v {L['kv']}, "
+                             f"o {L['d']}, gate/up {L['nf']} at k={L['d']}; down {L['d']} at k={L['nf']}) + LM head "
+                             f"{L['vocab']}x{L['d']}, one call per projection ({7 * L['layers'] + 1} calls per pass) on "
+                             "one q8_0 plane of T tokens per width",
+                 "tokens": sw,
+                 "launch": "calls issued eagerly behind a device-side sleep; per-shape times from a second pass with "
+                           "CUDA events around every call (mean over layers); 7.5 GB of weights per pass (> L2)"}
+        if args.workload == "stack":
+            top = sw[str(max(stk))]
+            line.update({"value": round(world * top["tops"], 2), "unit": "TOPS", "ms_per_step": top["ms_per_pass"],
+                         "config": {"workload": sobj3["workload"] + f", T={max(stk)}",
+                                    "l2": "7.5 GB of weights per pass > L2", "parallelism": "replicas"},
+                         "roofline": top["roofline"], "cpu_baseline": top["cpu_baseline"]})
+        line["layer_stack_tokens"] = sobj3
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
