@@ -469,12 +469,13 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
                     unsigned int done = 0u;
                     if (lane == 0) {
                         pbuf[ul * 64 + w] = a;
-                        __threadfence_block();
+                        __threadfence_block();            // release this row's value
                         done = atomicAdd(&pcnt[ul], 1u);
+                        __threadfence_block();            // acquire the other rows' values
                     }
                     done = __shfl_sync(Q8_FULL_MASK, done, 0);
                     if (done == 63u) {
-                        __threadfence_block();
+                        __syncwarp();  // orders lane 0's acquire before every lane's reads
                         const float gv = pbuf[ul * 64 + lane], uv = pbuf[ul * 64 + 32 + lane];
                         uint32_t dsw;
                         const int q = q8::q8_encode32(q8::silu_mul(gv, uv), dsw);

@@ -65,6 +65,8 @@ def _load():
         lib.oracle_block_dots.argtypes = [P, I64, I64, P, I64, P]
         lib.oracle_q4a_gemm.argtypes = [P, I64, I64, P, P, P, I64, P, I64, P, P]
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_div_reading_diff.argtypes = [P, I64, I64]
+        lib.oracle_div_reading_diff.restype = ctypes.c_int64
         _lib = lib
         return lib
 
@@ -115,6 +117,15 @@ def quantize(x, rows_pad: int | None = None):
     ds = np.empty((rows_pad, k // QK), dtype=np.uint32)
     _load().oracle_quantize(_ptr(x), rows, k, _ptr(qs), _ptr(ds), rows_pad)
     return qs, ds
+
+
+def div_reading_diff(x) -> int:
+    """Diagnostic: elements of f32 rows x[rows][k] whose q8_0 code would differ if
+    the quantize step were read as rint(x/d) instead of the adopted rint(x*(1/d))."""
+    x = _c(x, np.float32)
+    rows, k = x.shape
+    assert k % QK == 0
+    return int(_load().oracle_div_reading_diff(_ptr(x), rows, k))
 
 
 def unpack_ds(ds):

@@ -155,6 +155,44 @@ static void quantize_block(const float *x, uint16_t *d16, int8_t *q, int16_t *ss
     *ssum = (int16_t)s;
 }
 
+/* Diagnostic, not part of the path: how many elements would get a different
+ * code under the other reading of the quantize step, q = rint(x/d) (one f32
+ * division) instead of the adopted q = rint(x * (1/d)) (a rounded reciprocal,
+ * then a rounded product), both clamped to +-127 with d = amax/127 in f32.
+ * [R51 3.2] prints the product form; the other form is the plain definition
+ * q = rint(x/d).  Returns the count over rows x k elements.                 */
+int64_t oracle_div_reading_diff(const float *x, int64_t rows, int64_t k)
+{
+    int64_t nb = k / QK, count = 0;
+#pragma omp parallel for schedule(static) reduction(+ : count)
+    for (int64_t t = 0; t < rows; t++) {
+        for (int64_t b = 0; b < nb; b++) {
+            const float *xb = x + t * k + b * QK;
+            float amax = 0.0f;
+            for (int j = 0; j < QK; j++) {
+                float a = fabsf(xb[j]);
+                if (a > amax)
+                    amax = a;
+            }
+            float d = amax / 127.0f;
+            if (d == 0.0f)
+                continue; /* both readings give 0 */
+            float di = 1.0f / d;
+            for (int j = 0; j < QK; j++) {
+                float r_mul = rintf(xb[j] * di);
+                float r_div = rintf(xb[j] / d);
+                if (r_mul > 127.0f) r_mul = 127.0f;
+                if (r_mul < -127.0f) r_mul = -127.0f;
+                if (r_div > 127.0f) r_div = 127.0f;
+                if (r_div < -127.0f) r_div = -127.0f;
+                if (r_mul != r_div)
+                    count++;
+            }
+        }
+    }
+    return count;
+}
+
 /* The f32 d of a block (before f16 storage), exported for round-trip pins. */
 float oracle_block_d32(const float *x)
 {

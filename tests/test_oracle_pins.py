@@ -416,3 +416,45 @@ def test_page_byte_accounts():
             if "exact" in e:
                 assert got == e["exact"]
         assert abs(got / 1e6 - e["printed"]) <= e["rel_tol"] * e["printed"], e["what"]
+
+
+# --------------------------------------------------------------------------
+# The x/d reading of the quantize step against the adopted x*(1/d) reading
+# ("54 - r51 - producer-fused A-quantize mode 1", sec. 3.2 prints the product
+# form; the plain definition is q = rint(x/d)).  A diagnostic count, pinned to
+# numpy's IEEE f32 arithmetic, then reported on the workloads' activations.
+# --------------------------------------------------------------------------
+
+def _div_reading_diff_numpy(x):
+    b = x.astype(np.float32).reshape(x.shape[0], -1, 32)
+    d = (np.abs(b).max(-1, keepdims=True) / np.float32(127)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        di = np.where(d != 0, np.float32(1) / d, np.float32(0)).astype(np.float32)
+        q_mul = np.clip(np.rint((b * di).astype(np.float32)), -127, 127)
+        q_div = np.where(d != 0, np.clip(np.rint((b / d).astype(np.float32)), -127, 127), 0)
+    return int((q_mul != q_div).sum())
+
+
+def test_div_reading_diagnostic_matches_numpy():
+    g = syn.rng(95, 0)
+    x = syn.activations(g, 2000, 4096, sigma=1.5, outlier_frac=0.01)
+    got = oracle.div_reading_diff(x)
+    assert got == _div_reading_diff_numpy(x)
+    assert got > 0  # the two readings do differ on some of these 8 M elements
+    # a constant block: x = amax, both readings give exactly 127
+    assert oracle.div_reading_diff(np.full((1, 32), 3.0, np.float32)) == 0
+
+
+def test_div_reading_count_on_the_workloads(capsys):
+    """Elements whose code the other reading would change, per workload
+    activation recipe.  The two forms differ only by an f32 rounding or two,
+    so only values within a few ulp of a half-integer step can change: about
+    one code in a million."""
+    cases = {"decode x (1 x 7168, N(0,1.5), 1% x20)": syn.activations(syn.rng(1, 0), 1, 7168, 1.5, 0.01),
+             "prefill x (3325 x 3584, N(0,1))": syn.activations(syn.rng(3, 0), 3325, 3584),
+             "prefill SwiGLU width (3325 x 18944, N(0,1))": syn.activations(syn.rng(3, 9), 3325, 18944)}
+    for name, x in cases.items():
+        c = oracle.div_reading_diff(x)
+        with capsys.disabled():
+            print(f"\n  x/d vs x*(1/d): {c} of {x.size} codes differ on {name}")
+        assert c <= 4e-6 * x.size
