@@ -362,8 +362,9 @@ Q8_API int q8_0_gemm(const void *w, int64_t n, int64_t k,
  *   which needs no scratch at all).
  *   The entry point itself calls no cudaMalloc/cudaFree or allocating
  *   routine.  Its first call on a device looks up that device's address of
- *   the array (cudaGetSymbolAddress, with the device current); make that
- *   first call before any stream capture.
+ *   the array (cudaGetSymbolAddress, with the device current), and so does
+ *   the first call after the device's context has been replaced (for
+ *   instance by cudaDeviceReset); make those calls before any stream capture.
  *   All calls share the one array and it keeps the last call's contents;
  *   nothing in it needs to start at zero (each call rewrites every byte it
  *   reads), but calls that overlap on the GPU -- different streams, or

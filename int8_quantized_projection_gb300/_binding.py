@@ -377,20 +377,33 @@ def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, workspace=None, stream=None,
     return None
 
 
+_noalloc_devices = set()  # devices on which an eager q8_0_gemm_noalloc call has succeeded
+
+
 def q8_0_gemm_noalloc(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=False):
     """q8_0_gemm whose scratch is the library's fixed device array (no allocation anywhere).
 
     For callers that cannot allocate device memory here; requests larger than
     q8_0_gemm_noalloc_max_bytes() raise Q8Error(Q8_ERR_TOO_BIG).  Calls that overlap
-    on the GPU share that array and race."""
+    on the GPU share that array and race.  The first call on a device looks the
+    array up (a host-side CUDA call), so ``bind=True`` -- the form used to record
+    launches into a CUDA graph -- is refused until one eager call has been made on
+    that device."""
     import torch
 
     _need(w, torch.uint8, "w"), _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds"), _need(y, torch.float32, "y")
     rows_pad = qs.shape[0]
     if w.numel() != n * (k // 32) * 34 or y.numel() < t * n or qs.shape[-1] != k or ds.shape[0] != rows_pad:
         raise ValueError("shape mismatch")
-    return _launch("q8_0_gemm_noalloc", (_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y), _stream(stream)),
-                   bind)
+    dev = y.device.index if y.device.index is not None else torch.cuda.current_device()
+    if bind and dev not in _noalloc_devices:
+        raise RuntimeError("q8_0_gemm_noalloc: make one eager call on this device before binding it (its first call "
+                           "looks up the scratch array's device address, which must not happen inside a stream capture)")
+    out = _launch("q8_0_gemm_noalloc", (_ptr(w), n, k, _ptr(qs), _ptr(ds), t, rows_pad, _ptr(y), _stream(stream)),
+                  bind)
+    if not bind:
+        _noalloc_devices.add(dev)
+    return out
 
 
 def q8_0_gemm_mma(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=False):

@@ -41,8 +41,8 @@ def _deps():
         os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
 
 
-def _compile(src: str, ptxas_v: bool, extra: list[str]) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, ptxas_v: bool, extra: list[str], objdir: str = BUILD) -> tuple[str, str]:
+    obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *NVFLAGS, *extra, "-c", src, "-o", obj]
     if ptxas_v:
         cmd.insert(1, "-Xptxas=-v")
@@ -52,27 +52,34 @@ def _compile(src: str, ptxas_v: bool, extra: list[str]) -> tuple[str, str]:
     return obj, r.stderr
 
 
-def build(force: bool = False, ptxas_v: bool = False, extra: list[str] | None = None, verbose: bool = False) -> str:
-    """Compile and link; skipped when the library is newer than every source."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, ptxas_v: bool = False, extra: list[str] | None = None, verbose: bool = False,
+          lib_path: str | None = None) -> str:
+    """Compile and link; skipped when the library is newer than every source.
+
+    ``lib_path`` builds a separate copy there (with its objects beside it),
+    always from scratch, e.g. with ``extra`` macro definitions; the in-tree
+    library is left alone."""
+    out = lib_path or LIB
+    objdir = os.path.join(os.path.dirname(out), "obj") if lib_path else BUILD
+    os.makedirs(objdir, exist_ok=True)
     extra = list(extra or [])
-    if not force and not ptxas_v and not extra and os.path.exists(LIB):
+    if lib_path is None and not force and not ptxas_v and not extra and os.path.exists(LIB):
         newest = max(os.path.getmtime(p) for p in _deps())
         if os.path.getmtime(LIB) >= newest:
             return LIB
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(lambda s: _compile(s, ptxas_v, extra), srcs))
+        results = list(ex.map(lambda s: _compile(s, ptxas_v, extra, objdir), srcs))
     if verbose or ptxas_v:
         for _, log in results:
             if log.strip():
                 print(log, file=sys.stderr)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -165,6 +165,18 @@ __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
 // the time limit (then raises the flag and the error word).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag)
 {
+    if (Q8_WAIT_LIMIT_NS == 0) {  // a build that gives up at once: one non-blocking test
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        *abort_flag = 1;
+        atomicOr(&g_gemm_err, 1u);
+        return false;
+    }
     if (try_wait(bar, parity)) return true;
     const uint64_t t0 = q8::globaltimer_ns();
     for (;;) {
@@ -184,7 +196,7 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity)
 {
     const uint64_t t0 = q8::globaltimer_ns();
     while (!try_wait(bar, parity)) {
-        if (q8::globaltimer_ns() - t0 > Q8_WAIT_LIMIT_NS) {
+        if (q8::globaltimer_ns() - t0 > Q8_DRAIN_LIMIT_NS) {
             atomicOr(&g_gemm_err, 1u);
             return;
         }
@@ -713,19 +725,44 @@ constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;  // 32 Mi
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[64];  // device address of g_noalloc_scratch, per device ordinal
+void *g_noalloc_ptr[64];      // device address of g_noalloc_scratch, per device ordinal
+CUcontext g_noalloc_ctx[64];  // the context that address belongs to
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the array's name in host code is only a stand-in for it).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+// cuCtxGetCurrent through the runtime's driver entry point (the library does
+// not link libcuda); looked up once.
+CtxGetCurrentFn ctx_get_current_fn()
+{
+    static const CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrentFn>(p);
+        return nullptr;
+    }();
+    return fn;
+}
+
+// Device address of the scratch array on the current device (the array's
+// name in host code is only a stand-in for it).  It is looked up on the first
+// call on a device and again whenever the current context is not the one it
+// was looked up in (after a device reset the module is loaded anew and the
+// array may sit elsewhere).
 int noalloc_scratch(void **out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q8_ERR_DEVICE;
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return Q8_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (!g_noalloc_ptr[dev] || g_noalloc_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return Q8_ERR_CUDA;
         g_noalloc_ptr[dev] = p;
+        g_noalloc_ctx[dev] = ctx;
     }
     *out = g_noalloc_ptr[dev];
     return Q8_OK;

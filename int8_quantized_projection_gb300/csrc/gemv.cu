@@ -424,7 +424,7 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
             // wait bounded): no copy may still write into shared memory once
             // the CTA has exited
             for (uint32_t j = 0; j < static_cast<uint32_t>(kStages); ++j)
-                (void)q8::mbar_wait_bounded(&mybar[(i + j) % kStages], ((i + j) / kStages) & 1u);
+                (void)q8::mbar_wait_bounded(&mybar[(i + j) % kStages], ((i + j) / kStages) & 1u, Q8_DRAIN_LIMIT_NS);
             return;
         }
         const int2 m = mymeta[s];
@@ -877,7 +877,8 @@ gemv_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
             }
             // let every issued stage land (bounded) before the CTA can exit
             for (int j = (i > kSbStages ? i - kSbStages : 0); j < i; ++j)
-                if (!q8::mbar_wait_bounded(&full[j % kSbStages], static_cast<uint32_t>(j / kSbStages) & 1u)) {
+                if (!q8::mbar_wait_bounded(&full[j % kSbStages], static_cast<uint32_t>(j / kSbStages) & 1u,
+                                           Q8_DRAIN_LIMIT_NS)) {
                     atomicOr(&g_gemv_err, 1u);
                     *bad = 1;
                 }

@@ -20,6 +20,13 @@
 #ifndef Q8_WAIT_LIMIT_NS
 #define Q8_WAIT_LIMIT_NS 1000000000ull
 #endif
+// Waits that let a kernel's own copies (and tensor-core work) in flight land
+// before it exits -- on the normal path and after another wait gave up -- have
+// a limit of their own, so that a build with a short main-loop limit still
+// never exits with a copy writing into its shared memory.
+#ifndef Q8_DRAIN_LIMIT_NS
+#define Q8_DRAIN_LIMIT_NS 1000000000ull
+#endif
 
 namespace q8 {
 
@@ -167,11 +174,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; false if the wait
-// ran past `limit_ns`.
+// ran past `limit_ns`.  A limit of 0 (a build that gives up at once) makes
+// the wait one non-blocking test.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t limit_ns = Q8_WAIT_LIMIT_NS)
 {
+    if (limit_ns == 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {

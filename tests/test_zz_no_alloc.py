@@ -69,6 +69,59 @@ def test_noalloc_gemm_two_calls_match_workspace_gemm(q8):
         assert_gemm_close(host(y), yr, ar, f"noalloc gemm {n}x{k} t={t}")
 
 
+def test_noalloc_gemm_unsplit_and_near_its_limit(q8):
+    """Two more shapes on the fixed scratch: one whose tiles fill the GPU (the
+    GEMM runs without a k split and the weight pre-pass takes its wide form),
+    and one whose scratch need is just under the array's size."""
+    import torch
+
+    lib = q8.lib()
+    cap = lib.q8_0_gemm_noalloc_max_bytes()
+    n, k = 4096, 2048
+    t_hi = 65
+    while lib.q8_0_gemm_workspace_bytes(n, t_hi + 64, k) <= cap:
+        t_hi += 64
+    assert cap - lib.q8_0_gemm_workspace_bytes(n, t_hi, k) < 64 * k * 2 + (1 << 20)
+    for seed, (n_, k_, t_) in enumerate([(4096, 1024, 1920), (n, k, t_hi)]):
+        assert lib.q8_0_gemm_workspace_bytes(n_, t_, k_) <= cap
+        blob, qs, ds = _case(10 + seed, n_, k_, t_)
+        bd, qd, dd = dev(blob), dev(qs), dev(ds.view(np.int32))
+        y_ref_gpu = nan_f32(t_, n_)
+        _call_c_abi(q8, "q8_0_gemm", bd, n_, k_, qd, dd, t_, y_ref_gpu)
+        y = nan_f32(t_, n_)
+        _call_c_abi(q8, "q8_0_gemm_noalloc", bd, n_, k_, qd, dd, t_, y)
+        assert torch.equal(y, y_ref_gpu), f"no-allocation GEMM differs from the workspace GEMM at {n_}x{k_} t={t_}"
+        g = syn.rng(71, seed)
+        ti = np.unique(np.concatenate([[0, t_ - 1], g.integers(0, t_, 16)]))
+        ni = np.unique(np.concatenate([[0, n_ - 1], g.integers(0, n_, 64)]))
+        yr, ar = oracle.gemm(blob, n_, k_, qs, ds, t_idx=ti, n_idx=ni)
+        assert_gemm_close(host(y)[np.ix_(ti, ni)], yr, ar, f"noalloc gemm {n_}x{k_} t={t_} (sampled)")
+
+
+def test_noalloc_binding_refuses_bind_before_an_eager_call(q8):
+    """The binding's bound (graph-capture) form needs the scratch address looked
+    up by an earlier eager call on the device."""
+    import torch
+
+    saved = set(q8._binding._noalloc_devices)
+    try:
+        q8._binding._noalloc_devices.clear()
+        n, k, t = 256, 256, 100
+        w = torch.zeros(n * (k // 32) * 34, dtype=torch.uint8, device="cuda")
+        qs, ds = q8.empty_plane(128, k)
+        y = torch.empty(t, n, device="cuda")
+        with pytest.raises(RuntimeError):
+            q8.q8_0_gemm_noalloc(w, n, k, qs, ds, t, y, bind=True)
+        qs.zero_(), ds.zero_()
+        q8.q8_0_gemm_noalloc(w, n, k, qs, ds, t, y)
+        q8.q8_check()
+        q8.q8_0_gemm_noalloc(w, n, k, qs, ds, t, y, bind=True)()
+        q8.q8_check()
+        assert not torch.isnan(y).any() and not y.any()
+    finally:
+        q8._binding._noalloc_devices.update(saved)
+
+
 def test_noalloc_gemm_refuses_requests_beyond_its_scratch(q8):
     import torch
 
