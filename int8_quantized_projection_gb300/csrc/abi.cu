@@ -8,7 +8,7 @@ namespace q8 {
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSlots = 12;
+constexpr int kMaxSlots = 20;
 int g_sms[kMaxDevices];        // 0 = not queried yet
 int g_is103[kMaxDevices];      // 0 = unknown, 1 = yes, 2 = no
 int g_smem_set[kMaxDevices][kMaxSlots];
@@ -153,9 +153,11 @@ extern "C" int q8_check(void *stream)
     if (cudaStreamSynchronize(s) != cudaSuccess) return Q8_ERR_CUDA;
     const int a = q8::gemv_take_error(s);
     const int b = q8::gemm_take_error(s);
-    if (a == Q8_ERR_CUDA || b == Q8_ERR_CUDA) return Q8_ERR_CUDA;
+    const int c = q8::quant_take_error(s);
+    if (a == Q8_ERR_CUDA || b == Q8_ERR_CUDA || c == Q8_ERR_CUDA) return Q8_ERR_CUDA;
     if (a != Q8_OK) return a;
-    return b;
+    if (b != Q8_OK) return b;
+    return c;
 }
 
 namespace q8 {

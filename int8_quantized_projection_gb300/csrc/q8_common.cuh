@@ -119,6 +119,7 @@ constexpr int kGemvStagedMaxChunks = 512;
 int gemv_staged_q4a_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
                            cudaStream_t s);
 int gemm_take_error(cudaStream_t s);
+int quant_take_error(cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // device-side PTX wrappers

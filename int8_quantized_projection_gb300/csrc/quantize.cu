@@ -15,6 +15,8 @@
 
 namespace {
 
+__device__ unsigned int g_quant_err;
+
 constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;  // float4 loads in flight per lane
 
@@ -154,6 +156,174 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
 }
 
 // --------------------------------------------------------------------------
+// rmsnorm_quant for many rows (more than one per SM) of moderate width: one
+// persistent CTA per SM made of row groups of four warps.  A group owns a row
+// at a time; its rows arrive by bulk copy into the group's two shared-memory
+// slots, the next while it works on the current one, so each SM keeps a
+// dozen rows in flight and no group waits for another (groups synchronise on
+// named barriers of their own).  Thread b of a group owns the row's 32-element
+// block b whole: its amax and code sum are register reductions and its d and
+// 1/d are computed once, so the encoder costs a fraction of the per-lane
+// (8 lanes per block) form.  Per row: each thread sums the squares of its
+// block, the warps reduce by xor shuffles and their four sums are added in
+// warp order; then scale, write y (mode 1) and encode.  A thread reads its
+// block's eight float4 starting at float4 (b mod 8), so the lanes of a warp
+// spread over all banks.  The weight vector is staged once per CTA.
+// --------------------------------------------------------------------------
+constexpr int kGrpThreads = 128;     // four warps per row, one block per thread
+constexpr int kGrpSlots = 2;         // row slots per group
+constexpr int kGrpMax = 8;           // groups per CTA (1024 threads)
+constexpr int kGrpSmemBudget = 200 * 1024;  // weight vector + every group's slots
+constexpr int kGrpMaxD = 32 * kGrpThreads;  // 4096: one block per thread
+
+int rowgroup_groups(int d)
+{
+    const int per = d * 4;
+    const int g = (kGrpSmemBudget - per) / (per * kGrpSlots);
+    return g > kGrpMax ? kGrpMax : g;
+}
+
+__device__ __forceinline__ void group_sync(int id)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kGrpThreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
+{
+    return (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(b) & 0xffu) << 8) |
+           ((static_cast<uint32_t>(c) & 0xffu) << 16) | (static_cast<uint32_t>(d) << 24);
+}
+
+__global__ void __launch_bounds__(kGrpThreads * kGrpMax, 1)
+rmsnorm_quant_rowgroup_kernel(const float *__restrict__ x, const float *__restrict__ w, float eps,
+                              float *__restrict__ y, int64_t rows, int64_t rows_pad, int d,
+                              uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
+{
+    extern __shared__ __align__(128) uint8_t smem_rg[];
+    __shared__ __align__(8) uint64_t full[kGrpMax * kGrpSlots];
+    __shared__ float red[kGrpMax][2][kGrpThreads / 32];
+    __shared__ int okf[kGrpMax][2][kGrpThreads / 32];
+    const int F = d >> 2, nb = d >> 5;
+    const int grp = threadIdx.x / kGrpThreads, gt = threadIdx.x % kGrpThreads;
+    const int lane = gt & 31, gw = gt >> 5;
+    const int ngroups = blockDim.x / kGrpThreads;
+    const float4 *wsm = reinterpret_cast<const float4 *>(smem_rg);
+    float4 *myslots = reinterpret_cast<float4 *>(smem_rg) + static_cast<int64_t>(F) * (1 + kGrpSlots * grp);
+    uint64_t *mybar = full + kGrpSlots * grp;
+    const uint32_t row_bytes = static_cast<uint32_t>(d) * 4u;  // a multiple of 128
+    const bool mine_blk = gt < nb;                             // this thread's block exists
+    const int rot = gt & 7;                                    // first float4 read (bank spread)
+    q8::griddep_launch_dependents();  // consumers may start their prologue
+    // the weight vector is a constant input: staged before the dependency wait
+    for (int f = threadIdx.x; f < F; f += blockDim.x)
+        reinterpret_cast<float4 *>(smem_rg)[f] = __ldg(reinterpret_cast<const float4 *>(w) + f);
+    if (gt == 0) {
+        for (int s = 0; s < kGrpSlots; ++s) q8::mbar_init(&mybar[s], 1);
+        q8::fence_mbar_init();
+    }
+    __syncthreads();
+    q8::griddep_wait();  // x may come from the previous kernel
+
+    // this group's rows: t = g0 + i * stride; rows at or past `rows` (the zero
+    // tail, all at the end) are not loaded
+    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * ngroups + grp;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * ngroups;
+    const int64_t mine = g0 < rows_pad ? (rows_pad - g0 + stride - 1) / stride : 0;
+    int64_t issued = 0;  // thread gt == 0: rows whose load has been issued (or that need none)
+    auto issue_upto = [&](int64_t upto) {
+        for (; issued < upto && issued < mine; ++issued) {
+            const int64_t t = g0 + issued * stride;
+            if (t >= rows) continue;
+            const int s = static_cast<int>(issued % kGrpSlots);
+            q8::mbar_arrive_expect_tx(&mybar[s], row_bytes);
+            q8::bulk_g2s(myslots + static_cast<int64_t>(s) * F, x + t * d, row_bytes, &mybar[s]);
+        }
+    };
+    if (gt == 0) issue_upto(kGrpSlots);
+    int64_t i = 0;
+    for (; i < mine; ++i) {
+        const int64_t t = g0 + i * stride;
+        uint4 *qrow = reinterpret_cast<uint4 *>(qs + t * F);  // 32 codes = two uint4 per block
+        uint32_t *drow = ds + t * nb;
+        if (t >= rows) {  // padded token row: zero plane row
+            if (mine_blk) {
+                qrow[2 * gt] = make_uint4(0u, 0u, 0u, 0u);
+                qrow[2 * gt + 1] = make_uint4(0u, 0u, 0u, 0u);
+                drow[gt] = 0u;
+            }
+            continue;
+        }
+        const int s = static_cast<int>(i % kGrpSlots);
+        const bool got = q8::mbar_wait_bounded(&mybar[s], static_cast<uint32_t>(i / kGrpSlots) & 1u);
+        const float4 *xb = myslots + static_cast<int64_t>(s) * F + 8 * gt;
+        float4 v[8];
+        float ss = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int e = (k + rot) & 7;  // element group e of the block, read in rotated order
+            v[k] = (got && mine_blk) ? xb[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ss = q8::rms_sumsq4(ss, v[k]);
+        ss = q8::rms_warp_sum(ss);
+        const int rb = static_cast<int>(i & 1);  // alternate buffers: one exchange barrier per row suffices
+        const bool all_got = __all_sync(Q8_FULL_MASK, got);
+        if (lane == 0) {
+            red[grp][rb][gw] = ss;
+            okf[grp][rb][gw] = all_got ? 1 : 0;
+        }
+        group_sync(1 + grp);
+        bool all_ok = true;
+        float tot = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kGrpThreads / 32; ++k) {
+            tot += red[grp][rb][k];  // same fixed order in every thread
+            all_ok = all_ok && okf[grp][rb][k] != 0;
+        }
+        if (!all_ok) {  // a load did not arrive in time: report, stop (the whole group alike)
+            if (gt == 0) atomicOr(&g_quant_err, 1u);
+            break;
+        }
+        if (mine_blk) {
+            const float scale = q8::rms_scale(tot, d, eps);
+            const float4 *wb = wsm + 8 * gt;
+            float4 *yb = reinterpret_cast<float4 *>(y + t * static_cast<int64_t>(d)) + 8 * gt;
+            float amax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int e = (k + rot) & 7;
+                v[k] = q8::rms_apply4(v[k], scale, wb[e]);
+                if (y) yb[e] = v[k];  // mode 2 (y == NULL): only the plane is written
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+            }
+            const float dq = q8::q8_block_d(amax);
+            const float di = q8::q8_block_di(dq);
+            uint32_t *qw = reinterpret_cast<uint32_t *>(qrow) + 8 * gt;
+            int sum = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int c0 = q8::q8_code(v[k].x, di), c1 = q8::q8_code(v[k].y, di);
+                const int c2 = q8::q8_code(v[k].z, di), c3 = q8::q8_code(v[k].w, di);
+                sum += c0 + c1 + c2 + c3;
+                qw[(k + rot) & 7] = pack4(c0, c1, c2, c3);  // codes of element group (k + rot) mod 8
+            }
+            drow[gt] = q8::q8_dsword(dq, sum);
+        }
+        group_sync(1 + grp);  // every thread of the group is done with this row's slot
+        if (gt == 0) {
+            q8::fence_proxy_async_smem();  // the slot's reads come before the next copy into it
+            issue_upto(i + 1 + kGrpSlots);
+        }
+    }
+    // after a timeout, let this group's loads still in flight land before it exits
+    if (gt == 0)
+        for (int64_t k = i; k < issued; ++k)
+            if (g0 + k * stride < rows)
+                (void)q8::mbar_wait_bounded(&mybar[k % kGrpSlots], static_cast<uint32_t>(k / kGrpSlots) & 1u,
+                                            Q8_DRAIN_LIMIT_NS);
+}
+
+// --------------------------------------------------------------------------
 // swiglu_quant: flat elementwise stream, y = g / (1 + exp(-g)) * u
 // ("54 - r51 - producer-fused A-quantize mode 1", sec. 3.2), encoded from
 // registers into the plane in the same pass.
@@ -239,6 +409,19 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     const int F = static_cast<int>(d / 4);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int sms = q8::device_sm_count();
+    const int nsm = sms > 0 ? sms : 152;
+    uint32_t *q32 = reinterpret_cast<uint32_t *>(qs);
+    const int di = static_cast<int>(d);
+    const int ng = rowgroup_groups(di);
+    if (rows_pad > nsm && d <= kGrpMaxD && ng >= 2) {
+        // many rows: row groups streaming their rows through shared memory, one CTA per SM
+        const size_t smem = static_cast<size_t>(d) * 4 * (1 + kGrpSlots * ng);
+        if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(rmsnorm_quant_rowgroup_kernel),
+                                      static_cast<int>(smem), 12))
+            return Q8_ERR_LAUNCH;
+        return q8::launch_pdl(rmsnorm_quant_rowgroup_kernel, dim3(static_cast<unsigned>(nsm)), dim3(kGrpThreads * ng),
+                              smem, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+    }
     // float4 per thread: up to 256 threads per row when CTAs take several rows
     // (four CTAs per SM keep four rows in flight), up to 512 when every CTA
     // has at most one row (a decode token: shorter chains per thread)
@@ -250,8 +433,6 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     const int64_t per_sm = P <= 256 ? 4 : 2;
     const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 152) * per_sm;
     const dim3 grid(static_cast<unsigned>(rows_pad < cap ? rows_pad : cap));
-    uint32_t *q32 = reinterpret_cast<uint32_t *>(qs);
-    const int di = static_cast<int>(d);
     const size_t wsmem = d <= kNormSmemMax ? static_cast<size_t>(d) * 4 : 0;
     switch (J) {
     case 1: return q8::launch_pdl(rmsnorm_quant_kernel<1>, grid, dim3(P), wsmem, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
@@ -276,3 +457,17 @@ extern "C" int swiglu_quant(const float *gate, const float *up, float *y, int64_
                           reinterpret_cast<const float4 *>(up), reinterpret_cast<float4 *>(y), n4_valid, n4_total,
                           reinterpret_cast<uint32_t *>(qs), ds);
 }
+
+namespace q8 {
+
+int quant_take_error(cudaStream_t s)
+{
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_quant_err, sizeof(v), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_quant_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return Q8_ERR_CUDA;
+    return v ? Q8_ERR_DEVICE_TIMEOUT : Q8_OK;
+}
+
+} // namespace q8

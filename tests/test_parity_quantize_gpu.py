@@ -60,7 +60,10 @@ def test_quantize_q8_0_zero_rows_only_fills_tail(q8):
 @pytest.mark.parametrize("rows,d,rows_pad", [(1, 3584, 1), (63, 3584, 64), (64, 3584, 64), (129, 3584, 192),
                                              (300, 896, 384), (100, 640, 128), (1, 7168, 1), (7, 18944, 8),
                                              (3354, 3584, 3456), (2, 32768, 2),
-                                             (3, 8192, 3), (3, 8224, 4)])  # weight vector staged / read directly
+                                             (3, 8192, 3), (3, 8224, 4),  # weight vector staged / read directly
+                                             # more rows than SMs: the shared-memory row ring (up to d = 16384)
+                                             (3325, 3584, 3328), (1000, 8192, 1024), (500, 32, 512),
+                                             (400, 16384, 512), (153, 896, 153), (300, 16416, 384)])
 def test_rmsnorm_quant(q8, rows, d, rows_pad):
     import torch
 

@@ -1,7 +1,7 @@
 """Bounded on-device waits: a wait that runs out is reported, never hangs.
 
 Every kernel that waits on a barrier (the staged and small-batch GEMVs, the
-tcgen05 GEMM) gives up after a time limit, records Q8_ERR_DEVICE_TIMEOUT in
+tcgen05 GEMM, the many-row RMSNorm's row ring) gives up after a time limit, records Q8_ERR_DEVICE_TIMEOUT in
 the library's error word and returns, after letting its own copies and
 tensor-core work in flight land (those drain waits have a separate, long
 limit).  q8_check reports the error and clears it.  The pages' counterpart is
@@ -12,8 +12,8 @@ returned to the caller, which falls back).
 The test builds a second copy of the library whose main-loop waits give up
 at once (a zero limit: any wait that is not already satisfied times out;
 drains keep their limit), loads it in a subprocess bounded by a host-side
-timeout, and checks that a GEMM and a batch-1 GEMV each report the timeout,
-that the report is cleared, and that nothing hangs.  A fresh process with the
+timeout, and checks that a GEMM, a batch-1 GEMV and a many-row RMSNorm each
+report the timeout, that the report is cleared, and that nothing hangs.  A fresh process with the
 normal library then gives a correct result.  Nothing here faults or hangs the
 GPU: each wait is bounded, and every kernel reaches its exit after a timeout.
 """
@@ -61,6 +61,15 @@ _CHILD = textwrap.dedent(
     assert lib.q8_0_gemv(P(w), n, k, P(qs), P(ds), P(y), st) == 0
     out["gemv"] = lib.q8_check(st)
     out["gemv_after"] = lib.q8_check(st)
+    # RMSNorm over many rows: the shared-memory row ring waits for each row's copy
+    rows, d = 3325, 3584
+    x = torch.randn(rows, d, device="cuda")
+    nw = torch.ones(d, device="cuda")
+    qs = torch.empty(3328, d, dtype=torch.int8, device="cuda")
+    ds = torch.empty(3328, d // 32, dtype=torch.int32, device="cuda")
+    assert lib.rmsnorm_quant(P(x), P(nw), ctypes.c_float(1e-6), None, rows, d, P(qs), P(ds), 3328, st) == 0
+    out["rmsnorm"] = lib.q8_check(st)
+    out["rmsnorm_after"] = lib.q8_check(st)
     print("RESULT", out)
     """
 )
@@ -101,8 +110,8 @@ def test_waits_that_run_out_report_a_timeout(tmp_path):
 
     lib = build.build(extra=["-DQ8_WAIT_LIMIT_NS=0ull"], lib_path=str(tmp_path / "libq8proj_waits0.so"))
     got = _run(_CHILD, ROOT=ROOT, LIB=lib)
-    assert got["gemm"] == 5 and got["gemv"] == 5, got          # Q8_ERR_DEVICE_TIMEOUT
-    assert got["gemm_after"] == 0 and got["gemv_after"] == 0, got  # reported once, then cleared
+    assert got["gemm"] == 5 and got["gemv"] == 5 and got["rmsnorm"] == 5, got  # Q8_ERR_DEVICE_TIMEOUT
+    assert got["gemm_after"] == 0 and got["gemv_after"] == 0 and got["rmsnorm_after"] == 0, got  # then cleared
     # a fresh process with the normal library computes correctly
     err = _run(_FRESH, ROOT=ROOT)
     assert err <= 1e-5
