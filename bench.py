@@ -177,6 +177,7 @@ def max_over_ranks(torch, values, device):
 
 
 GRAPH_STEPS = 60  # steps per timed CUDA graph (rounded to a multiple of the weight copies)
+E2E_MIN_STEPS = 300  # steps the end-to-end loops time at least
 
 
 def hold_device(torch, launches):
@@ -356,48 +357,69 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     # end to end through the public API with host buffers (weights resident).
     # A serving loop records its step once -- the host-to-device copy of the
     # inputs from pinned memory, the library calls, the device-to-host copy of
-    # the outputs -- as a CUDA graph and replays it every step.  It keeps two
-    # steps in flight: it enqueues step i, then waits for step i-2 and reads
-    # its outputs, so the host's launch and wake-up overlap the GPU's work;
-    # the three host buffers rotate between steps, so a step never writes the
-    # buffer the host is reading (`e2e_s`).  `e2e_serial_s` waits for every
-    # step before enqueuing the next; `e2e_eager_s` also issues the step call
-    # by call.
-    nbuf = 3
+    # the outputs -- as a CUDA graph and replays it every step.  Independent
+    # requests let it keep several steps in flight: consecutive steps use two
+    # sets of device buffers on two streams, so one step's copies overlap the
+    # other's kernels, and the host enqueues step i, then waits for step i-3
+    # and reads its outputs; the four host buffers rotate, so a step never
+    # writes the buffer the host is reading (`e2e_s`).  `e2e_serial_s` waits
+    # for every step before enqueuing the next (one buffer set);
+    # `e2e_eager_s` also issues the step call by call.
+    nbuf, nsets = 4, 2
     xh = [x_all.cpu().pin_memory() for _ in range(nbuf)]
     yh = [torch.empty(y_all.shape, dtype=torch.float32).pin_memory() for _ in range(nbuf)]
 
-    def e2e_body(i, par):  # on the capture streams: the inputs in, one step, the outputs out
-        x_all.copy_(xh[par], non_blocking=True)
-        side.wait_stream(cap)
-        gemvs_c[i][0]()
-        quant_side()
-        gemvs_c[i][1]()
-        cap.wait_stream(side)
-        yh[par].copy_(y_all, non_blocking=True)
+    def make_set(k):  # device buffers, streams and bound calls of buffer set k
+        if k == 0:
+            xa, ya, pl, cp_, sd_ = x_all, y_all, planes[128], cap, side
+        else:
+            xa, ya = torch.empty_like(x_all), torch.empty_like(y_all)
+            pl, cp_, sd_ = q8p.empty_plane(1, 128, dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        yv = list(torch.split(ya, [n for n, _ in DECODE_SHAPES]))
+        mains = [q8p.q8_0_gemv_fused([(wset[0], DECODE_SHAPES[0][0], yv[0]), (wset[1], DECODE_SHAPES[1][0], yv[1])],
+                                     7168, q8p.PRODUCER_QUANT, xa[0, :7168], stream=cp_, bind=True) for wset in ws]
+        q128 = q8p.quantize_q8_0(xa[:, 7168:], *pl, stream=sd_, bind=True)
+        g128 = [q8p.q8_0_gemv(wset[2], *DECODE_SHAPES[2], *pl, yv[2], stream=sd_, bind=True) for wset in ws]
+        return dict(x=xa, y=ya, cap=cp_, side=sd_, mains=mains, q128=q128, g128=g128, launch=torch.cuda.Stream(dev))
 
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        for i in range(copies):  # once outside the capture
-            e2e_body(i, i % nbuf)
-    stream.wait_stream(cap)
-    e2e_graphs = []  # [weight copy][host buffer]
+    sets = [make_set(k) for k in range(nsets)]
+
+    def e2e_body(st, i, par):  # on set st's capture streams: the inputs in, one step, the outputs out
+        st["x"].copy_(xh[par], non_blocking=True)
+        st["side"].wait_stream(st["cap"])
+        st["mains"][i]()
+        st["q128"]()
+        st["g128"][i]()
+        st["cap"].wait_stream(st["side"])
+        yh[par].copy_(st["y"], non_blocking=True)
+
+    e2e_graphs = []  # [weight copy][host buffer]; host buffer h runs on buffer set h % nsets
+    for st_i, st in enumerate(sets):
+        st["cap"].wait_stream(stream)
+        with torch.cuda.stream(st["cap"]):
+            for i in range(copies):  # once outside the capture
+                e2e_body(st, i, st_i)
+        stream.wait_stream(st["cap"])
     for i in range(copies):
         row = []
         for par in range(nbuf):
+            st = sets[par % nsets]
             gi = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gi, stream=cap):
-                e2e_body(i, par)
+            with torch.cuda.graph(gi, stream=st["cap"]):
+                e2e_body(st, i, par)
             row.append(gi)
         e2e_graphs.append(row)
     torch.cuda.synchronize(dev)
     done = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def e2e_run(n, start):  # up to nbuf - 1 steps in flight
+    def e2e_run(n, start):  # up to nbuf - 1 steps in flight, alternating buffer sets and streams
         for j in range(n):
             i = start + j
-            e2e_graphs[i % copies][i % nbuf].replay()
-            done[i % nbuf].record(stream)
+            h = i % nbuf
+            ls = sets[h % nsets]["launch"]
+            with torch.cuda.stream(ls):
+                e2e_graphs[i % copies][h].replay()
+                done[h].record(ls)
             if j >= nbuf - 1:
                 done[(i - nbuf + 1) % nbuf].synchronize()  # that step's outputs are in yh[(i - nbuf + 1) % nbuf]
         for j in range(max(0, n - nbuf + 1), n):
@@ -406,7 +428,7 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     def e2e_serial_run(n, start):
         for j in range(n):
             i = start + j
-            e2e_graphs[i % copies][i % 2].replay()
+            e2e_graphs[i % copies][0].replay()
             stream.synchronize()
 
     def e2e_eager_run(n, start):
@@ -416,16 +438,19 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
             yh[0].copy_(y_all, non_blocking=True)
             stream.synchronize()
 
+    # the end-to-end loops run at least E2E_MIN_STEPS steps, so that filling and
+    # draining the steps in flight does not dominate a short run
+    e2e_steps = max(steps, E2E_MIN_STEPS)
     res = {}
     for name, fn in (("e2e_s", e2e_run), ("e2e_serial_s", e2e_serial_run), ("e2e_eager_s", e2e_eager_run)):
         fn(warmup, 0)
         torch.cuda.synchronize(dev)
         e0 = time.perf_counter()
-        fn(steps, warmup)
-        res[name] = time.perf_counter() - e0
+        fn(e2e_steps, warmup)
+        res[name] = (time.perf_counter() - e0) * steps / e2e_steps  # seconds for `steps` steps at that rate
         q8p.q8_check()
     e2e_s, e2e_serial_s, e2e_eager_s = res["e2e_s"], res["e2e_serial_s"], res["e2e_eager_s"]
-    return dict(ms=ms, kern_ms=kern_ms, iso_ms=iso_ms, clocks=clocks, e2e_s=e2e_s, e2e_serial_s=e2e_serial_s, e2e_eager_s=e2e_eager_s,
+    return dict(ms=ms, kern_ms=kern_ms, iso_ms=iso_ms, clocks=clocks, e2e_steps=e2e_steps, e2e_s=e2e_s, e2e_serial_s=e2e_serial_s, e2e_eager_s=e2e_eager_s,
                 copies=copies, ms_two=ms_two,
                 h2d=sum(v.nbytes for v in xs_h.values()), d2h=4 * sum(n for n, _ in DECODE_SHAPES))
 
@@ -1328,8 +1353,10 @@ def main():
             "e2e": {"value": round(world * step_bytes * args.steps / dec["e2e_s"] / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"],
                     "launch": "per step: one CUDA graph replay (pinned-memory copy in, the library calls, copy out; "
-                              "recorded once); two steps in flight: the host reads step i-2's outputs after "
-                              "enqueuing step i (three host buffers rotate)",
+                              "recorded once); consecutive steps on two device buffer sets and streams (one step's "
+                              "copies overlap the other's kernels); up to three steps in flight: the host reads step "
+                              "i-3's outputs after enqueuing step i (four host buffers rotate)",
+                    "steps_timed": dec["e2e_steps"],
                     "serial_value": round(world * step_bytes * args.steps / dec["e2e_serial_s"] / 1e9, 2),
                     "eager_value": round(world * step_bytes * args.steps / dec["e2e_eager_s"] / 1e9, 2)},
             "clocks": dec["clocks"],
