@@ -176,10 +176,10 @@ constexpr int kGrpMax = 8;           // groups per CTA (1024 threads)
 constexpr int kGrpSmemBudget = 200 * 1024;  // weight vector + every group's slots
 constexpr int kGrpMaxD = 32 * kGrpThreads;  // 4096: one block per thread
 
-int rowgroup_groups(int d)
+int rowgroup_groups(int d, bool norm)
 {
     const int per = d * 4;
-    const int g = (kGrpSmemBudget - per) / (per * kGrpSlots);
+    const int g = (kGrpSmemBudget - (norm ? per : 0)) / (per * kGrpSlots);
     return g > kGrpMax ? kGrpMax : g;
 }
 
@@ -194,10 +194,12 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
            ((static_cast<uint32_t>(c) & 0xffu) << 16) | (static_cast<uint32_t>(d) << 24);
 }
 
-__global__ void __launch_bounds__(kGrpThreads * kGrpMax, 1)
-rmsnorm_quant_rowgroup_kernel(const float *__restrict__ x, const float *__restrict__ w, float eps,
-                              float *__restrict__ y, int64_t rows, int64_t rows_pad, int d,
-                              uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
+// The body shared by RMSNorm + quantize (kNorm) and the plain quantizer
+// (rows of x encoded as they are: no sum of squares, weight or y).
+template <bool kNorm>
+__device__ __forceinline__ void rowgroup_body(const float *__restrict__ x, const float *__restrict__ w, float eps,
+                                              float *__restrict__ y, int64_t rows, int64_t rows_pad, int d,
+                                              uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
     extern __shared__ __align__(128) uint8_t smem_rg[];
     __shared__ __align__(8) uint64_t full[kGrpMax * kGrpSlots];
@@ -208,15 +210,16 @@ rmsnorm_quant_rowgroup_kernel(const float *__restrict__ x, const float *__restri
     const int lane = gt & 31, gw = gt >> 5;
     const int ngroups = blockDim.x / kGrpThreads;
     const float4 *wsm = reinterpret_cast<const float4 *>(smem_rg);
-    float4 *myslots = reinterpret_cast<float4 *>(smem_rg) + static_cast<int64_t>(F) * (1 + kGrpSlots * grp);
+    float4 *myslots = reinterpret_cast<float4 *>(smem_rg) + static_cast<int64_t>(F) * ((kNorm ? 1 : 0) + kGrpSlots * grp);
     uint64_t *mybar = full + kGrpSlots * grp;
     const uint32_t row_bytes = static_cast<uint32_t>(d) * 4u;  // a multiple of 128
     const bool mine_blk = gt < nb;                             // this thread's block exists
     const int rot = gt & 7;                                    // first float4 read (bank spread)
     q8::griddep_launch_dependents();  // consumers may start their prologue
     // the weight vector is a constant input: staged before the dependency wait
-    for (int f = threadIdx.x; f < F; f += blockDim.x)
-        reinterpret_cast<float4 *>(smem_rg)[f] = __ldg(reinterpret_cast<const float4 *>(w) + f);
+    if (kNorm)
+        for (int f = threadIdx.x; f < F; f += blockDim.x)
+            reinterpret_cast<float4 *>(smem_rg)[f] = __ldg(reinterpret_cast<const float4 *>(w) + f);
     if (gt == 0) {
         for (int s = 0; s < kGrpSlots; ++s) q8::mbar_init(&mybar[s], 1);
         q8::fence_mbar_init();
@@ -263,9 +266,11 @@ rmsnorm_quant_rowgroup_kernel(const float *__restrict__ x, const float *__restri
             const int e = (k + rot) & 7;  // element group e of the block, read in rotated order
             v[k] = (got && mine_blk) ? xb[e] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        if (kNorm) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ss = q8::rms_sumsq4(ss, v[k]);
-        ss = q8::rms_warp_sum(ss);
+            for (int k = 0; k < 8; ++k) ss = q8::rms_sumsq4(ss, v[k]);
+            ss = q8::rms_warp_sum(ss);
+        }
         const int rb = static_cast<int>(i & 1);  // alternate buffers: one exchange barrier per row suffices
         const bool all_got = __all_sync(Q8_FULL_MASK, got);
         if (lane == 0) {
@@ -285,17 +290,21 @@ rmsnorm_quant_rowgroup_kernel(const float *__restrict__ x, const float *__restri
             break;
         }
         if (mine_blk) {
-            const float scale = q8::rms_scale(tot, d, eps);
-            const float4 *wb = wsm + 8 * gt;
-            float4 *yb = reinterpret_cast<float4 *>(y + t * static_cast<int64_t>(d)) + 8 * gt;
             float amax = 0.0f;
+            if (kNorm) {
+                const float scale = q8::rms_scale(tot, d, eps);
+                const float4 *wb = wsm + 8 * gt;
+                float4 *yb = reinterpret_cast<float4 *>(y + t * static_cast<int64_t>(d)) + 8 * gt;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int e = (k + rot) & 7;
-                v[k] = q8::rms_apply4(v[k], scale, wb[e]);
-                if (y) yb[e] = v[k];  // mode 2 (y == NULL): only the plane is written
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+                for (int k = 0; k < 8; ++k) {
+                    const int e = (k + rot) & 7;
+                    v[k] = q8::rms_apply4(v[k], scale, wb[e]);
+                    if (y) yb[e] = v[k];  // mode 2 (y == NULL): only the plane is written
+                }
             }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
             const float dq = q8::q8_block_d(amax);
             const float di = q8::q8_block_di(dq);
             uint32_t *qw = reinterpret_cast<uint32_t *>(qrow) + 8 * gt;
@@ -321,6 +330,21 @@ rmsnorm_quant_rowgroup_kernel(const float *__restrict__ x, const float *__restri
             if (g0 + k * stride < rows)
                 (void)q8::mbar_wait_bounded(&mybar[k % kGrpSlots], static_cast<uint32_t>(k / kGrpSlots) & 1u,
                                             Q8_DRAIN_LIMIT_NS);
+}
+
+__global__ void __launch_bounds__(kGrpThreads * kGrpMax, 1)
+rmsnorm_quant_rowgroup_kernel(const float *__restrict__ x, const float *__restrict__ w, float eps,
+                              float *__restrict__ y, int64_t rows, int64_t rows_pad, int d,
+                              uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
+{
+    rowgroup_body<true>(x, w, eps, y, rows, rows_pad, d, qs, ds);
+}
+
+__global__ void __launch_bounds__(kGrpThreads * kGrpMax, 1)
+quantize_q8_0_rowgroup_kernel(const float *__restrict__ x, int64_t rows, int64_t rows_pad, int d,
+                              uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
+{
+    rowgroup_body<false>(x, nullptr, 0.0f, nullptr, rows, rows_pad, d, qs, ds);
 }
 
 // --------------------------------------------------------------------------
@@ -391,6 +415,19 @@ extern "C" int quantize_q8_0(const float *x, int64_t rows, int64_t k, int8_t *qs
     if (st != Q8_OK) return st;
     if (rows > 0 && !q8::aligned16(x)) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    const int sms = q8::device_sm_count();
+    const int nsm = sms > 0 ? sms : 152;
+    const int ng = k <= kGrpMaxD ? rowgroup_groups(static_cast<int>(k), false) : 0;
+    if (rows_pad > nsm && ng >= 2) {
+        // many rows: row groups streaming the rows through shared memory, one CTA per SM
+        const size_t smem = static_cast<size_t>(k) * 4 * kGrpSlots * ng;
+        if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(quantize_q8_0_rowgroup_kernel),
+                                      static_cast<int>(smem), 13))
+            return Q8_ERR_LAUNCH;
+        return q8::launch_pdl(quantize_q8_0_rowgroup_kernel, dim3(static_cast<unsigned>(nsm)),
+                              dim3(kGrpThreads * ng), smem, static_cast<cudaStream_t>(stream), x, rows, rows_pad,
+                              static_cast<int>(k), reinterpret_cast<uint32_t *>(qs), ds);
+    }
     const int64_t n4_valid = rows * k / 4, n4_total = rows_pad * k / 4;
     return q8::launch_pdl(quantize_q8_0_kernel, dim3(flat_grid(n4_total, kQuantUnroll)), dim3(kQuantThreads), 0,
                           static_cast<cudaStream_t>(stream), reinterpret_cast<const float4 *>(x), n4_valid, n4_total,
@@ -412,7 +449,7 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     const int nsm = sms > 0 ? sms : 152;
     uint32_t *q32 = reinterpret_cast<uint32_t *>(qs);
     const int di = static_cast<int>(d);
-    const int ng = rowgroup_groups(di);
+    const int ng = rowgroup_groups(di, true);
     if (rows_pad > nsm && d <= kGrpMaxD && ng >= 2) {
         // many rows: row groups streaming their rows through shared memory, one CTA per SM
         const size_t smem = static_cast<size_t>(d) * 4 * (1 + kGrpSlots * ng);

@@ -35,7 +35,10 @@ def _edge_rows(k):
 
 
 @pytest.mark.parametrize("rows,k,rows_pad", [(1, 32, 1), (1, 7168, 1), (5, 96, 128), (63, 3584, 128),
-                                             (64, 3584, 64), (129, 640, 256), (300, 896, 300), (3354, 3584, 3456)])
+                                             (64, 3584, 64), (129, 640, 256), (300, 896, 300), (3354, 3584, 3456),
+                                             # more rows than SMs: row groups (k <= 4096) or the flat stream
+                                             (3325, 3584, 3328), (500, 32, 512), (1000, 4096, 1024),
+                                             (153, 96, 153), (300, 4128, 384), (0, 256, 1024)])
 def test_quantize_q8_0_bit_exact(q8, rows, k, rows_pad):
     g = syn.rng(51, rows, k)
     x = syn.activations(g, rows, k, sigma=1.5, outlier_frac=0.01)
