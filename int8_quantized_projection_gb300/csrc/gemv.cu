@@ -222,20 +222,42 @@ __device__ __forceinline__ float FmtQ8_0::dot(const uint8_t *wc, const uint8_t *
 
 // Fused activation staging: the producer's f32 row and its q8_0 encoding,
 // computed by this CTA into the staged layout (chunk c: 32 qs words, then
-// the d|ssum words of its 4 blocks).  Warp w encodes chunks w, w + nwarps,
-// ...: lane l holds float4 32c + l, so 8 adjacent lanes hold one block, as
-// in the standalone producers.  For RMSNorm the row's sum of squares is
-// first formed exactly as the standalone kernel forms it with P threads:
-// this CTA's warps play its P/32 warps in turn (a CTA's thread count is a
-// multiple of 32, so lane l plays lane l), `red` collects the warp sums,
-// and every thread adds them in warp order.
+// the d|ssum words of its 4 blocks).  A pair of adjacent threads encodes one
+// 32-element block (pair i takes blocks i, i + blockDim.x/2, ...; thread half
+// h holds elements 16h..16h+15): the block's amax and code sum are register
+// reductions and one shuffle, and d and 1/d are computed once per thread
+// (the codes are those any other split of the block gives: a maximum,
+// elementwise codes and an integer sum).  Every input of a thread's first
+// block (x and the norm weight, or gate and up) is loaded before anything
+// else, so for RMSNorm those loads are in flight together with the loads of
+// the sum of squares: the prologue waits for one round trip to L2.  The
+// row's sum of squares is formed exactly as the standalone kernel forms it
+// with P threads: this CTA's warps play its P/32 warps in turn (a CTA's
+// thread count is a multiple of 32, so lane l plays lane l), `red` collects
+// the warp sums, and every thread adds them in warp order.
 __device__ __forceinline__ void stage_produced(const GvGeom &g, uint8_t *act, float *red, int warp, int lane)
 {
     constexpr int kBatch = 4;  // loads a thread keeps in flight before it uses them
     const int nwarps = static_cast<int>(blockDim.x >> 5);
-    const int F = g.nc * 32;  // float4 per row
+    const int nblk = g.nc * 4;  // 32-element blocks of the row
+    const int F = g.nc * 32;    // float4 per row
     const GvAct &A = g.act;
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool second = A.producer != Q8_PRODUCER_QUANT;  // norm weight (RMSNorm) or up (SwiGLU)
+    const float4 *pa = A.a;
+    const float4 *pb = A.producer == Q8_PRODUCER_SWIGLU ? A.b : A.w;
+    const int h = lane & 1;                                   // half of the block
+    const int pstride = static_cast<int>(blockDim.x >> 1);    // thread pairs
+    int blk = static_cast<int>(threadIdx.x >> 1);
+    float4 va[4], vb[4];
+    auto load = [&](int b) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) va[e] = __ldg(pa + 8 * b + 4 * h + e);
+        if (second)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vb[e] = __ldg(pb + 8 * b + 4 * h + e);
+    };
+    if (blk < nblk) load(blk);
     float scale = 0.0f;
     if (A.producer == Q8_PRODUCER_RMSNORM) {
         const int vws = A.rms_p >> 5;
@@ -247,7 +269,7 @@ __device__ __forceinline__ void stage_produced(const GvGeom &g, uint8_t *act, fl
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u) {
                     const int f = vt + (j0 + u) * A.rms_p;
-                    v[u] = (j0 + u < A.rms_j && f < F) ? __ldg(A.a + f) : zero;
+                    v[u] = (j0 + u < A.rms_j && f < F) ? __ldg(pa + f) : zero;
                 }
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u) ss = q8::rms_sumsq4(ss, v[u]);  // zeros leave ss as it is
@@ -260,33 +282,38 @@ __device__ __forceinline__ void stage_produced(const GvGeom &g, uint8_t *act, fl
         for (int i = 0; i < vws; ++i) tot += red[i];
         scale = q8::rms_scale(tot, F * 4, A.eps);
     }
-    for (int c0 = warp; c0 < g.nc; c0 += nwarps * kBatch) {
-        float4 p[kBatch], q[kBatch];
+    // the pairs stay whole through the loop: blockDim.x is even and the pair's
+    // threads see the same block index, so both take part in every shuffle
+    for (int first = 1; blk < nblk; blk += pstride, first = 0) {
+        if (!first) load(blk);  // a later block (rows longer than 16 x threads)
+        float amax = 0.0f;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int c = c0 + u * nwarps, f = c * 32 + lane;
-            const bool ok = c < g.nc;
-            p[u] = ok ? __ldg(A.a + f) : zero;
-            q[u] = (ok && A.producer != Q8_PRODUCER_QUANT)
-                       ? __ldg((A.producer == Q8_PRODUCER_RMSNORM ? A.w : A.b) + f)
-                       : zero;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int c = c0 + u * nwarps;
-            if (c >= g.nc) break;  // uniform over the warp
-            float4 o;
+        for (int e = 0; e < 4; ++e) {
+            float4 o = va[e];
             if (A.producer == Q8_PRODUCER_RMSNORM)
-                o = q8::rms_apply4(p[u], scale, q[u]);
+                o = q8::rms_apply4(o, scale, vb[e]);
             else if (A.producer == Q8_PRODUCER_SWIGLU)
-                o = q8::silu_mul4(p[u], q[u]);
-            else
-                o = p[u];
-            const q8::Q8Enc e = q8::q8_encode8(o);
-            uint8_t *ch = act + c * kActChunkBytes;
-            reinterpret_cast<uint32_t *>(ch)[lane] = e.qword;
-            if ((lane & 7) == 0) reinterpret_cast<uint32_t *>(ch + 128)[lane >> 3] = e.dsword;
+                o = q8::silu_mul4(o, vb[e]);
+            va[e] = o;
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w))));
         }
+        const unsigned pair_mask = 3u << (lane & ~1);
+        amax = fmaxf(amax, __shfl_xor_sync(pair_mask, amax, 1));
+        const float d = q8::q8_block_d(amax);
+        const float di = q8::q8_block_di(d);
+        uint32_t qw[4];
+        int sum = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c0 = q8::q8_code(va[e].x, di), c1 = q8::q8_code(va[e].y, di);
+            const int c2 = q8::q8_code(va[e].z, di), c3 = q8::q8_code(va[e].w, di);
+            sum += c0 + c1 + c2 + c3;
+            qw[e] = q8::pack4(c0, c1, c2, c3);
+        }
+        sum += __shfl_xor_sync(pair_mask, sum, 1);
+        uint8_t *ch = act + (blk >> 2) * kActChunkBytes;
+        *reinterpret_cast<uint4 *>(ch + 32 * (blk & 3) + 16 * h) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+        if (h == 0) reinterpret_cast<uint32_t *>(ch + 128)[blk & 3] = q8::q8_dsword(d, sum);
     }
 }
 

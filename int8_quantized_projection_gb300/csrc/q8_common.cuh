@@ -297,6 +297,13 @@ __device__ __forceinline__ uint32_t q8_dsword(float d, int ssum)
            (static_cast<uint32_t>(static_cast<uint16_t>(static_cast<int16_t>(ssum))) << 16);
 }
 
+// Four codes (each in [-127, 127]) packed little-endian into a word.
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
+{
+    return (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(b) & 0xffu) << 8) |
+           ((static_cast<uint32_t>(c) & 0xffu) << 16) | (static_cast<uint32_t>(d) << 24);
+}
+
 // 8 adjacent lanes hold one 32-element block, a float4 each.
 __device__ __forceinline__ Q8Enc q8_encode8(float4 v)
 {

@@ -188,12 +188,6 @@ __device__ __forceinline__ void group_sync(int id)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kGrpThreads) : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
-{
-    return (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(b) & 0xffu) << 8) |
-           ((static_cast<uint32_t>(c) & 0xffu) << 16) | (static_cast<uint32_t>(d) << 24);
-}
-
 // The body shared by RMSNorm + quantize (kNorm) and the plain quantizer
 // (rows of x encoded as they are: no sum of squares, weight or y).
 template <bool kNorm>
@@ -314,7 +308,7 @@ __device__ __forceinline__ void rowgroup_body(const float *__restrict__ x, const
                 const int c0 = q8::q8_code(v[k].x, di), c1 = q8::q8_code(v[k].y, di);
                 const int c2 = q8::q8_code(v[k].z, di), c3 = q8::q8_code(v[k].w, di);
                 sum += c0 + c1 + c2 + c3;
-                qw[(k + rot) & 7] = pack4(c0, c1, c2, c3);  // codes of element group (k + rot) mod 8
+                qw[(k + rot) & 7] = q8::pack4(c0, c1, c2, c3);  // codes of element group (k + rot) mod 8
             }
             drow[gt] = q8::q8_dsword(dq, sum);
         }
