@@ -601,7 +601,25 @@ def run_prefill(torch, q8p, steps, warmup, dev):
     torch.cuda.synchronize(dev)
     q8p.q8_check()
     per["quantize_q8_0 (standalone, not in the chain)"] = statistics.mean(a.elapsed_time(b) for a, b in qev)
-    return per
+    # the same chain on weights prepared once per matrix (q8_0_gemm_prepare_weights,
+    # outside the timed region): the GEMMs skip their per-call weight pre-pass
+    wg_p, wu_p = (q8p.q8_0_gemm_prepare_weights(m, nf, d) for m in (wg, wu))
+    wd_p = q8p.q8_0_gemm_prepare_weights(wd, d, nf)
+    wsp_d = torch.empty(q8p.q8_0_gemm_prepared_workspace_bytes(nf, T, d), dtype=torch.uint8, device=dev)
+    wsp_f = torch.empty(q8p.q8_0_gemm_prepared_workspace_bytes(d, T, nf), dtype=torch.uint8, device=dev)
+    calls[1] = q8p.q8_0_gemm_prepared(None, wg_p, nf, d, *pa, T, G, workspace=wsp_d, bind=True)
+    calls[2] = q8p.q8_0_gemm_prepared(None, wu_p, nf, d, *pa, T, U, workspace=wsp_d, bind=True)
+    calls[4] = q8p.q8_0_gemm_prepared(None, wd_p, d, nf, *pb, T, O, workspace=wsp_f, bind=True)
+    for _ in range(warmup):
+        step()
+    q8p.q8_check()
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    q8p.q8_check()
+    prepared = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, nm in enumerate(names)}
+    return per, prepared
 
 
 # ---------------------------------------------------------------------------
@@ -995,6 +1013,35 @@ def run_stack_tokens(torch, q8p, reps, warmup, dev, tokens=STACK_TOKENS, layer_c
         for (name, _), (a, b) in zip(calls, evs):
             per.setdefault(name, []).append(a.elapsed_time(b))
         out[T] = dict(stack_ms=stack_ms, per_ms={nm: statistics.mean(v) for nm, v in per.items()}, reps=reps)
+    # the same passes on weights prepared once per matrix (f16 codes + d_w,
+    # q8_0_gemm_prepare_weights outside the timed region), for the token counts
+    # that take the tcgen05 GEMM
+    big = [T for T in tokens if q8p.q8_0_gemm_prepared_workspace_bytes(d, T, d) > 0]
+    if big:
+        prep = [[q8p.q8_0_gemm_prepare_weights(w, n, k) for (_, n, k), w in zip(shapes, lw)] for lw in layers]
+        head_p = q8p.q8_0_gemm_prepare_weights(head, V, d)
+        wsb = max(q8p.q8_0_gemm_prepared_workspace_bytes(n, T, k) for T in big for (_, n, k) in all_shapes)
+        wsp = torch.empty(max(wsb, 1024), dtype=torch.uint8, device=dev)
+        for T in big:
+            calls = [q8p.q8_0_gemm_prepared(None, wp, n, k, *planes[k], T, Y, workspace=wsp, bind=True)
+                     for pl in prep for (_, n, k), wp in zip(shapes, pl)]
+            calls.append(q8p.q8_0_gemm_prepared(None, head_p, V, d, *planes[d], T, Y, workspace=wsp, bind=True))
+            for _ in range(max(1, warmup // 3)):
+                for c in calls:
+                    c()
+            q8p.q8_check()
+            torch.cuda.synchronize(dev)
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hold_device(torch, 8 * len(calls))
+            t0.record(stream)
+            for _ in range(reps):
+                for c in calls:
+                    c()
+            t1.record(stream)
+            torch.cuda.synchronize(dev)
+            q8p.q8_check()
+            out[T]["stack_ms_prepared"] = t0.elapsed_time(t1) / reps
+        del prep, head_p, wsp
     return out
 
 
@@ -1302,21 +1349,23 @@ def main():
     if world > 1:  # every duration becomes the slowest rank's (same legs on every rank)
         vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"],
                   dec["iso_ms"]] if dec else [])
-                + (list(pre.values()) if pre else [])
+                + (list(pre[0].values()) + list(pre[1].values()) if pre else [])
                 + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else [])
                 + ([lay["ms"], lay["ms_two"], lay["ms_fused"]] if lay else [])
                 + ([shr["us"], shr["us_two"]] if shr else [])
                 + ([tiny["us"]] if tiny else [])
                 + ([v for T in sorted(stk) for v in [stk[T]["stack_ms"]] + [stk[T]["per_ms"][nm] for nm in
-                                                                             sorted(stk[T]["per_ms"])]] if stk else []))
+                                                                             sorted(stk[T]["per_ms"])]
+                    + ([stk[T]["stack_ms_prepared"]] if "stack_ms_prepared" in stk[T] else [])] if stk else []))
         red = max_over_ranks(torch, vals, dev)
         if dec:
             (dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"],
              dec["iso_ms"]) = red[:7]
             red = red[7:]
         if pre:
-            pre = dict(zip(pre.keys(), red[:len(pre)]))
-            red = red[len(pre):]
+            n0, n1 = len(pre[0]), len(pre[1])
+            pre = (dict(zip(pre[0].keys(), red[:n0])), dict(zip(pre[1].keys(), red[n0:n0 + n1])))
+            red = red[n0 + n1:]
         if small:
             small["us"], small["us_b2b"] = red.pop(0), red.pop(0)
         if asym:
@@ -1332,6 +1381,8 @@ def main():
                 stk[T]["stack_ms"] = red.pop(0)
                 for nm in sorted(stk[T]["per_ms"]):
                     stk[T]["per_ms"][nm] = red.pop(0)
+                if "stack_ms_prepared" in stk[T]:
+                    stk[T]["stack_ms_prepared"] = red.pop(0)
 
     if rank != 0:
         if world > 1:
@@ -1376,8 +1427,11 @@ def main():
         })
     if pre is not None:
         T, d, nf = PREFILL["tokens"], PREFILL["d"], PREFILL["nf"]
+        pre, pre_prep = pre
         gemm_ms = pre["gemm_gate"] + pre["gemm_up"] + pre["gemm_down"]
         tops = 3 * ops_gemm(T, nf, d) / (gemm_ms / 1e3) / 1e12
+        gemm_ms_p = pre_prep["gemm_gate"] + pre_prep["gemm_up"] + pre_prep["gemm_down"]
+        tops_p = 3 * ops_gemm(T, nf, d) / (gemm_ms_p / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         pobj = {
             "workload": f"prefill chain T={T} d={d} nf={nf}: rmsnorm_quant, gate/up GEMM, swiglu_quant, down GEMM "
@@ -1399,6 +1453,13 @@ def main():
                              "timing": "each call bracketed by its own CUDA events (no overlap with its neighbours)",
                              "peak": peaks["hbm_gbs"]},
             "l2": "step working set ~1.2 GB > L2",
+            "prepared_weights": {
+                "calls": "the same chain with q8_0_gemm_prepared: each weight matrix widened to f16 once "
+                         "(q8_0_gemm_prepare_weights, outside the timed region), so a GEMM call runs its "
+                         "activation pre-pass and the tcgen05 kernel only",
+                "ms_per_chain": round(sum(pre_prep.values()), 4),
+                "ms": {k: round(v, 4) for k, v in pre_prep.items()},
+                "gemm_tops": round(tops_p, 2), "frac": round(tops_p / peak, 4)},
         }
         if dec is None:  # prefill-only run: the GEMM throughput (all replicas) is the headline
             line.update({"value": round(world * pobj["gemm_tops"], 2), "unit": "TOPS",
@@ -1550,6 +1611,12 @@ def main():
             sw[str(T)] = {"tokens": T, "ms_per_pass": round(r["stack_ms"], 4), "tops": round(tops, 2),
                           "gbs": round(gbs, 1), "int8_ops": ops, "algorithmic_bytes": byts, "roofline": roof,
                           "per_shape": per, "cpu_baseline": cpu_legs.get(f"stack_{T}"), "passes_timed": r["reps"]}
+            if "stack_ms_prepared" in r:
+                tp = ops / (r["stack_ms_prepared"] / 1e3) / 1e12
+                sw[str(T)]["prepared_weights"] = {
+                    "ms_per_pass": round(r["stack_ms_prepared"], 4), "tops": round(tp, 2),
+                    "frac": round(tp / peaks["bf16_tflops_sustained"], 4),
+                    "calls": "q8_0_gemm_prepared on weights widened once per matrix (outside the timed region)"}
         sobj3 = {"workload": f"layer-stack sweep through q8_0_gemm: {L['layers']} layers x (q {L['q']}, k/v {L['kv']}, "
                              f"o {L['d']}, gate/up {L['nf']} at k={L['d']}; down {L['d']} at k={L['nf']}) + LM head "
                              f"{L['vocab']}x{L['d']}, one call per projection ({7 * L['layers'] + 1} calls per pass) on "

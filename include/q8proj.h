@@ -345,6 +345,54 @@ Q8_API int q8_0_gemm(const void *w, int64_t n, int64_t k,
                      float *y, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Prepared weights for the prefill GEMM.  A model's weights do not change
+ * between calls, so the weight pre-pass that q8_0_gemm enqueues on every
+ * call (the codes widened to f16 exactly, d_w as f32 in the epilogue's
+ * order) can run once per matrix instead:
+ *
+ * q8_0_gemm_prepared_weights_bytes -- size of the prepared form of an n x k
+ * Q8_0 matrix: n*k*2 bytes of f16 codes and k/32*4 bytes of d_w per weight
+ * row (rows rounded up to the GEMM's 128-row tiles), each part starting on a
+ * 1 KiB boundary.  0 when (k/32) % 8 != 0 or the shape is past the GEMM's
+ * grid limits (n > 65535*128, k > 2^30).
+ *
+ * q8_0_gemm_prepare_weights -- write that form of w into wprep (caller-owned
+ * device memory of at least q8_0_gemm_prepared_weights_bytes(n, k) bytes,
+ * 16-byte aligned; its layout is private to this library and valid for this
+ * (n, k) only).  One kernel, enqueued on `stream` with programmatic dependent
+ * launch.  Q8_ERR_ARG for a NULL pointer, a short buffer or a shape the GEMM
+ * does not take, Q8_ERR_ALIGN for misaligned pointers.
+ *
+ * q8_0_gemm_prepared_workspace_bytes -- device workspace q8_0_gemm_prepared
+ * needs: q8_0_gemm_workspace_bytes without the two weight parts.  0 when the
+ * call takes a path that needs none (t <= 64 or (k/32) % 8 != 0).
+ *
+ * q8_0_gemm_prepared -- q8_0_gemm whose tcgen05 path reads prepared weights:
+ * the same result, bit for bit, as q8_0_gemm(w, ...) (the same kernels on
+ * the same operands), without the per-call weight pre-pass.
+ *   w      : the Q8_0 matrix, read by the paths for t <= 64 and for
+ *            (k/32) % 8 != 0; may be NULL when the call takes the tcgen05
+ *            path (t > 64 and (k/32) % 8 == 0)
+ *   wprep  : q8_0_gemm_prepare_weights(w, n, k, ...)'s output, read by the
+ *            tcgen05 path (may be NULL otherwise).  Written earlier on this
+ *            stream, or ordered before this call by the caller.
+ *   qs, ds, t, rows_pad, y : as for q8_0_gemm
+ *   workspace, workspace_bytes : at least
+ *            q8_0_gemm_prepared_workspace_bytes(n, t, k) bytes, as for
+ *            q8_0_gemm
+ * "12 - r5-r6 re-ranking + structural rewrite spec", sec. 2 and 3.1 (the
+ * per-block scale correction); "54 - r51 - producer-fused A-quantize mode 1",
+ * sec. 2.1 (the plane).
+ */
+Q8_API size_t q8_0_gemm_prepared_weights_bytes(int64_t n, int64_t k);
+Q8_API int q8_0_gemm_prepare_weights(const void *w, int64_t n, int64_t k,
+                                     void *wprep, size_t wprep_bytes, void *stream);
+Q8_API size_t q8_0_gemm_prepared_workspace_bytes(int64_t n, int64_t t, int64_t k);
+Q8_API int q8_0_gemm_prepared(const void *w, const void *wprep, int64_t n, int64_t k,
+                              const int8_t *qs, const uint32_t *ds, int64_t t, int64_t rows_pad,
+                              float *y, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * q8_0_gemm_noalloc -- q8_0_gemm without a workspace argument, for callers
  * that cannot allocate device memory at this point: a serving engine that
  * handed all of the GPU's memory to its own pool at start-up, a plugin whose

@@ -17,6 +17,10 @@ from ._binding import (  # noqa: F401
     q8_0_gemm,
     q8_0_gemm_mma,
     q8_0_gemm_noalloc,
+    q8_0_gemm_prepare_weights,
+    q8_0_gemm_prepared,
+    q8_0_gemm_prepared_weights_bytes,
+    q8_0_gemm_prepared_workspace_bytes,
     q8_0_gemm_workspace_bytes,
     q8_0_gemv,
     q8_0_gemv_grouped,

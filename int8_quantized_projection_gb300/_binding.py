@@ -33,6 +33,10 @@ SIGNATURES = {
     "q8_0_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q8_0_gemm_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "q8_0_gemm": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, ctypes.c_size_t, _P]),
+    "q8_0_gemm_prepared_weights_bytes": (ctypes.c_size_t, [_I64, _I64]),
+    "q8_0_gemm_prepare_weights": (_INT, [_P, _I64, _I64, _P, ctypes.c_size_t, _P]),
+    "q8_0_gemm_prepared_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64]),
+    "q8_0_gemm_prepared": (_INT, [_P, _P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, ctypes.c_size_t, _P]),
     "q8_0_gemm_mma": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
     "q8_0_gemm_noalloc": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P]),
     "q8_0_gemm_noalloc_max_bytes": (ctypes.c_size_t, []),
@@ -349,6 +353,66 @@ def gemm_workspace(n: int, t: int, k: int, device="cuda"):
 
     nbytes = q8_0_gemm_workspace_bytes(n, t, k)
     return torch.empty(nbytes, dtype=torch.uint8, device=device) if nbytes else None
+
+
+def q8_0_gemm_prepared_weights_bytes(n: int, k: int) -> int:
+    return int(lib().q8_0_gemm_prepared_weights_bytes(n, k))
+
+
+def q8_0_gemm_prepared_workspace_bytes(n: int, t: int, k: int) -> int:
+    return int(lib().q8_0_gemm_prepared_workspace_bytes(n, t, k))
+
+
+def q8_0_gemm_prepare_weights(w, n: int, k: int, wprep=None, stream=None):
+    """Write the GEMM's prepared form of the Q8_0 matrix ``w`` (n x k) into
+    ``wprep`` (a uint8 CUDA tensor of q8_0_gemm_prepared_weights_bytes(n, k)
+    bytes; allocated here with PyTorch when None) and return it."""
+    import torch
+
+    _need(w, torch.uint8, "w")
+    if w.numel() != n * (k // 32) * 34:
+        raise ValueError("shape mismatch")
+    nbytes = q8_0_gemm_prepared_weights_bytes(n, k)
+    if nbytes == 0:
+        raise ValueError("no prepared form for this shape ((k/32) % 8 != 0 or past the GEMM's limits)")
+    if wprep is None:
+        wprep = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    _need(wprep, torch.uint8, "wprep")
+    _check("q8_0_gemm_prepare_weights",
+           lib().q8_0_gemm_prepare_weights(_ptr(w), n, k, _ptr(wprep), wprep.numel(), _stream(stream)))
+    return wprep
+
+
+def q8_0_gemm_prepared(w, wprep, n: int, k: int, qs, ds, t: int, y, workspace=None, stream=None, bind=False):
+    """q8_0_gemm whose tcgen05 path reads ``wprep`` (q8_0_gemm_prepare_weights's
+    output) instead of widening ``w`` on every call; ``w`` serves the other
+    paths (t <= 64, (k/32) % 8 != 0) and may be None when the call takes the
+    tcgen05 path."""
+    import torch
+
+    _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds"), _need(y, torch.float32, "y")
+    if w is not None:
+        _need(w, torch.uint8, "w")
+    if wprep is not None:
+        _need(wprep, torch.uint8, "wprep")
+    rows_pad = qs.shape[0]
+    if y.numel() < t * n or qs.shape[-1] != k or ds.shape[0] != rows_pad:
+        raise ValueError("shape mismatch")
+    nbytes = q8_0_gemm_prepared_workspace_bytes(n, t, k)
+    if workspace is None and nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=y.device)
+    if workspace is not None:
+        _need(workspace, torch.uint8, "workspace")
+    nul = ctypes.c_void_p(0)
+    args = (_ptr(w) if w is not None else nul, _ptr(wprep) if wprep is not None else nul, n, k, _ptr(qs), _ptr(ds),
+            t, rows_pad, _ptr(y), _ptr(workspace) if workspace is not None else nul,
+            workspace.numel() if workspace is not None else 0, _stream(stream))
+    if bind:
+        b = Bound("q8_0_gemm_prepared", args)
+        b._keep = (workspace, w, wprep)
+        return b
+    _check("q8_0_gemm_prepared", lib().q8_0_gemm_prepared(*args))
+    return None
 
 
 def q8_0_gemm(w, n: int, k: int, qs, ds, t: int, y, workspace=None, stream=None, bind=False):

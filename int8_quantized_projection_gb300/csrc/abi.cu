@@ -121,6 +121,11 @@ int gemm_mma_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const
 int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t, float *y,
                    void *workspace, cudaStream_t s);
 size_t gemm_workspace_bytes(int64_t n, int64_t t, int64_t k);
+size_t gemm_prepared_workspace_bytes(int64_t n, int64_t t, int64_t k);
+size_t gemm_prepared_weights_bytes(int64_t n, int64_t k);
+int gemm_prepare_weights_launch(const void *w, int64_t n, int64_t k, void *wprep, cudaStream_t s);
+int gemm_tc_prepared_launch(const void *wprep, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t,
+                            float *y, void *workspace, cudaStream_t s);
 
 } // namespace q8
 
@@ -176,6 +181,13 @@ int gemv_sliced_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, co
 
 } // namespace q8
 
+// The tcgen05 GEMM's grid limits: token tiles of 192 along x, weight-row
+// tiles of 128 along y (at most 65535), f16 operand rows addressed in 32 bits.
+static bool gemm_tc_shape_ok(int64_t n, int64_t t, int64_t k)
+{
+    return n <= int64_t(65535) * 128 && t <= (int64_t(1) << 31) - 256 && k <= (int64_t(1) << 31) / 2;
+}
+
 extern "C" size_t q8_0_gemm_workspace_bytes(int64_t n, int64_t t, int64_t k)
 {
     if (n < 1 || t <= q8::kSlicedMaxTokens || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0) return 0;
@@ -199,9 +211,50 @@ extern "C" int q8_0_gemm(const void *w, int64_t n, int64_t k, const int8_t *qs, 
     }
     if (t <= Q8_GEMV_MAX_TOKENS) return q8::gemv_small_launch(w, n, k, qs, ds, y, t, s);
     if (t <= q8::kSlicedMaxTokens) return q8::gemv_sliced_launch(w, n, k, qs, ds, y, t, s);
-    // grid: token tiles of 192 along x, weight-row tiles of 128 along y (at most 65535)
-    if (n > int64_t(65535) * 128 || t > (int64_t(1) << 31) - 256 || k > (int64_t(1) << 31) / 2) return Q8_ERR_ARG;
+    if (!gemm_tc_shape_ok(n, t, k)) return Q8_ERR_ARG;
     return q8::gemm_tc_launch(w, n, k, qs, ds, t, y, workspace, s);
+}
+
+extern "C" size_t q8_0_gemm_prepared_weights_bytes(int64_t n, int64_t k)
+{
+    if (n < 1 || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0 || !gemm_tc_shape_ok(n, 1, k)) return 0;
+    return q8::gemm_prepared_weights_bytes(n, k);
+}
+
+extern "C" int q8_0_gemm_prepare_weights(const void *w, int64_t n, int64_t k, void *wprep, size_t wprep_bytes,
+                                         void *stream)
+{
+    if (!w || !wprep || n < 1 || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0 || !gemm_tc_shape_ok(n, 1, k))
+        return Q8_ERR_ARG;
+    if (wprep_bytes < q8_0_gemm_prepared_weights_bytes(n, k)) return Q8_ERR_ARG;
+    if (!q8::aligned16(w) || !q8::aligned16(wprep)) return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    return q8::gemm_prepare_weights_launch(w, n, k, wprep, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t q8_0_gemm_prepared_workspace_bytes(int64_t n, int64_t t, int64_t k)
+{
+    if (n < 1 || t <= q8::kSlicedMaxTokens || k <= 0 || (k % 32) != 0 || (k / 32) % 8 != 0) return 0;
+    return q8::gemm_prepared_workspace_bytes(n, t, k);
+}
+
+extern "C" int q8_0_gemm_prepared(const void *w, const void *wprep, int64_t n, int64_t k, const int8_t *qs,
+                                  const uint32_t *ds, int64_t t, int64_t rows_pad, float *y, void *workspace,
+                                  size_t workspace_bytes, void *stream)
+{
+    if (!qs || !ds || !y || n < 1 || t < 1 || k <= 0 || (k % 32) != 0 || rows_pad < t) return Q8_ERR_ARG;
+    const bool tc = (k / 32) % 8 == 0 && t > q8::kSlicedMaxTokens;  // the tcgen05 path reads wprep, the rest w
+    if (tc ? !wprep : !w) return Q8_ERR_ARG;
+    if (!q8::aligned16(qs) || !q8::aligned16(ds) || !q8::aligned16(y) ||
+        (tc ? !q8::aligned16(wprep) : !q8::aligned16(w)))
+        return Q8_ERR_ALIGN;
+    if (!tc) return q8_0_gemm(w, n, k, qs, ds, t, rows_pad, y, nullptr, 0, stream);
+    const size_t need = q8_0_gemm_prepared_workspace_bytes(n, t, k);
+    if (!workspace || workspace_bytes < need) return Q8_ERR_ARG;
+    if (!q8::aligned16(workspace)) return Q8_ERR_ALIGN;
+    if (!gemm_tc_shape_ok(n, t, k)) return Q8_ERR_ARG;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    return q8::gemm_tc_prepared_launch(wprep, n, k, qs, ds, t, y, workspace, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int q8_0_gemm_mma(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t,

@@ -612,25 +612,94 @@ int gemm_splits(int64_t n, int64_t t, int64_t k)
 }
 
 // Workspace layout for (n, t, k): [f16 weights | f16 activation | d_w tiles |
-// d_a tiles | partial tiles (split-K only: splits x t x n f32)].
+// d_a tiles | partial tiles (split-K only: splits x t x n f32)].  With
+// prepared weights (q8_0_gemm_prepared) the two weight parts live in the
+// caller's prepared buffer instead, [f16 weights | d_w tiles], and the
+// workspace holds the rest in the same order.
 struct WsLayout {
     size_t a16, b16, dwt, dat, part, total;
     int splits;
 };
 
-WsLayout ws_layout(int64_t n, int64_t t, int64_t k)
+size_t up1k(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
+
+size_t dwt_bytes(int64_t n, int64_t k) { return static_cast<size_t>((n + BM - 1) / BM) * (k / 32) * BM * 4; }
+
+WsLayout ws_layout(int64_t n, int64_t t, int64_t k, bool prepared = false)
 {
-    auto up = [](size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); };
     const size_t nb = static_cast<size_t>(k / 32);
     WsLayout L;
     L.splits = gemm_splits(n, t, k);
     L.a16 = 0;
-    L.b16 = up(L.a16 + static_cast<size_t>(n) * k * 2);
-    L.dwt = up(L.b16 + static_cast<size_t>(t) * k * 2);
-    L.dat = up(L.dwt + static_cast<size_t>((n + BM - 1) / BM) * nb * BM * 4);
-    L.part = up(L.dat + static_cast<size_t>((t + BN - 1) / BN) * nb * BN * 4);
-    L.total = up(L.part + (L.splits > 1 ? static_cast<size_t>(L.splits) * t * n * 4 : 0));
+    L.b16 = prepared ? 0 : up1k(L.a16 + static_cast<size_t>(n) * k * 2);
+    L.dwt = up1k(L.b16 + static_cast<size_t>(t) * k * 2);
+    L.dat = prepared ? L.dwt : up1k(L.dwt + dwt_bytes(n, k));
+    L.part = up1k(L.dat + static_cast<size_t>((t + BN - 1) / BN) * nb * BN * 4);
+    L.total = up1k(L.part + (L.splits > 1 ? static_cast<size_t>(L.splits) * t * n * 4 : 0));
     return L;
+}
+
+// Prepared weights: [f16 codes n x k | d_w tiles], the weight pre-pass's output.
+size_t prep_w_dwt_offset(int64_t n, int64_t k) { return up1k(static_cast<size_t>(n) * k * 2); }
+size_t prep_w_bytes(int64_t n, int64_t k) { return up1k(prep_w_dwt_offset(n, k) + dwt_bytes(n, k)); }
+
+// The weight pre-pass: Q8_0 rows -> f16 codes [n][k] and d_w in tile order.
+int launch_prep_w(const void *w, int64_t n, int64_t k, uint8_t *a16, float *dwt, cudaStream_t s)
+{
+    const int64_t nb = k / 32;
+    const int sms = q8::device_sm_count();
+    const int64_t pcap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
+    const int64_t groups = (n + BM - 1) / BM * (BM / 32);
+    const int64_t wide = groups * ((nb + 31) / 32);  // items of 32 blocks
+    const bool many = wide >= static_cast<int64_t>(sms > 0 ? sms : 152) * 4;
+    const int64_t witems = many ? wide : groups * ((nb + 7) / 8);
+    const unsigned wgrid = static_cast<unsigned>(witems < pcap ? witems : pcap);
+    return many ? q8::launch_pdl(gemm_prep_w_kernel<32, 256>, dim3(wgrid), dim3(256), 0, s,
+                                 static_cast<const uint8_t *>(w), n, static_cast<int>(nb),
+                                 reinterpret_cast<uint4 *>(a16), dwt)
+                : q8::launch_pdl(gemm_prep_w_kernel<8, 256>, dim3(wgrid), dim3(256), 0, s,
+                                 static_cast<const uint8_t *>(w), n, static_cast<int>(nb),
+                                 reinterpret_cast<uint4 *>(a16), dwt);
+}
+
+// The activation pre-pass, the GEMM and (split-K) the reduction, on weight
+// operands already in the pre-pass's form.
+int gemm_tc_core(const uint8_t *a16, const float *dwt, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds,
+                 int64_t t, float *y, uint8_t *b16, float *dat, float *part, int splits, cudaStream_t s)
+{
+    const int64_t nb = k / 32;
+    CUtensorMap ma, mb;
+    if (!q8::make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, a16, static_cast<uint64_t>(k), static_cast<uint64_t>(n),
+                         static_cast<uint64_t>(k * 2), 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !q8::make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT16, b16, static_cast<uint64_t>(k), static_cast<uint64_t>(t),
+                         static_cast<uint64_t>(k * 2), 64, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return Q8_ERR_LAUNCH;
+    const int sms = q8::device_sm_count();
+    const int64_t pcap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
+    const int64_t awork = t * (k / 16) + (t + BN - 1) / BN * nb * BN;
+    int64_t agrid = (awork + 255) / 256;
+    agrid = agrid < pcap ? agrid : pcap;
+    int st = q8::launch_pdl(gemm_prep_a_kernel, dim3(static_cast<unsigned>(agrid)), dim3(256), 0, s,
+                            reinterpret_cast<const uint4 *>(qs), ds, t, k, reinterpret_cast<uint4 *>(b16), dat);
+    if (st != Q8_OK) return st;
+    const dim3 grid(static_cast<unsigned>((t + BN - 1) / BN), static_cast<unsigned>((n + BM - 1) / BM),
+                    static_cast<unsigned>(splits));
+    if (splits == 1) {
+        if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel<false>), kSmemBytes, 2))
+            return Q8_ERR_LAUNCH;
+        return q8::launch_pdl(gemm_tc_kernel<false>, grid, dim3(kThreads), kSmemBytes, s, ma, mb, dwt, dat, n, t,
+                              static_cast<int>(nb), y, part);
+    }
+    if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel<true>), kSmemBytes, 9))
+        return Q8_ERR_LAUNCH;
+    st = q8::launch_pdl(gemm_tc_kernel<true>, grid, dim3(kThreads), kSmemBytes, s, ma, mb, dwt, dat, n, t,
+                        static_cast<int>(nb), y, part);
+    if (st != Q8_OK) return st;
+    const int64_t count = t * n;
+    int64_t rgrid = (count + 255) / 256;
+    rgrid = rgrid < pcap ? rgrid : pcap;
+    return q8::launch_pdl(gemm_split_reduce_kernel, dim3(static_cast<unsigned>(rgrid)), dim3(256), 0, s,
+                          static_cast<const float *>(part), splits, count, y);
 }
 
 } // namespace
@@ -649,60 +718,43 @@ int gemm_take_error(cudaStream_t s)
 
 size_t gemm_workspace_bytes(int64_t n, int64_t t, int64_t k) { return ws_layout(n, t, k).total; }
 
+size_t gemm_prepared_workspace_bytes(int64_t n, int64_t t, int64_t k) { return ws_layout(n, t, k, true).total; }
+
+size_t gemm_prepared_weights_bytes(int64_t n, int64_t k) { return prep_w_bytes(n, k); }
+
 // Requires k/32 % 8 == 0, 16-byte aligned pointers and a workspace of at least
 // gemm_workspace_bytes(n, t, k) bytes (checked by the caller).
 int gemm_tc_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t, float *y,
                    void *workspace, cudaStream_t s)
 {
-    const int64_t nb = k / 32;
     const WsLayout L = ws_layout(n, t, k);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    uint8_t *a16 = ws + L.a16, *b16 = ws + L.b16;
-    float *dwt = reinterpret_cast<float *>(ws + L.dwt), *dat = reinterpret_cast<float *>(ws + L.dat);
-    CUtensorMap ma, mb;
-    if (!make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, a16, static_cast<uint64_t>(k), static_cast<uint64_t>(n),
-                     static_cast<uint64_t>(k * 2), 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT16, b16, static_cast<uint64_t>(k), static_cast<uint64_t>(t),
-                     static_cast<uint64_t>(k * 2), 64, BN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return Q8_ERR_LAUNCH;
-    const int sms = device_sm_count();
-    const int64_t pcap = static_cast<int64_t>(sms > 0 ? sms : 152) * 8;
-    const int64_t groups = (n + BM - 1) / BM * (BM / 32);
-    const int64_t wide = groups * ((nb + 31) / 32);  // items of 32 blocks
-    const bool many = wide >= static_cast<int64_t>(sms > 0 ? sms : 152) * 4;
-    const int64_t witems = many ? wide : groups * ((nb + 7) / 8);
-    const unsigned wgrid = static_cast<unsigned>(witems < pcap ? witems : pcap);
-    int st = many ? launch_pdl(gemm_prep_w_kernel<32, 256>, dim3(wgrid), dim3(256), 0, s,
-                               static_cast<const uint8_t *>(w), n, static_cast<int>(nb),
-                               reinterpret_cast<uint4 *>(a16), dwt)
-                  : launch_pdl(gemm_prep_w_kernel<8, 256>, dim3(wgrid), dim3(256), 0, s,
-                               static_cast<const uint8_t *>(w), n, static_cast<int>(nb),
-                               reinterpret_cast<uint4 *>(a16), dwt);
+    uint8_t *a16 = ws + L.a16;
+    float *dwt = reinterpret_cast<float *>(ws + L.dwt);
+    const int st = launch_prep_w(w, n, k, a16, dwt, s);
     if (st != Q8_OK) return st;
-    const int64_t awork = t * (k / 16) + (t + BN - 1) / BN * nb * BN;
-    int64_t agrid = (awork + 255) / 256;
-    agrid = agrid < pcap ? agrid : pcap;
-    st = launch_pdl(gemm_prep_a_kernel, dim3(static_cast<unsigned>(agrid)), dim3(256), 0, s,
-                    reinterpret_cast<const uint4 *>(qs), ds, t, k, reinterpret_cast<uint4 *>(b16), dat);
-    if (st != Q8_OK) return st;
-    float *part = reinterpret_cast<float *>(ws + L.part);
-    const dim3 grid(static_cast<unsigned>((t + BN - 1) / BN), static_cast<unsigned>((n + BM - 1) / BM),
-                    static_cast<unsigned>(L.splits));
-    if (L.splits == 1) {
-        if (!set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel<false>), kSmemBytes, 2))
-            return Q8_ERR_LAUNCH;
-        return launch_pdl(gemm_tc_kernel<false>, grid, dim3(kThreads), kSmemBytes, s, ma, mb, dwt, dat, n, t,
-                          static_cast<int>(nb), y, part);
-    }
-    if (!set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel<true>), kSmemBytes, 9)) return Q8_ERR_LAUNCH;
-    st = launch_pdl(gemm_tc_kernel<true>, grid, dim3(kThreads), kSmemBytes, s, ma, mb, dwt, dat, n, t,
-                    static_cast<int>(nb), y, part);
-    if (st != Q8_OK) return st;
-    const int64_t count = t * n;
-    int64_t rgrid = (count + 255) / 256;
-    rgrid = rgrid < pcap ? rgrid : pcap;
-    return launch_pdl(gemm_split_reduce_kernel, dim3(static_cast<unsigned>(rgrid)), dim3(256), 0, s,
-                      static_cast<const float *>(part), L.splits, count, y);
+    return gemm_tc_core(a16, dwt, n, k, qs, ds, t, y, ws + L.b16, reinterpret_cast<float *>(ws + L.dat),
+                        reinterpret_cast<float *>(ws + L.part), L.splits, s);
+}
+
+// The weight pre-pass alone, into a caller's buffer of prep_w_bytes(n, k).
+int gemm_prepare_weights_launch(const void *w, int64_t n, int64_t k, void *wprep, cudaStream_t s)
+{
+    uint8_t *p = static_cast<uint8_t *>(wprep);
+    return launch_prep_w(w, n, k, p, reinterpret_cast<float *>(p + prep_w_dwt_offset(n, k)), s);
+}
+
+// The GEMM on prepared weights: the activation pre-pass, the GEMM and (split-K)
+// the reduction; the workspace is gemm_prepared_workspace_bytes(n, t, k).
+int gemm_tc_prepared_launch(const void *wprep, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, int64_t t,
+                            float *y, void *workspace, cudaStream_t s)
+{
+    const WsLayout L = ws_layout(n, t, k, true);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const uint8_t *p = static_cast<const uint8_t *>(wprep);
+    return gemm_tc_core(p, reinterpret_cast<const float *>(p + prep_w_dwt_offset(n, k)), n, k, qs, ds, t, y,
+                        ws + L.b16, reinterpret_cast<float *>(ws + L.dat), reinterpret_cast<float *>(ws + L.part),
+                        L.splits, s);
 }
 
 } // namespace q8

@@ -155,6 +155,51 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert gu(64, 3584, 0, 0, 1, MISALIGNED, 0, 0, FAKE, FAKE) == ERR_ALIGN
 
 
+def test_prepared_gemm_sizes_and_argument_errors(lib):
+    """The prepared-weight GEMM entry points: sizes as a function of the shape
+    (the weight pre-pass's two parts; the workspace without them) and the
+    argument errors reported before any device work."""
+    s = P(0)
+    ERR_ARG, ERR_ALIGN = 1, 2
+    up = lambda v: -(-v // 1024) * 1024  # noqa: E731
+    # [f16 codes n x k | d_w per 128-row tile], each from a 1 KiB boundary
+    assert lib.q8_0_gemm_prepared_weights_bytes(8, 256) == up(up(8 * 256 * 2) + 1 * 8 * 128 * 4)
+    assert lib.q8_0_gemm_prepared_weights_bytes(18944, 3584) == up(up(18944 * 3584 * 2) + 148 * 112 * 128 * 4)
+    assert lib.q8_0_gemm_prepared_weights_bytes(8, 96) == 0           # (k/32) % 8 != 0: no tcgen05 path
+    assert lib.q8_0_gemm_prepared_weights_bytes(65535 * 128 + 1, 256) == 0  # past the grid's weight-row tiles
+    # the workspace is q8_0_gemm's without the weight parts
+    assert lib.q8_0_gemm_prepared_workspace_bytes(8, 100, 256) == up(up(100 * 256 * 2) + 1 * 8 * 192 * 4)
+    for n, t, k in ((18944, 3325, 3584), (256, 130, 2048), (512, 512, 3584)):
+        full = lib.q8_0_gemm_workspace_bytes(n, t, k)
+        prep = lib.q8_0_gemm_prepared_workspace_bytes(n, t, k)
+        wparts = up(n * k * 2) + up(-(-n // 128) * (k // 32) * 128 * 4)
+        assert prep == full - wparts, (n, t, k)
+    assert lib.q8_0_gemm_prepared_workspace_bytes(8, 64, 256) == 0  # t <= 64: no workspace
+    assert lib.q8_0_gemm_prepared_workspace_bytes(8, 100, 96) == 0  # generic kernel
+    wpb = lib.q8_0_gemm_prepared_weights_bytes(8, 256)
+    prep = lib.q8_0_gemm_prepare_weights
+    assert prep(P(0), 8, 256, P(FAKE), wpb, s) == ERR_ARG               # no weights
+    assert prep(P(FAKE), 8, 256, P(0), wpb, s) == ERR_ARG               # no buffer
+    assert prep(P(FAKE), 8, 256, P(FAKE), wpb - 1, s) == ERR_ARG        # short buffer
+    assert prep(P(FAKE), 8, 96, P(FAKE), 1 << 20, s) == ERR_ARG         # no prepared form
+    assert prep(P(FAKE), 0, 256, P(FAKE), wpb, s) == ERR_ARG            # n < 1
+    assert prep(P(FAKE + 2), 8, 256, P(FAKE), wpb, s) == ERR_ALIGN
+    assert prep(P(FAKE), 8, 256, P(MISALIGNED), wpb, s) == ERR_ALIGN
+    ws = lib.q8_0_gemm_prepared_workspace_bytes(8, 100, 256)
+    gp = lambda w, wp, k, t, rp, wsp, wsb: lib.q8_0_gemm_prepared(  # noqa: E731
+        P(w), P(wp), 8, k, P(FAKE), P(FAKE), t, rp, P(FAKE), P(wsp), wsb, s)
+    assert gp(FAKE, 0, 256, 100, 100, FAKE, ws) == ERR_ARG          # the tcgen05 path needs the prepared weights
+    assert gp(0, FAKE, 256, 40, 40, 0, 0) == ERR_ARG                # t <= 64 reads the Q8_0 weights
+    assert gp(0, FAKE, 96, 100, 100, 0, 0) == ERR_ARG               # so does the generic kernel
+    assert gp(0, FAKE, 256, 100, 100, FAKE, ws - 1) == ERR_ARG      # short workspace
+    assert gp(0, FAKE, 256, 100, 100, 0, ws) == ERR_ARG             # no workspace
+    assert gp(0, FAKE, 256, 100, 99, FAKE, ws) == ERR_ARG           # rows_pad < t
+    assert gp(0, FAKE, 256, 0, 4, FAKE, ws) == ERR_ARG              # t < 1
+    assert gp(0, MISALIGNED, 256, 100, 100, FAKE, ws) == ERR_ALIGN
+    assert gp(0, FAKE, 256, 100, 100, MISALIGNED, ws) == ERR_ALIGN
+    assert gp(FAKE + 2, 0, 256, 40, 40, 0, 0) == ERR_ALIGN
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_binding, "_lib", None)
     monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
