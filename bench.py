@@ -44,7 +44,7 @@ PREFILL = dict(tokens=3325, d=3584, nf=18944, eps=1e-6)
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of a kernel, from
 # the ncu capture summarised under profiles/; None until taken, and reset to
 # None whenever that kernel changes (the figure would describe old code).
-NCU_TRAFFIC_BYTES = {"gemv_fused 12288x7168+96x7168": 97_675_776,      # profiles/gemv_fused_quant_12288x7168_plus_96x7168.md
+NCU_TRAFFIC_BYTES = {"gemv_fused 12288x7168+96x7168": 97_524_224,      # profiles/gemv_fused_quant_12288x7168_plus_96x7168.md
                      "gemm_tc 18944x3584 t=3325": 397_260_544,         # profiles/gemm_tc_18944x3584_t3325.md
                      "gemv_small 12288x7168 t=16": 97_903_616,         # profiles/gemv_small_12288x7168_t16.md
                      "gemv_staged_q4a 12288x7168": 55_095_552}         # profiles/gemv_staged_q4a_12288x7168.md
@@ -601,6 +601,28 @@ def run_prefill(torch, q8p, steps, warmup, dev):
     torch.cuda.synchronize(dev)
     q8p.q8_check()
     per["quantize_q8_0 (standalone, not in the chain)"] = statistics.mean(a.elapsed_time(b) for a, b in qev)
+    # each producer back to back (as in a chain of layers, the next call's start
+    # under the previous one's tail): 20 calls between one pair of events, the
+    # f32 inputs rotating over copies that together exceed L2
+    xs = [x] + [x.clone() for _ in range(-(-L2_BYTES // (4 * x.numel())))]  # > L2 together
+    b2b = {}
+    for nm, cl in (("rmsnorm_quant", [q8p.rmsnorm_quant(xc, w, eps, None, *pa, bind=True) for xc in xs]),
+                   ("swiglu_quant", [q8p.swiglu_quant(G, U, None, *pb, bind=True)]),
+                   ("quantize_q8_0", [q8p.quantize_q8_0(xc, *pa, bind=True) for xc in xs])):
+        for i in range(max(3, warmup)):
+            cl[i % len(cl)]()
+        q8p.q8_check()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_device(torch, 20)
+        e0.record(stream)
+        for i in range(20):
+            cl[i % len(cl)]()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        q8p.q8_check()
+        b2b[nm] = e0.elapsed_time(e1) / 20
+    del xs
     # the same chain on weights prepared once per matrix (q8_0_gemm_prepare_weights,
     # outside the timed region): the GEMMs skip their per-call weight pre-pass
     wg_p, wu_p = (q8p.q8_0_gemm_prepare_weights(m, nf, d) for m in (wg, wu))
@@ -619,7 +641,7 @@ def run_prefill(torch, q8p, steps, warmup, dev):
     torch.cuda.synchronize(dev)
     q8p.q8_check()
     prepared = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, nm in enumerate(names)}
-    return per, prepared
+    return per, prepared, b2b
 
 
 # ---------------------------------------------------------------------------
@@ -1349,7 +1371,7 @@ def main():
     if world > 1:  # every duration becomes the slowest rank's (same legs on every rank)
         vals = (([dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"],
                   dec["iso_ms"]] if dec else [])
-                + (list(pre[0].values()) + list(pre[1].values()) if pre else [])
+                + (list(pre[0].values()) + list(pre[1].values()) + list(pre[2].values()) if pre else [])
                 + ([small["us"], small["us_b2b"]] if small else []) + ([asym["us"], asym["us_b2b"]] if asym else [])
                 + ([lay["ms"], lay["ms_two"], lay["ms_fused"]] if lay else [])
                 + ([shr["us"], shr["us_two"]] if shr else [])
@@ -1363,9 +1385,10 @@ def main():
              dec["iso_ms"]) = red[:7]
             red = red[7:]
         if pre:
-            n0, n1 = len(pre[0]), len(pre[1])
-            pre = (dict(zip(pre[0].keys(), red[:n0])), dict(zip(pre[1].keys(), red[n0:n0 + n1])))
-            red = red[n0 + n1:]
+            n0, n1, n2 = len(pre[0]), len(pre[1]), len(pre[2])
+            pre = (dict(zip(pre[0].keys(), red[:n0])), dict(zip(pre[1].keys(), red[n0:n0 + n1])),
+                   dict(zip(pre[2].keys(), red[n0 + n1:n0 + n1 + n2])))
+            red = red[n0 + n1 + n2:]
         if small:
             small["us"], small["us_b2b"] = red.pop(0), red.pop(0)
         if asym:
@@ -1427,7 +1450,7 @@ def main():
         })
     if pre is not None:
         T, d, nf = PREFILL["tokens"], PREFILL["d"], PREFILL["nf"]
-        pre, pre_prep = pre
+        pre, pre_prep, pre_b2b = pre
         gemm_ms = pre["gemm_gate"] + pre["gemm_up"] + pre["gemm_down"]
         tops = 3 * ops_gemm(T, nf, d) / (gemm_ms / 1e3) / 1e12
         gemm_ms_p = pre_prep["gemm_gate"] + pre_prep["gemm_up"] + pre_prep["gemm_down"]
@@ -1451,7 +1474,17 @@ def main():
                              "quantize_q8_0": round(bytes_quantize(T, d) /
                                                     pre["quantize_q8_0 (standalone, not in the chain)"] / 1e6, 1),
                              "timing": "each call bracketed by its own CUDA events (no overlap with its neighbours)",
-                             "peak": peaks["hbm_gbs"]},
+                             "peak": peaks["hbm_gbs"],
+                             "back_to_back": {
+                                 "rmsnorm_quant_mode2": round(bytes_rmsnorm_quant(T, d, False)
+                                                              / pre_b2b["rmsnorm_quant"] / 1e6, 1),
+                                 "swiglu_quant_mode2": round(bytes_swiglu_quant(T, nf, False)
+                                                             / pre_b2b["swiglu_quant"] / 1e6, 1),
+                                 "quantize_q8_0": round(bytes_quantize(T, d) / pre_b2b["quantize_q8_0"] / 1e6, 1),
+                                 "us": {k: round(1e3 * v, 2) for k, v in pre_b2b.items()},
+                                 "timing": "20 calls back to back between one pair of CUDA events (programmatic "
+                                           "dependent launch: each call's start overlaps the previous one's tail), "
+                                           "f32 inputs rotating over copies that together exceed L2"}},
             "l2": "step working set ~1.2 GB > L2",
             "prepared_weights": {
                 "calls": "the same chain with q8_0_gemm_prepared: each weight matrix widened to f16 once "
