@@ -158,17 +158,24 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
 // --------------------------------------------------------------------------
 // rmsnorm_quant for many rows (more than one per SM) of moderate width: one
 // persistent CTA per SM made of row groups of four warps.  A group owns a row
-// at a time; its rows arrive by bulk copy into the group's two shared-memory
-// slots, the next while it works on the current one, so each SM keeps a
-// dozen rows in flight and no group waits for another (groups synchronise on
-// named barriers of their own).  Thread b of a group owns the row's 32-element
+// at a time; its rows arrive by TMA into the group's two shared-memory slots,
+// the next while it works on the current one, so each SM keeps a dozen rows
+// in flight and no group waits for another (groups synchronise on named
+// barriers of their own).  Thread b of a group owns the row's 32-element
 // block b whole: its amax and code sum are register reductions and its d and
-// 1/d are computed once, so the encoder costs a fraction of the per-lane
-// (8 lanes per block) form.  Per row: each thread sums the squares of its
-// block, the warps reduce by xor shuffles and their four sums are added in
-// warp order; then scale, write y (mode 1) and encode.  A thread reads its
-// block's eight float4 starting at float4 (b mod 8), so the lanes of a warp
-// spread over all banks.  The weight vector is staged once per CTA.
+// 1/d are computed once, so the encoder costs a fraction of the per-lane (8
+// lanes per block) form.  Per row: each thread sums the squares of its block,
+// the warps reduce by xor shuffles and their four sums are added in warp
+// order; then scale, write y (mode 1) and encode.
+//
+// A row is loaded as a 3-D tensor box [1 row][d/32 blocks][32 floats] with
+// the 128-byte swizzle: block b's 16-byte chunk c lands at chunk c ^ (b mod 8)
+// of its 128-byte line (slots start on 1024-byte boundaries, so the line's
+// address bits 7..9 are b mod 8).  Thread b reads its chunk c from there into
+// register c, so the eight threads of a quarter warp hit eight different bank
+// groups while every register index stays static, and the block's 32 codes
+// leave as two 16-byte stores.  The weight vector is staged once per CTA in
+// the same swizzled order.
 // --------------------------------------------------------------------------
 constexpr int kGrpThreads = 128;     // four warps per row, one block per thread
 constexpr int kGrpSlots = 2;         // row slots per group
@@ -176,11 +183,23 @@ constexpr int kGrpMax = 8;           // groups per CTA (1024 threads)
 constexpr int kGrpSmemBudget = 200 * 1024;  // weight vector + every group's slots
 constexpr int kGrpMaxD = 32 * kGrpThreads;  // 4096: one block per thread
 
+// bytes of one row slot (and of the staged weight vector): d floats, rounded
+// up to whole 1024-byte swizzle atoms
+int rowgroup_slot_bytes(int d) { return (d * 4 + 1023) / 1024 * 1024; }
+
 int rowgroup_groups(int d, bool norm)
 {
-    const int per = d * 4;
+    const int per = rowgroup_slot_bytes(d);
     const int g = (kGrpSmemBudget - (norm ? per : 0)) / (per * kGrpSlots);
     return g > kGrpMax ? kGrpMax : g;
+}
+
+// dynamic shared memory of a launch: 1024 bytes of alignment slack, the
+// weight vector (RMSNorm) and every group's slots
+size_t rowgroup_smem(int d, bool norm, int groups)
+{
+    const size_t per = static_cast<size_t>(rowgroup_slot_bytes(d));
+    return 1024 + (norm ? per : 0) + per * kGrpSlots * groups;
 }
 
 __device__ __forceinline__ void group_sync(int id)
@@ -190,8 +209,9 @@ __device__ __forceinline__ void group_sync(int id)
 
 // The body shared by RMSNorm + quantize (kNorm) and the plain quantizer
 // (rows of x encoded as they are: no sum of squares, weight or y).
+// tmx: x as [rows][d/32][32] f32, box {32, d/32, 1}, 128-byte swizzle.
 template <bool kNorm>
-__device__ __forceinline__ void rowgroup_body(const float *__restrict__ x, const float *__restrict__ w, float eps,
+__device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const float *__restrict__ w, float eps,
                                               float *__restrict__ y, int64_t rows, int64_t rows_pad, int d,
                                               uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
@@ -203,17 +223,22 @@ __device__ __forceinline__ void rowgroup_body(const float *__restrict__ x, const
     const int grp = threadIdx.x / kGrpThreads, gt = threadIdx.x % kGrpThreads;
     const int lane = gt & 31, gw = gt >> 5;
     const int ngroups = blockDim.x / kGrpThreads;
-    const float4 *wsm = reinterpret_cast<const float4 *>(smem_rg);
-    float4 *myslots = reinterpret_cast<float4 *>(smem_rg) + static_cast<int64_t>(F) * ((kNorm ? 1 : 0) + kGrpSlots * grp);
+    const uint32_t raw = q8::smem_u32(smem_rg);
+    uint8_t *base = smem_rg + (((raw + 1023u) & ~1023u) - raw);  // 1024-byte aligned
+    const int slot_f4 = ((d * 4 + 1023) / 1024 * 1024) / 16;      // float4 per slot
+    const float4 *wsm = reinterpret_cast<const float4 *>(base);
+    float4 *myslots = reinterpret_cast<float4 *>(base) + static_cast<int64_t>(slot_f4) * ((kNorm ? 1 : 0) + kGrpSlots * grp);
     uint64_t *mybar = full + kGrpSlots * grp;
-    const uint32_t row_bytes = static_cast<uint32_t>(d) * 4u;  // a multiple of 128
+    const uint32_t row_bytes = static_cast<uint32_t>(d) * 4u;  // the box's bytes
     const bool mine_blk = gt < nb;                             // this thread's block exists
-    const int rot = gt & 7;                                    // first float4 read (bank spread)
+    const int sw = gt & 7;                                     // chunk c of block gt sits at c ^ sw
     q8::griddep_launch_dependents();  // consumers may start their prologue
-    // the weight vector is a constant input: staged before the dependency wait
+    // the weight vector is a constant input: staged (swizzled like the rows)
+    // before the dependency wait
     if (kNorm)
         for (int f = threadIdx.x; f < F; f += blockDim.x)
-            reinterpret_cast<float4 *>(smem_rg)[f] = __ldg(reinterpret_cast<const float4 *>(w) + f);
+            reinterpret_cast<float4 *>(base)[(f & ~7) | ((f ^ (f >> 3)) & 7)] =
+                __ldg(reinterpret_cast<const float4 *>(w) + f);
     if (gt == 0) {
         for (int s = 0; s < kGrpSlots; ++s) q8::mbar_init(&mybar[s], 1);
         q8::fence_mbar_init();
@@ -233,7 +258,8 @@ __device__ __forceinline__ void rowgroup_body(const float *__restrict__ x, const
             if (t >= rows) continue;
             const int s = static_cast<int>(issued % kGrpSlots);
             q8::mbar_arrive_expect_tx(&mybar[s], row_bytes);
-            q8::bulk_g2s(myslots + static_cast<int64_t>(s) * F, x + t * d, row_bytes, &mybar[s]);
+            q8::tma_load_3d(q8::smem_u32(myslots + static_cast<int64_t>(s) * slot_f4), tmx, 0, 0,
+                            static_cast<int>(t), q8::smem_u32(&mybar[s]));
         }
     };
     if (gt == 0) issue_upto(kGrpSlots);
@@ -252,14 +278,11 @@ __device__ __forceinline__ void rowgroup_body(const float *__restrict__ x, const
         }
         const int s = static_cast<int>(i % kGrpSlots);
         const bool got = q8::mbar_wait_bounded(&mybar[s], static_cast<uint32_t>(i / kGrpSlots) & 1u);
-        const float4 *xb = myslots + static_cast<int64_t>(s) * F + 8 * gt;
+        const float4 *xb = myslots + static_cast<int64_t>(s) * slot_f4 + 8 * gt;
         float4 v[8];
         float ss = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int e = (k + rot) & 7;  // element group e of the block, read in rotated order
-            v[k] = (got && mine_blk) ? xb[e] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int k = 0; k < 8; ++k) v[k] = (got && mine_blk) ? xb[k ^ sw] : make_float4(0.f, 0.f, 0.f, 0.f);
         if (kNorm) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) ss = q8::rms_sumsq4(ss, v[k]);
@@ -288,12 +311,12 @@ __device__ __forceinline__ void rowgroup_body(const float *__restrict__ x, const
             if (kNorm) {
                 const float scale = q8::rms_scale(tot, d, eps);
                 const float4 *wb = wsm + 8 * gt;
-                float4 *yb = reinterpret_cast<float4 *>(y + t * static_cast<int64_t>(d)) + 8 * gt;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int e = (k + rot) & 7;
-                    v[k] = q8::rms_apply4(v[k], scale, wb[e]);
-                    if (y) yb[e] = v[k];  // mode 2 (y == NULL): only the plane is written
+                for (int k = 0; k < 8; ++k) v[k] = q8::rms_apply4(v[k], scale, wb[k ^ sw]);
+                if (y) {  // mode 2 (y == NULL): only the plane is written
+                    float4 *yb = reinterpret_cast<float4 *>(y + t * static_cast<int64_t>(d)) + 8 * gt;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) yb[k] = v[k];
                 }
             }
 #pragma unroll
@@ -301,15 +324,17 @@ __device__ __forceinline__ void rowgroup_body(const float *__restrict__ x, const
                 amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
             const float dq = q8::q8_block_d(amax);
             const float di = q8::q8_block_di(dq);
-            uint32_t *qw = reinterpret_cast<uint32_t *>(qrow) + 8 * gt;
+            uint32_t qw[8];
             int sum = 0;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int c0 = q8::q8_code(v[k].x, di), c1 = q8::q8_code(v[k].y, di);
                 const int c2 = q8::q8_code(v[k].z, di), c3 = q8::q8_code(v[k].w, di);
                 sum += c0 + c1 + c2 + c3;
-                qw[(k + rot) & 7] = q8::pack4(c0, c1, c2, c3);  // codes of element group (k + rot) mod 8
+                qw[k] = q8::pack4(c0, c1, c2, c3);
             }
+            qrow[2 * gt] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+            qrow[2 * gt + 1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
             drow[gt] = q8::q8_dsword(dq, sum);
         }
         group_sync(1 + grp);  // every thread of the group is done with this row's slot
@@ -327,18 +352,26 @@ __device__ __forceinline__ void rowgroup_body(const float *__restrict__ x, const
 }
 
 __global__ void __launch_bounds__(kGrpThreads * kGrpMax, 1)
-rmsnorm_quant_rowgroup_kernel(const float *__restrict__ x, const float *__restrict__ w, float eps,
+rmsnorm_quant_rowgroup_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restrict__ w, float eps,
                               float *__restrict__ y, int64_t rows, int64_t rows_pad, int d,
                               uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
-    rowgroup_body<true>(x, w, eps, y, rows, rows_pad, d, qs, ds);
+    rowgroup_body<true>(&tmx, w, eps, y, rows, rows_pad, d, qs, ds);
 }
 
 __global__ void __launch_bounds__(kGrpThreads * kGrpMax, 1)
-quantize_q8_0_rowgroup_kernel(const float *__restrict__ x, int64_t rows, int64_t rows_pad, int d,
+quantize_q8_0_rowgroup_kernel(const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t rows_pad, int d,
                               uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
 {
-    rowgroup_body<false>(x, nullptr, 0.0f, nullptr, rows, rows_pad, d, qs, ds);
+    rowgroup_body<false>(&tmx, nullptr, 0.0f, nullptr, rows, rows_pad, d, qs, ds);
+}
+
+// x as the row-group kernels' TMA source: [rows][d/32][32] f32, one row per box
+bool rowgroup_x_map(CUtensorMap *m, const float *x, int64_t rows, int d)
+{
+    return q8::make_map_3d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x, 32, static_cast<uint64_t>(d / 32),
+                           static_cast<uint64_t>(rows), 128, static_cast<uint64_t>(d) * 4, 32,
+                           static_cast<uint32_t>(d / 32), 1, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // --------------------------------------------------------------------------
@@ -412,14 +445,16 @@ extern "C" int quantize_q8_0(const float *x, int64_t rows, int64_t k, int8_t *qs
     const int sms = q8::device_sm_count();
     const int nsm = sms > 0 ? sms : 152;
     const int ng = k <= kGrpMaxD ? rowgroup_groups(static_cast<int>(k), false) : 0;
-    if (rows_pad > nsm && ng >= 2) {
+    if (rows_pad > nsm && ng >= 2 && rows < (int64_t(1) << 31)) {
         // many rows: row groups streaming the rows through shared memory, one CTA per SM
-        const size_t smem = static_cast<size_t>(k) * 4 * kGrpSlots * ng;
+        const size_t smem = rowgroup_smem(static_cast<int>(k), false, ng);
+        CUtensorMap mx{};
+        if (rows > 0 && !rowgroup_x_map(&mx, x, rows, static_cast<int>(k))) return Q8_ERR_LAUNCH;
         if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(quantize_q8_0_rowgroup_kernel),
                                       static_cast<int>(smem), 13))
             return Q8_ERR_LAUNCH;
         return q8::launch_pdl(quantize_q8_0_rowgroup_kernel, dim3(static_cast<unsigned>(nsm)),
-                              dim3(kGrpThreads * ng), smem, static_cast<cudaStream_t>(stream), x, rows, rows_pad,
+                              dim3(kGrpThreads * ng), smem, static_cast<cudaStream_t>(stream), mx, rows, rows_pad,
                               static_cast<int>(k), reinterpret_cast<uint32_t *>(qs), ds);
     }
     const int64_t n4_valid = rows * k / 4, n4_total = rows_pad * k / 4;
@@ -444,14 +479,16 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     uint32_t *q32 = reinterpret_cast<uint32_t *>(qs);
     const int di = static_cast<int>(d);
     const int ng = rowgroup_groups(di, true);
-    if (rows_pad > nsm && d <= kGrpMaxD && ng >= 2) {
+    if (rows_pad > nsm && d <= kGrpMaxD && ng >= 2 && rows < (int64_t(1) << 31)) {
         // many rows: row groups streaming their rows through shared memory, one CTA per SM
-        const size_t smem = static_cast<size_t>(d) * 4 * (1 + kGrpSlots * ng);
+        const size_t smem = rowgroup_smem(di, true, ng);
+        CUtensorMap mx{};
+        if (rows > 0 && !rowgroup_x_map(&mx, x, rows, di)) return Q8_ERR_LAUNCH;
         if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(rmsnorm_quant_rowgroup_kernel),
                                       static_cast<int>(smem), 12))
             return Q8_ERR_LAUNCH;
         return q8::launch_pdl(rmsnorm_quant_rowgroup_kernel, dim3(static_cast<unsigned>(nsm)), dim3(kGrpThreads * ng),
-                              smem, s, x, w, eps, y, rows, rows_pad, di, q32, ds);
+                              smem, s, mx, w, eps, y, rows, rows_pad, di, q32, ds);
     }
     // float4 per thread: up to 256 threads per row when CTAs take several rows
     // (four CTAs per SM keep four rows in flight), up to 512 when every CTA
