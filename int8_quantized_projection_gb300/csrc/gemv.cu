@@ -303,12 +303,22 @@ __device__ __forceinline__ void stage_produced(const GvGeom &g, uint8_t *act, fl
         const float di = q8::q8_block_di(d);
         uint32_t qw[4];
         int sum = 0;
+        if (!q8::q8_block_needs_clamp(d)) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int c0 = q8::q8_code(va[e].x, di), c1 = q8::q8_code(va[e].y, di);
-            const int c2 = q8::q8_code(va[e].z, di), c3 = q8::q8_code(va[e].w, di);
-            sum += c0 + c1 + c2 + c3;
-            qw[e] = q8::pack4(c0, c1, c2, c3);
+            for (int e = 0; e < 4; ++e) {
+                const int c0 = q8::q8_code_unclamped(va[e].x, di), c1 = q8::q8_code_unclamped(va[e].y, di);
+                const int c2 = q8::q8_code_unclamped(va[e].z, di), c3 = q8::q8_code_unclamped(va[e].w, di);
+                sum += c0 + c1 + c2 + c3;
+                qw[e] = q8::pack4(c0, c1, c2, c3);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c0 = q8::q8_code(va[e].x, di), c1 = q8::q8_code(va[e].y, di);
+                const int c2 = q8::q8_code(va[e].z, di), c3 = q8::q8_code(va[e].w, di);
+                sum += c0 + c1 + c2 + c3;
+                qw[e] = q8::pack4(c0, c1, c2, c3);
+            }
         }
         sum += __shfl_xor_sync(pair_mask, sum, 1);
         uint8_t *ch = act + (blk >> 2) * kActChunkBytes;

@@ -291,17 +291,31 @@ __device__ __forceinline__ int clamp127(int v) { return max(-127, min(127, v)); 
 __device__ __forceinline__ float q8_block_d(float amax) { return __fdiv_rn(amax, 127.0f); }
 __device__ __forceinline__ float q8_block_di(float d) { return (d != 0.0f) ? __frcp_rn(d) : 0.0f; }
 __device__ __forceinline__ int q8_code(float v, float di) { return clamp127(__float2int_rn(__fmul_rn(v, di))); }
+
+// Whether the clamp in q8_code can change a code of this block.  When d is
+// a normal float (or 0, infinite or NaN) every |v| <= amax gives
+// |v * di| <= 127 (1 + 2^-24)^2 / (1 - 2^-24) < 127.5 (three round-to-nearest
+// steps, each within 2^-24), so rint(v * di) already lies in [-127, 127], and
+// a non-finite product converts to 0 either way.  Only a subnormal d (amax
+// below 127 * 2^-126), where d carries fewer significant bits, can push a
+// code past 127.
+__device__ __forceinline__ bool q8_block_needs_clamp(float d) { return d > 0.0f && d < 1.17549435e-38f; }
+
+// q8_code for a block whose d does not need the clamp (the same code).
+__device__ __forceinline__ int q8_code_unclamped(float v, float di) { return __float2int_rn(__fmul_rn(v, di)); }
 __device__ __forceinline__ uint32_t q8_dsword(float d, int ssum)
 {
     return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(d))) |
            (static_cast<uint32_t>(static_cast<uint16_t>(static_cast<int16_t>(ssum))) << 16);
 }
 
-// Four codes (each in [-127, 127]) packed little-endian into a word.
+// Four codes (each in [-127, 127]) packed little-endian into a word: the low
+// byte of each, by byte permutes.
 __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
 {
-    return (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(b) & 0xffu) << 8) |
-           ((static_cast<uint32_t>(c) & 0xffu) << 16) | (static_cast<uint32_t>(d) << 24);
+    const uint32_t ab = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040u);  // a0 b0 . .
+    const uint32_t cd = __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040u);  // c0 d0 . .
+    return __byte_perm(ab, cd, 0x5410u);                                                          // a0 b0 c0 d0
 }
 
 // 8 adjacent lanes hold one 32-element block, a float4 each.

@@ -326,12 +326,22 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
             const float di = q8::q8_block_di(dq);
             uint32_t qw[8];
             int sum = 0;
+            if (!q8::q8_block_needs_clamp(dq)) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int c0 = q8::q8_code(v[k].x, di), c1 = q8::q8_code(v[k].y, di);
-                const int c2 = q8::q8_code(v[k].z, di), c3 = q8::q8_code(v[k].w, di);
-                sum += c0 + c1 + c2 + c3;
-                qw[k] = q8::pack4(c0, c1, c2, c3);
+                for (int k = 0; k < 8; ++k) {
+                    const int c0 = q8::q8_code_unclamped(v[k].x, di), c1 = q8::q8_code_unclamped(v[k].y, di);
+                    const int c2 = q8::q8_code_unclamped(v[k].z, di), c3 = q8::q8_code_unclamped(v[k].w, di);
+                    sum += c0 + c1 + c2 + c3;
+                    qw[k] = q8::pack4(c0, c1, c2, c3);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int c0 = q8::q8_code(v[k].x, di), c1 = q8::q8_code(v[k].y, di);
+                    const int c2 = q8::q8_code(v[k].z, di), c3 = q8::q8_code(v[k].w, di);
+                    sum += c0 + c1 + c2 + c3;
+                    qw[k] = q8::pack4(c0, c1, c2, c3);
+                }
             }
             qrow[2 * gt] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
             qrow[2 * gt + 1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);

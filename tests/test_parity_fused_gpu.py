@@ -87,6 +87,33 @@ def test_fused_equals_two_launches_and_oracle(q8, producer, k, ns):
         assert_gemm_close(host(yf), yr, ar, f"fused producer {producer} {n}x{k}")
 
 
+@pytest.mark.parametrize("producer", [1, 2])
+def test_fused_subnormal_scales_equal_two_launches(q8, producer):
+    """Activations whose blocks have subnormal d (the clamp decides codes):
+    the fused prologue's plane equals the standalone producer's."""
+    import torch
+
+    from .test_parity_quantize_gpu import _tiny_rows
+
+    k, ns = 3584, [300, 64]
+    if producer == 1:  # the activation itself has subnormal block scales
+        a_h, w_h = _tiny_rows(1, k, 7)[0], None
+    else:              # a norm weight that makes every normalized value subnormal
+        a_h = syn.activations(syn.rng(72, k), 1, k)[0]
+        w_h = np.full(k, 1e-38, np.float32)
+    a = dev(a_h)
+    w = dev(w_h) if w_h is not None else None
+    blobs = [_weights(20 + i, n, k) for i, n in enumerate(ns)]
+    wd = [dev(bl) for bl in blobs]
+    yf = [nan_f32(n) for n in ns]
+    q8.q8_0_gemv_fused([(x, n, y) for x, n, y in zip(wd, ns, yf)], k, producer, a, None, w, 1e-6)
+    q8.q8_check()
+    yt = [nan_f32(n) for n in ns]
+    _two_launch(q8, producer, k, a, None, w, 1e-6, [(x, n, y) for x, n, y in zip(wd, ns, yt)])
+    for n, f, t in zip(ns, yf, yt):
+        assert torch.equal(f, t), f"producer {producer} {n}x{k}: fused != two launches"
+
+
 def test_fused_rmsnorm_zero_row(q8):
     """An all-zero row: the scale is rsqrt(eps), every code and d is 0, every output exactly 0."""
     k, n = 3584, 300

@@ -51,6 +51,61 @@ def test_quantize_q8_0_bit_exact(q8, rows, k, rows_pad):
     assert_plane_equal(qs, ds, qr, dr, f"quantize {rows}x{k}")
 
 
+# Block maxima around the edge of the normal f32 range.  d = amax/127 is
+# subnormal below 127 * 2^-126 = 1.49e-36, and 1/d overflows to infinity
+# below about 127 * 2^-128 = 3.7e-37: there the products x * (1/d) are
+# infinite and the clamp to +-127 decides every code, the one case where it
+# can.  Every element is non-zero (0 * inf has no code).  Above 1.49e-36 d is
+# normal and the clamp never changes a code.
+TINY_AMAX = (1e-44, 1e-40, 1e-38, 1e-37, 3.6e-37, 3.8e-37, 1e-36, 1.4e-36, 1.6e-36, 1e-30)
+
+
+def _tiny_rows(rows, k, seed):
+    g = syn.rng(53, seed, rows, k)
+    nb = k // 32
+    mag = g.uniform(0.25, 1.0, size=(rows, k)).astype(np.float32)
+    sign = np.where(g.integers(0, 2, size=(rows, k)) == 0, -1.0, 1.0).astype(np.float32)
+    scale = np.array([TINY_AMAX[(r * nb + b) % len(TINY_AMAX)] for r in range(rows) for b in range(nb)],
+                     np.float32).reshape(rows, nb)
+    x = (sign * mag).reshape(rows, nb, 32) * scale[:, :, None]
+    x = x.astype(np.float32)
+    x[x == 0] = np.float32(1e-45)  # the smallest subnormal: no element underflows to 0
+    return x.reshape(rows, k)
+
+
+@pytest.mark.parametrize("rows,k,rows_pad", [(3, 320, 3), (2, 8192, 2), (700, 320, 704), (400, 4096, 512),
+                                             (300, 4128, 384)])
+def test_quantize_q8_0_subnormal_scales(q8, rows, k, rows_pad):
+    """Blocks whose d is subnormal (and whose 1/d may be infinite): the codes
+    the clamp decides, on the one-row, row-group and flat kernels."""
+    x = _tiny_rows(rows, k, 1)
+    assert (x != 0).all()
+    qs, ds = poisoned_plane(rows_pad, k)
+    q8.quantize_q8_0(dev(x), qs, ds)
+    q8.q8_check()
+    qr, dr = oracle.quantize(x, rows_pad)
+    assert (np.abs(qr[:rows].astype(np.int32)) == 127).any()  # the data reaches the clamped case
+    assert_plane_equal(qs, ds, qr, dr, f"quantize subnormal scales {rows}x{k}")
+
+
+@pytest.mark.parametrize("rows,d,rows_pad", [(1, 3584, 1), (400, 3584, 512), (3, 8192, 3)])
+def test_rmsnorm_quant_subnormal_outputs(q8, rows, d, rows_pad):
+    """A norm weight small enough that y (and every block's d) is subnormal:
+    the plane is still the exact encoding of the kernel's own y."""
+    g = syn.rng(54, rows, d)
+    x = syn.activations(g, rows, d)
+    x = np.where(np.abs(x) < 1e-3, np.copysign(np.float32(1e-3), x), x).astype(np.float32)  # no y underflows to 0
+    w = (syn.uniform(g, d, 0.5, 1.5) * np.float32(1e-38)).astype(np.float32)
+    y = nan_f32(rows, d)
+    qs, ds = poisoned_plane(rows_pad, d)
+    q8.rmsnorm_quant(dev(x), dev(w), 1e-6, y, qs, ds)
+    q8.q8_check()
+    yh = host(y)
+    assert (yh != 0).all() and np.abs(yh).max() < 1.49e-36  # no zero output; every block's d is subnormal
+    qr, dr = oracle.quantize(yh, rows_pad)
+    assert_plane_equal(qs, ds, qr, dr, f"rmsnorm subnormal plane {rows}x{d}")
+
+
 def test_quantize_q8_0_zero_rows_only_fills_tail(q8):
     import torch
 
