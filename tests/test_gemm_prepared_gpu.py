@@ -134,3 +134,26 @@ def test_prepared_tc_path_without_prepared_weights_is_an_argument_error(q8):
     with pytest.raises(q8.Q8Error) as e:
         q8.q8_0_gemm_prepared(None, None, n, k, dev(qs), dev(ds.view(np.int32)), t, y)
     assert e.value.status == 1  # Q8_ERR_ARG, before any device work
+
+
+@pytest.mark.parametrize("n,k,t", [(18944, 3584, 3325), (3584, 18944, 3325)])
+def test_prepared_full_size_prefill_shapes(q8, n, k, t):
+    """The prefill chain's GEMM shapes as the bench times them: equal to
+    q8_0_gemm bit for bit, no unwritten output, a sample against the oracle."""
+    import torch
+
+    blob = syn.q8_0_weights(syn.rng(100, n, k), n, k)[0]
+    qs, ds = _plane(50, t, k)
+    w, qd, dd = dev(blob), dev(qs), dev(ds.view(np.int32))
+    wprep = q8.q8_0_gemm_prepare_weights(w, n, k)
+    y_plain, y_prep = nan_f32(t, n), nan_f32(t, n)
+    q8.q8_0_gemm(w, n, k, qd, dd, t, y_plain)
+    q8.q8_0_gemm_prepared(None, wprep, n, k, qd, dd, t, y_prep)
+    q8.q8_check()
+    assert not torch.isnan(y_prep).any().item(), "unwritten outputs"
+    assert torch.equal(y_plain, y_prep)
+    g = syn.rng(101, n, k, t)
+    ti = np.unique(np.concatenate([[0, t - 1], g.integers(0, t, 16)]))
+    ni = np.unique(np.concatenate([[0, n - 1], g.integers(0, n, 64)]))
+    yr, ar = oracle.gemm(blob, n, k, qs, ds, t_idx=ti, n_idx=ni)
+    assert_gemm_close(host(y_prep)[np.ix_(ti, ni)], yr, ar, f"prepared {n}x{k} t={t} (sampled)")
