@@ -25,6 +25,7 @@ pytestmark = pytest.mark.gpu
 CASES = [
     # (k, ns)
     (256, (64,)),
+    (512, (256,)),      # the tiny configuration: 16 blocks per row, one launch per step
     (3584, (3584, 512, 512)),
     (3584, (37,)),
     (7168, (3072, 512, 512, 3072)),
