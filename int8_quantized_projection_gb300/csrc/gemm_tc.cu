@@ -596,19 +596,52 @@ gemm_split_reduce_kernel(const float *__restrict__ part, int splits, int64_t cou
 
 // How many CTAs share k (1 = none).  When the tiles alone leave most SMs idle
 // (a few weight rows or tokens), k is split so that about one wave of CTAs
-// runs, each over at least 4 stages (8 blocks).  A fixed SM count is used so
-// that the workspace size is a function of the shape alone; splits * tiles
-// stays at most that count, which bounds the partial tiles by about 15 MB.
-constexpr int kSplitSms = 152, kMaxSplits = 12;
+// runs, each over at least 4 stages (8 blocks).  With more tiles, k is split
+// only when the last wave of whole tiles would leave enough SMs idle to pay
+// for the partial tiles' traffic: a split s is scored by its waves of CTAs
+// times a CTA's time (its stages plus a fixed ramp and store) plus the time to
+// write and add the s partial tiles of every output, in the units of one
+// stage of one CTA as measured on this kernel; the best score wins if it
+// saves at least 3 % (e.g. 3584 x 18944 at t = 3325: 504 tiles fill 3.3
+// waves, split 3 fills 9.9).  A fixed SM count is used so that the workspace
+// size is a function of the shape alone; the first rule keeps splits * tiles
+// at most that count, which bounds its partial tiles by about 15 MB, and the
+// second allows at most 4 splits.
+constexpr int kSplitSms = 152, kMaxSplits = 12, kMaxSplitsMany = 4;
+constexpr double kStageUs = 0.886;        // one stage (two blocks) of one CTA
+constexpr double kCtaFixedUs = 4.0;       // a CTA's pipeline ramp and output store
+constexpr double kPartialBytesPerUs = 6.5e6;  // partial tiles written and read back at about HBM rate
+constexpr double kReduceLaunchUs = 3.0;
 int gemm_splits(int64_t n, int64_t t, int64_t k)
 {
     const int64_t tiles = ((n + BM - 1) / BM) * ((t + BN - 1) / BN);
     const int64_t nst = k / 32 / kStageBlocks;
-    if (2 * tiles > kSplitSms) return 1;
-    int64_t sp = kSplitSms / tiles;
-    sp = sp > kMaxSplits ? kMaxSplits : sp;
-    sp = sp > nst / 4 ? nst / 4 : sp;
-    return sp < 1 ? 1 : static_cast<int>(sp);
+    if (2 * tiles <= kSplitSms) {
+        int64_t sp = kSplitSms / tiles;
+        sp = sp > kMaxSplits ? kMaxSplits : sp;
+        sp = sp > nst / 4 ? nst / 4 : sp;
+        return sp < 1 ? 1 : static_cast<int>(sp);
+    }
+    auto score = [&](int64_t s) {
+        const int64_t waves = (tiles * s + kSplitSms - 1) / kSplitSms;
+        const int64_t stages = (nst + s - 1) / s;
+        double us = static_cast<double>(waves) * (static_cast<double>(stages) * kStageUs + kCtaFixedUs);
+        if (s > 1)  // the partials replace one f32 write of Y: 2s - 1 more passes over t x n f32
+            us += static_cast<double>(2 * s - 1) * static_cast<double>(t) * static_cast<double>(n) * 4.0 /
+                      kPartialBytesPerUs + kReduceLaunchUs;
+        return us;
+    };
+    const double base = score(1);
+    int best = 1;
+    double best_us = base;
+    for (int s = 2; s <= kMaxSplitsMany && nst / s >= 4; ++s) {
+        const double us = score(s);
+        if (us < best_us) {
+            best_us = us;
+            best = s;
+        }
+    }
+    return best_us <= 0.97 * base ? best : 1;
 }
 
 // Workspace layout for (n, t, k): [f16 weights | f16 activation | d_w tiles |

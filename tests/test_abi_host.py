@@ -94,6 +94,11 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert lib.q8_0_gemm_workspace_bytes(512, 2048, 3584) == up(up(up(up(512 * 3584 * 2) + 2048 * 3584 * 2)
                                                                   + 4 * 112 * 128 * 4) + 11 * 112 * 192 * 4) \
         + 3 * 2048 * 512 * 4
+    # many tiles whose last wave would leave most SMs idle: 28 x 18 = 504 tiles fill 3.3 waves of 152 CTAs, so
+    # k (296 stages) is split 3 ways (9.9 waves) -> 3 x t x n f32 partial tiles; gate/up's 2664 tiles stay unsplit
+    assert lib.q8_0_gemm_workspace_bytes(3584, 3325, 18944) == up(up(up(up(3584 * 18944 * 2) + 3325 * 18944 * 2)
+                                                                    + 28 * 592 * 128 * 4) + 18 * 592 * 192 * 4) \
+        + 3 * 3325 * 3584 * 4
     assert lib.q8_0_gemm_workspace_bytes(8, 20, 64) == 0      # k/32 % 8 != 0: generic kernel, no workspace
     assert lib.q8_0_gemm_workspace_bytes(8, 16, 256) == 0     # t <= 16: small-batch kernel, no workspace
     assert lib.q8_0_gemm_workspace_bytes(8, 64, 256) == 0     # t <= 64: 16-token slices, no workspace
