@@ -766,8 +766,8 @@ def run_shared(torch, q8p, steps, warmup, dev):
     """RMSNorm + q8_0 quantize feeding the four projections, timed two ways:
     one q8_0_gemv_fused launch per step (the norm computed inside the grouped
     GEMV), and rmsnorm_quant (mode 2) -> q8_0_gemv_grouped (two launches).
-    Each is recorded as a CUDA graph of one step per weight copy (copies
-    together > 4 x L2)."""
+    Each is recorded as a CUDA graph of about GRAPH_STEPS steps (the weight
+    copies in turn, together > 4 x L2), as the decode step is."""
     d, ns, eps = SHARED["d"], SHARED["ns"], SHARED["eps"]
     g = syn.rng(2, 0)
     x = torch.from_numpy(syn.activations(g, 1, d)).to(dev)
@@ -786,7 +786,8 @@ def run_shared(torch, q8p, steps, warmup, dev):
     steps_two = [[norm, gm] for gm in gemvs]  # one step per weight copy
     steps_fused = [[fu] for fu in fused]
     stream = torch.cuda.current_stream(dev)
-    reps = max(1, steps // copies)
+    per_graph = copies * max(1, GRAPH_STEPS // copies)  # steps per graph, as the decode step's graphs
+    reps = max(1, steps // per_graph)
     res = {}
     for name, per_copy_calls in (("fused", steps_fused), ("two", steps_two)):
         cap.wait_stream(stream)
@@ -796,8 +797,8 @@ def run_shared(torch, q8p, steps, warmup, dev):
         q8p.q8_check()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap):
-            for calls in per_copy_calls:
-                for c in calls:
+            for i in range(per_graph):
+                for c in per_copy_calls[i % copies]:
                     c()
         stream.wait_stream(cap)
         graph.replay()
@@ -810,9 +811,9 @@ def run_shared(torch, q8p, steps, warmup, dev):
         t1.record(stream)
         torch.cuda.synchronize(dev)
         q8p.q8_check()
-        res[name] = 1e3 * t0.elapsed_time(t1) / (reps * copies)
+        res[name] = 1e3 * t0.elapsed_time(t1) / (reps * per_graph)
         del graph
-    return dict(us=res["fused"], us_two=res["two"], copies=copies, steps=reps * copies)
+    return dict(us=res["fused"], us_two=res["two"], copies=copies, steps=reps * per_graph, per_graph=per_graph)
 
 
 # ---------------------------------------------------------------------------
@@ -1589,7 +1590,8 @@ def main():
                                 "us_per_step": round(shr["us_two"], 2),
                                 "gbs": round(byts2 / (shr["us_two"] / 1e6) / 1e9, 1), "algorithmic_bytes": byts2,
                                 "launches_per_step": 2},
-                 "launch": f"CUDA graph of one step per weight copy ({shr['copies']} copies > 4 x L2), replayed"}
+                 "launch": f"CUDA graphs of {shr['per_graph']} steps (the {shr['copies']} weight copies in turn, "
+                           "> 4 x L2), replayed; programmatic dependent launch between steps, as the decode step"}
         if args.workload == "shared":
             line.update({"value": round(world * gbs, 1), "unit": "GB/s", "ms_per_step": round(shr["us"] / 1e3, 5),
                          "config": {"workload": sobj2["workload"], "l2": f"{shr['copies']} weight copies > 4 x L2",
