@@ -217,6 +217,32 @@ def test_gemm_full_size_sampled(q8, n, k, t, entry):
     assert_gemm_close(host(y)[np.ix_(ti, ni)], yr, ar, f"gemm {n}x{k} t={t} (sampled)")
 
 
+@pytest.mark.parametrize("n,k,t,splits", [(3584, 18944, 512, 3), (3584, 3584, 1000, 2), (3584, 18944, 2048, 4),
+                                           (18944, 3584, 1000, 1)])
+def test_gemm_wave_split_shapes(q8, n, k, t, splits):
+    """Shapes with many tiles whose last wave would leave most SMs idle, so k
+    is split (the workspace holds `splits` partial tiles of t x n f32): every
+    output written, a sample against the oracle, and the split as expected."""
+    import torch
+
+    lib = q8.lib()
+    up = lambda v: -(-v // 1024) * 1024  # noqa: E731
+    nb = k // 32
+    base = up(up(up(up(n * k * 2) + t * k * 2) + -(-n // 128) * nb * 128 * 4) + -(-t // 192) * nb * 192 * 4)
+    assert lib.q8_0_gemm_workspace_bytes(n, t, k) == base + (splits * t * n * 4 if splits > 1 else 0)
+    blob = _weights(9, n, k)
+    qs, ds = _plane(9, t, k, rows_pad=((t + 127) // 128) * 128)
+    y = nan_f32(t, n)
+    q8.q8_0_gemm(dev(blob), n, k, dev(qs), dev(ds.view(np.int32)), t, y)
+    q8.q8_check()
+    assert not torch.isnan(y).any().item(), "unwritten outputs"
+    g = syn.rng(63, n, k, t)
+    ti = np.unique(np.concatenate([[0, t - 1], g.integers(0, t, 16)]))
+    ni = np.unique(np.concatenate([[0, n - 1], g.integers(0, n, 64)]))
+    yr, ar = oracle.gemm(blob, n, k, qs, ds, t_idx=ti, n_idx=ni)
+    assert_gemm_close(host(y)[np.ix_(ti, ni)], yr, ar, f"gemm {n}x{k} t={t} split {splits} (sampled)")
+
+
 def test_gemm_deterministic(q8):
     import torch
 
