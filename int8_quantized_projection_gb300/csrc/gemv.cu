@@ -139,6 +139,7 @@ __device__ __forceinline__ void locate(const GvGeom &g, int64_t G, int &pi, int6
 #define Q8_Q80_WARPS 16
 #endif
 struct FmtQ8_0 {
+    static constexpr bool kFused = true;  // produced rows (q8_0_gemv_fused) and gate/up pairing (q8_0_gemv_gate_up)
     static constexpr int kChunkBytes = 136;
     static constexpr int kLaneChunks = Q8_Q80_J;
     static constexpr int kStages = Q8_Q80_STAGES;
@@ -162,6 +163,7 @@ struct FmtQ8_0 {
 #define Q8_Q4A_WARPS 16
 #endif
 struct FmtQ4A {
+    static constexpr bool kFused = false;  // plane input and y outputs only
     static constexpr int kChunkBytes = q8::kA4ChunkBytes;
     static constexpr int kLaneChunks = Q8_Q4A_J;
     static constexpr int kStages = Q8_Q4A_STAGES;
@@ -434,7 +436,7 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
             const uint4 v = (j < 8) ? __ldg(qs_row + c * 8 + j) : __ldg(reinterpret_cast<const uint4 *>(ds_row) + c);
             *reinterpret_cast<uint4 *>(act + c * kActChunkBytes + 16 * j) = v;
         }
-    } else {
+    } else if constexpr (F::kFused) {
         // RMSNorm's warp sums: the free upper 64 bytes of the header's last 128
         stage_produced(g, act, reinterpret_cast<float *>(counter + 16), warp, lane);
     }
@@ -498,7 +500,7 @@ gemv_staged_kernel(const uint4 *__restrict__ qs_row, const uint32_t *__restrict_
                 for (int j = 1; j < J; ++j) a += acc[j];
                 for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(Q8_FULL_MASK, a, o);
                 if (lane == 0 && pj.y) pj.y[Gl] = a;  // y may be absent only in pairing mode
-                if (g.pair_upc) {
+                if (F::kFused && g.pair_upc) {
                     // this row's result into its unit; the warp that brings the
                     // unit's count to 64 encodes silu(gate) * up for its 32 rows
                     const int64_t ul = m.x >> 6;  // unit within this CTA (cg0 is unit-aligned)
