@@ -160,11 +160,13 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
 // persistent CTA per SM made of row groups of four warps.  A group owns a row
 // at a time; its rows arrive by TMA into the group's two shared-memory slots,
 // the next while it works on the current one, so each SM keeps a dozen rows
-// in flight and no group waits for another (groups synchronise on named
-// barriers of their own).  Thread b of a group owns the row's 32-element
-// block b whole: its amax and code sum are register reductions and its d and
-// 1/d are computed once, so the encoder costs a fraction of the per-lane (8
-// lanes per block) form.  Per row: each thread sums the squares of its block,
+// in flight and no group waits for another (a group meets once per row on a
+// named barrier of its own, to add its warps' sums of squares; each warp then
+// releases the row's slot through an mbarrier that the thread refilling the
+// slot waits on, so the other warps go on to the next row).  Thread b of a
+// group owns the row's 32-element block b whole: its amax and code sum are
+// register reductions and its d and 1/d are computed once, so the encoder
+// costs a fraction of the per-lane (8 lanes per block) form.  Per row: each thread sums the squares of its block,
 // the warps reduce by xor shuffles and their four sums are added in warp
 // order; then scale, write y (mode 1) and encode.
 //
@@ -217,6 +219,7 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
 {
     extern __shared__ __align__(128) uint8_t smem_rg[];
     __shared__ __align__(8) uint64_t full[kGrpMax * kGrpSlots];
+    __shared__ __align__(8) uint64_t empty[kGrpMax * kGrpSlots];  // the group's four warps are done with a slot
     __shared__ float red[kGrpMax][2][kGrpThreads / 32];
     __shared__ int okf[kGrpMax][2][kGrpThreads / 32];
     const int F = d >> 2, nb = d >> 5;
@@ -229,6 +232,7 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
     const float4 *wsm = reinterpret_cast<const float4 *>(base);
     float4 *myslots = reinterpret_cast<float4 *>(base) + static_cast<int64_t>(slot_f4) * ((kNorm ? 1 : 0) + kGrpSlots * grp);
     uint64_t *mybar = full + kGrpSlots * grp;
+    uint64_t *myempty = empty + kGrpSlots * grp;
     const uint32_t row_bytes = static_cast<uint32_t>(d) * 4u;  // the box's bytes
     const bool mine_blk = gt < nb;                             // this thread's block exists
     const int sw = gt & 7;                                     // chunk c of block gt sits at c ^ sw
@@ -240,7 +244,10 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
             reinterpret_cast<float4 *>(base)[(f & ~7) | ((f ^ (f >> 3)) & 7)] =
                 __ldg(reinterpret_cast<const float4 *>(w) + f);
     if (gt == 0) {
-        for (int s = 0; s < kGrpSlots; ++s) q8::mbar_init(&mybar[s], 1);
+        for (int s = 0; s < kGrpSlots; ++s) {
+            q8::mbar_init(&mybar[s], 1);
+            q8::mbar_init(&myempty[s], kGrpThreads / 32);
+        }
         q8::fence_mbar_init();
     }
     __syncthreads();
@@ -257,6 +264,14 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
             const int64_t t = g0 + issued * stride;
             if (t >= rows) continue;
             const int s = static_cast<int>(issued % kGrpSlots);
+            if (issued >= kGrpSlots) {
+                // the row that used this slot before must be read by all four warps
+                if (!q8::mbar_wait_bounded(&myempty[s], static_cast<uint32_t>((issued - kGrpSlots) / kGrpSlots) & 1u)) {
+                    atomicOr(&g_quant_err, 1u);
+                    break;
+                }
+                q8::fence_proxy_async_smem();  // those reads come before the copy into the slot
+            }
             q8::mbar_arrive_expect_tx(&mybar[s], row_bytes);
             q8::tma_load_3d(q8::smem_u32(myslots + static_cast<int64_t>(s) * slot_f4), tmx, 0, 0,
                             static_cast<int>(t), q8::smem_u32(&mybar[s]));
@@ -347,11 +362,9 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
             qrow[2 * gt + 1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
             drow[gt] = q8::q8_dsword(dq, sum);
         }
-        group_sync(1 + grp);  // every thread of the group is done with this row's slot
-        if (gt == 0) {
-            q8::fence_proxy_async_smem();  // the slot's reads come before the next copy into it
-            issue_upto(i + 1 + kGrpSlots);
-        }
+        __syncwarp();
+        if (lane == 0) q8::mbar_arrive(&myempty[s]);  // this warp is done with the row's slot
+        if (gt == 0) issue_upto(i + 1 + kGrpSlots);
     }
     // after a timeout, let this group's loads still in flight land before it exits
     if (gt == 0)
