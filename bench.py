@@ -1064,6 +1064,35 @@ def run_stack_tokens(torch, q8p, reps, warmup, dev, tokens=STACK_TOKENS, layer_c
         for (name, _), (a, b) in zip(calls, evs):
             per.setdefault(name, []).append(a.elapsed_time(b))
         out[T] = dict(stack_ms=stack_ms, per_ms={nm: statistics.mean(v) for nm, v in per.items()}, reps=reps)
+    # at T <= 16 the same pass with the projections of one activation grouped:
+    # q, k, v one launch, gate and up one launch (4 launches per layer + head)
+    for T in [T for T in tokens if T <= q8p.GEMV_MAX_TOKENS]:
+        Yg = [torch.empty(T * n, dtype=torch.float32, device=dev) for (_, n, _) in shapes]
+        calls = []
+        for lw in layers:
+            pj = [(w, n, y) for ((_, n, _), w, y) in zip(shapes, lw, Yg)]
+            calls.append(q8p.q8_0_gemv_batched_grouped(pj[0:3], d, *planes[d], T, bind=True))
+            calls.append(q8p.q8_0_gemm(lw[3], d, d, *planes[d], T, Y, workspace=ws, bind=True))
+            calls.append(q8p.q8_0_gemv_batched_grouped(pj[4:6], d, *planes[d], T, bind=True))
+            calls.append(q8p.q8_0_gemm(lw[6], d, nf, *planes[nf], T, Y, workspace=ws, bind=True))
+        calls.append(q8p.q8_0_gemm(head, V, d, *planes[d], T, Y, workspace=ws, bind=True))
+        for _ in range(max(1, warmup // 3)):
+            for c in calls:
+                c()
+        q8p.q8_check()
+        torch.cuda.synchronize(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_device(torch, 8 * len(calls))
+        t0.record(stream)
+        for _ in range(reps):
+            for c in calls:
+                c()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        q8p.q8_check()
+        out[T]["stack_ms_grouped"] = t0.elapsed_time(t1) / reps
+        out[T]["grouped_calls"] = len(calls)
+        del Yg
     # the same passes on weights prepared once per matrix (f16 codes + d_w,
     # q8_0_gemm_prepare_weights outside the timed region), for the token counts
     # that take the tcgen05 GEMM
@@ -1407,7 +1436,8 @@ def main():
                 + ([tiny["us"], tiny["us_two"]] if tiny else [])
                 + ([v for T in sorted(stk) for v in [stk[T]["stack_ms"]] + [stk[T]["per_ms"][nm] for nm in
                                                                              sorted(stk[T]["per_ms"])]
-                    + ([stk[T]["stack_ms_prepared"]] if "stack_ms_prepared" in stk[T] else [])] if stk else []))
+                    + ([stk[T]["stack_ms_prepared"]] if "stack_ms_prepared" in stk[T] else [])
+                    + ([stk[T]["stack_ms_grouped"]] if "stack_ms_grouped" in stk[T] else [])] if stk else []))
         red = max_over_ranks(torch, vals, dev)
         if dec:
             (dec["ms"], dec["e2e_s"], dec["kern_ms"], dec["e2e_eager_s"], dec["e2e_serial_s"], dec["ms_two"],
@@ -1435,6 +1465,8 @@ def main():
                     stk[T]["per_ms"][nm] = red.pop(0)
                 if "stack_ms_prepared" in stk[T]:
                     stk[T]["stack_ms_prepared"] = red.pop(0)
+                if "stack_ms_grouped" in stk[T]:
+                    stk[T]["stack_ms_grouped"] = red.pop(0)
 
     if rank != 0:
         if world > 1:
@@ -1689,6 +1721,13 @@ def main():
                     "ms_per_pass": round(r["stack_ms_prepared"], 4), "tops": round(tp, 2),
                     "frac": round(tp / peaks["bf16_tflops_sustained"], 4),
                     "calls": "q8_0_gemm_prepared on weights widened once per matrix (outside the timed region)"}
+            if "stack_ms_grouped" in r:
+                gg = byts / (r["stack_ms_grouped"] / 1e3) / 1e9
+                sw[str(T)]["grouped"] = {
+                    "ms_per_pass": round(r["stack_ms_grouped"], 4), "gbs": round(gg, 1),
+                    "frac": round(gg / peaks["hbm_gbs"], 4), "launches": r["grouped_calls"],
+                    "calls": "q8_0_gemv_batched_grouped for q/k/v and for gate/up of each layer, q8_0_gemm for o, "
+                             "down and the head"}
         sobj3 = {"workload": f"layer-stack sweep through q8_0_gemm: {L['layers']} layers x (q {L['q']}, k/v {L['kv']}, "
                              f"o {L['d']}, gate/up {L['nf']} at k={L['d']}; down {L['d']} at k={L['nf']}) + LM head "
                              f"{L['vocab']}x{L['d']}, one call per projection ({7 * L['layers'] + 1} calls per pass) on "

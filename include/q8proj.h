@@ -259,6 +259,33 @@ Q8_API int q8_0_gemv_batched(const void *w, int64_t n, int64_t k,
                              float *y, void *stream);
 
 /*
+ * q8_0_gemv_batched_grouped -- q8_0_gemv_batched for several projections of
+ * the same activation rows in one launch: for each i < count,
+ *     projs[i].y[t][r] = sum_b d_w(r,b) * d_a(t,b) * isum   (t < tokens)
+ * over the rows of projs[i].w, all with the same k and plane.
+ *   projs : host array of `count` descriptors (read during the call only);
+ *           w and y are device pointers (16-byte aligned); y is f32
+ *           [tokens][projs[i].n] row-major.
+ *   count : 1..Q8_MAX_GROUP.
+ *   qs, ds, tokens : as for q8_0_gemv_batched.
+ * The projections' 128-row tiles form one grid, so a narrow projection (a
+ * K or V of grouped-query attention) rides along with a wide one instead of
+ * paying its own launch and a partly idle GPU.  The per-block arithmetic is
+ * q8_0_gemv_batched's; the number of CTAs that split k for one tile (1..8) is
+ * chosen from the launch's total tile count, so the partial sums over k may
+ * be grouped differently than in a single call of one projection (equal bit
+ * for bit where that number is the same).  Results are run-to-run identical.
+ * When (k/32) % 8 != 0 the projections run one by one on the generic kernel.
+ * Errors: Q8_ERR_ARG (count, shape, tokens, a NULL pointer), Q8_ERR_ALIGN,
+ * Q8_ERR_DEVICE, Q8_ERR_LAUNCH.  Programmatic dependent launch as for
+ * q8_0_gemv.  "Part 4 - Lecture 05", sec. 2.5 (one launch for the consumers
+ * of one activation), applied to the small-batch formula above.
+ */
+Q8_API int q8_0_gemv_batched_grouped(const q8_gemv_proj *projs, int count, int64_t k,
+                                     const int8_t *qs, const uint32_t *ds, int64_t tokens,
+                                     void *stream);
+
+/*
  * q4a_gemv -- batch-1 projection with asymmetric 4-bit weight blocks, the
  * consumer of the plane's int16 block sums:
  *     y[i] = sum_b ( d*d_a * sum_e nib_e*q_e  -  m*d_a * ssum_b ).

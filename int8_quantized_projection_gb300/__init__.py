@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     q8_0_gemv_fused,
     q8_0_gemv_gate_up,
     q8_0_gemv_batched,
+    q8_0_gemv_batched_grouped,
     PRODUCER_QUANT,
     PRODUCER_RMSNORM,
     PRODUCER_SWIGLU,

@@ -44,6 +44,7 @@ SIGNATURES = {
     "q8_0_gemv_fused": (_INT, [_P, _INT, _I64, _INT, _P, _P, _P, ctypes.c_float, _P]),
     "q8_0_gemv_gate_up": (_INT, [_P, _P, _I64, _I64, _P, _P, _INT, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P]),
     "q8_0_gemv_batched": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P]),
+    "q8_0_gemv_batched_grouped": (_INT, [_P, _INT, _I64, _P, _P, _I64, _P]),
     "q4a_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q4a_gemv_batched": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P]),
     "q8_check": (_INT, [_P]),
@@ -223,6 +224,32 @@ def q8_0_gemv_batched(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=Fa
     if w.numel() != n * (k // 32) * 34 or y.numel() < t * n or qs.shape[-1] != k or qs.shape[0] < t:
         raise ValueError("shape mismatch")
     return _launch("q8_0_gemv_batched", (_ptr(w), n, k, _ptr(qs), _ptr(ds), t, _ptr(y), _stream(stream)), bind)
+
+
+def q8_0_gemv_batched_grouped(projs, k: int, qs, ds, t: int, stream=None, bind=False):
+    """Several small-batch projections of the same plane rows [0, t) in one launch.
+
+    ``projs`` is a sequence of (w uint8 Q8_0 blocks, n, y f32 [t][n]) sharing k."""
+    import torch
+
+    _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds")
+    if not 1 <= len(projs) <= MAX_GROUP or qs.shape[-1] != k or qs.shape[0] < t:
+        raise ValueError("1..8 projections sharing k and the plane")
+    arr = (GemvProj * len(projs))()
+    keep = []
+    for i, (w, n, y) in enumerate(projs):
+        _need(w, torch.uint8, "w"), _need(y, torch.float32, "y")
+        if w.numel() != n * (k // 32) * 34 or y.numel() < t * n:
+            raise ValueError("shape mismatch")
+        arr[i] = GemvProj(w.data_ptr(), n, y.data_ptr())
+        keep.append((w, y))
+    args = (ctypes.cast(arr, ctypes.c_void_p), len(projs), k, _ptr(qs), _ptr(ds), t, _stream(stream))
+    if bind:
+        b = Bound("q8_0_gemv_batched_grouped", args)
+        b._keep = (arr, keep)  # the descriptor array must outlive the bound launch
+        return b
+    _check("q8_0_gemv_batched_grouped", lib().q8_0_gemv_batched_grouped(*args))
+    return None
 
 
 def q4a_gemv(w, n: int, k: int, qs, ds, y, stream=None, bind=False):

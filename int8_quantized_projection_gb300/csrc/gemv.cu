@@ -843,10 +843,21 @@ __device__ __forceinline__ void sb_step(const uint8_t *wpiece, const uint8_t *st
         sb_block<W, BB, NT>(wpiece, stage, pc, g, t4, da, ss, acc);
 }
 
+// The projections of one small-batch launch (they share the activation and k):
+// per projection its weight map, row count, output and first row tile in the
+// launch's tile order; tile_begin[count] is the total.
+struct alignas(64) SbGroup {
+    CUtensorMap w[kMaxProj];
+    float *y[kMaxProj];
+    int64_t n[kMaxProj];
+    int tile_begin[kMaxProj + 1];
+    int count;
+};
+
 template <class W, int NT>
 __global__ void __launch_bounds__(kSbThreads)
-gemv_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmQ,
-                  const __grid_constant__ CUtensorMap tmD, int64_t n, int nb, int t, float *__restrict__ y)
+gemv_small_kernel(const __grid_constant__ SbGroup grp, const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmD, int nb, int t)
 {
     using L = SbLayout<W>;
     constexpr int kSbOffBar = L::kOffBar, kSbStageBytes = L::kStageBytes, kSbStageTx = L::kStageTx;
@@ -861,8 +872,15 @@ gemv_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + kSbOffBar);  // [stage]: the stage's boxes landed
     uint64_t *empty = full + kSbStages;                                 // [stage]: consumer warps done
     volatile int *bad = reinterpret_cast<volatile int *>(ring + kSbOffBar + kSbStages * 16);
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x / ks) * kSbRows;
-    const int rows = static_cast<int>(min(static_cast<int64_t>(kSbRows), n - row0));
+    // this CTA's projection and first row (found where needed, not held across the main loop)
+    auto locate = [&](int &pi) -> int64_t {
+        const int rtile = static_cast<int>(blockIdx.x) / ks;  // row tile of the launch, over all projections
+        pi = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxProj; ++i)
+            if (i < grp.count && rtile >= grp.tile_begin[i]) pi = i;
+        return static_cast<int64_t>(rtile - grp.tile_begin[pi]) * kSbRows;
+    };
     // the last stage may hang past the end of the rows: those pieces, codes
     // and scales arrive as zeros and add exactly nothing
     const int stages_total = (nb + kSbGroup * kSbPieces - 1) / (kSbGroup * kSbPieces);
@@ -887,9 +905,12 @@ gemv_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
             // the first stages' weight boxes go out before waiting for it
             // (programmatic dependent launch), every activation box after.
             const uint32_t rb = q8::smem_u32(ring);
+            int pi;
+            const int64_t row0 = locate(pi);
+            const CUtensorMap *tmW = &grp.w[pi];
             auto issue_w = [&](int s, int gi) {
                 q8::mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(kSbStageTx));
-                q8::tma_load_3d(rb + s * kSbStageBytes + kSbOffW, &tmW, 0, gi * kSbPieces, static_cast<int>(row0),
+                q8::tma_load_3d(rb + s * kSbStageBytes + kSbOffW, tmW, 0, gi * kSbPieces, static_cast<int>(row0),
                                 q8::smem_u32(&full[s]));
             };
             auto issue_a = [&](int s, int gi) {
@@ -990,6 +1011,11 @@ gemv_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
         bool any_bad = *bad != 0;
         for (int r = 1; r < ks; ++r) any_bad |= *cluster.map_shared_rank(const_cast<int *>(bad), r) != 0;
         if (!any_bad) {
+            int pi;
+            const int64_t row0 = locate(pi);
+            const int64_t n = grp.n[pi];
+            float *__restrict__ y = grp.y[pi];
+            const int rows = static_cast<int>(min(static_cast<int64_t>(kSbRows), n - row0));
             for (int o = threadIdx.x; o < 8 * NT * kSbRows; o += kSbThreads) {
                 const int tok = o / kSbRows, r = o % kSbRows;
                 if (tok < t && r < rows) {
@@ -1041,17 +1067,21 @@ int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, c
 
 namespace {
 
-// Launch the small-batch kernel for weight format W: 1 <= tokens <= 16,
-// (k/32) % 8 == 0.  The cluster size (CTAs splitting k, 1..8) makes the grid
-// about one wave of the CTAs that fit on the GPU at once (the occupancy the
-// runtime reports for this kernel, its shared memory and its registers).
+// Launch the small-batch kernel for weight format W over `count` projections
+// of one activation: 1 <= tokens <= 16, (k/32) % 8 == 0.  Their row tiles form
+// one grid (small projections ride along with large ones).  The cluster size
+// (CTAs splitting k, 1..8) makes the grid about one wave of the CTAs that fit
+// on the GPU at once (the occupancy the runtime reports for this kernel, its
+// shared memory and its registers).
 template <class W>
-int gemv_small_launch_t(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
+int gemv_small_launch_t(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds,
                         int64_t tokens, cudaStream_t s, int slot1, int slot2)
 {
     using L = SbLayout<W>;
     const int64_t nb = k / 32;
-    if (tokens < 1 || tokens > kSbMaxTokens || nb % kSbGroup != 0 || nb > (int64_t(1) << 30)) return Q8_ERR_ARG;
+    if (count < 1 || count > kMaxProj || tokens < 1 || tokens > kSbMaxTokens || nb % kSbGroup != 0 ||
+        nb > (int64_t(1) << 30))
+        return Q8_ERR_ARG;
     const int64_t stages = (nb + kSbGroup * kSbPieces - 1) / (kSbGroup * kSbPieces);
     const int sms = q8::device_sm_count();
     if (sms <= 0) return Q8_ERR_DEVICE;
@@ -1064,28 +1094,41 @@ int gemv_small_launch_t(const void *w, int64_t n, int64_t k, const int8_t *qs, c
             cudaSuccess ||
         per_sm < 1)
         return Q8_ERR_LAUNCH;
-    const int64_t tiles = (n + kSbRows - 1) / kSbRows;
+    SbGroup grp;
+    std::memset(&grp, 0, sizeof(grp));
+    grp.count = count;
+    int64_t tiles = 0;
+    for (int i = 0; i < count; ++i) {
+        grp.tile_begin[i] = static_cast<int>(tiles);
+        tiles += (projs[i].n + kSbRows - 1) / kSbRows;
+        if (tiles > 0x7fffffff) return Q8_ERR_ARG;
+        grp.y[i] = projs[i].y;
+        grp.n[i] = projs[i].n;
+        // weights as [n rows][nb/8 pieces][piece bytes / 2 u16]; box = kSbRows rows x kSbPieces pieces
+        if (!q8::make_map_3d(&grp.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, projs[i].w, L::kPieceBytes / 2,
+                             static_cast<uint64_t>(nb / kSbGroup), static_cast<uint64_t>(projs[i].n), L::kPieceBytes,
+                             static_cast<uint64_t>(nb * W::kBlockBytes), L::kPieceBytes / 2, kSbPieces, kSbRows,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+            return Q8_ERR_LAUNCH;
+    }
+    for (int i = count; i <= kMaxProj; ++i) grp.tile_begin[i] = static_cast<int>(tiles);
     // about one wave of resident CTAs, at least one stage per CTA
     int64_t ks = (static_cast<int64_t>(per_sm) * sms) / tiles;
     ks = ks < 1 ? 1 : (ks > kSbMaxCluster ? kSbMaxCluster : ks);
     if (ks > stages) ks = stages;
     if (tiles * ks > 0x7fffffff) return Q8_ERR_ARG;
     const dim3 grid(static_cast<unsigned>(tiles * ks));
-    CUtensorMap mw, mq, md;
-    // weights as [n rows][nb/8 pieces][piece bytes / 2 u16]; box = kSbRows rows x kSbPieces pieces
-    if (!q8::make_map_3d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, L::kPieceBytes / 2, static_cast<uint64_t>(nb / kSbGroup),
-                     static_cast<uint64_t>(n), L::kPieceBytes, static_cast<uint64_t>(nb * W::kBlockBytes),
-                     L::kPieceBytes / 2, kSbPieces, kSbRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !q8::make_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qs, static_cast<uint64_t>(k), static_cast<uint64_t>(tokens),
-                     static_cast<uint64_t>(k), 128, kSbMaxTokens, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    CUtensorMap mq, md;
+    if (!q8::make_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qs, static_cast<uint64_t>(k), static_cast<uint64_t>(tokens),
+                         static_cast<uint64_t>(k), 128, kSbMaxTokens, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !q8::make_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT32, ds, static_cast<uint64_t>(nb), static_cast<uint64_t>(tokens),
-                     static_cast<uint64_t>(nb * 4), kSbGroup * kSbPieces, kSbMaxTokens, CU_TENSOR_MAP_SWIZZLE_NONE))
+                         static_cast<uint64_t>(nb * 4), kSbGroup * kSbPieces, kSbMaxTokens, CU_TENSOR_MAP_SWIZZLE_NONE))
         return Q8_ERR_LAUNCH;
     if (wide)
         return q8::launch_pdl_cluster(gemv_small_kernel<W, 2>, grid, dim3(kSbThreads), L::kSmem, s, static_cast<int>(ks),
-                                  mw, mq, md, n, static_cast<int>(nb), static_cast<int>(tokens), y);
-    return q8::launch_pdl_cluster(gemv_small_kernel<W, 1>, grid, dim3(kSbThreads), L::kSmem, s, static_cast<int>(ks), mw,
-                              mq, md, n, static_cast<int>(nb), static_cast<int>(tokens), y);
+                                      grp, mq, md, static_cast<int>(nb), static_cast<int>(tokens));
+    return q8::launch_pdl_cluster(gemv_small_kernel<W, 1>, grid, dim3(kSbThreads), L::kSmem, s, static_cast<int>(ks),
+                                  grp, mq, md, static_cast<int>(nb), static_cast<int>(tokens));
 }
 
 } // namespace
@@ -1095,13 +1138,21 @@ namespace q8 {
 int gemv_small_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
                       int64_t tokens, cudaStream_t s)
 {
-    return gemv_small_launch_t<SbQ8_0>(w, n, k, qs, ds, y, tokens, s, 3, 4);
+    const q8_gemv_proj p = {w, n, y};
+    return gemv_small_launch_t<SbQ8_0>(&p, 1, k, qs, ds, tokens, s, 3, 4);
+}
+
+int gemv_small_grouped_launch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds,
+                              int64_t tokens, cudaStream_t s)
+{
+    return gemv_small_launch_t<SbQ8_0>(projs, count, k, qs, ds, tokens, s, 3, 4);
 }
 
 int gemv_small_q4a_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
                           int64_t tokens, cudaStream_t s)
 {
-    return gemv_small_launch_t<SbQ4A>(w, n, k, qs, ds, y, tokens, s, 7, 8);
+    const q8_gemv_proj p = {w, n, y};
+    return gemv_small_launch_t<SbQ4A>(&p, 1, k, qs, ds, tokens, s, 7, 8);
 }
 
 } // namespace q8
@@ -1345,4 +1396,25 @@ extern "C" int q8_0_gemv_batched(const void *w, int64_t n, int64_t k, const int8
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((k / 32) % 8 != 0) return q8::gemv_generic_launch(w, n, k, qs, ds, y, tokens, s);
     return q8::gemv_small_launch(w, n, k, qs, ds, y, tokens, s);
+}
+
+extern "C" int q8_0_gemv_batched_grouped(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs,
+                                         const uint32_t *ds, int64_t tokens, void *stream)
+{
+    if (!projs || count < 1 || count > kMaxProj || !qs || !ds || k <= 0 || (k % 32) != 0 || tokens < 1 ||
+        tokens > Q8_GEMV_MAX_TOKENS)
+        return Q8_ERR_ARG;
+    for (int i = 0; i < count; ++i)
+        if (!projs[i].w || !projs[i].y || projs[i].n < 1 || projs[i].n > (int64_t(1) << 40)) return Q8_ERR_ARG;
+    if (!q8::aligned16(qs) || !q8::aligned16(ds)) return Q8_ERR_ALIGN;
+    for (int i = 0; i < count; ++i)
+        if (!q8::aligned16(projs[i].w) || !q8::aligned16(projs[i].y)) return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((k / 32) % 8 == 0) return q8::gemv_small_grouped_launch(projs, count, k, qs, ds, tokens, s);
+    for (int i = 0; i < count; ++i) {
+        const int st = q8::gemv_generic_launch(projs[i].w, projs[i].n, k, qs, ds, projs[i].y, tokens, s);
+        if (st != Q8_OK) return st;
+    }
+    return Q8_OK;
 }

@@ -104,6 +104,8 @@ int gemv_generic_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, c
 // small-batch kernel (gemv.cu): 1 <= tokens <= Q8_GEMV_MAX_TOKENS, (k/32) % 8 == 0
 int gemv_small_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
                       int64_t tokens, cudaStream_t s);
+int gemv_small_grouped_launch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs, const uint32_t *ds,
+                              int64_t tokens, cudaStream_t s);
 // Token counts up to kSlicedMaxTokens run the small-batch kernel over 16-token
 // slices of the plane (each slice streams the weights once more): up to four
 // passes cost less than the GEMM's weight pre-pass and its f16 re-read.

@@ -114,6 +114,24 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert lib.q8_0_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 17, P(FAKE), s) == ERR_ARG
     assert lib.q8_0_gemv_batched(P(FAKE), 8, 100, P(FAKE), P(FAKE), 4, P(FAKE), s) == ERR_ARG
     assert lib.q8_0_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 4, P(MISALIGNED), s) == ERR_ALIGN
+    # q8_0_gemv_batched_grouped: count 1..8, tokens 1..16, k % 32, each projection's pointers and n, alignment
+    grp = (_binding.GemvProj * 2)(_binding.GemvProj(FAKE, 8, FAKE), _binding.GemvProj(FAKE, 40, FAKE))
+    gp = ctypes.cast(grp, ctypes.c_void_p)
+    bgrp = lib.q8_0_gemv_batched_grouped
+    assert bgrp(None, 1, 256, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert bgrp(gp, 0, 256, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert bgrp(gp, 9, 256, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert bgrp(gp, 2, 256, P(FAKE), P(FAKE), 0, s) == ERR_ARG
+    assert bgrp(gp, 2, 256, P(FAKE), P(FAKE), 17, s) == ERR_ARG
+    assert bgrp(gp, 2, 100, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert bgrp(gp, 2, 256, P(0), P(FAKE), 4, s) == ERR_ARG
+    assert bgrp(gp, 2, 256, P(FAKE), P(MISALIGNED), 4, s) == ERR_ALIGN
+    grp[1] = _binding.GemvProj(FAKE, 0, FAKE)
+    assert bgrp(gp, 2, 256, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    grp[1] = _binding.GemvProj(FAKE, 40, None)
+    assert bgrp(gp, 2, 256, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    grp[1] = _binding.GemvProj(FAKE, 40, MISALIGNED)
+    assert bgrp(gp, 2, 256, P(FAKE), P(FAKE), 4, s) == ERR_ALIGN
     # q4a_gemv: k % 128, n < 1, alignment
     assert lib.q4a_gemv(P(FAKE), 8, 96, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG
     assert lib.q4a_gemv(P(FAKE), 0, 256, P(FAKE), P(FAKE), P(FAKE), s) == ERR_ARG

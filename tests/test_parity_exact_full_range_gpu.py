@@ -22,7 +22,8 @@ producer-fused A-quantize mode 1", sec. 2.1).
 
 Paths: q8_0_gemv (staged kernel at k = 256/512/1024, generic at k = 96/128),
 q8_0_gemv_grouped, q8_0_gemv_gate_up (its f32 gate/up outputs),
-q8_0_gemv_batched (t = 1..8 on the int8 MMA, 9..16 on the f16 MMA), q8_0_gemm
+q8_0_gemv_batched (t = 1..8 on the int8 MMA, 9..16 on the f16 MMA),
+q8_0_gemv_batched_grouped, q8_0_gemm
 (16-token slices for 16 < t <= 64, the tcgen05 kernel unsplit and split over
 k, the generic kernel), q8_0_gemm_mma, q4a_gemv and q4a_gemv_batched.
 """
@@ -154,6 +155,20 @@ def test_gemv_batched_full_range_bit_exact(q8, n, k, t):
     q8.q8_check()
     yr, ar = oracle.gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
     _assert_exact(host(y), yr, ar, f"gemv_batched {n}x{k} t={t}")
+
+
+@pytest.mark.parametrize("t", [3, 16])
+def test_gemv_batched_grouped_full_range_bit_exact(q8, t):
+    k, ns = 1024, [300, 37, 129, 7]
+    qs, ds = _unit_plane(31, t, k, rows_pad=128)
+    blobs = [_unit_weights(32 + i, n, k) for i, n in enumerate(ns)]
+    ys = [nan_f32(t, n) for n in ns]
+    q8.q8_0_gemv_batched_grouped([(dev(b), n, y) for b, n, y in zip(blobs, ns, ys)], k, dev(qs),
+                                 dev(ds.view(np.int32)), t)
+    q8.q8_check()
+    for blob, n, y in zip(blobs, ns, ys):
+        yr, ar = oracle.gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+        _assert_exact(host(y), yr, ar, f"grouped gemv_batched {n}x{k} t={t}")
 
 
 # ---------------------------------------------------------------------------
