@@ -711,8 +711,7 @@ struct SbLayout {
 
 __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
@@ -772,13 +771,18 @@ __device__ __forceinline__ void sb_block(const uint8_t *wpiece, const uint8_t *s
     q8::i8x4_to_f16x4(chi.y, a1[1], a1[3]);
     const float dlo = W::template d<BB>(rlo), dhi = W::template d<BB>(rhi);
     const float mlo = W::template m<BB>(rlo), mhi = W::template m<BB>(rhi);
+    // the token tiles' first k-halves, then their second halves: consecutive
+    // MMAs are independent when NT > 1
+    float c[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        mma_f16_16816(c, a0, bf[j][0], bf[j][1]);
-        mma_f16_16816(c, a1, bf[j][2], bf[j][3]);
-        sb_epilogue<W>(acc[j], c, dlo, dhi, mlo, mhi, da[j], ss[j]);
+        c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+        mma_f16_16816(c[j], a0, bf[j][0], bf[j][1]);
     }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) mma_f16_16816(c[j], a1, bf[j][2], bf[j][3]);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) sb_epilogue<W>(acc[j], c[j], dlo, dhi, mlo, mhi, da[j], ss[j]);
 }
 
 __device__ __forceinline__ void mma_s8_16832(int (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -855,7 +859,7 @@ struct alignas(64) SbGroup {
 };
 
 template <class W, int NT>
-__global__ void __launch_bounds__(kSbThreads)
+__global__ void __launch_bounds__(kSbThreads, 2)
 gemv_small_kernel(const __grid_constant__ SbGroup grp, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmD, int nb, int t)
 {
@@ -1007,26 +1011,38 @@ gemv_small_kernel(const __grid_constant__ SbGroup grp, const __grid_constant__ C
         part[o] = v;
     }
     cluster.sync();  // every CTA's partial sums are in its shared memory
-    if (rank == 0) {
-        bool any_bad = *bad != 0;
-        for (int r = 1; r < ks; ++r) any_bad |= *cluster.map_shared_rank(const_cast<int *>(bad), r) != 0;
-        if (!any_bad) {
-            int pi;
-            const int64_t row0 = locate(pi);
-            const int64_t n = grp.n[pi];
-            float *__restrict__ y = grp.y[pi];
-            const int rows = static_cast<int>(min(static_cast<int64_t>(kSbRows), n - row0));
-            for (int o = threadIdx.x; o < 8 * NT * kSbRows; o += kSbThreads) {
-                const int tok = o / kSbRows, r = o % kSbRows;
-                if (tok < t && r < rows) {
-                    float v = part[o];
-                    for (int pr = 1; pr < ks; ++pr) v += *cluster.map_shared_rank(part + o, pr);
-                    y[tok * n + row0 + r] = v;
-                }
+    // Each CTA of the cluster finishes a 1/ks share of the tile's outputs: it
+    // loads the ks partial sums of an output together (distributed shared
+    // memory) and adds them in rank order.
+    bool any_bad = false;
+    for (int r = 0; r < ks; ++r) any_bad |= *cluster.map_shared_rank(const_cast<int *>(bad), r) != 0;
+    if (!any_bad) {
+        int pi;
+        const int64_t row0 = locate(pi);
+        const int64_t n = grp.n[pi];
+        float *__restrict__ y = grp.y[pi];
+        const int rows = static_cast<int>(min(static_cast<int64_t>(kSbRows), n - row0));
+        constexpr int kOut = 8 * NT * kSbRows;
+        const int share = (kOut + ks - 1) / ks;
+        const int o_end = min(kOut, (rank + 1) * share);
+        const float *src[kSbMaxCluster];
+#pragma unroll
+        for (int pr = 0; pr < kSbMaxCluster; ++pr) src[pr] = pr < ks ? cluster.map_shared_rank(part, pr) : part;
+        for (int o = rank * share + static_cast<int>(threadIdx.x); o < o_end; o += kSbThreads) {
+            const int tok = o / kSbRows, r = o % kSbRows;
+            if (tok < t && r < rows) {
+                float pv[kSbMaxCluster];
+#pragma unroll
+                for (int pr = 0; pr < kSbMaxCluster; ++pr) pv[pr] = pr < ks ? src[pr][o] : 0.0f;
+                float v = pv[0];
+#pragma unroll
+                for (int pr = 1; pr < kSbMaxCluster; ++pr)
+                    if (pr < ks) v += pv[pr];
+                y[tok * n + row0 + r] = v;
             }
         }
     }
-    cluster.sync();  // peers keep their shared memory until rank 0 has read it
+    cluster.sync();  // every CTA keeps its shared memory until its peers have read it
 }
 
 int ceil_log2(int v)
