@@ -702,7 +702,13 @@ struct SbLayout {
     static constexpr int kPieceBytes = kSbGroup * W::kBlockBytes;   // 272 (Q8_0), 160 (Q4A): multiples of 16
     static constexpr int kRowBytes = kSbPieces * kPieceBytes;       // weight bytes per row and stage
     static constexpr int kStageTx = kSbOffW + kSbRows * kRowBytes;  // bytes the TMA writes per stage
-    static constexpr int kStageBytes = (kStageTx + 1023) / 1024 * 1024;
+    // the f16 path's prepared activation (written by the consumer warps, not
+    // the TMA): codes as f16 in fragment order [block][token][t4][4 words],
+    // and per (block, token tile, t4) {d_a, d_a, ssum, ssum} of tokens
+    // 8j + 2*t4 and 8j + 2*t4 + 1 as f32
+    static constexpr int kOffAh = (kStageTx + 127) / 128 * 128;
+    static constexpr int kOffDc = kOffAh + kSbPieces * kSbGroup * kSbMaxTokens * 64;
+    static constexpr int kStageBytes = (kOffDc + kSbPieces * kSbGroup * 2 * 4 * 16 + 1023) / 1024 * 1024;
     static constexpr int kOffBar = kSbStages * kStageBytes;         // full[], empty[], error flag
     static constexpr int kSmem = kOffBar + 128 + 1024;              // + alignment slack
     static_assert(kPieceBytes % 16 == 0, "TMA box rows");
@@ -751,15 +757,21 @@ __device__ __forceinline__ void sb_epilogue(float2 (&acc)[2], const float (&c)[4
 // (+8 per token tile), kept as token pairs.  da[j] is the d_a pair of tile j.
 template <class W, int BB, int NT>
 __device__ __forceinline__ void sb_block(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
-                                         const float2 (&da)[NT], const float2 (&ss)[NT], float2 (&acc)[NT][2])
+                                         float2 (&acc)[NT][2])
 {
-    constexpr int kRowBytes = SbLayout<W>::kRowBytes;
+    using L = SbLayout<W>;
+    constexpr int kRowBytes = L::kRowBytes;
+    const int bb = pc * kSbGroup + BB;  // block of the stage
     uint32_t bf[NT][4];  // token 8j+g: step 0 {codes 0,1 | 2,3} of word t4, step 1 the same of word t4 + 4
+    float2 da[NT], ss[NT];  // d_a and ssum of tokens 8j + 2*t4, 8j + 2*t4 + 1
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-        const uint2 v = sb_act<BB>(stage, pc, 8 * j + g, t4);
-        q8::i8x4_to_f16x4(v.x, bf[j][0], bf[j][1]);
-        q8::i8x4_to_f16x4(v.y, bf[j][2], bf[j][3]);
+        const uint4 v = *reinterpret_cast<const uint4 *>(stage + L::kOffAh + (((bb * kSbMaxTokens + 8 * j + g) * 4 + t4)
+                                                                              << 4));
+        bf[j][0] = v.x, bf[j][1] = v.y, bf[j][2] = v.z, bf[j][3] = v.w;
+        const float4 e = *reinterpret_cast<const float4 *>(stage + L::kOffDc + (((bb * 2 + j) * 4 + t4) << 4));
+        da[j] = make_float2(e.x, e.y);
+        ss[j] = make_float2(e.z, e.w);
     }
     const uint8_t *rlo = wpiece + g * kRowBytes;  // row g of the tile
     const uint8_t *rhi = rlo + 8 * kRowBytes;      // row g + 8
@@ -830,27 +842,79 @@ template <class W, int BB, int NT>
 __device__ __forceinline__ void sb_step(const uint8_t *wpiece, const uint8_t *stage, int pc, int g, int t4,
                                         const uint4 (&dsv)[NT][2][2], float2 (&acc)[NT][2])
 {
-    float2 da[NT], ss[NT];  // d_a and (asymmetric weights) the plane's ssum of the token pair
+    if constexpr (NT > Q8_SB_S8_TILES) {
+        sb_block<W, BB, NT>(wpiece, stage, pc, g, t4, acc);  // the prepared f16 activation
+    } else {
+        float2 da[NT], ss[NT];  // d_a and (asymmetric weights) the plane's ssum of the token pair
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        const uint4 &e = dsv[j][0][BB >> 2], &o = dsv[j][1][BB >> 2];  // tokens 8j + 2*t4, 8j + 2*t4 + 1
-        constexpr int q = BB & 3;
-        const uint32_t we = q == 0 ? e.x : q == 1 ? e.y : q == 2 ? e.z : e.w;
-        const uint32_t wo = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
-        da[j] = make_float2(sb_half_lo(we), sb_half_lo(wo));
-        ss[j] = make_float2(static_cast<float>(static_cast<int16_t>(we >> 16)),
-                            static_cast<float>(static_cast<int16_t>(wo >> 16)));
-    }
-    if constexpr (NT <= Q8_SB_S8_TILES)
+        for (int j = 0; j < NT; ++j) {
+            const uint4 &e = dsv[j][0][BB >> 2], &o = dsv[j][1][BB >> 2];  // tokens 8j + 2*t4, 8j + 2*t4 + 1
+            constexpr int q = BB & 3;
+            const uint32_t we = q == 0 ? e.x : q == 1 ? e.y : q == 2 ? e.z : e.w;
+            const uint32_t wo = q == 0 ? o.x : q == 1 ? o.y : q == 2 ? o.z : o.w;
+            da[j] = make_float2(sb_half_lo(we), sb_half_lo(wo));
+            ss[j] = make_float2(static_cast<float>(static_cast<int16_t>(we >> 16)),
+                                static_cast<float>(static_cast<int16_t>(wo >> 16)));
+        }
         sb_block_s8<W, BB, NT>(wpiece, stage, pc, g, t4, da, ss, acc);
-    else
-        sb_block<W, BB, NT>(wpiece, stage, pc, g, t4, da, ss, acc);
+    }
+}
+
+// The f16 path's activation, prepared once per stage by the consumer warps
+// together (thread u of kSbWarps * 32) instead of by each warp per block: per
+// item (block, token, t4) the code words t4 and t4 + 4 of the token's block
+// (TMA box 2*pc + BB/4, 128-byte swizzled) widened exactly to four f16 pairs
+// at item * 16 of the f16 area; per item (block, token tile j, t4) the d_a
+// and ssum of tokens 8j + 2*t4 and 8j + 2*t4 + 1.
+template <class W>
+__device__ __forceinline__ void sb_prep_act(uint8_t *stage, int u)
+{
+    using L = SbLayout<W>;
+    constexpr int kItems = kSbPieces * kSbGroup * kSbMaxTokens * 4;
+#pragma unroll
+    for (int it = u; it < kItems; it += kSbWarps * 32) {
+        const int t4 = it & 3, tok = (it >> 2) & (kSbMaxTokens - 1), bb = it >> 6;
+        const int pc = bb / kSbGroup, BB = bb % kSbGroup;
+        const int c0 = 2 * (BB & 3);
+        const uint8_t *line = stage + kSbOffAct + (2 * pc + (BB >> 2)) * 2048 + tok * 128;
+        const uint32_t lo = *reinterpret_cast<const uint32_t *>(line + ((c0 ^ (tok & 7)) << 4) + 4 * t4);
+        const uint32_t hi = *reinterpret_cast<const uint32_t *>(line + (((c0 + 1) ^ (tok & 7)) << 4) + 4 * t4);
+        uint4 v;
+        q8::i8x4_to_f16x4(lo, v.x, v.y);
+        q8::i8x4_to_f16x4(hi, v.z, v.w);
+        *reinterpret_cast<uint4 *>(stage + L::kOffAh + (it << 4)) = v;
+    }
+    constexpr int kScaleItems = kSbPieces * kSbGroup * 2 * 4;
+    if (u < kScaleItems) {
+        const int t4 = u & 3, j = (u >> 2) & 1, bb = u >> 3;
+        const int pc = bb / kSbGroup, BB = bb % kSbGroup;
+        const uint8_t *dw = stage + kSbOffDs + 4 * kSbGroup * pc + 4 * BB;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(dw + (8 * j + 2 * t4) * (32 * kSbPieces));
+        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(dw + (8 * j + 2 * t4 + 1) * (32 * kSbPieces));
+        *reinterpret_cast<float4 *>(stage + L::kOffDc + (u << 4)) =
+            make_float4(sb_half_lo(w0), sb_half_lo(w1), static_cast<float>(static_cast<int16_t>(w0 >> 16)),
+                        static_cast<float>(static_cast<int16_t>(w1 >> 16)));
+    }
+}
+
+// Named barrier `id` of `n` threads that also reports whether p held on every
+// one of them (all participants get the same answer).
+__device__ __forceinline__ bool bar_all(int id, int n, bool p)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
 }
 
 // The projections of one small-batch launch (they share the activation and k):
 // per projection its weight map, row count, output and first row tile in the
 // launch's tile order; tile_begin[count] is the total.
-struct alignas(64) SbGroup {
+struct SbGroup {
     CUtensorMap w[kMaxProj];
     float *y[kMaxProj];
     int64_t n[kMaxProj];
@@ -958,25 +1022,38 @@ gemv_small_kernel(const __grid_constant__ SbGroup grp, const __grid_constant__ C
         for (int i = 0; i < ng; ++i) {
             const int s = i % kSbStages;
             const bool got = q8::mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / kSbStages) & 1u);
-            if (!__all_sync(Q8_FULL_MASK, got)) {
-                if (lane == 0) {
-                    atomicOr(&g_gemv_err, 1u);
-                    *bad = 1;
+            uint8_t *st = ring + s * kSbStageBytes;
+            uint4 dsv[NT][2][2];  // [tile][token 2*t4 + e][blocks 0-3, 4-7]: the stage's d|ssum words (int8 path)
+            if constexpr (NT > Q8_SB_S8_TILES) {
+                // f16 path: the consumer warps prepare the stage's activation together;
+                // the barrier publishes it and tells every warp whether all stages arrived
+                if (got) sb_prep_act<W>(st, static_cast<int>(threadIdx.x));
+                if (!bar_all(1, kSbWarps * 32, got)) {
+                    if (lane == 0) {
+                        atomicOr(&g_gemv_err, 1u);
+                        *bad = 1;
+                    }
+                    break;
                 }
-                break;
+            } else {
+                if (!__all_sync(Q8_FULL_MASK, got)) {
+                    if (lane == 0) {
+                        atomicOr(&g_gemv_err, 1u);
+                        *bad = 1;
+                    }
+                    break;
+                }
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint4 *dw = reinterpret_cast<const uint4 *>(st + kSbOffDs + 4 * kSbGroup * pc +
+                                                                          (8 * j + 2 * t4 + e) * (32 * kSbPieces));
+                        dsv[j][e][0] = dw[0];
+                        dsv[j][e][1] = dw[1];
+                    }
             }
-            const uint8_t *st = ring + s * kSbStageBytes;
             const uint8_t *wp = st + kSbOffW + tile * 16 * kSbRowBytes + pc * kSbPieceBytes;
-            uint4 dsv[NT][2][2];  // [tile][token 2*t4 + e][blocks 0-3, 4-7]: the stage's d|ssum words
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint4 *dw = reinterpret_cast<const uint4 *>(st + kSbOffDs + 4 * kSbGroup * pc +
-                                                                      (8 * j + 2 * t4 + e) * (32 * kSbPieces));
-                    dsv[j][e][0] = dw[0];
-                    dsv[j][e][1] = dw[1];
-                }
             sb_step<W, 0, NT>(wp, st, pc, g, t4, dsv, acc);
             sb_step<W, 1, NT>(wp, st, pc, g, t4, dsv, acc);
             sb_step<W, 2, NT>(wp, st, pc, g, t4, dsv, acc);
