@@ -885,6 +885,7 @@ __device__ __forceinline__ void sb_prep_act(uint8_t *stage, int u)
         *reinterpret_cast<uint4 *>(stage + L::kOffAh + (it << 4)) = v;
     }
     constexpr int kScaleItems = kSbPieces * kSbGroup * 2 * 4;
+    static_assert(kScaleItems <= kSbWarps * 32, "one scale item per thread at most");
     if (u < kScaleItems) {
         const int t4 = u & 3, j = (u >> 2) & 1, bb = u >> 3;
         const int pc = bb / kSbGroup, BB = bb % kSbGroup;
