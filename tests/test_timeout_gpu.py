@@ -12,8 +12,8 @@ returned to the caller, which falls back).
 The test builds a second copy of the library whose main-loop waits give up
 at once (a zero limit: any wait that is not already satisfied times out;
 drains keep their limit), loads it in a subprocess bounded by a host-side
-timeout, and checks that a GEMM, a batch-1 GEMV and a many-row RMSNorm each
-report the timeout, that the report is cleared, and that nothing hangs.  A fresh process with the
+timeout, and checks that a GEMM, a batch-1 GEMV, the small-batch GEMV on
+both of its MMA paths and a many-row RMSNorm each report the timeout, that the report is cleared, and that nothing hangs.  A fresh process with the
 normal library then gives a correct result.  Nothing here faults or hangs the
 GPU: each wait is bounded, and every kernel reaches its exit after a timeout.
 """
@@ -61,6 +61,17 @@ _CHILD = textwrap.dedent(
     assert lib.q8_0_gemv(P(w), n, k, P(qs), P(ds), P(y), st) == 0
     out["gemv"] = lib.q8_check(st)
     out["gemv_after"] = lib.q8_check(st)
+    # small-batch GEMV: t = 16 (f16 path, where the consumer warps agree on each
+    # stage's arrival at a barrier and leave together) and t = 4 (int8 path)
+    n, k = 4096, 7168
+    w = torch.from_numpy(syn.q8_0_weights(syn.rng(75, 2), n, k)[0]).cuda()
+    qs = torch.randint(-127, 128, (128, k), dtype=torch.int8, device="cuda")
+    ds = torch.full((128, k // 32), 0x3C00, dtype=torch.int32, device="cuda")
+    for tt in (16, 4):
+        y = torch.empty(tt, n, device="cuda")
+        assert lib.q8_0_gemv_batched(P(w), n, k, P(qs), P(ds), tt, P(y), st) == 0
+        out["small%d" % tt] = lib.q8_check(st)
+        out["small%d_after" % tt] = lib.q8_check(st)
     # RMSNorm over many rows: the shared-memory row ring waits for each row's copy
     rows, d = 3325, 3584
     x = torch.randn(rows, d, device="cuda")
@@ -110,8 +121,9 @@ def test_waits_that_run_out_report_a_timeout(tmp_path):
 
     lib = build.build(extra=["-DQ8_WAIT_LIMIT_NS=0ull"], lib_path=str(tmp_path / "libq8proj_waits0.so"))
     got = _run(_CHILD, ROOT=ROOT, LIB=lib)
-    assert got["gemm"] == 5 and got["gemv"] == 5 and got["rmsnorm"] == 5, got  # Q8_ERR_DEVICE_TIMEOUT
-    assert got["gemm_after"] == 0 and got["gemv_after"] == 0 and got["rmsnorm_after"] == 0, got  # then cleared
+    calls = ("gemm", "gemv", "small16", "small4", "rmsnorm")
+    assert all(got[c] == 5 for c in calls), got  # Q8_ERR_DEVICE_TIMEOUT
+    assert all(got[c + "_after"] == 0 for c in calls), got  # then cleared
     # a fresh process with the normal library computes correctly
     err = _run(_FRESH, ROOT=ROOT)
     assert err <= 1e-5
