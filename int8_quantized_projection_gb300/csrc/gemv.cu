@@ -1029,6 +1029,7 @@ gemv_small_kernel(const __grid_constant__ SbGroup grp, const __grid_constant__ C
                 // f16 path: the consumer warps prepare the stage's activation together;
                 // the barrier publishes it and tells every warp whether all stages arrived
                 if (got) sb_prep_act<W>(st, static_cast<int>(threadIdx.x));
+                __syncwarp();  // the barrier below is warp-aligned; got may differ between lanes on a timeout
                 if (!bar_all(1, kSbWarps * 32, got)) {
                     if (lane == 0) {
                         atomicOr(&g_gemv_err, 1u);
