@@ -107,3 +107,23 @@ def test_gemv_batched_grouped_rejects_bad_arguments(q8):
             q8.q8_0_gemv_batched_grouped([(w, 8, y)], k, qs, ds, t)
     with pytest.raises(ValueError):
         q8.q8_0_gemv_batched_grouped([(w, 8, y)] * 9, k, qs, ds, 4)
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_gemv_batched_grouped_random_groups(q8, case):
+    """Seeded random groups: 1..8 projections of 1..5000 rows, k a multiple of
+    256 up to 4096 (or 96 for the generic kernel), 1..16 tokens."""
+    import torch
+
+    g = np.random.default_rng(1000 + case)
+    count = int(g.integers(1, 9))
+    k = 96 if case == 5 else 256 * int(g.integers(1, 17))
+    t = int(g.integers(1, 17))
+    ns = [int(g.integers(1, 5001)) for _ in range(count)]
+    blobs = [_weights(200 + 10 * case + i, n, k) for i, n in enumerate(ns)]
+    qs, ds = _plane(200 + case, t, k, rows_pad=128)
+    ys = _run(q8, k, blobs, ns, qs, ds, t)
+    for i, (blob, n, y) in enumerate(zip(blobs, ns, ys)):
+        assert not torch.isnan(y).any().item(), f"projection {i}: unwritten outputs"
+        yr, ar = oracle.gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+        assert_gemm_close(host(y), yr, ar, f"random group {case}, projection {i}: {n}x{k} t={t}")
