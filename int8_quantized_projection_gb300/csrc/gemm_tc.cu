@@ -150,6 +150,18 @@ __device__ __forceinline__ void tc_regs16(uint32_t (&r)[16])
                    "+r"(r[15]));
 }
 
+// Pass 16 accumulator pairs through an empty statement: the arithmetic that
+// produced them is done before any later volatile statement (a TMEM wait).
+__device__ __forceinline__ void acc_order16(float2 *a)
+{
+    asm volatile(""
+                 : "+f"(a[0].x), "+f"(a[0].y), "+f"(a[1].x), "+f"(a[1].y), "+f"(a[2].x), "+f"(a[2].y), "+f"(a[3].x),
+                   "+f"(a[3].y), "+f"(a[4].x), "+f"(a[4].y), "+f"(a[5].x), "+f"(a[5].y), "+f"(a[6].x), "+f"(a[6].y),
+                   "+f"(a[7].x), "+f"(a[7].y), "+f"(a[8].x), "+f"(a[8].y), "+f"(a[9].x), "+f"(a[9].y), "+f"(a[10].x),
+                   "+f"(a[10].y), "+f"(a[11].x), "+f"(a[11].y), "+f"(a[12].x), "+f"(a[12].y), "+f"(a[13].x),
+                   "+f"(a[13].y), "+f"(a[14].x), "+f"(a[14].y), "+f"(a[15].x), "+f"(a[15].y));
+}
+
 __device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
@@ -393,31 +405,43 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int ab = j % kAcc, ss = j % kScSlots;
             if (!wait_bar(B.acc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            // the whole share of the block at once: chunk c = (cg = c / 2,
-            // sub = c % 2) is 16 lanes x 32 columns; one wait, then the TMEM
-            // buffer is free for the MMAs of block j + 2
+            if (!wait_bar(B.sc_full(ss), static_cast<uint32_t>(j / kScSlots) & 1u, abort_flag)) { ok = false; break; }
+            // the block's share in two halves of 32 token columns: chunk c =
+            // (cg = c / 2, sub = c % 2) is 16 lanes x 32 columns.  The second
+            // half's TMEM loads are in flight while the first half's math
+            // runs; once they land the buffer is free for the MMAs of block j + 2
             const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) +
                                    static_cast<uint32_t>(ab * kTmemBuf + kEpiCols * hcol);
             uint32_t p[4][16];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tc_ld16x256b_x4(tbase + (static_cast<uint32_t>(16 * (c & 1)) << 16) + 32 * (c >> 1), p[c]);
+            tc_ld16x256b_x4(tbase, p[0]);
+            tc_ld16x256b_x4(tbase + (16u << 16), p[1]);
             tc_wait_ld_all();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tc_regs16(p[c]);
-            tc_fence_before();
-            arrive(B.acc_empty(ab));
-            if (!wait_bar(B.sc_full(ss), static_cast<uint32_t>(j / kScSlots) & 1u, abort_flag)) { ok = false; break; }
+            tc_regs16(p[0]);
+            tc_regs16(p[1]);
+            tc_ld16x256b_x4(tbase + 32, p[2]);
+            tc_ld16x256b_x4(tbase + (16u << 16) + 32, p[3]);
             const float *sw = reinterpret_cast<const float *>(sm + OFF_SC + ss * kScBytes);
             const float4 w4 = *reinterpret_cast<const float4 *>(sw + 32 * q + 4 * g);  // dw_slot order
             const float *sa = sw + BM + kEpiCols * hcol + 8 * m;                        // da_slot order, + 32*cg
-#pragma unroll
-            for (int cg = 0; cg < 2; ++cg) {
-                const float4 a0 = *reinterpret_cast<const float4 *>(sa + 32 * cg);
-                const float4 a1 = *reinterpret_cast<const float4 *>(sa + 32 * cg + 4);
+            {
+                const float4 a0 = *reinterpret_cast<const float4 *>(sa);
+                const float4 a1 = *reinterpret_cast<const float4 *>(sa + 4);
                 const float da[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                epi_math(acc + 8 * (2 * cg), p[2 * cg], da, w4.x, w4.y);
-                epi_math(acc + 8 * (2 * cg + 1), p[2 * cg + 1], da, w4.z, w4.w);
+                epi_math(acc, p[0], da, w4.x, w4.y);
+                epi_math(acc + 8, p[1], da, w4.z, w4.w);
+            }
+            acc_order16(acc);  // the first half's math stays ahead of the second wait
+            tc_wait_ld_all();
+            tc_regs16(p[2]);
+            tc_regs16(p[3]);
+            tc_fence_before();
+            arrive(B.acc_empty(ab));
+            {
+                const float4 a0 = *reinterpret_cast<const float4 *>(sa + 32);
+                const float4 a1 = *reinterpret_cast<const float4 *>(sa + 36);
+                const float da[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                epi_math(acc + 16, p[2], da, w4.x, w4.y);
+                epi_math(acc + 24, p[3], da, w4.z, w4.w);
             }
             arrive(B.sc_empty(ss));
         }
