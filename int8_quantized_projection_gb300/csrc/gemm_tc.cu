@@ -69,12 +69,18 @@ static_assert(128 * kRegsCtl + kEpiThreads * kRegsEpi <= 128 * kThreads, "regist
 constexpr int kATileBytes = BM * 128;              // 16384: 128 rows x 64 f16, 128B swizzle
 constexpr int kBTileBytes = BN * 128;              // 24576: 192 tokens x 64 f16, 128B swizzle
 constexpr int kStageBytes = kATileBytes + kBTileBytes;  // 40960
-constexpr int kScBytes = (BM + BN) * 4;            // 1280: d_w[128], d_a[192] as f32
+constexpr int kScBytes = (BM + BN) * 4;            // 1280: d_w[128], d_a[192] as f32, per block
+#ifndef Q8_GEMM_SC_GROUP
+#define Q8_GEMM_SC_GROUP 4
+#endif
+constexpr int kScGroup = Q8_GEMM_SC_GROUP;         // blocks whose scales share a ring slot (one wait per group)
+constexpr int kScSlotBytes = kScGroup * kScBytes;  // 5120: d_w[4][128], then d_a[4][192]
+static_assert(kScGroup >= 1 && kScGroup <= 8, "scale slots fit beside the operand stages");
 
 // shared-memory map (offsets from a 1024-byte aligned base)
 constexpr int OFF_STAGE = 0;                                    // 4 x 40960
 constexpr int OFF_SC = OFF_STAGE + kStages * kStageBytes;       // 163840
-constexpr int OFF_BAR = OFF_SC + kScSlots * kScBytes;           // 168960
+constexpr int OFF_BAR = OFF_SC + kScSlots * kScSlotBytes;       // 184320 (kScGroup = 4)
 static_assert(kStageBytes % 1024 == 0 && kATileBytes % 1024 == 0, "swizzle atoms stay aligned");
 constexpr int kNumBars = 2 * kStages + 2 * kScSlots + 2 * kAcc + kAcc;  // 22
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8 + 8;
@@ -351,19 +357,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             q8::griddep_wait();
             const float *dw_tile = dwt + (static_cast<int64_t>(blockIdx.y) * nb + j0) * BM;
             const float *da_tile = dat + (static_cast<int64_t>(blockIdx.x) * nb + j0) * BN;
+            // one slot per group of kScGroup blocks (the last group may be short)
+            const int ngr = (nbl + kScGroup - 1) / kScGroup;
             int issued = 0;
-            for (int j = 0; j < nbl && !*abort_flag; ++j) {
-                const int ss = j % kScSlots;
-                if (!wait_bar(B.sc_empty(ss), (static_cast<uint32_t>(j / kScSlots) & 1u) ^ 1u, abort_flag)) break;
+            for (int G = 0; G < ngr && !*abort_flag; ++G) {
+                const int ss = G % kScSlots;
+                if (!wait_bar(B.sc_empty(ss), (static_cast<uint32_t>(G / kScSlots) & 1u) ^ 1u, abort_flag)) break;
+                const int nbk = nbl - G * kScGroup < kScGroup ? nbl - G * kScGroup : kScGroup;
                 uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR) + 2 * kStages + ss;
-                q8::mbar_arrive_expect_tx(bar, kScBytes);
-                uint8_t *dst = sm + OFF_SC + ss * kScBytes;
-                q8::bulk_g2s(dst, dw_tile + static_cast<int64_t>(j) * BM, BM * 4, bar);
-                q8::bulk_g2s(dst + BM * 4, da_tile + static_cast<int64_t>(j) * BN, BN * 4, bar);
-                issued = j + 1;
+                q8::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbk * kScBytes));
+                uint8_t *dst = sm + OFF_SC + ss * kScSlotBytes;
+                q8::bulk_g2s(dst, dw_tile + static_cast<int64_t>(G) * kScGroup * BM, nbk * BM * 4, bar);
+                q8::bulk_g2s(dst + kScGroup * BM * 4, da_tile + static_cast<int64_t>(G) * kScGroup * BN, nbk * BN * 4,
+                             bar);
+                issued = G + 1;
             }
-            for (int j = issued - kScSlots < 0 ? 0 : issued - kScSlots; j < issued; ++j)
-                drain_bar(B.sc_full(j % kScSlots), static_cast<uint32_t>(j / kScSlots) & 1u);
+            for (int G = issued - kScSlots < 0 ? 0 : issued - kScSlots; G < issued; ++G)
+                drain_bar(B.sc_full(G % kScSlots), static_cast<uint32_t>(G / kScSlots) & 1u);
         } else if ((warp == 1 || warp == 3) && lane == 0) {
             // ------------------------------------------------------------ MMA issuers
             // Warp 1 issues the even blocks (TMEM buffer 0), warp 3 the odd
@@ -402,10 +412,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.0f, 0.0f);
         bool ok = true;
         for (int j = 0; j < nbl; ++j) {
-            const int ab = j % kAcc, ss = j % kScSlots;
+            const int ab = j % kAcc, grp = j / kScGroup, bq = j % kScGroup, ss = grp % kScSlots;
             if (!wait_bar(B.acc_full(ab), static_cast<uint32_t>(j / kAcc) & 1u, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            if (!wait_bar(B.sc_full(ss), static_cast<uint32_t>(j / kScSlots) & 1u, abort_flag)) { ok = false; break; }
+            // the scale slot of this block's group: waited for at the group's first block
+            if (bq == 0 &&
+                !wait_bar(B.sc_full(ss), static_cast<uint32_t>(grp / kScSlots) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
             // the block's share in two halves of 32 token columns: chunk c =
             // (cg = c / 2, sub = c % 2) is 16 lanes x 32 columns.  The second
             // half's TMEM loads are in flight while the first half's math
@@ -420,9 +435,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_regs16(p[1]);
             tc_ld16x256b_x4(tbase + 32, p[2]);
             tc_ld16x256b_x4(tbase + (16u << 16) + 32, p[3]);
-            const float *sw = reinterpret_cast<const float *>(sm + OFF_SC + ss * kScBytes);
-            const float4 w4 = *reinterpret_cast<const float4 *>(sw + 32 * q + 4 * g);  // dw_slot order
-            const float *sa = sw + BM + kEpiCols * hcol + 8 * m;                        // da_slot order, + 32*cg
+            const float *sw = reinterpret_cast<const float *>(sm + OFF_SC + ss * kScSlotBytes);
+            const float4 w4 = *reinterpret_cast<const float4 *>(sw + bq * BM + 32 * q + 4 * g);  // dw_slot order
+            const float *sa = sw + kScGroup * BM + bq * BN + kEpiCols * hcol + 8 * m;            // da_slot order, + 32*cg
             {
                 const float4 a0 = *reinterpret_cast<const float4 *>(sa);
                 const float4 a1 = *reinterpret_cast<const float4 *>(sa + 4);
@@ -443,7 +458,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 epi_math(acc + 16, p[2], da, w4.x, w4.y);
                 epi_math(acc + 24, p[3], da, w4.z, w4.w);
             }
-            arrive(B.sc_empty(ss));
+            if (bq == kScGroup - 1 || j == nbl - 1) arrive(B.sc_empty(ss));  // the group's last block
         }
         if (ok && !*abort_flag) {
 #pragma unroll
