@@ -602,14 +602,18 @@ gemv_generic_kernel(const uint8_t *__restrict__ w, int64_t n, int nb, const int8
 // contiguous in memory, so a stage reads kSbPieces*272 consecutive bytes per
 // row).  One thread of a ninth warp moves each stage with three TMA loads:
 // the weights (one 3-D box: rows x pieces x 272 bytes), the tokens' code
-// bytes (128-byte boxes, 128-byte swizzled so the consumer warps' fragment
-// reads spread over the banks) and their d|ssum words; rows past n and
-// tokens past t arrive as zeros.  Consumer warp w takes 16 rows (tile
-// w % (kSbRows/16)) and one piece (w / (kSbRows/16)) of every stage.  The
+// bytes (128-byte boxes, 128-byte swizzled so fragment reads spread over the
+// banks) and their d|ssum words; rows past n and tokens past t arrive as
+// zeros.  Consumer warp w takes 16 rows (tile w % (kSbRows/16)) and one piece
+// (w / (kSbRows/16)) of every stage.  For more than 8 tokens the consumer
+// warps first widen the stage's activation codes to f16 together, in the
+// order of the MMA's B fragments, and unpack its scales (sb_prep_act).  The
 // CTAs of a thread-block cluster (1..8) split k between them, so narrow
-// matrices still fill the GPU.  Partial sums are added in piece order inside
-// a CTA, then in cluster-rank order by rank 0, which reads its peers' shared
-// memory: results are run-to-run identical.
+// matrices still fill the GPU; one launch may cover several projections of
+// the same activation (their row tiles form one grid).  Partial sums are
+// added in piece order inside a CTA, then in cluster-rank order (every CTA
+// finishes a share of the outputs, reading its peers' shared memory):
+// results are run-to-run identical.
 // ---------------------------------------------------------------------------
 #ifndef Q8_SB_PIECES
 #define Q8_SB_PIECES 1
