@@ -29,13 +29,15 @@
 // queues little ahead of the thread issuing to it, so each TMEM buffer has
 // its own issuing thread.  A TMEM load takes ~130 cycles to land and
 // tcgen05.wait::ld waits for all of a thread's loads, so each epilogue thread
-// loads its whole share of a block (64 values) at once and waits once, frees
-// the buffer, then scales and accumulates; three warps per TMEM lane quarter
-// keep the f32 pipe busy meanwhile.
+// reads its share of a block (64 values) in two halves: the first half's
+// loads and wait, then the second half's loads in flight while the first
+// half is scaled and accumulated, then the buffer is freed and the second
+// half's math follows; three warps per TMEM lane quarter keep the f32 pipe
+// busy meanwhile.
 // Warp roles (512 threads; setmaxnreg moves registers to the epilogue):
 //   warp 0      TMA producer: the weight and activation tiles of 2 blocks
 //   warp 1      TMEM allocator; MMA issuer (one thread) for the even blocks
-//   warp 2      bulk-copy producer: each block's d_w and d_a into a ring
+//   warp 2      bulk-copy producer: the d_w and d_a of 4 blocks per ring slot
 //   warp 3      MMA issuer (one thread) for the odd blocks
 //   warps 4-15  epilogue: three warps per TMEM lane quarter, 64 tokens each,
 //               read in the 16x256b shape (4 rows x 16 tokens per thread and
