@@ -330,6 +330,23 @@ Q8_API int q4a_gemv_batched(const void *w, int64_t n, int64_t k,
                             float *y, void *stream);
 
 /*
+ * q4a_gemv_batched_grouped -- q4a_gemv_batched for up to Q8_MAX_GROUP
+ * projections of the same plane rows, as q8_0_gemv_batched_grouped is for
+ * Q8_0 weights: projs[i].w holds projs[i].n rows of the 20-byte asymmetric
+ * blocks, projs[i].y is f32 [tokens][projs[i].n]; k % 256 == 0, 1 <= tokens
+ * <= Q8_GEMV_MAX_TOKENS.  For tokens >= 2 the projections' row tiles form one
+ * launch of the small-batch kernel (per block the arithmetic of
+ * q4a_gemv_batched; the number of CTAs splitting k follows the launch's total
+ * tile count, so partial sums may be grouped differently than in a single
+ * call, bit for bit equal where that number is the same); tokens == 1 runs
+ * q4a_gemv projection by projection.  Errors as q4a_gemv_batched, plus
+ * Q8_ERR_ARG for count outside 1..Q8_MAX_GROUP or a NULL descriptor.
+ */
+Q8_API int q4a_gemv_batched_grouped(const q8_gemv_proj *projs, int count, int64_t k,
+                                    const int8_t *qs, const uint32_t *ds, int64_t tokens,
+                                    void *stream);
+
+/*
  * q8_0_gemm_workspace_bytes -- device workspace q8_0_gemm needs for n weight
  * rows, t tokens and width k: the weight codes as f16 (n*k*2 bytes), the
  * activation codes as f16 (t*k*2), and both sides' block scales as f32

@@ -33,6 +33,7 @@ from ._binding import (  # noqa: F401
     PRODUCER_SWIGLU,
     q4a_gemv,
     q4a_gemv_batched,
+    q4a_gemv_batched_grouped,
     GEMV_MAX_TOKENS,
     q8_check,
     q8_num_sms,

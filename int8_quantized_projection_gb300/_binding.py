@@ -47,6 +47,7 @@ SIGNATURES = {
     "q8_0_gemv_batched_grouped": (_INT, [_P, _INT, _I64, _P, _P, _I64, _P]),
     "q4a_gemv": (_INT, [_P, _I64, _I64, _P, _P, _P, _P]),
     "q4a_gemv_batched": (_INT, [_P, _I64, _I64, _P, _P, _I64, _P, _P]),
+    "q4a_gemv_batched_grouped": (_INT, [_P, _INT, _I64, _P, _P, _I64, _P]),
     "q8_check": (_INT, [_P]),
     "q8_num_sms": (_INT, []),
 }
@@ -270,6 +271,32 @@ def q4a_gemv_batched(w, n: int, k: int, qs, ds, t: int, y, stream=None, bind=Fal
     if w.numel() != n * (k // 32) * 20 or y.numel() < t * n or qs.shape[-1] != k or qs.shape[0] < t:
         raise ValueError("shape mismatch")
     return _launch("q4a_gemv_batched", (_ptr(w), n, k, _ptr(qs), _ptr(ds), t, _ptr(y), _stream(stream)), bind)
+
+
+def q4a_gemv_batched_grouped(projs, k: int, qs, ds, t: int, stream=None, bind=False):
+    """Several asymmetric 4-bit small-batch projections of the same plane rows [0, t) in one launch.
+
+    ``projs`` is a sequence of (w uint8 20-byte blocks, n, y f32 [t][n]) sharing k."""
+    import torch
+
+    _need(qs, torch.int8, "qs"), _need(ds, torch.int32, "ds")
+    if not 1 <= len(projs) <= MAX_GROUP or qs.shape[-1] != k or qs.shape[0] < t:
+        raise ValueError("1..8 projections sharing k and the plane")
+    arr = (GemvProj * len(projs))()
+    keep = []
+    for i, (w, n, y) in enumerate(projs):
+        _need(w, torch.uint8, "w"), _need(y, torch.float32, "y")
+        if w.numel() != n * (k // 32) * 20 or y.numel() < t * n:
+            raise ValueError("shape mismatch")
+        arr[i] = GemvProj(w.data_ptr(), n, y.data_ptr())
+        keep.append((w, y))
+    args = (ctypes.cast(arr, ctypes.c_void_p), len(projs), k, _ptr(qs), _ptr(ds), t, _stream(stream))
+    if bind:
+        b = Bound("q4a_gemv_batched_grouped", args)
+        b._keep = (arr, keep)  # the descriptor array must outlive the bound launch
+        return b
+    _check("q4a_gemv_batched_grouped", lib().q4a_gemv_batched_grouped(*args))
+    return None
 
 
 def q8_0_gemv_grouped(projs, k: int, qs, ds, stream=None, bind=False):

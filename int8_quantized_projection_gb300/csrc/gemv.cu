@@ -1254,6 +1254,12 @@ int gemv_small_q4a_launch(const void *w, int64_t n, int64_t k, const int8_t *qs,
     return gemv_small_launch_t<SbQ4A>(&p, 1, k, qs, ds, tokens, s, 7, 8);
 }
 
+int gemv_small_q4a_grouped_launch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs,
+                                  const uint32_t *ds, int64_t tokens, cudaStream_t s)
+{
+    return gemv_small_launch_t<SbQ4A>(projs, count, k, qs, ds, tokens, s, 7, 8);
+}
+
 } // namespace q8
 
 namespace {

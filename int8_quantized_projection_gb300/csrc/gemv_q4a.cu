@@ -159,3 +159,25 @@ extern "C" int q4a_gemv_batched(const void *w, int64_t n, int64_t k, const int8_
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     return q8::gemv_small_q4a_launch(w, n, k, qs, ds, y, tokens, static_cast<cudaStream_t>(stream));
 }
+
+extern "C" int q4a_gemv_batched_grouped(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs,
+                                        const uint32_t *ds, int64_t tokens, void *stream)
+{
+    if (!projs || count < 1 || count > Q8_MAX_GROUP || !qs || !ds || k <= 0 || (k % 256) != 0 || tokens < 1 ||
+        tokens > Q8_GEMV_MAX_TOKENS)
+        return Q8_ERR_ARG;
+    for (int i = 0; i < count; ++i)
+        if (!projs[i].w || !projs[i].y || projs[i].n < 1 || projs[i].n > (int64_t(1) << 40)) return Q8_ERR_ARG;
+    if (!q8::aligned16(qs) || !q8::aligned16(ds)) return Q8_ERR_ALIGN;
+    for (int i = 0; i < count; ++i)
+        if (!q8::aligned16(projs[i].w) || !q8::aligned16(projs[i].y)) return Q8_ERR_ALIGN;
+    if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
+    if (tokens == 1) {  // one token: the batch-1 kernel, projection by projection (as q4a_gemv_batched)
+        for (int i = 0; i < count; ++i) {
+            const int st = q4a_gemv(projs[i].w, projs[i].n, k, qs, ds, projs[i].y, stream);
+            if (st != Q8_OK) return st;
+        }
+        return Q8_OK;
+    }
+    return q8::gemv_small_q4a_grouped_launch(projs, count, k, qs, ds, tokens, static_cast<cudaStream_t>(stream));
+}

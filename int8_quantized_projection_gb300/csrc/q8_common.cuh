@@ -115,6 +115,8 @@ int gemv_sliced_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, co
 // small-batch kernel (gemv.cu) for asymmetric 4-bit blocks: 1 <= tokens <= 16, (k/32) % 8 == 0
 int gemv_small_q4a_launch(const void *w, int64_t n, int64_t k, const int8_t *qs, const uint32_t *ds, float *y,
                           int64_t tokens, cudaStream_t s);
+int gemv_small_q4a_grouped_launch(const q8_gemv_proj *projs, int count, int64_t k, const int8_t *qs,
+                                  const uint32_t *ds, int64_t tokens, cudaStream_t s);
 // staged batch-1 kernel (gemv.cu) for asymmetric 4-bit blocks: k % 128 == 0,
 // k / 128 <= kGemvStagedMaxChunks (the activation is staged in shared memory)
 constexpr int kGemvStagedMaxChunks = 512;

@@ -142,6 +142,21 @@ def test_argument_errors_are_reported_before_any_device_work(lib):
     assert lib.q4a_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 17, P(FAKE), s) == ERR_ARG
     assert lib.q4a_gemv_batched(P(0), 8, 256, P(FAKE), P(FAKE), 4, P(FAKE), s) == ERR_ARG
     assert lib.q4a_gemv_batched(P(FAKE), 8, 256, P(FAKE), P(FAKE), 4, P(MISALIGNED), s) == ERR_ALIGN
+    # q4a_gemv_batched_grouped: count 1..8, k % 256, tokens 1..16, descriptors, alignment
+    qgrp = (_binding.GemvProj * 2)(_binding.GemvProj(FAKE, 8, FAKE), _binding.GemvProj(FAKE, 40, FAKE))
+    qp = ctypes.cast(qgrp, ctypes.c_void_p)
+    qb = lib.q4a_gemv_batched_grouped
+    assert qb(None, 1, 256, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert qb(qp, 0, 256, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert qb(qp, 9, 256, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert qb(qp, 2, 128, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    assert qb(qp, 2, 256, P(FAKE), P(FAKE), 0, s) == ERR_ARG
+    assert qb(qp, 2, 256, P(FAKE), P(FAKE), 17, s) == ERR_ARG
+    assert qb(qp, 2, 256, P(FAKE), P(MISALIGNED), 4, s) == ERR_ALIGN
+    qgrp[1] = _binding.GemvProj(FAKE, 0, FAKE)
+    assert qb(qp, 2, 256, P(FAKE), P(FAKE), 4, s) == ERR_ARG
+    qgrp[1] = _binding.GemvProj(MISALIGNED, 40, FAKE)
+    assert qb(qp, 2, 256, P(FAKE), P(FAKE), 4, s) == ERR_ALIGN
     # q8_0_gemv_fused: producer code, its inputs, the staged path's k, RMSNorm's row limit, alignment
     one = (_binding.GemvProj * 1)(_binding.GemvProj(FAKE, 8, FAKE))
     pr = ctypes.cast(one, ctypes.c_void_p)

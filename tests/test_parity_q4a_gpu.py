@@ -215,3 +215,52 @@ def test_q4a_gemv_batched_deterministic(q8):
         q8.q8_check()
         outs.append(y.clone())
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+# ---------------------------------------------------------------------------
+# q4a_gemv_batched_grouped: several projections of the same plane rows in one
+# launch (the small-batch kernel over their joined row tiles; one token: the
+# batch-1 kernel projection by projection)
+# ---------------------------------------------------------------------------
+def _run_grouped(q8, k, blobs, ns, qs, ds, t):
+    ys = [nan_f32(t, n) for n in ns]
+    q8.q4a_gemv_batched_grouped([(dev(b), n, y) for b, n, y in zip(blobs, ns, ys)], k, dev(qs),
+                                dev(ds.view(np.int32)), t)
+    q8.q8_check()
+    return ys
+
+
+@pytest.mark.parametrize("k,ns,t", [(3584, (3584, 512, 512), 16), (1024, (37, 1000, 300), 5),
+                                    (2048, (129, 64, 700, 1, 256, 96, 33, 512), 12), (512, (300, 77), 1)])
+def test_q4a_gemv_batched_grouped_matches_oracle(q8, k, ns, t):
+    import torch
+
+    blobs = [_weights(50 + i, n, k) for i, n in enumerate(ns)]
+    qs, ds = _plane_t(50, t, k)
+    ys = _run_grouped(q8, k, blobs, ns, qs, ds, t)
+    for i, (blob, n, y) in enumerate(zip(blobs, ns, ys)):
+        assert not torch.isnan(y).any().item(), f"projection {i}: unwritten outputs"
+        yr, ar = oracle.q4a_gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+        assert_gemm_close(host(y), yr, ar, f"q4a grouped {i}: {n}x{k} t={t}")
+
+
+def test_q4a_gemv_batched_grouped_exact_epilogue_bit_equal(q8):
+    k, ns, t = 2048, (300, 64, 129), 9
+    blobs = [_weights(60 + i, n, k, exact=True) for i, n in enumerate(ns)]
+    qs, ds = _plane_t(60, t, k, exact=True)
+    ys = _run_grouped(q8, k, blobs, ns, qs, ds, t)
+    for blob, n, y in zip(blobs, ns, ys):
+        yr, _ = oracle.q4a_gemm(blob, n, k, qs, ds, t_idx=np.arange(t))
+        assert np.array_equal(host(y).astype(np.float64), yr)
+
+
+@pytest.mark.parametrize("t", [1, 6, 16])
+def test_q4a_group_of_one_is_the_single_call(q8, t):
+    import torch
+
+    n, k = 1000, 2048
+    blob = _weights(70, n, k)
+    qs, ds = _plane_t(70, t, k)
+    (y_grp,) = _run_grouped(q8, k, [blob], [n], qs, ds, t)
+    y_one = _run_batched(q8, blob, n, k, qs, ds, t)
+    assert torch.equal(y_grp, y_one)
