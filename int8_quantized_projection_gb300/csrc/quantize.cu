@@ -467,16 +467,19 @@ extern "C" int quantize_q8_0(const float *x, int64_t rows, int64_t k, int8_t *qs
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     const int sms = q8::device_sm_count();
     const int nsm = sms > 0 ? sms : 152;
-    const int ng = k <= kGrpMaxD ? rowgroup_groups(static_cast<int>(k), false) : 0;
+    // two CTAs per SM, each with half the groups that fit: an SM takes the next
+    // launch's first CTA as soon as one of them ends (the norm kernel keeps one
+    // CTA per SM: a second copy of its weight vector costs more than that gains)
+    const int ng = k <= kGrpMaxD ? rowgroup_groups(static_cast<int>(k), false) / 2 : 0;
     if (rows_pad > nsm && ng >= 2 && rows < (int64_t(1) << 31)) {
-        // many rows: row groups streaming the rows through shared memory, one CTA per SM
+        // many rows: row groups streaming the rows through shared memory
         const size_t smem = rowgroup_smem(static_cast<int>(k), false, ng);
         CUtensorMap mx{};
         if (rows > 0 && !rowgroup_x_map(&mx, x, rows, static_cast<int>(k))) return Q8_ERR_LAUNCH;
         if (!q8::set_max_dynamic_smem(reinterpret_cast<const void *>(quantize_q8_0_rowgroup_kernel),
                                       static_cast<int>(smem), 13))
             return Q8_ERR_LAUNCH;
-        return q8::launch_pdl(quantize_q8_0_rowgroup_kernel, dim3(static_cast<unsigned>(nsm)),
+        return q8::launch_pdl(quantize_q8_0_rowgroup_kernel, dim3(static_cast<unsigned>(2 * nsm)),
                               dim3(kGrpThreads * ng), smem, static_cast<cudaStream_t>(stream), mx, rows, rows_pad,
                               static_cast<int>(k), reinterpret_cast<uint32_t *>(qs), ds);
     }
