@@ -621,14 +621,33 @@ gemm_prep_a_kernel(const uint4 *__restrict__ qs, const uint32_t *__restrict__ ds
     }
 }
 
+constexpr int kSplitSms = 152, kMaxSplits = 12, kMaxSplitsMany = 4;  // split-K bounds (see gemm_splits)
+
 // Split-K: y = sum over z of part[z], added in z order (deterministic).
 __global__ void __launch_bounds__(256)
 gemm_split_reduce_kernel(const float *__restrict__ part, int splits, int64_t count, float *__restrict__ y)
 {
     q8::griddep_launch_dependents();
     q8::griddep_wait();  // the partial tiles come from the GEMM just before
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (count % 4 == 0) {  // four outputs per thread: 16-byte loads and stores (part and y are 16-byte aligned)
+        const int64_t c4 = count / 4;
+        const float4 *p4 = reinterpret_cast<const float4 *>(part);
+        for (int64_t i = i0; i < c4; i += stride) {
+            float4 pz[kMaxSplits];  // every split's loads in flight before the adds
+#pragma unroll
+            for (int z = 0; z < kMaxSplits; ++z)
+                if (z < splits) pz[z] = __ldg(p4 + static_cast<int64_t>(z) * c4 + i);
+            float4 v = pz[0];
+#pragma unroll
+            for (int z = 1; z < kMaxSplits; ++z)
+                if (z < splits) v.x += pz[z].x, v.y += pz[z].y, v.z += pz[z].z, v.w += pz[z].w;
+            reinterpret_cast<float4 *>(y)[i] = v;
+        }
+        return;
+    }
+    for (int64_t i = i0; i < count; i += stride) {
         float v = part[i];
         for (int z = 1; z < splits; ++z) v += part[static_cast<int64_t>(z) * count + i];
         y[i] = v;
@@ -648,7 +667,6 @@ gemm_split_reduce_kernel(const float *__restrict__ part, int splits, int64_t cou
 // size is a function of the shape alone; the first rule keeps splits * tiles
 // at most that count, which bounds its partial tiles by about 15 MB, and the
 // second allows at most 4 splits.
-constexpr int kSplitSms = 152, kMaxSplits = 12, kMaxSplitsMany = 4;
 constexpr double kStageUs = 0.886;        // one stage (two blocks) of one CTA
 constexpr double kCtaFixedUs = 4.0;       // a CTA's pipeline ramp and output store
 constexpr double kPartialBytesPerUs = 6.5e6;  // partial tiles written and read back at about HBM rate
@@ -770,7 +788,7 @@ int gemm_tc_core(const uint8_t *a16, const float *dwt, int64_t n, int64_t k, con
                         static_cast<int>(nb), y, part);
     if (st != Q8_OK) return st;
     const int64_t count = t * n;
-    int64_t rgrid = (count + 255) / 256;
+    int64_t rgrid = (count % 4 == 0 ? count / 4 + 255 : count + 255) / 256;
     rgrid = rgrid < pcap ? rgrid : pcap;
     return q8::launch_pdl(gemm_split_reduce_kernel, dim3(static_cast<unsigned>(rgrid)), dim3(256), 0, s,
                           static_cast<const float *>(part), splits, count, y);
