@@ -411,7 +411,7 @@ swiglu_quant_kernel(const float4 *__restrict__ g, const float4 *__restrict__ u, 
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    constexpr int U = 2;
+    constexpr int U = 4;  // float4 pairs in flight per lane (2: 104 us at 3325 x 18944, 4: 91 us, 8 spills)
     for (int64_t base = warp * 32 * U; base < n4_total; base += nwarps * 32 * U) {
         float4 gv[U], uv[U];
 #pragma unroll
@@ -546,7 +546,7 @@ extern "C" int swiglu_quant(const float *gate, const float *up, float *y, int64_
     if (rows > 0 && (!q8::aligned16(gate) || !q8::aligned16(up) || (y && !q8::aligned16(y)))) return Q8_ERR_ALIGN;
     if (!q8::device_is_sm103()) return Q8_ERR_DEVICE;
     const int64_t n4_valid = rows * nf / 4, n4_total = rows_pad * nf / 4;
-    return q8::launch_pdl(swiglu_quant_kernel, dim3(flat_grid(n4_total, 2)), dim3(kQuantThreads), 0,
+    return q8::launch_pdl(swiglu_quant_kernel, dim3(flat_grid(n4_total, 4)), dim3(kQuantThreads), 0,
                           static_cast<cudaStream_t>(stream), reinterpret_cast<const float4 *>(gate),
                           reinterpret_cast<const float4 *>(up), reinterpret_cast<float4 *>(y), n4_valid, n4_total,
                           reinterpret_cast<uint32_t *>(qs), ds);
