@@ -358,14 +358,15 @@ def run_decode(torch, q8p, steps, warmup, dev, sampler):
     # A serving loop records its step once -- the host-to-device copy of the
     # inputs from pinned memory, the library calls, the device-to-host copy of
     # the outputs -- as a CUDA graph and replays it every step.  Independent
-    # requests let it keep several steps in flight: consecutive steps use two
-    # sets of device buffers on two streams, so one step's copies overlap the
-    # other's kernels, and the host enqueues step i, then waits for step i-3
-    # and reads its outputs; the four host buffers rotate, so a step never
-    # writes the buffer the host is reading (`e2e_s`).  `e2e_serial_s` waits
+    # requests let it keep several steps in flight: consecutive steps use three
+    # sets of device buffers on three streams, so one step's copies and its
+    # launch's ramp and tail overlap the other steps' kernels, and the host
+    # enqueues step i, then waits for step i-5 and reads its outputs; the six
+    # host buffers rotate, so a step never writes the buffer the host is
+    # reading (`e2e_s`).  `e2e_serial_s` waits
     # for every step before enqueuing the next (one buffer set);
     # `e2e_eager_s` also issues the step call by call.
-    nbuf, nsets = 4, 2
+    nbuf, nsets = 6, 3
     xh = [x_all.cpu().pin_memory() for _ in range(nbuf)]
     yh = [torch.empty(y_all.shape, dtype=torch.float32).pin_memory() for _ in range(nbuf)]
 
@@ -1500,9 +1501,11 @@ def main():
             "e2e": {"value": round(world * step_bytes * args.steps / dec["e2e_s"] / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"],
                     "launch": "per step: one CUDA graph replay (pinned-memory copy in, the library calls, copy out; "
-                              "recorded once); consecutive steps on two device buffer sets and streams (one step's "
-                              "copies overlap the other's kernels); up to three steps in flight: the host reads step "
-                              "i-3's outputs after enqueuing step i (four host buffers rotate)",
+                              "recorded once); consecutive steps on three device buffer sets and streams, so "
+                              "independent steps overlap on the device (one step's copies and its launch's ramp and "
+                              "tail under the others' kernels: this can exceed `value`, whose steps run one after "
+                              "another on one stream); up to five steps in flight: the host reads step i-5's outputs "
+                              "after enqueuing step i (six host buffers rotate)",
                     "steps_timed": dec["e2e_steps"],
                     "serial_value": round(world * step_bytes * args.steps / dec["e2e_serial_s"] / 1e9, 2),
                     "eager_value": round(world * step_bytes * args.steps / dec["e2e_eager_s"] / 1e9, 2)},
