@@ -166,9 +166,15 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
 // slot waits on, so the other warps go on to the next row).  Thread b of a
 // group owns the row's 32-element block b whole: its amax and code sum are
 // register reductions and its d and 1/d are computed once, so the encoder
-// costs a fraction of the per-lane (8 lanes per block) form.  Per row: each thread sums the squares of its block,
-// the warps reduce by xor shuffles and their four sums are added in warp
-// order; then scale, write y (mode 1) and encode.
+// costs a fraction of the per-lane (8 lanes per block) form.  Per row: each
+// thread sums the squares of its block (two partial sums, even and odd
+// elements), the warps reduce by xor shuffles and their four sums are added
+// in warp order; then scale, write y (mode 1) and encode.  The kernel is
+// bound by instruction issue rather than by DRAM, so the arithmetic runs two
+// elements per instruction where it can (packed f32x2 sums of squares,
+// scaling and code products, three-input maxima) and the codes are rounded
+// by an add on the FMA pipe instead of one conversion per element; every
+// element still takes the same roundings as the scalar form.
 //
 // A row is loaded as a 3-D tensor box [1 row][d/32 blocks][32 floats] with
 // the 128-byte swizzle: block b's 16-byte chunk c lands at chunk c ^ (b mod 8)
@@ -182,6 +188,7 @@ rmsnorm_quant_kernel(const float *__restrict__ x, const float *__restrict__ w, f
 constexpr int kGrpThreads = 128;     // four warps per row, one block per thread
 constexpr int kGrpSlots = 2;         // row slots per group
 constexpr int kGrpMax = 8;           // groups per CTA (1024 threads)
+constexpr int kGrpMaxNorm = 6;       // RMSNorm groups per CTA (768 threads: up to 80 registers a thread)
 constexpr int kGrpSmemBudget = 200 * 1024;  // weight vector + every group's slots
 constexpr int kGrpMaxD = 32 * kGrpThreads;  // 4096: one block per thread
 
@@ -207,6 +214,43 @@ size_t rowgroup_smem(int d, bool norm, int groups)
 __device__ __forceinline__ void group_sync(int id)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kGrpThreads) : "memory");
+}
+
+// Maximum of three floats in one instruction (the three-input max.f32 of
+// the sm_100 family).
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Codes rounded on the FMA pipe.  p = fma(x, 1/d, +0) is the f32 product
+// rounded once (IEEE: adding +0 changes no non-zero result, and a compiler
+// may not drop it, since it turns a -0 product into +0), and p + 1.5 * 2^23
+// rounded to f32 is rint(p), ties to even, for |p| < 2^22: the sum lies
+// where the f32 spacing is 1.  Its bits are 0x4B400000 + rint(p): the low
+// byte is the code and the wrapped sum of the bits gives the code sum.
+// Because p comes from an FMA, the add cannot be fused with the multiply
+// (which would round the exact product instead: another code where p is
+// exactly k + 0.5).
+constexpr float kRoundMagic = 12582912.0f;
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
+
+__device__ __forceinline__ void round_by_add2(float a, float b, float di, uint32_t &ba, uint32_t &bb)
+{
+    const float2 p = __ffma2_rn(make_float2(a, b), make_float2(di, di), make_float2(0.0f, 0.0f));
+    const float2 r = __fadd2_rn(p, make_float2(kRoundMagic, kRoundMagic));
+    ba = __float_as_uint(r.x);
+    bb = __float_as_uint(r.y);
+}
+
+// Whether a block's codes may be rounded by the add: d is 0 (every product
+// is +-0) or a normal finite float (every |p| < 127.5, as for the unclamped
+// codes).  A subnormal or non-finite d takes the clamped codes.
+__device__ __forceinline__ bool block_rounds_by_add(float d)
+{
+    return d == 0.0f || (d >= 1.17549435e-38f && d <= 3.40282347e+38f);
 }
 
 // The body shared by RMSNorm + quantize (kNorm) and the plain quantizer
@@ -299,9 +343,15 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
 #pragma unroll
         for (int k = 0; k < 8; ++k) v[k] = (got && mine_blk) ? xb[k ^ sw] : make_float4(0.f, 0.f, 0.f, 0.f);
         if (kNorm) {
+            // two partial sums (even and odd elements), one packed FMA per pair
+            float2 s2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) ss = q8::rms_sumsq4(ss, v[k]);
-            ss = q8::rms_warp_sum(ss);
+            for (int k = 0; k < 8; ++k) {
+                const float2 lo = make_float2(v[k].x, v[k].y), hi = make_float2(v[k].z, v[k].w);
+                s2 = __ffma2_rn(lo, lo, s2);
+                s2 = __ffma2_rn(hi, hi, s2);
+            }
+            ss = q8::rms_warp_sum(s2.x + s2.y);
         }
         const int rb = static_cast<int>(i & 1);  // alternate buffers: one exchange barrier per row suffices
         const bool all_got = __all_sync(Q8_FULL_MASK, got);
@@ -326,29 +376,45 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
             if (kNorm) {
                 const float scale = q8::rms_scale(tot, d, eps);
                 const float4 *wb = wsm + 8 * gt;
+                const float2 sc2 = make_float2(scale, scale);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = q8::rms_apply4(v[k], scale, wb[k ^ sw]);
+                for (int k = 0; k < 8; ++k) {  // (x * scale) * w, two roundings per element, two elements per op
+                    const float4 wv = wb[k ^ sw];
+                    const float2 lo = __fmul2_rn(__fmul2_rn(make_float2(v[k].x, v[k].y), sc2), make_float2(wv.x, wv.y));
+                    const float2 hi = __fmul2_rn(__fmul2_rn(make_float2(v[k].z, v[k].w), sc2), make_float2(wv.z, wv.w));
+                    v[k] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                }
                 if (y) {  // mode 2 (y == NULL): only the plane is written
                     float4 *yb = reinterpret_cast<float4 *>(y + t * static_cast<int64_t>(d)) + 8 * gt;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) yb[k] = v[k];
                 }
             }
+            {
+                float m[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+                for (int k = 0; k < 8; ++k) {
+                    m[k] = max3f(fabsf(v[k].x), fabsf(v[k].y), fabsf(v[k].z));
+                    m[k] = fmaxf(m[k], fabsf(v[k].w));
+                }
+                amax = max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+            }
             const float dq = q8::q8_block_d(amax);
             const float di = q8::q8_block_di(dq);
             uint32_t qw[8];
             int sum = 0;
-            if (!q8::q8_block_needs_clamp(dq)) {
+            if (block_rounds_by_add(dq)) {
+                uint32_t bsum = 0u;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const int c0 = q8::q8_code_unclamped(v[k].x, di), c1 = q8::q8_code_unclamped(v[k].y, di);
-                    const int c2 = q8::q8_code_unclamped(v[k].z, di), c3 = q8::q8_code_unclamped(v[k].w, di);
-                    sum += c0 + c1 + c2 + c3;
-                    qw[k] = q8::pack4(c0, c1, c2, c3);
+                    uint32_t b0, b1, b2, b3;
+                    round_by_add2(v[k].x, v[k].y, di, b0, b1);
+                    round_by_add2(v[k].z, v[k].w, di, b2, b3);
+                    bsum += b0 + b1 + b2 + b3;
+                    qw[k] = q8::pack4(static_cast<int>(b0), static_cast<int>(b1), static_cast<int>(b2),
+                                      static_cast<int>(b3));
                 }
+                sum = static_cast<int>(bsum - 32u * kRoundMagicBits);
             } else {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -374,7 +440,7 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
                                             Q8_DRAIN_LIMIT_NS);
 }
 
-__global__ void __launch_bounds__(kGrpThreads * kGrpMax, 1)
+__global__ void __launch_bounds__(kGrpThreads * kGrpMaxNorm, 1)
 rmsnorm_quant_rowgroup_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restrict__ w, float eps,
                               float *__restrict__ y, int64_t rows, int64_t rows_pad, int d,
                               uint32_t *__restrict__ qs, uint32_t *__restrict__ ds)
@@ -504,7 +570,7 @@ extern "C" int rmsnorm_quant(const float *x, const float *w, float eps, float *y
     const int nsm = sms > 0 ? sms : 152;
     uint32_t *q32 = reinterpret_cast<uint32_t *>(qs);
     const int di = static_cast<int>(d);
-    const int ng = rowgroup_groups(di, true);
+    const int ng = rowgroup_groups(di, true) < kGrpMaxNorm ? rowgroup_groups(di, true) : kGrpMaxNorm;
     if (rows_pad > nsm && d <= kGrpMaxD && ng >= 2 && rows < (int64_t(1) << 31)) {
         // many rows: row groups streaming their rows through shared memory, one CTA per SM
         const size_t smem = rowgroup_smem(di, true, ng);

@@ -106,6 +106,68 @@ def test_rmsnorm_quant_subnormal_outputs(q8, rows, d, rows_pad):
     assert_plane_equal(qs, ds, qr, dr, f"rmsnorm subnormal plane {rows}x{d}")
 
 
+def _tie_set(amax, g):
+    """31 values below amax whose products with the block's 1/d round, in
+    f32, to exactly k + 0.5 while the exact product is not k + 0.5: the code
+    is rint of the rounded product (ties to even), and a kernel that formed
+    the product and its rounding as one fused operation would get the other
+    neighbour for about half of them."""
+    d = np.float32(np.float32(amax) / np.float32(127))
+    di = np.float32(np.float32(1) / d)
+    out = []
+    for k in g.permutation(np.arange(-126, 126)):
+        v0 = np.float32((k + 0.5) / float(di))
+        up = dn = v0
+        cand = [v0]
+        for _ in range(40):
+            up = np.nextafter(up, np.float32(np.inf))
+            dn = np.nextafter(dn, np.float32(-np.inf))
+            cand += [up, dn]
+        for v in cand:
+            if (float(np.float32(v * di)) == k + 0.5 and float(v) * float(di) != k + 0.5
+                    and abs(float(v)) < amax):
+                out.append(v)
+                break
+        if len(out) == 31:
+            return np.array(out, np.float32)
+    raise AssertionError("too few tie values")
+
+
+def _tie_rows(rows, k):
+    g = syn.rng(55, rows, k)
+    amaxes = (1.0, 3.7, 0.013, 250.0, 0.5, 17.25)
+    sets = [_tie_set(a, g) for a in amaxes]
+    nb = rows * k // 32
+    pick = g.integers(0, len(amaxes), size=nb)
+    blocks = np.empty((nb, 32), np.float32)
+    for j, a in enumerate(amaxes):
+        sel = np.flatnonzero(pick == j)
+        vals = np.concatenate([np.full((len(sel), 1), a, np.float32), np.tile(sets[j], (len(sel), 1))], axis=1)
+        vals *= np.where(g.integers(0, 2, size=vals.shape) == 0, -1.0, 1.0).astype(np.float32)
+        blocks[sel] = np.take_along_axis(vals, g.permuted(np.tile(np.arange(32), (len(sel), 1)), axis=1), axis=1)
+    return blocks.reshape(rows, k)
+
+
+@pytest.mark.parametrize("rows,k,rows_pad", [(2, 640, 2), (300, 640, 384), (3325, 3584, 3328), (200, 8192, 256)])
+def test_quantize_q8_0_product_ties(q8, rows, k, rows_pad):
+    """Every block holds its amax and 31 elements whose f32 product with 1/d
+    lands exactly on k + 0.5 ("54 - r51 - producer-fused A-quantize mode 1",
+    sec. 3.2: the code is rint of x times the f32 reciprocal of d, ties to
+    even), on the one-row, row-group and flat kernels."""
+    x = _tie_rows(rows, k)
+    b = x.reshape(-1, 32)
+    d = (np.abs(b).max(axis=1) / np.float32(127)).astype(np.float32)
+    di = (np.float32(1) / d).astype(np.float32)
+    p = (b * di[:, None]).astype(np.float32)
+    split = np.rint(p) != np.rint(b.astype(np.float64) * di[:, None].astype(np.float64))
+    assert split.sum() > len(b)  # the data reaches the case, more than once per block on average
+    qs, ds = poisoned_plane(rows_pad, k)
+    q8.quantize_q8_0(dev(x), qs, ds)
+    q8.q8_check()
+    qr, dr = oracle.quantize(x, rows_pad)
+    assert_plane_equal(qs, ds, qr, dr, f"quantize product ties {rows}x{k}")
+
+
 def test_quantize_q8_0_zero_rows_only_fills_tail(q8):
     import torch
 
