@@ -297,9 +297,11 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
     __syncthreads();
     q8::griddep_wait();  // x may come from the previous kernel
 
-    // this group's rows: t = g0 + i * stride; rows at or past `rows` (the zero
-    // tail, all at the end) are not loaded
-    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * ngroups + grp;
+    // this group's rows: t = g0 + i * stride, dealt round-robin over the CTAs
+    // first (row t to CTA t mod the grid), so every SM gets the same number
+    // of rows to within one; rows at or past `rows` (the zero tail, all at
+    // the end) are not loaded
+    const int64_t g0 = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(grp) * gridDim.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * ngroups;
     const int64_t mine = g0 < rows_pad ? (rows_pad - g0 + stride - 1) / stride : 0;
     int64_t issued = 0;  // thread gt == 0: rows whose load has been issued (or that need none)
