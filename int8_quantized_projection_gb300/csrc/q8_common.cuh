@@ -322,6 +322,34 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
     return __byte_perm(ab, cd, 0x5410u);                                                          // a0 b0 c0 d0
 }
 
+// Codes rounded on the FMA pipe.  p = fma(x, 1/d, +0) is the f32 product
+// rounded once (IEEE: adding +0 changes no non-zero result, and a compiler
+// may not drop it, since it turns a -0 product into +0), and p + 1.5 * 2^23
+// rounded to f32 is rint(p), ties to even, for |p| < 2^22: the sum lies
+// where the f32 spacing is 1.  Its bits are 0x4B400000 + rint(p): the low
+// byte is the code and the wrapped sum of the bits gives the code sum.
+// Because p comes from an FMA, the add cannot be fused with the multiply
+// (which would round the exact product instead: another code where p is
+// exactly k + 0.5).
+constexpr float kRoundMagic = 12582912.0f;
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
+
+__device__ __forceinline__ void round_by_add2(float a, float b, float di, uint32_t &ba, uint32_t &bb)
+{
+    const float2 p = __ffma2_rn(make_float2(a, b), make_float2(di, di), make_float2(0.0f, 0.0f));
+    const float2 r = __fadd2_rn(p, make_float2(kRoundMagic, kRoundMagic));
+    ba = __float_as_uint(r.x);
+    bb = __float_as_uint(r.y);
+}
+
+// Whether a block's codes may be rounded by the add: d is 0 (every product
+// is +-0) or a normal finite float (every |p| < 127.5, as for the unclamped
+// codes).  A subnormal or non-finite d takes the clamped codes.
+__device__ __forceinline__ bool block_rounds_by_add(float d)
+{
+    return d == 0.0f || (d >= 1.17549435e-38f && d <= 3.40282347e+38f);
+}
+
 // 8 adjacent lanes hold one 32-element block, a float4 each.
 __device__ __forceinline__ Q8Enc q8_encode8(float4 v)
 {
@@ -331,17 +359,26 @@ __device__ __forceinline__ Q8Enc q8_encode8(float4 v)
     a = fmaxf(a, __shfl_xor_sync(Q8_FULL_MASK, a, 4));
     const float d = q8_block_d(a);
     const float di = q8_block_di(d);
-    const int q0 = q8_code(v.x, di);
-    const int q1 = q8_code(v.y, di);
-    const int q2 = q8_code(v.z, di);
-    const int q3 = q8_code(v.w, di);
-    int s = q0 + q1 + q2 + q3;
+    int s;
+    Q8Enc e;
+    if (block_rounds_by_add(d)) {  // the codes' low bytes straight from the rounded sums' bits
+        uint32_t b0, b1, b2, b3;
+        round_by_add2(v.x, v.y, di, b0, b1);
+        round_by_add2(v.z, v.w, di, b2, b3);
+        s = static_cast<int>(b0 + b1 + b2 + b3 - 4u * kRoundMagicBits);
+        e.qword = __byte_perm(__byte_perm(b0, b1, 0x0040u), __byte_perm(b2, b3, 0x0040u), 0x5410u);
+    } else {
+        const int q0 = q8_code(v.x, di);
+        const int q1 = q8_code(v.y, di);
+        const int q2 = q8_code(v.z, di);
+        const int q3 = q8_code(v.w, di);
+        s = q0 + q1 + q2 + q3;
+        e.qword = (static_cast<uint32_t>(q0) & 0xffu) | ((static_cast<uint32_t>(q1) & 0xffu) << 8) |
+                  ((static_cast<uint32_t>(q2) & 0xffu) << 16) | (static_cast<uint32_t>(q3) << 24);
+    }
     s += __shfl_xor_sync(Q8_FULL_MASK, s, 1);
     s += __shfl_xor_sync(Q8_FULL_MASK, s, 2);
     s += __shfl_xor_sync(Q8_FULL_MASK, s, 4);
-    Q8Enc e;
-    e.qword = (static_cast<uint32_t>(q0) & 0xffu) | ((static_cast<uint32_t>(q1) & 0xffu) << 8) |
-              ((static_cast<uint32_t>(q2) & 0xffu) << 16) | (static_cast<uint32_t>(q3) << 24);
     e.dsword = q8_dsword(d, s);
     return e;
 }

@@ -225,34 +225,6 @@ __device__ __forceinline__ float max3f(float a, float b, float c)
     return r;
 }
 
-// Codes rounded on the FMA pipe.  p = fma(x, 1/d, +0) is the f32 product
-// rounded once (IEEE: adding +0 changes no non-zero result, and a compiler
-// may not drop it, since it turns a -0 product into +0), and p + 1.5 * 2^23
-// rounded to f32 is rint(p), ties to even, for |p| < 2^22: the sum lies
-// where the f32 spacing is 1.  Its bits are 0x4B400000 + rint(p): the low
-// byte is the code and the wrapped sum of the bits gives the code sum.
-// Because p comes from an FMA, the add cannot be fused with the multiply
-// (which would round the exact product instead: another code where p is
-// exactly k + 0.5).
-constexpr float kRoundMagic = 12582912.0f;
-constexpr uint32_t kRoundMagicBits = 0x4B400000u;
-
-__device__ __forceinline__ void round_by_add2(float a, float b, float di, uint32_t &ba, uint32_t &bb)
-{
-    const float2 p = __ffma2_rn(make_float2(a, b), make_float2(di, di), make_float2(0.0f, 0.0f));
-    const float2 r = __fadd2_rn(p, make_float2(kRoundMagic, kRoundMagic));
-    ba = __float_as_uint(r.x);
-    bb = __float_as_uint(r.y);
-}
-
-// Whether a block's codes may be rounded by the add: d is 0 (every product
-// is +-0) or a normal finite float (every |p| < 127.5, as for the unclamped
-// codes).  A subnormal or non-finite d takes the clamped codes.
-__device__ __forceinline__ bool block_rounds_by_add(float d)
-{
-    return d == 0.0f || (d >= 1.17549435e-38f && d <= 3.40282347e+38f);
-}
-
 // The body shared by RMSNorm + quantize (kNorm) and the plain quantizer
 // (rows of x encoded as they are: no sum of squares, weight or y).
 // tmx: x as [rows][d/32][32] f32, box {32, d/32, 1}, 128-byte swizzle.
@@ -405,18 +377,18 @@ __device__ __forceinline__ void rowgroup_body(const CUtensorMap *tmx, const floa
             const float di = q8::q8_block_di(dq);
             uint32_t qw[8];
             int sum = 0;
-            if (block_rounds_by_add(dq)) {
+            if (q8::block_rounds_by_add(dq)) {
                 uint32_t bsum = 0u;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     uint32_t b0, b1, b2, b3;
-                    round_by_add2(v[k].x, v[k].y, di, b0, b1);
-                    round_by_add2(v[k].z, v[k].w, di, b2, b3);
+                    q8::round_by_add2(v[k].x, v[k].y, di, b0, b1);
+                    q8::round_by_add2(v[k].z, v[k].w, di, b2, b3);
                     bsum += b0 + b1 + b2 + b3;
                     qw[k] = q8::pack4(static_cast<int>(b0), static_cast<int>(b1), static_cast<int>(b2),
                                       static_cast<int>(b3));
                 }
-                sum = static_cast<int>(bsum - 32u * kRoundMagicBits);
+                sum = static_cast<int>(bsum - 32u * q8::kRoundMagicBits);
             } else {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
