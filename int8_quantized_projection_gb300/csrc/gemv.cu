@@ -305,14 +305,17 @@ __device__ __forceinline__ void stage_produced(const GvGeom &g, uint8_t *act, fl
         const float di = q8::q8_block_di(d);
         uint32_t qw[4];
         int sum = 0;
-        if (!q8::q8_block_needs_clamp(d)) {
+        if (q8::block_rounds_by_add(d)) {  // codes rounded on the FMA pipe (q8_common.cuh)
+            uint32_t bsum = 0u;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int c0 = q8::q8_code_unclamped(va[e].x, di), c1 = q8::q8_code_unclamped(va[e].y, di);
-                const int c2 = q8::q8_code_unclamped(va[e].z, di), c3 = q8::q8_code_unclamped(va[e].w, di);
-                sum += c0 + c1 + c2 + c3;
-                qw[e] = q8::pack4(c0, c1, c2, c3);
+                uint32_t b0, b1, b2, b3;
+                q8::round_by_add2(va[e].x, va[e].y, di, b0, b1);
+                q8::round_by_add2(va[e].z, va[e].w, di, b2, b3);
+                bsum += b0 + b1 + b2 + b3;
+                qw[e] = __byte_perm(__byte_perm(b0, b1, 0x0040u), __byte_perm(b2, b3, 0x0040u), 0x5410u);
             }
+            sum = static_cast<int>(bsum - 16u * q8::kRoundMagicBits);
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
